@@ -1,0 +1,198 @@
+/*
+ * kvq.h -- C ABI of the low-bit KV-cache library (libkvq.so).
+ *
+ * One operation family: single-token decode attention over a key/value cache
+ * whose older tokens are stored as asymmetric uniform INT4 or INT2 codes and
+ * whose most recent Nr tokens stay fp16.
+ *
+ * Sources the operations follow (web pages on low-bit KV-cache decoding):
+ *   - "Tensor Core accelerated low-bit KV cache decoding" (BitDecoding page),
+ *     section 2.1: scale = (max - min) / (2^b - 1), code = round((K - min) / scale).
+ *   - same page, section 2.2: residual partition, K_pack = KV[:L-Nr] quantized,
+ *     K_res = KV[L-Nr:] kept fp16.
+ *   - same page, section 2.3: GQA query regrouping, one KV read serves gq query heads.
+ *   - same page, section 3.1: per-thread min/max, warp shuffle reduction, pack in registers.
+ *   - same page, section 5.1: cache pointers aligned to 128 bytes.
+ *   - "KV cache quantization InnerQ" page, section 2.1: groups of G = 32 along the
+ *     inner (head_dim) dimension, one row shares its group parameters.
+ *   - same page, section 2.3: recent-token window; a new token enters the window and,
+ *     when the window is full, its oldest token is quantized into the main cache.
+ *   - same page, section 3.1: dequantized value = scale * q + zero.
+ *   - same page, section 3.2: 32 consecutive head_dim values packed together.
+ *
+ * ---------------------------------------------------------------------------
+ * Notation
+ *   B   batch (sequences)             Hkv  KV heads        Hq  query heads (Hq % Hkv == 0)
+ *   gq  = Hq / Hkv                    d    head_dim (multiple of 32, 32..256)
+ *   G   = 32 group size along d       Ng   = d / 32 groups per token and head
+ *   b   bits per code, 2 or 4         Nr   fp16 residual window length (0..1024)
+ *   cap packed-token capacity per (sequence, KV head)
+ *
+ * ---------------------------------------------------------------------------
+ * Memory layout (all arrays are plain device memory owned by the caller; K and V
+ * each have their own four arrays with identical shapes)
+ *
+ *   codes    uint8  [B][Hkv][cap][d*b/8]
+ *            One token row holds d codes as a little-endian bit string: element
+ *            e (0 <= e < d) occupies bits [e*b, e*b + b) of the row, so group g
+ *            is the contiguous bytes [g*4*b, (g+1)*4*b): 16 bytes for INT4, 8 for INT2.
+ *            INT4 byte k = c[2k] | c[2k+1] << 4.
+ *            INT2 byte k = c[4k] | c[4k+1] << 2 | c[4k+2] << 4 | c[4k+3] << 6.
+ *   params   uint32 [B][Hkv][cap][Ng]
+ *            One half2 per group: low 16 bits = scale (fp16), high 16 bits =
+ *            min (fp16).  Dequantized value x^ = min + code * scale.
+ *   residual fp16   [B][Hkv][Nr][d]
+ *            Ring of the most recent tokens, kept in full precision.
+ *   packed_len, res_len, res_head   int32 [B]   (device)
+ *            Per sequence: packed tokens, residual tokens, ring slot of the oldest
+ *            residual token.  Sequence b attends over packed_len[b] + res_len[b] tokens.
+ *   err_word uint32 (device, sticky bit set, see KVQ_ERRBIT_*)
+ *
+ * Every device pointer must be 16-byte aligned (KVQ_ERR_MISALIGNED otherwise);
+ * 128-byte alignment is recommended.
+ *
+ * ---------------------------------------------------------------------------
+ * Quantization rule, per (sequence, head, token, group) with fp16 inputs x_0..x_31
+ *   Q1  mn = min_j x_j, mx = max_j x_j
+ *   Q2  scale_f = ((float)mx - (float)mn) / (float)(2^b - 1)   fp32, round-to-nearest-even divide
+ *   Q3  scale_h = fp16_rne(scale_f) (subnormals kept); min_h = fp16(mn + 0.0f) (-0 stored as +0)
+ *   Q4  s = (float)scale_h; code_j = 0 if s == 0, else
+ *       clamp(rint(((float)x_j - (float)mn) / s), 0, 2^b - 1)   fp32 subtract and divide,
+ *       rint = round half to even
+ *   Q5  pack as in the layout above
+ *   Q6  tokens [0, L - min(Nr, L)) are packed, the rest are copied to the residual ring
+ *       in order, res_head = 0.
+ *
+ * Decode: O[b][hq] = softmax(q[b][hq] . K^T / sqrt(d)) V over the dequantized packed
+ * tokens and the residual tokens of KV head hq / gq, returned as fp16.
+ *
+ * ---------------------------------------------------------------------------
+ * Conventions
+ *   Ownership: the caller owns all memory and the stream.  The library allocates
+ *     nothing and never synchronizes, except kvq_read_error.
+ *   Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   Errors: argument errors return synchronously and launch nothing.  A failed
+ *     launch returns KVQ_ERR_CUDA.  Data-dependent errors (capacity overflow, an
+ *     empty sequence, a bounded wait that ran out) set bits in *err_word on the
+ *     device; kvq_read_error reads and clears them.
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1, /* a bad shape, a NULL pointer, a size mismatch */
+  KVQ_ERR_UNSUPPORTED = 2, /* a valid but unsupported configuration (bits, d, gq) */
+  KVQ_ERR_MISALIGNED = 3,  /* a device pointer that is not 16-byte aligned */
+  KVQ_ERR_CAPACITY = 4,    /* a sequence does not fit in the packed capacity */
+  KVQ_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
+  KVQ_ERR_TIMEOUT = 6,     /* a bounded device-side wait ran out */
+  KVQ_ERR_EMPTY = 7        /* decode over a sequence with no tokens */
+} kvq_status;
+
+/* Bits of *err_word (sticky until kvq_read_error clears them). */
+#define KVQ_ERRBIT_CAPACITY 0x1u /* pack or append would pass cap; the token was dropped */
+#define KVQ_ERRBIT_EMPTY 0x2u    /* decode saw packed_len + res_len == 0; output zeroed */
+#define KVQ_ERRBIT_TIMEOUT 0x4u  /* a bounded wait gave up; that CTA wrote nothing */
+#define KVQ_ERRBIT_BADLEN 0x8u   /* seq_lens[b] < 0 or > Lmax; that sequence was skipped */
+
+/* Static description of one layer's cache.  group must be 32. */
+typedef struct {
+  int32_t batch;        /* B   >= 1 */
+  int32_t num_kv_heads; /* Hkv >= 1 */
+  int32_t head_dim;     /* d: multiple of 32, 32..256 */
+  int32_t bits;         /* b: 2 or 4 */
+  int32_t group;        /* G: 32 */
+  int32_t capacity;     /* packed tokens per (sequence, KV head), >= 0 */
+  int32_t residual;     /* Nr: 0..1024 */
+} kvq_cache_desc;
+
+/* Device pointers of one layer's cache (layout above).  k_res/v_res may be NULL
+ * when residual == 0. */
+typedef struct {
+  uint8_t* k_codes;
+  uint8_t* v_codes;
+  uint32_t* k_params;
+  uint32_t* v_params;
+  uint16_t* k_res; /* fp16 bits */
+  uint16_t* v_res;
+  int32_t* packed_len;
+  int32_t* res_len;
+  int32_t* res_head;
+  uint32_t* err_word;
+} kvq_cache_view;
+
+/* Which array kvq_cache_bytes sizes (each of K and V has one of each). */
+#define KVQ_ARRAY_CODES 0
+#define KVQ_ARRAY_PARAMS 1
+#define KVQ_ARRAY_RESIDUAL 2
+
+/* Bytes of one array of the layout (for K or for V; allocate twice).
+ * Returns 0 for an invalid desc or `which`. */
+size_t kvq_cache_bytes(const kvq_cache_desc* desc, int which);
+
+/* Bytes of scratch kvq_decode_attention needs for num_q_heads query heads on the
+ * current device.  Returns 0 for an invalid desc. */
+size_t kvq_decode_workspace_bytes(const kvq_cache_desc* desc, int32_t num_q_heads);
+
+/* Quantize and pack a prefill (Q1-Q6; BitDecoding page section 2.1 for the rule,
+ * section 2.2 for the residual split, section 3.1 for the warp-shuffle kernel;
+ * InnerQ page section 2.1 for the grouping along head_dim).
+ *   k, v      fp16 device [B][Hkv][Lmax][d], row-major.
+ *   seq_lens  int32 device [B], 0 <= seq_lens[b] <= Lmax.
+ *   Lmax      host int, >= 0.
+ * For each sequence b with L = seq_lens[b]: tokens [0, L - min(Nr, L)) become
+ * codes and params in slots [0, ...), the rest are copied to the residual ring;
+ * packed_len[b], res_len[b] = min(Nr, L) and res_head[b] = 0 are written.
+ * A sequence with more than cap packed tokens sets KVQ_ERRBIT_CAPACITY and stores
+ * only the first cap (packed_len[b] = cap).  Asynchronous on `stream`. */
+kvq_status kvq_quantize_pack(const kvq_cache_desc* desc, const kvq_cache_view* view,
+                             const void* k, const void* v, const int32_t* seq_lens,
+                             int32_t Lmax, void* stream);
+
+/* Append one decode token per sequence (InnerQ page section 2.3, sliding recent
+ * window).
+ *   k_new, v_new  fp16 device [B][Hkv][d].
+ * Per sequence: if res_len == Nr, the oldest residual token (ring slot res_head)
+ * is quantized by Q1-Q5 into packed slot packed_len (which then grows by one)
+ * and the new token takes its ring slot (res_head advances); otherwise the new
+ * token goes to slot (res_head + res_len) % Nr and res_len grows.  With Nr == 0
+ * the new token is packed directly.  A full packed cache sets
+ * KVQ_ERRBIT_CAPACITY and leaves that sequence unchanged.  Asynchronous. */
+kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache_view* view,
+                      const void* k_new, const void* v_new, void* stream);
+
+/* Decode attention (BitDecoding page sections 2.2-2.3; InnerQ page section 3.1).
+ *   q          fp16 device [B][Hq][d]; query head hq uses KV head hq / (Hq / Hkv).
+ *   out        fp16 device [B][Hq][d]: softmax(q K^T / sqrt(d)) V over the
+ *              packed tokens (dequantized as min + code * scale) and the residual.
+ *   workspace  device scratch of ws_bytes >= kvq_decode_workspace_bytes(desc, Hq),
+ *              16-byte aligned.  Its contents on entry do not matter.
+ * A sequence with no tokens gets a zero output and sets KVQ_ERRBIT_EMPTY.
+ * Asynchronous; lengths are read on the device. */
+kvq_status kvq_decode_attention(const kvq_cache_desc* desc, const kvq_cache_view* view,
+                                const void* q, int32_t num_q_heads, void* out,
+                                void* workspace, size_t ws_bytes, void* stream);
+
+/* Synchronize `stream`, copy *err_word to *word_out (may be NULL), clear it, and
+ * return KVQ_OK if it was 0, else the status of its lowest set bit. */
+kvq_status kvq_read_error(const kvq_cache_view* view, uint32_t* word_out, void* stream);
+
+/* Static text for a status code. */
+const char* kvq_status_string(kvq_status status);
+
+/* Library version as 10000 * major + 100 * minor + patch. */
+int32_t kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H_ */
