@@ -1,0 +1,456 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark of the low-bit KV-cache path on GB300.
+
+Workload (default): the Llama-3.1-8B-shaped INT4 32K decode layer -- B1, Hq32,
+Hkv8, d128, 32640 packed tokens + a 128-token fp16 residual window, group 32.
+A step is one pass of the whole decode hot path: kvq_append of the step's new
+K/V token (the residual window is full, so its oldest token is quantized and
+packed) followed by kvq_decode_attention of the step's 32 query heads.
+
+Timing: the steps are captured in a CUDA graph and replayed; the step rotates
+over copies of the cache whose total size is at least 3x the L2 cache, so the
+packed cache streams from HBM.  value = packed code + scale bytes per step
+(K and V, all heads, the tokens the decode reads) / step time.  The decode
+kernels alone are timed the same way in a decode-only graph for the roofline.
+
+Output: one JSON line (see --help).  --impl reference times the CPU oracle
+(the plain fp64 implementation) on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+WORKLOAD = 2
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SOURCES = ("kvq_decode.cu", "kvq_decode_generic.cu", "kvq_decode_common.cuh")
+
+
+# ----------------------------------------------------------------- helpers --
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def aggregate(values, ms_list):
+    """Whole-job figures from per-rank results: value summed (replicas, weak
+    scaling), time the max over ranks."""
+    return sum(values), max(ms_list)
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_quantized_kv_pack_gb300", "csrc")
+    for n in DECODE_SOURCES:
+        p = os.path.join(csrc, n)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_name: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode sources (else None)."""
+    p = os.path.join(ROOT, "profiles", f"decode_{workload_name}.md")
+    if not os.path.exists(p):
+        return None
+    src_hash, traffic = None, None
+    for line in open(p):
+        if line.startswith("source_hash:"):
+            src_hash = line.split(":", 1)[1].strip()
+        if line.startswith("traffic_bytes_per_launch:"):
+            traffic = float(line.split(":", 1)[1].strip())
+    if src_hash != decode_source_hash():
+        return None
+    return traffic
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ our arm ------
+
+def build_state(dev, steps, warmup, e2e_steps, l2_bytes):
+    """Pack the workload once, clone it into enough copies to exceed 3x L2,
+    and pre-generate the per-step queries and new tokens on the device."""
+    from bit_quantized_kv_pack_gb300 import kvq, synth
+
+    w = synth.WORKLOADS[WORKLOAD]
+    k, v, lens = w.prefill(device=dev)
+    npk0 = w.len_max - w.residual
+    per_tok = 2 * (w.head_dim * w.bits // 8 + 4 * (w.head_dim // 32))
+    step_bytes0 = npk0 * w.num_kv_heads * w.batch * per_tok
+    res_bytes = w.batch * w.num_kv_heads * w.residual * w.head_dim * 2 * 2
+    ncopy = max(2, math.ceil(3 * l2_bytes / (step_bytes0 + res_bytes)))
+    # appends each copy sees: warm-up and timed graph passes, then the e2e loop
+    appends = (math.ceil(warmup / ncopy) + math.ceil(steps / ncopy)
+               + math.ceil((ncopy + max(ncopy, e2e_steps)) / ncopy) + 2)
+    cap = npk0 + appends + 8
+    base = kvq.KVCache(w.batch, w.num_kv_heads, w.head_dim, w.bits, cap, w.residual, device=dev)
+    kvq.kvq_quantize_pack(base, k, v, lens.to(dev))
+    st, word = kvq.kvq_read_error(base)
+    if st != kvq.KVQ_OK:
+        raise RuntimeError(f"prefill pack failed: {kvq.status_string(st)}")
+    del k, v
+    copies = [base]
+    for _ in range(ncopy - 1):
+        c = kvq.KVCache(w.batch, w.num_kv_heads, w.head_dim, w.bits, cap, w.residual, device=dev)
+        for name in ("k_codes", "v_codes", "k_params", "v_params", "k_res", "v_res", "counters"):
+            getattr(c, name).copy_(getattr(base, name))
+        copies.append(c)
+    nslot = ncopy  # one graph = one pass over the copies
+    q = torch.stack([w.query(s, device=dev) for s in range(nslot)])
+    kn, vn = zip(*[w.new_tokens(s, device=dev) for s in range(nslot)])
+    kn, vn = torch.stack(kn), torch.stack(vn)
+    out = torch.empty_like(q)
+    ws = kvq.workspace_for(base, w.num_q_heads)
+    return dict(w=w, copies=copies, q=q, kn=kn, vn=vn, out=out, ws=ws, npk0=npk0,
+                per_tok=per_tok, nslot=nslot)
+
+
+def capture(state, with_append=True, with_decode=True, ncopies=None):
+    """A graph of one step on each of the first `ncopies` cache copies."""
+    from bit_quantized_kv_pack_gb300 import kvq
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    n = len(state["copies"]) if ncopies is None else ncopies
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i, c in enumerate(state["copies"][:n]):
+                if with_append:
+                    kvq.kvq_append(c, state["kn"][i], state["vn"][i])
+                if with_decode:
+                    kvq.kvq_decode_attention(c, state["q"][i], state["out"][i], state["ws"])
+    torch.cuda.current_stream().wait_stream(s)
+    return g
+
+
+def time_graph(g, reps, g_rem=None):
+    """ms for `reps` replays of g plus one of g_rem, bracketed by CUDA events on
+    the current stream (graphs replay on it)."""
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    b.record()
+    b.synchronize()
+    return a.elapsed_time(b)
+
+
+def run_ours(args, rank, world, local):
+    from bit_quantized_kv_pack_gb300 import _build, kvq
+    _build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
+
+    st = build_state(dev, args.steps, args.warmup, args.e2e_steps, l2)
+    w, ncopy = st["w"], st["nslot"]
+    K = args.steps
+    reps, rem = divmod(K, ncopy)  # K steps = reps whole passes over the copies + rem
+    wreps = math.ceil(args.warmup / ncopy)
+
+    g_step = capture(st, True, True)
+    g_dec = capture(st, False, True)
+    g_step_rem = capture(st, True, True, rem) if rem else None
+    g_dec_rem = capture(st, False, True, rem) if rem else None
+    for _ in range(wreps):
+        g_step.replay()
+        g_dec.replay()
+    torch.cuda.synchronize()
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        time.sleep(0.25)  # let the sampler start
+        ms = time_graph(g_step, reps, g_step_rem)
+        ms_dec = time_graph(g_dec, reps, g_dec_rem)
+        # keep the same kernels running long enough for several clock samples
+        # (decode only: appends would grow the caches)
+        t_end = time.time() + 0.8
+        while time.time() < t_end:
+            time_graph(g_dec, max(reps, 1))
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+
+    # packed bytes the decode reads per step: the prefill's packed tokens (each
+    # append adds one more token per copy, < 0.1% over the run, not counted)
+    step_bytes = st["npk0"] * w.batch * w.num_kv_heads * st["per_tok"]
+    ms_per_step = ms / K
+    value = step_bytes / (ms_per_step * 1e-3) / 1e9
+
+    dec_ms_per_launch = ms_dec / K
+    achieved = step_bytes / (dec_ms_per_launch * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+
+    # end to end through the public binding: pinned host inputs -> device,
+    # append + decode, output -> pinned host, eager calls (no graph)
+    e2e = run_e2e(st, args)
+
+    clocks = clk.summary()
+    if world > 1:
+        t = torch.tensor([ms_per_step, value, e2e["value"]], device=dev, dtype=torch.float64)
+        tmax = t.clone()
+        torch.distributed.all_reduce(tmax, op=torch.distributed.ReduceOp.MAX)
+        tsum = t.clone()
+        torch.distributed.all_reduce(tsum, op=torch.distributed.ReduceOp.SUM)
+        ms_step_all = float(tmax[0])
+        value_all = step_bytes * world / (ms_step_all * 1e-3) / 1e9
+        e2e["value"] = float(tsum[2])
+    else:
+        ms_step_all, value_all = ms_per_step, value
+
+    plan_kernels = 1 + 2  # append + (split-KV decode, combine)
+    res = {
+        "metric": "quantized-KV decode attention: achieved HBM GB/s (% of peak), us/step",
+        "value": round(value_all, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": wreps * ncopy,
+        "ms_per_step": round(ms_step_all, 6),
+        "us_per_step": round(ms_step_all * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u4 codes, fp16 scale/min, fp32 accumulate",
+        "data": "synthetic (seeded SplitMix64 + Box-Muller, fp16)",
+        "config": {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "bits": w.bits,
+                   "packed_tokens": st["npk0"], "residual": w.residual, "group": 32,
+                   "step": "append + decode_attention",
+                   "l2": f"rotating {ncopy} cache copies ({ncopy * step_bytes / 2**20:.0f} MiB "
+                         f"packed) > 3x L2 ({l2 / 2**20:.0f} MiB)",
+                   "timing": "CUDA graph replays, CUDA events", "parallelism": "replicas"},
+        "gpu_launches": plan_kernels * K,
+        "roofline": {"bound": "hbm", "kernel": "decode (split-KV + combine)",
+                     "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic(w.name),
+                     "algorithmic_bytes_per_launch": step_bytes,
+                     "us_per_launch": round(dec_ms_per_launch * 1e3, 3)},
+        "e2e": e2e,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return res
+
+
+def run_e2e(st, args):
+    from bit_quantized_kv_pack_gb300 import kvq
+    n = st["nslot"]
+    q_h = st["q"].cpu().pin_memory()
+    kn_h = st["kn"].cpu().pin_memory()
+    vn_h = st["vn"].cpu().pin_memory()
+    out_h = torch.empty_like(q_h).pin_memory()
+    dev = st["q"].device
+    q_d = torch.empty_like(st["q"][0])
+    kn_d = torch.empty_like(st["kn"][0])
+    vn_d = torch.empty_like(st["vn"][0])
+    out_d = torch.empty_like(st["out"][0])
+    K = max(n, args.e2e_steps)
+
+    def step(i):
+        j = i % n
+        q_d.copy_(q_h[j], non_blocking=True)
+        kn_d.copy_(kn_h[j], non_blocking=True)
+        vn_d.copy_(vn_h[j], non_blocking=True)
+        c = st["copies"][j]
+        kvq.kvq_append(c, kn_d, vn_d)
+        kvq.kvq_decode_attention(c, q_d, out_d, st["ws"])
+        out_h[j].copy_(out_d, non_blocking=True)
+
+    for i in range(n):
+        step(i)
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(K):
+        step(i)
+    b.record()
+    b.synchronize()
+    ms = a.elapsed_time(b) / K
+    w = st["w"]
+    step_bytes = st["npk0"] * w.batch * w.num_kv_heads * st["per_tok"]
+    return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "us_per_step": round(ms * 1e3, 3),
+            "h2d_bytes_per_step": int(q_d.numel() * 2 + kn_d.numel() * 2 + vn_d.numel() * 2),
+            "d2h_bytes_per_step": int(out_d.numel() * 2),
+            "how": "eager ctypes calls per step: pinned H2D of q/k_new/v_new, append, decode, D2H of out"}
+
+
+# ---------------------------------------------------------- oracle arm -----
+
+def cpu_baseline(seconds: float, steps: int | None = None):
+    """The CPU oracle as it stands (single thread) on whole steps of the same
+    workload: append + fp64 decode of all 32 query heads."""
+    import numpy as np
+    import oracle
+    from bit_quantized_kv_pack_gb300 import synth
+
+    w = synth.WORKLOADS[WORKLOAD]
+    k, v, lens = w.prefill()
+    npk0 = w.len_max - w.residual
+    n_steps_max = steps if steps is not None else 1000
+    r = oracle.Cache(w.batch, w.num_kv_heads, w.head_dim, w.bits, npk0 + n_steps_max + 8, w.residual)
+    oracle.quantize_pack(r, k.numpy(), v.numpy(), lens.numpy())
+    del k, v
+    per_tok = 2 * (w.head_dim * w.bits // 8 + 4 * (w.head_dim // 32))
+    step_bytes = npk0 * w.batch * w.num_kv_heads * per_tok
+    t0 = time.time()
+    n = 0
+    while True:
+        kn, vn = w.new_tokens(n)
+        oracle.append(r, kn.numpy(), vn.numpy())
+        oracle.decode(r, w.query(n).numpy())
+        n += 1
+        el = time.time() - t0
+        if (steps is not None and n >= steps) or (steps is None and el >= seconds):
+            break
+    el = time.time() - t0
+    return {"value": round(step_bytes * n / el / 1e9, 6), "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "sample": f"{n} whole steps (append + decode of 32 heads over "
+                                        f"{npk0}+{w.residual} tokens), {el:.1f} s, single thread",
+            "s_per_step": round(el / n, 4)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    steps = max(1, args.steps_reference if args.steps_reference else min(args.steps, 5))
+    # warm-up: one step, untimed
+    cpu_baseline(0.0, steps=1)
+    cb = cpu_baseline(0.0, steps=steps)
+    from bit_quantized_kv_pack_gb300 import synth
+    w = synth.WORKLOADS[WORKLOAD]
+    return {
+        "impl": "reference",
+        "metric": "quantized-KV decode attention: achieved HBM GB/s (% of peak), us/step",
+        "value": cb["value"], "unit": "GB/s", "n_gpus": world, "steps": steps, "warmup": 1,
+        "ms_per_step": cb["s_per_step"] * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "bits": w.bits,
+                   "step": "append + decode_attention"},
+        "cpu_baseline": {"value": cb["value"], "unit": "GB/s", "cores": cb["cores"],
+                         "kind": "oracle", "sample": cb["sample"]},
+        "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--steps-reference", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_info()
+    if world > 1:
+        torch.distributed.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    try:
+        if args.impl == "reference":
+            res = run_reference(args, rank, world)
+        else:
+            res = run_ours(args, rank, world, local)
+        if rank == 0 and res is not None:
+            print(json.dumps(res), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

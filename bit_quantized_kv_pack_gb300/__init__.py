@@ -2,22 +2,18 @@
 
 The compute path is the C-ABI library ``libkvq.so`` built from ``csrc/``; this
 package holds its thin ctypes binding (``kvq``), a cache allocator over torch
-device memory (``KVCache``) and the seeded input generator (``synth``).
-Importing the package loads nothing; the library is loaded on first use and an
-absent or unbuilt library raises instead of falling back to anything else.
+device memory (``kvq.KVCache``), the build step (``_build``) and the seeded
+input generator (``synth``).  Importing the package loads nothing; the library
+is loaded on first use, and an absent or unbuilt library raises instead of
+falling back to anything else.
 """
 
-__all__ = ["kvq", "synth", "build"]
+import importlib
+
+__all__ = ["kvq", "synth"]
 
 
 def __getattr__(name):
-    if name == "kvq":
-        from . import kvq as _kvq
-        return _kvq
-    if name == "synth":
-        from . import synth as _synth
-        return _synth
-    if name == "build":
-        from ._build import build as _b
-        return _b
+    if name in ("kvq", "synth", "_build"):
+        return importlib.import_module(f"{__name__}.{name}")
     raise AttributeError(name)

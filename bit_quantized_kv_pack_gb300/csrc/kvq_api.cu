@@ -1,0 +1,143 @@
+// kvq_api.cu -- the C ABI of libkvq.so: argument checks, launch, status codes.
+// Every entry point validates on the host and launches nothing on an error.
+#include <string.h>
+
+#include "kvq_internal.cuh"
+
+namespace {
+
+using kvq::Dims;
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+kvq_status check_desc(const kvq_cache_desc* D) {
+  if (!D) return KVQ_ERR_INVALID_ARG;
+  if (D->batch < 1 || D->num_kv_heads < 1 || D->capacity < 0 || D->residual < 0 ||
+      D->group != kvq::kGroup || D->head_dim < 32 || D->head_dim % 32 != 0)
+    return KVQ_ERR_INVALID_ARG;
+  if (D->bits != 2 && D->bits != 4) return KVQ_ERR_UNSUPPORTED;
+  if (D->head_dim != 32 && D->head_dim != 64 && D->head_dim != 128 && D->head_dim != 256)
+    return KVQ_ERR_UNSUPPORTED;
+  if (D->residual > 1024) return KVQ_ERR_UNSUPPORTED;
+  if ((int64_t)D->batch * D->num_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
+  return KVQ_OK;
+}
+
+kvq_status check_view(const kvq_cache_desc& D, const kvq_cache_view* v) {
+  if (!v) return KVQ_ERR_INVALID_ARG;
+  if (!v->packed_len || !v->res_len || !v->res_head || !v->err_word) return KVQ_ERR_INVALID_ARG;
+  if (D.capacity > 0 && (!v->k_codes || !v->v_codes || !v->k_params || !v->v_params))
+    return KVQ_ERR_INVALID_ARG;
+  if (D.residual > 0 && (!v->k_res || !v->v_res)) return KVQ_ERR_INVALID_ARG;
+  const void* a16[] = {v->k_codes, v->v_codes, v->k_params, v->v_params, v->k_res, v->v_res};
+  for (const void* p : a16)
+    if (!aligned(p, 16)) return KVQ_ERR_MISALIGNED;
+  const void* a4[] = {v->packed_len, v->res_len, v->res_head, v->err_word};
+  for (const void* p : a4)
+    if (!aligned(p, 4)) return KVQ_ERR_MISALIGNED;
+  return KVQ_OK;
+}
+
+kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t kvq_cache_bytes(const kvq_cache_desc* desc, int which) {
+  if (check_desc(desc) != KVQ_OK) return 0;
+  const Dims s = kvq::dims_of(*desc);
+  const size_t rows = (size_t)s.B * s.Hkv;
+  switch (which) {
+    case KVQ_ARRAY_CODES: return rows * (size_t)s.cap * s.row_bytes;
+    case KVQ_ARRAY_PARAMS: return rows * (size_t)s.cap * s.Ng * sizeof(uint32_t);
+    case KVQ_ARRAY_RESIDUAL: return rows * (size_t)s.Nr * s.d * sizeof(uint16_t);
+    default: return 0;
+  }
+}
+
+size_t kvq_decode_workspace_bytes(const kvq_cache_desc* desc, int32_t num_q_heads) {
+  if (check_desc(desc) != KVQ_OK || num_q_heads < 1 || num_q_heads % desc->num_kv_heads) return 0;
+  return kvq::plan_decode(*desc, num_q_heads, kvq::device_sm_count()).ws_total;
+}
+
+kvq_status kvq_quantize_pack(const kvq_cache_desc* desc, const kvq_cache_view* view,
+                             const void* k, const void* v, const int32_t* seq_lens,
+                             int32_t Lmax, void* stream) {
+  kvq_status st = check_desc(desc);
+  if (st != KVQ_OK) return st;
+  if ((st = check_view(*desc, view)) != KVQ_OK) return st;
+  if (Lmax < 0 || !seq_lens || (Lmax > 0 && (!k || !v))) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(seq_lens, 4)) return KVQ_ERR_MISALIGNED;
+  const Dims s = kvq::dims_of(*desc);
+  return from_cuda(kvq::launch_quantize_pack(s, *view, static_cast<const __half*>(k),
+                                             static_cast<const __half*>(v), seq_lens, Lmax,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache_view* view, const void* k_new,
+                      const void* v_new, void* stream) {
+  kvq_status st = check_desc(desc);
+  if (st != KVQ_OK) return st;
+  if ((st = check_view(*desc, view)) != KVQ_OK) return st;
+  if (!k_new || !v_new) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16)) return KVQ_ERR_MISALIGNED;
+  const Dims s = kvq::dims_of(*desc);
+  return from_cuda(kvq::launch_append(s, *view, static_cast<const __half*>(k_new),
+                                      static_cast<const __half*>(v_new),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_decode_attention(const kvq_cache_desc* desc, const kvq_cache_view* view,
+                                const void* q, int32_t num_q_heads, void* out, void* workspace,
+                                size_t ws_bytes, void* stream) {
+  kvq_status st = check_desc(desc);
+  if (st != KVQ_OK) return st;
+  if ((st = check_view(*desc, view)) != KVQ_OK) return st;
+  if (!q || !out || !workspace || num_q_heads < 1 || num_q_heads % desc->num_kv_heads)
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 16)) return KVQ_ERR_MISALIGNED;
+  if ((int64_t)desc->batch * num_q_heads > 2147483647LL) return KVQ_ERR_UNSUPPORTED;
+  const kvq::DecodePlan p = kvq::plan_decode(*desc, num_q_heads, kvq::device_sm_count());
+  if ((int64_t)desc->num_kv_heads * p.nqb > 65535) return KVQ_ERR_UNSUPPORTED;
+  if (ws_bytes < p.ws_total) return KVQ_ERR_INVALID_ARG;
+  const Dims s = kvq::dims_of(*desc);
+  return from_cuda(kvq::launch_decode(s, p, *view, static_cast<const __half*>(q), num_q_heads,
+                                      static_cast<__half*>(out), workspace,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_read_error(const kvq_cache_view* view, uint32_t* word_out, void* stream) {
+  if (!view || !view->err_word) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(view->err_word, 4)) return KVQ_ERR_MISALIGNED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t w = 0;
+  cudaError_t e = cudaMemcpyAsync(&w, view->err_word, sizeof(w), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(view->err_word, 0, sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return KVQ_ERR_CUDA;
+  if (word_out) *word_out = w;
+  if (w & KVQ_ERRBIT_CAPACITY) return KVQ_ERR_CAPACITY;
+  if (w & KVQ_ERRBIT_EMPTY) return KVQ_ERR_EMPTY;
+  if (w & KVQ_ERRBIT_TIMEOUT) return KVQ_ERR_TIMEOUT;
+  if (w & KVQ_ERRBIT_BADLEN) return KVQ_ERR_INVALID_ARG;
+  return KVQ_OK;
+}
+
+const char* kvq_status_string(kvq_status status) {
+  switch (status) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KVQ_ERR_MISALIGNED: return "misaligned pointer";
+    case KVQ_ERR_CAPACITY: return "packed capacity exceeded";
+    case KVQ_ERR_CUDA: return "CUDA error";
+    case KVQ_ERR_TIMEOUT: return "device wait timed out";
+    case KVQ_ERR_EMPTY: return "sequence with no tokens";
+    default: return "unknown status";
+  }
+}
+
+int32_t kvq_version(void) { return 100; }
+
+}  // extern "C"

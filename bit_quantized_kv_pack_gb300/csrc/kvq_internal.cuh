@@ -1,0 +1,128 @@
+// kvq_internal.cuh -- device helpers and launch plans shared by the kernels of
+// libkvq.so.  Layout and semantics are those of include/kvq.h.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+constexpr int kGroup = 32;  // G: values per quantization group along head_dim
+
+// ----------------------------------------------------------------- sizes ---
+
+struct Dims {
+  int B, Hkv, d, bits, cap, Nr;
+  int Ng;        // groups per token row
+  int row_bytes; // packed code bytes per token row
+};
+
+inline Dims dims_of(const kvq_cache_desc& D) {
+  Dims s;
+  s.B = D.batch;
+  s.Hkv = D.num_kv_heads;
+  s.d = D.head_dim;
+  s.bits = D.bits;
+  s.cap = D.capacity;
+  s.Nr = D.residual;
+  s.Ng = D.head_dim / kGroup;
+  s.row_bytes = D.head_dim * D.bits / 8;
+  return s;
+}
+
+// ------------------------------------------------------------ error word ---
+
+__device__ __forceinline__ void set_error(uint32_t* err_word, uint32_t bit) {
+  if (err_word) atomicOr(err_word, bit);
+}
+
+// ----------------------------------------------------- group quantizer ------
+//
+// One group of 32 fp16 values is held by 4 consecutive lanes, 8 values each
+// (lane q of the quad holds values 8q .. 8q+7).  Steps Q1-Q4 with the op order
+// fixed by the header:
+//   Q1  min/max over the quad (local over 8, then shuffle-xor 1 and 2)
+//   Q2  scale_f = (mx - mn) / (2^b - 1) in fp32, IEEE divide
+//   Q3  scale_h = fp16_rne(scale_f); min_h = fp16(mn + 0)
+//   Q4  code = clamp(rint((x - mn) / s), 0, 2^b - 1) with s = (float)scale_h,
+//       or 0 when s == 0.
+// Returns the lane's 8 codes packed little-endian (b = 4: 32 bits, b = 2: 16
+// bits) and the group's {scale, min} half2 bits.  All 32 lanes of the warp must
+// call it (the shuffles use the full mask); `active` lanes only matter for the
+// result, inactive lanes pass any finite values.
+template <int BITS>
+__device__ __forceinline__ uint32_t quantize_quad(const float (&x)[8], uint32_t& params_out) {
+  constexpr int kQmax = (1 << BITS) - 1;
+  float mn = x[0], mx = x[0];
+#pragma unroll
+  for (int j = 1; j < 8; ++j) {
+    mn = fminf(mn, x[j]);
+    mx = fmaxf(mx, x[j]);
+  }
+#pragma unroll
+  for (int o = 1; o <= 2; o <<= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  const float scale_f = __fdiv_rn(__fsub_rn(mx, mn), (float)kQmax);
+  const __half scale_h = __float2half_rn(scale_f);
+  const __half min_h = __float2half_rn(__fadd_rn(mn, 0.0f));
+  const float s = __half2float(scale_h);
+  uint32_t packed = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    int c = 0;
+    if (s != 0.0f) {
+      c = __float2int_rn(__fdiv_rn(__fsub_rn(x[j], mn), s));
+      c = min(max(c, 0), kQmax);
+    }
+    packed |= (uint32_t)c << (BITS * j);
+  }
+  params_out = (uint32_t)__half_as_ushort(scale_h) | ((uint32_t)__half_as_ushort(min_h) << 16);
+  return packed;
+}
+
+__device__ __forceinline__ void unpack8_f16(const uint4& v, float (&x)[8]) {
+  const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f = __half22float2(h[i]);
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+}
+
+// -------------------------------------------------------- decode planning ---
+
+// Work split of one decode call.  Each (sequence, KV head, query block) is cut
+// into `splits` pieces of roughly equal byte cost; partials (o, m, l) go to the
+// workspace and a combine step merges them by log-sum-exp.
+struct DecodePlan {
+  int kernel;   // 0 = generic CUDA-core path, 1 = tensor-core path
+  int gq;       // query heads per KV head
+  int qb;       // query heads handled by one CTA (power of two, <= 8)
+  int nqb;      // query blocks per KV head = ceil(gq / qb)
+  int splits;   // S
+  int threads;  // threads per CTA of the split kernel
+  size_t ws_partials;  // bytes of the o partials
+  size_t ws_total;     // bytes of the whole workspace
+};
+
+DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count);
+int device_sm_count();
+
+// ------------------------------------------------------------- launchers ---
+
+cudaError_t launch_quantize_pack(const Dims& s, const kvq_cache_view& v, const __half* k,
+                                 const __half* vv, const int32_t* seq_lens, int Lmax,
+                                 cudaStream_t st);
+cudaError_t launch_append(const Dims& s, const kvq_cache_view& v, const __half* k_new,
+                          const __half* v_new, cudaStream_t st);
+cudaError_t launch_decode(const Dims& s, const DecodePlan& p, const kvq_cache_view& v,
+                          const __half* q, int Hq, __half* out, void* workspace,
+                          cudaStream_t st);
+
+}  // namespace kvq

@@ -1,0 +1,245 @@
+// kvq_quant.cu -- quantize/pack of a prefill and the decode-step append.
+//
+// Rule: asymmetric uniform quantization with scale = (max - min) / (2^b - 1) and
+// code = round((x - min) / scale) ("Tensor Core accelerated low-bit KV cache
+// decoding" page, section 2.1), over groups of 32 consecutive head_dim values
+// (InnerQ page, section 2.1).  Kernel shape: per-thread min/max over its values,
+// a shuffle-xor reduction inside the group, codes packed in registers and
+// written straight out (BitDecoding page, section 3.1).  Residual split: the
+// last min(Nr, L) tokens stay fp16 (BitDecoding page, section 2.2); append
+// follows the sliding recent window (InnerQ page, section 2.3).
+//
+// Thread mapping.  The tokens of one (sequence, KV head) are contiguous rows of
+// d fp16 values, so its groups are contiguous 64-byte pieces of memory, and so
+// are their outputs (4*b code bytes, one 4-byte param).  A warp takes 8
+// consecutive groups: lane l holds values 8*(l%4) .. +7 of group l/4, one
+// 16-byte load.  Every store of the warp is contiguous (128 or 64 bytes of codes,
+// 32 bytes of params).
+#include "kvq_internal.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr int kPackThreads = 256;  // 8 warps
+constexpr int kPackUnroll = 4;     // independent 16-byte loads in flight per thread
+constexpr int kGroupsPerIter = kPackThreads / 4;
+constexpr int kGroupsPerCta = kGroupsPerIter * kPackUnroll;
+
+// Index 0 = K, 1 = V (blockIdx.z).
+struct PackArgs {
+  const __half* x[2];    // [B][Hkv][Lmax][d]
+  uint8_t* codes[2];     // [B][Hkv][cap][row_bytes]
+  uint32_t* params[2];   // [B][Hkv][cap][Ng]
+  __half* res[2];        // [B][Hkv][Nr][d]
+  const int32_t* seq_lens;
+  int32_t* packed_len;
+  int32_t* res_len;
+  int32_t* res_head;
+  uint32_t* err_word;
+  int Hkv, d, Ng, row_bytes, cap, Nr, Lmax;
+};
+
+template <int BITS>
+__global__ void __launch_bounds__(kPackThreads) quantize_pack_kernel(PackArgs a) {
+  const int bh = blockIdx.y;
+  const int which = blockIdx.z;
+  const int b = bh / a.Hkv;
+  const int L = a.seq_lens[b];
+  const bool bad = (L < 0 || L > a.Lmax);
+  const int nres = bad ? 0 : min(L, a.Nr);
+  const int npk_all = bad ? 0 : L - nres;
+  const int npk = min(npk_all, a.cap);
+
+  if (which == 0 && blockIdx.x == 0 && (bh % a.Hkv) == 0 && threadIdx.x == 0) {
+    a.packed_len[b] = npk;
+    a.res_len[b] = nres;
+    a.res_head[b] = 0;
+    if (bad) set_error(a.err_word, KVQ_ERRBIT_BADLEN);
+    if (npk_all > a.cap) set_error(a.err_word, KVQ_ERRBIT_CAPACITY);
+  }
+  if (bad) return;
+
+  const int64_t groups_used = (int64_t)L * a.Ng;
+  const int64_t g0 = (int64_t)blockIdx.x * kGroupsPerCta;
+  if (g0 >= groups_used) return;
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int quad = lane & 3;
+  const __half* src = a.x[which] + (int64_t)bh * a.Lmax * a.d;
+
+  uint4 raw[kPackUnroll];
+  int64_t gi[kPackUnroll];
+#pragma unroll
+  for (int u = 0; u < kPackUnroll; ++u) {
+    gi[u] = g0 + u * kGroupsPerIter + warp * 8 + (lane >> 2);
+    raw[u] = make_uint4(0, 0, 0, 0);
+    if (gi[u] < groups_used)
+      raw[u] = __ldg(reinterpret_cast<const uint4*>(src + gi[u] * kGroup + quad * 8));
+  }
+
+#pragma unroll
+  for (int u = 0; u < kPackUnroll; ++u) {
+    const bool in_range = gi[u] < groups_used;
+    const int t = in_range ? (int)(gi[u] / a.Ng) : 0;
+    const int g = in_range ? (int)(gi[u] % a.Ng) : 0;
+    float x[8];
+    unpack8_f16(raw[u], x);
+    uint32_t prm;
+    const uint32_t packed = quantize_quad<BITS>(x, prm);  // all lanes take part
+    if (!in_range) continue;
+    if (t < npk) {
+      const int64_t row = (int64_t)bh * a.cap + t;
+      uint8_t* dst = a.codes[which] + row * a.row_bytes + g * (4 * BITS) + quad * BITS;
+      if (BITS == 4)
+        *reinterpret_cast<uint32_t*>(dst) = packed;
+      else
+        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
+      if (quad == 0) a.params[which][row * a.Ng + g] = prm;
+    } else if (t >= npk_all) {
+      const int j = t - npk_all;  // ring slot; res_head = 0 after a prefill
+      __half* dst = a.res[which] + ((int64_t)bh * a.Nr + j) * a.d + g * kGroup + quad * 8;
+      *reinterpret_cast<uint4*>(dst) = raw[u];
+    }
+    // tokens in [cap, npk_all) are dropped (capacity error raised above)
+  }
+}
+
+// One CTA per sequence; warps take (KV head, K-or-V) items.
+struct AppendArgs {
+  const __half* k_new;  // [B][Hkv][d]
+  const __half* v_new;
+  uint8_t* codes[2];
+  uint32_t* params[2];
+  __half* res[2];
+  int32_t* packed_len;
+  int32_t* res_len;
+  int32_t* res_head;
+  uint32_t* err_word;
+  int Hkv, d, Ng, row_bytes, cap, Nr;
+};
+
+template <int BITS>
+__global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
+  const int b = blockIdx.x;
+  const int pl = a.packed_len[b];
+  const int rl = a.res_len[b];
+  const int rh = a.res_head[b];
+  const bool pack_now = (a.Nr == 0) || (rl == a.Nr);
+  if (pack_now && pl >= a.cap) {
+    if (threadIdx.x == 0) set_error(a.err_word, KVQ_ERRBIT_CAPACITY);
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const bool active = lane * 8 < a.d;
+  const int slot_new = (a.Nr == 0) ? 0 : (pack_now ? rh : (rh + rl) % a.Nr);
+
+  for (int item = warp; item < 2 * a.Hkv; item += nwarps) {
+    const int which = item & 1;
+    const int h = item >> 1;
+    const int64_t bh = (int64_t)b * a.Hkv + h;
+    const __half* nsrc = (which ? a.v_new : a.k_new) + bh * a.d;
+    uint4 newv = make_uint4(0, 0, 0, 0);
+    if (active) newv = __ldg(reinterpret_cast<const uint4*>(nsrc + lane * 8));
+    __half* ring_row = (a.Nr > 0) ? a.res[which] + (bh * a.Nr + slot_new) * a.d : nullptr;
+    if (pack_now) {
+      uint4 oldv = newv;
+      if (a.Nr > 0 && active) oldv = *reinterpret_cast<const uint4*>(ring_row + lane * 8);
+      float x[8];
+      unpack8_f16(oldv, x);
+      uint32_t prm;
+      const uint32_t packed = quantize_quad<BITS>(x, prm);
+      if (active) {
+        const int64_t row = bh * a.cap + pl;
+        const int g = lane >> 2, quad = lane & 3;
+        uint8_t* dst = a.codes[which] + row * a.row_bytes + g * (4 * BITS) + quad * BITS;
+        if (BITS == 4)
+          *reinterpret_cast<uint32_t*>(dst) = packed;
+        else
+          *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
+        if (quad == 0) a.params[which][row * a.Ng + g] = prm;
+      }
+    }
+    if (a.Nr > 0 && active) *reinterpret_cast<uint4*>(ring_row + lane * 8) = newv;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (a.Nr == 0) {
+      a.packed_len[b] = pl + 1;
+    } else if (pack_now) {
+      a.packed_len[b] = pl + 1;
+      a.res_head[b] = (rh + 1) % a.Nr;
+    } else {
+      a.res_len[b] = rl + 1;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_pack(const Dims& s, const kvq_cache_view& v, const __half* k,
+                                 const __half* vv, const int32_t* seq_lens, int Lmax,
+                                 cudaStream_t st) {
+  // With Lmax == 0 one CTA per (sequence, head) still runs to write the counters.
+  const int64_t groups = (int64_t)(Lmax > 0 ? Lmax : 1) * s.Ng;
+  dim3 grid((unsigned)((groups + kGroupsPerCta - 1) / kGroupsPerCta), (unsigned)(s.B * s.Hkv), 2);
+  PackArgs a;
+  a.x[0] = k;
+  a.x[1] = vv;
+  a.codes[0] = v.k_codes;
+  a.codes[1] = v.v_codes;
+  a.params[0] = v.k_params;
+  a.params[1] = v.v_params;
+  a.res[0] = reinterpret_cast<__half*>(v.k_res);
+  a.res[1] = reinterpret_cast<__half*>(v.v_res);
+  a.seq_lens = seq_lens;
+  a.packed_len = v.packed_len;
+  a.res_len = v.res_len;
+  a.res_head = v.res_head;
+  a.err_word = v.err_word;
+  a.Hkv = s.Hkv;
+  a.d = s.d;
+  a.Ng = s.Ng;
+  a.row_bytes = s.row_bytes;
+  a.cap = s.cap;
+  a.Nr = s.Nr;
+  a.Lmax = Lmax;
+  if (s.bits == 4)
+    quantize_pack_kernel<4><<<grid, kPackThreads, 0, st>>>(a);
+  else
+    quantize_pack_kernel<2><<<grid, kPackThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(const Dims& s, const kvq_cache_view& v, const __half* k_new,
+                          const __half* v_new, cudaStream_t st) {
+  AppendArgs a;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.codes[0] = v.k_codes;
+  a.codes[1] = v.v_codes;
+  a.params[0] = v.k_params;
+  a.params[1] = v.v_params;
+  a.res[0] = reinterpret_cast<__half*>(v.k_res);
+  a.res[1] = reinterpret_cast<__half*>(v.v_res);
+  a.packed_len = v.packed_len;
+  a.res_len = v.res_len;
+  a.res_head = v.res_head;
+  a.err_word = v.err_word;
+  a.Hkv = s.Hkv;
+  a.d = s.d;
+  a.Ng = s.Ng;
+  a.row_bytes = s.row_bytes;
+  a.cap = s.cap;
+  a.Nr = s.Nr;
+  const int threads = 32 * (2 * s.Hkv < 8 ? 2 * s.Hkv : 8);
+  if (s.bits == 4)
+    append_kernel<4><<<s.B, threads, 0, st>>>(a);
+  else
+    append_kernel<2><<<s.B, threads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -1,0 +1,243 @@
+"""ctypes binding of libkvq.so (include/kvq.h): same names, argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels.  Torch supplies
+device memory (``KVCache`` allocates the layout's arrays as torch tensors) and the
+stream (the current torch stream unless one is given).  The library must be
+built (``bit_quantized_kv_pack_gb300._build.build()``); if it is missing, loading
+raises: there is no other implementation to fall back to.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+# ------------------------------------------------------------------- ABI ----
+
+KVQ_OK = 0
+KVQ_ERR_INVALID_ARG = 1
+KVQ_ERR_UNSUPPORTED = 2
+KVQ_ERR_MISALIGNED = 3
+KVQ_ERR_CAPACITY = 4
+KVQ_ERR_CUDA = 5
+KVQ_ERR_TIMEOUT = 6
+KVQ_ERR_EMPTY = 7
+
+KVQ_ERRBIT_CAPACITY = 0x1
+KVQ_ERRBIT_EMPTY = 0x2
+KVQ_ERRBIT_TIMEOUT = 0x4
+KVQ_ERRBIT_BADLEN = 0x8
+
+KVQ_ARRAY_CODES = 0
+KVQ_ARRAY_PARAMS = 1
+KVQ_ARRAY_RESIDUAL = 2
+
+# Every function the header declares (the tests check the library exports them).
+EXPORTS = ("kvq_cache_bytes", "kvq_decode_workspace_bytes", "kvq_quantize_pack", "kvq_append",
+           "kvq_decode_attention", "kvq_read_error", "kvq_status_string", "kvq_version")
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("bits", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("capacity", ctypes.c_int32), ("residual", ctypes.c_int32)]
+
+
+class CacheView(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "k_codes", "v_codes", "k_params", "v_params", "k_res", "v_res",
+        "packed_len", "res_len", "res_head", "err_word")]
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load libkvq.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or library_path()
+            if not os.path.exists(p):
+                raise RuntimeError(f"libkvq.so not built ({p}); run __graft_entry__.build()")
+            lib = ctypes.CDLL(p)
+            P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+            DP, VP = ctypes.POINTER(CacheDesc), ctypes.POINTER(CacheView)
+            lib.kvq_cache_bytes.argtypes = [DP, ctypes.c_int]
+            lib.kvq_cache_bytes.restype = sz
+            lib.kvq_decode_workspace_bytes.argtypes = [DP, i32]
+            lib.kvq_decode_workspace_bytes.restype = sz
+            lib.kvq_quantize_pack.argtypes = [DP, VP, P, P, P, i32, P]
+            lib.kvq_quantize_pack.restype = ctypes.c_int
+            lib.kvq_append.argtypes = [DP, VP, P, P, P]
+            lib.kvq_append.restype = ctypes.c_int
+            lib.kvq_decode_attention.argtypes = [DP, VP, P, i32, P, P, sz, P]
+            lib.kvq_decode_attention.restype = ctypes.c_int
+            lib.kvq_read_error.argtypes = [VP, ctypes.POINTER(ctypes.c_uint32), P]
+            lib.kvq_read_error.restype = ctypes.c_int
+            lib.kvq_status_string.argtypes = [ctypes.c_int]
+            lib.kvq_status_string.restype = ctypes.c_char_p
+            lib.kvq_version.argtypes = []
+            lib.kvq_version.restype = i32
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().kvq_status_string(status).decode()
+
+
+kvq_status_string = status_string
+
+
+def _check(status: int, where: str) -> None:
+    if status != KVQ_OK:
+        raise KvqError(status, where)
+
+
+def _ptr(t: torch.Tensor | None):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream, device) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    return ctypes.c_void_p(int(stream))
+
+
+def _f16(t: torch.Tensor, name: str) -> torch.Tensor:
+    if t.dtype != torch.float16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous float16 CUDA tensor")
+    return t
+
+
+# --------------------------------------------------------------- caches ----
+
+
+class KVCache:
+    """One layer's packed cache in device memory (torch tensors in the layout of
+    include/kvq.h).  Holds the description and the view the calls take."""
+
+    def __init__(self, batch, num_kv_heads, head_dim, bits, capacity, residual, device="cuda"):
+        self.desc = CacheDesc(batch, num_kv_heads, head_dim, bits, 32, capacity, residual)
+        self.device = torch.device(device)
+        B, H, d = batch, num_kv_heads, head_dim
+        rb, ng = d * bits // 8, d // 32
+        kw = dict(device=self.device)
+        self.k_codes = torch.zeros(B, H, capacity, rb, dtype=torch.uint8, **kw)
+        self.v_codes = torch.zeros(B, H, capacity, rb, dtype=torch.uint8, **kw)
+        self.k_params = torch.zeros(B, H, capacity, ng, dtype=torch.int32, **kw)
+        self.v_params = torch.zeros(B, H, capacity, ng, dtype=torch.int32, **kw)
+        self.k_res = torch.zeros(B, H, residual, d, dtype=torch.float16, **kw)
+        self.v_res = torch.zeros(B, H, residual, d, dtype=torch.float16, **kw)
+        self.counters = torch.zeros(3, B, dtype=torch.int32, **kw)
+        self.err = torch.zeros(4, dtype=torch.int32, **kw)
+        self.view = self._make_view()
+
+    def _make_view(self) -> CacheView:
+        r = lambda t: _ptr(t) if t.numel() else ctypes.c_void_p(0)
+        return CacheView(r(self.k_codes), r(self.v_codes), r(self.k_params), r(self.v_params),
+                         r(self.k_res), r(self.v_res), _ptr(self.counters[0]),
+                         _ptr(self.counters[1]), _ptr(self.counters[2]), _ptr(self.err))
+
+    @property
+    def packed_len(self):
+        return self.counters[0]
+
+    @property
+    def res_len(self):
+        return self.counters[1]
+
+    @property
+    def res_head(self):
+        return self.counters[2]
+
+    def packed_bytes(self) -> int:
+        """Code + param bytes of the tokens currently packed (K and V)."""
+        D = self.desc
+        per_tok = 2 * (D.head_dim * D.bits // 8 + 4 * (D.head_dim // 32))
+        return int(self.packed_len.sum().item()) * D.num_kv_heads * per_tok
+
+
+def kvq_cache_bytes(desc: CacheDesc, which: int) -> int:
+    return int(load().kvq_cache_bytes(ctypes.byref(desc), which))
+
+
+def kvq_decode_workspace_bytes(desc: CacheDesc, num_q_heads: int) -> int:
+    return int(load().kvq_decode_workspace_bytes(ctypes.byref(desc), num_q_heads))
+
+
+def kvq_quantize_pack(cache: KVCache, k: torch.Tensor, v: torch.Tensor, seq_lens: torch.Tensor,
+                      stream=None) -> None:
+    """Pack a prefill; k, v fp16 [B][Hkv][Lmax][d], seq_lens int32 [B] on the device."""
+    _f16(k, "k"), _f16(v, "v")
+    if k.shape != v.shape or k.dim() != 4:
+        raise ValueError("k and v must both be [B][Hkv][Lmax][d]")
+    if seq_lens.dtype != torch.int32 or not seq_lens.is_cuda:
+        raise ValueError("seq_lens must be an int32 CUDA tensor")
+    st = load().kvq_quantize_pack(ctypes.byref(cache.desc), ctypes.byref(cache.view), _ptr(k),
+                                  _ptr(v), _ptr(seq_lens), int(k.shape[2]),
+                                  _stream(stream, k.device))
+    _check(st, "kvq_quantize_pack")
+
+
+def kvq_append(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, stream=None) -> None:
+    """Append one token per sequence; k_new, v_new fp16 [B][Hkv][d]."""
+    _f16(k_new, "k_new"), _f16(v_new, "v_new")
+    st = load().kvq_append(ctypes.byref(cache.desc), ctypes.byref(cache.view), _ptr(k_new),
+                           _ptr(v_new), _stream(stream, k_new.device))
+    _check(st, "kvq_append")
+
+
+def workspace_for(cache: KVCache, num_q_heads: int) -> torch.Tensor:
+    n = kvq_decode_workspace_bytes(cache.desc, num_q_heads)
+    if n == 0:
+        raise KvqError(KVQ_ERR_INVALID_ARG, "kvq_decode_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=cache.device)
+
+
+def kvq_decode_attention(cache: KVCache, q: torch.Tensor, out: torch.Tensor | None = None,
+                         workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """O = softmax(q K^T / sqrt(d)) V; q fp16 [B][Hq][d] -> out fp16 [B][Hq][d]."""
+    _f16(q, "q")
+    if out is None:
+        out = torch.empty_like(q)
+    _f16(out, "out")
+    if workspace is None:
+        workspace = workspace_for(cache, q.shape[1])
+    st = load().kvq_decode_attention(ctypes.byref(cache.desc), ctypes.byref(cache.view), _ptr(q),
+                                     int(q.shape[1]), _ptr(out), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(),
+                                     _stream(stream, q.device))
+    _check(st, "kvq_decode_attention")
+    return out
+
+
+def kvq_read_error(cache: KVCache, stream=None) -> tuple[int, int]:
+    """(status, raw error word); synchronizes the stream and clears the word."""
+    word = ctypes.c_uint32(0)
+    st = load().kvq_read_error(ctypes.byref(cache.view), ctypes.byref(word),
+                               _stream(stream, cache.device))
+    return st, word.value
+
+
+def kvq_version() -> int:
+    return int(load().kvq_version())

@@ -1,0 +1,60 @@
+"""Shared helpers of the GPU parity tests: run the same seeded inputs through the
+CUDA path (C ABI via the ctypes binding) and the CPU oracle, and compare."""
+
+import numpy as np
+import torch
+
+import oracle
+from bit_quantized_kv_pack_gb300 import kvq
+
+ATOL = 2e-3   # max abs error of the fp16 attention output vs the fp64 oracle
+RTOL_L2 = 1e-3  # relative L2 error of the same
+
+
+def gpu_cache(B, H, d, bits, cap, Nr, dev="cuda"):
+    return kvq.KVCache(B, H, d, bits, cap, Nr, device=dev)
+
+
+def ref_cache(B, H, d, bits, cap, Nr):
+    return oracle.Cache(B, H, d, bits, cap, Nr)
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().numpy()
+
+
+def assert_cache_equal(g, r, batches=None):
+    """Packed bytes of every used slot, the residual ring and the counters."""
+    pl = to_np(g.packed_len)
+    rl = to_np(g.res_len)
+    rh = to_np(g.res_head)
+    rows = range(len(r.packed_len)) if batches is None else batches
+    for i, b in enumerate(rows):
+        assert pl[b] == r.packed_len[i], (b, pl[b], r.packed_len[i])
+        assert rl[b] == r.res_len[i] and rh[b] == r.res_head[i], b
+        n = int(r.packed_len[i])
+        for name in ("k_codes", "v_codes", "k_params", "v_params"):
+            got = to_np(getattr(g, name)[b, :, :n]).view(getattr(r, name).dtype)
+            want = getattr(r, name)[i, :, :n]
+            if not np.array_equal(got, want):
+                bad = np.argwhere(got != want)[:5]
+                raise AssertionError(f"{name} differs for sequence {b} at {bad.tolist()}")
+        nres = int(r.res_len[i])
+        for name in ("k_res", "v_res"):
+            got = to_np(getattr(g, name)[b]).view(np.uint16)
+            want = getattr(r, name)[i]
+            assert np.array_equal(got[:, :nres], want[:, :nres]), (name, b)
+
+
+def attn_errors(out: torch.Tensor, want: np.ndarray):
+    o = to_np(out.float()).astype(np.float64)
+    err = np.abs(o - want)
+    rel = np.linalg.norm(o - want) / max(np.linalg.norm(want), 1e-300)
+    return float(err.max()), float(rel)
+
+
+def assert_attn_close(out, want, atol=ATOL, rtol=RTOL_L2):
+    err, rel = attn_errors(out, want)
+    assert np.isfinite(to_np(out.float())).all()
+    assert err <= atol and rel <= rtol, f"max abs {err:.3e} (<= {atol}), rel L2 {rel:.3e} (<= {rtol})"
+    return err, rel

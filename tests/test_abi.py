@@ -1,0 +1,128 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads,
+exports every function include/kvq.h declares, and the pure host entry points
+(sizes, status strings, argument validation) behave as documented.  Calls that
+would launch kernels are only made with arguments the host rejects."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from bit_quantized_kv_pack_gb300 import _build, kvq
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "kvq.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return kvq.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]*?\b(kvq_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_and_library_exports(lib):
+    names = _declared()
+    assert set(kvq.EXPORTS) <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in kvq.h but not exported"
+    assert kvq.kvq_version() == 100
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert kvq.status_string(code) and kvq.status_string(code) != "unknown status"
+    assert kvq.status_string(99) == "unknown status"
+
+
+def _desc(**kw):
+    base = dict(batch=2, num_kv_heads=8, head_dim=128, bits=4, group=32, capacity=1000, residual=128)
+    base.update(kw)
+    return kvq.CacheDesc(**base)
+
+
+def test_cache_bytes(lib):
+    D = _desc()
+    assert kvq.kvq_cache_bytes(D, kvq.KVQ_ARRAY_CODES) == 2 * 8 * 1000 * 64
+    assert kvq.kvq_cache_bytes(D, kvq.KVQ_ARRAY_PARAMS) == 2 * 8 * 1000 * 4 * 4
+    assert kvq.kvq_cache_bytes(D, kvq.KVQ_ARRAY_RESIDUAL) == 2 * 8 * 128 * 128 * 2
+    D2 = _desc(bits=2, head_dim=64)
+    assert kvq.kvq_cache_bytes(D2, kvq.KVQ_ARRAY_CODES) == 2 * 8 * 1000 * 16
+    assert kvq.kvq_cache_bytes(D2, kvq.KVQ_ARRAY_PARAMS) == 2 * 8 * 1000 * 2 * 4
+    assert kvq.kvq_cache_bytes(D, 7) == 0
+    for bad in (dict(bits=3), dict(head_dim=96), dict(head_dim=100), dict(group=64),
+                dict(batch=0), dict(residual=-1), dict(residual=2000), dict(capacity=-5)):
+        assert kvq.kvq_cache_bytes(_desc(**bad), kvq.KVQ_ARRAY_CODES) == 0, bad
+
+
+def test_workspace_bytes(lib):
+    D = _desc()
+    n = kvq.kvq_decode_workspace_bytes(D, 32)
+    assert n > 0 and n % 8 == 0
+    assert kvq.kvq_decode_workspace_bytes(D, 12) == 0  # 12 % 8 != 0
+    assert kvq.kvq_decode_workspace_bytes(D, 0) == 0
+
+
+def _view(addr=0x10000):
+    # fake, well-aligned addresses: only ever passed to calls the host rejects
+    return kvq.CacheView(*[ctypes.c_void_p(addr + 0x1000 * i) for i in range(10)])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(bits=3), kvq.KVQ_ERR_UNSUPPORTED),
+    (dict(head_dim=96), kvq.KVQ_ERR_UNSUPPORTED),
+    (dict(head_dim=40), kvq.KVQ_ERR_INVALID_ARG),
+    (dict(group=16), kvq.KVQ_ERR_INVALID_ARG),
+    (dict(batch=0), kvq.KVQ_ERR_INVALID_ARG),
+])
+def test_rejects_bad_desc(lib, kw, expect):
+    D, V = _desc(**kw), _view()
+    P = ctypes.c_void_p
+    assert lib.kvq_quantize_pack(ctypes.byref(D), ctypes.byref(V), P(0x100000), P(0x200000),
+                                 P(0x300000), 16, None) == expect
+    assert lib.kvq_append(ctypes.byref(D), ctypes.byref(V), P(0x100000), P(0x200000), None) == expect
+    assert lib.kvq_decode_attention(ctypes.byref(D), ctypes.byref(V), P(0x100000), 8, P(0x200000),
+                                    P(0x300000), 1 << 30, None) == expect
+
+
+def test_rejects_bad_view_and_args(lib):
+    D = _desc()
+    P = ctypes.c_void_p
+    assert lib.kvq_append(ctypes.byref(D), None, P(0x100000), P(0x200000), None) == kvq.KVQ_ERR_INVALID_ARG
+    V = _view()
+    V.k_codes = 0
+    assert lib.kvq_append(ctypes.byref(D), ctypes.byref(V), P(0x100000), P(0x200000), None) == kvq.KVQ_ERR_INVALID_ARG
+    V = _view()
+    V.k_params = 0x10008  # 8-byte aligned only
+    assert lib.kvq_append(ctypes.byref(D), ctypes.byref(V), P(0x100000), P(0x200000), None) == kvq.KVQ_ERR_MISALIGNED
+    V = _view()
+    assert lib.kvq_append(ctypes.byref(D), ctypes.byref(V), P(0x100004), P(0x200000), None) == kvq.KVQ_ERR_MISALIGNED
+    assert lib.kvq_append(ctypes.byref(D), ctypes.byref(V), None, P(0x200000), None) == kvq.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_quantize_pack(ctypes.byref(D), ctypes.byref(V), P(0x100000), P(0x200000),
+                                 P(0x300000), -1, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_quantize_pack(ctypes.byref(D), ctypes.byref(V), P(0x100000), P(0x200000),
+                                 None, 16, None) == kvq.KVQ_ERR_INVALID_ARG
+    # decode: Hq not a multiple of Hkv, too small a workspace, misaligned q
+    assert lib.kvq_decode_attention(ctypes.byref(D), ctypes.byref(V), P(0x100000), 12, P(0x200000),
+                                    P(0x300000), 1 << 30, None) == kvq.KVQ_ERR_INVALID_ARG
+    need = kvq.kvq_decode_workspace_bytes(D, 32)
+    assert lib.kvq_decode_attention(ctypes.byref(D), ctypes.byref(V), P(0x100000), 32, P(0x200000),
+                                    P(0x300000), need - 1, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_decode_attention(ctypes.byref(D), ctypes.byref(V), P(0x100002), 32, P(0x200000),
+                                    P(0x300000), need, None) == kvq.KVQ_ERR_MISALIGNED
+    assert lib.kvq_read_error(None, None, None) == kvq.KVQ_ERR_INVALID_ARG
+
+
+def test_missing_library_raises(tmp_path):
+    import importlib
+    mod = importlib.reload(kvq)
+    try:
+        with pytest.raises(RuntimeError, match="not built"):
+            mod._lib = None
+            mod.load(str(tmp_path / "nope.so"))
+    finally:
+        mod._lib = None

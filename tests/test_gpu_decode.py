@@ -1,0 +1,132 @@
+"""GPU parity of decode attention: the fp16 output of the CUDA path against the
+fp64 oracle on the same packed cache, within max abs 2e-3 and relative L2 1e-3,
+on the five workloads' decode shapes (the batched one sampled) and a sweep of
+small shapes with ragged tails; plus the device-side error paths."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_quantized_kv_pack_gb300 import kvq, synth
+
+from _util import assert_attn_close, attn_errors, gpu_cache, ref_cache, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _setup(k, v, lens, bits, cap, Nr):
+    B, H, Lmax, d = k.shape
+    g = gpu_cache(B, H, d, bits, cap, Nr)
+    kvq.kvq_quantize_pack(g, k.to(DEV), v.to(DEV), lens.to(DEV))
+    r = ref_cache(B, H, d, bits, cap, Nr)
+    assert oracle.quantize_pack(r, to_np(k), to_np(v), to_np(lens)) == 0
+    return g, r
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+@pytest.mark.parametrize("d,gq", [(32, 1), (64, 2), (128, 4), (128, 3), (256, 8), (64, 16), (128, 5)])
+def test_decode_sweep(bits, d, gq):
+    rng = np.random.default_rng(bits * 1000 + d * 10 + gq)
+    B, H, Nr = 3, 2, 19
+    lens = torch.tensor([700, 1, 243], dtype=torch.int32)
+    Lmax = int(lens.max())
+    k = torch.from_numpy((rng.standard_normal((B, H, Lmax, d)) * 2).astype(np.float16))
+    v = torch.from_numpy(rng.standard_normal((B, H, Lmax, d)).astype(np.float16))
+    q = torch.from_numpy(rng.standard_normal((B, H * gq, d)).astype(np.float16))
+    g, r = _setup(k, v, lens, bits, Lmax, Nr)
+    ws = kvq.workspace_for(g, H * gq)
+    ws.fill_(0xFF)  # NaN bytes: the workspace's prior contents must not matter
+    out = kvq.kvq_decode_attention(g, q.to(DEV), workspace=ws)
+    assert kvq.kvq_read_error(g)[0] == kvq.KVQ_OK
+    assert_attn_close(out, oracle.decode(r, q.numpy()))
+
+
+@pytest.mark.parametrize("Nr", [0, 64])
+def test_decode_residual_only_and_packed_only(Nr):
+    rng = np.random.default_rng(Nr + 5)
+    B, H, d, gq = 2, 2, 128, 4
+    lens = torch.tensor([40, 64], dtype=torch.int32)
+    k = torch.from_numpy(rng.standard_normal((B, H, 64, d)).astype(np.float16))
+    v = torch.from_numpy(rng.standard_normal((B, H, 64, d)).astype(np.float16))
+    q = torch.from_numpy(rng.standard_normal((B, H * gq, d)).astype(np.float16))
+    g, r = _setup(k, v, lens, 4, 64, Nr)
+    out = kvq.kvq_decode_attention(g, q.to(DEV))
+    assert_attn_close(out, oracle.decode(r, q.numpy()))
+
+
+def test_decode_empty_sequence_sets_error_and_zeros():
+    rng = np.random.default_rng(77)
+    B, H, d = 2, 1, 64
+    k = torch.from_numpy(rng.standard_normal((B, H, 10, d)).astype(np.float16))
+    lens = torch.tensor([10, 0], dtype=torch.int32)
+    g, r = _setup(k, k, lens, 4, 10, 4)
+    q = torch.from_numpy(rng.standard_normal((B, H, d)).astype(np.float16))
+    out = kvq.kvq_decode_attention(g, q.to(DEV))
+    st, word = kvq.kvq_read_error(g)
+    assert st == kvq.KVQ_ERR_EMPTY and word == kvq.KVQ_ERRBIT_EMPTY
+    assert torch.all(out[1] == 0)
+    want = oracle.decode(r, q.numpy())
+    assert_attn_close(out[:1], want[:1])
+
+
+@pytest.mark.parametrize("num", [1, 2, 3])
+def test_decode_workload_full_size(num):
+    """Workloads 1-3 at full size: prefill packed (Nr in the residual), then one
+    decode step of append + attention, every output row against the oracle."""
+    w = synth.WORKLOADS[num]
+    k, v, lens = w.prefill(device=DEV)
+    cap = w.len_max - w.residual + 8
+    g, r = _setup(k, v, lens, w.bits, cap, w.residual)
+    kn, vn = w.new_tokens(0)
+    kvq.kvq_append(g, kn.to(DEV), vn.to(DEV))
+    oracle.append(r, kn.numpy(), vn.numpy())
+    q = w.query(0)
+    out = kvq.kvq_decode_attention(g, q.to(DEV))
+    assert kvq.kvq_read_error(g)[0] == kvq.KVQ_OK
+    err, rel = assert_attn_close(out, oracle.decode(r, q.numpy()))
+    print(f"workload {num}: max abs {err:.2e}, rel L2 {rel:.2e}")
+
+
+def test_decode_ragged_batch_workload_sampled():
+    """Llama-2-13B batch at full size (B64, 40 heads, ragged 1024..4096, Nr96):
+    the oracle recomputes 48 sampled (sequence, head) rows, including the
+    shortest and longest sequences."""
+    w = synth.WORKLOADS[4]
+    k, v, lens = w.prefill(device=DEV)
+    cap = w.len_max - w.residual
+    g = gpu_cache(w.batch, w.num_kv_heads, w.head_dim, w.bits, cap, w.residual)
+    kvq.kvq_quantize_pack(g, k, v, lens.to(DEV))
+    q = w.query(0)
+    out = kvq.kvq_decode_attention(g, q.to(DEV))
+    assert kvq.kvq_read_error(g)[0] == kvq.KVQ_OK
+    order = torch.argsort(lens)
+    seqs = sorted({int(order[0]), int(order[-1]), 3, 20, 41, 62})
+    r = ref_cache(len(seqs), w.num_kv_heads, w.head_dim, w.bits, cap, w.residual)
+    sub = torch.tensor(seqs)
+    sd = sub.to(DEV)
+    assert oracle.quantize_pack(r, to_np(k[sd]), to_np(v[sd]), to_np(lens[sub])) == 0
+    rng = np.random.default_rng(4)
+    pairs = np.array([(i, int(h)) for i in range(len(seqs)) for h in rng.choice(40, 8, replace=False)],
+                     np.int32)
+    want = oracle.decode(r, q[sub].numpy(), pairs)
+    rows_b = sub[torch.from_numpy(pairs[:, 0]).long()].to(DEV)
+    rows_h = torch.from_numpy(pairs[:, 1]).long().to(DEV)
+    got = out[rows_b, rows_h]
+    err, rel = assert_attn_close(got, want)
+    print(f"workload 4 (48 rows): max abs {err:.2e}, rel L2 {rel:.2e}")
+
+
+def test_decode_is_deterministic_and_stream_ordered():
+    rng = np.random.default_rng(8)
+    B, H, d, L = 1, 8, 128, 3000
+    k = torch.from_numpy(rng.standard_normal((B, H, L, d)).astype(np.float16))
+    g, r = _setup(k, k, torch.tensor([L], dtype=torch.int32), 4, L, 128)
+    q = torch.from_numpy(rng.standard_normal((B, 32, d)).astype(np.float16)).to(DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        a = kvq.kvq_decode_attention(g, q)
+        b = kvq.kvq_decode_attention(g, q)
+    s.synchronize()
+    assert torch.equal(a, b)
