@@ -89,6 +89,8 @@ def load(path: str | None = None):
             lib.kvq_append.restype = ctypes.c_int
             lib.kvq_decode_attention.argtypes = [DP, VP, P, i32, P, P, sz, P]
             lib.kvq_decode_attention.restype = ctypes.c_int
+            lib.kvq_decode_attention_noalloc.argtypes = [DP, VP, P, i32, P, P]
+            lib.kvq_decode_attention_noalloc.restype = ctypes.c_int
             lib.kvq_read_error.argtypes = [VP, ctypes.POINTER(ctypes.c_uint32), P]
             lib.kvq_read_error.restype = ctypes.c_int
             lib.kvq_status_string.argtypes = [ctypes.c_int]
@@ -228,6 +230,25 @@ def kvq_decode_attention(cache: KVCache, q: torch.Tensor, out: torch.Tensor | No
                                      workspace.numel() * workspace.element_size(),
                                      _stream(stream, q.device))
     _check(st, "kvq_decode_attention")
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def kvq_decode_attention_noalloc(cache: KVCache, q: torch.Tensor, out: torch.Tensor | None = None,
+                                 stream=None) -> torch.Tensor:
+    """Decode attention for callers that cannot allocate device scratch: the
+    library's own static device array holds the split partials.  Calls that
+    overlap on the GPU share that array and race; keep them on one stream."""
+    _f16(q, "q")
+    if out is None:
+        out = torch.empty_like(q)
+    _f16(out, "out")
+    st = load().kvq_decode_attention_noalloc(ctypes.byref(cache.desc), ctypes.byref(cache.view),
+                                             _ptr(q), int(q.shape[1]), _ptr(out),
+                                             _stream(stream, q.device))
+    _check(st, "kvq_decode_attention_noalloc")
     return out
 
 

@@ -181,6 +181,29 @@ kvq_status kvq_decode_attention(const kvq_cache_desc* desc, const kvq_cache_view
                                 const void* q, int32_t num_q_heads, void* out,
                                 void* workspace, size_t ws_bytes, void* stream);
 
+/* Size of the device scratch array behind kvq_decode_attention_noalloc (8 MiB). */
+#define KVQ_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* Decode attention without any caller-provided scratch, for callers that cannot
+ * allocate device memory when they decode (a runtime that forbids cudaMalloc in
+ * its serving loop, an allocator the caller does not own, memory fixed at start
+ * up).  No passage of the pages corresponds to this call; it is an addition of
+ * this library.
+ * Same arguments, output and error bits as kvq_decode_attention, minus the
+ * workspace: the split partials go to one static device array of
+ * KVQ_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until the
+ * process exits.  Returns KVQ_ERR_UNSUPPORTED when the decode would need more
+ * than that (kvq_decode_workspace_bytes(desc, num_q_heads) > the maximum) and
+ * KVQ_ERR_INVALID_ARG for an invalid description or head count.  Allocates
+ * nothing.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call before
+ * any stream capture.  All calls share the array and it keeps the last call's
+ * contents (none of which need to start at zero), so calls whose kernels
+ * overlap on the GPU race: keep them on one stream or order the streams. */
+kvq_status kvq_decode_attention_noalloc(const kvq_cache_desc* desc, const kvq_cache_view* view,
+                                        const void* q, int32_t num_q_heads, void* out,
+                                        void* stream);
+
 /* Synchronize `stream`, copy *err_word to *word_out (may be NULL), clear it, and
  * return KVQ_OK if it was 0, else the status of its lowest set bit. */
 kvq_status kvq_read_error(const kvq_cache_view* view, uint32_t* word_out, void* stream);

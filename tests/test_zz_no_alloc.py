@@ -1,0 +1,61 @@
+"""The allocation-free decode entry point (for callers that cannot allocate
+device memory while decoding): called through the C ABI, its output must match
+the regular entry point's within the attention tolerance of the other tests,
+on two calls in a row (the static scratch keeps the first call's contents).
+This file is collected last on purpose."""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from bit_quantized_kv_pack_gb300 import _build, kvq
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _decode_noalloc_abi(cache, q, out):
+    lib = kvq.load()
+    st = lib.kvq_decode_attention_noalloc(
+        ctypes.byref(cache.desc), ctypes.byref(cache.view), ctypes.c_void_p(q.data_ptr()),
+        int(q.shape[1]), ctypes.c_void_p(out.data_ptr()),
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    return st
+
+
+def test_noalloc_matches_regular_decode_twice():
+    _build.build()
+    rng = np.random.default_rng(2024)
+    B, H, gq, d, Nr = 2, 8, 4, 128, 128
+    lens = torch.tensor([5000, 1300], dtype=torch.int32)
+    L = int(lens.max())
+    cache = kvq.KVCache(B, H, d, 4, L, Nr, device=DEV)
+    k = torch.from_numpy((rng.standard_normal((B, H, L, d)) * 2).astype(np.float16)).to(DEV)
+    v = torch.from_numpy(rng.standard_normal((B, H, L, d)).astype(np.float16)).to(DEV)
+    kvq.kvq_quantize_pack(cache, k, v, lens.to(DEV))
+    assert kvq.kvq_decode_workspace_bytes(cache.desc, H * gq) <= kvq.NOALLOC_SCRATCH_BYTES
+    for call in range(2):
+        q = torch.from_numpy(rng.standard_normal((B, H * gq, d)).astype(np.float16)).to(DEV)
+        want = kvq.kvq_decode_attention(cache, q)
+        got = torch.full_like(q, float("nan"))
+        assert _decode_noalloc_abi(cache, q, got) == kvq.KVQ_OK
+        torch.cuda.synchronize()
+        diff = (got.float() - want.float()).abs().max().item()
+        rel = ((got.float() - want.float()).norm() / want.float().norm()).item()
+        assert diff <= 2e-3 and rel <= 1e-3, (call, diff, rel)
+    st, word = kvq.kvq_read_error(cache)
+    assert st == kvq.KVQ_OK and word == 0
+
+
+def test_noalloc_rejects_oversized_request():
+    # a description whose decode scratch exceeds the static array
+    D = kvq.CacheDesc(2048, 16, 256, 4, 32, 1 << 20, 0)
+    need = kvq.kvq_decode_workspace_bytes(D, 16 * 8)
+    assert need > kvq.NOALLOC_SCRATCH_BYTES
+    V = kvq.CacheView(*[ctypes.c_void_p(0x100000 * (i + 1)) for i in range(10)])
+    st = kvq.load().kvq_decode_attention_noalloc(ctypes.byref(D), ctypes.byref(V),
+                                                 ctypes.c_void_p(0x100000), 16 * 8,
+                                                 ctypes.c_void_p(0x200000), None)
+    assert st == kvq.KVQ_ERR_UNSUPPORTED
