@@ -36,7 +36,8 @@ import torch  # noqa: E402
 
 WORKLOAD = 2
 FALLBACK_HBM_GBS = 6800.0
-DECODE_SOURCES = ("kvq_decode.cu", "kvq_decode_generic.cu", "kvq_decode_common.cuh")
+DECODE_SOURCES = ("kvq_decode.cu", "kvq_decode_generic.cu", "kvq_decode_common.cuh",
+                  "kvq_decode_tc.cu", "kvq_ptx.cuh")
 
 
 # ----------------------------------------------------------------- helpers --
@@ -48,10 +49,21 @@ def dist_info():
     return rank, world, local
 
 
-def aggregate(values, ms_list):
-    """Whole-job figures from per-rank results: value summed (replicas, weak
-    scaling), time the max over ranks."""
-    return sum(values), max(ms_list)
+def reduce_across_ranks(ms_per_step: float, e2e_value: float, step_bytes: int, device):
+    """Whole-job figures of N independent replicas: the step time is the max over
+    ranks, the throughput counts every rank's bytes over that time (weak
+    scaling), and the end-to-end throughputs add up.  Works with any
+    torch.distributed backend (nccl on GPUs, gloo on CPU)."""
+    import torch.distributed as dist
+    world = dist.get_world_size()
+    t = torch.tensor([ms_per_step, e2e_value], dtype=torch.float64, device=device)
+    tmax = t.clone()
+    dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+    tsum = t.clone()
+    dist.all_reduce(tsum, op=dist.ReduceOp.SUM)
+    ms_all = float(tmax[0])
+    value_all = step_bytes * world / (ms_all * 1e-3) / 1e9
+    return ms_all, value_all, float(tsum[1])
 
 
 def measured_peak():
@@ -105,6 +117,8 @@ class ClockSampler:
         self.lines = []
 
     def __enter__(self):
+        import threading
+        self._first = threading.Event()
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
@@ -112,17 +126,29 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+            return self
+
+        def reader():
+            for ln in self.proc.stdout:
+                if ln.strip():
+                    self.lines.append(ln.strip())
+                    self._first.set()
+        self._thread = threading.Thread(target=reader, daemon=True)
+        self._thread.start()
+        # nvidia-smi's start-up can stall the GPU briefly: let it reach steady
+        # sampling before the timed region begins
+        self._first.wait(timeout=10.0)
+        time.sleep(0.3)
         return self
 
     def __exit__(self, *exc):
         if self.proc is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+            self._thread.join(timeout=5)
 
     def summary(self):
         sm, mx, reasons = [], None, set()
@@ -245,7 +271,6 @@ def run_ours(args, rank, world, local):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        time.sleep(0.25)  # let the sampler start
         ms = time_graph(g_step, reps, g_step_rem)
         ms_dec = time_graph(g_dec, reps, g_dec_rem)
         # keep the same kernels running long enough for several clock samples
@@ -273,14 +298,8 @@ def run_ours(args, rank, world, local):
 
     clocks = clk.summary()
     if world > 1:
-        t = torch.tensor([ms_per_step, value, e2e["value"]], device=dev, dtype=torch.float64)
-        tmax = t.clone()
-        torch.distributed.all_reduce(tmax, op=torch.distributed.ReduceOp.MAX)
-        tsum = t.clone()
-        torch.distributed.all_reduce(tsum, op=torch.distributed.ReduceOp.SUM)
-        ms_step_all = float(tmax[0])
-        value_all = step_bytes * world / (ms_step_all * 1e-3) / 1e9
-        e2e["value"] = float(tsum[2])
+        ms_step_all, value_all, e2e["value"] = reduce_across_ranks(ms_per_step, e2e["value"],
+                                                                   step_bytes, dev)
     else:
         ms_step_all, value_all = ms_per_step, value
 
