@@ -1,5 +1,5 @@
 // kvq_decode_generic.cu -- split-KV decode attention on CUDA cores (any head_dim
-// in {32, 64, 128, 256}, any GQA ratio) and the log-sum-exp combine.
+// in {32, 64, 128, 256}, any GQA ratio).
 //
 // Computes O = softmax(q K^T / sqrt(d)) V for every query head over the packed
 // tokens, dequantized as min + code * scale (InnerQ page, section 3.1), and the
@@ -14,7 +14,7 @@
 // Split-KV: each (sequence, KV head, query block) is cut into S pieces of about
 // equal byte cost (a packed token costs its code and param bytes, a residual
 // token its fp16 bytes, both for K and V); each CTA writes a partial (o, m, l)
-// and the combine kernel merges the S partials.
+// and the last one to finish merges the S partials (combine_unit).
 #include <math.h>
 
 #include "kvq_internal.cuh"
@@ -223,18 +223,38 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(DecodeArgs a) 
     a.o_part[(pidx * QB + i) * D + e] = osum;
     if (e == 0) a.ml_part[pidx * QB + i] = make_float2(M, lsum);
   }
+  // the last split of this (KV head, query block) to finish merges all S partials
+  __shared__ int s_last;
+  if (take_last_ticket<kThreads>(a, ((int64_t)b * a.Hkv + h) * a.nqb + qbi, &s_last)) {
+    extern __shared__ float dyn_scratch[];
+    combine_unit<kThreads, D>(a, b, h, qbi, dyn_scratch);
+  }
+}
+
+template <int D, int BITS, int QB>
+cudaError_t launch_one(dim3 grid, size_t smem, const DecodeArgs& a, cudaStream_t st) {
+  static size_t smem_set = 0;  // largest dynamic size opted in so far for this instance
+  if (smem > smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(decode_generic_kernel<D, BITS, QB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    smem_set = smem;
+  }
+  decode_generic_kernel<D, BITS, QB><<<grid, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
 }
 
 template <int D, int BITS>
 cudaError_t launch_generic_d_bits(const DecodePlan& p, dim3 grid, const DecodeArgs& a,
                                   cudaStream_t st) {
+  // dynamic shared memory: the combine's weights, S * qb + 2 * qb floats
+  const size_t smem = (size_t)(p.splits * p.qb + 2 * p.qb) * sizeof(float);
   switch (p.qb) {
-    case 1: decode_generic_kernel<D, BITS, 1><<<grid, kThreads, 0, st>>>(a); break;
-    case 2: decode_generic_kernel<D, BITS, 2><<<grid, kThreads, 0, st>>>(a); break;
-    case 4: decode_generic_kernel<D, BITS, 4><<<grid, kThreads, 0, st>>>(a); break;
-    default: decode_generic_kernel<D, BITS, 8><<<grid, kThreads, 0, st>>>(a); break;
+    case 1: return launch_one<D, BITS, 1>(grid, smem, a, st);
+    case 2: return launch_one<D, BITS, 2>(grid, smem, a, st);
+    case 4: return launch_one<D, BITS, 4>(grid, smem, a, st);
+    default: return launch_one<D, BITS, 8>(grid, smem, a, st);
   }
-  return cudaGetLastError();
 }
 
 template <int D>

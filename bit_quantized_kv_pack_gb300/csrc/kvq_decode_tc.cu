@@ -1,0 +1,759 @@
+// kvq_decode_tc.cu -- split-KV decode attention on the tensor cores (head_dim
+// 128, up to 4 query heads per KV head, INT4 or INT2 codes).
+//
+// What it computes is the same as the generic kernel: O = softmax(q K^T /
+// sqrt(d)) V over the packed tokens (dequantized min + code * scale, InnerQ page
+// section 3.1) and the fp16 residual window (BitDecoding page section 2.2), all
+// query heads of one KV head served by one read of the cache (BitDecoding page
+// section 2.3).  How:
+//
+//  * 128-token tiles -- K codes, V codes, K params, V params -- stream in by 2D
+//    TMA tile loads into a 4-stage (INT4) or 6-stage (INT2) shared-memory ring
+//    guarded by mbarriers (the asynchronous staging of the BitDecoding page,
+//    section 2.3, done with the bulk tensor copy instead of per-thread
+//    cp.async).  One thread issues the first stages up front and refills a
+//    stage as soon as all four warps have released it.  Code
+//    tiles use the TMA 64-byte (INT4) or 32-byte (INT2) swizzle, the XOR
+//    swizzle of the BitDecoding page's equation (2), which makes every ldmatrix
+//    below conflict-free.
+//  * Four warps take 32 tokens (two independent 16-token sub-tiles) each per
+//    tile.  ldmatrix brings code words to
+//    registers; a magic-number lop3 (0x6400 | c is the fp16 value 1024 + c) and
+//    one HADD2/HFMA2 turn them into the exact fp16 integers c - C (C = 8 for
+//    INT4, 2 for INT2).  Integer codes are exact in fp16, so the tensor cores
+//    see exact operands; scale and min are applied in fp32.
+//  * QK:  S^T = K q^T with tokens on M (mma.sync m16n8k16, fp32 accumulate).
+//    Two groups share one MMA through a block-diagonal q operand (columns 0-3
+//    hold group a's queries, columns 4-7 group b's), then per thread
+//      s = sum_g scale_g * acc_g + (min_g + C * scale_g) * sum_{d in g} q_d.
+//  * Online softmax in fp32 (exp2 domain) with a lazy rescale: the running max
+//    only moves when it grows by more than 2^8.
+//  * PV:  O^T = (c - C)^T (p * scale)^T with V codes read through
+//    ldmatrix.trans; the per-token, per-group p * scale is the B operand.  A
+//    ninth MMA accumulates sum p * min_g, sum p * scale_g and sum p (= l) per
+//    group, so O = O_c + sum p min_g + C sum p scale_g.
+//  * Residual tokens (fp16) use the CUDA-core loop of the generic kernel; the
+//    per-warp states merge in shared memory, and the last split of a KV head to
+//    finish merges the split partials (combine_unit).
+//
+// Every mbarrier wait is bounded; a wait that runs out sets KVQ_ERRBIT_TIMEOUT.
+#include <math.h>
+
+#include "kvq_decode_common.cuh"
+#include "kvq_ptx.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr int D = 128;
+constexpr int NG = D / kGroup;  // 4 groups per row
+constexpr int QB = 4;           // query heads per CTA
+constexpr int T = 128;          // tokens per pipeline stage
+constexpr int NCW = 4;          // warps, 32 tokens (two 16-token sub-tiles) each per stage
+constexpr int NSUB = 2;         // sub-tiles per warp per stage
+constexpr int NTHREADS = NCW * 32;
+
+template <int BITS>
+struct Geo {
+  static constexpr int RB = D * BITS / 8;      // code bytes per token row
+  static constexpr int CODE_TILE = T * RB;     // 8192 (INT4) / 4096 (INT2)
+  static constexpr int PAR_TILE = T * NG * 4;  // 2048
+  static constexpr int KC = 0;
+  static constexpr int VC = CODE_TILE;
+  static constexpr int KP = 2 * CODE_TILE;
+  static constexpr int VP = 2 * CODE_TILE + PAR_TILE;
+  static constexpr int STAGE = 2 * CODE_TILE + 2 * PAR_TILE;  // 20 KB / 12 KB
+  static constexpr int NSTAGE = BITS == 4 ? 4 : 6;               // 80 KB / 72 KB in flight
+  static constexpr int CENTER = BITS == 4 ? 8 : 2;
+  static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned");
+};
+
+// Shared scratch for the final merge (overlaps the stage ring once it is idle).
+struct MergeSmem {
+  float o[2 * NCW][QB][D];
+  float m[2 * NCW][QB];
+  float l[2 * NCW][QB];
+  float mn[NCW][9][8];
+};
+
+template <int BITS>
+constexpr size_t tc_smem_bytes() {
+  constexpr size_t ring = (size_t)Geo<BITS>::NSTAGE * Geo<BITS>::STAGE;
+  return 1024 + (ring > sizeof(MergeSmem) ? ring : sizeof(MergeSmem));
+}
+
+// ------------------------------------------------------- code conversion ---
+
+__device__ __forceinline__ uint32_t h2const(float v) {
+  return ptx::h2_as_u32(__float2half2_rn(v));
+}
+
+// INT4: word with 8 nibbles (n0 at bits 0-3 ... n7 at 28-31) -> 4 half2 of c - 8:
+// out[0] = (n0, n4), out[1] = (n1, n5), out[2] = (n2, n6), out[3] = (n3, n7).
+__device__ __forceinline__ void cvt_int4(uint32_t w, uint32_t (&o)[4]) {
+  const uint32_t magic = 0x64006400u;
+  const uint32_t sub_lo = h2const(-(1024.f + 8.f));
+  const uint32_t mul_hi = h2const(1.f / 16.f);
+  const uint32_t sub_hi = h2const(-(64.f + 8.f));
+  const uint32_t w8 = w >> 8;
+  o[0] = ptx::hadd2_u32(ptx::and_or(w, 0x000F000Fu, magic), sub_lo);
+  o[1] = ptx::hfma2_u32(ptx::and_or(w, 0x00F000F0u, magic), mul_hi, sub_hi);
+  o[2] = ptx::hadd2_u32(ptx::and_or(w8, 0x000F000Fu, magic), sub_lo);
+  o[3] = ptx::hfma2_u32(ptx::and_or(w8, 0x00F000F0u, magic), mul_hi, sub_hi);
+}
+
+// INT2: the four 2-bit codes at bits [2j, 2j+2) of each 16-bit half (j = 0..3)
+// -> 4 half2 of c - 2: out[j] = (code j of the low half, code j of the high half).
+__device__ __forceinline__ void cvt_int2_lo4(uint32_t w, uint32_t (&o)[4]) {
+  const uint32_t magic = 0x64006400u;
+  o[0] = ptx::hadd2_u32(ptx::and_or(w, 0x00030003u, magic), h2const(-(1024.f + 2.f)));
+  o[1] = ptx::hfma2_u32(ptx::and_or(w, 0x000C000Cu, magic), h2const(0.25f), h2const(-(256.f + 2.f)));
+  o[2] = ptx::hfma2_u32(ptx::and_or(w, 0x00300030u, magic), h2const(1.f / 16.f), h2const(-(64.f + 2.f)));
+  o[3] = ptx::hfma2_u32(ptx::and_or(w, 0x00C000C0u, magic), h2const(1.f / 64.f), h2const(-(16.f + 2.f)));
+}
+
+// INT2: 16 codes (j = 0..15 at bits [2j, 2j+2)) -> 8 half2, out[m] = (code m, code m+8).
+__device__ __forceinline__ void cvt_int2_8(uint32_t w, uint32_t (&o)[8]) {
+  uint32_t a[4], b[4];
+  cvt_int2_lo4(w, a);
+  cvt_int2_lo4(w >> 8, b);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    o[j] = a[j];
+    o[4 + j] = b[j];
+  }
+}
+
+__device__ __forceinline__ uint32_t grp_of(const uint4& u, int x) {
+  return x == 0 ? u.x : (x == 1 ? u.y : (x == 2 ? u.z : u.w));
+}
+
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// QK of one 16-token sub-tile (rows r0 .. r0+15 of the stage): acc[P] holds the
+// per-pair partial dot products (fragment layout of S^T = K q^T).
+template <int BITS>
+__device__ __forceinline__ void qk_subtile(uint32_t kc, int r0, int lane,
+                                           const uint32_t (&bq)[2][4][2], float (&acc)[2][4]) {
+  const int mj = lane >> 3, mi = lane & 7;
+  const int lrow = r0 + (mj & 1) * 8 + mi;
+#pragma unroll
+  for (int P = 0; P < 2; ++P)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[P][r] = 0.f;
+  if (BITS == 4) {
+#pragma unroll
+    for (int P = 0; P < 2; ++P) {
+      const int chunk = (mj < 2) ? P : P + 2;
+      const uint32_t addr = kc + lrow * 64 + ((chunk ^ ((lrow >> 1) & 3)) << 4);
+      uint32_t w0, w1, w2, w3;
+      ptx::ldmatrix_x4(addr, w0, w1, w2, w3);
+      uint32_t c0[4], c1[4], c2[4], c3[4];
+      cvt_int4(w0, c0);
+      cvt_int4(w1, c1);
+      cvt_int4(w2, c2);
+      cvt_int4(w3, c3);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        ptx::mma_16816(acc[P], c0[k], c1[k], c2[k], c3[k], bq[P][k][0], bq[P][k][1]);
+    }
+  } else {
+    const int chunk = mj >> 1;
+    const uint32_t addr = kc + lrow * 32 + ((chunk ^ ((lrow >> 2) & 1)) << 4);
+    uint32_t w[4];
+    ptx::ldmatrix_x4(addr, w[0], w[1], w[2], w[3]);
+#pragma unroll
+    for (int P = 0; P < 2; ++P) {
+      uint32_t ca[8], cb[8];
+      cvt_int2_8(w[2 * P], ca);      // token g
+      cvt_int2_8(w[2 * P + 1], cb);  // token g + 8
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        ptx::mma_16816(acc[P], ca[2 * k], cb[2 * k], ca[2 * k + 1], cb[2 * k + 1], bq[P][k][0],
+                       bq[P][k][1]);
+    }
+  }
+}
+
+// PV of one 16-token sub-tile: O^T += (c - C)^T (p * scale)^T per group, and the
+// min/scale/ones MMA.  pb0/pb1 are the sub-tile's p as B fragments.
+template <int BITS>
+__device__ __forceinline__ void pv_subtile(uint32_t vc, const uint32_t* vp, int r0, int lane,
+                                           uint32_t pb0, uint32_t pb1, float (&oc)[NG][2][4],
+                                           float (&mnacc)[4]) {
+  const int g = lane >> 2, t = lane & 3;
+  const int mj = lane >> 3, mi = lane & 7;
+  const int lrow = r0 + (mj & 1) * 8 + mi;
+  const uint4* vrow = reinterpret_cast<const uint4*>(vp);
+  uint4 vpt[4];
+  vpt[0] = vrow[r0 + 2 * t];
+  vpt[1] = vrow[r0 + 2 * t + 1];
+  vpt[2] = vrow[r0 + 2 * t + 8];
+  vpt[3] = vrow[r0 + 2 * t + 9];
+  {
+    // A rows 0-3 = min_x, 4-7 = scale_x (x = g & 3), row 8 = ones; B = p
+    const int xg = g & 3;
+    const uint32_t hsel = g < 4 ? 0x7632u : 0x5410u;  // min (high half) or scale (low half)
+    const uint32_t am0 = ptx::prmt(vp[(r0 + 2 * t) * NG + xg], vp[(r0 + 2 * t + 1) * NG + xg], hsel);
+    const uint32_t am2 = ptx::prmt(vp[(r0 + 2 * t + 8) * NG + xg], vp[(r0 + 2 * t + 9) * NG + xg], hsel);
+    const uint32_t ones = g == 0 ? 0x3C003C00u : 0u;
+    ptx::mma_16816(mnacc, am0, ones, am2, ones, pb0, pb1);
+  }
+  if (BITS == 4) {
+#pragma unroll
+    for (int Pv = 0; Pv < 2; ++Pv) {
+      const int chunk = 2 * Pv + (mj >> 1);
+      const uint32_t addr = vc + lrow * 64 + ((chunk ^ ((lrow >> 1) & 3)) << 4);
+      uint32_t w[4];
+      ptx::ldmatrix_x4_trans(addr, w[0], w[1], w[2], w[3]);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int x = 2 * Pv + u;
+        const uint32_t bs0 = ptx::hmul2_u32(pb0, ptx::prmt(grp_of(vpt[0], x), grp_of(vpt[1], x), 0x5410u));
+        const uint32_t bs1 = ptx::hmul2_u32(pb1, ptx::prmt(grp_of(vpt[2], x), grp_of(vpt[3], x), 0x5410u));
+        uint32_t lo[4], hi[4];
+        cvt_int4(w[2 * u], lo);      // tokens 2t, 2t+1: d = 32x + 4g + j
+        cvt_int4(w[2 * u + 1], hi);  // tokens 2t+8, 2t+9
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+          ptx::mma_16816(oc[x][m], lo[2 * m], lo[2 * m + 1], hi[2 * m], hi[2 * m + 1], bs0, bs1);
+      }
+    }
+  } else {
+    const int chunk = mj >> 1;
+    const uint32_t addr = vc + lrow * 32 + ((chunk ^ ((lrow >> 2) & 1)) << 4);
+    uint32_t w[4];
+    ptx::ldmatrix_x4_trans(addr, w[0], w[1], w[2], w[3]);
+    const bool low = g < 4;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      // one b16 unit holds 8 codes of group 2c + (g >> 2); partner lanes
+      // (lane ^ 16) swap half of them so each lane holds 4 codes of each group
+      uint32_t X[2], Y[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t wv = w[2 * c + hh];
+        const uint32_t keep = low ? wv : (wv >> 8);
+        const uint32_t send = low ? (wv >> 8) : wv;
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 16);
+        X[hh] = low ? keep : recv;  // group 2c
+        Y[hh] = low ? recv : keep;  // group 2c + 1
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int x = 2 * c + u;
+        const uint32_t bs0 = ptx::hmul2_u32(pb0, ptx::prmt(grp_of(vpt[0], x), grp_of(vpt[1], x), 0x5410u));
+        const uint32_t bs1 = ptx::hmul2_u32(pb1, ptx::prmt(grp_of(vpt[2], x), grp_of(vpt[3], x), 0x5410u));
+        uint32_t lo[4], hi[4];
+        cvt_int2_lo4(u == 0 ? X[0] : Y[0], lo);  // tokens 2t, 2t+1
+        cvt_int2_lo4(u == 0 ? X[1] : Y[1], hi);  // tokens 2t+8, 2t+9
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+          ptx::mma_16816(oc[x][m], lo[2 * m], lo[2 * m + 1], hi[2 * m], hi[2 * m + 1], bs0, bs1);
+      }
+    }
+  }
+}
+
+// --------------------------------------------------------------- kernel ----
+
+template <int BITS>
+__global__ void __launch_bounds__(NTHREADS, 2)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
+                     const __grid_constant__ CUtensorMap tm_kp, const __grid_constant__ CUtensorMap tm_vp,
+                     const DecodeArgs a) {
+  using G = Geo<BITS>;
+  constexpr int C = G::CENTER;
+  constexpr int NSTAGE = G::NSTAGE;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  __shared__ __align__(8) uint64_t full_bar[NSTAGE];
+  __shared__ __align__(8) uint64_t empty_bar[NSTAGE];
+  __shared__ float q_s[QB][D];
+  __shared__ volatile int s_abort;
+  __shared__ int s_last;
+
+  const int s = blockIdx.x;
+  const int h = blockIdx.y;  // one query block per KV head (gq <= 4)
+  const int b = blockIdx.z;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;  // MMA group id
+  const int t = lane & 3;   // thread in group
+
+  // Prologue that touches no global memory; the rest waits for the grid this
+  // launch depends on (the append of the same step) to complete.
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < NSTAGE; ++st) {
+      ptx::mbar_init(ptx::smem_u32(&full_bar[st]), 1);
+      ptx::mbar_init(ptx::smem_u32(&empty_bar[st]), NCW);
+    }
+    s_abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (threadIdx.x == 0) {
+    ptx::prefetch_tensormap(&tm_kc);
+    ptx::prefetch_tensormap(&tm_vc);
+    ptx::prefetch_tensormap(&tm_kp);
+    ptx::prefetch_tensormap(&tm_vp);
+  }
+  grid_dependency_wait();
+
+  const int Lp = a.packed_len[b];
+  const int Lr = a.res_len[b];
+  const int rh = a.res_head[b];
+  int i0, i1, j0, j1;
+  split_range(Lp, Lr, s, a.S, 2 * (G::RB + 4 * NG), 4 * D, i0, i1, j0, j1);
+  const int npk = i1 - i0;
+  const int ntiles = (npk + T - 1) / T;
+  const int64_t bh = (int64_t)b * a.Hkv + h;
+  const int row0 = (int)(bh * a.cap + i0);  // first packed row of this split (TMA y)
+
+  for (int idx = threadIdx.x; idx < QB * D; idx += NTHREADS) {
+    const int i = idx / D, e = idx % D;
+    float v = 0.f;
+    if (i < a.gq) v = __half2float(a.q[((int64_t)b * a.Hq + h * a.gq + i) * D + e]);
+    q_s[i][e] = v;
+  }
+  if (s == 0 && Lp + Lr == 0 && threadIdx.x == 0) set_error(a.err_word, KVQ_ERRBIT_EMPTY);
+  __syncthreads();  // barriers initialised, q staged
+
+  // Issue tile `tile` into its stage (one thread).
+  auto issue = [&](int tile) {
+    const int st = tile % NSTAGE;
+    uint8_t* base = smem + (size_t)st * G::STAGE;
+    const uint32_t fb = ptx::smem_u32(&full_bar[st]);
+    ptx::mbar_arrive_expect_tx(fb, G::STAGE);
+    const int y = row0 + tile * T;
+    ptx::tma_load_2d(ptx::smem_u32(base + G::KC), &tm_kc, 0, y, fb);
+    ptx::tma_load_2d(ptx::smem_u32(base + G::VC), &tm_vc, 0, y, fb);
+    ptx::tma_load_2d(ptx::smem_u32(base + G::KP), &tm_kp, 0, y, fb);
+    ptx::tma_load_2d(ptx::smem_u32(base + G::VP), &tm_vp, 0, y, fb);
+  };
+  int issued = 0;  // meaningful in thread 0 only
+  if (threadIdx.x == 0) {
+    for (; issued < ntiles && issued < NSTAGE; ++issued) issue(issued);
+  }
+
+  const float kq = a.qk_scale_log2;
+
+  float m_ref[2] = {-INFINITY, -INFINITY};  // queries 2(t&1) + e, log2 units
+  float oc[NG][2][4];                        // O^T accumulators: [group][m-tile][frag]
+  float mnacc[4];                            // C-fragment of the min/scale/l MMA
+#pragma unroll
+  for (int x = 0; x < NG; ++x)
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) oc[x][m][r] = 0.f;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) mnacc[r] = 0.f;
+  // residual-token state (CUDA cores): lane owns head_dim values 4*lane .. 4*lane+3
+  float rm[QB], rl[QB], ro[QB][4];
+#pragma unroll
+  for (int i = 0; i < QB; ++i) {
+    rm[i] = -INFINITY;
+    rl[i] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) ro[i][j] = 0.f;
+  }
+
+  {
+    // ------------------------------------------------- consumers: residual
+    // The fp16 residual tokens go first, while the first tiles are in flight.
+    // Chunks of 32 tokens per warp: lane = token for the scores, lane = 4
+    // head_dim values for the weighted sum; every load of a chunk is issued
+    // before its arithmetic.
+    for (int base = j0 + warp * 32; base < j1; base += NCW * 32) {
+      const int j = base + lane;
+      const bool valid = j < j1;
+      float scv[QB];
+#pragma unroll
+      for (int i = 0; i < QB; ++i) scv[i] = 0.f;
+      {
+        const uint4* krow = reinterpret_cast<const uint4*>(a.k_res + (bh * a.Nr + (rh + (valid ? j : j0)) % a.Nr) * D);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint4 kr[D / 16];
+#pragma unroll
+          for (int e8 = 0; e8 < D / 16; ++e8)
+            kr[e8] = valid ? __ldg(krow + half * (D / 16) + e8) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int e8 = 0; e8 < D / 16; ++e8) {
+            float xv[8];
+            unpack8_f16(kr[e8], xv);
+            const int d0 = (half * (D / 16) + e8) * 8;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+#pragma unroll
+              for (int i = 0; i < QB; ++i) scv[i] = fmaf(xv[e], q_s[i][d0 + e], scv[i]);
+          }
+        }
+      }
+      float pr[QB];
+#pragma unroll
+      for (int i = 0; i < QB; ++i) {
+        const float v = valid ? scv[i] * kq : -INFINITY;
+        const float mnew = fmaxf(rm[i], warp_max(v));
+        const float al = exp2f(rm[i] - mnew);
+        pr[i] = valid ? exp2f(v - mnew) : 0.f;
+        rl[i] = rl[i] * al + warp_sum(pr[i]);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) ro[i][jj] *= al;
+        rm[i] = mnew;
+      }
+      const int nv = min(32, j1 - base);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint2 vv[16];
+#pragma unroll
+        for (int tt = 0; tt < 16; ++tt) {
+          const int idx = half * 16 + tt;
+          const int jj = base + (idx < nv ? idx : 0);
+          vv[tt] = __ldg(reinterpret_cast<const uint2*>(a.v_res + (bh * a.Nr + (rh + jj) % a.Nr) * D + lane * 4));
+        }
+#pragma unroll
+        for (int tt = 0; tt < 16; ++tt) {
+          const int idx = half * 16 + tt;
+          const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&vv[tt].x));
+          const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&vv[tt].y));
+#pragma unroll
+          for (int i = 0; i < QB; ++i) {
+            float pt = __shfl_sync(0xffffffffu, pr[i], idx);
+            pt = idx < nv ? pt : 0.f;
+            ro[i][0] = fmaf(pt, f01.x, ro[i][0]);
+            ro[i][1] = fmaf(pt, f01.y, ro[i][1]);
+            ro[i][2] = fmaf(pt, f23.x, ro[i][2]);
+            ro[i][3] = fmaf(pt, f23.y, ro[i][3]);
+          }
+        }
+      }
+    }
+
+    // --------------------------------------------- consumers: packed tiles
+    // q as B fragments: bq[P][s][0] for k rows 2t, 2t+1; bq[P][s][1] for 2t+8, 2t+9.
+    uint32_t bq[2][4][2];
+    float qsum[2][2];  // [pair][e]: sum of q over the thread's group of that pair
+#pragma unroll
+    for (int P = 0; P < 2; ++P) {
+#pragma unroll
+      for (int st = 0; st < 4; ++st) {
+        if (BITS == 4) {
+          // k-cols 2t, 2t+1 <- group P, d = 8t + st (+4); 2t+8, 2t+9 <- group P+2
+          const int da = 32 * P + 8 * t + st;
+          const int db = 32 * (P + 2) + 8 * t + st;
+          bq[P][st][0] = g < 4 ? ptx::pack_h2(q_s[g][da], q_s[g][da + 4]) : 0u;
+          bq[P][st][1] = g >= 4 ? ptx::pack_h2(q_s[g - 4][db], q_s[g - 4][db + 4]) : 0u;
+        } else {
+          // thread t's codes: d = 64P + 16t + j; k-cols 2t, 2t+1 <- j = 2st, 2st+8;
+          // 2t+8, 2t+9 <- j = 2st+1, 2st+9; group 2P + (t >> 1) -> column block
+          const bool nz = (g < 4) == ((t >> 1) == 0);
+          const int qi = g & 3;
+          const int d0 = 64 * P + 16 * t + 2 * st;
+          bq[P][st][0] = nz ? ptx::pack_h2(q_s[qi][d0], q_s[qi][d0 + 8]) : 0u;
+          bq[P][st][1] = nz ? ptx::pack_h2(q_s[qi][d0 + 1], q_s[qi][d0 + 9]) : 0u;
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int qi = 2 * (t & 1) + e;
+        const int grp = BITS == 4 ? P + 2 * (t >> 1) : 2 * P + (t >> 1);
+        float sum = 0.f;
+        for (int k = 0; k < kGroup; ++k) sum += q_s[qi][grp * kGroup + k];
+        qsum[P][e] = sum;
+      }
+    }
+
+    for (int tile = 0; tile < ntiles; ++tile) {
+      const int st = tile % NSTAGE;
+      if (!ptx::mbar_wait_bounded(ptx::smem_u32(&full_bar[st]), (tile / NSTAGE) & 1)) {
+        if (lane == 0) set_error(a.err_word, KVQ_ERRBIT_TIMEOUT);
+        s_abort = 1;
+        break;
+      }
+      uint8_t* base = smem + (size_t)st * G::STAGE;
+      const int wrow = 32 * warp;                            // first row of this warp
+      const int nvalid = min(npk - tile * T - wrow, 32);     // rows of this warp still ours
+      if (nvalid > 0) {
+        // rows past the split end may hold anything: zero their params so no
+        // Inf/NaN reaches the arithmetic (their scores are masked anyway)
+        if (nvalid < 32) {
+          if (lane >= nvalid) {
+            reinterpret_cast<uint4*>(base + G::KP)[wrow + lane] = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4*>(base + G::VP)[wrow + lane] = make_uint4(0, 0, 0, 0);
+          }
+          __syncwarp();
+        }
+        const uint32_t kc = ptx::smem_u32(base + G::KC);
+        const uint32_t vc = ptx::smem_u32(base + G::VC);
+        const uint32_t* kp = reinterpret_cast<const uint32_t*>(base + G::KP);
+        const uint32_t* vp = reinterpret_cast<const uint32_t*>(base + G::VP);
+
+        // ---------------- QK for both sub-tiles
+        float acc[NSUB][2][4];
+#pragma unroll
+        for (int u = 0; u < NSUB; ++u) qk_subtile<BITS>(kc, wrow + 16 * u, lane, bq, acc[u]);
+
+        // fix-up: scale, min and centre per (row, group), fp32; rows past the end masked
+        float sv[NSUB][2][2];  // [sub-tile][row g / g+8][e]
+#pragma unroll
+        for (int u = 0; u < NSUB; ++u) {
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const int row = wrow + 16 * u + g + 8 * rr;
+            const uint32_t* prow = kp + row * NG;
+            float part[2] = {0.f, 0.f};
+#pragma unroll
+            for (int P = 0; P < 2; ++P) {
+              const int grp = BITS == 4 ? P + 2 * (t >> 1) : 2 * P + (t >> 1);
+              const uint32_t pr = prow[grp];
+              const float scale = half_lo(pr);
+              const float mnc = fmaf((float)C, scale, half_hi(pr));
+#pragma unroll
+              for (int e = 0; e < 2; ++e)
+                part[e] = fmaf(scale, acc[u][P][2 * rr + e], fmaf(mnc, qsum[P][e], part[e]));
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float tot = part[e] + __shfl_xor_sync(0xffffffffu, part[e], 2);
+              sv[u][rr][e] = (16 * u + g + 8 * rr < nvalid) ? tot : -INFINITY;
+            }
+          }
+        }
+
+        // ---------------- online softmax over the warp's 32 rows (lazy rescale)
+        float mloc[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float mx = fmaxf(fmaxf(sv[0][0][e], sv[0][1][e]), fmaxf(sv[1][0][e], sv[1][1][e]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          mloc[e] = mx * kq;
+        }
+        const bool need0 = mloc[0] > m_ref[0] + 8.f;
+        const bool need1 = mloc[1] > m_ref[1] + 8.f;
+        if (__any_sync(0xffffffffu, need0 || need1)) {
+          const float m0 = need0 ? mloc[0] : m_ref[0];
+          const float m1 = need1 ? mloc[1] : m_ref[1];
+          const float al0 = need0 ? exp2f(m_ref[0] - m0) : 1.f;
+          const float al1 = need1 ? exp2f(m_ref[1] - m1) : 1.f;
+          m_ref[0] = m0;
+          m_ref[1] = m1;
+#pragma unroll
+          for (int x = 0; x < NG; ++x)
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+              oc[x][m][0] *= al0;
+              oc[x][m][1] *= al1;
+              oc[x][m][2] *= al0;
+              oc[x][m][3] *= al1;
+            }
+          mnacc[0] *= al0;
+          mnacc[1] *= al1;
+          mnacc[2] *= al0;
+          mnacc[3] *= al1;
+        }
+        const float mu0 = m_ref[0] == -INFINITY ? 0.f : m_ref[0];
+        const float mu1 = m_ref[1] == -INFINITY ? 0.f : m_ref[1];
+        const int srcA = (2 * t) * 4 + ((g >> 1) & 1);
+        const int srcB = (2 * t + 1) * 4 + ((g >> 1) & 1);
+        const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;
+        const bool qreal = g < 4;
+#pragma unroll
+        for (int u = 0; u < NSUB; ++u) {
+          // p as the PV B fragment: this thread needs p(query g, tokens 2t, 2t+1, 2t+8, 2t+9)
+          const uint32_t plo = ptx::pack_h2(exp2f(fmaf(sv[u][0][0], kq, -mu0)), exp2f(fmaf(sv[u][0][1], kq, -mu1)));
+          const uint32_t phi = ptx::pack_h2(exp2f(fmaf(sv[u][1][0], kq, -mu0)), exp2f(fmaf(sv[u][1][1], kq, -mu1)));
+          const uint32_t x0 = __shfl_sync(0xffffffffu, plo, srcA);
+          const uint32_t x1 = __shfl_sync(0xffffffffu, plo, srcB);
+          const uint32_t y0 = __shfl_sync(0xffffffffu, phi, srcA);
+          const uint32_t y1 = __shfl_sync(0xffffffffu, phi, srcB);
+          const uint32_t pb0 = qreal ? ptx::prmt(x0, x1, sel) : 0u;  // tokens 2t, 2t+1
+          const uint32_t pb1 = qreal ? ptx::prmt(y0, y1, sel) : 0u;  // tokens 2t+8, 2t+9
+          pv_subtile<BITS>(vc, vp, wrow + 16 * u, lane, pb0, pb1, oc, mnacc);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&empty_bar[st]));
+      // refill this stage with tile + NSTAGE once all warps have released it
+      if (threadIdx.x == 0 && issued < ntiles && !s_abort) {
+        if (ptx::mbar_wait_bounded(ptx::smem_u32(&empty_bar[st]), (tile / NSTAGE) & 1)) {
+          issue(issued);
+          ++issued;
+        } else {
+          set_error(a.err_word, KVQ_ERRBIT_TIMEOUT);
+          s_abort = 1;
+        }
+      }
+      __syncwarp();  // reconverge warp 0 before the next tile's .sync.aligned instructions
+      if (s_abort) break;
+    }
+  }
+  // Copies still in flight (only after an abort) land before the ring is reused.
+  if (threadIdx.x == 0) {
+    const int first = issued > NSTAGE ? issued - NSTAGE : 0;
+    for (int tile = first; tile < issued; ++tile)
+      ptx::mbar_wait_bounded(ptx::smem_u32(&full_bar[tile % NSTAGE]), (tile / NSTAGE) & 1);
+  }
+
+  // ---------------- merge the warps' states and write this split's partial
+  __syncthreads();  // the stage ring is idle from here on
+  MergeSmem& ms = *reinterpret_cast<MergeSmem*>(smem);
+  {
+    // tensor-core state: min/scale/l rows to shared memory first
+    ms.mn[warp][g][2 * t] = mnacc[0];
+    ms.mn[warp][g][2 * t + 1] = mnacc[1];
+    if (g == 0) {
+      ms.mn[warp][8][2 * t] = mnacc[2];
+      ms.mn[warp][8][2 * t + 1] = mnacc[3];
+    }
+    if (g == 0 && t < 2) {
+      ms.m[warp][2 * t] = m_ref[0];
+      ms.m[warp][2 * t + 1] = m_ref[1];
+    }
+    __syncwarp();
+    if (t < 2) {
+#pragma unroll
+      for (int x = 0; x < NG; ++x)
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int qi = 2 * t + (r & 1);
+            const int jrow = (r >> 1);  // 0: row g, 1: row g+8
+            int dd;
+            if (BITS == 4) {
+              dd = 32 * x + 4 * g + 2 * m + jrow;
+            } else {
+              dd = 32 * x + 8 * (g & 3) + 4 * (g >> 2) + 2 * m + jrow;
+            }
+            ms.o[warp][qi][dd] = oc[x][m][r] + ms.mn[warp][x][qi] + (float)C * ms.mn[warp][4 + x][qi];
+          }
+    }
+    if (lane < QB) ms.l[warp][lane] = ms.mn[warp][8][lane];
+    // residual state
+    if (lane == 0) {
+#pragma unroll
+      for (int i = 0; i < QB; ++i) {
+        ms.m[NCW + warp][i] = rm[i];
+        ms.l[NCW + warp][i] = rl[i];
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < QB; ++i)
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) ms.o[NCW + warp][i][lane * 4 + jj] = ro[i][jj];
+  }
+  __syncthreads();
+  const int64_t pidx = ((int64_t)b * a.Hkv + h) * a.S + s;
+  for (int idx = threadIdx.x; idx < QB * D; idx += NTHREADS) {
+    const int i = idx / D, e = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 2 * NCW; ++w) M = fmaxf(M, ms.m[w][i]);
+    float osum = 0.f, lsum = 0.f;
+    if (M > -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < 2 * NCW; ++w) {
+        const float f = exp2f(ms.m[w][i] - M);
+        if (f > 0.f) {
+          osum = fmaf(ms.o[w][i][e], f, osum);
+          lsum = fmaf(ms.l[w][i], f, lsum);
+        }
+      }
+    }
+    a.o_part[(pidx * QB + i) * D + e] = osum;
+    if (e == 0) a.ml_part[pidx * QB + i] = make_float2(M, lsum);
+  }
+  // the last split of this KV head to finish merges all S partials
+  if (take_last_ticket<NTHREADS>(a, (int64_t)b * a.Hkv + h, &s_last))
+    combine_unit<NTHREADS, D>(a, b, h, 0, reinterpret_cast<float*>(smem));
+}
+
+// --------------------------------------------------------- tensor maps -----
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+// A 2D view [rows][row_bytes] of uint8 with a box of T whole rows.
+bool make_rows_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
+                   CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows == 0) return false;
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)row_bytes, (cuuint32_t)T};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BITS>
+cudaError_t launch_bits(const Dims& s, const DecodePlan& p, const DecodeArgs& a, cudaStream_t st) {
+  using Gm = Geo<BITS>;
+  const uint64_t rows = (uint64_t)s.B * s.Hkv * s.cap;
+  CUtensorMap kc, vc, kp, vp;
+  const CUtensorMapSwizzle swz = BITS == 4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  if (!make_rows_map(&kc, a.k_codes, Gm::RB, rows, swz) || !make_rows_map(&vc, a.v_codes, Gm::RB, rows, swz) ||
+      !make_rows_map(&kp, a.k_params, NG * 4, rows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_rows_map(&vp, a.v_params, NG * 4, rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  constexpr size_t smem = tc_smem_bytes<BITS>();
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<BITS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.splits, (unsigned)s.Hkv, (unsigned)s.B);
+  cfg.blockDim = dim3(NTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<BITS>, kc, vc, kp, vp, a);
+}
+
+}  // namespace
+
+bool tc_supported(const kvq_cache_desc& D, int gq) {
+  return D.head_dim == 128 && gq >= 1 && gq <= QB && D.capacity > 0 && encode_fn() != nullptr;
+}
+
+int tc_threads() { return NTHREADS; }
+
+cudaError_t launch_decode_tc(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
+                             cudaStream_t st) {
+  return s.bits == 4 ? launch_bits<4>(s, p, a, st) : launch_bits<2>(s, p, a, st);
+}
+
+}  // namespace kvq

@@ -99,7 +99,7 @@ __device__ __forceinline__ void unpack8_f16(const uint4& v, float (&x)[8]) {
 
 // Work split of one decode call.  Each (sequence, KV head, query block) is cut
 // into `splits` pieces of roughly equal byte cost; partials (o, m, l) go to the
-// workspace and a combine step merges them by log-sum-exp.
+// workspace and the last split to finish merges them by log-sum-exp.
 struct DecodePlan {
   int kernel;   // 0 = generic CUDA-core path, 1 = tensor-core path
   int gq;       // query heads per KV head
@@ -107,7 +107,9 @@ struct DecodePlan {
   int nqb;      // query blocks per KV head = ceil(gq / qb)
   int splits;   // S
   int threads;  // threads per CTA of the split kernel
-  size_t ws_partials;  // bytes of the o partials
+  size_t ws_partials;  // bytes of the o partials (offset 0)
+  size_t ws_ml_off;    // offset of the {m, l} partials
+  size_t ws_cnt_off;   // offset of the per-unit arrival counters (zero between calls)
   size_t ws_total;     // bytes of the whole workspace
 };
 

@@ -11,11 +11,11 @@
 // (KVQ_NOALLOC_SCRATCH_BYTES) until the process exits, and every call on a
 // device shares it.  The host only ever sees a stand-in for its name, so its
 // device address is looked up once per device with cudaGetSymbolAddress, with
-// that device current, on the first call there; make that first call before
-// any stream capture.  Nothing in the scratch needs to start at zero (each
-// split writes its partial before the combine reads it), so nothing is
-// cleared.  Two calls whose kernels overlap on the GPU race on the array: issue
-// them on one stream, or order the streams.
+// that device current, on the first call there, which also clears the array
+// once (its arrival counters must start at zero; every completed call leaves
+// them at zero again); make that first call before any stream capture.  Two
+// calls whose kernels overlap on the GPU race on the array: issue them on one
+// stream, or order the streams.
 #include <mutex>
 
 #include "kvq_internal.cuh"
@@ -36,6 +36,7 @@ kvq_status scratch_address(void** out) {
   if (!g_scratch_ptr[dev]) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e == cudaSuccess && p != nullptr) e = cudaMemset(p, 0, KVQ_NOALLOC_SCRATCH_BYTES);
     if (e != cudaSuccess || p == nullptr) {
       cudaGetLastError();
       return KVQ_ERR_CUDA;

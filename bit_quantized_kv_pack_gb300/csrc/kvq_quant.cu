@@ -121,6 +121,9 @@ struct AppendArgs {
 
 template <int BITS>
 __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
+  // The decode of the same step may start launching now; it waits for this
+  // grid to finish (griddepcontrol.wait) before it reads the cache.
+  asm volatile("griddepcontrol.launch_dependents;");
   const int b = blockIdx.x;
   const int pl = a.packed_len[b];
   const int rl = a.res_len[b];

@@ -210,10 +210,11 @@ def kvq_append(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, stream=
 
 
 def workspace_for(cache: KVCache, num_q_heads: int) -> torch.Tensor:
+    """A zeroed decode workspace (zeroed once; the decode keeps it ready)."""
     n = kvq_decode_workspace_bytes(cache.desc, num_q_heads)
     if n == 0:
         raise KvqError(KVQ_ERR_INVALID_ARG, "kvq_decode_workspace_bytes")
-    return torch.empty(n, dtype=torch.uint8, device=cache.device)
+    return torch.zeros(n, dtype=torch.uint8, device=cache.device)
 
 
 def kvq_decode_attention(cache: KVCache, q: torch.Tensor, out: torch.Tensor | None = None,

@@ -174,7 +174,11 @@ kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache_view* view,
  *   out        fp16 device [B][Hq][d]: softmax(q K^T / sqrt(d)) V over the
  *              packed tokens (dequantized as min + code * scale) and the residual.
  *   workspace  device scratch of ws_bytes >= kvq_decode_workspace_bytes(desc, Hq),
- *              16-byte aligned.  Its contents on entry do not matter.
+ *              16-byte aligned, zeroed before its first use.  Each completed call
+ *              leaves it ready for the next one (its arrival counters back at
+ *              zero), so it is zeroed once, not per call; zero it again after a
+ *              call that reported KVQ_ERR_TIMEOUT.  One workspace serves one call
+ *              at a time.
  * A sequence with no tokens gets a zero output and sets KVQ_ERRBIT_EMPTY.
  * Asynchronous; lengths are read on the device. */
 kvq_status kvq_decode_attention(const kvq_cache_desc* desc, const kvq_cache_view* view,
@@ -196,10 +200,11 @@ kvq_status kvq_decode_attention(const kvq_cache_desc* desc, const kvq_cache_view
  * than that (kvq_decode_workspace_bytes(desc, num_q_heads) > the maximum) and
  * KVQ_ERR_INVALID_ARG for an invalid description or head count.  Allocates
  * nothing.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call before
- * any stream capture.  All calls share the array and it keeps the last call's
- * contents (none of which need to start at zero), so calls whose kernels
- * overlap on the GPU race: keep them on one stream or order the streams. */
+ * (cudaGetSymbolAddress, with that device current) and clears the array once
+ * (cudaMemset); make that first call before any stream capture.  All calls share
+ * the array and it keeps the last call's contents (its counters back at zero),
+ * so calls whose kernels overlap on the GPU race: keep them on one stream or
+ * order the streams. */
 kvq_status kvq_decode_attention_noalloc(const kvq_cache_desc* desc, const kvq_cache_view* view,
                                         const void* q, int32_t num_q_heads, void* out,
                                         void* stream);

@@ -37,10 +37,12 @@ def test_decode_sweep(bits, d, gq):
     q = torch.from_numpy(rng.standard_normal((B, H * gq, d)).astype(np.float16))
     g, r = _setup(k, v, lens, bits, Lmax, Nr)
     ws = kvq.workspace_for(g, H * gq)
-    ws.fill_(0xFF)  # NaN bytes: the workspace's prior contents must not matter
     out = kvq.kvq_decode_attention(g, q.to(DEV), workspace=ws)
     assert kvq.kvq_read_error(g)[0] == kvq.KVQ_OK
     assert_attn_close(out, oracle.decode(r, q.numpy()))
+    # the workspace is left ready: a second call through it gives the same bytes
+    again = kvq.kvq_decode_attention(g, q.to(DEV), workspace=ws)
+    assert torch.equal(out, again)
 
 
 @pytest.mark.parametrize("Nr", [0, 64])
