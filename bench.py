@@ -173,22 +173,23 @@ class ClockSampler:
 
 # ------------------------------------------------------------ our arm ------
 
-def build_state(dev, steps, warmup, e2e_steps, l2_bytes):
+def build_state(dev, steps, warmup, e2e_steps, l2_bytes, workload):
     """Pack the workload once, clone it into enough copies to exceed 3x L2,
     and pre-generate the per-step queries and new tokens on the device."""
     from bit_quantized_kv_pack_gb300 import kvq, synth
 
-    w = synth.WORKLOADS[WORKLOAD]
+    w = synth.WORKLOADS[workload]
     k, v, lens = w.prefill(device=dev)
-    npk0 = w.len_max - w.residual
+    npk_b = [int(L) - min(int(L), w.residual) for L in lens.tolist()]
+    npk0 = sum(npk_b)  # packed tokens over the batch, per KV head
     per_tok = 2 * (w.head_dim * w.bits // 8 + 4 * (w.head_dim // 32))
-    step_bytes0 = npk0 * w.num_kv_heads * w.batch * per_tok
+    step_bytes0 = npk0 * w.num_kv_heads * per_tok
     res_bytes = w.batch * w.num_kv_heads * w.residual * w.head_dim * 2 * 2
     ncopy = max(2, math.ceil(3 * l2_bytes / (step_bytes0 + res_bytes)))
     # appends each copy sees: warm-up and timed graph passes, then the e2e loop
     appends = (math.ceil(warmup / ncopy) + math.ceil(steps / ncopy)
                + math.ceil((ncopy + max(ncopy, e2e_steps)) / ncopy) + 2)
-    cap = npk0 + appends + 8
+    cap = max(npk_b) + appends + 8
     base = kvq.KVCache(w.batch, w.num_kv_heads, w.head_dim, w.bits, cap, w.residual, device=dev)
     kvq.kvq_quantize_pack(base, k, v, lens.to(dev))
     st, word = kvq.kvq_read_error(base)
@@ -252,7 +253,7 @@ def run_ours(args, rank, world, local):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
 
-    st = build_state(dev, args.steps, args.warmup, args.e2e_steps, l2)
+    st = build_state(dev, args.steps, args.warmup, args.e2e_steps, l2, args.workload)
     w, ncopy = st["w"], st["nslot"]
     K = args.steps
     reps, rem = divmod(K, ncopy)  # K steps = reps whole passes over the copies + rem
@@ -283,8 +284,8 @@ def run_ours(args, rank, world, local):
         torch.distributed.barrier()
 
     # packed bytes the decode reads per step: the prefill's packed tokens (each
-    # append adds one more token per copy, < 0.1% over the run, not counted)
-    step_bytes = st["npk0"] * w.batch * w.num_kv_heads * st["per_tok"]
+    # append adds one more token per sequence and copy, < 0.1% over the run, not counted)
+    step_bytes = st["npk0"] * w.num_kv_heads * st["per_tok"]
     ms_per_step = ms / K
     value = step_bytes / (ms_per_step * 1e-3) / 1e9
 
@@ -320,7 +321,7 @@ def run_ours(args, rank, world, local):
         "data": "synthetic (seeded SplitMix64 + Box-Muller, fp16)",
         "config": {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "bits": w.bits,
-                   "packed_tokens": st["npk0"], "residual": w.residual, "group": 32,
+                   "packed_tokens_per_head": st["npk0"], "residual": w.residual, "group": 32,
                    "step": "append + decode_attention",
                    "l2": f"rotating {ncopy} cache copies ({ncopy * step_bytes / 2**20:.0f} MiB "
                          f"packed) > 3x L2 ({l2 / 2**20:.0f} MiB)",
@@ -336,7 +337,7 @@ def run_ours(args, rank, world, local):
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        res["cpu_baseline"] = cpu_baseline(args.cpu_seconds, workload=args.workload)
     return res
 
 
@@ -375,7 +376,7 @@ def run_e2e(st, args):
     b.synchronize()
     ms = a.elapsed_time(b) / K
     w = st["w"]
-    step_bytes = st["npk0"] * w.batch * w.num_kv_heads * st["per_tok"]
+    step_bytes = st["npk0"] * w.num_kv_heads * st["per_tok"]
     return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "us_per_step": round(ms * 1e3, 3),
             "h2d_bytes_per_step": int(q_d.numel() * 2 + kn_d.numel() * 2 + vn_d.numel() * 2),
@@ -385,22 +386,23 @@ def run_e2e(st, args):
 
 # ---------------------------------------------------------- oracle arm -----
 
-def cpu_baseline(seconds: float, steps: int | None = None):
+def cpu_baseline(seconds: float, steps: int | None = None, workload: int = WORKLOAD):
     """The CPU oracle as it stands (single thread) on whole steps of the same
-    workload: append + fp64 decode of all 32 query heads."""
-    import numpy as np
+    workload: append + fp64 decode of every query head."""
     import oracle
     from bit_quantized_kv_pack_gb300 import synth
 
-    w = synth.WORKLOADS[WORKLOAD]
+    w = synth.WORKLOADS[workload]
     k, v, lens = w.prefill()
-    npk0 = w.len_max - w.residual
+    npk_b = [int(L) - min(int(L), w.residual) for L in lens.tolist()]
+    npk0 = sum(npk_b)
     n_steps_max = steps if steps is not None else 1000
-    r = oracle.Cache(w.batch, w.num_kv_heads, w.head_dim, w.bits, npk0 + n_steps_max + 8, w.residual)
+    r = oracle.Cache(w.batch, w.num_kv_heads, w.head_dim, w.bits, max(npk_b) + n_steps_max + 8,
+                     w.residual)
     oracle.quantize_pack(r, k.numpy(), v.numpy(), lens.numpy())
     del k, v
     per_tok = 2 * (w.head_dim * w.bits // 8 + 4 * (w.head_dim // 32))
-    step_bytes = npk0 * w.batch * w.num_kv_heads * per_tok
+    step_bytes = npk0 * w.num_kv_heads * per_tok
     t0 = time.time()
     n = 0
     while True:
@@ -413,8 +415,8 @@ def cpu_baseline(seconds: float, steps: int | None = None):
             break
     el = time.time() - t0
     return {"value": round(step_bytes * n / el / 1e9, 6), "unit": "GB/s", "cores": 1,
-            "kind": "oracle", "sample": f"{n} whole steps (append + decode of 32 heads over "
-                                        f"{npk0}+{w.residual} tokens), {el:.1f} s, single thread",
+            "kind": "oracle", "sample": f"{n} whole steps (append + decode of all {w.num_q_heads} "
+                                        f"query heads of {w.name}), {el:.1f} s, single thread",
             "s_per_step": round(el / n, 4)}
 
 
@@ -423,10 +425,10 @@ def run_reference(args, rank, world):
         return None
     steps = max(1, args.steps_reference if args.steps_reference else min(args.steps, 5))
     # warm-up: one step, untimed
-    cpu_baseline(0.0, steps=1)
-    cb = cpu_baseline(0.0, steps=steps)
+    cpu_baseline(0.0, steps=1, workload=args.workload)
+    cb = cpu_baseline(0.0, steps=steps, workload=args.workload)
     from bit_quantized_kv_pack_gb300 import synth
-    w = synth.WORKLOADS[WORKLOAD]
+    w = synth.WORKLOADS[args.workload]
     return {
         "impl": "reference",
         "metric": "quantized-KV decode attention: achieved HBM GB/s (% of peak), us/step",
@@ -449,6 +451,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", type=int, default=WORKLOAD, choices=(1, 2, 3, 4),
+                    help="decode workload (default 2: Llama-3.1-8B INT4 32K)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--steps-reference", type=int, default=0)

@@ -54,7 +54,15 @@ DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count) {
   if (S < 1) S = 1;
   if (S > 1024) S = 1024;
   p.splits = (int)S;
-  const int64_t nparts = units * S * p.qb;
+  p.splits_packed = p.splits;
+  if (p.kernel == 1) {
+    // the fp16 residual tokens get splits of their own, one per 128 tokens of the window
+    const int sr = (D.residual + 127) / 128;
+    const int sp = (int)S - sr > 1 ? (int)S - sr : 1;
+    p.splits_packed = sp;
+    p.splits = sp + sr;
+  }
+  const int64_t nparts = units * p.splits * p.qb;
   p.ws_partials = (size_t)nparts * D.head_dim * sizeof(float);
   p.ws_ml_off = (p.ws_partials + 255) & ~(size_t)255;
   p.ws_cnt_off = (p.ws_ml_off + (size_t)nparts * sizeof(float2) + 255) & ~(size_t)255;
@@ -87,6 +95,7 @@ cudaError_t launch_decode(const Dims& s, const DecodePlan& p, const kvq_cache_vi
   a.qb = p.qb;
   a.nqb = p.nqb;
   a.S = p.splits;
+  a.Sp = p.splits_packed;
   a.cap = s.cap;
   a.Nr = s.Nr;
   a.d = s.d;

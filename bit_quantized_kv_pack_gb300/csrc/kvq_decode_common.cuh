@@ -27,6 +27,7 @@ struct DecodeArgs {
   float2* ml_part;
   uint32_t* counters;  // [B][Hkv][nqb] arrival tickets, zero between calls
   int Hkv, Hq, gq, qb, nqb, S, cap, Nr, d;
+  int Sp;  // tensor-core kernel: splits s < Sp take packed tokens, s >= Sp residual ones
   float qk_scale_log2;  // log2(e) / sqrt(d)
 };
 
@@ -79,69 +80,116 @@ cudaError_t launch_decode_tc(const Dims& s, const DecodePlan& p, const DecodeArg
 // merges the S partials by log-sum-exp and writes the fp16 output:
 //   M = max_s m_s,  O = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
 // atomicInc wraps the counter back to zero, so it is ready for the next call.
-// `scratch` holds at least S * qb + 2 * qb floats of shared memory.
 template <int NT>
 __device__ __forceinline__ bool take_last_ticket(const DecodeArgs& a, int64_t unit, int* flag) {
-  __threadfence();  // this CTA's partial is visible before its ticket
-  __syncthreads();
+  __syncthreads();  // every thread's partial stores precede thread 0's fence
   if (threadIdx.x == 0) {
+    __threadfence();  // cumulative: the CTA's partial is visible before its ticket
     const unsigned old = atomicInc(&a.counters[unit], (unsigned)(a.S - 1));
     *flag = (old == (unsigned)(a.S - 1));
+    if (*flag) __threadfence();  // the other CTAs' partials are visible after it
   }
   __syncthreads();
-  const bool last = *flag != 0;
-  if (last) __threadfence();  // the other CTAs' partials are visible after it
-  return last;
+  return *flag != 0;
 }
 
-template <int NT, int D>
+// Merge the S partials of one (sequence, KV head, query block).  The first CH
+// partials of a thread's first output are loaded in one round together with the
+// m/l values (all of them when S <= CH); maxima, weights and sums use warp
+// reductions.  `scratch` holds at least 2 * S * qb + qb floats of shared memory.
+template <int NT, int D, int CH>
 __device__ __forceinline__ void combine_unit(const DecodeArgs& a, int b, int h, int qbi,
                                              float* scratch) {
+  constexpr int D4 = D / 4;
+  constexpr int NW = NT / 32;
   const int S = a.S, qb = a.qb;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t unit = ((int64_t)b * a.Hkv + h) * a.nqb + qbi;
   const int64_t base = unit * S;
-  float* w = scratch;              // [S][qb]: m_s, then the weights 2^(m_s - M)
-  float* Mq = scratch + S * qb;    // [qb]
-  float* Lq = Mq + qb;             // [qb]
-  for (int idx = threadIdx.x; idx < S * qb; idx += NT) w[idx] = __ldcg(&a.ml_part[base * qb + idx].x);
-  __syncthreads();
-  if (threadIdx.x < qb) {
-    float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, w[s * qb + threadIdx.x]);
-    Mq[threadIdx.x] = M;
-  }
-  __syncthreads();
+  float* w = scratch;            // [S][qb]: m_s, then the weights 2^(m_s - M)
+  float* lv = w + S * qb;        // [S][qb]: l_s
+  float* Lq = lv + S * qb;       // [qb]
+  const int64_t stride = (int64_t)qb * D4;  // float4 elements between splits
+
+  // this thread's first output: one query, four consecutive head_dim values
+  const int idx0 = threadIdx.x;
+  const int i_0 = idx0 / D4;
+  const bool has0 = idx0 < qb * D4 && (qbi * qb + i_0) < a.gq;
+  const float4* op0 = reinterpret_cast<const float4*>(a.o_part + (base * qb + i_0) * D) + idx0 % D4;
+  float4 v0[CH];
+#pragma unroll
+  for (int k = 0; k < CH; ++k)
+    v0[k] = (has0 && k < S) ? __ldcg(op0 + k * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
   for (int idx = threadIdx.x; idx < S * qb; idx += NT) {
-    const float M = Mq[idx % qb];
-    w[idx] = M > -INFINITY ? exp2f(w[idx] - M) : 0.f;
+    const float2 ml = __ldcg(&a.ml_part[base * qb + idx]);
+    w[idx] = ml.x;
+    lv[idx] = ml.y;
   }
   __syncthreads();
-  if (threadIdx.x < qb) {
+  for (int q = warp; q < qb; q += NW) {
+    float M = -INFINITY;
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, w[s * qb + q]);
+    M = warp_max(M);
     float L = 0.f;
-    for (int s = 0; s < S; ++s) L = fmaf(w[s * qb + threadIdx.x], __ldcg(&a.ml_part[(base + s) * qb + threadIdx.x].y), L);
-    Lq[threadIdx.x] = L;
+    for (int s = lane; s < S; s += 32) {
+      const float wt = M > -INFINITY ? exp2f(w[s * qb + q] - M) : 0.f;
+      w[s * qb + q] = wt;
+      L = fmaf(wt, lv[s * qb + q], L);
+    }
+    L = warp_sum(L);
+    if (lane == 0) Lq[q] = L;
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < qb * D; idx += NT) {
-    const int i = idx / D, e = idx % D;
-    const int qi = qbi * qb + i;
-    if (qi >= a.gq) continue;
-    const float* op = a.o_part + (base * qb + i) * D + e;
-    const int64_t stride = (int64_t)qb * D;
-    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-    int s = 0;
-    for (; s + 4 <= S; s += 4) {  // four independent loads in flight
-      const float o0 = __ldcg(op + (s + 0) * stride), o1 = __ldcg(op + (s + 1) * stride);
-      const float o2 = __ldcg(op + (s + 2) * stride), o3 = __ldcg(op + (s + 3) * stride);
-      acc0 = fmaf(w[(s + 0) * qb + i], o0, acc0);
-      acc1 = fmaf(w[(s + 1) * qb + i], o1, acc1);
-      acc2 = fmaf(w[(s + 2) * qb + i], o2, acc2);
-      acc3 = fmaf(w[(s + 3) * qb + i], o3, acc3);
-    }
-    for (; s < S; ++s) acc0 = fmaf(w[s * qb + i], __ldcg(op + s * stride), acc0);
+  auto finish = [&](int i, int e4, float4 acc) {
     const float L = Lq[i];
-    const float o = (acc0 + acc1) + (acc2 + acc3);
-    a.out[((int64_t)b * a.Hq + h * a.gq + qi) * D + e] = __float2half_rn(L > 0.f ? o / L : 0.f);
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    __half2* dst = reinterpret_cast<__half2*>(
+        a.out + ((int64_t)b * a.Hq + h * a.gq + qbi * qb + i) * D + 4 * e4);
+    dst[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
+    dst[1] = __floats2half2_rn(acc.z * inv, acc.w * inv);
+  };
+  // the first output: its first CH partials are already in registers
+  if (has0) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+      const float wk = k < S ? w[k * qb + i_0] : 0.f;
+      acc.x = fmaf(wk, v0[k].x, acc.x);
+      acc.y = fmaf(wk, v0[k].y, acc.y);
+      acc.z = fmaf(wk, v0[k].z, acc.z);
+      acc.w = fmaf(wk, v0[k].w, acc.w);
+    }
+    for (int s = CH; s < S; ++s) {
+      const float4 v = __ldcg(op0 + s * stride);
+      const float wk = w[s * qb + i_0];
+      acc.x = fmaf(wk, v.x, acc.x);
+      acc.y = fmaf(wk, v.y, acc.y);
+      acc.z = fmaf(wk, v.z, acc.z);
+      acc.w = fmaf(wk, v.w, acc.w);
+    }
+    finish(i_0, idx0 % D4, acc);
+  }
+  // further outputs (when qb * D / 4 > NT): eight loads in flight
+  for (int idx = threadIdx.x + NT; idx < qb * D4; idx += NT) {
+    const int i = idx / D4, e4 = idx % D4;
+    if (qbi * qb + i >= a.gq) continue;
+    const float4* op = reinterpret_cast<const float4*>(a.o_part + (base * qb + i) * D) + e4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < S; s0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        v[k] = (s0 + k < S) ? __ldcg(op + (s0 + k) * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float wk = (s0 + k < S) ? w[(s0 + k) * qb + i] : 0.f;
+        acc.x = fmaf(wk, v[k].x, acc.x);
+        acc.y = fmaf(wk, v[k].y, acc.y);
+        acc.z = fmaf(wk, v[k].z, acc.z);
+        acc.w = fmaf(wk, v[k].w, acc.w);
+      }
+    }
+    finish(i, e4, acc);
   }
 }
 

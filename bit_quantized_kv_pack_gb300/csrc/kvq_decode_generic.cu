@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(DecodeArgs a) 
   __shared__ int s_last;
   if (take_last_ticket<kThreads>(a, ((int64_t)b * a.Hkv + h) * a.nqb + qbi, &s_last)) {
     extern __shared__ float dyn_scratch[];
-    combine_unit<kThreads, D>(a, b, h, qbi, dyn_scratch);
+    combine_unit<kThreads, D, 8>(a, b, h, qbi, dyn_scratch);
   }
 }
 
@@ -247,8 +247,8 @@ cudaError_t launch_one(dim3 grid, size_t smem, const DecodeArgs& a, cudaStream_t
 template <int D, int BITS>
 cudaError_t launch_generic_d_bits(const DecodePlan& p, dim3 grid, const DecodeArgs& a,
                                   cudaStream_t st) {
-  // dynamic shared memory: the combine's weights, S * qb + 2 * qb floats
-  const size_t smem = (size_t)(p.splits * p.qb + 2 * p.qb) * sizeof(float);
+  // dynamic shared memory: the combine's weights and sums, 2 * S * qb + qb floats
+  const size_t smem = (size_t)(2 * p.splits * p.qb + p.qb) * sizeof(float);
   switch (p.qb) {
     case 1: return launch_one<D, BITS, 1>(grid, smem, a, st);
     case 2: return launch_one<D, BITS, 2>(grid, smem, a, st);

@@ -23,18 +23,19 @@
 //    INT4, 2 for INT2).  Integer codes are exact in fp16, so the tensor cores
 //    see exact operands; scale and min are applied in fp32.
 //  * QK:  S^T = K q^T with tokens on M (mma.sync m16n8k16, fp32 accumulate).
-//    Two groups share one MMA through a block-diagonal q operand (columns 0-3
-//    hold group a's queries, columns 4-7 group b's), then per thread
-//      s = sum_g scale_g * acc_g + (min_g + C * scale_g) * sum_{d in g} q_d.
+//    Two groups share one MMA through a block-diagonal q operand (column
+//    2 * query + group bit), so each thread holds one query for both groups,
+//    then  s = sum_g scale_g * acc_g + (min_g + C * scale_g) * sum_{d in g} q_d.
 //  * Online softmax in fp32 (exp2 domain) with a lazy rescale: the running max
 //    only moves when it grows by more than 2^8.
 //  * PV:  O^T = (c - C)^T (p * scale)^T with V codes read through
 //    ldmatrix.trans; the per-token, per-group p * scale is the B operand.  A
 //    ninth MMA accumulates sum p * min_g, sum p * scale_g and sum p (= l) per
 //    group, so O = O_c + sum p min_g + C sum p scale_g.
-//  * Residual tokens (fp16) use the CUDA-core loop of the generic kernel; the
-//    per-warp states merge in shared memory, and the last split of a KV head to
-//    finish merges the split partials (combine_unit).
+//  * The fp16 residual tokens get splits of their own (CUDA cores, all loads of
+//    a chunk in one round), so no packed split waits on them.  Per-warp states
+//    merge in shared memory, and the last split of a KV head to finish merges
+//    the split partials (combine_unit).
 //
 // Every mbarrier wait is bounded; a wait that runs out sets KVQ_ERRBIT_TIMEOUT.
 #include <math.h>
@@ -70,9 +71,9 @@ struct Geo {
 
 // Shared scratch for the final merge (overlaps the stage ring once it is idle).
 struct MergeSmem {
-  float o[2 * NCW][QB][D];
-  float m[2 * NCW][QB];
-  float l[2 * NCW][QB];
+  float o[NCW][QB][D];
+  float m[NCW][QB];
+  float l[NCW][QB];
   float mn[NCW][9][8];
 };
 
@@ -257,8 +258,80 @@ __device__ __forceinline__ void pv_subtile(uint32_t vc, const uint32_t* vp, int 
   }
 }
 
+// ---------------------------------------------------------- residual ----
+
+// Residual-only CTA: the fp16 tokens [j0, j1) of the ring on the CUDA cores,
+// 32 tokens per warp and chunk -- lane = token for the scores, lane = four
+// head_dim values for the weighted sum.  All loads of a chunk (the lane's key
+// row, and four values of each of the 32 value rows) are issued before any
+// arithmetic, so a chunk costs one memory round trip.  Leaves the warp's state
+// in (rm, rl, ro).
+__device__ __forceinline__ void residual_tokens(const DecodeArgs& a, int64_t bh, int rh, int j0,
+                                                int j1, int warp, int lane, const float (&q_s)[QB][D],
+                                                float kq, float (&rm)[QB], float (&rl)[QB],
+                                                float (&ro)[QB][4]) {
+  for (int base = j0 + warp * 32; base < j1; base += NCW * 32) {
+    const int j = base + lane;
+    const bool valid = j < j1;
+    const int nv = min(32, j1 - base);
+    uint4 kr[D / 8];
+    uint2 vv[32];
+    {
+      const uint4* krow = reinterpret_cast<const uint4*>(a.k_res + (bh * a.Nr + (rh + (valid ? j : j0)) % a.Nr) * D);
+#pragma unroll
+      for (int e8 = 0; e8 < D / 8; ++e8) kr[e8] = valid ? __ldg(krow + e8) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int tt = 0; tt < 32; ++tt) {
+        const int jj = base + (tt < nv ? tt : 0);
+        vv[tt] = __ldg(reinterpret_cast<const uint2*>(a.v_res + (bh * a.Nr + (rh + jj) % a.Nr) * D + lane * 4));
+      }
+    }
+    float scv[QB];
+#pragma unroll
+    for (int i = 0; i < QB; ++i) scv[i] = 0.f;
+#pragma unroll
+    for (int e8 = 0; e8 < D / 8; ++e8) {
+      float xv[8];
+      unpack8_f16(kr[e8], xv);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+#pragma unroll
+        for (int i = 0; i < QB; ++i) scv[i] = fmaf(xv[e], q_s[i][e8 * 8 + e], scv[i]);
+    }
+    float pr[QB];
+#pragma unroll
+    for (int i = 0; i < QB; ++i) {
+      const float v = valid ? scv[i] * kq : -INFINITY;
+      const float mnew = fmaxf(rm[i], warp_max(v));
+      const float al = exp2f(rm[i] - mnew);
+      pr[i] = valid ? exp2f(v - mnew) : 0.f;
+      rl[i] = rl[i] * al + warp_sum(pr[i]);
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) ro[i][jj] *= al;
+      rm[i] = mnew;
+    }
+#pragma unroll
+    for (int tt = 0; tt < 32; ++tt) {
+      const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&vv[tt].x));
+      const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&vv[tt].y));
+#pragma unroll
+      for (int i = 0; i < QB; ++i) {
+        float pt = __shfl_sync(0xffffffffu, pr[i], tt);
+        pt = tt < nv ? pt : 0.f;
+        ro[i][0] = fmaf(pt, f01.x, ro[i][0]);
+        ro[i][1] = fmaf(pt, f01.y, ro[i][1]);
+        ro[i][2] = fmaf(pt, f23.x, ro[i][2]);
+        ro[i][3] = fmaf(pt, f23.y, ro[i][3]);
+      }
+    }
+  }
+}
+
 // --------------------------------------------------------------- kernel ----
 
+// Grid (S, Hkv, B): split s < Sp streams packed tokens of (sequence b, KV head h)
+// on the tensor cores; splits s >= Sp take the fp16 residual tokens.  Every
+// split writes a partial (o, m, l); the last one of the head merges them.
 template <int BITS>
 __global__ void __launch_bounds__(NTHREADS, 2)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
@@ -273,6 +346,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   __shared__ __align__(8) uint64_t full_bar[NSTAGE];
   __shared__ __align__(8) uint64_t empty_bar[NSTAGE];
   __shared__ float q_s[QB][D];
+  __shared__ float qsum_s[QB][NG];  // sum of q over each group
+  __shared__ int s_rng[3];
   __shared__ volatile int s_abort;
   __shared__ int s_last;
 
@@ -283,6 +358,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;  // MMA group id
   const int t = lane & 3;   // thread in group
+  const bool res_cta = s >= a.Sp;
+  const int64_t bh = (int64_t)b * a.Hkv + h;
 
   // Prologue that touches no global memory; the rest waits for the grid this
   // launch depends on (the append of the same step) to complete.
@@ -293,35 +370,24 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     }
     s_abort = 0;
     ptx::fence_mbar_init();
-  }
-  if (threadIdx.x == 0) {
-    ptx::prefetch_tensormap(&tm_kc);
-    ptx::prefetch_tensormap(&tm_vc);
-    ptx::prefetch_tensormap(&tm_kp);
-    ptx::prefetch_tensormap(&tm_vp);
+    if (!res_cta) {
+      ptx::prefetch_tensormap(&tm_kc);
+      ptx::prefetch_tensormap(&tm_vc);
+      ptx::prefetch_tensormap(&tm_kp);
+      ptx::prefetch_tensormap(&tm_vp);
+    }
   }
   grid_dependency_wait();
 
-  const int Lp = a.packed_len[b];
-  const int Lr = a.res_len[b];
-  const int rh = a.res_head[b];
-  int i0, i1, j0, j1;
-  split_range(Lp, Lr, s, a.S, 2 * (G::RB + 4 * NG), 4 * D, i0, i1, j0, j1);
-  const int npk = i1 - i0;
-  const int ntiles = (npk + T - 1) / T;
-  const int64_t bh = (int64_t)b * a.Hkv + h;
-  const int row0 = (int)(bh * a.cap + i0);  // first packed row of this split (TMA y)
-
-  for (int idx = threadIdx.x; idx < QB * D; idx += NTHREADS) {
-    const int i = idx / D, e = idx % D;
-    float v = 0.f;
-    if (i < a.gq) v = __half2float(a.q[((int64_t)b * a.Hq + h * a.gq + i) * D + e]);
-    q_s[i][e] = v;
-  }
-  if (s == 0 && Lp + Lr == 0 && threadIdx.x == 0) set_error(a.err_word, KVQ_ERRBIT_EMPTY);
-  __syncthreads();  // barriers initialised, q staged
-
-  // Issue tile `tile` into its stage (one thread).
+  // The small loads go first -- q by every thread, the lengths by thread 0 --
+  // so they are not queued behind the bulk tile copies.  QB * D / 128 = 4 halves
+  // per thread; query heads past gq (gq < 4) stay zero.
+  const int q_i = (threadIdx.x * 4) / D;
+  uint2 qraw = make_uint2(0, 0);
+  if (q_i < a.gq)
+    qraw = *reinterpret_cast<const uint2*>(a.q + ((int64_t)b * a.Hq + h * a.gq) * D + threadIdx.x * 4);
+  int i0 = 0, i1 = 0, ntiles = 0, row0 = 0;
+  int issued = 0;  // meaningful in thread 0 only
   auto issue = [&](int tile) {
     const int st = tile % NSTAGE;
     uint8_t* base = smem + (size_t)st * G::STAGE;
@@ -333,137 +399,126 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     ptx::tma_load_2d(ptx::smem_u32(base + G::KP), &tm_kp, 0, y, fb);
     ptx::tma_load_2d(ptx::smem_u32(base + G::VP), &tm_vp, 0, y, fb);
   };
-  int issued = 0;  // meaningful in thread 0 only
   if (threadIdx.x == 0) {
-    for (; issued < ntiles && issued < NSTAGE; ++issued) issue(issued);
+    const int Lp = a.packed_len[b];
+    const int Lr = a.res_len[b];
+    int r0_, r1_;
+    if (!res_cta) {
+      r0_ = (int)((int64_t)Lp * s / a.Sp);
+      r1_ = (int)((int64_t)Lp * (s + 1) / a.Sp);
+    } else {
+      const int Sr = a.S - a.Sp, sr = s - a.Sp;
+      r0_ = (int)((int64_t)Lr * sr / Sr);
+      r1_ = (int)((int64_t)Lr * (sr + 1) / Sr);
+    }
+    s_rng[0] = r0_;
+    s_rng[1] = r1_;
+    s_rng[2] = a.res_head[b];
+    if (s == 0 && Lp + Lr == 0) set_error(a.err_word, KVQ_ERRBIT_EMPTY);
+    if (!res_cta) {
+      i0 = r0_;
+      i1 = r1_;
+      ntiles = (i1 - i0 + T - 1) / T;
+      row0 = (int)(bh * a.cap + i0);  // first packed row of this split (TMA y)
+      for (; issued < ntiles && issued < NSTAGE; ++issued) issue(issued);
+    }
   }
-
-  const float kq = a.qk_scale_log2;
-
-  float m_ref[2] = {-INFINITY, -INFINITY};  // queries 2(t&1) + e, log2 units
-  float oc[NG][2][4];                        // O^T accumulators: [group][m-tile][frag]
-  float mnacc[4];                            // C-fragment of the min/scale/l MMA
-#pragma unroll
-  for (int x = 0; x < NG; ++x)
-#pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) oc[x][m][r] = 0.f;
-#pragma unroll
-  for (int r = 0; r < 4; ++r) mnacc[r] = 0.f;
-  // residual-token state (CUDA cores): lane owns head_dim values 4*lane .. 4*lane+3
-  float rm[QB], rl[QB], ro[QB][4];
-#pragma unroll
-  for (int i = 0; i < QB; ++i) {
-    rm[i] = -INFINITY;
-    rl[i] = 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) ro[i][j] = 0.f;
-  }
-
   {
-    // ------------------------------------------------- consumers: residual
-    // The fp16 residual tokens go first, while the first tiles are in flight.
-    // Chunks of 32 tokens per warp: lane = token for the scores, lane = 4
-    // head_dim values for the weighted sum; every load of a chunk is issued
-    // before its arithmetic.
-    for (int base = j0 + warp * 32; base < j1; base += NCW * 32) {
-      const int j = base + lane;
-      const bool valid = j < j1;
-      float scv[QB];
+    const int e = (threadIdx.x * 4) % D;
+    const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&qraw.x));
+    const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&qraw.y));
+    q_s[q_i][e] = f01.x;
+    q_s[q_i][e + 1] = f01.y;
+    q_s[q_i][e + 2] = f23.x;
+    q_s[q_i][e + 3] = f23.y;
+  }
+  __syncthreads();  // barriers initialised, range and q staged
+  const float kq = a.qk_scale_log2;
+  MergeSmem& ms = *reinterpret_cast<MergeSmem*>(smem);
+
+  if (res_cta) {
+    // ------------------------------------------------ residual-token split
+    float rm[QB], rl[QB], ro[QB][4];
 #pragma unroll
-      for (int i = 0; i < QB; ++i) scv[i] = 0.f;
-      {
-        const uint4* krow = reinterpret_cast<const uint4*>(a.k_res + (bh * a.Nr + (rh + (valid ? j : j0)) % a.Nr) * D);
+    for (int i = 0; i < QB; ++i) {
+      rm[i] = -INFINITY;
+      rl[i] = 0.f;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint4 kr[D / 16];
-#pragma unroll
-          for (int e8 = 0; e8 < D / 16; ++e8)
-            kr[e8] = valid ? __ldg(krow + half * (D / 16) + e8) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-          for (int e8 = 0; e8 < D / 16; ++e8) {
-            float xv[8];
-            unpack8_f16(kr[e8], xv);
-            const int d0 = (half * (D / 16) + e8) * 8;
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-#pragma unroll
-              for (int i = 0; i < QB; ++i) scv[i] = fmaf(xv[e], q_s[i][d0 + e], scv[i]);
-          }
-        }
-      }
-      float pr[QB];
+      for (int j = 0; j < 4; ++j) ro[i][j] = 0.f;
+    }
+    residual_tokens(a, bh, s_rng[2], s_rng[0], s_rng[1], warp, lane, q_s, kq, rm, rl, ro);
+    if (lane == 0) {
 #pragma unroll
       for (int i = 0; i < QB; ++i) {
-        const float v = valid ? scv[i] * kq : -INFINITY;
-        const float mnew = fmaxf(rm[i], warp_max(v));
-        const float al = exp2f(rm[i] - mnew);
-        pr[i] = valid ? exp2f(v - mnew) : 0.f;
-        rl[i] = rl[i] * al + warp_sum(pr[i]);
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) ro[i][jj] *= al;
-        rm[i] = mnew;
-      }
-      const int nv = min(32, j1 - base);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint2 vv[16];
-#pragma unroll
-        for (int tt = 0; tt < 16; ++tt) {
-          const int idx = half * 16 + tt;
-          const int jj = base + (idx < nv ? idx : 0);
-          vv[tt] = __ldg(reinterpret_cast<const uint2*>(a.v_res + (bh * a.Nr + (rh + jj) % a.Nr) * D + lane * 4));
-        }
-#pragma unroll
-        for (int tt = 0; tt < 16; ++tt) {
-          const int idx = half * 16 + tt;
-          const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&vv[tt].x));
-          const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&vv[tt].y));
-#pragma unroll
-          for (int i = 0; i < QB; ++i) {
-            float pt = __shfl_sync(0xffffffffu, pr[i], idx);
-            pt = idx < nv ? pt : 0.f;
-            ro[i][0] = fmaf(pt, f01.x, ro[i][0]);
-            ro[i][1] = fmaf(pt, f01.y, ro[i][1]);
-            ro[i][2] = fmaf(pt, f23.x, ro[i][2]);
-            ro[i][3] = fmaf(pt, f23.y, ro[i][3]);
-          }
-        }
+        ms.m[warp][i] = rm[i];
+        ms.l[warp][i] = rl[i];
       }
     }
+#pragma unroll
+    for (int i = 0; i < QB; ++i)
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) ms.o[warp][i][lane * 4 + jj] = ro[i][jj];
+  } else {
+    // ---------------------------------------------------- packed-token split
+    {
+      // sum of q per (query, group), eight threads each
+      const int sidx = threadIdx.x >> 3, part = threadIdx.x & 7;
+      const int qi = sidx >> 2, grp = sidx & 3;
+      float sum = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sum += q_s[qi][grp * kGroup + part * 4 + k];
+#pragma unroll
+      for (int o = 1; o <= 4; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      if (part == 0) qsum_s[qi][grp] = sum;
+    }
+    i0 = s_rng[0];
+    i1 = s_rng[1];
+    const int npk = i1 - i0;
+    ntiles = (npk + T - 1) / T;
+    row0 = (int)(bh * a.cap + i0);
+    __syncthreads();  // qsum_s ready
 
-    // --------------------------------------------- consumers: packed tiles
-    // q as B fragments: bq[P][s][0] for k rows 2t, 2t+1; bq[P][s][1] for 2t+8, 2t+9.
+    float m_ref = -INFINITY;  // running max of query t, log2 units
+    float oc[NG][2][4];       // O^T accumulators: [group][m-tile][frag]
+    float mnacc[4];           // C-fragment of the min/scale/l MMA
+#pragma unroll
+    for (int x = 0; x < NG; ++x)
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) oc[x][m][r] = 0.f;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) mnacc[r] = 0.f;
+
+    // q as B fragments of the K-side MMA.  Column n = 2 * query + group bit:
+    // even columns take the pair's first group, odd ones its second, so the
+    // accumulator a thread holds (columns 2t, 2t+1) is query t for both groups.
+    // bq[P][s][0] covers k rows 2t, 2t+1 and bq[P][s][1] rows 2t+8, 2t+9.
     uint32_t bq[2][4][2];
-    float qsum[2][2];  // [pair][e]: sum of q over the thread's group of that pair
+    float qs_t[NG];  // query t: group sums of q
 #pragma unroll
-    for (int P = 0; P < 2; ++P) {
+    for (int x = 0; x < NG; ++x) qs_t[x] = qsum_s[t][x];
+    {
+      const int qi = g >> 1;
 #pragma unroll
-      for (int st = 0; st < 4; ++st) {
-        if (BITS == 4) {
-          // k-cols 2t, 2t+1 <- group P, d = 8t + st (+4); 2t+8, 2t+9 <- group P+2
-          const int da = 32 * P + 8 * t + st;
-          const int db = 32 * (P + 2) + 8 * t + st;
-          bq[P][st][0] = g < 4 ? ptx::pack_h2(q_s[g][da], q_s[g][da + 4]) : 0u;
-          bq[P][st][1] = g >= 4 ? ptx::pack_h2(q_s[g - 4][db], q_s[g - 4][db + 4]) : 0u;
-        } else {
-          // thread t's codes: d = 64P + 16t + j; k-cols 2t, 2t+1 <- j = 2st, 2st+8;
-          // 2t+8, 2t+9 <- j = 2st+1, 2st+9; group 2P + (t >> 1) -> column block
-          const bool nz = (g < 4) == ((t >> 1) == 0);
-          const int qi = g & 3;
-          const int d0 = 64 * P + 16 * t + 2 * st;
-          bq[P][st][0] = nz ? ptx::pack_h2(q_s[qi][d0], q_s[qi][d0 + 8]) : 0u;
-          bq[P][st][1] = nz ? ptx::pack_h2(q_s[qi][d0 + 1], q_s[qi][d0 + 9]) : 0u;
+      for (int P = 0; P < 2; ++P) {
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+          if (BITS == 4) {
+            // k rows 2t, 2t+1 <- group P, d = 8t + st (+4); 2t+8, 2t+9 <- group P+2
+            const int da = 32 * P + 8 * t + st;
+            const int db = 32 * (P + 2) + 8 * t + st;
+            bq[P][st][0] = (g & 1) == 0 ? ptx::pack_h2(q_s[qi][da], q_s[qi][da + 4]) : 0u;
+            bq[P][st][1] = (g & 1) == 1 ? ptx::pack_h2(q_s[qi][db], q_s[qi][db + 4]) : 0u;
+          } else {
+            // thread t's codes: d = 64P + 16t + j, group 2P + (t >> 1); k rows
+            // 2t, 2t+1 <- j = 2st, 2st+8; 2t+8, 2t+9 <- j = 2st+1, 2st+9
+            const bool nz = (g & 1) == (t >> 1);
+            const int d0 = 64 * P + 16 * t + 2 * st;
+            bq[P][st][0] = nz ? ptx::pack_h2(q_s[qi][d0], q_s[qi][d0 + 8]) : 0u;
+            bq[P][st][1] = nz ? ptx::pack_h2(q_s[qi][d0 + 1], q_s[qi][d0 + 9]) : 0u;
+          }
         }
-      }
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int qi = 2 * (t & 1) + e;
-        const int grp = BITS == 4 ? P + 2 * (t >> 1) : 2 * P + (t >> 1);
-        float sum = 0.f;
-        for (int k = 0; k < kGroup; ++k) sum += q_s[qi][grp * kGroup + k];
-        qsum[P][e] = sum;
       }
     }
 
@@ -475,8 +530,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         break;
       }
       uint8_t* base = smem + (size_t)st * G::STAGE;
-      const int wrow = 32 * warp;                            // first row of this warp
-      const int nvalid = min(npk - tile * T - wrow, 32);     // rows of this warp still ours
+      const int wrow = 32 * warp;                         // first row of this warp
+      const int nvalid = min(npk - tile * T - wrow, 32);  // rows of this warp still ours
       if (nvalid > 0) {
         // rows past the split end may hold anything: zero their params so no
         // Inf/NaN reaches the arithmetic (their scores are masked anyway)
@@ -497,52 +552,46 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 #pragma unroll
         for (int u = 0; u < NSUB; ++u) qk_subtile<BITS>(kc, wrow + 16 * u, lane, bq, acc[u]);
 
-        // fix-up: scale, min and centre per (row, group), fp32; rows past the end masked
-        float sv[NSUB][2][2];  // [sub-tile][row g / g+8][e]
+        // fix-up, fp32: acc_g = sum (c - C) q, so s = sum_g scale_g acc_g +
+        // (min_g + C scale_g) qsum_g for query t; rows past the split end masked
+        float sv[NSUB][2];  // [sub-tile][row g / g+8]
 #pragma unroll
         for (int u = 0; u < NSUB; ++u) {
 #pragma unroll
           for (int rr = 0; rr < 2; ++rr) {
             const int row = wrow + 16 * u + g + 8 * rr;
-            const uint32_t* prow = kp + row * NG;
-            float part[2] = {0.f, 0.f};
+            const uint4 pr = reinterpret_cast<const uint4*>(kp)[row];
+            const uint32_t prm[NG] = {pr.x, pr.y, pr.z, pr.w};
+            float acc_s = 0.f;
 #pragma unroll
             for (int P = 0; P < 2; ++P) {
-              const int grp = BITS == 4 ? P + 2 * (t >> 1) : 2 * P + (t >> 1);
-              const uint32_t pr = prow[grp];
-              const float scale = half_lo(pr);
-              const float mnc = fmaf((float)C, scale, half_hi(pr));
-#pragma unroll
-              for (int e = 0; e < 2; ++e)
-                part[e] = fmaf(scale, acc[u][P][2 * rr + e], fmaf(mnc, qsum[P][e], part[e]));
+              const int ga = BITS == 4 ? P : 2 * P;
+              const int gb = BITS == 4 ? P + 2 : 2 * P + 1;
+              acc_s = fmaf(half_lo(prm[ga]), acc[u][P][2 * rr], acc_s);
+              acc_s = fmaf(half_lo(prm[gb]), acc[u][P][2 * rr + 1], acc_s);
             }
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float tot = part[e] + __shfl_xor_sync(0xffffffffu, part[e], 2);
-              sv[u][rr][e] = (16 * u + g + 8 * rr < nvalid) ? tot : -INFINITY;
-            }
+            for (int x = 0; x < NG; ++x)
+              acc_s = fmaf(fmaf((float)C, half_lo(prm[x]), half_hi(prm[x])), qs_t[x], acc_s);
+            sv[u][rr] = (16 * u + g + 8 * rr < nvalid) ? acc_s : -INFINITY;
           }
         }
 
         // ---------------- online softmax over the warp's 32 rows (lazy rescale)
-        float mloc[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float mx = fmaxf(fmaxf(sv[0][0][e], sv[0][1][e]), fmaxf(sv[1][0][e], sv[1][1][e]));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          mloc[e] = mx * kq;
-        }
-        const bool need0 = mloc[0] > m_ref[0] + 8.f;
-        const bool need1 = mloc[1] > m_ref[1] + 8.f;
-        if (__any_sync(0xffffffffu, need0 || need1)) {
-          const float m0 = need0 ? mloc[0] : m_ref[0];
-          const float m1 = need1 ? mloc[1] : m_ref[1];
-          const float al0 = need0 ? exp2f(m_ref[0] - m0) : 1.f;
-          const float al1 = need1 ? exp2f(m_ref[1] - m1) : 1.f;
-          m_ref[0] = m0;
-          m_ref[1] = m1;
+        float mx = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mloc = mx * kq;
+        const bool need = mloc > m_ref + 8.f;
+        if (__any_sync(0xffffffffu, need)) {
+          const float mnew = need ? mloc : m_ref;
+          const float al = need ? exp2f(m_ref - mnew) : 1.f;
+          m_ref = mnew;
+          // this thread's O columns are queries 2t and 2t+1: their factors live
+          // in lanes whose t is 2t and 2t+1
+          const float al0 = __shfl_sync(0xffffffffu, al, (lane & ~3) | ((2 * t) & 3));
+          const float al1 = __shfl_sync(0xffffffffu, al, (lane & ~3) | ((2 * t + 1) & 3));
 #pragma unroll
           for (int x = 0; x < NG; ++x)
 #pragma unroll
@@ -557,23 +606,19 @@ __global__ void __launch_bounds__(NTHREADS, 2)
           mnacc[2] *= al0;
           mnacc[3] *= al1;
         }
-        const float mu0 = m_ref[0] == -INFINITY ? 0.f : m_ref[0];
-        const float mu1 = m_ref[1] == -INFINITY ? 0.f : m_ref[1];
-        const int srcA = (2 * t) * 4 + ((g >> 1) & 1);
-        const int srcB = (2 * t + 1) * 4 + ((g >> 1) & 1);
-        const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;
+        const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+        // p as the PV B fragment: thread (g, t) needs p(query g, tokens 2t, 2t+1,
+        // 2t+8, 2t+9); lane (token % 8) * 4 + g holds query g for rows token and token + 8
+        const int srcA = (2 * t) * 4 + (g & 3);
+        const int srcB = (2 * t + 1) * 4 + (g & 3);
         const bool qreal = g < 4;
 #pragma unroll
         for (int u = 0; u < NSUB; ++u) {
-          // p as the PV B fragment: this thread needs p(query g, tokens 2t, 2t+1, 2t+8, 2t+9)
-          const uint32_t plo = ptx::pack_h2(exp2f(fmaf(sv[u][0][0], kq, -mu0)), exp2f(fmaf(sv[u][0][1], kq, -mu1)));
-          const uint32_t phi = ptx::pack_h2(exp2f(fmaf(sv[u][1][0], kq, -mu0)), exp2f(fmaf(sv[u][1][1], kq, -mu1)));
-          const uint32_t x0 = __shfl_sync(0xffffffffu, plo, srcA);
-          const uint32_t x1 = __shfl_sync(0xffffffffu, plo, srcB);
-          const uint32_t y0 = __shfl_sync(0xffffffffu, phi, srcA);
-          const uint32_t y1 = __shfl_sync(0xffffffffu, phi, srcB);
-          const uint32_t pb0 = qreal ? ptx::prmt(x0, x1, sel) : 0u;  // tokens 2t, 2t+1
-          const uint32_t pb1 = qreal ? ptx::prmt(y0, y1, sel) : 0u;  // tokens 2t+8, 2t+9
+          const uint32_t pk = ptx::pack_h2(exp2f(fmaf(sv[u][0], kq, -mu)), exp2f(fmaf(sv[u][1], kq, -mu)));
+          const uint32_t x0 = __shfl_sync(0xffffffffu, pk, srcA);  // (p(2t), p(2t+8))
+          const uint32_t x1 = __shfl_sync(0xffffffffu, pk, srcB);  // (p(2t+1), p(2t+9))
+          const uint32_t pb0 = qreal ? ptx::prmt(x0, x1, 0x5410u) : 0u;  // tokens 2t, 2t+1
+          const uint32_t pb1 = qreal ? ptx::prmt(x0, x1, 0x7632u) : 0u;  // tokens 2t+8, 2t+9
           pv_subtile<BITS>(vc, vp, wrow + 16 * u, lane, pb0, pb1, oc, mnacc);
         }
       }
@@ -592,28 +637,20 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       __syncwarp();  // reconverge warp 0 before the next tile's .sync.aligned instructions
       if (s_abort) break;
     }
-  }
-  // Copies still in flight (only after an abort) land before the ring is reused.
-  if (threadIdx.x == 0) {
-    const int first = issued > NSTAGE ? issued - NSTAGE : 0;
-    for (int tile = first; tile < issued; ++tile)
-      ptx::mbar_wait_bounded(ptx::smem_u32(&full_bar[tile % NSTAGE]), (tile / NSTAGE) & 1);
-  }
-
-  // ---------------- merge the warps' states and write this split's partial
-  __syncthreads();  // the stage ring is idle from here on
-  MergeSmem& ms = *reinterpret_cast<MergeSmem*>(smem);
-  {
-    // tensor-core state: min/scale/l rows to shared memory first
+    // Copies still in flight (only after an abort) land before the ring is reused.
+    if (threadIdx.x == 0) {
+      const int first = issued > NSTAGE ? issued - NSTAGE : 0;
+      for (int tile = first; tile < issued; ++tile)
+        ptx::mbar_wait_bounded(ptx::smem_u32(&full_bar[tile % NSTAGE]), (tile / NSTAGE) & 1);
+    }
+    __syncthreads();  // the stage ring is idle from here on: reuse it for the merge
+    // min/scale/l rows to shared memory first, then the full outputs
     ms.mn[warp][g][2 * t] = mnacc[0];
     ms.mn[warp][g][2 * t + 1] = mnacc[1];
     if (g == 0) {
       ms.mn[warp][8][2 * t] = mnacc[2];
       ms.mn[warp][8][2 * t + 1] = mnacc[3];
-    }
-    if (g == 0 && t < 2) {
-      ms.m[warp][2 * t] = m_ref[0];
-      ms.m[warp][2 * t + 1] = m_ref[1];
+      ms.m[warp][t] = m_ref;
     }
     __syncwarp();
     if (t < 2) {
@@ -635,30 +672,20 @@ __global__ void __launch_bounds__(NTHREADS, 2)
           }
     }
     if (lane < QB) ms.l[warp][lane] = ms.mn[warp][8][lane];
-    // residual state
-    if (lane == 0) {
-#pragma unroll
-      for (int i = 0; i < QB; ++i) {
-        ms.m[NCW + warp][i] = rm[i];
-        ms.l[NCW + warp][i] = rl[i];
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < QB; ++i)
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) ms.o[NCW + warp][i][lane * 4 + jj] = ro[i][jj];
   }
+
+  // ---------------- merge the four warps' states and write this split's partial
   __syncthreads();
-  const int64_t pidx = ((int64_t)b * a.Hkv + h) * a.S + s;
+  const int64_t pidx = bh * a.S + s;
   for (int idx = threadIdx.x; idx < QB * D; idx += NTHREADS) {
     const int i = idx / D, e = idx % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < 2 * NCW; ++w) M = fmaxf(M, ms.m[w][i]);
+    for (int w = 0; w < NCW; ++w) M = fmaxf(M, ms.m[w][i]);
     float osum = 0.f, lsum = 0.f;
     if (M > -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < 2 * NCW; ++w) {
+      for (int w = 0; w < NCW; ++w) {
         const float f = exp2f(ms.m[w][i] - M);
         if (f > 0.f) {
           osum = fmaf(ms.o[w][i][e], f, osum);
@@ -670,8 +697,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     if (e == 0) a.ml_part[pidx * QB + i] = make_float2(M, lsum);
   }
   // the last split of this KV head to finish merges all S partials
-  if (take_last_ticket<NTHREADS>(a, (int64_t)b * a.Hkv + h, &s_last))
-    combine_unit<NTHREADS, D>(a, b, h, 0, reinterpret_cast<float*>(smem));
+  if (take_last_ticket<NTHREADS>(a, bh, &s_last))
+    combine_unit<NTHREADS, D, 40>(a, b, h, 0, reinterpret_cast<float*>(smem));
 }
 
 // --------------------------------------------------------- tensor maps -----

@@ -105,7 +105,8 @@ struct DecodePlan {
   int gq;       // query heads per KV head
   int qb;       // query heads handled by one CTA (power of two, <= 8)
   int nqb;      // query blocks per KV head = ceil(gq / qb)
-  int splits;   // S
+  int splits;   // S (all splits)
+  int splits_packed;  // tensor-core kernel: the first splits_packed take packed tokens
   int threads;  // threads per CTA of the split kernel
   size_t ws_partials;  // bytes of the o partials (offset 0)
   size_t ws_ml_off;    // offset of the {m, l} partials

@@ -120,11 +120,28 @@ struct AppendArgs {
 };
 
 template <int BITS>
-__global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
+__global__ void __launch_bounds__(1024) append_kernel(AppendArgs a) {
   // The decode of the same step may start launching now; it waits for this
   // grid to finish (griddepcontrol.wait) before it reads the cache.
   asm volatile("griddepcontrol.launch_dependents;");
   const int b = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const bool active = lane * 8 < a.d;
+  // the new tokens do not depend on the counters: start their loads first
+  constexpr int kMaxItems = 4;  // items per warp whose new token is loaded up front
+  uint4 newv[kMaxItems];
+#pragma unroll
+  for (int k = 0; k < kMaxItems; ++k) {
+    const int item = warp + k * nwarps;
+    newv[k] = make_uint4(0, 0, 0, 0);
+    if (item < 2 * a.Hkv && active) {
+      const int64_t bh = (int64_t)b * a.Hkv + (item >> 1);
+      const __half* nsrc = ((item & 1) ? a.v_new : a.k_new) + bh * a.d;
+      newv[k] = __ldg(reinterpret_cast<const uint4*>(nsrc + lane * 8));
+    }
+  }
   const int pl = a.packed_len[b];
   const int rl = a.res_len[b];
   const int rh = a.res_head[b];
@@ -133,22 +150,29 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
     if (threadIdx.x == 0) set_error(a.err_word, KVQ_ERRBIT_CAPACITY);
     return;
   }
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int nwarps = blockDim.x >> 5;
-  const bool active = lane * 8 < a.d;
   const int slot_new = (a.Nr == 0) ? 0 : (pack_now ? rh : (rh + rl) % a.Nr);
 
-  for (int item = warp; item < 2 * a.Hkv; item += nwarps) {
+  for (int k = 0;; ++k) {
+    const int item = warp + k * nwarps;
+    if (item >= 2 * a.Hkv) break;  // warp-uniform
     const int which = item & 1;
     const int h = item >> 1;
     const int64_t bh = (int64_t)b * a.Hkv + h;
-    const __half* nsrc = (which ? a.v_new : a.k_new) + bh * a.d;
-    uint4 newv = make_uint4(0, 0, 0, 0);
-    if (active) newv = __ldg(reinterpret_cast<const uint4*>(nsrc + lane * 8));
-    __half* ring_row = (a.Nr > 0) ? a.res[which] + (bh * a.Nr + slot_new) * a.d : nullptr;
+    uint4 nv = make_uint4(0, 0, 0, 0);
+    if (k < kMaxItems) {
+#pragma unroll
+      for (int kk = 0; kk < kMaxItems; ++kk)
+        if (kk == k) nv = newv[kk];
+    } else if (active) {  // more than four items per warp: load here
+      const __half* nsrc = (which ? a.v_new : a.k_new) + bh * a.d;
+      nv = __ldg(reinterpret_cast<const uint4*>(nsrc + lane * 8));
+    }
+    __half* const res_base = which ? a.res[1] : a.res[0];
+    uint8_t* const codes_base = which ? a.codes[1] : a.codes[0];
+    uint32_t* const params_base = which ? a.params[1] : a.params[0];
+    __half* ring_row = (a.Nr > 0) ? res_base + (bh * a.Nr + slot_new) * a.d : nullptr;
     if (pack_now) {
-      uint4 oldv = newv;
+      uint4 oldv = nv;
       if (a.Nr > 0 && active) oldv = *reinterpret_cast<const uint4*>(ring_row + lane * 8);
       float x[8];
       unpack8_f16(oldv, x);
@@ -157,15 +181,15 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
       if (active) {
         const int64_t row = bh * a.cap + pl;
         const int g = lane >> 2, quad = lane & 3;
-        uint8_t* dst = a.codes[which] + row * a.row_bytes + g * (4 * BITS) + quad * BITS;
+        uint8_t* dst = codes_base + row * a.row_bytes + g * (4 * BITS) + quad * BITS;
         if (BITS == 4)
           *reinterpret_cast<uint32_t*>(dst) = packed;
         else
           *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
-        if (quad == 0) a.params[which][row * a.Ng + g] = prm;
+        if (quad == 0) params_base[row * a.Ng + g] = prm;
       }
     }
-    if (a.Nr > 0 && active) *reinterpret_cast<uint4*>(ring_row + lane * 8) = newv;
+    if (a.Nr > 0 && active) *reinterpret_cast<uint4*>(ring_row + lane * 8) = nv;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -237,7 +261,9 @@ cudaError_t launch_append(const Dims& s, const kvq_cache_view& v, const __half* 
   a.row_bytes = s.row_bytes;
   a.cap = s.cap;
   a.Nr = s.Nr;
-  const int threads = 32 * (2 * s.Hkv < 8 ? 2 * s.Hkv : 8);
+  // one warp per (KV head, K or V) item, up to 32 warps (then more items per warp)
+  const int items = 2 * s.Hkv;
+  const int threads = 32 * (items < 32 ? items : 32);
   if (s.bits == 4)
     append_kernel<4><<<s.B, threads, 0, st>>>(a);
   else
