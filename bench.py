@@ -304,7 +304,7 @@ def run_ours(args, rank, world, local):
     else:
         ms_step_all, value_all = ms_per_step, value
 
-    plan_kernels = 1 + 2  # append + (split-KV decode, combine)
+    plan_kernels = 2  # append, then split-KV decode with its combine fused in
     res = {
         "metric": "quantized-KV decode attention: achieved HBM GB/s (% of peak), us/step",
         "value": round(value_all, 2),

@@ -11,8 +11,8 @@
 //    TMA tile loads into a 4-stage (INT4) or 6-stage (INT2) shared-memory ring
 //    guarded by mbarriers (the asynchronous staging of the BitDecoding page,
 //    section 2.3, done with the bulk tensor copy instead of per-thread
-//    cp.async).  One thread issues the first stages up front and refills a
-//    stage as soon as all four warps have released it.  Code
+//    cp.async).  One thread issues the first stages up front; the warp that
+//    releases a stage last refills it at once.  Code
 //    tiles use the TMA 64-byte (INT4) or 32-byte (INT2) swizzle, the XOR
 //    swizzle of the BitDecoding page's equation (2), which makes every ldmatrix
 //    below conflict-free.
@@ -344,7 +344,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
   __shared__ __align__(8) uint64_t full_bar[NSTAGE];
-  __shared__ __align__(8) uint64_t empty_bar[NSTAGE];
+  __shared__ int s_rel[NSTAGE];        // warps done with the stage's current tile
+  __shared__ int s_last_tile[NSTAGE];  // last tile issued into each stage (-1: none)
   __shared__ float q_s[QB][D];
   __shared__ float qsum_s[QB][NG];  // sum of q over each group
   __shared__ int s_rng[3];
@@ -366,7 +367,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   if (threadIdx.x == 0) {
     for (int st = 0; st < NSTAGE; ++st) {
       ptx::mbar_init(ptx::smem_u32(&full_bar[st]), 1);
-      ptx::mbar_init(ptx::smem_u32(&empty_bar[st]), NCW);
+      s_rel[st] = 0;
+      s_last_tile[st] = -1;
     }
     s_abort = 0;
     ptx::fence_mbar_init();
@@ -387,9 +389,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   if (q_i < a.gq)
     qraw = *reinterpret_cast<const uint2*>(a.q + ((int64_t)b * a.Hq + h * a.gq) * D + threadIdx.x * 4);
   int i0 = 0, i1 = 0, ntiles = 0, row0 = 0;
-  int issued = 0;  // meaningful in thread 0 only
   auto issue = [&](int tile) {
     const int st = tile % NSTAGE;
+    s_last_tile[st] = tile;
     uint8_t* base = smem + (size_t)st * G::STAGE;
     const uint32_t fb = ptx::smem_u32(&full_bar[st]);
     ptx::mbar_arrive_expect_tx(fb, G::STAGE);
@@ -420,7 +422,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       i1 = r1_;
       ntiles = (i1 - i0 + T - 1) / T;
       row0 = (int)(bh * a.cap + i0);  // first packed row of this split (TMA y)
-      for (; issued < ntiles && issued < NSTAGE; ++issued) issue(issued);
+      for (int tile = 0; tile < ntiles && tile < NSTAGE; ++tile) issue(tile);
     }
   }
   {
@@ -623,25 +625,28 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         }
       }
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&empty_bar[st]));
-      // refill this stage with tile + NSTAGE once all warps have released it
-      if (threadIdx.x == 0 && issued < ntiles && !s_abort) {
-        if (ptx::mbar_wait_bounded(ptx::smem_u32(&empty_bar[st]), (tile / NSTAGE) & 1)) {
-          issue(issued);
-          ++issued;
-        } else {
-          set_error(a.err_word, KVQ_ERRBIT_TIMEOUT);
-          s_abort = 1;
+      // Release the stage.  The warp that releases it last refills it with tile
+      // + NSTAGE straight away: nobody waits for the slowest warp.
+      if (lane == 0) {
+        __threadfence_block();  // this warp's reads of the stage come first
+        if (atomicAdd(&s_rel[st], 1) == NCW - 1) {
+          s_rel[st] = 0;
+          const int next = tile + NSTAGE;
+          if (next < ntiles && !s_abort) {
+            ptx::fence_proxy_async_shared();  // generic reads before the TMA overwrite
+            issue(next);
+          }
         }
       }
-      __syncwarp();  // reconverge warp 0 before the next tile's .sync.aligned instructions
+      __syncwarp();
       if (s_abort) break;
     }
+    __syncthreads();
     // Copies still in flight (only after an abort) land before the ring is reused.
     if (threadIdx.x == 0) {
-      const int first = issued > NSTAGE ? issued - NSTAGE : 0;
-      for (int tile = first; tile < issued; ++tile)
-        ptx::mbar_wait_bounded(ptx::smem_u32(&full_bar[tile % NSTAGE]), (tile / NSTAGE) & 1);
+      for (int st = 0; st < NSTAGE; ++st)
+        if (s_last_tile[st] >= 0)
+          ptx::mbar_wait_bounded(ptx::smem_u32(&full_bar[st]), (s_last_tile[st] / NSTAGE) & 1);
     }
     __syncthreads();  // the stage ring is idle from here on: reuse it for the merge
     // min/scale/l rows to shared memory first, then the full outputs
