@@ -17,21 +17,24 @@
 //    swizzle of the BitDecoding page's equation (2), which makes every ldmatrix
 //    below conflict-free.
 //  * Four warps take 32 tokens (two independent 16-token sub-tiles) each per
-//    tile.  ldmatrix brings code words to
-//    registers; a magic-number lop3 (0x6400 | c is the fp16 value 1024 + c) and
-//    one HADD2/HFMA2 turn them into the exact fp16 integers c - C (C = 8 for
-//    INT4, 2 for INT2).  Integer codes are exact in fp16, so the tensor cores
-//    see exact operands; scale and min are applied in fp32.
+//    tile.  ldmatrix brings code words to registers, and a single AND turns
+//    two codes into one exact half2: a code c sitting in the low mantissa bits
+//    of an fp16 whose exponent field is zero is the subnormal c * 2^-24 (a code
+//    at bit offset 2 or 4 is 4c or 16c times 2^-24).  The tensor cores take
+//    these exact operands as they are; the per-position weight 1/4/16 is
+//    divided out of the q operand (K side) or out of the output row (V side),
+//    and 2^24 goes into the softmax scale.  Scale and min are applied in fp32.
 //  * QK:  S^T = K q^T with tokens on M (mma.sync m16n8k16, fp32 accumulate).
 //    Two groups share one MMA through a block-diagonal q operand (column
 //    2 * query + group bit), so each thread holds one query for both groups,
-//    then  s = sum_g scale_g * acc_g + (min_g + C * scale_g) * sum_{d in g} q_d.
+//    then  s = sum_g scale_g * acc_g + min_g * sum_{d in g} q_d.
 //  * Online softmax in fp32 (exp2 domain) with a lazy rescale: the running max
 //    only moves when it grows by more than 2^8.
-//  * PV:  O^T = (c - C)^T (p * scale)^T with V codes read through
-//    ldmatrix.trans; the per-token, per-group p * scale is the B operand.  A
-//    ninth MMA accumulates sum p * min_g, sum p * scale_g and sum p (= l) per
-//    group, so O = O_c + sum p min_g + C sum p scale_g.
+//  * PV:  O^T = c^T (p * scale)^T with V codes read through ldmatrix.trans.
+//    The B operand uses the same column order (2 * query + group bit) with
+//    p * scale of that group, so one MMA serves two groups and each thread
+//    again holds one query.  A ninth MMA accumulates sum p * min_g and sum p
+//    (= l), so O = O_c + sum_g p min_g.
 //  * The fp16 residual tokens get splits of their own (CUDA cores, all loads of
 //    a chunk in one round), so no packed split waits on them.  Per-warp states
 //    merge in shared memory, and the last split of a KV head to finish merges
@@ -65,7 +68,7 @@ struct Geo {
   static constexpr int VP = 2 * CODE_TILE + PAR_TILE;
   static constexpr int STAGE = 2 * CODE_TILE + 2 * PAR_TILE;  // 20 KB / 12 KB
   static constexpr int NSTAGE = BITS == 4 ? 4 : 6;               // 80 KB / 72 KB in flight
-  static constexpr int CENTER = BITS == 4 ? 8 : 2;
+  static constexpr float CENTER = BITS == 4 ? 7.5f : 1.5f;       // mid code
   static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned");
 };
 
@@ -85,56 +88,47 @@ constexpr size_t tc_smem_bytes() {
 
 // ------------------------------------------------------- code conversion ---
 
-__device__ __forceinline__ uint32_t h2const(float v) {
-  return ptx::h2_as_u32(__float2half2_rn(v));
-}
-
-// INT4: word with 8 nibbles (n0 at bits 0-3 ... n7 at 28-31) -> 4 half2 of c - 8:
-// out[0] = (n0, n4), out[1] = (n1, n5), out[2] = (n2, n6), out[3] = (n3, n7).
-__device__ __forceinline__ void cvt_int4(uint32_t w, uint32_t (&o)[4]) {
-  const uint32_t magic = 0x64006400u;
-  const uint32_t sub_lo = h2const(-(1024.f + 8.f));
-  const uint32_t mul_hi = h2const(1.f / 16.f);
-  const uint32_t sub_hi = h2const(-(64.f + 8.f));
+// Code words -> exact half2 operands (subnormal fp16, see the file comment).
+// INT4: nibble j of each 16-bit half (j = 0..3) -> out[j] = (nibble j of the
+// low half, nibble j of the high half) times W4[j] * 2^-24.
+__device__ __forceinline__ void split_int4(uint32_t w, uint32_t (&o)[4]) {
   const uint32_t w8 = w >> 8;
-  o[0] = ptx::hadd2_u32(ptx::and_or(w, 0x000F000Fu, magic), sub_lo);
-  o[1] = ptx::hfma2_u32(ptx::and_or(w, 0x00F000F0u, magic), mul_hi, sub_hi);
-  o[2] = ptx::hadd2_u32(ptx::and_or(w8, 0x000F000Fu, magic), sub_lo);
-  o[3] = ptx::hfma2_u32(ptx::and_or(w8, 0x00F000F0u, magic), mul_hi, sub_hi);
+  o[0] = w & 0x000F000Fu;
+  o[1] = w & 0x00F000F0u;
+  o[2] = w8 & 0x000F000Fu;
+  o[3] = w8 & 0x00F000F0u;
+}
+__host__ __device__ constexpr float w4_weight(int j) { return (j & 1) ? 16.f : 1.f; }
+
+// INT2: code j of each 16-bit half (bits 2j, 2j+1; j = 0..7) -> out[j] = (code
+// j of the low half, code j of the high half) times W2[j] * 2^-24, W2 = 1, 4,
+// 16, 1, 4, 16, 1, 4 (shifts by 6 and 12 keep every weight <= 16).
+__device__ __forceinline__ void split_int2(uint32_t w, uint32_t (&o)[8]) {
+  const uint32_t w6 = w >> 6, w12 = w >> 12;
+  o[0] = w & 0x00030003u;
+  o[1] = w & 0x000C000Cu;
+  o[2] = w & 0x00300030u;
+  o[3] = w6 & 0x00030003u;
+  o[4] = w6 & 0x000C000Cu;
+  o[5] = w6 & 0x00300030u;
+  o[6] = w12 & 0x00030003u;
+  o[7] = w12 & 0x000C000Cu;
+}
+__host__ __device__ constexpr float w2_weight(int j) {
+  return (j % 3) == 0 ? 1.f : ((j % 3) == 1 ? 4.f : 16.f);
 }
 
-// INT2: the four 2-bit codes at bits [2j, 2j+2) of each 16-bit half (j = 0..3)
-// -> 4 half2 of c - 2: out[j] = (code j of the low half, code j of the high half).
-__device__ __forceinline__ void cvt_int2_lo4(uint32_t w, uint32_t (&o)[4]) {
-  const uint32_t magic = 0x64006400u;
-  o[0] = ptx::hadd2_u32(ptx::and_or(w, 0x00030003u, magic), h2const(-(1024.f + 2.f)));
-  o[1] = ptx::hfma2_u32(ptx::and_or(w, 0x000C000Cu, magic), h2const(0.25f), h2const(-(256.f + 2.f)));
-  o[2] = ptx::hfma2_u32(ptx::and_or(w, 0x00300030u, magic), h2const(1.f / 16.f), h2const(-(64.f + 2.f)));
-  o[3] = ptx::hfma2_u32(ptx::and_or(w, 0x00C000C0u, magic), h2const(1.f / 64.f), h2const(-(16.f + 2.f)));
-}
-
-// INT2: 16 codes (j = 0..15 at bits [2j, 2j+2)) -> 8 half2, out[m] = (code m, code m+8).
-__device__ __forceinline__ void cvt_int2_8(uint32_t w, uint32_t (&o)[8]) {
-  uint32_t a[4], b[4];
-  cvt_int2_lo4(w, a);
-  cvt_int2_lo4(w >> 8, b);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    o[j] = a[j];
-    o[4 + j] = b[j];
-  }
-}
-
-__device__ __forceinline__ uint32_t grp_of(const uint4& u, int x) {
-  return x == 0 ? u.x : (x == 1 ? u.y : (x == 2 ? u.z : u.w));
-}
+constexpr float kTwo24 = 16777216.f;  // 2^24
 
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // QK of one 16-token sub-tile (rows r0 .. r0+15 of the stage): acc[P] holds the
-// per-pair partial dot products (fragment layout of S^T = K q^T).
+// per-pair partial dot products (fragment layout of S^T = K q^T), times 2^-24.
+// A operand registers: a0 = (row g, k 2t..2t+1), a1 = (row g+8, same k),
+// a2 = (row g, k 2t+8..2t+9), a3 = (row g+8, same k); one k-step uses one code
+// position, so one weight, which the matching bq fragment has divided out.
 template <int BITS>
 __device__ __forceinline__ void qk_subtile(uint32_t kc, int r0, int lane,
                                            const uint32_t (&bq)[2][4][2], float (&acc)[2][4]) {
@@ -147,20 +141,22 @@ __device__ __forceinline__ void qk_subtile(uint32_t kc, int r0, int lane,
   if (BITS == 4) {
 #pragma unroll
     for (int P = 0; P < 2; ++P) {
+      // w0/w1: rows g/g+8, group P; w2/w3: the same rows, group P+2 (dims 8t..8t+7)
       const int chunk = (mj < 2) ? P : P + 2;
       const uint32_t addr = kc + lrow * 64 + ((chunk ^ ((lrow >> 1) & 3)) << 4);
       uint32_t w0, w1, w2, w3;
       ptx::ldmatrix_x4(addr, w0, w1, w2, w3);
       uint32_t c0[4], c1[4], c2[4], c3[4];
-      cvt_int4(w0, c0);
-      cvt_int4(w1, c1);
-      cvt_int4(w2, c2);
-      cvt_int4(w3, c3);
+      split_int4(w0, c0);
+      split_int4(w1, c1);
+      split_int4(w2, c2);
+      split_int4(w3, c3);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         ptx::mma_16816(acc[P], c0[k], c1[k], c2[k], c3[k], bq[P][k][0], bq[P][k][1]);
     }
   } else {
+    // w[2P]/w[2P+1]: rows g/g+8, dims 64P + 16t .. +15 (one group per thread)
     const int chunk = mj >> 1;
     const uint32_t addr = kc + lrow * 32 + ((chunk ^ ((lrow >> 2) & 1)) << 4);
     uint32_t w[4];
@@ -168,8 +164,8 @@ __device__ __forceinline__ void qk_subtile(uint32_t kc, int r0, int lane,
 #pragma unroll
     for (int P = 0; P < 2; ++P) {
       uint32_t ca[8], cb[8];
-      cvt_int2_8(w[2 * P], ca);      // token g
-      cvt_int2_8(w[2 * P + 1], cb);  // token g + 8
+      split_int2(w[2 * P], ca);      // token g
+      split_int2(w[2 * P + 1], cb);  // token g + 8
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         ptx::mma_16816(acc[P], ca[2 * k], cb[2 * k], ca[2 * k + 1], cb[2 * k + 1], bq[P][k][0],
@@ -178,82 +174,75 @@ __device__ __forceinline__ void qk_subtile(uint32_t kc, int r0, int lane,
   }
 }
 
-// PV of one 16-token sub-tile: O^T += (c - C)^T (p * scale)^T per group, and the
-// min/scale/ones MMA.  pb0/pb1 are the sub-tile's p as B fragments.
+// PV of one 16-token sub-tile: O^T += c^T (p * scale)^T, sb[c] += the column
+// sums of p * scale (fragments 0/1: groups 2c / 2c+1 of query t), and the
+// min/scale/l MMA.
+// pb0/pb1 are the sub-tile's p as B fragments (column n -> query n / 2, tokens
+// 2t, 2t+1 and 2t+8, 2t+9).  The B operand of a code MMA scales column n by
+// the scale of group base + (n & 1), so rows of group base + 1 are right in the
+// odd columns and rows of group base in the even ones.
+//   INT4: oc[Pv][j]: row g = dim 64Pv + 4g + j (group 2Pv, fragment 0), row
+//         g+8 = dim 64Pv + 32 + 4g + j (group 2Pv+1, fragment 3).
+//   INT2: oc[c][pp]: rows g / g+8 = dims 64c + 8g + 2pp / +1, group 2c + g/4
+//         (fragments 0, 2 for g < 4; 1, 3 for g >= 4).
 template <int BITS>
 __device__ __forceinline__ void pv_subtile(uint32_t vc, const uint32_t* vp, int r0, int lane,
-                                           uint32_t pb0, uint32_t pb1, float (&oc)[NG][2][4],
-                                           float (&mnacc)[4]) {
+                                           uint32_t pb0, uint32_t pb1, float (&oc)[2][4][4],
+                                           float (&sb)[2][4], float (&mnacc)[4]) {
   const int g = lane >> 2, t = lane & 3;
   const int mj = lane >> 3, mi = lane & 7;
   const int lrow = r0 + (mj & 1) * 8 + mi;
-  const uint4* vrow = reinterpret_cast<const uint4*>(vp);
-  uint4 vpt[4];
-  vpt[0] = vrow[r0 + 2 * t];
-  vpt[1] = vrow[r0 + 2 * t + 1];
-  vpt[2] = vrow[r0 + 2 * t + 8];
-  vpt[3] = vrow[r0 + 2 * t + 9];
+  const int ra = r0 + 2 * t, rb = r0 + 2 * t + 8;  // this thread's B rows: ra, ra+1, rb, rb+1
   {
-    // A rows 0-3 = min_x, 4-7 = scale_x (x = g & 3), row 8 = ones; B = p
+    // A rows 0-3 = min of group g, rows 4-7 = scale of group g - 4, row 8 =
+    // ones, others zero; B = p
     const int xg = g & 3;
-    const uint32_t hsel = g < 4 ? 0x7632u : 0x5410u;  // min (high half) or scale (low half)
-    const uint32_t am0 = ptx::prmt(vp[(r0 + 2 * t) * NG + xg], vp[(r0 + 2 * t + 1) * NG + xg], hsel);
-    const uint32_t am2 = ptx::prmt(vp[(r0 + 2 * t + 8) * NG + xg], vp[(r0 + 2 * t + 9) * NG + xg], hsel);
+    const uint32_t hsel = g < 4 ? 0x7632u : 0x5410u;
+    const uint32_t am0 = ptx::prmt(vp[ra * NG + xg], vp[(ra + 1) * NG + xg], hsel);
+    const uint32_t am2 = ptx::prmt(vp[rb * NG + xg], vp[(rb + 1) * NG + xg], hsel);
     const uint32_t ones = g == 0 ? 0x3C003C00u : 0u;
     ptx::mma_16816(mnacc, am0, ones, am2, ones, pb0, pb1);
   }
-  if (BITS == 4) {
+  constexpr uint32_t kOnes = 0x3C003C00u;
+  const int gb = g & 1;
+  // INT2: w2[2c]/w2[2c+1] = tokens (2t, 2t+1) / (2t+8, 2t+9), dims 64c + 8g .. +7
+  uint32_t w2[4];
+  if (BITS == 2) {
+    const int chunk = mj >> 1;
+    const uint32_t addr = vc + lrow * 32 + ((chunk ^ ((lrow >> 2) & 1)) << 4);
+    ptx::ldmatrix_x4_trans(addr, w2[0], w2[1], w2[2], w2[3]);
+  }
 #pragma unroll
-    for (int Pv = 0; Pv < 2; ++Pv) {
-      const int chunk = 2 * Pv + (mj >> 1);
+  for (int c = 0; c < 2; ++c) {
+    // p * scale of group 2c + (n & 1) for this thread's column n = g
+    const int x = 2 * c + gb;
+    const uint32_t bs0 = ptx::hmul2_u32(pb0, ptx::prmt(vp[ra * NG + x], vp[(ra + 1) * NG + x], 0x5410u));
+    const uint32_t bs1 = ptx::hmul2_u32(pb1, ptx::prmt(vp[rb * NG + x], vp[(rb + 1) * NG + x], 0x5410u));
+    // the same rounded p * scale summed over the tokens (all-ones A): lets the
+    // epilogue centre the codes, so the fp16 rounding of p * scale meets
+    // |c - mid| rather than c
+    ptx::mma_16816(sb[c], kOnes, kOnes, kOnes, kOnes, bs0, bs1);
+    if (BITS == 4) {
+      // w[0]/w[1]: group 2c, tokens (2t, 2t+1) / (2t+8, 2t+9), dims 4g..4g+3;
+      // w[2]/w[3]: the same for group 2c+1
+      const int chunk = 2 * c + (mj >> 1);
       const uint32_t addr = vc + lrow * 64 + ((chunk ^ ((lrow >> 1) & 3)) << 4);
       uint32_t w[4];
       ptx::ldmatrix_x4_trans(addr, w[0], w[1], w[2], w[3]);
+      uint32_t s0[4], s1[4], s2[4], s3[4];
+      split_int4(w[0], s0);
+      split_int4(w[1], s1);
+      split_int4(w[2], s2);
+      split_int4(w[3], s3);
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int x = 2 * Pv + u;
-        const uint32_t bs0 = ptx::hmul2_u32(pb0, ptx::prmt(grp_of(vpt[0], x), grp_of(vpt[1], x), 0x5410u));
-        const uint32_t bs1 = ptx::hmul2_u32(pb1, ptx::prmt(grp_of(vpt[2], x), grp_of(vpt[3], x), 0x5410u));
-        uint32_t lo[4], hi[4];
-        cvt_int4(w[2 * u], lo);      // tokens 2t, 2t+1: d = 32x + 4g + j
-        cvt_int4(w[2 * u + 1], hi);  // tokens 2t+8, 2t+9
+      for (int j = 0; j < 4; ++j) ptx::mma_16816(oc[c][j], s0[j], s2[j], s1[j], s3[j], bs0, bs1);
+    } else {
+      uint32_t lo[8], hi[8];
+      split_int2(w2[2 * c], lo);
+      split_int2(w2[2 * c + 1], hi);
 #pragma unroll
-        for (int m = 0; m < 2; ++m)
-          ptx::mma_16816(oc[x][m], lo[2 * m], lo[2 * m + 1], hi[2 * m], hi[2 * m + 1], bs0, bs1);
-      }
-    }
-  } else {
-    const int chunk = mj >> 1;
-    const uint32_t addr = vc + lrow * 32 + ((chunk ^ ((lrow >> 2) & 1)) << 4);
-    uint32_t w[4];
-    ptx::ldmatrix_x4_trans(addr, w[0], w[1], w[2], w[3]);
-    const bool low = g < 4;
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      // one b16 unit holds 8 codes of group 2c + (g >> 2); partner lanes
-      // (lane ^ 16) swap half of them so each lane holds 4 codes of each group
-      uint32_t X[2], Y[2];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const uint32_t wv = w[2 * c + hh];
-        const uint32_t keep = low ? wv : (wv >> 8);
-        const uint32_t send = low ? (wv >> 8) : wv;
-        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 16);
-        X[hh] = low ? keep : recv;  // group 2c
-        Y[hh] = low ? recv : keep;  // group 2c + 1
-      }
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int x = 2 * c + u;
-        const uint32_t bs0 = ptx::hmul2_u32(pb0, ptx::prmt(grp_of(vpt[0], x), grp_of(vpt[1], x), 0x5410u));
-        const uint32_t bs1 = ptx::hmul2_u32(pb1, ptx::prmt(grp_of(vpt[2], x), grp_of(vpt[3], x), 0x5410u));
-        uint32_t lo[4], hi[4];
-        cvt_int2_lo4(u == 0 ? X[0] : Y[0], lo);  // tokens 2t, 2t+1
-        cvt_int2_lo4(u == 0 ? X[1] : Y[1], hi);  // tokens 2t+8, 2t+9
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-          ptx::mma_16816(oc[x][m], lo[2 * m], lo[2 * m + 1], hi[2 * m], hi[2 * m + 1], bs0, bs1);
-      }
+      for (int pp = 0; pp < 4; ++pp)
+        ptx::mma_16816(oc[c][pp], lo[2 * pp], lo[2 * pp + 1], hi[2 * pp], hi[2 * pp + 1], bs0, bs1);
     }
   }
 }
@@ -338,7 +327,6 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                      const __grid_constant__ CUtensorMap tm_kp, const __grid_constant__ CUtensorMap tm_vp,
                      const DecodeArgs a) {
   using G = Geo<BITS>;
-  constexpr int C = G::CENTER;
   constexpr int NSTAGE = G::NSTAGE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -479,14 +467,20 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     ntiles = (npk + T - 1) / T;
     row0 = (int)(bh * a.cap + i0);
     __syncthreads();  // qsum_s ready
+    const float kq24 = kq * kTwo24;  // scores come out of the fix-up times 2^-24
 
     float m_ref = -INFINITY;  // running max of query t, log2 units
-    float oc[NG][2][4];       // O^T accumulators: [group][m-tile][frag]
+    float oc[2][4][4];        // O^T accumulators (layout at pv_subtile), times 2^-24
     float mnacc[4];           // C-fragment of the min/scale/l MMA
+    float sb[2][4];           // column sums of the rounded p * scale (pv_subtile)
 #pragma unroll
-    for (int x = 0; x < NG; ++x)
+    for (int c = 0; c < 2; ++c)
 #pragma unroll
-      for (int m = 0; m < 2; ++m)
+      for (int r = 0; r < 4; ++r) sb[c][r] = 0.f;
+#pragma unroll
+    for (int x = 0; x < 2; ++x)
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
 #pragma unroll
         for (int r = 0; r < 4; ++r) oc[x][m][r] = 0.f;
 #pragma unroll
@@ -495,11 +489,12 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     // q as B fragments of the K-side MMA.  Column n = 2 * query + group bit:
     // even columns take the pair's first group, odd ones its second, so the
     // accumulator a thread holds (columns 2t, 2t+1) is query t for both groups.
-    // bq[P][s][0] covers k rows 2t, 2t+1 and bq[P][s][1] rows 2t+8, 2t+9.
+    // bq[P][s][0] covers k rows 2t, 2t+1 and bq[P][s][1] rows 2t+8, 2t+9, each
+    // divided by the weight of the code position it meets.
     uint32_t bq[2][4][2];
-    float qs_t[NG];  // query t: group sums of q
+    float qs_t[NG];  // query t: group sums of q, times 2^-24 like the accumulators
 #pragma unroll
-    for (int x = 0; x < NG; ++x) qs_t[x] = qsum_s[t][x];
+    for (int x = 0; x < NG; ++x) qs_t[x] = qsum_s[t][x] * (1.f / kTwo24);
     {
       const int qi = g >> 1;
 #pragma unroll
@@ -510,15 +505,17 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             // k rows 2t, 2t+1 <- group P, d = 8t + st (+4); 2t+8, 2t+9 <- group P+2
             const int da = 32 * P + 8 * t + st;
             const int db = 32 * (P + 2) + 8 * t + st;
-            bq[P][st][0] = (g & 1) == 0 ? ptx::pack_h2(q_s[qi][da], q_s[qi][da + 4]) : 0u;
-            bq[P][st][1] = (g & 1) == 1 ? ptx::pack_h2(q_s[qi][db], q_s[qi][db + 4]) : 0u;
+            const float iw = 1.f / w4_weight(st);
+            bq[P][st][0] = (g & 1) == 0 ? ptx::pack_h2(q_s[qi][da] * iw, q_s[qi][da + 4] * iw) : 0u;
+            bq[P][st][1] = (g & 1) == 1 ? ptx::pack_h2(q_s[qi][db] * iw, q_s[qi][db + 4] * iw) : 0u;
           } else {
             // thread t's codes: d = 64P + 16t + j, group 2P + (t >> 1); k rows
             // 2t, 2t+1 <- j = 2st, 2st+8; 2t+8, 2t+9 <- j = 2st+1, 2st+9
             const bool nz = (g & 1) == (t >> 1);
             const int d0 = 64 * P + 16 * t + 2 * st;
-            bq[P][st][0] = nz ? ptx::pack_h2(q_s[qi][d0], q_s[qi][d0 + 8]) : 0u;
-            bq[P][st][1] = nz ? ptx::pack_h2(q_s[qi][d0 + 1], q_s[qi][d0 + 9]) : 0u;
+            const float iw0 = 1.f / w2_weight(2 * st), iw1 = 1.f / w2_weight(2 * st + 1);
+            bq[P][st][0] = nz ? ptx::pack_h2(q_s[qi][d0] * iw0, q_s[qi][d0 + 8] * iw0) : 0u;
+            bq[P][st][1] = nz ? ptx::pack_h2(q_s[qi][d0 + 1] * iw1, q_s[qi][d0 + 9] * iw1) : 0u;
           }
         }
       }
@@ -554,8 +551,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 #pragma unroll
         for (int u = 0; u < NSUB; ++u) qk_subtile<BITS>(kc, wrow + 16 * u, lane, bq, acc[u]);
 
-        // fix-up, fp32: acc_g = sum (c - C) q, so s = sum_g scale_g acc_g +
-        // (min_g + C scale_g) qsum_g for query t; rows past the split end masked
+        // fix-up, fp32: acc_g = 2^-24 sum c q, so 2^-24 s = sum_g scale_g acc_g +
+        // min_g (2^-24 qsum_g) for query t; rows past the split end masked
         float sv[NSUB][2];  // [sub-tile][row g / g+8]
 #pragma unroll
         for (int u = 0; u < NSUB; ++u) {
@@ -573,8 +570,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
               acc_s = fmaf(half_lo(prm[gb]), acc[u][P][2 * rr + 1], acc_s);
             }
 #pragma unroll
-            for (int x = 0; x < NG; ++x)
-              acc_s = fmaf(fmaf((float)C, half_lo(prm[x]), half_hi(prm[x])), qs_t[x], acc_s);
+            for (int x = 0; x < NG; ++x) acc_s = fmaf(half_hi(prm[x]), qs_t[x], acc_s);
             sv[u][rr] = (16 * u + g + 8 * rr < nvalid) ? acc_s : -INFINITY;
           }
         }
@@ -584,44 +580,40 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float mloc = mx * kq;
+        const float mloc = mx * kq24;
         const bool need = mloc > m_ref + 8.f;
         if (__any_sync(0xffffffffu, need)) {
           const float mnew = need ? mloc : m_ref;
           const float al = need ? exp2f(m_ref - mnew) : 1.f;
           m_ref = mnew;
-          // this thread's O columns are queries 2t and 2t+1: their factors live
-          // in lanes whose t is 2t and 2t+1
-          const float al0 = __shfl_sync(0xffffffffu, al, (lane & ~3) | ((2 * t) & 3));
-          const float al1 = __shfl_sync(0xffffffffu, al, (lane & ~3) | ((2 * t + 1) & 3));
+          // every O accumulator of this thread is query t
 #pragma unroll
-          for (int x = 0; x < NG; ++x)
+          for (int x = 0; x < 2; ++x)
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
-              oc[x][m][0] *= al0;
-              oc[x][m][1] *= al1;
-              oc[x][m][2] *= al0;
-              oc[x][m][3] *= al1;
-            }
-          mnacc[0] *= al0;
-          mnacc[1] *= al1;
-          mnacc[2] *= al0;
-          mnacc[3] *= al1;
+            for (int m = 0; m < 4; ++m)
+#pragma unroll
+              for (int r = 0; r < 4; ++r) oc[x][m][r] *= al;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            mnacc[r] *= al;
+            sb[0][r] *= al;
+            sb[1][r] *= al;
+          }
         }
         const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-        // p as the PV B fragment: thread (g, t) needs p(query g, tokens 2t, 2t+1,
-        // 2t+8, 2t+9); lane (token % 8) * 4 + g holds query g for rows token and token + 8
-        const int srcA = (2 * t) * 4 + (g & 3);
-        const int srcB = (2 * t + 1) * 4 + (g & 3);
-        const bool qreal = g < 4;
+        // p as the PV B fragment: thread (g, t) needs p(query g / 2, tokens 2t,
+        // 2t+1, 2t+8, 2t+9); lane 4 * token + query holds that query for rows
+        // token and token + 8 of the sub-tile
+        const int srcA = (2 * t) * 4 + (g >> 1);
+        const int srcB = (2 * t + 1) * 4 + (g >> 1);
 #pragma unroll
         for (int u = 0; u < NSUB; ++u) {
-          const uint32_t pk = ptx::pack_h2(exp2f(fmaf(sv[u][0], kq, -mu)), exp2f(fmaf(sv[u][1], kq, -mu)));
+          const uint32_t pk = ptx::pack_h2(exp2f(fmaf(sv[u][0], kq24, -mu)), exp2f(fmaf(sv[u][1], kq24, -mu)));
           const uint32_t x0 = __shfl_sync(0xffffffffu, pk, srcA);  // (p(2t), p(2t+8))
           const uint32_t x1 = __shfl_sync(0xffffffffu, pk, srcB);  // (p(2t+1), p(2t+9))
-          const uint32_t pb0 = qreal ? ptx::prmt(x0, x1, 0x5410u) : 0u;  // tokens 2t, 2t+1
-          const uint32_t pb1 = qreal ? ptx::prmt(x0, x1, 0x7632u) : 0u;  // tokens 2t+8, 2t+9
-          pv_subtile<BITS>(vc, vp, wrow + 16 * u, lane, pb0, pb1, oc, mnacc);
+          const uint32_t pb0 = ptx::prmt(x0, x1, 0x5410u);  // tokens 2t, 2t+1
+          const uint32_t pb1 = ptx::prmt(x0, x1, 0x7632u);  // tokens 2t+8, 2t+9
+          pv_subtile<BITS>(vc, vp, wrow + 16 * u, lane, pb0, pb1, oc, sb, mnacc);
         }
       }
       __syncwarp();
@@ -649,34 +641,36 @@ __global__ void __launch_bounds__(NTHREADS, 2)
           ptx::mbar_wait_bounded(ptx::smem_u32(&full_bar[st]), (s_last_tile[st] / NSTAGE) & 1);
     }
     __syncthreads();  // the stage ring is idle from here on: reuse it for the merge
-    // min/scale/l rows to shared memory first, then the full outputs
-    ms.mn[warp][g][2 * t] = mnacc[0];
-    ms.mn[warp][g][2 * t + 1] = mnacc[1];
+    // per group x and query t, corr_x = sum p min_x + mid (sum p scale_x -
+    // sum of the rounded p * scale_x), to shared memory first; then the outputs
+    // O = 2^24 oc / weight + corr (the layout is at pv_subtile)
+    {
+      const float psc = __shfl_down_sync(0xffffffffu, mnacc[0], 16);  // lane g + 4: sum p scale_g
+      const float sbx = (g & 2) ? ((g & 1) ? sb[1][1] : sb[1][0]) : ((g & 1) ? sb[0][1] : sb[0][0]);
+      if (g < 4) ms.mn[warp][g][t] = fmaf(G::CENTER, psc - sbx, mnacc[0]);
+    }
     if (g == 0) {
-      ms.mn[warp][8][2 * t] = mnacc[2];
-      ms.mn[warp][8][2 * t + 1] = mnacc[3];
+      ms.l[warp][t] = mnacc[2];
       ms.m[warp][t] = m_ref;
     }
     __syncwarp();
-    if (t < 2) {
 #pragma unroll
-      for (int x = 0; x < NG; ++x)
+    for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int m = 0; m < 2; ++m)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int qi = 2 * t + (r & 1);
-            const int jrow = (r >> 1);  // 0: row g, 1: row g+8
-            int dd;
-            if (BITS == 4) {
-              dd = 32 * x + 4 * g + 2 * m + jrow;
-            } else {
-              dd = 32 * x + 8 * (g & 3) + 4 * (g >> 2) + 2 * m + jrow;
-            }
-            ms.o[warp][qi][dd] = oc[x][m][r] + ms.mn[warp][x][qi] + (float)C * ms.mn[warp][4 + x][qi];
-          }
-    }
-    if (lane < QB) ms.l[warp][lane] = ms.mn[warp][8][lane];
+      for (int j = 0; j < 4; ++j) {
+        if (BITS == 4) {
+          const float f = kTwo24 / w4_weight(j);
+          const int d0 = 64 * c + 4 * g + j;
+          ms.o[warp][t][d0] = fmaf(oc[c][j][0], f, ms.mn[warp][2 * c][t]);
+          ms.o[warp][t][d0 + 32] = fmaf(oc[c][j][3], f, ms.mn[warp][2 * c + 1][t]);
+        } else {
+          const int hb = g >> 2;
+          const float mnv = ms.mn[warp][2 * c + hb][t];
+          const int d0 = 64 * c + 8 * g + 2 * j;
+          ms.o[warp][t][d0] = fmaf(hb ? oc[c][j][1] : oc[c][j][0], kTwo24 / w2_weight(2 * j), mnv);
+          ms.o[warp][t][d0 + 1] = fmaf(hb ? oc[c][j][3] : oc[c][j][2], kTwo24 / w2_weight(2 * j + 1), mnv);
+        }
+      }
   }
 
   // ---------------- merge the four warps' states and write this split's partial

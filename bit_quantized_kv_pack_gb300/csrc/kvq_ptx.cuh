@@ -99,10 +99,12 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, u
                : "r"(addr));
 }
 
-// D = A (16x16 f16, row) * B (16x8 f16, col) + C, fp32 accumulate.
+// D = A (16x16 f16, row) * B (16x8 f16, col) + C, fp32 accumulate.  A pure
+// register operation, so not volatile: the compiler may interleave
+// independent accumulator chains.
 __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
       " {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
