@@ -3,15 +3,17 @@
 
 Workload (default): the Llama-3.1-8B-shaped INT4 32K decode layer -- B1, Hq32,
 Hkv8, d128, 32640 packed tokens + a 128-token fp16 residual window, group 32.
-A step is one pass of the whole decode hot path: kvq_append of the step's new
-K/V token (the residual window is full, so its oldest token is quantized and
-packed) followed by kvq_decode_attention of the step's 32 query heads.
+A step is one pass of the whole decode hot path, one kvq_decode_step call: the
+append of the step's new K/V token (the residual window is full, so its oldest
+token is quantized and packed) and decode attention of the step's 32 query
+heads over the updated cache -- one kernel launch on the tensor-core path.
 
 Timing: the steps are captured in a CUDA graph and replayed; the step rotates
 over copies of the cache whose total size is at least 3x the L2 cache, so the
 packed cache streams from HBM.  value = packed code + scale bytes per step
-(K and V, all heads, the tokens the decode reads) / step time.  The decode
-kernels alone are timed the same way in a decode-only graph for the roofline.
+(K and V, all heads, the tokens the decode reads) / step time.  The roofline is
+that of the step kernel; kvq_decode_attention alone is timed the same way in a
+decode-only graph and reported beside it.
 
 Output: one JSON line (see --help).  --impl reference times the CPU oracle
 (the plain fp64 implementation) on a bounded sample of the same workload.
@@ -37,7 +39,7 @@ import torch  # noqa: E402
 WORKLOAD = 2
 FALLBACK_HBM_GBS = 6800.0
 DECODE_SOURCES = ("kvq_decode.cu", "kvq_decode_generic.cu", "kvq_decode_common.cuh",
-                  "kvq_decode_tc.cu", "kvq_ptx.cuh")
+                  "kvq_decode_tc.cu", "kvq_ptx.cuh", "kvq_internal.cuh")
 
 
 # ----------------------------------------------------------------- helpers --
@@ -87,10 +89,11 @@ def decode_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload_name: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current decode sources (else None)."""
-    p = os.path.join(ROOT, "profiles", f"decode_{workload_name}.md")
+def profiled_traffic(workload_name: str, fused: bool = True):
+    """DRAM bytes per launch of the roofline kernel from the committed ncu
+    summary, if it was taken on the current decode sources (else None)."""
+    kind = "decode_step" if fused else "decode"
+    p = os.path.join(ROOT, "profiles", f"{kind}_{workload_name}.md")
     if not os.path.exists(p):
         return None
     src_hash, traffic = None, None
@@ -222,9 +225,12 @@ def capture(state, with_append=True, with_decode=True, ncopies=None):
     with torch.cuda.stream(s):
         with torch.cuda.graph(g, stream=s):
             for i, c in enumerate(state["copies"][:n]):
-                if with_append:
+                if with_append and with_decode:  # one fused launch: append, then attend
+                    kvq.kvq_decode_step(c, state["q"][i], state["kn"][i], state["vn"][i],
+                                        state["out"][i], state["ws"])
+                elif with_append:
                     kvq.kvq_append(c, state["kn"][i], state["vn"][i])
-                if with_decode:
+                else:
                     kvq.kvq_decode_attention(c, state["q"][i], state["out"][i], state["ws"])
     torch.cuda.current_stream().wait_stream(s)
     return g
@@ -290,11 +296,20 @@ def run_ours(args, rank, world, local):
     value = step_bytes / (ms_per_step * 1e-3) / 1e9
 
     dec_ms_per_launch = ms_dec / K
-    achieved = step_bytes / (dec_ms_per_launch * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
+    # the step is one fused launch on the tensor-core path (append + decode),
+    # else an append and a decode launch
+    fused = w.head_dim == 128 and 1 <= w.num_q_heads // w.num_kv_heads <= 4
+    launches = 1 if fused else 2
+    if fused:  # the dominant kernel is the step kernel itself
+        rf_kernel, rf_us = "decode_step (append + split-KV decode + combine, one launch)", ms_per_step * 1e3
+    else:
+        rf_kernel, rf_us = "decode (split-KV + combine)", dec_ms_per_launch * 1e3
+    achieved = step_bytes / (rf_us * 1e-6) / 1e9
+    dec_achieved = step_bytes / (dec_ms_per_launch * 1e-3) / 1e9
 
     # end to end through the public binding: pinned host inputs -> device,
-    # append + decode, output -> pinned host, eager calls (no graph)
+    # the step call, output -> pinned host, eager calls (no graph)
     e2e = run_e2e(st, args)
 
     clocks = clk.summary()
@@ -304,7 +319,6 @@ def run_ours(args, rank, world, local):
     else:
         ms_step_all, value_all = ms_per_step, value
 
-    plan_kernels = 2  # append, then split-KV decode with its combine fused in
     res = {
         "metric": "quantized-KV decode attention: achieved HBM GB/s (% of peak), us/step",
         "value": round(value_all, 2),
@@ -322,17 +336,20 @@ def run_ours(args, rank, world, local):
         "config": {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "bits": w.bits,
                    "packed_tokens_per_head": st["npk0"], "residual": w.residual, "group": 32,
-                   "step": "append + decode_attention",
+                   "step": "kvq_decode_step: append + decode attention",
                    "l2": f"rotating {ncopy} cache copies ({ncopy * step_bytes / 2**20:.0f} MiB "
                          f"packed) > 3x L2 ({l2 / 2**20:.0f} MiB)",
                    "timing": "CUDA graph replays, CUDA events", "parallelism": "replicas"},
-        "gpu_launches": plan_kernels * K,
-        "roofline": {"bound": "hbm", "kernel": "decode (split-KV + combine)",
+        "gpu_launches": launches * K,
+        "roofline": {"bound": "hbm", "kernel": rf_kernel,
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": profiled_traffic(w.name),
+                     "traffic": profiled_traffic(w.name, fused),
                      "algorithmic_bytes_per_launch": step_bytes,
-                     "us_per_launch": round(dec_ms_per_launch * 1e3, 3)},
+                     "us_per_launch": round(rf_us, 3)},
+        "decode_only": {"us_per_launch": round(dec_ms_per_launch * 1e3, 3),
+                        "achieved": round(dec_achieved, 2), "frac": round(dec_achieved / peak, 4),
+                        "how": "kvq_decode_attention alone, same copies, same timing"},
         "e2e": e2e,
         "clocks": clocks,
     }
@@ -360,9 +377,7 @@ def run_e2e(st, args):
         q_d.copy_(q_h[j], non_blocking=True)
         kn_d.copy_(kn_h[j], non_blocking=True)
         vn_d.copy_(vn_h[j], non_blocking=True)
-        c = st["copies"][j]
-        kvq.kvq_append(c, kn_d, vn_d)
-        kvq.kvq_decode_attention(c, q_d, out_d, st["ws"])
+        kvq.kvq_decode_step(st["copies"][j], q_d, kn_d, vn_d, out_d, st["ws"])
         out_h[j].copy_(out_d, non_blocking=True)
 
     for i in range(n):
@@ -381,7 +396,7 @@ def run_e2e(st, args):
             "us_per_step": round(ms * 1e3, 3),
             "h2d_bytes_per_step": int(q_d.numel() * 2 + kn_d.numel() * 2 + vn_d.numel() * 2),
             "d2h_bytes_per_step": int(out_d.numel() * 2),
-            "how": "eager ctypes calls per step: pinned H2D of q/k_new/v_new, append, decode, D2H of out"}
+            "how": "eager calls per step: pinned H2D of q/k_new/v_new, kvq_decode_step, D2H of out"}
 
 
 # ---------------------------------------------------------- oracle arm -----

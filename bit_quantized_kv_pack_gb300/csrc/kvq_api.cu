@@ -58,7 +58,8 @@ size_t kvq_cache_bytes(const kvq_cache_desc* desc, int which) {
 
 size_t kvq_decode_workspace_bytes(const kvq_cache_desc* desc, int32_t num_q_heads) {
   if (check_desc(desc) != KVQ_OK || num_q_heads < 1 || num_q_heads % desc->num_kv_heads) return 0;
-  return kvq::plan_decode(*desc, num_q_heads, kvq::device_sm_count()).ws_total;
+  // the fused step's plan has at least as many splits; tickets sit at fixed offsets
+  return kvq::plan_decode(*desc, num_q_heads, kvq::device_sm_count(), true).ws_total;
 }
 
 kvq_status kvq_quantize_pack(const kvq_cache_desc* desc, const kvq_cache_view* view,
@@ -105,6 +106,30 @@ kvq_status kvq_decode_attention(const kvq_cache_desc* desc, const kvq_cache_view
   return from_cuda(kvq::launch_decode(s, p, *view, static_cast<const __half*>(q), num_q_heads,
                                       static_cast<__half*>(out), workspace,
                                       static_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_decode_step(const kvq_cache_desc* desc, const kvq_cache_view* view, const void* q,
+                           int32_t num_q_heads, const void* k_new, const void* v_new, void* out,
+                           void* workspace, size_t ws_bytes, void* stream) {
+  kvq_status st = check_desc(desc);
+  if (st != KVQ_OK) return st;
+  if ((st = check_view(*desc, view)) != KVQ_OK) return st;
+  if (!q || !out || !workspace || !k_new || !v_new || num_q_heads < 1 ||
+      num_q_heads % desc->num_kv_heads)
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 16) || !aligned(k_new, 16) ||
+      !aligned(v_new, 16))
+    return KVQ_ERR_MISALIGNED;
+  if ((int64_t)desc->batch * num_q_heads > 2147483647LL) return KVQ_ERR_UNSUPPORTED;
+  const kvq::DecodePlan p = kvq::plan_decode(*desc, num_q_heads, kvq::device_sm_count(), true);
+  if ((int64_t)desc->num_kv_heads * p.nqb > 65535) return KVQ_ERR_UNSUPPORTED;
+  if (ws_bytes < p.ws_total) return KVQ_ERR_INVALID_ARG;
+  const Dims s = kvq::dims_of(*desc);
+  return from_cuda(kvq::launch_decode(s, p, *view, static_cast<const __half*>(q), num_q_heads,
+                                      static_cast<__half*>(out), workspace,
+                                      static_cast<cudaStream_t>(stream),
+                                      static_cast<const __half*>(k_new),
+                                      static_cast<const __half*>(v_new)));
 }
 
 kvq_status kvq_read_error(const kvq_cache_view* view, uint32_t* word_out, void* stream) {

@@ -26,7 +26,7 @@ int device_sm_count() {
   return n;
 }
 
-DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count) {
+DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count, bool step) {
   DecodePlan p;
   p.gq = num_q_heads / D.num_kv_heads;
   int64_t target, min_tokens;
@@ -56,23 +56,27 @@ DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count) {
   p.splits = (int)S;
   p.splits_packed = p.splits;
   if (p.kernel == 1) {
-    // the fp16 residual tokens get splits of their own, one per 128 tokens of the window
-    const int sr = (D.residual + 127) / 128;
+    // the fp16 residual tokens get splits of their own, one per 128 tokens of
+    // the window (at least one in a fused step: it takes the appended token)
+    int sr = (D.residual + 127) / 128;
+    if (step && sr < 1) sr = 1;
     const int sp = (int)S - sr > 1 ? (int)S - sr : 1;
     p.splits_packed = sp;
     p.splits = sp + sr;
   }
   const int64_t nparts = units * p.splits * p.qb;
-  p.ws_partials = (size_t)nparts * D.head_dim * sizeof(float);
-  p.ws_ml_off = (p.ws_partials + 255) & ~(size_t)255;
-  p.ws_cnt_off = (p.ws_ml_off + (size_t)nparts * sizeof(float2) + 255) & ~(size_t)255;
-  p.ws_total = p.ws_cnt_off + (size_t)units * sizeof(uint32_t);
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  p.ws_cnt_off = 0;
+  p.ws_seq_off = up((size_t)units * sizeof(uint32_t));
+  p.ws_ml_off = up(p.ws_seq_off + (size_t)D.batch * sizeof(uint32_t));
+  p.ws_part_off = up(p.ws_ml_off + (size_t)nparts * sizeof(float2));
+  p.ws_total = p.ws_part_off + (size_t)nparts * D.head_dim * sizeof(float);
   return p;
 }
 
 cudaError_t launch_decode(const Dims& s, const DecodePlan& p, const kvq_cache_view& v,
                           const __half* q, int Hq, __half* out, void* workspace,
-                          cudaStream_t st) {
+                          cudaStream_t st, const __half* k_new, const __half* v_new) {
   DecodeArgs a;
   a.k_codes = v.k_codes;
   a.v_codes = v.v_codes;
@@ -86,9 +90,23 @@ cudaError_t launch_decode(const Dims& s, const DecodePlan& p, const kvq_cache_vi
   a.err_word = v.err_word;
   a.q = q;
   a.out = out;
-  a.o_part = reinterpret_cast<float*>(workspace);
-  a.ml_part = reinterpret_cast<float2*>(reinterpret_cast<char*>(workspace) + p.ws_ml_off);
-  a.counters = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(workspace) + p.ws_cnt_off);
+  char* ws = reinterpret_cast<char*>(workspace);
+  a.o_part = reinterpret_cast<float*>(ws + p.ws_part_off);
+  a.ml_part = reinterpret_cast<float2*>(ws + p.ws_ml_off);
+  a.counters = reinterpret_cast<uint32_t*>(ws + p.ws_cnt_off);
+  a.seq_tickets = reinterpret_cast<uint32_t*>(ws + p.ws_seq_off);
+  // the fused step (tensor-core kernel only) writes the cache
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.w_codes[0] = v.k_codes;
+  a.w_codes[1] = v.v_codes;
+  a.w_params[0] = v.k_params;
+  a.w_params[1] = v.v_params;
+  a.w_res[0] = reinterpret_cast<__half*>(v.k_res);
+  a.w_res[1] = reinterpret_cast<__half*>(v.v_res);
+  a.w_packed_len = v.packed_len;
+  a.w_res_len = v.res_len;
+  a.w_res_head = v.res_head;
   a.Hkv = s.Hkv;
   a.Hq = Hq;
   a.gq = p.gq;
@@ -99,8 +117,14 @@ cudaError_t launch_decode(const Dims& s, const DecodePlan& p, const kvq_cache_vi
   a.cap = s.cap;
   a.Nr = s.Nr;
   a.d = s.d;
+  a.row_bytes = s.row_bytes;
   a.qk_scale_log2 = (float)(1.4426950408889634 / sqrt((double)s.d));
-  return p.kernel == 1 ? launch_decode_tc(s, p, a, st) : launch_decode_generic(s, p, a, st);
+  const bool step = k_new != nullptr;
+  if (p.kernel == 1) return launch_decode_tc(s, p, a, st, step);
+  cudaError_t e = cudaSuccess;
+  if (step) e = launch_append(s, v, k_new, v_new, st);  // generic path: two launches
+  if (e != cudaSuccess) return e;
+  return launch_decode_generic(s, p, a, st);
 }
 
 }  // namespace kvq

@@ -25,8 +25,18 @@ struct DecodeArgs {
   __half* out;      // [B][Hq][d]
   float* o_part;
   float2* ml_part;
-  uint32_t* counters;  // [B][Hkv][nqb] arrival tickets, zero between calls
-  int Hkv, Hq, gq, qb, nqb, S, cap, Nr, d;
+  uint32_t* counters;     // [B][Hkv][nqb] arrival tickets, zero between calls
+  uint32_t* seq_tickets;  // [B] fused step: units of the sequence done, zero between calls
+  // fused step (append, then attend): the new token and the cache as writable
+  const __half* k_new;  // [B][Hkv][d]
+  const __half* v_new;
+  uint8_t* w_codes[2];
+  uint32_t* w_params[2];
+  __half* w_res[2];
+  int32_t* w_packed_len;
+  int32_t* w_res_len;
+  int32_t* w_res_head;
+  int Hkv, Hq, gq, qb, nqb, S, cap, Nr, d, row_bytes;
   int Sp;  // tensor-core kernel: splits s < Sp take packed tokens, s >= Sp residual ones
   float qk_scale_log2;  // log2(e) / sqrt(d)
 };
@@ -71,7 +81,7 @@ __device__ __forceinline__ void split_range(int Lp, int Lr, int s, int S, int64_
 bool tc_supported(const kvq_cache_desc& D, int gq);
 int tc_threads();
 cudaError_t launch_decode_tc(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
-                             cudaStream_t st);
+                             cudaStream_t st, bool step);
 
 // ------------------------------------------------ last-CTA combine ---------
 //

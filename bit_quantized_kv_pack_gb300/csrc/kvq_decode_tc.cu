@@ -80,10 +80,13 @@ struct MergeSmem {
   float mn[NCW][9][8];
 };
 
+// The merge scratch, then the fused step's extra tokens [2][2][D] fp32, overlap
+// the stage ring once it is idle (residual splits never use the ring).
 template <int BITS>
 constexpr size_t tc_smem_bytes() {
   constexpr size_t ring = (size_t)Geo<BITS>::NSTAGE * Geo<BITS>::STAGE;
-  return 1024 + (ring > sizeof(MergeSmem) ? ring : sizeof(MergeSmem));
+  constexpr size_t merge = sizeof(MergeSmem) + 4 * D * sizeof(float);
+  return 1024 + (ring > merge ? ring : merge);
 }
 
 // ------------------------------------------------------- code conversion ---
@@ -321,7 +324,17 @@ __device__ __forceinline__ void residual_tokens(const DecodeArgs& a, int64_t bh,
 // Grid (S, Hkv, B): split s < Sp streams packed tokens of (sequence b, KV head h)
 // on the tensor cores; splits s >= Sp take the fp16 residual tokens.  Every
 // split writes a partial (o, m, l); the last one of the head merges them.
-template <int BITS>
+//
+// STEP: the same launch first appends one token per (sequence, KV head), as
+// kvq_append does, and attends over the cache as it is after the append.  The
+// packed splits only read rows that existed before the step.  The last residual
+// split of each head does the append's writes: it quantizes the token that
+// leaves the window (or, with no window, the new token) into packed slot
+// packed_len with the pack kernel's quantizer, stores the new token in its ring
+// slot, and attends over the window without the leaving token plus the new token
+// (fp16) and the quantized one (dequantized in fp32).  The last head of a
+// sequence to finish commits the counters.
+template <int BITS, bool STEP>
 __global__ void __launch_bounds__(NTHREADS, 2)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
                      const __grid_constant__ CUtensorMap tm_kp, const __grid_constant__ CUtensorMap tm_vp,
@@ -336,7 +349,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   __shared__ int s_last_tile[NSTAGE];  // last tile issued into each stage (-1: none)
   __shared__ float q_s[QB][D];
   __shared__ float qsum_s[QB][NG];  // sum of q over each group
-  __shared__ int s_rng[3];
+  __shared__ int s_rng[6];  // range lo, hi, ring head, step flags, packed_len, res_len
   __shared__ volatile int s_abort;
   __shared__ int s_last;
 
@@ -392,19 +405,32 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   if (threadIdx.x == 0) {
     const int Lp = a.packed_len[b];
     const int Lr = a.res_len[b];
-    int r0_, r1_;
+    // fused step: the append packs a token when the window is full (or absent),
+    // and changes nothing when that would overflow the packed capacity
+    const bool pack_now = a.Nr == 0 || Lr == a.Nr;
+    const bool full = STEP && pack_now && Lp >= a.cap;
+    const bool adds = STEP && !full;
+    int r0_, r1_, xflags = 0;
     if (!res_cta) {
       r0_ = (int)((int64_t)Lp * s / a.Sp);
       r1_ = (int)((int64_t)Lp * (s + 1) / a.Sp);
     } else {
       const int Sr = a.S - a.Sp, sr = s - a.Sp;
-      r0_ = (int)((int64_t)Lr * sr / Sr);
-      r1_ = (int)((int64_t)Lr * (sr + 1) / Sr);
+      // window tokens [jlo, Lr) in age order; a flushed oldest token leaves it
+      const int jlo = (adds && a.Nr > 0 && pack_now) ? 1 : 0;
+      r0_ = jlo + (int)((int64_t)(Lr - jlo) * sr / Sr);
+      r1_ = jlo + (int)((int64_t)(Lr - jlo) * (sr + 1) / Sr);
+      // bit 0: the new token joins the window; bit 1: a token is packed into slot Lp
+      if (adds && sr == Sr - 1) xflags = (a.Nr > 0 ? 1 : 0) | (pack_now ? 2 : 0);
     }
     s_rng[0] = r0_;
     s_rng[1] = r1_;
     s_rng[2] = a.res_head[b];
-    if (s == 0 && Lp + Lr == 0) set_error(a.err_word, KVQ_ERRBIT_EMPTY);
+    s_rng[3] = xflags;
+    s_rng[4] = Lp;
+    s_rng[5] = Lr;
+    if (s == 0 && Lp + Lr == 0 && !adds) set_error(a.err_word, KVQ_ERRBIT_EMPTY);
+    if (full && s == 0 && h == 0) set_error(a.err_word, KVQ_ERRBIT_CAPACITY);
     if (!res_cta) {
       i0 = r0_;
       i1 = r1_;
@@ -426,6 +452,53 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   const float kq = a.qk_scale_log2;
   MergeSmem& ms = *reinterpret_cast<MergeSmem*>(smem);
 
+  // extra tokens of a fused step, fp32: [K, V][new token, packed token][D]
+  float* xbuf = reinterpret_cast<float*>(smem + sizeof(MergeSmem));
+  if (STEP && res_cta && s_rng[3] != 0 && warp < 2) {
+    // the append's writes for this (sequence, KV head): warp 0 the K row, warp
+    // 1 the V row, lane l < 16 holding values 8l .. 8l+7 (as in kvq_append)
+    const int which = warp;
+    const int xflags = s_rng[3], rh = s_rng[2], Lp = s_rng[4], Lr = s_rng[5];
+    const bool active = lane < D / 8;
+    uint4 nv = make_uint4(0, 0, 0, 0);
+    if (active)
+      nv = __ldg(reinterpret_cast<const uint4*>((which ? a.v_new : a.k_new) + bh * D) + lane);
+    float* xb = xbuf + which * 2 * D;
+    if (xflags & 2) {
+      // the oldest window token (or, with no window, the new one) -> slot Lp
+      uint4 src = nv;
+      if (a.Nr > 0 && active)
+        src = *reinterpret_cast<const uint4*>(a.w_res[which] + (bh * a.Nr + rh) * D + lane * 8);
+      float x[8];
+      unpack8_f16(src, x);
+      uint32_t prm;
+      const uint32_t packed = quantize_quad<BITS>(x, prm);
+      if (active) {
+        const int64_t row = bh * a.cap + Lp;
+        const int gi = lane >> 2, quad = lane & 3;
+        uint8_t* dst = a.w_codes[which] + row * a.row_bytes + gi * (4 * BITS) + quad * BITS;
+        if (BITS == 4)
+          *reinterpret_cast<uint32_t*>(dst) = packed;
+        else
+          *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
+        if (quad == 0) a.w_params[which][row * NG + gi] = prm;
+        const float sc = half_lo(prm), mn = half_hi(prm);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          xb[D + lane * 8 + j] = fmaf((float)((packed >> (BITS * j)) & ((1u << BITS) - 1u)), sc, mn);
+      }
+    }
+    if ((xflags & 1) && active) {
+      // the new token takes the leaving token's slot, or the next free one
+      float x[8];
+      unpack8_f16(nv, x);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) xb[lane * 8 + j] = x[j];
+      const int slot = (xflags & 2) ? rh : (rh + Lr) % a.Nr;
+      *reinterpret_cast<uint4*>(a.w_res[which] + (bh * a.Nr + slot) * D + lane * 8) = nv;
+    }
+  }
+
   if (res_cta) {
     // ------------------------------------------------ residual-token split
     float rm[QB], rl[QB], ro[QB][4];
@@ -437,6 +510,36 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       for (int j = 0; j < 4; ++j) ro[i][j] = 0.f;
     }
     residual_tokens(a, bh, s_rng[2], s_rng[0], s_rng[1], warp, lane, q_s, kq, rm, rl, ro);
+    if (STEP) {
+      __syncthreads();  // the extra tokens are in shared memory
+      const int xflags = s_rng[3];
+      if (xflags != 0 && warp == 0) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          if (!(xflags & (1 << e))) continue;
+          float kx[4], vx[4];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            kx[jj] = xbuf[e * D + lane * 4 + jj];
+            vx[jj] = xbuf[2 * D + e * D + lane * 4 + jj];
+          }
+#pragma unroll
+          for (int i = 0; i < QB; ++i) {
+            float part = 0.f;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) part = fmaf(kx[jj], q_s[i][lane * 4 + jj], part);
+            const float v = warp_sum(part) * kq;
+            const float mnew = fmaxf(rm[i], v);
+            const float al = exp2f(rm[i] - mnew);
+            const float pe = exp2f(v - mnew);
+            rl[i] = fmaf(rl[i], al, pe);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) ro[i][jj] = fmaf(pe, vx[jj], ro[i][jj] * al);
+            rm[i] = mnew;
+          }
+        }
+      }
+    }
     if (lane == 0) {
 #pragma unroll
       for (int i = 0; i < QB; ++i) {
@@ -696,8 +799,25 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     if (e == 0) a.ml_part[pidx * QB + i] = make_float2(M, lsum);
   }
   // the last split of this KV head to finish merges all S partials
-  if (take_last_ticket<NTHREADS>(a, bh, &s_last))
+  if (take_last_ticket<NTHREADS>(a, bh, &s_last)) {
     combine_unit<NTHREADS, D, 40>(a, b, h, 0, reinterpret_cast<float*>(smem));
+    if (STEP && threadIdx.x == 0) {
+      // every split of this head has read the counters; the last head of the
+      // sequence to get here commits the append's new counters
+      if (atomicInc(&a.seq_tickets[b], (unsigned)(a.Hkv - 1)) == (unsigned)(a.Hkv - 1)) {
+        const int Lp = a.w_packed_len[b], Lr = a.w_res_len[b], rh = a.w_res_head[b];
+        const bool pack_now = a.Nr == 0 || Lr == a.Nr;
+        if (!(pack_now && Lp >= a.cap)) {
+          if (pack_now) {
+            a.w_packed_len[b] = Lp + 1;
+            if (a.Nr > 0) a.w_res_head[b] = (rh + 1) % a.Nr;
+          } else {
+            a.w_res_len[b] = Lr + 1;
+          }
+        }
+      }
+    }
+  }
 }
 
 // --------------------------------------------------------- tensor maps -----
@@ -738,7 +858,7 @@ bool make_rows_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint6
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BITS>
+template <int BITS, bool STEP>
 cudaError_t launch_bits(const Dims& s, const DecodePlan& p, const DecodeArgs& a, cudaStream_t st) {
   using Gm = Geo<BITS>;
   const uint64_t rows = (uint64_t)s.B * s.Hkv * s.cap;
@@ -751,7 +871,7 @@ cudaError_t launch_bits(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
   constexpr size_t smem = tc_smem_bytes<BITS>();
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<BITS>,
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<BITS, STEP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -766,7 +886,7 @@ cudaError_t launch_bits(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<BITS>, kc, vc, kp, vp, a);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<BITS, STEP>, kc, vc, kp, vp, a);
 }
 
 }  // namespace
@@ -778,8 +898,9 @@ bool tc_supported(const kvq_cache_desc& D, int gq) {
 int tc_threads() { return NTHREADS; }
 
 cudaError_t launch_decode_tc(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
-                             cudaStream_t st) {
-  return s.bits == 4 ? launch_bits<4>(s, p, a, st) : launch_bits<2>(s, p, a, st);
+                             cudaStream_t st, bool step) {
+  if (step) return s.bits == 4 ? launch_bits<4, true>(s, p, a, st) : launch_bits<2, true>(s, p, a, st);
+  return s.bits == 4 ? launch_bits<4, false>(s, p, a, st) : launch_bits<2, false>(s, p, a, st);
 }
 
 }  // namespace kvq

@@ -108,13 +108,19 @@ struct DecodePlan {
   int splits;   // S (all splits)
   int splits_packed;  // tensor-core kernel: the first splits_packed take packed tokens
   int threads;  // threads per CTA of the split kernel
-  size_t ws_partials;  // bytes of the o partials (offset 0)
-  size_t ws_ml_off;    // offset of the {m, l} partials
-  size_t ws_cnt_off;   // offset of the per-unit arrival counters (zero between calls)
+  // Workspace layout.  The tickets sit at fixed offsets (they depend only on the
+  // cache shape and head count), so a workspace shared by calls with different
+  // split counts never has a partial land on a ticket.
+  size_t ws_cnt_off;   // 0: per-unit arrival tickets [B][Hkv][nqb] (zero between calls)
+  size_t ws_seq_off;   // per-sequence tickets [B] of the fused step (zero between calls)
+  size_t ws_ml_off;    // {m, l} partials
+  size_t ws_part_off;  // o partials
   size_t ws_total;     // bytes of the whole workspace
 };
 
-DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count);
+// step: plan for kvq_decode_step (the tensor-core kernel then always has a
+// residual split per KV head, which takes the appended token).
+DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count, bool step = false);
 int device_sm_count();
 
 // ------------------------------------------------------------- launchers ---
@@ -124,8 +130,10 @@ cudaError_t launch_quantize_pack(const Dims& s, const kvq_cache_view& v, const _
                                  cudaStream_t st);
 cudaError_t launch_append(const Dims& s, const kvq_cache_view& v, const __half* k_new,
                           const __half* v_new, cudaStream_t st);
+// k_new/v_new non-null: the fused step (append, then attend).
 cudaError_t launch_decode(const Dims& s, const DecodePlan& p, const kvq_cache_view& v,
                           const __half* q, int Hq, __half* out, void* workspace,
-                          cudaStream_t st);
+                          cudaStream_t st, const __half* k_new = nullptr,
+                          const __half* v_new = nullptr);
 
 }  // namespace kvq

@@ -39,7 +39,8 @@ KVQ_ARRAY_RESIDUAL = 2
 
 # Every function the header declares (the tests check the library exports them).
 EXPORTS = ("kvq_cache_bytes", "kvq_decode_workspace_bytes", "kvq_quantize_pack", "kvq_append",
-           "kvq_decode_attention", "kvq_read_error", "kvq_status_string", "kvq_version")
+           "kvq_decode_attention", "kvq_decode_step", "kvq_decode_attention_noalloc",
+           "kvq_read_error", "kvq_status_string", "kvq_version")
 
 
 class CacheDesc(ctypes.Structure):
@@ -89,6 +90,8 @@ def load(path: str | None = None):
             lib.kvq_append.restype = ctypes.c_int
             lib.kvq_decode_attention.argtypes = [DP, VP, P, i32, P, P, sz, P]
             lib.kvq_decode_attention.restype = ctypes.c_int
+            lib.kvq_decode_step.argtypes = [DP, VP, P, i32, P, P, P, P, sz, P]
+            lib.kvq_decode_step.restype = ctypes.c_int
             lib.kvq_decode_attention_noalloc.argtypes = [DP, VP, P, i32, P, P]
             lib.kvq_decode_attention_noalloc.restype = ctypes.c_int
             lib.kvq_read_error.argtypes = [VP, ctypes.POINTER(ctypes.c_uint32), P]
@@ -231,6 +234,26 @@ def kvq_decode_attention(cache: KVCache, q: torch.Tensor, out: torch.Tensor | No
                                      workspace.numel() * workspace.element_size(),
                                      _stream(stream, q.device))
     _check(st, "kvq_decode_attention")
+    return out
+
+
+def kvq_decode_step(cache: KVCache, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                    out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """One serving-loop step: append k_new/v_new (fp16 [B][Hkv][d]), then decode
+    attention of q over the updated cache; one kernel launch where the tensor-core
+    kernel applies."""
+    _f16(q, "q"), _f16(k_new, "k_new"), _f16(v_new, "v_new")
+    if out is None:
+        out = torch.empty_like(q)
+    _f16(out, "out")
+    if workspace is None:
+        workspace = workspace_for(cache, q.shape[1])
+    st = load().kvq_decode_step(ctypes.byref(cache.desc), ctypes.byref(cache.view), _ptr(q),
+                                int(q.shape[1]), _ptr(k_new), _ptr(v_new), _ptr(out),
+                                _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                _stream(stream, q.device))
+    _check(st, "kvq_decode_step")
     return out
 
 

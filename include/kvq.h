@@ -138,8 +138,8 @@ typedef struct {
  * Returns 0 for an invalid desc or `which`. */
 size_t kvq_cache_bytes(const kvq_cache_desc* desc, int which);
 
-/* Bytes of scratch kvq_decode_attention needs for num_q_heads query heads on the
- * current device.  Returns 0 for an invalid desc. */
+/* Bytes of scratch kvq_decode_attention and kvq_decode_step need for num_q_heads
+ * query heads on the current device.  Returns 0 for an invalid desc. */
 size_t kvq_decode_workspace_bytes(const kvq_cache_desc* desc, int32_t num_q_heads);
 
 /* Quantize and pack a prefill (Q1-Q6; BitDecoding page section 2.1 for the rule,
@@ -184,6 +184,28 @@ kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache_view* view,
 kvq_status kvq_decode_attention(const kvq_cache_desc* desc, const kvq_cache_view* view,
                                 const void* q, int32_t num_q_heads, void* out,
                                 void* workspace, size_t ws_bytes, void* stream);
+
+/* One decode step of the serving loop: kvq_append(k_new, v_new) and then
+ * kvq_decode_attention(q) over the cache as it is after the append (InnerQ page
+ * section 2.3 for the window, BitDecoding page sections 2.2-2.3 for the
+ * attention; fusing the two is this library's addition).
+ *   q, out, workspace, ws_bytes, num_q_heads  as for kvq_decode_attention (the
+ *              workspace size from kvq_decode_workspace_bytes covers this call).
+ *   k_new, v_new  fp16 device [B][Hkv][d], as for kvq_append.
+ * The cache bytes, counters and error bits afterwards are exactly those of the
+ * two calls; the output equals the two calls' within rounding (the token packed
+ * by this step is attended in fp32 from its codes rather than on the tensor
+ * cores).  With head_dim 128 and at most 4 query heads per KV head this is one
+ * kernel launch: the packed splits read only rows written before the step, the
+ * residual split of each head does the append's writes and attends over the new
+ * and the packed token, and the counters move when the last head of a sequence
+ * finishes.  Other shapes launch the append and the decode kernels in turn.  A
+ * sequence whose packed cache is full is left unchanged, sets
+ * KVQ_ERRBIT_CAPACITY and is attended as it was.  Asynchronous. */
+kvq_status kvq_decode_step(const kvq_cache_desc* desc, const kvq_cache_view* view,
+                           const void* q, int32_t num_q_heads, const void* k_new,
+                           const void* v_new, void* out, void* workspace, size_t ws_bytes,
+                           void* stream);
 
 /* Size of the device scratch array behind kvq_decode_attention_noalloc (8 MiB). */
 #define KVQ_NOALLOC_SCRATCH_BYTES (8u << 20)

@@ -1,0 +1,112 @@
+"""GPU parity of the fused decode step (kvq_decode_step = kvq_append followed by
+kvq_decode_attention in one call): after every step the cache bytes and
+counters equal those of the two separate calls and of the oracle, bit for bit,
+and the output is within max abs 2e-3 / relative L2 1e-3 of the fp64 oracle.
+The runs cross every append case: window filling, window full (a token packed
+per step, the ring head wrapping), no window at all, and a full packed cache."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_quantized_kv_pack_gb300 import kvq, synth
+
+from _util import assert_attn_close, assert_cache_equal, gpu_cache, ref_cache, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+CACHE_ARRAYS = ("k_codes", "v_codes", "k_params", "v_params", "k_res", "v_res", "counters")
+
+
+def _assert_gpu_caches_equal(a, b):
+    for name in CACHE_ARRAYS:
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+
+
+def _run_steps(rng, B, H, d, gq, bits, cap, Nr, lens, nsteps, scale=1.0):
+    """Prefill `lens`, then `nsteps` fused steps on one cache and append + decode
+    on a twin; both against the oracle after every step."""
+    Lmax = max(max(lens), 1)
+    k = torch.from_numpy((rng.standard_normal((B, H, Lmax, d)) * scale).astype(np.float16))
+    v = torch.from_numpy(rng.standard_normal((B, H, Lmax, d)).astype(np.float16))
+    seq = torch.tensor(lens, dtype=torch.int32)
+    fused, twin = gpu_cache(B, H, d, bits, cap, Nr), gpu_cache(B, H, d, bits, cap, Nr)
+    for c in (fused, twin):
+        kvq.kvq_quantize_pack(c, k.to(DEV), v.to(DEV), seq.to(DEV))
+        assert kvq.kvq_read_error(c)[0] == kvq.KVQ_OK
+    r = ref_cache(B, H, d, bits, cap, Nr)
+    assert oracle.quantize_pack(r, to_np(k), to_np(v), to_np(seq)) == 0
+    ws = kvq.workspace_for(fused, H * gq)
+    words = []
+    for _ in range(nsteps):
+        kn = torch.from_numpy((rng.standard_normal((B, H, d)) * scale).astype(np.float16))
+        vn = torch.from_numpy(rng.standard_normal((B, H, d)).astype(np.float16))
+        q = torch.from_numpy(rng.standard_normal((B, H * gq, d)).astype(np.float16))
+        out = kvq.kvq_decode_step(fused, q.to(DEV), kn.to(DEV), vn.to(DEV), workspace=ws)
+        st_f, w_f = kvq.kvq_read_error(fused)
+        kvq.kvq_append(twin, kn.to(DEV), vn.to(DEV))
+        out2 = kvq.kvq_decode_attention(twin, q.to(DEV))
+        st_t, w_t = kvq.kvq_read_error(twin)
+        err = oracle.append(r, kn.numpy(), vn.numpy())
+        assert w_f == w_t and st_f == st_t
+        words.append((w_f, err))
+        _assert_gpu_caches_equal(fused, twin)
+        assert_cache_equal(fused, r)
+        want = oracle.decode(r, q.numpy())
+        assert_attn_close(out, want)
+        assert_attn_close(out2, want)
+    return words
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+@pytest.mark.parametrize("Nr,lens", [(16, [3, 16, 40]), (0, [5, 130, 1]), (128, [700, 10, 128])])
+def test_step_tensor_core_path(bits, Nr, lens):
+    """head_dim 128, 4 query heads per KV head: one launch per step.  Nr 16 with
+    lens 3/16/40: one window fills then packs, two pack every step and wrap."""
+    rng = np.random.default_rng(bits * 100 + Nr)
+    words = _run_steps(rng, 3, 2, 128, 4, bits, 800, Nr, lens, 20, scale=2.0)
+    assert all(w == 0 and e == 0 for w, e in words)
+
+
+@pytest.mark.parametrize("d,gq", [(64, 2), (128, 8)])
+def test_step_generic_path(d, gq):
+    """Shapes the tensor-core kernel does not take: append and decode launches."""
+    rng = np.random.default_rng(d + gq)
+    words = _run_steps(rng, 2, 2, d, gq, 4, 300, 8, [20, 4], 12)
+    assert all(w == 0 and e == 0 for w, e in words)
+
+
+@pytest.mark.parametrize("Nr", [4, 0])
+def test_step_capacity_full(Nr):
+    """Sequence 0 reaches the packed capacity mid-run: from then on its cache is
+    left as it is, the capacity bit is raised, and it is still attended."""
+    rng = np.random.default_rng(31 + Nr)
+    cap = 10
+    words = _run_steps(rng, 2, 2, 128, 4, 4, cap, Nr, [cap + Nr - 2, 1], 5)
+    assert words[0] == (0, 0) and words[1] == (0, 0)
+    assert all(w == kvq.KVQ_ERRBIT_CAPACITY and e & 1 for w, e in words[2:])
+
+
+@pytest.mark.parametrize("num", [2, 3])
+def test_step_workload_full_size(num):
+    """Llama-3.1-8B layer (32K INT4, 128K INT2; 128-token window, full): three
+    fused steps, each packing the oldest window token; every output row and the
+    packed slots written against the oracle."""
+    w = synth.WORKLOADS[num]
+    k, v, lens = w.prefill(device=DEV)
+    cap = w.len_max - w.residual + 8
+    g = gpu_cache(w.batch, w.num_kv_heads, w.head_dim, w.bits, cap, w.residual)
+    kvq.kvq_quantize_pack(g, k, v, lens.to(DEV))
+    r = ref_cache(w.batch, w.num_kv_heads, w.head_dim, w.bits, cap, w.residual)
+    assert oracle.quantize_pack(r, to_np(k), to_np(v), to_np(lens)) == 0
+    del k, v
+    for step in range(3):
+        kn, vn = w.new_tokens(step)
+        q = w.query(step)
+        out = kvq.kvq_decode_step(g, q.to(DEV), kn.to(DEV), vn.to(DEV))
+        assert kvq.kvq_read_error(g)[0] == kvq.KVQ_OK
+        oracle.append(r, kn.numpy(), vn.numpy())
+        err, rel = assert_attn_close(out, oracle.decode(r, q.numpy()))
+        print(f"workload {num} step {step}: max abs {err:.2e}, rel L2 {rel:.2e}")
+    assert_cache_equal(g, r)
