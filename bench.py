@@ -226,8 +226,11 @@ def capture(state, with_append=True, with_decode=True, ncopies=None):
         with torch.cuda.graph(g, stream=s):
             for i, c in enumerate(state["copies"][:n]):
                 if with_append and with_decode:  # one fused launch: append, then attend
+                    # consecutive steps use different cache copies, so the kernel
+                    # before each step never writes its cache
                     kvq.kvq_decode_step(c, state["q"][i], state["kn"][i], state["vn"][i],
-                                        state["out"][i], state["ws"])
+                                        state["out"][i], state["ws"],
+                                        flags=kvq.KVQ_STEP_EARLY_CACHE_READ)
                 elif with_append:
                     kvq.kvq_append(c, state["kn"][i], state["vn"][i])
                 else:
@@ -377,7 +380,8 @@ def run_e2e(st, args):
         q_d.copy_(q_h[j], non_blocking=True)
         kn_d.copy_(kn_h[j], non_blocking=True)
         vn_d.copy_(vn_h[j], non_blocking=True)
-        kvq.kvq_decode_step(st["copies"][j], q_d, kn_d, vn_d, out_d, st["ws"])
+        kvq.kvq_decode_step(st["copies"][j], q_d, kn_d, vn_d, out_d, st["ws"],
+                            flags=kvq.KVQ_STEP_EARLY_CACHE_READ)
         out_h[j].copy_(out_d, non_blocking=True)
 
     for i in range(n):

@@ -110,12 +110,12 @@ kvq_status kvq_decode_attention(const kvq_cache_desc* desc, const kvq_cache_view
 
 kvq_status kvq_decode_step(const kvq_cache_desc* desc, const kvq_cache_view* view, const void* q,
                            int32_t num_q_heads, const void* k_new, const void* v_new, void* out,
-                           void* workspace, size_t ws_bytes, void* stream) {
+                           void* workspace, size_t ws_bytes, uint32_t flags, void* stream) {
   kvq_status st = check_desc(desc);
   if (st != KVQ_OK) return st;
   if ((st = check_view(*desc, view)) != KVQ_OK) return st;
   if (!q || !out || !workspace || !k_new || !v_new || num_q_heads < 1 ||
-      num_q_heads % desc->num_kv_heads)
+      num_q_heads % desc->num_kv_heads || (flags & ~(uint32_t)KVQ_STEP_EARLY_CACHE_READ))
     return KVQ_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 16) || !aligned(k_new, 16) ||
       !aligned(v_new, 16))
@@ -129,7 +129,7 @@ kvq_status kvq_decode_step(const kvq_cache_desc* desc, const kvq_cache_view* vie
                                       static_cast<__half*>(out), workspace,
                                       static_cast<cudaStream_t>(stream),
                                       static_cast<const __half*>(k_new),
-                                      static_cast<const __half*>(v_new)));
+                                      static_cast<const __half*>(v_new), flags));
 }
 
 kvq_status kvq_read_error(const kvq_cache_view* view, uint32_t* word_out, void* stream) {

@@ -76,7 +76,8 @@ DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count, b
 
 cudaError_t launch_decode(const Dims& s, const DecodePlan& p, const kvq_cache_view& v,
                           const __half* q, int Hq, __half* out, void* workspace,
-                          cudaStream_t st, const __half* k_new, const __half* v_new) {
+                          cudaStream_t st, const __half* k_new, const __half* v_new,
+                          uint32_t step_flags) {
   DecodeArgs a;
   a.k_codes = v.k_codes;
   a.v_codes = v.v_codes;
@@ -118,6 +119,7 @@ cudaError_t launch_decode(const Dims& s, const DecodePlan& p, const kvq_cache_vi
   a.Nr = s.Nr;
   a.d = s.d;
   a.row_bytes = s.row_bytes;
+  a.early = (step_flags & KVQ_STEP_EARLY_CACHE_READ) ? 1 : 0;
   a.qk_scale_log2 = (float)(1.4426950408889634 / sqrt((double)s.d));
   const bool step = k_new != nullptr;
   if (p.kernel == 1) return launch_decode_tc(s, p, a, st, step);

@@ -37,6 +37,7 @@ struct DecodeArgs {
   int32_t* w_res_len;
   int32_t* w_res_head;
   int Hkv, Hq, gq, qb, nqb, S, cap, Nr, d, row_bytes;
+  int early;  // fused step: counters and first tiles may be read before griddepcontrol.wait
   int Sp;  // tensor-core kernel: splits s < Sp take packed tokens, s >= Sp residual ones
   float qk_scale_log2;  // log2(e) / sqrt(d)
 };

@@ -380,16 +380,13 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       ptx::prefetch_tensormap(&tm_vp);
     }
   }
-  grid_dependency_wait();
+  // A launch that depends on this one programmatically (the next step) may
+  // start filling the SMs this grid frees; it waits for this grid before it
+  // touches anything this grid writes.
+  asm volatile("griddepcontrol.launch_dependents;");
 
-  // The small loads go first -- q by every thread, the lengths by thread 0 --
-  // so they are not queued behind the bulk tile copies.  QB * D / 128 = 4 halves
-  // per thread; query heads past gq (gq < 4) stay zero.
-  const int q_i = (threadIdx.x * 4) / D;
-  uint2 qraw = make_uint2(0, 0);
-  if (q_i < a.gq)
-    qraw = *reinterpret_cast<const uint2*>(a.q + ((int64_t)b * a.Hq + h * a.gq) * D + threadIdx.x * 4);
   int i0 = 0, i1 = 0, ntiles = 0, row0 = 0;
+  uint32_t err_bits = 0;
   auto issue = [&](int tile) {
     const int st = tile % NSTAGE;
     s_last_tile[st] = tile;
@@ -402,7 +399,9 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     ptx::tma_load_2d(ptx::smem_u32(base + G::KP), &tm_kp, 0, y, fb);
     ptx::tma_load_2d(ptx::smem_u32(base + G::VP), &tm_vp, 0, y, fb);
   };
-  if (threadIdx.x == 0) {
+  // Thread 0: read the counters, cut this split's range and start its first
+  // NSTAGE tiles.
+  auto plan = [&]() {
     const int Lp = a.packed_len[b];
     const int Lr = a.res_len[b];
     // fused step: the append packs a token when the window is full (or absent),
@@ -429,8 +428,8 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     s_rng[3] = xflags;
     s_rng[4] = Lp;
     s_rng[5] = Lr;
-    if (s == 0 && Lp + Lr == 0 && !adds) set_error(a.err_word, KVQ_ERRBIT_EMPTY);
-    if (full && s == 0 && h == 0) set_error(a.err_word, KVQ_ERRBIT_CAPACITY);
+    if (s == 0 && Lp + Lr == 0 && !adds) err_bits |= KVQ_ERRBIT_EMPTY;
+    if (full && s == 0 && h == 0) err_bits |= KVQ_ERRBIT_CAPACITY;
     if (!res_cta) {
       i0 = r0_;
       i1 = r1_;
@@ -438,6 +437,24 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       row0 = (int)(bh * a.cap + i0);  // first packed row of this split (TMA y)
       for (int tile = 0; tile < ntiles && tile < NSTAGE; ++tile) issue(tile);
     }
+  };
+  // With the caller's word that the kernel before this launch does not write
+  // this cache (KVQ_STEP_EARLY_CACHE_READ), the counters and the first tiles
+  // are read before waiting for that kernel; q and the new token never are.
+  const bool early = STEP && a.early != 0;
+  if (early && threadIdx.x == 0) plan();
+  grid_dependency_wait();
+
+  // The small loads go first -- q by every thread, the lengths by thread 0 --
+  // so they are not queued behind the bulk tile copies.  QB * D / 128 = 4 halves
+  // per thread; query heads past gq (gq < 4) stay zero.
+  const int q_i = (threadIdx.x * 4) / D;
+  uint2 qraw = make_uint2(0, 0);
+  if (q_i < a.gq)
+    qraw = *reinterpret_cast<const uint2*>(a.q + ((int64_t)b * a.Hq + h * a.gq) * D + threadIdx.x * 4);
+  if (threadIdx.x == 0) {
+    if (!early) plan();
+    if (err_bits) set_error(a.err_word, err_bits);
   }
   {
     const int e = (threadIdx.x * 4) % D;
@@ -800,20 +817,22 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   }
   // the last split of this KV head to finish merges all S partials
   if (take_last_ticket<NTHREADS>(a, bh, &s_last)) {
+    // Fused step: every split of this head has read the counters.  The head
+    // takes a ticket on its sequence now, so the round trip overlaps the
+    // combine; the last head of the sequence commits the append's counters,
+    // computed from the values this CTA read at its start.
+    unsigned seq_ticket = 0;
+    if (STEP && threadIdx.x == 0) seq_ticket = atomicInc(&a.seq_tickets[b], (unsigned)(a.Hkv - 1));
     combine_unit<NTHREADS, D, 40>(a, b, h, 0, reinterpret_cast<float*>(smem));
-    if (STEP && threadIdx.x == 0) {
-      // every split of this head has read the counters; the last head of the
-      // sequence to get here commits the append's new counters
-      if (atomicInc(&a.seq_tickets[b], (unsigned)(a.Hkv - 1)) == (unsigned)(a.Hkv - 1)) {
-        const int Lp = a.w_packed_len[b], Lr = a.w_res_len[b], rh = a.w_res_head[b];
-        const bool pack_now = a.Nr == 0 || Lr == a.Nr;
-        if (!(pack_now && Lp >= a.cap)) {
-          if (pack_now) {
-            a.w_packed_len[b] = Lp + 1;
-            if (a.Nr > 0) a.w_res_head[b] = (rh + 1) % a.Nr;
-          } else {
-            a.w_res_len[b] = Lr + 1;
-          }
+    if (STEP && threadIdx.x == 0 && seq_ticket == (unsigned)(a.Hkv - 1)) {
+      const int Lp = s_rng[4], Lr = s_rng[5], rh = s_rng[2];
+      const bool pack_now = a.Nr == 0 || Lr == a.Nr;
+      if (!(pack_now && Lp >= a.cap)) {
+        if (pack_now) {
+          a.w_packed_len[b] = Lp + 1;
+          if (a.Nr > 0) a.w_res_head[b] = (rh + 1) % a.Nr;
+        } else {
+          a.w_res_len[b] = Lr + 1;
         }
       }
     }

@@ -134,6 +134,6 @@ cudaError_t launch_append(const Dims& s, const kvq_cache_view& v, const __half* 
 cudaError_t launch_decode(const Dims& s, const DecodePlan& p, const kvq_cache_view& v,
                           const __half* q, int Hq, __half* out, void* workspace,
                           cudaStream_t st, const __half* k_new = nullptr,
-                          const __half* v_new = nullptr);
+                          const __half* v_new = nullptr, uint32_t step_flags = 0);
 
 }  // namespace kvq

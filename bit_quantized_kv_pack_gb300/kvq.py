@@ -90,7 +90,7 @@ def load(path: str | None = None):
             lib.kvq_append.restype = ctypes.c_int
             lib.kvq_decode_attention.argtypes = [DP, VP, P, i32, P, P, sz, P]
             lib.kvq_decode_attention.restype = ctypes.c_int
-            lib.kvq_decode_step.argtypes = [DP, VP, P, i32, P, P, P, P, sz, P]
+            lib.kvq_decode_step.argtypes = [DP, VP, P, i32, P, P, P, P, sz, ctypes.c_uint32, P]
             lib.kvq_decode_step.restype = ctypes.c_int
             lib.kvq_decode_attention_noalloc.argtypes = [DP, VP, P, i32, P, P]
             lib.kvq_decode_attention_noalloc.restype = ctypes.c_int
@@ -237,12 +237,16 @@ def kvq_decode_attention(cache: KVCache, q: torch.Tensor, out: torch.Tensor | No
     return out
 
 
+KVQ_STEP_EARLY_CACHE_READ = 1
+
+
 def kvq_decode_step(cache: KVCache, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                     out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                    stream=None) -> torch.Tensor:
+                    stream=None, flags: int = 0) -> torch.Tensor:
     """One serving-loop step: append k_new/v_new (fp16 [B][Hkv][d]), then decode
     attention of q over the updated cache; one kernel launch where the tensor-core
-    kernel applies."""
+    kernel applies.  flags=KVQ_STEP_EARLY_CACHE_READ: the kernel enqueued just
+    before does not write this cache (see kvq.h)."""
     _f16(q, "q"), _f16(k_new, "k_new"), _f16(v_new, "v_new")
     if out is None:
         out = torch.empty_like(q)
@@ -252,7 +256,7 @@ def kvq_decode_step(cache: KVCache, q: torch.Tensor, k_new: torch.Tensor, v_new:
     st = load().kvq_decode_step(ctypes.byref(cache.desc), ctypes.byref(cache.view), _ptr(q),
                                 int(q.shape[1]), _ptr(k_new), _ptr(v_new), _ptr(out),
                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                _stream(stream, q.device))
+                                int(flags), _stream(stream, q.device))
     _check(st, "kvq_decode_step")
     return out
 

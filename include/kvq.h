@@ -201,11 +201,23 @@ kvq_status kvq_decode_attention(const kvq_cache_desc* desc, const kvq_cache_view
  * and the packed token, and the counters move when the last head of a sequence
  * finishes.  Other shapes launch the append and the decode kernels in turn.  A
  * sequence whose packed cache is full is left unchanged, sets
- * KVQ_ERRBIT_CAPACITY and is attended as it was.  Asynchronous. */
+ * KVQ_ERRBIT_CAPACITY and is attended as it was.
+ *   flags      0, or KVQ_STEP_EARLY_CACHE_READ: the caller states that the
+ *              kernel enqueued on `stream` just before this call does not write
+ *              this cache (codes, params, window, counters) -- in a serving loop
+ *              it computes q, k_new and v_new, and the cache was last written by
+ *              this layer's previous step.  The step (launched as a programmatic
+ *              dependent of that kernel) then reads the counters and starts its
+ *              first tile copies before it waits for that kernel; q, k_new and
+ *              v_new are read, and anything is written, only after the wait.
+ *              Without the flag nothing is read before the wait.  Other bits
+ *              return KVQ_ERR_INVALID_ARG.
+ * Asynchronous. */
+#define KVQ_STEP_EARLY_CACHE_READ 1u
 kvq_status kvq_decode_step(const kvq_cache_desc* desc, const kvq_cache_view* view,
                            const void* q, int32_t num_q_heads, const void* k_new,
                            const void* v_new, void* out, void* workspace, size_t ws_bytes,
-                           void* stream);
+                           uint32_t flags, void* stream);
 
 /* Size of the device scratch array behind kvq_decode_attention_noalloc (8 MiB). */
 #define KVQ_NOALLOC_SCRATCH_BYTES (8u << 20)

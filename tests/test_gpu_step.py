@@ -110,3 +110,55 @@ def test_step_workload_full_size(num):
         err, rel = assert_attn_close(out, oracle.decode(r, q.numpy()))
         print(f"workload {num} step {step}: max abs {err:.2e}, rel L2 {rel:.2e}")
     assert_cache_equal(g, r)
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_step_early_cache_read_alternating_caches(bits):
+    """KVQ_STEP_EARLY_CACHE_READ on steps that alternate between two caches, all
+    enqueued back to back (each step's predecessor writes the other cache, as the
+    flag requires): every output and both caches match the oracle run step by
+    step, and match the same run without the flag."""
+    rng = np.random.default_rng(500 + bits)
+    B, H, d, gq, Nr, cap, nsteps = 2, 2, 128, 4, 16, 900, 12
+    lens = torch.tensor([600, 17], dtype=torch.int32)
+    k = torch.from_numpy((rng.standard_normal((2, B, H, 600, d)) * 2).astype(np.float16))
+    v = torch.from_numpy(rng.standard_normal((2, B, H, 600, d)).astype(np.float16))
+    qs = torch.from_numpy(rng.standard_normal((nsteps, 2, B, H * gq, d)).astype(np.float16))
+    kns = torch.from_numpy((rng.standard_normal((nsteps, 2, B, H, d)) * 2).astype(np.float16))
+    vns = torch.from_numpy(rng.standard_normal((nsteps, 2, B, H, d)).astype(np.float16))
+    results = {}
+    for flags in (kvq.KVQ_STEP_EARLY_CACHE_READ, 0):
+        caches = [gpu_cache(B, H, d, bits, cap, Nr) for _ in range(2)]
+        for c, kk, vv in zip(caches, k, v):
+            kvq.kvq_quantize_pack(c, kk.to(DEV), vv.to(DEV), lens.to(DEV))
+        ws = kvq.workspace_for(caches[0], H * gq)
+        qd, knd, vnd = qs.to(DEV), kns.to(DEV), vns.to(DEV)
+        outs = torch.empty_like(qd)
+        torch.cuda.synchronize()
+        for t in range(nsteps):  # no host synchronisation between the launches
+            for i in range(2):
+                kvq.kvq_decode_step(caches[i], qd[t, i], knd[t, i], vnd[t, i], outs[t, i], ws,
+                                    flags=flags)
+        torch.cuda.synchronize()
+        for c in caches:
+            assert kvq.kvq_read_error(c)[0] == kvq.KVQ_OK
+        results[flags] = (caches, outs)
+    (ca, oa), (cb, ob) = results[kvq.KVQ_STEP_EARLY_CACHE_READ], results[0]
+    for i in range(2):
+        _assert_gpu_caches_equal(ca[i], cb[i])
+    assert torch.equal(oa, ob)
+    for i in range(2):
+        r = ref_cache(B, H, d, bits, cap, Nr)
+        assert oracle.quantize_pack(r, k[i].numpy(), v[i].numpy(), lens.numpy()) == 0
+        for t in range(nsteps):
+            assert oracle.append(r, kns[t, i].numpy(), vns[t, i].numpy()) == 0
+            assert_attn_close(oa[t, i], oracle.decode(r, qs[t, i].numpy()))
+        assert_cache_equal(ca[i], r)
+
+
+def test_step_rejects_unknown_flags():
+    g = gpu_cache(1, 1, 128, 4, 16, 4)
+    q = torch.zeros(1, 4, 128, dtype=torch.float16, device=DEV)
+    kn = torch.zeros(1, 1, 128, dtype=torch.float16, device=DEV)
+    with pytest.raises(kvq.KvqError):
+        kvq.kvq_decode_step(g, q, kn, kn, flags=2)
