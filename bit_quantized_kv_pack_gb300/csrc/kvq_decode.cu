@@ -31,12 +31,12 @@ DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count, b
   p.gq = num_q_heads / D.num_kv_heads;
   int64_t target, min_tokens;
   if (tc_supported(D, p.gq)) {
-    // tensor-core kernel: 4 query heads per CTA, two CTAs per SM
+    // tensor-core kernel: 4 query heads per CTA, one wave of resident CTAs
     p.kernel = 1;
     p.qb = 4;
     p.nqb = 1;
     p.threads = tc_threads();
-    target = (int64_t)sm_count * 2;
+    target = (int64_t)sm_count * tc_ctas_per_sm();
     min_tokens = 256;
   } else {
     p.kernel = 0;
@@ -56,9 +56,11 @@ DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count, b
   p.splits = (int)S;
   p.splits_packed = p.splits;
   if (p.kernel == 1) {
-    // the fp16 residual tokens get splits of their own, one per 128 tokens of
-    // the window (at least one in a fused step: it takes the appended token)
-    int sr = (D.residual + 127) / 128;
+    // the fp16 residual tokens get splits of their own, one per block of
+    // tc_residual_rows() ring slots (at least one in a fused step: it takes the
+    // appended token)
+    const int rr = tc_residual_rows();
+    int sr = (D.residual + rr - 1) / rr;
     if (step && sr < 1) sr = 1;
     const int sp = (int)S - sr > 1 ? (int)S - sr : 1;
     p.splits_packed = sp;
@@ -66,9 +68,14 @@ DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count, b
   }
   const int64_t nparts = units * p.splits * p.qb;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const size_t uq = (size_t)units * p.qb;
   p.ws_cnt_off = 0;
   p.ws_seq_off = up((size_t)units * sizeof(uint32_t));
-  p.ws_ml_off = up(p.ws_seq_off + (size_t)D.batch * sizeof(uint32_t));
+  p.ws_ref_off = up(p.ws_seq_off + (size_t)D.batch * sizeof(uint32_t));
+  p.ws_flag_off = up(p.ws_ref_off + uq * sizeof(uint32_t));
+  p.ws_oacc_off = up(p.ws_flag_off + (size_t)units * sizeof(uint32_t));
+  p.ws_lacc_off = up(p.ws_oacc_off + uq * D.head_dim * sizeof(float));
+  p.ws_ml_off = up(p.ws_lacc_off + uq * sizeof(float));
   p.ws_part_off = up(p.ws_ml_off + (size_t)nparts * sizeof(float2));
   p.ws_total = p.ws_part_off + (size_t)nparts * D.head_dim * sizeof(float);
   return p;
@@ -96,6 +103,10 @@ cudaError_t launch_decode(const Dims& s, const DecodePlan& p, const kvq_cache_vi
   a.ml_part = reinterpret_cast<float2*>(ws + p.ws_ml_off);
   a.counters = reinterpret_cast<uint32_t*>(ws + p.ws_cnt_off);
   a.seq_tickets = reinterpret_cast<uint32_t*>(ws + p.ws_seq_off);
+  a.ref_max = reinterpret_cast<uint32_t*>(ws + p.ws_ref_off);
+  a.fb_flag = reinterpret_cast<uint32_t*>(ws + p.ws_flag_off);
+  a.o_acc = reinterpret_cast<float*>(ws + p.ws_oacc_off);
+  a.l_acc = reinterpret_cast<float*>(ws + p.ws_lacc_off);
   // the fused step (tensor-core kernel only) writes the cache
   a.k_new = k_new;
   a.v_new = v_new;

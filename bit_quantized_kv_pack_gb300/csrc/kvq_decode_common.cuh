@@ -27,6 +27,12 @@ struct DecodeArgs {
   float2* ml_part;
   uint32_t* counters;     // [B][Hkv][nqb] arrival tickets, zero between calls
   uint32_t* seq_tickets;  // [B] fused step: units of the sequence done, zero between calls
+  // tensor-core kernel: shared-reference accumulation of the split results
+  // (zero between calls; layout at DecodePlan)
+  uint32_t* ref_max;
+  uint32_t* fb_flag;
+  float* o_acc;
+  float* l_acc;
   // fused step (append, then attend): the new token and the cache as writable
   const __half* k_new;  // [B][Hkv][d]
   const __half* v_new;
@@ -81,6 +87,8 @@ __device__ __forceinline__ void split_range(int Lp, int Lr, int s, int S, int64_
 // Tensor-core kernel: head_dim 128, 1 <= gq <= 4 (kvq_decode_tc.cu).
 bool tc_supported(const kvq_cache_desc& D, int gq);
 int tc_threads();
+int tc_ctas_per_sm();
+int tc_residual_rows();
 cudaError_t launch_decode_tc(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
                              cudaStream_t st, bool step);
 

@@ -8,7 +8,7 @@
 // section 2.3).  How:
 //
 //  * 128-token tiles -- K codes, V codes, K params, V params -- stream in by 2D
-//    TMA tile loads into a 4-stage (INT4) or 6-stage (INT2) shared-memory ring
+//    TMA tile loads into a 3-stage (INT4) or 5-stage (INT2) shared-memory ring
 //    guarded by mbarriers (the asynchronous staging of the BitDecoding page,
 //    section 2.3, done with the bulk tensor copy instead of per-thread
 //    cp.async).  One thread issues the first stages up front; the warp that
@@ -36,9 +36,15 @@
 //    again holds one query.  A ninth MMA accumulates sum p * min_g and sum p
 //    (= l), so O = O_c + sum_g p min_g.
 //  * The fp16 residual tokens get splits of their own (CUDA cores, all loads of
-//    a chunk in one round), so no packed split waits on them.  Per-warp states
-//    merge in shared memory, and the last split of a KV head to finish merges
-//    the split partials (combine_unit).
+//    a chunk in one round), so no packed split waits on them.
+//  * Per-warp states merge in shared memory.  The first split of a KV head to
+//    finish its first tile sets the head's reference max per query (atomicCAS);
+//    every split adds its (o, l), scaled to that reference, into the head's fp32
+//    accumulators (vector red.add), and the last split to finish divides by l.
+//    A split whose max lies too far above the reference sends the head to the
+//    exact log-sum-exp merge of the split partials (combine_unit) instead.
+//  * Three CTAs per SM (168 registers each): twelve warps hide the latency of
+//    the dequantize-and-MMA chain.
 //
 // Every mbarrier wait is bounded; a wait that runs out sets KVQ_ERRBIT_TIMEOUT.
 #include <math.h>
@@ -56,6 +62,8 @@ constexpr int T = 128;          // tokens per pipeline stage
 constexpr int NCW = 4;          // warps, 32 tokens (two 16-token sub-tiles) each per stage
 constexpr int NSUB = 2;         // sub-tiles per warp per stage
 constexpr int NTHREADS = NCW * 32;
+constexpr int kCtasPerSm = 3;   // 12 warps per SM: 168 registers, ~62 KB of shared memory each
+static_assert(NCW == QB, "the merge gives each warp one query");
 
 template <int BITS>
 struct Geo {
@@ -67,7 +75,7 @@ struct Geo {
   static constexpr int KP = 2 * CODE_TILE;
   static constexpr int VP = 2 * CODE_TILE + PAR_TILE;
   static constexpr int STAGE = 2 * CODE_TILE + 2 * PAR_TILE;  // 20 KB / 12 KB
-  static constexpr int NSTAGE = BITS == 4 ? 4 : 6;               // 80 KB / 72 KB in flight
+  static constexpr int NSTAGE = BITS == 4 ? 3 : 5;               // 60 KB in flight per CTA
   static constexpr float CENTER = BITS == 4 ? 7.5f : 1.5f;       // mid code
   static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned");
 };
@@ -80,13 +88,15 @@ struct MergeSmem {
   float mn[NCW][9][8];
 };
 
-// The merge scratch, then the fused step's extra tokens [2][2][D] fp32, overlap
-// the stage ring once it is idle (residual splits never use the ring).
+// The merge scratch, then the fused step's extra tokens [2][2][D] fp32, then a
+// residual split's K and V rows overlap the stage ring (residual splits never
+// use the ring; packed splits reuse it for the merge once it is idle).
+constexpr size_t kResTilesOff = (sizeof(MergeSmem) + 4 * D * sizeof(float) + 127) & ~(size_t)127;
 template <int BITS>
 constexpr size_t tc_smem_bytes() {
   constexpr size_t ring = (size_t)Geo<BITS>::NSTAGE * Geo<BITS>::STAGE;
-  constexpr size_t merge = sizeof(MergeSmem) + 4 * D * sizeof(float);
-  return 1024 + (ring > merge ? ring : merge);
+  constexpr size_t res = kResTilesOff + 2 * 64 * (2 * D + 16);  // kResRows rows of K and V
+  return 1024 + (ring > res ? ring : res);
 }
 
 // ------------------------------------------------------- code conversion ---
@@ -122,6 +132,9 @@ __host__ __device__ constexpr float w2_weight(int j) {
 }
 
 constexpr float kTwo24 = 16777216.f;  // 2^24
+// A split whose max (log2 units) is more than this above the head's reference
+// could overflow fp32 once scaled to it: the head then takes the exact merge.
+constexpr float kRefSlack = 80.f;
 
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -252,70 +265,90 @@ __device__ __forceinline__ void pv_subtile(uint32_t vc, const uint32_t* vp, int 
 
 // ---------------------------------------------------------- residual ----
 
-// Residual-only CTA: the fp16 tokens [j0, j1) of the ring on the CUDA cores,
-// 32 tokens per warp and chunk -- lane = token for the scores, lane = four
-// head_dim values for the weighted sum.  All loads of a chunk (the lane's key
-// row, and four values of each of the 32 value rows) are issued before any
-// arithmetic, so a chunk costs one memory round trip.  Leaves the warp's state
-// in (rm, rl, ro).
-__device__ __forceinline__ void residual_tokens(const DecodeArgs& a, int64_t bh, int rh, int j0,
-                                                int j1, int warp, int lane, const float (&q_s)[QB][D],
-                                                float kq, float (&rm)[QB], float (&rl)[QB],
-                                                float (&ro)[QB][4]) {
-  for (int base = j0 + warp * 32; base < j1; base += NCW * 32) {
-    const int j = base + lane;
-    const bool valid = j < j1;
-    const int nv = min(32, j1 - base);
-    uint4 kr[D / 8];
-    uint2 vv[32];
-    {
-      const uint4* krow = reinterpret_cast<const uint4*>(a.k_res + (bh * a.Nr + (rh + (valid ? j : j0)) % a.Nr) * D);
+// Residual split: ring slots [c0, c0 + kResRows) of (sequence, KV head) bh, fp16,
+// on the tensor cores.  A slot takes part when its age (slot - ring head, mod
+// Nr) lies in [age0, age1); only those rows are copied (zero-filled otherwise),
+// so no stale bytes of unused slots enter the arithmetic.  Rows are padded to
+// 272 bytes, which makes every ldmatrix conflict-free.  Warp w takes rows
+// 16w .. 16w+15 as one sub-tile: S^T = K q^T (query columns duplicated, so each
+// thread holds one query), softmax, O^T = V^T p^T, and writes its (m, l, o) to
+// the merge scratch.
+constexpr int kResRows = 64;
+constexpr int kResStride = D * 2 + 16;  // bytes per row in shared memory
+
+__device__ __forceinline__ void residual_tc(const DecodeArgs& a, int64_t bh, int rh, int age0,
+                                            int age1, int c0, uint8_t* tiles, int warp, int lane,
+                                            const float (&q_s)[QB][D], float kq, MergeSmem& ms) {
+  const int g = lane >> 2, t = lane & 3;
+  const int Nr = a.Nr;
+  auto valid_slot = [&](int slot) {
+    if (slot >= Nr) return false;
+    int age = slot - rh;
+    if (age < 0) age += Nr;
+    return age >= age0 && age < age1;
+  };
+  // stage K (rows 0..63) and V (rows 64..127) of the valid slots
+  const uint32_t tbase = ptx::smem_u32(tiles);
+  for (int idx = threadIdx.x; idx < 2 * kResRows * (D / 8); idx += NTHREADS) {
+    const int arr = idx / (kResRows * (D / 8));
+    const int rem = idx % (kResRows * (D / 8));
+    const int row = rem / (D / 8), chunk = rem % (D / 8);
+    const int slot = c0 + row;
+    const bool ok = valid_slot(slot);
+    const __half* src = (arr ? a.v_res : a.k_res) + (bh * Nr + (ok ? slot : 0)) * D + chunk * 8;
+    ptx::cp_async_16(tbase + (arr * kResRows + row) * kResStride + chunk * 16, src, ok ? 16u : 0u);
+  }
+  ptx::cp_async_wait_all();
+  __syncthreads();
+
+  const int r0 = 16 * warp;
+  const int mj = lane >> 3, mi = lane & 7;
+  // ---- S^T = K q^T, one MMA per 16 head_dim values
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int e8 = 0; e8 < D / 8; ++e8) kr[e8] = valid ? __ldg(krow + e8) : make_uint4(0, 0, 0, 0);
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const int row = r0 + (mj & 1) * 8 + mi;
+    const uint32_t addr = tbase + row * kResStride + (16 * ks + (mj >> 1) * 8) * 2;
+    uint32_t a0, a1, a2, a3;
+    ptx::ldmatrix_x4(addr, a0, a1, a2, a3);
+    const int qi = g >> 1, d0 = 16 * ks + 2 * t;
+    const uint32_t b0 = ptx::pack_h2(q_s[qi][d0], q_s[qi][d0 + 1]);
+    const uint32_t b1 = ptx::pack_h2(q_s[qi][d0 + 8], q_s[qi][d0 + 9]);
+    ptx::mma_16816(acc, a0, a1, a2, a3, b0, b1);
+  }
+  // ---- softmax of query t over the warp's 16 rows
+  const float s0 = valid_slot(c0 + r0 + g) ? acc[0] * kq : -INFINITY;
+  const float s1 = valid_slot(c0 + r0 + g + 8) ? acc[2] * kq : -INFINITY;
+  float m = fmaxf(s0, s1);
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+  const float mu = m == -INFINITY ? 0.f : m;
+  const uint32_t pk = ptx::pack_h2(exp2f(s0 - mu), exp2f(s1 - mu));
+  const uint32_t x0 = __shfl_sync(0xffffffffu, pk, (2 * t) * 4 + (g >> 1));
+  const uint32_t x1 = __shfl_sync(0xffffffffu, pk, (2 * t + 1) * 4 + (g >> 1));
+  const uint32_t pb0 = ptx::prmt(x0, x1, 0x5410u);  // tokens 2t, 2t+1 of query g / 2
+  const uint32_t pb1 = ptx::prmt(x0, x1, 0x7632u);  // tokens 2t+8, 2t+9
+  // ---- O^T = V^T p^T, one MMA per 16 head_dim values; l = sum of the same p
+  float lacc[4] = {0.f, 0.f, 0.f, 0.f};
+  constexpr uint32_t kOnes = 0x3C003C00u;
+  ptx::mma_16816(lacc, kOnes, kOnes, kOnes, kOnes, pb0, pb1);
+  const uint32_t vbase = tbase + kResRows * kResStride;
 #pragma unroll
-      for (int tt = 0; tt < 32; ++tt) {
-        const int jj = base + (tt < nv ? tt : 0);
-        vv[tt] = __ldg(reinterpret_cast<const uint2*>(a.v_res + (bh * a.Nr + (rh + jj) % a.Nr) * D + lane * 4));
-      }
-    }
-    float scv[QB];
-#pragma unroll
-    for (int i = 0; i < QB; ++i) scv[i] = 0.f;
-#pragma unroll
-    for (int e8 = 0; e8 < D / 8; ++e8) {
-      float xv[8];
-      unpack8_f16(kr[e8], xv);
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-#pragma unroll
-        for (int i = 0; i < QB; ++i) scv[i] = fmaf(xv[e], q_s[i][e8 * 8 + e], scv[i]);
-    }
-    float pr[QB];
-#pragma unroll
-    for (int i = 0; i < QB; ++i) {
-      const float v = valid ? scv[i] * kq : -INFINITY;
-      const float mnew = fmaxf(rm[i], warp_max(v));
-      const float al = exp2f(rm[i] - mnew);
-      pr[i] = valid ? exp2f(v - mnew) : 0.f;
-      rl[i] = rl[i] * al + warp_sum(pr[i]);
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) ro[i][jj] *= al;
-      rm[i] = mnew;
-    }
-#pragma unroll
-    for (int tt = 0; tt < 32; ++tt) {
-      const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&vv[tt].x));
-      const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&vv[tt].y));
-#pragma unroll
-      for (int i = 0; i < QB; ++i) {
-        float pt = __shfl_sync(0xffffffffu, pr[i], tt);
-        pt = tt < nv ? pt : 0.f;
-        ro[i][0] = fmaf(pt, f01.x, ro[i][0]);
-        ro[i][1] = fmaf(pt, f01.y, ro[i][1]);
-        ro[i][2] = fmaf(pt, f23.x, ro[i][2]);
-        ro[i][3] = fmaf(pt, f23.y, ro[i][3]);
-      }
-    }
+  for (int mb = 0; mb < D / 16; ++mb) {
+    // matrices: tokens 0-7 | dims +0, tokens 0-7 | dims +8, tokens 8-15 | +0, 8-15 | +8
+    const int row = r0 + (mj >> 1) * 8 + mi;
+    const uint32_t addr = vbase + row * kResStride + (16 * mb + (mj & 1) * 8) * 2;
+    uint32_t v0, v1, v2, v3;
+    ptx::ldmatrix_x4_trans(addr, v0, v1, v2, v3);
+    float o[4] = {0.f, 0.f, 0.f, 0.f};
+    ptx::mma_16816(o, v0, v1, v2, v3, pb0, pb1);
+    ms.o[warp][t][16 * mb + g] = o[0];
+    ms.o[warp][t][16 * mb + g + 8] = o[2];
+  }
+  if (g == 0) {
+    ms.m[warp][t] = m;
+    ms.l[warp][t] = lacc[0];
   }
 }
 
@@ -335,7 +368,7 @@ __device__ __forceinline__ void residual_tokens(const DecodeArgs& a, int64_t bh,
 // (fp16) and the quantized one (dequantized in fp32).  The last head of a
 // sequence to finish commits the counters.
 template <int BITS, bool STEP>
-__global__ void __launch_bounds__(NTHREADS, 2)
+__global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
                      const __grid_constant__ CUtensorMap tm_kp, const __grid_constant__ CUtensorMap tm_vp,
                      const DecodeArgs a) {
@@ -352,6 +385,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   __shared__ int s_rng[6];  // range lo, hi, ring head, step flags, packed_len, res_len
   __shared__ volatile int s_abort;
   __shared__ int s_last;
+  __shared__ uint32_t s_ref[QB];  // the head's reference max per query (float bits + 1; 0: unknown)
 
   const int s = blockIdx.x;
   const int h = blockIdx.y;  // one query block per KV head (gq <= 4)
@@ -372,6 +406,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       s_last_tile[st] = -1;
     }
     s_abort = 0;
+    for (int i = 0; i < QB; ++i) s_ref[i] = 0u;
     ptx::fence_mbar_init();
     if (!res_cta) {
       ptx::prefetch_tensormap(&tm_kc);
@@ -415,10 +450,11 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       r1_ = (int)((int64_t)Lp * (s + 1) / a.Sp);
     } else {
       const int Sr = a.S - a.Sp, sr = s - a.Sp;
-      // window tokens [jlo, Lr) in age order; a flushed oldest token leaves it
+      // window tokens of age [jlo, Lr) take part (a flushed oldest token leaves
+      // the window); residual split sr holds ring slots [64 sr, 64 sr + 64)
       const int jlo = (adds && a.Nr > 0 && pack_now) ? 1 : 0;
-      r0_ = jlo + (int)((int64_t)(Lr - jlo) * sr / Sr);
-      r1_ = jlo + (int)((int64_t)(Lr - jlo) * (sr + 1) / Sr);
+      r0_ = jlo;
+      r1_ = Lr;
       // bit 0: the new token joins the window; bit 1: a token is packed into slot Lp
       if (adds && sr == Sr - 1) xflags = (a.Nr > 0 ? 1 : 0) | (pack_now ? 2 : 0);
     }
@@ -518,56 +554,59 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 
   if (res_cta) {
     // ------------------------------------------------ residual-token split
-    float rm[QB], rl[QB], ro[QB][4];
+    uint8_t* tiles = smem + kResTilesOff;
+    const int c0 = kResRows * (s - a.Sp);
+    if (a.Nr > 0) {
+      residual_tc(a, bh, s_rng[2], s_rng[0], s_rng[1], c0, tiles, warp, lane, q_s, kq, ms);
+    } else {  // no window (the split only takes a fused step's packed token)
+      __syncthreads();  // warp 1's V row of the extra token is staged
+      if (lane < QB) {
+        ms.m[warp][lane] = -INFINITY;
+        ms.l[warp][lane] = 0.f;
+      }
 #pragma unroll
-    for (int i = 0; i < QB; ++i) {
-      rm[i] = -INFINITY;
-      rl[i] = 0.f;
+      for (int i = 0; i < QB; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) ro[i][j] = 0.f;
+        for (int jj = 0; jj < 4; ++jj) ms.o[warp][i][lane * 4 + jj] = 0.f;
     }
-    residual_tokens(a, bh, s_rng[2], s_rng[0], s_rng[1], warp, lane, q_s, kq, rm, rl, ro);
     if (STEP) {
-      __syncthreads();  // the extra tokens are in shared memory
+      // the appended tokens (new fp16 token, quantized token), staged in xbuf by
+      // warps 0 and 1 before the barrier above, join warp 0's state; lane = four
+      // head_dim values
       const int xflags = s_rng[3];
+      __syncwarp();
       if (xflags != 0 && warp == 0) {
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          if (!(xflags & (1 << e))) continue;
-          float kx[4], vx[4];
+        for (int i = 0; i < QB; ++i) {
+          float rm = ms.m[0][i], rl = ms.l[0][i];
+          float ro[4];
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            kx[jj] = xbuf[e * D + lane * 4 + jj];
-            vx[jj] = xbuf[2 * D + e * D + lane * 4 + jj];
-          }
+          for (int jj = 0; jj < 4; ++jj) ro[jj] = ms.o[0][i][lane * 4 + jj];
 #pragma unroll
-          for (int i = 0; i < QB; ++i) {
+          for (int e = 0; e < 2; ++e) {
+            if (!(xflags & (1 << e))) continue;
             float part = 0.f;
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) part = fmaf(kx[jj], q_s[i][lane * 4 + jj], part);
+            for (int jj = 0; jj < 4; ++jj) part = fmaf(xbuf[e * D + lane * 4 + jj], q_s[i][lane * 4 + jj], part);
             const float v = warp_sum(part) * kq;
-            const float mnew = fmaxf(rm[i], v);
-            const float al = exp2f(rm[i] - mnew);
+            const float mnew = fmaxf(rm, v);
+            const float al = exp2f(rm - mnew);
             const float pe = exp2f(v - mnew);
-            rl[i] = fmaf(rl[i], al, pe);
+            rl = fmaf(rl, al, pe);
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) ro[i][jj] = fmaf(pe, vx[jj], ro[i][jj] * al);
-            rm[i] = mnew;
+            for (int jj = 0; jj < 4; ++jj) ro[jj] = fmaf(pe, xbuf[2 * D + e * D + lane * 4 + jj], ro[jj] * al);
+            rm = mnew;
           }
+          __syncwarp();
+          if (lane == 0) {
+            ms.m[0][i] = rm;
+            ms.l[0][i] = rl;
+          }
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) ms.o[0][i][lane * 4 + jj] = ro[jj];
         }
       }
     }
-    if (lane == 0) {
-#pragma unroll
-      for (int i = 0; i < QB; ++i) {
-        ms.m[warp][i] = rm[i];
-        ms.l[warp][i] = rl[i];
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < QB; ++i)
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) ms.o[warp][i][lane * 4 + jj] = ro[i][jj];
   } else {
     // ---------------------------------------------------- packed-token split
     {
@@ -641,6 +680,11 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       }
     }
 
+    // After its first tile, warp 0 offers its running max of each query as the
+    // head's reference (first offer wins); the answer is only needed at the end.
+    uint32_t ref_cas = 0u;
+    float ref_mine = 0.f;
+    bool ref_offered = false;
     for (int tile = 0; tile < ntiles; ++tile) {
       const int st = tile % NSTAGE;
       if (!ptx::mbar_wait_bounded(ptx::smem_u32(&full_bar[st]), (tile / NSTAGE) & 1)) {
@@ -720,6 +764,11 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             sb[1][r] *= al;
           }
         }
+        if (tile == 0 && warp == 0 && lane < QB) {
+          ref_mine = m_ref;
+          ref_cas = atomicCAS(&a.ref_max[bh * QB + lane], 0u, __float_as_uint(m_ref) + 1u);
+          ref_offered = true;
+        }
         const float mu = m_ref == -INFINITY ? 0.f : m_ref;
         // p as the PV B fragment: thread (g, t) needs p(query g / 2, tokens 2t,
         // 2t+1, 2t+8, 2t+9); lane 4 * token + query holds that query for rows
@@ -761,6 +810,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
           ptx::mbar_wait_bounded(ptx::smem_u32(&full_bar[st]), (s_last_tile[st] / NSTAGE) & 1);
     }
     __syncthreads();  // the stage ring is idle from here on: reuse it for the merge
+    if (ref_offered) s_ref[lane] = ref_cas == 0u ? __float_as_uint(ref_mine) + 1u : ref_cas;
     // per group x and query t, corr_x = sum p min_x + mid (sum p scale_x -
     // sum of the rounded p * scale_x), to shared memory first; then the outputs
     // O = 2^24 oc / weight + corr (the layout is at pv_subtile)
@@ -793,27 +843,55 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       }
   }
 
-  // ---------------- merge the four warps' states and write this split's partial
+  // ---------------- merge the four warps' states.  The split's partial (o, m, l)
+  // goes to the workspace for the fallback merge, and the same state, scaled to
+  // the head's reference max, is added into the head's fp32 accumulators.
   __syncthreads();
   const int64_t pidx = bh * a.S + s;
-  for (int idx = threadIdx.x; idx < QB * D; idx += NTHREADS) {
-    const int i = idx / D, e = idx % D;
+  {
+    const int i = warp;              // query
+    const int e = lane * 4;          // four head_dim values
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < NCW; ++w) M = fmaxf(M, ms.m[w][i]);
-    float osum = 0.f, lsum = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    float lsum = 0.f;
     if (M > -INFINITY) {
 #pragma unroll
       for (int w = 0; w < NCW; ++w) {
         const float f = exp2f(ms.m[w][i] - M);
         if (f > 0.f) {
-          osum = fmaf(ms.o[w][i][e], f, osum);
+          const float4 ow = *reinterpret_cast<const float4*>(&ms.o[w][i][e]);
+          o.x = fmaf(ow.x, f, o.x);
+          o.y = fmaf(ow.y, f, o.y);
+          o.z = fmaf(ow.z, f, o.z);
+          o.w = fmaf(ow.w, f, o.w);
           lsum = fmaf(ms.l[w][i], f, lsum);
         }
       }
     }
-    a.o_part[(pidx * QB + i) * D + e] = osum;
-    if (e == 0) a.ml_part[pidx * QB + i] = make_float2(M, lsum);
+    *reinterpret_cast<float4*>(a.o_part + (pidx * QB + i) * D + e) = o;
+    if (lane == 0) a.ml_part[pidx * QB + i] = make_float2(M, lsum);
+    if (M > -INFINITY) {  // warp-uniform
+      uint32_t ref = s_ref[i];
+      if (ref == 0u) {  // this split offered nothing yet: offer (or learn) now
+        uint32_t r = 0u;
+        if (lane == 0) {
+          const uint32_t mine = __float_as_uint(M) + 1u;
+          const uint32_t old = atomicCAS(&a.ref_max[bh * QB + i], 0u, mine);
+          r = old == 0u ? mine : old;
+        }
+        ref = __shfl_sync(0xffffffffu, r, 0);
+      }
+      const float dm = M - __uint_as_float(ref - 1u);
+      if (dm > kRefSlack) {
+        if (lane == 0) atomicOr(&a.fb_flag[bh], 1u);  // too far above: exact merge instead
+      } else {
+        const float g = exp2f(dm);
+        ptx::red_add_v4(a.o_acc + (bh * QB + i) * D + e, o.x * g, o.y * g, o.z * g, o.w * g);
+        if (lane == 0) atomicAdd(&a.l_acc[bh * QB + i], lsum * g);
+      }
+    }
   }
   // the last split of this KV head to finish merges all S partials
   if (take_last_ticket<NTHREADS>(a, bh, &s_last)) {
@@ -823,7 +901,27 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     // computed from the values this CTA read at its start.
     unsigned seq_ticket = 0;
     if (STEP && threadIdx.x == 0) seq_ticket = atomicInc(&a.seq_tickets[b], (unsigned)(a.Hkv - 1));
-    combine_unit<NTHREADS, D, 40>(a, b, h, 0, reinterpret_cast<float*>(smem));
+    const int i = warp, e = lane * 4;
+    float* oacc = a.o_acc + (bh * QB + i) * D + e;
+    if (__ldcg(&a.fb_flag[bh]) != 0u) {
+      // some split's max was too far above the reference: log-sum-exp merge of
+      // the S partials
+      combine_unit<NTHREADS, D, 8>(a, b, h, 0, reinterpret_cast<float*>(smem));
+    } else if (i < a.gq) {
+      const float4 o = __ldcg(reinterpret_cast<const float4*>(oacc));
+      const float L = __ldcg(&a.l_acc[bh * QB + i]);
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      __half2* dst = reinterpret_cast<__half2*>(a.out + ((int64_t)b * a.Hq + h * a.gq + i) * D + e);
+      dst[0] = __floats2half2_rn(o.x * inv, o.y * inv);
+      dst[1] = __floats2half2_rn(o.z * inv, o.w * inv);
+    }
+    // leave the head's accumulators, reference and flag at zero for the next call
+    *reinterpret_cast<float4*>(oacc) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane == 0) {
+      a.l_acc[bh * QB + i] = 0.f;
+      a.ref_max[bh * QB + i] = 0u;
+    }
+    if (threadIdx.x == 0) a.fb_flag[bh] = 0u;
     if (STEP && threadIdx.x == 0 && seq_ticket == (unsigned)(a.Hkv - 1)) {
       const int Lp = s_rng[4], Lr = s_rng[5], rh = s_rng[2];
       const bool pack_now = a.Nr == 0 || Lr == a.Nr;
@@ -915,6 +1013,8 @@ bool tc_supported(const kvq_cache_desc& D, int gq) {
 }
 
 int tc_threads() { return NTHREADS; }
+int tc_ctas_per_sm() { return kCtasPerSm; }
+int tc_residual_rows() { return kResRows; }
 
 cudaError_t launch_decode_tc(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
                              cudaStream_t st, bool step) {

@@ -113,6 +113,13 @@ struct DecodePlan {
   // split counts never has a partial land on a ticket.
   size_t ws_cnt_off;   // 0: per-unit arrival tickets [B][Hkv][nqb] (zero between calls)
   size_t ws_seq_off;   // per-sequence tickets [B] of the fused step (zero between calls)
+  // tensor-core kernel, zero between calls: per unit and query the reference
+  // max (float bits + 1, 0 = unset), a fallback flag per unit, and the fp32
+  // accumulators of o [qb][d] and l [qb]
+  size_t ws_ref_off;   // uint32 [units][qb]
+  size_t ws_flag_off;  // uint32 [units]
+  size_t ws_oacc_off;  // float [units][qb][d]
+  size_t ws_lacc_off;  // float [units][qb]
   size_t ws_ml_off;    // {m, l} partials
   size_t ws_part_off;  // o partials
   size_t ws_total;     // bytes of the whole workspace
