@@ -48,6 +48,9 @@ DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count, b
   }
   const int64_t units = (int64_t)D.batch * D.num_kv_heads * p.nqb;
   const int64_t tokens_max = (int64_t)D.capacity + D.residual;
+  // one CTA per unit short of a full wave: the previous launch's last CTA of
+  // each unit (its merger) still holds a slot when this launch starts
+  if (p.kernel == 1 && units * 4 <= target) target -= units;
   int64_t S = (target + units - 1) / units;
   const int64_t by_len = (tokens_max + min_tokens - 1) / min_tokens;
   if (S > by_len) S = by_len;

@@ -276,29 +276,39 @@ __device__ __forceinline__ void pv_subtile(uint32_t vc, const uint32_t* vp, int 
 constexpr int kResRows = 64;
 constexpr int kResStride = D * 2 + 16;  // bytes per row in shared memory
 
-__device__ __forceinline__ void residual_tc(const DecodeArgs& a, int64_t bh, int rh, int age0,
-                                            int age1, int c0, uint8_t* tiles, int warp, int lane,
-                                            const float (&q_s)[QB][D], float kq, MergeSmem& ms) {
-  const int g = lane >> 2, t = lane & 3;
+__device__ __forceinline__ bool residual_valid(int slot, int Nr, int rh, int age0, int age1) {
+  if (slot >= Nr) return false;
+  int age = slot - rh;
+  if (age < 0) age += Nr;
+  return age >= age0 && age < age1;
+}
+
+// Start the copies of the valid rows: K to rows 0..63, V to rows 64..127.
+__device__ __forceinline__ void residual_issue(const DecodeArgs& a, int64_t bh, int rh, int age0,
+                                               int age1, int c0, uint8_t* tiles) {
   const int Nr = a.Nr;
-  auto valid_slot = [&](int slot) {
-    if (slot >= Nr) return false;
-    int age = slot - rh;
-    if (age < 0) age += Nr;
-    return age >= age0 && age < age1;
-  };
-  // stage K (rows 0..63) and V (rows 64..127) of the valid slots
   const uint32_t tbase = ptx::smem_u32(tiles);
   for (int idx = threadIdx.x; idx < 2 * kResRows * (D / 8); idx += NTHREADS) {
     const int arr = idx / (kResRows * (D / 8));
     const int rem = idx % (kResRows * (D / 8));
     const int row = rem / (D / 8), chunk = rem % (D / 8);
     const int slot = c0 + row;
-    const bool ok = valid_slot(slot);
+    const bool ok = residual_valid(slot, Nr, rh, age0, age1);
     const __half* src = (arr ? a.v_res : a.k_res) + (bh * Nr + (ok ? slot : 0)) * D + chunk * 8;
     ptx::cp_async_16(tbase + (arr * kResRows + row) * kResStride + chunk * 16, src, ok ? 16u : 0u);
   }
-  ptx::cp_async_wait_all();
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait for the copies, then attend (every thread of the CTA calls it).
+__device__ __forceinline__ void residual_tc(const DecodeArgs& a, int rh, int age0, int age1,
+                                            int c0, uint8_t* tiles, int warp, int lane,
+                                            const float (&q_s)[QB][D], float kq, MergeSmem& ms) {
+  const int g = lane >> 2, t = lane & 3;
+  const int Nr = a.Nr;
+  auto valid_slot = [&](int slot) { return residual_valid(slot, Nr, rh, age0, age1); };
+  const uint32_t tbase = ptx::smem_u32(tiles);
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
   __syncthreads();
 
   const int r0 = 16 * warp;
@@ -479,6 +489,10 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
   // are read before waiting for that kernel; q and the new token never are.
   const bool early = STEP && a.early != 0;
   if (early && threadIdx.x == 0) plan();
+  if (early && res_cta && a.Nr > 0) {  // the window rows too (CTA-uniform branch)
+    __syncthreads();
+    residual_issue(a, bh, s_rng[2], s_rng[0], s_rng[1], kResRows * (s - a.Sp), smem + kResTilesOff);
+  }
   grid_dependency_wait();
 
   // The small loads go first -- q by every thread, the lengths by thread 0 --
@@ -504,6 +518,9 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
   __syncthreads();  // barriers initialised, range and q staged
   const float kq = a.qk_scale_log2;
   MergeSmem& ms = *reinterpret_cast<MergeSmem*>(smem);
+
+  if (!early && res_cta && a.Nr > 0)
+    residual_issue(a, bh, s_rng[2], s_rng[0], s_rng[1], kResRows * (s - a.Sp), smem + kResTilesOff);
 
   // extra tokens of a fused step, fp32: [K, V][new token, packed token][D]
   float* xbuf = reinterpret_cast<float*>(smem + sizeof(MergeSmem));
@@ -557,7 +574,7 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
     uint8_t* tiles = smem + kResTilesOff;
     const int c0 = kResRows * (s - a.Sp);
     if (a.Nr > 0) {
-      residual_tc(a, bh, s_rng[2], s_rng[0], s_rng[1], c0, tiles, warp, lane, q_s, kq, ms);
+      residual_tc(a, s_rng[2], s_rng[0], s_rng[1], c0, tiles, warp, lane, q_s, kq, ms);
     } else {  // no window (the split only takes a fused step's packed token)
       __syncthreads();  // warp 1's V row of the extra token is staged
       if (lane < QB) {
@@ -789,8 +806,9 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
       // Release the stage.  The warp that releases it last refills it with tile
       // + NSTAGE straight away: nobody waits for the slowest warp.
       if (lane == 0) {
-        __threadfence_block();  // this warp's reads of the stage come first
-        if (atomicAdd(&s_rel[st], 1) == NCW - 1) {
+        // release: this warp's reads of the stage come first; acquire: the
+        // warp that completes the count sees the others' releases
+        if (ptx::atom_add_acq_rel_cta(ptx::smem_u32(&s_rel[st]), 1u) == NCW - 1) {
           s_rel[st] = 0;
           const int next = tile + NSTAGE;
           if (next < ntiles && !s_abort) {
