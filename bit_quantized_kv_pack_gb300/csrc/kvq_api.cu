@@ -132,6 +132,57 @@ kvq_status kvq_decode_step(const kvq_cache_desc* desc, const kvq_cache_view* vie
                                       static_cast<const __half*>(v_new), flags));
 }
 
+namespace {
+struct StepIo {
+  size_t q, kv, in_bytes, out_off, total;
+};
+// Byte layout of the packed step input [q | k_new | v_new] and of the device
+// staging area (the input, then out at a 256-byte boundary).
+StepIo step_io(const kvq_cache_desc& D, int32_t num_q_heads) {
+  StepIo io;
+  io.q = (size_t)D.batch * num_q_heads * D.head_dim * sizeof(uint16_t);
+  io.kv = (size_t)D.batch * D.num_kv_heads * D.head_dim * sizeof(uint16_t);
+  io.in_bytes = io.q + 2 * io.kv;
+  io.out_off = (io.in_bytes + 255) & ~(size_t)255;
+  io.total = io.out_off + io.q;
+  return io;
+}
+}  // namespace
+
+size_t kvq_step_io_bytes(const kvq_cache_desc* desc, int32_t num_q_heads) {
+  if (check_desc(desc) != KVQ_OK || num_q_heads < 1 || num_q_heads % desc->num_kv_heads) return 0;
+  return step_io(*desc, num_q_heads).total;
+}
+
+kvq_status kvq_decode_step_host(const kvq_cache_desc* desc, const kvq_cache_view* view,
+                                const void* in_host, int32_t num_q_heads, void* out_host,
+                                void* dev_io, size_t dev_io_bytes, void* workspace,
+                                size_t ws_bytes, uint32_t flags, void* stream) {
+  kvq_status st = check_desc(desc);
+  if (st != KVQ_OK) return st;
+  if (!in_host || !out_host || !dev_io || num_q_heads < 1 || num_q_heads % desc->num_kv_heads)
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned(dev_io, 256)) return KVQ_ERR_MISALIGNED;
+  const StepIo io = step_io(*desc, num_q_heads);
+  if (dev_io_bytes < io.total) return KVQ_ERR_INVALID_ARG;
+  char* d = static_cast<char*>(dev_io);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // every argument the step itself checks is checked before anything is enqueued
+  const kvq::DecodePlan p = kvq::plan_decode(*desc, num_q_heads, kvq::device_sm_count(), true);
+  if ((st = check_view(*desc, view)) != KVQ_OK) return st;
+  if (!workspace || ws_bytes < p.ws_total || (flags & ~(uint32_t)KVQ_STEP_EARLY_CACHE_READ))
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned(workspace, 16)) return KVQ_ERR_MISALIGNED;
+  if (cudaMemcpyAsync(d, in_host, io.in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  st = kvq_decode_step(desc, view, d, num_q_heads, d + io.q, d + io.q + io.kv, d + io.out_off,
+                       workspace, ws_bytes, flags, stream);
+  if (st != KVQ_OK) return st;
+  if (cudaMemcpyAsync(out_host, d + io.out_off, io.q, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
 kvq_status kvq_read_error(const kvq_cache_view* view, uint32_t* word_out, void* stream) {
   if (!view || !view->err_word) return KVQ_ERR_INVALID_ARG;
   if (!aligned(view->err_word, 4)) return KVQ_ERR_MISALIGNED;

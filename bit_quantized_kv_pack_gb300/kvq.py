@@ -39,7 +39,8 @@ KVQ_ARRAY_RESIDUAL = 2
 
 # Every function the header declares (the tests check the library exports them).
 EXPORTS = ("kvq_cache_bytes", "kvq_decode_workspace_bytes", "kvq_quantize_pack", "kvq_append",
-           "kvq_decode_attention", "kvq_decode_step", "kvq_decode_attention_noalloc",
+           "kvq_decode_attention", "kvq_decode_step", "kvq_decode_step_host", "kvq_step_io_bytes",
+           "kvq_decode_attention_noalloc",
            "kvq_read_error", "kvq_status_string", "kvq_version")
 
 
@@ -92,6 +93,10 @@ def load(path: str | None = None):
             lib.kvq_decode_attention.restype = ctypes.c_int
             lib.kvq_decode_step.argtypes = [DP, VP, P, i32, P, P, P, P, sz, ctypes.c_uint32, P]
             lib.kvq_decode_step.restype = ctypes.c_int
+            lib.kvq_step_io_bytes.argtypes = [DP, i32]
+            lib.kvq_step_io_bytes.restype = sz
+            lib.kvq_decode_step_host.argtypes = [DP, VP, P, i32, P, P, sz, P, sz, ctypes.c_uint32, P]
+            lib.kvq_decode_step_host.restype = ctypes.c_int
             lib.kvq_decode_attention_noalloc.argtypes = [DP, VP, P, i32, P, P]
             lib.kvq_decode_attention_noalloc.restype = ctypes.c_int
             lib.kvq_read_error.argtypes = [VP, ctypes.POINTER(ctypes.c_uint32), P]
@@ -259,6 +264,36 @@ def kvq_decode_step(cache: KVCache, q: torch.Tensor, k_new: torch.Tensor, v_new:
                                 int(flags), _stream(stream, q.device))
     _check(st, "kvq_decode_step")
     return out
+
+
+def kvq_step_io_bytes(cache: KVCache, num_q_heads: int) -> int:
+    return int(load().kvq_step_io_bytes(ctypes.byref(cache.desc), int(num_q_heads)))
+
+
+def step_io_for(cache: KVCache, num_q_heads: int) -> torch.Tensor:
+    """Device staging for kvq_decode_step_host (256-byte aligned)."""
+    n = kvq_step_io_bytes(cache, num_q_heads)
+    if n == 0:
+        raise ValueError("invalid cache description or head count")
+    buf = torch.empty(n + 256, dtype=torch.uint8, device=cache.device)
+    off = (-buf.data_ptr()) % 256
+    return buf[off:off + n]
+
+
+def kvq_decode_step_host(cache: KVCache, in_host: torch.Tensor, num_q_heads: int,
+                         out_host: torch.Tensor, dev_io: torch.Tensor, workspace: torch.Tensor,
+                         stream=None, flags: int = 0) -> None:
+    """One step from host memory: in_host = [q | k_new | v_new] fp16 (pinned for
+    an asynchronous call), out_host fp16 [B][Hq][d]; copies, step and copy back
+    enqueued on the stream by one library call."""
+    if in_host.is_cuda or out_host.is_cuda:
+        raise ValueError("in_host and out_host must be host tensors")
+    st = load().kvq_decode_step_host(ctypes.byref(cache.desc), ctypes.byref(cache.view),
+                                     _ptr(in_host), int(num_q_heads), _ptr(out_host), _ptr(dev_io),
+                                     dev_io.numel() * dev_io.element_size(), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), int(flags),
+                                     _stream(stream, dev_io.device))
+    _check(st, "kvq_decode_step_host")
 
 
 NOALLOC_SCRATCH_BYTES = 8 << 20

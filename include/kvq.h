@@ -219,6 +219,29 @@ kvq_status kvq_decode_step(const kvq_cache_desc* desc, const kvq_cache_view* vie
                            const void* v_new, void* out, void* workspace, size_t ws_bytes,
                            uint32_t flags, void* stream);
 
+/* Bytes of device staging kvq_decode_step_host needs: the packed input
+ * [q | k_new | v_new] (fp16, in that order, no padding) and, at the next
+ * 256-byte boundary, out.  Returns 0 for an invalid desc or head count. */
+size_t kvq_step_io_bytes(const kvq_cache_desc* desc, int32_t num_q_heads);
+
+/* kvq_decode_step with its inputs and output in host memory (no passage of the
+ * pages corresponds to it; it is this library's serving-loop entry point).
+ *   in_host    host [q (B*Hq*d) | k_new (B*Hkv*d) | v_new (B*Hkv*d)] fp16, the
+ *              layouts of kvq_decode_step, contiguous in that order.
+ *   out_host   host [B][Hq][d] fp16.
+ *   dev_io     device staging of dev_io_bytes >= kvq_step_io_bytes(desc, Hq),
+ *              256-byte aligned, owned by the caller.
+ * Enqueues on `stream`: one host-to-device copy of the input block, the step
+ * (as kvq_decode_step with the same workspace and flags), and one
+ * device-to-host copy of out.  Asynchronous when the host buffers are pinned
+ * (page-locked), in which case they must stay valid until the stream reaches
+ * the copies; with pageable memory the copies are synchronous.  Argument errors
+ * return before anything is enqueued. */
+kvq_status kvq_decode_step_host(const kvq_cache_desc* desc, const kvq_cache_view* view,
+                                const void* in_host, int32_t num_q_heads, void* out_host,
+                                void* dev_io, size_t dev_io_bytes, void* workspace,
+                                size_t ws_bytes, uint32_t flags, void* stream);
+
 /* Size of the device scratch array behind kvq_decode_attention_noalloc (8 MiB). */
 #define KVQ_NOALLOC_SCRATCH_BYTES (8u << 20)
 

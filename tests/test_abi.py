@@ -117,6 +117,36 @@ def test_rejects_bad_view_and_args(lib):
     assert lib.kvq_read_error(None, None, None) == kvq.KVQ_ERR_INVALID_ARG
 
 
+def test_step_io_bytes(lib):
+    D = _desc()  # B2, Hkv8, d128
+    q, kv = 2 * 32 * 128 * 2, 2 * 8 * 128 * 2
+    n_in = q + 2 * kv
+    assert lib.kvq_step_io_bytes(ctypes.byref(D), 32) == ((n_in + 255) // 256) * 256 + q
+    assert lib.kvq_step_io_bytes(ctypes.byref(D), 12) == 0
+    assert lib.kvq_step_io_bytes(ctypes.byref(_desc(bits=3)), 32) == 0
+
+
+def test_step_host_rejects_bad_args(lib):
+    D, V = _desc(), _view()
+    P = ctypes.c_void_p
+    io = lib.kvq_step_io_bytes(ctypes.byref(D), 32)
+    ws = kvq.kvq_decode_workspace_bytes(D, 32)
+    host = P(0x7000000)  # never dereferenced: every call below fails its checks first
+
+    def call(in_h=host, out_h=host, dev=P(0x100000), dev_bytes=io, w=P(0x200000), w_bytes=ws, flags=0, hq=32):
+        return lib.kvq_decode_step_host(ctypes.byref(D), ctypes.byref(V), in_h, hq, out_h, dev, dev_bytes,
+                                        w, w_bytes, flags, None)
+    assert call(in_h=None) == kvq.KVQ_ERR_INVALID_ARG
+    assert call(out_h=None) == kvq.KVQ_ERR_INVALID_ARG
+    assert call(dev=None) == kvq.KVQ_ERR_INVALID_ARG
+    assert call(dev=P(0x100010)) == kvq.KVQ_ERR_MISALIGNED  # 16- but not 256-byte aligned
+    assert call(dev_bytes=io - 1) == kvq.KVQ_ERR_INVALID_ARG
+    assert call(w_bytes=ws - 1) == kvq.KVQ_ERR_INVALID_ARG
+    assert call(flags=4) == kvq.KVQ_ERR_INVALID_ARG
+    assert call(hq=12) == kvq.KVQ_ERR_INVALID_ARG
+    assert call(w=P(0x200008)) == kvq.KVQ_ERR_MISALIGNED
+
+
 def test_missing_library_raises(tmp_path):
     import importlib
     mod = importlib.reload(kvq)
@@ -126,3 +156,4 @@ def test_missing_library_raises(tmp_path):
             mod.load(str(tmp_path / "nope.so"))
     finally:
         mod._lib = None
+

@@ -161,3 +161,38 @@ def test_step_rejects_unknown_flags():
     kn = torch.zeros(1, 1, 128, dtype=torch.float16, device=DEV)
     with pytest.raises(kvq.KvqError):
         kvq.kvq_decode_step(g, q, kn, kn, flags=2)
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_step_host_matches_device_step(bits):
+    """kvq_decode_step_host (pinned host input block and output, one call per
+    step) on one cache and kvq_decode_step on its twin: identical cache bytes
+    after every step, both outputs within tolerance of the oracle."""
+    rng = np.random.default_rng(900 + bits)
+    B, H, d, gq, Nr, L = 2, 2, 128, 4, 16, 400
+    k = torch.from_numpy(rng.standard_normal((B, H, L, d)).astype(np.float16))
+    v = torch.from_numpy(rng.standard_normal((B, H, L, d)).astype(np.float16))
+    lens = torch.tensor([L, L - 55], dtype=torch.int32)
+    a, b = gpu_cache(B, H, d, bits, L + 16, Nr), gpu_cache(B, H, d, bits, L + 16, Nr)
+    for c in (a, b):
+        kvq.kvq_quantize_pack(c, k.to(DEV), v.to(DEV), lens.to(DEV))
+    r = ref_cache(B, H, d, bits, L + 16, Nr)
+    assert oracle.quantize_pack(r, k.numpy(), v.numpy(), lens.numpy()) == 0
+    ws_a, ws_b = kvq.workspace_for(a, H * gq), kvq.workspace_for(b, H * gq)
+    io = kvq.step_io_for(a, H * gq)
+    for _ in range(6):
+        q = rng.standard_normal((B, H * gq, d)).astype(np.float16)
+        kn = rng.standard_normal((B, H, d)).astype(np.float16)
+        vn = rng.standard_normal((B, H, d)).astype(np.float16)
+        in_h = torch.from_numpy(np.concatenate([q.ravel(), kn.ravel(), vn.ravel()])).pin_memory()
+        out_h = torch.empty((B, H * gq, d), dtype=torch.float16).pin_memory()
+        kvq.kvq_decode_step_host(a, in_h, H * gq, out_h, io, ws_a)
+        out_b = kvq.kvq_decode_step(b, torch.from_numpy(q).to(DEV), torch.from_numpy(kn).to(DEV),
+                                    torch.from_numpy(vn).to(DEV), workspace=ws_b)
+        torch.cuda.synchronize()
+        assert kvq.kvq_read_error(a)[0] == kvq.KVQ_OK
+        _assert_gpu_caches_equal(a, b)
+        assert oracle.append(r, kn, vn) == 0
+        want = oracle.decode(r, q)
+        assert_attn_close(out_h, want)
+        assert_attn_close(out_b, want)
