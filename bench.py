@@ -176,6 +176,16 @@ class ClockSampler:
 
 # ------------------------------------------------------------ our arm ------
 
+def workload_config(w, packed_tokens, extra=None):
+    """The config object of the JSON line (both arms)."""
+    cfg = {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
+           "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "bits": w.bits,
+           "packed_tokens_per_head": packed_tokens, "residual": w.residual, "group": 32,
+           "step": "kvq_decode_step: append + decode attention"}
+    cfg.update(extra or {})
+    return cfg
+
+
 def build_state(dev, steps, warmup, e2e_steps, l2_bytes, workload):
     """Pack the workload once, clone it into enough copies to exceed 3x L2,
     and pre-generate the per-step queries and new tokens on the device."""
@@ -336,13 +346,10 @@ def run_ours(args, rank, world, local):
         "vs_baseline": None,
         "dtype": "u4 codes, fp16 scale/min, fp32 accumulate",
         "data": "synthetic (seeded SplitMix64 + Box-Muller, fp16)",
-        "config": {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
-                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "bits": w.bits,
-                   "packed_tokens_per_head": st["npk0"], "residual": w.residual, "group": 32,
-                   "step": "kvq_decode_step: append + decode attention",
-                   "l2": f"rotating {ncopy} cache copies ({ncopy * step_bytes / 2**20:.0f} MiB "
-                         f"packed) > 3x L2 ({l2 / 2**20:.0f} MiB)",
-                   "timing": "CUDA graph replays, CUDA events", "parallelism": "replicas"},
+        "config": workload_config(w, st["npk0"], {
+            "l2": f"rotating {ncopy} cache copies ({ncopy * step_bytes / 2**20:.0f} MiB "
+                  f"packed) > 3x L2 ({l2 / 2**20:.0f} MiB)",
+            "timing": "CUDA graph replays, CUDA events", "parallelism": "replicas"}),
         "gpu_launches": launches * K,
         "roofline": {"bound": "hbm", "kernel": rf_kernel,
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
@@ -436,27 +443,69 @@ def cpu_baseline(seconds: float, steps: int | None = None, workload: int = WORKL
             "s_per_step": round(el / n, 4)}
 
 
+REF_SLICE = 2048  # packed tokens one reference step decodes
+
+
 def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle as it stands (single thread), W untimed
+    and then exactly K timed steps.  A step is a bounded sample of the workload:
+    the append of the step's new token (every sequence and KV head), then the
+    fp64 decode of the gq query heads of one KV head over a REF_SLICE-token slice
+    of that head's packed cache (the head and the slice rotate) -- a piece of a
+    full step, credited with the slice's packed bytes."""
     if rank != 0:
         return None
-    steps = max(1, args.steps_reference if args.steps_reference else min(args.steps, 5))
-    # warm-up: one step, untimed
-    cpu_baseline(0.0, steps=1, workload=args.workload)
-    cb = cpu_baseline(0.0, steps=steps, workload=args.workload)
+    import numpy as np
+    import oracle
     from bit_quantized_kv_pack_gb300 import synth
+
     w = synth.WORKLOADS[args.workload]
+    k, v, lens = w.prefill()
+    npk_b = [int(L) - min(int(L), w.residual) for L in lens.tolist()]
+    n_total = args.warmup + args.steps
+    r = oracle.Cache(w.batch, w.num_kv_heads, w.head_dim, w.bits, max(npk_b) + n_total + 8, w.residual)
+    oracle.quantize_pack(r, k.numpy(), v.numpy(), lens.numpy())
+    del k, v
+    per_tok = 2 * (w.head_dim * w.bits // 8 + 4 * (w.head_dim // 32))
+    gq = w.num_q_heads // w.num_kv_heads
+
+    def step(i):
+        kn, vn = w.new_tokens(i)
+        oracle.append(r, kn.numpy(), vn.numpy())
+        b, h = (i // w.num_kv_heads) % w.batch, i % w.num_kv_heads
+        lp = int(r.packed_len[b])
+        n = min(REF_SLICE, lp)
+        t0 = (i * REF_SLICE) % max(lp - n + 1, 1)
+        sl = oracle.Cache(1, 1, w.head_dim, w.bits, max(n, 1), 0)  # one KV head, gq query heads
+        for name in ("k_codes", "v_codes", "k_params", "v_params"):
+            getattr(sl, name)[0, 0, :n] = getattr(r, name)[b, h, t0:t0 + n]
+        sl.packed_len[0] = n
+        q = w.query(i).numpy()[b:b + 1, h * gq:(h + 1) * gq]
+        oracle.decode(sl, np.ascontiguousarray(q))
+        return n * per_tok
+
+    for i in range(args.warmup):
+        step(i)
+    t_start = time.perf_counter()
+    nbytes = 0
+    for i in range(args.warmup, n_total):
+        nbytes += step(i)
+    el = time.perf_counter() - t_start
+    value = nbytes / el / 1e9
+    sample = (f"{args.steps} steps, each the append of the step's token and the fp64 decode of the {gq} "
+              f"query heads of one KV head over {REF_SLICE} of its packed tokens ({w.name}); "
+              f"{el:.2f} s, single thread")
     return {
         "impl": "reference",
         "metric": "quantized-KV decode attention: achieved HBM GB/s (% of peak), us/step",
-        "value": cb["value"], "unit": "GB/s", "n_gpus": world, "steps": steps, "warmup": 1,
-        "ms_per_step": cb["s_per_step"] * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
-                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "bits": w.bits,
-                   "step": "append + decode_attention"},
-        "cpu_baseline": {"value": cb["value"], "unit": "GB/s", "cores": cb["cores"],
-                         "kind": "oracle", "sample": cb["sample"]},
-        "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+        "value": round(value, 6), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded SplitMix64 + Box-Muller, fp16)",
+        "config": workload_config(w, sum(npk_b)),
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
 
@@ -471,7 +520,6 @@ def main():
                     help="decode workload (default 2: Llama-3.1-8B INT4 32K)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--steps-reference", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
