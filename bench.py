@@ -510,14 +510,89 @@ def run_reference(args, rank, world):
     }
 
 
+def run_pack(args, rank, world, local):
+    """Standalone quantize/pack: fp16 K and V of 32768 tokens x 8 KV heads x d128
+    (4 outlier channels x10 in K) packed to INT4 and to INT2, all tokens packed
+    (no window).  Two input copies alternate so the 134 MB input is not served
+    from L2 (129 MB) between packs; each pack is timed with CUDA events around K
+    launches after W warm-ups.  value = input bytes / time (INT4)."""
+    from bit_quantized_kv_pack_gb300 import _build, kvq, synth
+    _build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peak, peak_kind = measured_peak()
+    out = {}
+    for bits in (4, 2):
+        w = synth.scaled(synth.WORKLOADS[5], bits=bits)
+        ins = []
+        for _ in range(2):
+            k, v, lens = w.prefill(device=dev)
+            ins.append((k, v, lens.to(dev)))
+        in_bytes = 2 * ins[0][0].numel() * 2
+        cache = kvq.KVCache(w.batch, w.num_kv_heads, w.head_dim, bits, w.len_max, 0, device=dev)
+        out_bytes = sum(cache.k_codes.numel() + cache.k_params.numel() * 4 for _ in range(2))
+        for i in range(args.warmup):
+            k, v, lens = ins[i % 2]
+            kvq.kvq_quantize_pack(cache, k, v, lens)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(args.steps):
+            k, v, lens = ins[i % 2]
+            kvq.kvq_quantize_pack(cache, k, v, lens)
+        b.record()
+        b.synchronize()
+        st, _ = kvq.kvq_read_error(cache)
+        if st != kvq.KVQ_OK:
+            raise RuntimeError(f"pack failed: {kvq.status_string(st)}")
+        us = a.elapsed_time(b) * 1e3 / args.steps
+        out[bits] = dict(us=us, gbs=in_bytes / (us * 1e-6) / 1e9,
+                         traffic_gbs=(in_bytes + out_bytes) / (us * 1e-6) / 1e9)
+    res = {
+        "metric": "quantize/pack throughput: input GB/s (fp16 K+V in, codes + scale/min out)",
+        "value": round(out[4]["gbs"], 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(out[4]["us"] * 1e-3, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp16 in, u4/u2 codes + fp16 scale/min out, fp32 arithmetic",
+        "data": "synthetic (seeded SplitMix64 + Box-Muller, fp16)",
+        "config": {"workload": "pack-32768x8x128-kv", "tokens": 32768, "num_kv_heads": 8,
+                   "head_dim": 128, "group": 32, "l2": "two input copies alternate",
+                   "timing": "CUDA events around K launches"},
+        "int2": {"us_per_step": round(out[2]["us"], 3), "value": round(out[2]["gbs"], 2)},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "kernel": "quantize_pack (INT4)",
+                     "achieved": round(out[4]["traffic_gbs"], 2), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(out[4]["traffic_gbs"] / peak, 4), "traffic": None,
+                     "us_per_launch": round(out[4]["us"], 3),
+                     "note": "achieved counts input + output bytes"},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        w = synth.scaled(synth.WORKLOADS[5], bits=4)
+        k, v, lens = w.prefill()
+        r = oracle.Cache(w.batch, w.num_kv_heads, w.head_dim, 4, w.len_max, 0)
+        t0 = time.perf_counter()
+        n = 0
+        while n < 1 or time.perf_counter() - t0 < min(args.cpu_seconds, 10.0):
+            oracle.quantize_pack(r, k.numpy(), v.numpy(), lens.numpy())
+            n += 1
+        el = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": round(n * 2 * k.numel() * 2 / el / 1e9, 4), "unit": "GB/s",
+                               "cores": 1, "kind": "oracle",
+                               "sample": f"{n} whole INT4 packs of the same K and V, {el:.1f} s, single thread"}
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", type=int, default=WORKLOAD, choices=(1, 2, 3, 4),
-                    help="decode workload (default 2: Llama-3.1-8B INT4 32K)")
+    ap.add_argument("--workload", type=int, default=WORKLOAD, choices=(1, 2, 3, 4, 5),
+                    help="decode workload (default 2: Llama-3.1-8B INT4 32K); 5 = the "
+                         "standalone quantize/pack throughput case (INT4 and INT2)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -528,7 +603,11 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl" if args.impl == "ours" else "gloo")
     try:
-        if args.impl == "reference":
+        if args.workload == 5:
+            res = run_pack(args, rank, world, local) if args.impl == "ours" else \
+                {"impl": "reference", "unavailable": "the pack case is not the benchmark's decode "
+                 "workload; the CPU oracle's pack time is the cpu_baseline of the ours line"}
+        elif args.impl == "reference":
             res = run_reference(args, rank, world)
         else:
             res = run_ours(args, rank, world, local)

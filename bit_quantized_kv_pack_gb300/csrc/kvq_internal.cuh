@@ -47,8 +47,9 @@ __device__ __forceinline__ void set_error(uint32_t* err_word, uint32_t bit) {
 //   Q1  min/max over the quad (local over 8, then shuffle-xor 1 and 2)
 //   Q2  scale_f = (mx - mn) / (2^b - 1) in fp32, IEEE divide
 //   Q3  scale_h = fp16_rne(scale_f); min_h = fp16(mn + 0)
-//   Q4  code = clamp(rint((x - mn) / s), 0, 2^b - 1) with s = (float)scale_h,
-//       or 0 when s == 0.
+//   Q4  code = clamp(rint((x - mn) / s), 0, 2^b - 1) with s = (float)scale_h and
+//       the IEEE divide, or 0 when s == 0 (computed through a reciprocal with
+//       the divide taken near rounding boundaries: the same codes).
 // Returns the lane's 8 codes packed little-endian (b = 4: 32 bits, b = 2: 16
 // bits) and the group's {scale, min} half2 bits.  All 32 lanes of the warp must
 // call it (the shuffles use the full mask); `active` lanes only matter for the
@@ -71,12 +72,21 @@ __device__ __forceinline__ uint32_t quantize_quad(const float (&x)[8], uint32_t&
   const __half scale_h = __float2half_rn(scale_f);
   const __half min_h = __float2half_rn(__fadd_rn(mn, 0.0f));
   const float s = __half2float(scale_h);
+  // The code is rint of the IEEE quotient (x - mn) / s.  (x - mn) * rcp(s), with
+  // the correctly rounded reciprocal, is within 3 ulp of that quotient (it is
+  // at most about 2 * (2^b - 1), so within 6e-6); only when it lies within 1e-5
+  // of a half-integer can rint tell the two apart, and there the IEEE divide
+  // itself decides.  The codes are therefore those of the plain divide.
+  const float r = s != 0.0f ? __frcp_rn(s) : 0.0f;
   uint32_t packed = 0;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     int c = 0;
     if (s != 0.0f) {
-      c = __float2int_rn(__fdiv_rn(__fsub_rn(x[j], mn), s));
+      const float dx = __fsub_rn(x[j], mn);
+      float qf = __fmul_rn(dx, r);
+      if (fabsf(qf - floorf(qf) - 0.5f) < 1e-5f) qf = __fdiv_rn(dx, s);
+      c = __float2int_rn(qf);
       c = min(max(c, 0), kQmax);
     }
     packed |= (uint32_t)c << (BITS * j);
