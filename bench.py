@@ -310,6 +310,10 @@ def run_ours(args, rank, world, local):
 
     dec_ms_per_launch = ms_dec / K
     peak, peak_kind = measured_peak()
+    # every byte a step moves: packed codes + params, the fp16 window, q and O
+    res_bytes = w.batch * w.num_kv_heads * w.residual * w.head_dim * 2 * 2
+    qo_bytes = 2 * w.batch * w.num_q_heads * w.head_dim * 2
+    all_bytes_gbs = (step_bytes + res_bytes + qo_bytes) / (ms_per_step * 1e-3) / 1e9
     # the step is one fused launch on the tensor-core path (append + decode),
     # else an append and a decode launch
     fused = w.head_dim == 128 and 1 <= w.num_q_heads // w.num_kv_heads <= 4
@@ -350,6 +354,7 @@ def run_ours(args, rank, world, local):
             "l2": f"rotating {ncopy} cache copies ({ncopy * step_bytes / 2**20:.0f} MiB "
                   f"packed) > 3x L2 ({l2 / 2**20:.0f} MiB)",
             "timing": "CUDA graph replays, CUDA events", "parallelism": "replicas"}),
+        "all_bytes_gbs": round(all_bytes_gbs, 2),
         "gpu_launches": launches * K,
         "roofline": {"bound": "hbm", "kernel": rf_kernel,
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
@@ -365,6 +370,7 @@ def run_ours(args, rank, world, local):
     }
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args.cpu_seconds, workload=args.workload)
+        res["cpu_baseline_all_cores"] = cpu_baseline_all_cores(res["cpu_baseline"], args.workload)
     return res
 
 
@@ -441,6 +447,62 @@ def cpu_baseline(seconds: float, steps: int | None = None, workload: int = WORKL
             "kind": "oracle", "sample": f"{n} whole steps (append + decode of all {w.num_q_heads} "
                                         f"query heads of {w.name}), {el:.1f} s, single thread",
             "s_per_step": round(el / n, 4)}
+
+
+def _oracle_units_worker(job):
+    """One process of the all-cores CPU baseline: whole decode steps (append +
+    fp64 decode of every query head) for its (sequence, KV head) units, each in
+    a cache of its own.  Returns the seconds of its step loop."""
+    workload, units, n_steps = job
+    import oracle
+    from bit_quantized_kv_pack_gb300 import synth
+    w = synth.WORKLOADS[workload]
+    k, v, lens = w.prefill()
+    gq = w.num_q_heads // w.num_kv_heads
+    caches = []
+    for b, h in units:
+        L = int(lens[b])
+        r = oracle.Cache(1, 1, w.head_dim, w.bits, L + n_steps + 8, w.residual)
+        oracle.quantize_pack(r, k[b:b + 1, h:h + 1].numpy().copy(), v[b:b + 1, h:h + 1].numpy().copy(),
+                             lens[b:b + 1].numpy().copy())
+        caches.append((b, h, r))
+    t0 = time.perf_counter()
+    for st in range(n_steps):
+        kn, vn = w.new_tokens(st)
+        q = w.query(st)
+        for b, h, r in caches:
+            oracle.append(r, kn[b:b + 1, h:h + 1].numpy().copy(), vn[b:b + 1, h:h + 1].numpy().copy())
+            oracle.decode(r, q[b:b + 1, h * gq:(h + 1) * gq].numpy().copy())
+    return time.perf_counter() - t0
+
+
+def cpu_baseline_all_cores(single: dict, workload: int = WORKLOAD, seconds: float = 10.0):
+    """The same oracle on all host cores: (sequence, KV head) units spread over
+    spawned processes, each running whole steps on its units; throughput = step
+    bytes x steps / the slowest process's time."""
+    import multiprocessing as mp
+    from bit_quantized_kv_pack_gb300 import synth
+    w = synth.WORKLOADS[workload]
+    units = [(b, h) for b in range(w.batch) for h in range(w.num_kv_heads)]
+    procs = max(1, min(os.cpu_count() or 1, len(units)))
+    share = [units[i::procs] for i in range(procs)]
+    per_step_one = single["s_per_step"] * max(len(x) for x in share) / len(units)
+    n_steps = max(3, int(seconds / max(per_step_one, 1e-6)))
+    from concurrent.futures import ProcessPoolExecutor
+    # spawn (never fork after CUDA); a worker that fails to start raises instead
+    # of being restarted, and a stuck one times out
+    try:
+        with ProcessPoolExecutor(max_workers=procs, mp_context=mp.get_context("spawn")) as ex:
+            futs = [ex.submit(_oracle_units_worker, (workload, sh, n_steps)) for sh in share]
+            times = [f.result(timeout=600) for f in futs]
+    except Exception as e:  # report, do not hang the benchmark
+        return {"value": None, "unit": "GB/s", "cores": procs, "kind": "oracle",
+                "sample": f"not measured: {type(e).__name__}: {e}"[:200]}
+    el = max(times)
+    step_bytes = single["value"] * 1e9 * single["s_per_step"]
+    return {"value": round(step_bytes * n_steps / el / 1e9, 6), "unit": "GB/s", "cores": procs,
+            "kind": "oracle", "sample": f"{n_steps} whole steps on {procs} processes "
+                                        f"({len(units)} (sequence, KV head) units), slowest {el:.1f} s"}
 
 
 REF_SLICE = 2048  # packed tokens one reference step decodes
