@@ -42,7 +42,7 @@ def build(force: bool = False) -> str:
 
 
 class Desc(ctypes.Structure):
-    """Cache shape; the same seven integers as the library's description."""
+    """Cache shape; the same eight integers as the library's description."""
 
     _fields_ = [
         ("batch", ctypes.c_int32),
@@ -52,6 +52,7 @@ class Desc(ctypes.Structure):
         ("group", ctypes.c_int32),
         ("capacity", ctypes.c_int32),
         ("residual", ctypes.c_int32),
+        ("sink", ctypes.c_int32),
     ]
 
 
@@ -72,13 +73,13 @@ def _load():
             lib.oracle_pack_row.argtypes = [P, ctypes.c_int, ctypes.c_int, P]
             lib.oracle_pack_row.restype = ctypes.c_int
             lib.oracle_unpack_row.argtypes = [P, ctypes.c_int, ctypes.c_int, P]
-            lib.oracle_quantize_pack.argtypes = [P, P, P, i32, P, P, P, P, P, P]
+            lib.oracle_quantize_pack.argtypes = [P, P, P, i32, P, P, P, P, P, P, P, P]
             lib.oracle_quantize_pack.restype = ctypes.c_int
             lib.oracle_append.argtypes = [P] * 11
             lib.oracle_append.restype = ctypes.c_int
-            lib.oracle_decode_pairs.argtypes = [P] * 10 + [P, i32, P, i32, P]
+            lib.oracle_decode_pairs.argtypes = [P] * 13 + [P, i32, P, i32, P]
             lib.oracle_decode_pairs.restype = ctypes.c_int
-            lib.oracle_decode.argtypes = [P] * 10 + [P, i32, P]
+            lib.oracle_decode.argtypes = [P] * 13 + [P, i32, P]
             lib.oracle_decode.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -150,8 +151,8 @@ def unpack_row(packed, d: int, bits: int) -> np.ndarray:
 class Cache:
     """Host copy of one layer's cache in the library's layout (numpy arrays)."""
 
-    def __init__(self, batch, num_kv_heads, head_dim, bits, capacity, residual):
-        self.desc = Desc(batch, num_kv_heads, head_dim, bits, 32, capacity, residual)
+    def __init__(self, batch, num_kv_heads, head_dim, bits, capacity, residual, sink=0):
+        self.desc = Desc(batch, num_kv_heads, head_dim, bits, 32, capacity, residual, sink)
         B, H, d = batch, num_kv_heads, head_dim
         rb, ng = d * bits // 8, d // 32
         self.k_codes = np.zeros((B, H, capacity, rb), np.uint8)
@@ -163,16 +164,19 @@ class Cache:
         self.packed_len = np.zeros(B, np.int32)
         self.res_len = np.zeros(B, np.int32)
         self.res_head = np.zeros(B, np.int32)
+        self.k_sink = np.zeros((B, H, max(sink, 1), d), np.uint16)  # [B][Hkv][sink][d] fp16 bits
+        self.v_sink = np.zeros((B, H, max(sink, 1), d), np.uint16)
+        self.sink_len = np.zeros(B, np.int32)
 
     @property
     def shape(self):
         D = self.desc
-        return D.batch, D.num_kv_heads, D.head_dim, D.bits, D.capacity, D.residual
+        return D.batch, D.num_kv_heads, D.head_dim, D.bits, D.capacity, D.residual, D.sink
 
     def copy(self) -> "Cache":
         c = Cache(*self.shape)
         for name in ("k_codes", "v_codes", "k_params", "v_params", "k_res", "v_res",
-                     "packed_len", "res_len", "res_head"):
+                     "packed_len", "res_len", "res_head", "k_sink", "v_sink", "sink_len"):
             getattr(c, name)[...] = getattr(self, name)
         return c
 
@@ -186,11 +190,13 @@ def quantize_pack(cache: Cache, k, v, seq_lens) -> int:
     lib = _load()
     D = ctypes.byref(cache.desc)
     e1 = lib.oracle_quantize_pack(D, _ptr(k), _ptr(seq), Lmax, _ptr(cache.k_codes),
-                                  _ptr(cache.k_params), _ptr(cache.k_res),
-                                  _ptr(cache.packed_len), _ptr(cache.res_len), _ptr(cache.res_head))
+                                  _ptr(cache.k_params), _ptr(cache.k_res), _ptr(cache.k_sink),
+                                  _ptr(cache.packed_len), _ptr(cache.res_len), _ptr(cache.res_head),
+                                  _ptr(cache.sink_len))
     e2 = lib.oracle_quantize_pack(D, _ptr(v), _ptr(seq), Lmax, _ptr(cache.v_codes),
-                                  _ptr(cache.v_params), _ptr(cache.v_res),
-                                  _ptr(cache.packed_len), _ptr(cache.res_len), _ptr(cache.res_head))
+                                  _ptr(cache.v_params), _ptr(cache.v_res), _ptr(cache.v_sink),
+                                  _ptr(cache.packed_len), _ptr(cache.res_len), _ptr(cache.res_head),
+                                  _ptr(cache.sink_len))
     if e1 < 0 or e2 < 0:
         raise ValueError("invalid cache description")
     return e1 | e2
@@ -223,8 +229,9 @@ def decode(cache: Cache, q, pairs=None) -> np.ndarray:
     B, Hq, d = q.shape
     lib = _load()
     args = [ctypes.byref(cache.desc), _ptr(cache.k_codes), _ptr(cache.k_params),
-            _ptr(cache.k_res), _ptr(cache.v_codes), _ptr(cache.v_params), _ptr(cache.v_res),
-            _ptr(cache.packed_len), _ptr(cache.res_len), _ptr(cache.res_head), _ptr(q), Hq]
+            _ptr(cache.k_res), _ptr(cache.k_sink), _ptr(cache.v_codes), _ptr(cache.v_params),
+            _ptr(cache.v_res), _ptr(cache.v_sink), _ptr(cache.packed_len), _ptr(cache.res_len),
+            _ptr(cache.res_head), _ptr(cache.sink_len), _ptr(q), Hq]
     if pairs is None:
         out = np.zeros((B, Hq, d), np.float64)
         rc = lib.oracle_decode(*args, _ptr(out))

@@ -16,7 +16,8 @@
  *   Pack (Q5): codes as a little-endian bit string, 32 consecutive head_dim
  *     values per group (InnerQ page, section 3.2); params as half2 {scale, min}.
  *   Residual split (Q6): the last min(Nr, L) tokens stay fp16 (BitDecoding page,
- *     section 2.2).
+ *     section 2.2); with an attention-sink window the first min(sink, L) tokens
+ *     stay fp16 too, fixed after the prefill (InnerQ page, section 2.3).
  *   Append (Q7): sliding recent window, the oldest token is quantized when the
  *     window is full (InnerQ page, section 2.3).
  *   Decode (D1-D4): dequantize min + code * scale (InnerQ page, section 3.1),
@@ -204,25 +205,31 @@ static void quantize_token(const uint16_t* src, int d, int bits, uint8_t* code_r
 
 /* Shapes of one cache, mirroring the library's description. */
 typedef struct {
-  int32_t batch, num_kv_heads, head_dim, bits, group, capacity, residual;
+  int32_t batch, num_kv_heads, head_dim, bits, group, capacity, residual, sink;
 } oracle_desc;
 
 static int desc_ok(const oracle_desc* D) {
   return D && D->batch >= 1 && D->num_kv_heads >= 1 && D->head_dim >= 32 && D->head_dim <= 256 &&
          D->head_dim % 32 == 0 && (D->bits == 2 || D->bits == 4) && D->group == 32 &&
-         D->capacity >= 0 && D->residual >= 0 && D->residual <= 1024;
+         D->capacity >= 0 && D->residual >= 0 && D->residual <= 1024 && D->sink >= 0 &&
+         D->sink <= 256;
 }
 
 /* Q1-Q6 over a whole prefill for one of K or V.
  *   x         fp16 [B][Hkv][Lmax][d]
- *   codes     [B][Hkv][cap][d*b/8]; params [B][Hkv][cap][Ng]; res [B][Hkv][Nr][d]
- *   packed_len, res_len, res_head  [B] outputs.
+ *   codes     [B][Hkv][cap][d*b/8]; params [B][Hkv][cap][Ng]; res [B][Hkv][Nr][d];
+ *   sink_rows [B][Hkv][sink][d] (may be NULL when sink == 0)
+ *   packed_len, res_len, res_head, sink_len  [B] outputs.
+ * With an attention-sink window (InnerQ page, section 2.3), the first
+ * min(sink, L) tokens are kept verbatim in sink_rows and the rest is split as
+ * without one: the last min(Nr, rest) go to the residual, the others are packed.
  * Returns a bit set: 1 = a sequence passed the capacity, 8 = a bad length. */
 int oracle_quantize_pack(const oracle_desc* D, const uint16_t* x, const int32_t* seq_lens,
                          int32_t Lmax, uint8_t* codes, uint32_t* params, uint16_t* res,
-                         int32_t* packed_len, int32_t* res_len, int32_t* res_head) {
+                         uint16_t* sink_rows, int32_t* packed_len, int32_t* res_len,
+                         int32_t* res_head, int32_t* sink_len) {
   if (!desc_ok(D)) return -1;
-  const int d = D->head_dim, Ng = d / 32, rb = d * D->bits / 8, Nr = D->residual;
+  const int d = D->head_dim, Ng = d / 32, rb = d * D->bits / 8, Nr = D->residual, S = D->sink;
   const int64_t cap = D->capacity;
   int err = 0;
   for (int b = 0; b < D->batch; ++b) {
@@ -231,8 +238,10 @@ int oracle_quantize_pack(const oracle_desc* D, const uint16_t* x, const int32_t*
       err |= 8;
       continue;
     }
-    int32_t nres = L < Nr ? L : Nr;
-    int32_t npk = L - nres;
+    int32_t ns = L < S ? L : S;
+    int32_t rest = L - ns;
+    int32_t nres = rest < Nr ? rest : Nr;
+    int32_t npk = rest - nres;
     if (npk > cap) {
       err |= 1;
       npk = (int32_t)cap;
@@ -240,8 +249,10 @@ int oracle_quantize_pack(const oracle_desc* D, const uint16_t* x, const int32_t*
     for (int h = 0; h < D->num_kv_heads; ++h) {
       int64_t bh = (int64_t)b * D->num_kv_heads + h;
       const uint16_t* src = x + bh * Lmax * d;
+      for (int32_t j = 0; j < ns; ++j)
+        memcpy(sink_rows + (bh * S + j) * d, src + (int64_t)j * d, (size_t)d * sizeof(uint16_t));
       for (int32_t t = 0; t < npk; ++t)
-        quantize_token(src + (int64_t)t * d, d, D->bits, codes + (bh * cap + t) * rb,
+        quantize_token(src + (int64_t)(ns + t) * d, d, D->bits, codes + (bh * cap + t) * rb,
                        params + (bh * cap + t) * Ng);
       for (int32_t j = 0; j < nres; ++j)
         memcpy(res + (bh * Nr + j) * d, src + (int64_t)(L - nres + j) * d,
@@ -250,6 +261,7 @@ int oracle_quantize_pack(const oracle_desc* D, const uint16_t* x, const int32_t*
     packed_len[b] = npk;
     res_len[b] = nres;
     res_head[b] = 0;
+    sink_len[b] = ns;
   }
   return err;
 }
@@ -326,20 +338,25 @@ static void dequant_rows(const uint8_t* code_rows, const uint32_t* param_rows, i
   }
 }
 
-/* Gather the dequantized keys or values of (b, h): packed tokens first, then the
- * residual ring in age order.  Returns the token count; *rows is malloc'ed. */
+/* Gather the keys or values of (b, h) as doubles: the sink rows (fp16), the
+ * packed tokens (dequantized), then the residual ring in age order.  Returns
+ * the token count; *rows is malloc'ed. */
 static int64_t gather_kv(const oracle_desc* D, const uint8_t* codes, const uint32_t* params,
-                         const uint16_t* res, int32_t pl, int32_t rl, int32_t rh, int b, int h,
-                         double** rows) {
-  const int d = D->head_dim, Ng = d / 32, rb = d * D->bits / 8, Nr = D->residual;
+                         const uint16_t* res, const uint16_t* sink_rows, int32_t sl, int32_t pl,
+                         int32_t rl, int32_t rh, int b, int h, double** rows) {
+  const int d = D->head_dim, Ng = d / 32, rb = d * D->bits / 8, Nr = D->residual, S = D->sink;
   const int64_t cap = D->capacity;
-  int64_t n = (int64_t)pl + rl;
+  int64_t n = (int64_t)sl + pl + rl;
   double* x = (double*)malloc((size_t)(n > 0 ? n : 1) * d * sizeof(double));
   int64_t bh = (int64_t)b * D->num_kv_heads + h;
-  dequant_rows(codes + bh * cap * rb, params + bh * cap * Ng, pl, d, D->bits, x);
+  for (int32_t j = 0; j < sl; ++j) {
+    const uint16_t* src = sink_rows + (bh * S + j) * d;
+    for (int e = 0; e < d; ++e) x[(int64_t)j * d + e] = oracle_f16_to_f64(src[e]);
+  }
+  dequant_rows(codes + bh * cap * rb, params + bh * cap * Ng, pl, d, D->bits, x + (int64_t)sl * d);
   for (int32_t j = 0; j < rl; ++j) {
     const uint16_t* src = res + (bh * Nr + (rh + j) % Nr) * d;
-    for (int e = 0; e < d; ++e) x[(pl + j) * d + e] = oracle_f16_to_f64(src[e]);
+    for (int e = 0; e < d; ++e) x[((int64_t)sl + pl + j) * d + e] = oracle_f16_to_f64(src[e]);
   }
   *rows = x;
   return n;
@@ -372,10 +389,11 @@ static void attend(const double* q, const double* K, const double* V, int64_t n,
 /* Decode for a list of (b, hq) pairs (pairs[2i], pairs[2i+1]); out [npairs][d] double.
  * q is fp16 [B][Hq][d].  A sequence with no tokens gives zeros. */
 int oracle_decode_pairs(const oracle_desc* D, const uint8_t* k_codes, const uint32_t* k_params,
-                        const uint16_t* k_res, const uint8_t* v_codes, const uint32_t* v_params,
-                        const uint16_t* v_res, const int32_t* packed_len, const int32_t* res_len,
-                        const int32_t* res_head, const uint16_t* q, int32_t num_q_heads,
-                        const int32_t* pairs, int32_t npairs, double* out) {
+                        const uint16_t* k_res, const uint16_t* k_sink, const uint8_t* v_codes,
+                        const uint32_t* v_params, const uint16_t* v_res, const uint16_t* v_sink,
+                        const int32_t* packed_len, const int32_t* res_len,
+                        const int32_t* res_head, const int32_t* sink_len, const uint16_t* q,
+                        int32_t num_q_heads, const int32_t* pairs, int32_t npairs, double* out) {
   if (!desc_ok(D) || num_q_heads < 1 || num_q_heads % D->num_kv_heads) return -1;
   const int d = D->head_dim;
   const int gq = num_q_heads / D->num_kv_heads;
@@ -390,8 +408,10 @@ int oracle_decode_pairs(const oracle_desc* D, const uint8_t* k_codes, const uint
     if (b != cached_b || h != cached_h) {
       free(K);
       free(V);
-      n = gather_kv(D, k_codes, k_params, k_res, packed_len[b], res_len[b], res_head[b], b, h, &K);
-      gather_kv(D, v_codes, v_params, v_res, packed_len[b], res_len[b], res_head[b], b, h, &V);
+      n = gather_kv(D, k_codes, k_params, k_res, k_sink, sink_len[b], packed_len[b], res_len[b],
+                    res_head[b], b, h, &K);
+      gather_kv(D, v_codes, v_params, v_res, v_sink, sink_len[b], packed_len[b], res_len[b],
+                res_head[b], b, h, &V);
       cached_b = b;
       cached_h = h;
     }
@@ -405,9 +425,10 @@ int oracle_decode_pairs(const oracle_desc* D, const uint8_t* k_codes, const uint
 
 /* Decode for every (b, hq): out [B][Hq][d] double. */
 int oracle_decode(const oracle_desc* D, const uint8_t* k_codes, const uint32_t* k_params,
-                  const uint16_t* k_res, const uint8_t* v_codes, const uint32_t* v_params,
-                  const uint16_t* v_res, const int32_t* packed_len, const int32_t* res_len,
-                  const int32_t* res_head, const uint16_t* q, int32_t num_q_heads, double* out) {
+                  const uint16_t* k_res, const uint16_t* k_sink, const uint8_t* v_codes,
+                  const uint32_t* v_params, const uint16_t* v_res, const uint16_t* v_sink,
+                  const int32_t* packed_len, const int32_t* res_len, const int32_t* res_head,
+                  const int32_t* sink_len, const uint16_t* q, int32_t num_q_heads, double* out) {
   if (!desc_ok(D) || num_q_heads < 1 || num_q_heads % D->num_kv_heads) return -1;
   int32_t np = D->batch * num_q_heads;
   int32_t* pairs = (int32_t*)malloc((size_t)np * 2 * sizeof(int32_t));
@@ -416,8 +437,9 @@ int oracle_decode(const oracle_desc* D, const uint8_t* k_codes, const uint32_t* 
       pairs[2 * (b * num_q_heads + hq)] = b;
       pairs[2 * (b * num_q_heads + hq) + 1] = hq;
     }
-  int rc = oracle_decode_pairs(D, k_codes, k_params, k_res, v_codes, v_params, v_res, packed_len,
-                               res_len, res_head, q, num_q_heads, pairs, np, out);
+  int rc = oracle_decode_pairs(D, k_codes, k_params, k_res, k_sink, v_codes, v_params, v_res,
+                               v_sink, packed_len, res_len, res_head, sink_len, q, num_q_heads,
+                               pairs, np, out);
   free(pairs);
   return rc;
 }

@@ -7,7 +7,11 @@
     q = 0 -> the mean), textbook attention (scipy softmax on the fp16 inputs)
     where dequantization is exact (on-grid data, residual-only sequences), a
     second numpy formulation of dequantize-then-attend with its own unpacking,
-    GQA head mapping, and invariance under rotation of the residual ring.
+    GQA head mapping, and invariance under rotation of the residual ring,
+  - the attention-sink window: the first min(sink, L) tokens verbatim, the rest
+    split exactly as a cache without a sink splits tokens [sink:], sink-only
+    sequences are textbook attention, the second formulation with the sink rows
+    in front, and appends that never touch the sink.
 """
 
 import numpy as np
@@ -30,6 +34,8 @@ def _textbook(q, K, V):
 
 def _numpy_dequant(codes, params, d, bits):
     """Second reading of D1: unpack with numpy bit ops and apply min + c * scale."""
+    if codes.shape[0] == 0:
+        return np.zeros((0, d))
     bitstr = np.unpackbits(codes.reshape(codes.shape[0], -1), axis=1, bitorder="little")
     c = (bitstr.reshape(codes.shape[0], d, bits) * (1 << np.arange(bits))).sum(-1)
     scale = (params & 0xFFFF).astype(np.uint16).view(np.float16).astype(np.float64)
@@ -37,13 +43,13 @@ def _numpy_dequant(codes, params, d, bits):
     return mn[:, np.arange(d) // 32] + c * scale[:, np.arange(d) // 32]
 
 
-def _build(rng, B=2, H=2, d=64, bits=4, L=40, Nr=8, cap=None, lens=None, kscale=1.0):
+def _build(rng, B=2, H=2, d=64, bits=4, L=40, Nr=8, cap=None, lens=None, kscale=1.0, sink=0):
     lens = np.array(lens if lens is not None else [L] * B, np.int32)
     Lmax = int(lens.max())
     cap = cap if cap is not None else Lmax
     k = _f16(rng, (B, H, Lmax, d), kscale)
     v = _f16(rng, (B, H, Lmax, d))
-    c = oracle.Cache(B, H, d, bits, cap, Nr)
+    c = oracle.Cache(B, H, d, bits, cap, Nr, sink)
     err = oracle.quantize_pack(c, k, v, lens)
     return c, k, v, lens, err
 
@@ -226,3 +232,108 @@ def test_empty_sequence_gives_zeros():
     c = oracle.Cache(1, 1, 64, 4, 4, 4)
     out = oracle.decode(c, np.ones((1, 1, 64), np.float16))
     assert np.all(out == 0)
+
+
+# ---------------------------------------------------------- attention sink --
+
+
+@pytest.mark.parametrize("L,Nr,S", [(40, 8, 4), (10, 8, 4), (3, 8, 4), (4, 0, 4), (33, 0, 32), (0, 4, 4)])
+def test_sink_split(L, Nr, S):
+    """The sink holds tokens [0, min(S, L)) verbatim; everything after is laid
+    out byte for byte as a sink-free cache lays out the prefill without them."""
+    rng = np.random.default_rng(L * 7 + Nr + S)
+    B, H, d = 2, 2, 64
+    lens = np.array([L, max(L - 2, 0)], np.int32)
+    c, k, v, lens, err = _build(rng, B=B, H=H, d=d, Nr=Nr, cap=max(L, 1), lens=lens, sink=S)
+    assert err == 0
+    for b in range(B):
+        ns = min(S, int(lens[b]))
+        assert c.sink_len[b] == ns
+        assert np.array_equal(c.k_sink[b, :, :ns], k[b, :, :ns].view(np.uint16))
+        assert np.array_equal(c.v_sink[b, :, :ns], v[b, :, :ns].view(np.uint16))
+        rest = int(lens[b]) - ns
+        ref = oracle.Cache(1, H, d, 4, max(L, 1), Nr)
+        kr = k[b:b + 1, :, ns:].copy()
+        vr = v[b:b + 1, :, ns:].copy()
+        assert oracle.quantize_pack(ref, kr, vr, np.array([rest], np.int32)) == 0
+        assert c.packed_len[b] == ref.packed_len[0] and c.res_len[b] == ref.res_len[0]
+        npk = ref.packed_len[0]
+        for name in ("k_codes", "v_codes", "k_params", "v_params"):
+            assert np.array_equal(getattr(c, name)[b, :, :npk], getattr(ref, name)[0, :, :npk]), name
+        for name in ("k_res", "v_res"):
+            assert np.array_equal(getattr(c, name)[b, :, :ref.res_len[0]],
+                                  getattr(ref, name)[0, :, :ref.res_len[0]]), name
+
+
+def test_sink_bounds_rejected():
+    with pytest.raises(ValueError):
+        oracle.quantize_pack(oracle.Cache(1, 1, 64, 4, 4, 4, 257), np.zeros((1, 1, 1, 64), np.float16),
+                             np.zeros((1, 1, 1, 64), np.float16), np.array([1], np.int32))
+
+
+@pytest.mark.parametrize("L,Nr", [(5, 0), (9, 4), (32, 0)])
+def test_sink_only_is_textbook_attention(L, Nr):
+    """With nothing packed (L <= sink + Nr) every token is fp16: the output is
+    textbook attention over the inputs themselves."""
+    rng = np.random.default_rng(70 + L + Nr)
+    c, k, v, lens, _ = _build(rng, B=2, H=1, d=64, L=L, Nr=Nr, sink=32 if L == 32 else 5)
+    assert np.all(c.packed_len == 0)
+    q = _f16(rng, (2, 1, 64))
+    out = oracle.decode(c, q)
+    for b in range(2):
+        assert np.allclose(out[b, 0], _textbook(q[b, 0], k[b, 0], v[b, 0]), rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("bits,S,lens", [(4, 4, [20, 3]), (2, 32, [50, 40]), (4, 1, [9, 0])])
+def test_sink_second_formulation(bits, S, lens):
+    """Sink rows (fp16), then the packed tokens unpacked by numpy, then the ring:
+    textbook attention over that sequence equals the oracle's decode."""
+    rng = np.random.default_rng(bits + S + sum(lens))
+    B, H, d, gq, Nr = 2, 2, 64, 2, 3
+    c, k, v, lens, _ = _build(rng, B=B, H=H, d=d, bits=bits, Nr=Nr, lens=lens, kscale=4.0, sink=S)
+    q = _f16(rng, (B, H * gq, d))
+    out = oracle.decode(c, q)
+    for b in range(B):
+        L = int(lens[b])
+        if L == 0:
+            assert np.all(out[b] == 0)
+            continue
+        ns = min(S, L)
+        nres = min(Nr, L - ns)
+        npk = L - ns - nres
+        for hq in range(H * gq):
+            h = hq // gq
+            K = np.concatenate([k[b, h, :ns].astype(np.float64),
+                                _numpy_dequant(c.k_codes[b, h, :npk], c.k_params[b, h, :npk], d, bits),
+                                k[b, h, L - nres:L].astype(np.float64)])
+            V = np.concatenate([v[b, h, :ns].astype(np.float64),
+                                _numpy_dequant(c.v_codes[b, h, :npk], c.v_params[b, h, :npk], d, bits),
+                                v[b, h, L - nres:L].astype(np.float64)])
+            assert np.allclose(out[b, hq], _textbook(q[b, hq], K, V), rtol=1e-12, atol=1e-13)
+
+
+def test_sink_fixed_after_prefill():
+    """Appends go to the recent window and the packed cache only: the sink rows
+    and sink_len never change, also for a sequence whose sink is not full; past
+    a full sink, append equals a prefill of the same tokens."""
+    rng = np.random.default_rng(80)
+    B, H, d, S, Nr, L0, L = 2, 2, 64, 6, 4, 8, 30
+    k = _f16(rng, (B, H, L, d), 3.0)
+    v = _f16(rng, (B, H, L, d))
+    inc = oracle.Cache(B, H, d, 4, L, Nr, S)
+    assert oracle.quantize_pack(inc, k[:, :, :L0].copy(), v[:, :, :L0].copy(),
+                                np.array([L0, 2], np.int32)) == 0
+    before = inc.copy()
+    for t in range(L0, L):
+        assert oracle.append(inc, k[:, :, t].copy(), v[:, :, t].copy()) == 0
+    for name in ("k_sink", "v_sink", "sink_len"):
+        assert np.array_equal(getattr(inc, name), getattr(before, name)), name
+    assert list(inc.sink_len) == [S, 2]
+    full = oracle.Cache(1, H, d, 4, L, Nr, S)
+    assert oracle.quantize_pack(full, k[:1], v[:1], np.array([L], np.int32)) == 0
+    npk = full.packed_len[0]
+    assert inc.packed_len[0] == npk and inc.res_len[0] == full.res_len[0]
+    for name in ("k_codes", "v_codes", "k_params", "v_params"):
+        assert np.array_equal(getattr(inc, name)[0, :, :npk], getattr(full, name)[0, :, :npk]), name
+    q = _f16(rng, (B, H, d))
+    assert np.allclose(oracle.decode(inc, q)[:1], oracle.decode(full, q[:1]), rtol=1e-12, atol=1e-14)
