@@ -176,6 +176,16 @@ class ClockSampler:
 
 # ------------------------------------------------------------ our arm ------
 
+def packed_per_seq(w, lens, sink=0):
+    """Packed tokens of each sequence after the prefill: its length minus the
+    sink rows and the fp16 window."""
+    out = []
+    for L in lens.tolist():
+        ns = min(int(L), sink)
+        out.append(int(L) - ns - min(int(L) - ns, w.residual))
+    return out
+
+
 def workload_config(w, packed_tokens, extra=None):
     """The config object of the JSON line (both arms)."""
     cfg = {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
@@ -186,24 +196,25 @@ def workload_config(w, packed_tokens, extra=None):
     return cfg
 
 
-def build_state(dev, steps, warmup, e2e_steps, l2_bytes, workload):
+def build_state(dev, steps, warmup, e2e_steps, l2_bytes, workload, sink=0):
     """Pack the workload once, clone it into enough copies to exceed 3x L2,
     and pre-generate the per-step queries and new tokens on the device."""
     from bit_quantized_kv_pack_gb300 import kvq, synth
 
     w = synth.WORKLOADS[workload]
     k, v, lens = w.prefill(device=dev)
-    npk_b = [int(L) - min(int(L), w.residual) for L in lens.tolist()]
+    npk_b = packed_per_seq(w, lens, sink)
     npk0 = sum(npk_b)  # packed tokens over the batch, per KV head
     per_tok = 2 * (w.head_dim * w.bits // 8 + 4 * (w.head_dim // 32))
     step_bytes0 = npk0 * w.num_kv_heads * per_tok
-    res_bytes = w.batch * w.num_kv_heads * w.residual * w.head_dim * 2 * 2
+    res_bytes = w.batch * w.num_kv_heads * (w.residual + sink) * w.head_dim * 2 * 2
     ncopy = max(2, math.ceil(3 * l2_bytes / (step_bytes0 + res_bytes)))
     # appends each copy sees: warm-up and timed graph passes, then the e2e loop
     appends = (math.ceil(warmup / ncopy) + math.ceil(steps / ncopy)
                + math.ceil((ncopy + max(ncopy, e2e_steps)) / ncopy) + 2)
     cap = max(npk_b) + appends + 8
-    base = kvq.KVCache(w.batch, w.num_kv_heads, w.head_dim, w.bits, cap, w.residual, device=dev)
+    base = kvq.KVCache(w.batch, w.num_kv_heads, w.head_dim, w.bits, cap, w.residual, device=dev,
+                       sink=sink)
     kvq.kvq_quantize_pack(base, k, v, lens.to(dev))
     st, word = kvq.kvq_read_error(base)
     if st != kvq.KVQ_OK:
@@ -211,8 +222,10 @@ def build_state(dev, steps, warmup, e2e_steps, l2_bytes, workload):
     del k, v
     copies = [base]
     for _ in range(ncopy - 1):
-        c = kvq.KVCache(w.batch, w.num_kv_heads, w.head_dim, w.bits, cap, w.residual, device=dev)
-        for name in ("k_codes", "v_codes", "k_params", "v_params", "k_res", "v_res", "counters"):
+        c = kvq.KVCache(w.batch, w.num_kv_heads, w.head_dim, w.bits, cap, w.residual, device=dev,
+                        sink=sink)
+        for name in ("k_codes", "v_codes", "k_params", "v_params", "k_res", "v_res", "k_sink",
+                     "v_sink", "counters"):
             getattr(c, name).copy_(getattr(base, name))
         copies.append(c)
     nslot = ncopy  # one graph = one pass over the copies
@@ -272,7 +285,7 @@ def run_ours(args, rank, world, local):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
 
-    st = build_state(dev, args.steps, args.warmup, args.e2e_steps, l2, args.workload)
+    st = build_state(dev, args.steps, args.warmup, args.e2e_steps, l2, args.workload, args.sink)
     w, ncopy = st["w"], st["nslot"]
     K = args.steps
     reps, rem = divmod(K, ncopy)  # K steps = reps whole passes over the copies + rem
@@ -310,8 +323,8 @@ def run_ours(args, rank, world, local):
 
     dec_ms_per_launch = ms_dec / K
     peak, peak_kind = measured_peak()
-    # every byte a step moves: packed codes + params, the fp16 window, q and O
-    res_bytes = w.batch * w.num_kv_heads * w.residual * w.head_dim * 2 * 2
+    # every byte a step moves: packed codes + params, the fp16 window and sink, q and O
+    res_bytes = w.batch * w.num_kv_heads * (w.residual + args.sink) * w.head_dim * 2 * 2
     qo_bytes = 2 * w.batch * w.num_q_heads * w.head_dim * 2
     all_bytes_gbs = (step_bytes + res_bytes + qo_bytes) / (ms_per_step * 1e-3) / 1e9
     # the step is one fused launch on the tensor-core path (append + decode),
@@ -353,13 +366,14 @@ def run_ours(args, rank, world, local):
         "config": workload_config(w, st["npk0"], {
             "l2": f"rotating {ncopy} cache copies ({ncopy * step_bytes / 2**20:.0f} MiB "
                   f"packed) > 3x L2 ({l2 / 2**20:.0f} MiB)",
-            "timing": "CUDA graph replays, CUDA events", "parallelism": "replicas"}),
+            "timing": "CUDA graph replays, CUDA events", "parallelism": "replicas",
+            **({"sink": args.sink} if args.sink else {})}),
         "all_bytes_gbs": round(all_bytes_gbs, 2),
         "gpu_launches": launches * K,
         "roofline": {"bound": "hbm", "kernel": rf_kernel,
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": profiled_traffic(w.name, fused),
+                     "traffic": profiled_traffic(w.name, fused) if args.sink == 0 else None,
                      "algorithmic_bytes_per_launch": step_bytes,
                      "us_per_launch": round(rf_us, 3)},
         "decode_only": {"us_per_launch": round(dec_ms_per_launch * 1e3, 3),
@@ -369,8 +383,9 @@ def run_ours(args, rank, world, local):
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(args.cpu_seconds, workload=args.workload)
-        res["cpu_baseline_all_cores"] = cpu_baseline_all_cores(res["cpu_baseline"], args.workload)
+        res["cpu_baseline"] = cpu_baseline(args.cpu_seconds, workload=args.workload, sink=args.sink)
+        res["cpu_baseline_all_cores"] = cpu_baseline_all_cores(res["cpu_baseline"], args.workload,
+                                                               sink=args.sink)
     return res
 
 
@@ -415,7 +430,7 @@ def run_e2e(st, args):
 
 # ---------------------------------------------------------- oracle arm -----
 
-def cpu_baseline(seconds: float, steps: int | None = None, workload: int = WORKLOAD):
+def cpu_baseline(seconds: float, steps: int | None = None, workload: int = WORKLOAD, sink: int = 0):
     """The CPU oracle as it stands (single thread) on whole steps of the same
     workload: append + fp64 decode of every query head."""
     import oracle
@@ -423,11 +438,11 @@ def cpu_baseline(seconds: float, steps: int | None = None, workload: int = WORKL
 
     w = synth.WORKLOADS[workload]
     k, v, lens = w.prefill()
-    npk_b = [int(L) - min(int(L), w.residual) for L in lens.tolist()]
+    npk_b = packed_per_seq(w, lens, sink)
     npk0 = sum(npk_b)
     n_steps_max = steps if steps is not None else 1000
     r = oracle.Cache(w.batch, w.num_kv_heads, w.head_dim, w.bits, max(npk_b) + n_steps_max + 8,
-                     w.residual)
+                     w.residual, sink)
     oracle.quantize_pack(r, k.numpy(), v.numpy(), lens.numpy())
     del k, v
     per_tok = 2 * (w.head_dim * w.bits // 8 + 4 * (w.head_dim // 32))
@@ -453,7 +468,7 @@ def _oracle_units_worker(job):
     """One process of the all-cores CPU baseline: whole decode steps (append +
     fp64 decode of every query head) for its (sequence, KV head) units, each in
     a cache of its own.  Returns the seconds of its step loop."""
-    workload, units, n_steps = job
+    workload, units, n_steps, sink = job
     import oracle
     from bit_quantized_kv_pack_gb300 import synth
     w = synth.WORKLOADS[workload]
@@ -462,7 +477,7 @@ def _oracle_units_worker(job):
     caches = []
     for b, h in units:
         L = int(lens[b])
-        r = oracle.Cache(1, 1, w.head_dim, w.bits, L + n_steps + 8, w.residual)
+        r = oracle.Cache(1, 1, w.head_dim, w.bits, L + n_steps + 8, w.residual, sink)
         oracle.quantize_pack(r, k[b:b + 1, h:h + 1].numpy().copy(), v[b:b + 1, h:h + 1].numpy().copy(),
                              lens[b:b + 1].numpy().copy())
         caches.append((b, h, r))
@@ -476,7 +491,8 @@ def _oracle_units_worker(job):
     return time.perf_counter() - t0
 
 
-def cpu_baseline_all_cores(single: dict, workload: int = WORKLOAD, seconds: float = 10.0):
+def cpu_baseline_all_cores(single: dict, workload: int = WORKLOAD, seconds: float = 10.0,
+                           sink: int = 0):
     """The same oracle on all host cores: (sequence, KV head) units spread over
     spawned processes, each running whole steps on its units; throughput = step
     bytes x steps / the slowest process's time."""
@@ -493,7 +509,7 @@ def cpu_baseline_all_cores(single: dict, workload: int = WORKLOAD, seconds: floa
     # of being restarted, and a stuck one times out
     try:
         with ProcessPoolExecutor(max_workers=procs, mp_context=mp.get_context("spawn")) as ex:
-            futs = [ex.submit(_oracle_units_worker, (workload, sh, n_steps)) for sh in share]
+            futs = [ex.submit(_oracle_units_worker, (workload, sh, n_steps, sink)) for sh in share]
             times = [f.result(timeout=600) for f in futs]
     except Exception as e:  # report, do not hang the benchmark
         return {"value": None, "unit": "GB/s", "cores": procs, "kind": "oracle",
@@ -523,9 +539,10 @@ def run_reference(args, rank, world):
 
     w = synth.WORKLOADS[args.workload]
     k, v, lens = w.prefill()
-    npk_b = [int(L) - min(int(L), w.residual) for L in lens.tolist()]
+    npk_b = packed_per_seq(w, lens, args.sink)
     n_total = args.warmup + args.steps
-    r = oracle.Cache(w.batch, w.num_kv_heads, w.head_dim, w.bits, max(npk_b) + n_total + 8, w.residual)
+    r = oracle.Cache(w.batch, w.num_kv_heads, w.head_dim, w.bits, max(npk_b) + n_total + 8, w.residual,
+                     args.sink)
     oracle.quantize_pack(r, k.numpy(), v.numpy(), lens.numpy())
     del k, v
     per_tok = 2 * (w.head_dim * w.bits // 8 + 4 * (w.head_dim // 32))
@@ -564,7 +581,7 @@ def run_reference(args, rank, world):
         "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded SplitMix64 + Box-Muller, fp16)",
-        "config": workload_config(w, sum(npk_b)),
+        "config": workload_config(w, sum(npk_b), {"sink": args.sink} if args.sink else None),
         "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -655,6 +672,8 @@ def main():
     ap.add_argument("--workload", type=int, default=WORKLOAD, choices=(1, 2, 3, 4, 5),
                     help="decode workload (default 2: Llama-3.1-8B INT4 32K); 5 = the "
                          "standalone quantize/pack throughput case (INT4 and INT2)")
+    ap.add_argument("--sink", type=int, default=0,
+                    help="attention-sink rows kept fp16 per sequence (0..256; default 0)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

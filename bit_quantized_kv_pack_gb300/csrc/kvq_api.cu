@@ -18,7 +18,8 @@ kvq_status check_desc(const kvq_cache_desc* D) {
   if (D->bits != 2 && D->bits != 4) return KVQ_ERR_UNSUPPORTED;
   if (D->head_dim != 32 && D->head_dim != 64 && D->head_dim != 128 && D->head_dim != 256)
     return KVQ_ERR_UNSUPPORTED;
-  if (D->residual > 1024) return KVQ_ERR_UNSUPPORTED;
+  if (D->sink < 0) return KVQ_ERR_INVALID_ARG;
+  if (D->residual > 1024 || D->sink > 256) return KVQ_ERR_UNSUPPORTED;
   if ((int64_t)D->batch * D->num_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
 }
@@ -29,16 +30,20 @@ kvq_status check_view(const kvq_cache_desc& D, const kvq_cache_view* v) {
   if (D.capacity > 0 && (!v->k_codes || !v->v_codes || !v->k_params || !v->v_params))
     return KVQ_ERR_INVALID_ARG;
   if (D.residual > 0 && (!v->k_res || !v->v_res)) return KVQ_ERR_INVALID_ARG;
-  const void* a16[] = {v->k_codes, v->v_codes, v->k_params, v->v_params, v->k_res, v->v_res};
+  if (D.sink > 0 && (!v->k_sink || !v->v_sink || !v->sink_len)) return KVQ_ERR_INVALID_ARG;
+  const void* a16[] = {v->k_codes, v->v_codes, v->k_params, v->v_params,
+                       v->k_res,   v->v_res,   v->k_sink,   v->v_sink};
   for (const void* p : a16)
     if (!aligned(p, 16)) return KVQ_ERR_MISALIGNED;
-  const void* a4[] = {v->packed_len, v->res_len, v->res_head, v->err_word};
+  const void* a4[] = {v->packed_len, v->res_len, v->res_head, v->err_word, v->sink_len};
   for (const void* p : a4)
     if (!aligned(p, 4)) return KVQ_ERR_MISALIGNED;
   return KVQ_OK;
 }
 
 kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
+
+constexpr uint32_t kStepFlags = KVQ_STEP_EARLY_CACHE_READ | KVQ_OUT_F32;
 
 }  // namespace
 
@@ -52,6 +57,7 @@ size_t kvq_cache_bytes(const kvq_cache_desc* desc, int which) {
     case KVQ_ARRAY_CODES: return rows * (size_t)s.cap * s.row_bytes;
     case KVQ_ARRAY_PARAMS: return rows * (size_t)s.cap * s.Ng * sizeof(uint32_t);
     case KVQ_ARRAY_RESIDUAL: return rows * (size_t)s.Nr * s.d * sizeof(uint16_t);
+    case KVQ_ARRAY_SINK: return rows * (size_t)s.Ns * s.d * sizeof(uint16_t);
     default: return 0;
   }
 }
@@ -91,11 +97,12 @@ kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache_view* view, co
 
 kvq_status kvq_decode_attention(const kvq_cache_desc* desc, const kvq_cache_view* view,
                                 const void* q, int32_t num_q_heads, void* out, void* workspace,
-                                size_t ws_bytes, void* stream) {
+                                size_t ws_bytes, uint32_t flags, void* stream) {
   kvq_status st = check_desc(desc);
   if (st != KVQ_OK) return st;
   if ((st = check_view(*desc, view)) != KVQ_OK) return st;
-  if (!q || !out || !workspace || num_q_heads < 1 || num_q_heads % desc->num_kv_heads)
+  if (!q || !out || !workspace || num_q_heads < 1 || num_q_heads % desc->num_kv_heads ||
+      (flags & ~(uint32_t)KVQ_OUT_F32))
     return KVQ_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 16)) return KVQ_ERR_MISALIGNED;
   if ((int64_t)desc->batch * num_q_heads > 2147483647LL) return KVQ_ERR_UNSUPPORTED;
@@ -103,9 +110,9 @@ kvq_status kvq_decode_attention(const kvq_cache_desc* desc, const kvq_cache_view
   if ((int64_t)desc->num_kv_heads * p.nqb > 65535) return KVQ_ERR_UNSUPPORTED;
   if (ws_bytes < p.ws_total) return KVQ_ERR_INVALID_ARG;
   const Dims s = kvq::dims_of(*desc);
-  return from_cuda(kvq::launch_decode(s, p, *view, static_cast<const __half*>(q), num_q_heads,
-                                      static_cast<__half*>(out), workspace,
-                                      static_cast<cudaStream_t>(stream)));
+  return from_cuda(kvq::launch_decode(s, p, *view, static_cast<const __half*>(q), num_q_heads, out,
+                                      workspace, static_cast<cudaStream_t>(stream), nullptr,
+                                      nullptr, flags));
 }
 
 kvq_status kvq_decode_step(const kvq_cache_desc* desc, const kvq_cache_view* view, const void* q,
@@ -115,7 +122,7 @@ kvq_status kvq_decode_step(const kvq_cache_desc* desc, const kvq_cache_view* vie
   if (st != KVQ_OK) return st;
   if ((st = check_view(*desc, view)) != KVQ_OK) return st;
   if (!q || !out || !workspace || !k_new || !v_new || num_q_heads < 1 ||
-      num_q_heads % desc->num_kv_heads || (flags & ~(uint32_t)KVQ_STEP_EARLY_CACHE_READ))
+      num_q_heads % desc->num_kv_heads || (flags & ~kStepFlags))
     return KVQ_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 16) || !aligned(k_new, 16) ||
       !aligned(v_new, 16))
@@ -125,9 +132,8 @@ kvq_status kvq_decode_step(const kvq_cache_desc* desc, const kvq_cache_view* vie
   if ((int64_t)desc->num_kv_heads * p.nqb > 65535) return KVQ_ERR_UNSUPPORTED;
   if (ws_bytes < p.ws_total) return KVQ_ERR_INVALID_ARG;
   const Dims s = kvq::dims_of(*desc);
-  return from_cuda(kvq::launch_decode(s, p, *view, static_cast<const __half*>(q), num_q_heads,
-                                      static_cast<__half*>(out), workspace,
-                                      static_cast<cudaStream_t>(stream),
+  return from_cuda(kvq::launch_decode(s, p, *view, static_cast<const __half*>(q), num_q_heads, out,
+                                      workspace, static_cast<cudaStream_t>(stream),
                                       static_cast<const __half*>(k_new),
                                       static_cast<const __half*>(v_new), flags));
 }
@@ -144,7 +150,7 @@ StepIo step_io(const kvq_cache_desc& D, int32_t num_q_heads) {
   io.kv = (size_t)D.batch * D.num_kv_heads * D.head_dim * sizeof(uint16_t);
   io.in_bytes = io.q + 2 * io.kv;
   io.out_off = (io.in_bytes + 255) & ~(size_t)255;
-  io.total = io.out_off + io.q;
+  io.total = io.out_off + 2 * io.q;  // room for an fp32 out
   return io;
 }
 }  // namespace
@@ -170,15 +176,15 @@ kvq_status kvq_decode_step_host(const kvq_cache_desc* desc, const kvq_cache_view
   // every argument the step itself checks is checked before anything is enqueued
   const kvq::DecodePlan p = kvq::plan_decode(*desc, num_q_heads, kvq::device_sm_count(), true);
   if ((st = check_view(*desc, view)) != KVQ_OK) return st;
-  if (!workspace || ws_bytes < p.ws_total || (flags & ~(uint32_t)KVQ_STEP_EARLY_CACHE_READ))
-    return KVQ_ERR_INVALID_ARG;
+  if (!workspace || ws_bytes < p.ws_total || (flags & ~kStepFlags)) return KVQ_ERR_INVALID_ARG;
   if (!aligned(workspace, 16)) return KVQ_ERR_MISALIGNED;
   if (cudaMemcpyAsync(d, in_host, io.in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return KVQ_ERR_CUDA;
   st = kvq_decode_step(desc, view, d, num_q_heads, d + io.q, d + io.q + io.kv, d + io.out_off,
                        workspace, ws_bytes, flags, stream);
   if (st != KVQ_OK) return st;
-  if (cudaMemcpyAsync(out_host, d + io.out_off, io.q, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+  const size_t out_bytes = (flags & KVQ_OUT_F32) ? 2 * io.q : io.q;
+  if (cudaMemcpyAsync(out_host, d + io.out_off, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return KVQ_ERR_CUDA;
   return KVQ_OK;
 }
@@ -214,6 +220,6 @@ const char* kvq_status_string(kvq_status status) {
   }
 }
 
-int32_t kvq_version(void) { return 100; }
+int32_t kvq_version(void) { return 110; }
 
 }  // extern "C"

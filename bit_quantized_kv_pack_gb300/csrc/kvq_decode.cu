@@ -47,7 +47,7 @@ DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count, b
     min_tokens = 256;
   }
   const int64_t units = (int64_t)D.batch * D.num_kv_heads * p.nqb;
-  const int64_t tokens_max = (int64_t)D.capacity + D.residual;
+  const int64_t tokens_max = (int64_t)D.capacity + D.residual + D.sink;
   // one CTA per unit short of a full wave: the previous launch's last CTA of
   // each unit (its merger) still holds a slot when this launch starts
   if (p.kernel == 1 && units * 4 <= target) target -= units;
@@ -59,11 +59,11 @@ DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count, b
   p.splits = (int)S;
   p.splits_packed = p.splits;
   if (p.kernel == 1) {
-    // the fp16 residual tokens get splits of their own, one per block of
-    // tc_residual_rows() ring slots (at least one in a fused step: it takes the
-    // appended token)
+    // the fp16 tokens (window ring slots, then sink rows) get splits of their
+    // own, one per tc_residual_rows() rows (at least one in a fused step: it
+    // takes the appended token)
     const int rr = tc_residual_rows();
-    int sr = (D.residual + rr - 1) / rr;
+    int sr = (D.residual + D.sink + rr - 1) / rr;
     if (step && sr < 1) sr = 1;
     const int sp = (int)S - sr > 1 ? (int)S - sr : 1;
     p.splits_packed = sp;
@@ -85,9 +85,8 @@ DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count, b
 }
 
 cudaError_t launch_decode(const Dims& s, const DecodePlan& p, const kvq_cache_view& v,
-                          const __half* q, int Hq, __half* out, void* workspace,
-                          cudaStream_t st, const __half* k_new, const __half* v_new,
-                          uint32_t step_flags) {
+                          const __half* q, int Hq, void* out, void* workspace, cudaStream_t st,
+                          const __half* k_new, const __half* v_new, uint32_t flags) {
   DecodeArgs a;
   a.k_codes = v.k_codes;
   a.v_codes = v.v_codes;
@@ -99,8 +98,12 @@ cudaError_t launch_decode(const Dims& s, const DecodePlan& p, const kvq_cache_vi
   a.res_len = v.res_len;
   a.res_head = v.res_head;
   a.err_word = v.err_word;
+  a.k_sink = reinterpret_cast<const __half*>(v.k_sink);
+  a.v_sink = reinterpret_cast<const __half*>(v.v_sink);
+  a.sink_len = v.sink_len;
   a.q = q;
   a.out = out;
+  a.out_f32 = (flags & KVQ_OUT_F32) ? 1 : 0;
   char* ws = reinterpret_cast<char*>(workspace);
   a.o_part = reinterpret_cast<float*>(ws + p.ws_part_off);
   a.ml_part = reinterpret_cast<float2*>(ws + p.ws_ml_off);
@@ -129,11 +132,12 @@ cudaError_t launch_decode(const Dims& s, const DecodePlan& p, const kvq_cache_vi
   a.nqb = p.nqb;
   a.S = p.splits;
   a.Sp = p.splits_packed;
+  a.Ns = s.Ns;
   a.cap = s.cap;
   a.Nr = s.Nr;
   a.d = s.d;
   a.row_bytes = s.row_bytes;
-  a.early = (step_flags & KVQ_STEP_EARLY_CACHE_READ) ? 1 : 0;
+  a.early = (flags & KVQ_STEP_EARLY_CACHE_READ) ? 1 : 0;
   a.qk_scale_log2 = (float)(1.4426950408889634 / sqrt((double)s.d));
   const bool step = k_new != nullptr;
   if (p.kernel == 1) return launch_decode_tc(s, p, a, st, step);

@@ -21,8 +21,12 @@ struct DecodeArgs {
   const int32_t* res_len;
   const int32_t* res_head;
   uint32_t* err_word;
+  const __half* k_sink;  // [B][Hkv][Ns][d] (attention-sink window)
+  const __half* v_sink;
+  const int32_t* sink_len;
   const __half* q;  // [B][Hq][d]
-  __half* out;      // [B][Hq][d]
+  void* out;        // [B][Hq][d], fp16 or (out_f32) fp32
+  int out_f32;
   float* o_part;
   float2* ml_part;
   uint32_t* counters;     // [B][Hkv][nqb] arrival tickets, zero between calls
@@ -43,8 +47,9 @@ struct DecodeArgs {
   int32_t* w_res_len;
   int32_t* w_res_head;
   int Hkv, Hq, gq, qb, nqb, S, cap, Nr, d, row_bytes;
+  int Ns;  // sink rows per (sequence, KV head) in the layout (0: no sink)
   int early;  // fused step: counters and first tiles may be read before griddepcontrol.wait
-  int Sp;  // tensor-core kernel: splits s < Sp take packed tokens, s >= Sp residual ones
+  int Sp;  // tensor-core kernel: splits s < Sp take packed tokens, s >= Sp fp16 ones
   float qk_scale_log2;  // log2(e) / sqrt(d)
 };
 
@@ -67,6 +72,18 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 __device__ __forceinline__ int64_t ceil_div64(int64_t x, int64_t y) { return (x + y - 1) / y; }
+
+// Four consecutive output values starting at element `idx` of out (a multiple of
+// four), rounded once to the output type.
+__device__ __forceinline__ void store_out4(const DecodeArgs& a, int64_t idx, float4 o) {
+  if (a.out_f32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(a.out) + idx) = o;
+  } else {
+    __half2* dst = reinterpret_cast<__half2*>(static_cast<__half*>(a.out) + idx);
+    dst[0] = __floats2half2_rn(o.x, o.y);
+    dst[1] = __floats2half2_rn(o.z, o.w);
+  }
+}
 
 // Token range of split s of S over Lp packed tokens (cost cp bytes each) followed
 // by Lr residual tokens (cost cr each): the tokens whose byte offset in that
@@ -162,10 +179,8 @@ __device__ __forceinline__ void combine_unit(const DecodeArgs& a, int b, int h, 
   auto finish = [&](int i, int e4, float4 acc) {
     const float L = Lq[i];
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    __half2* dst = reinterpret_cast<__half2*>(
-        a.out + ((int64_t)b * a.Hq + h * a.gq + qbi * qb + i) * D + 4 * e4);
-    dst[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
-    dst[1] = __floats2half2_rn(acc.z * inv, acc.w * inv);
+    store_out4(a, ((int64_t)b * a.Hq + h * a.gq + qbi * qb + i) * D + 4 * e4,
+               make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
   };
   // the first output: its first CH partials are already in registers
   if (has0) {

@@ -2,8 +2,9 @@
 // in {32, 64, 128, 256}, any GQA ratio).
 //
 // Computes O = softmax(q K^T / sqrt(d)) V for every query head over the packed
-// tokens, dequantized as min + code * scale (InnerQ page, section 3.1), and the
-// fp16 residual window (BitDecoding page, section 2.2).  One CTA serves all query
+// tokens, dequantized as min + code * scale (InnerQ page, section 3.1), the
+// fp16 residual window (BitDecoding page, section 2.2) and the fp16
+// attention-sink rows (InnerQ page, section 2.3).  One CTA serves all query
 // heads of a KV head block, so the cache is read once per block of up to 8
 // query heads (the GQA regrouping of the BitDecoding page, section 2.3).
 //
@@ -12,8 +13,9 @@
 // so the inner loop multiplies integer codes by q in fp32.
 //
 // Split-KV: each (sequence, KV head, query block) is cut into S pieces of about
-// equal byte cost (a packed token costs its code and param bytes, a residual
-// token its fp16 bytes, both for K and V); each CTA writes a partial (o, m, l)
+// equal byte cost (a packed token costs its code and param bytes, an fp16 token
+// -- sink rows first, then the window in age order -- its fp16 bytes, both for
+// K and V); each CTA writes a partial (o, m, l)
 // and the last one to finish merges the S partials (combine_unit).
 #include <math.h>
 
@@ -50,6 +52,8 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(DecodeArgs a) 
   const int Lp = a.packed_len[b];
   const int Lr = a.res_len[b];
   const int rh = a.res_head[b];
+  const int Ls = a.Ns > 0 ? a.sink_len[b] : 0;
+  const int Lf = Ls + Lr;  // fp16 tokens: sink rows, then the window
 
   for (int idx = threadIdx.x; idx < QB * D; idx += kThreads) {
     const int i = idx / D, e = idx % D;
@@ -66,10 +70,10 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(DecodeArgs a) 
     qsum_s[i][g] = sum;
   }
   __syncthreads();
-  if (s == 0 && qbi == 0 && Lp + Lr == 0 && threadIdx.x == 0) set_error(a.err_word, KVQ_ERRBIT_EMPTY);
+  if (s == 0 && qbi == 0 && Lp + Lf == 0 && threadIdx.x == 0) set_error(a.err_word, KVQ_ERRBIT_EMPTY);
 
   int i0, i1, j0, j1;
-  split_range(Lp, Lr, s, a.S, 2 * (RB + 4 * NG), 4 * D, i0, i1, j0, j1);
+  split_range(Lp, Lf, s, a.S, 2 * (RB + 4 * NG), 4 * D, i0, i1, j0, j1);
 
   float m[QB], l[QB], o[QB][DPL];
 #pragma unroll
@@ -80,6 +84,10 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(DecodeArgs a) 
     for (int j = 0; j < DPL; ++j) o[i][j] = 0.f;
   }
   const int64_t bh = (int64_t)b * a.Hkv + h;
+  // fp16 token j: sink row j, or window token j - Ls (ring slot (rh + j - Ls) % Nr)
+  auto fp16_row = [&](const __half* sink, const __half* res, int j) {
+    return j < Ls ? sink + (bh * a.Ns + j) * D : res + (bh * a.Nr + (rh + j - Ls) % a.Nr) * D;
+  };
 
   // Online softmax over one chunk of up to 32 tokens (lane = token), given the
   // lane's raw scores; returns p per query for the lane's token.
@@ -160,7 +168,7 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(DecodeArgs a) 
     }
   }
 
-  // ---- residual tokens (ring slot (res_head + j) % Nr)
+  // ---- fp16 tokens (sink rows, then ring slots (res_head + j - Ls) % Nr)
   for (int base = j0 + warp * 32; base < j1; base += kThreads) {
     const int j = base + lane;
     const bool valid = j < j1;
@@ -168,7 +176,7 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(DecodeArgs a) 
 #pragma unroll
     for (int i = 0; i < QB; ++i) sc[i] = 0.f;
     if (valid) {
-      const __half* krow = a.k_res + (bh * a.Nr + (rh + j) % a.Nr) * D;
+      const __half* krow = fp16_row(a.k_sink, a.k_res, j);
       for (int e0 = 0; e0 < D; e0 += 8) {
         float x[8];
         unpack8_f16(*reinterpret_cast<const uint4*>(krow + e0), x);
@@ -182,7 +190,7 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(DecodeArgs a) 
     softmax_chunk(valid, sc, p);
     const int nvalid = min(32, j1 - base);
     for (int tt = 0; tt < nvalid; ++tt) {
-      const __half* vrow = a.v_res + (bh * a.Nr + (rh + base + tt) % a.Nr) * D + lane * DPL;
+      const __half* vrow = fp16_row(a.v_sink, a.v_res, base + tt) + lane * DPL;
 #pragma unroll
       for (int i = 0; i < QB; ++i) {
         const float pt = __shfl_sync(0xffffffffu, p[i], tt);

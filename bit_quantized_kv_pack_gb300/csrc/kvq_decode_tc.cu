@@ -35,8 +35,10 @@
 //    p * scale of that group, so one MMA serves two groups and each thread
 //    again holds one query.  A ninth MMA accumulates sum p * min_g and sum p
 //    (= l), so O = O_c + sum_g p min_g.
-//  * The fp16 residual tokens get splits of their own (CUDA cores, all loads of
-//    a chunk in one round), so no packed split waits on them.
+//  * The fp16 tokens -- the residual window, then the attention-sink rows
+//    (InnerQ page section 2.3) -- get splits of their own, 64 rows each (all
+//    loads of a split in one round, tensor cores), so no packed split waits on
+//    them.
 //  * Per-warp states merge in shared memory.  The first split of a KV head to
 //    finish its first tile sets the head's reference max per query (atomicCAS);
 //    every split adds its (o, l), scaled to that reference, into the head's fp32
@@ -265,9 +267,9 @@ __device__ __forceinline__ void pv_subtile(uint32_t vc, const uint32_t* vp, int 
 
 // ---------------------------------------------------------- residual ----
 
-// Residual split: ring slots [c0, c0 + kResRows) of (sequence, KV head) bh, fp16,
-// on the tensor cores.  A slot takes part when its age (slot - ring head, mod
-// Nr) lies in [age0, age1); only those rows are copied (zero-filled otherwise),
+// fp16 split: rows [c0, c0 + kResRows) of the fp16 rows of one (sequence, KV
+// head) (F16Rows), on the tensor cores.  Only the rows that take part are
+// copied (zero-filled otherwise),
 // so no stale bytes of unused slots enter the arithmetic.  Rows are padded to
 // 272 bytes, which makes every ldmatrix conflict-free.  Warp w takes rows
 // 16w .. 16w+15 as one sub-tile: S^T = K q^T (query columns duplicated, so each
@@ -276,37 +278,56 @@ __device__ __forceinline__ void pv_subtile(uint32_t vc, const uint32_t* vp, int 
 constexpr int kResRows = 64;
 constexpr int kResStride = D * 2 + 16;  // bytes per row in shared memory
 
-__device__ __forceinline__ bool residual_valid(int slot, int Nr, int rh, int age0, int age1) {
-  if (slot >= Nr) return false;
-  int age = slot - rh;
-  if (age < 0) age += Nr;
-  return age >= age0 && age < age1;
-}
+// The fp16 rows of one (sequence, KV head) as one index space: row j < Nr is
+// slot j of the window ring, which takes part when its age (slot - ring head,
+// mod Nr) lies in [age0, age1); row j >= Nr is sink row j - Nr, which takes part
+// below sink_len.  Attention does not depend on the order of its tokens.
+struct F16Rows {
+  const __half* k_ring;  // this head's Nr window rows
+  const __half* v_ring;
+  const __half* k_sink;  // this head's Ns sink rows
+  const __half* v_sink;
+  int Nr, rh, age0, age1, ls;
+
+  __device__ __forceinline__ bool valid(int j) const {
+    if (j < Nr) {
+      int age = j - rh;
+      if (age < 0) age += Nr;
+      return age >= age0 && age < age1;
+    }
+    return j - Nr < ls;
+  }
+  // row j of K (arr 0) or V (arr 1); an invalid j gives an in-bounds row that
+  // is never read (its copy is zero-filled)
+  __device__ __forceinline__ const __half* row(int arr, int j) const {
+    const __half* ring = arr ? v_ring : k_ring;
+    const __half* sink = arr ? v_sink : k_sink;
+    if (!valid(j)) return Nr > 0 ? ring : sink;
+    return j < Nr ? ring + (int64_t)j * D : sink + (int64_t)(j - Nr) * D;
+  }
+};
 
 // Start the copies of the valid rows: K to rows 0..63, V to rows 64..127.
-__device__ __forceinline__ void residual_issue(const DecodeArgs& a, int64_t bh, int rh, int age0,
-                                               int age1, int c0, uint8_t* tiles) {
-  const int Nr = a.Nr;
+__device__ __forceinline__ void residual_issue(const F16Rows& fr, int c0, uint8_t* tiles) {
   const uint32_t tbase = ptx::smem_u32(tiles);
   for (int idx = threadIdx.x; idx < 2 * kResRows * (D / 8); idx += NTHREADS) {
     const int arr = idx / (kResRows * (D / 8));
     const int rem = idx % (kResRows * (D / 8));
     const int row = rem / (D / 8), chunk = rem % (D / 8);
-    const int slot = c0 + row;
-    const bool ok = residual_valid(slot, Nr, rh, age0, age1);
-    const __half* src = (arr ? a.v_res : a.k_res) + (bh * Nr + (ok ? slot : 0)) * D + chunk * 8;
+    const int j = c0 + row;
+    const __half* src = fr.row(arr, j) + chunk * 8;
+    const bool ok = fr.valid(j);
     ptx::cp_async_16(tbase + (arr * kResRows + row) * kResStride + chunk * 16, src, ok ? 16u : 0u);
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
 // Wait for the copies, then attend (every thread of the CTA calls it).
-__device__ __forceinline__ void residual_tc(const DecodeArgs& a, int rh, int age0, int age1,
-                                            int c0, uint8_t* tiles, int warp, int lane,
-                                            const float (&q_s)[QB][D], float kq, MergeSmem& ms) {
+__device__ __forceinline__ void residual_tc(const F16Rows& fr, int c0, uint8_t* tiles, int warp,
+                                            int lane, const float (&q_s)[QB][D], float kq,
+                                            MergeSmem& ms) {
   const int g = lane >> 2, t = lane & 3;
-  const int Nr = a.Nr;
-  auto valid_slot = [&](int slot) { return residual_valid(slot, Nr, rh, age0, age1); };
+  auto valid_slot = [&](int j) { return fr.valid(j); };
   const uint32_t tbase = ptx::smem_u32(tiles);
   asm volatile("cp.async.wait_group 0;" ::: "memory");
   __syncthreads();
@@ -365,8 +386,9 @@ __device__ __forceinline__ void residual_tc(const DecodeArgs& a, int rh, int age
 // --------------------------------------------------------------- kernel ----
 
 // Grid (S, Hkv, B): split s < Sp streams packed tokens of (sequence b, KV head h)
-// on the tensor cores; splits s >= Sp take the fp16 residual tokens.  Every
-// split writes a partial (o, m, l); the last one of the head merges them.
+// on the tensor cores; splits s >= Sp take 64 fp16 rows each (window ring slots,
+// then sink rows).  Every split writes a partial (o, m, l); the last one of the
+// head merges them.
 //
 // STEP: the same launch first appends one token per (sequence, KV head), as
 // kvq_append does, and attends over the cache as it is after the append.  The
@@ -392,7 +414,7 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
   __shared__ int s_last_tile[NSTAGE];  // last tile issued into each stage (-1: none)
   __shared__ float q_s[QB][D];
   __shared__ float qsum_s[QB][NG];  // sum of q over each group
-  __shared__ int s_rng[6];  // range lo, hi, ring head, step flags, packed_len, res_len
+  __shared__ int s_rng[7];  // range lo, hi, ring head, step flags, packed_len, res_len, sink_len
   __shared__ volatile int s_abort;
   __shared__ int s_last;
   __shared__ uint32_t s_ref[QB];  // the head's reference max per query (float bits + 1; 0: unknown)
@@ -404,8 +426,24 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;  // MMA group id
   const int t = lane & 3;   // thread in group
-  const bool res_cta = s >= a.Sp;
+  const bool res_cta = s >= a.Sp;  // an fp16 split: window and sink rows
   const int64_t bh = (int64_t)b * a.Hkv + h;
+  const int f0 = kResRows * (s - a.Sp);  // an fp16 split's first row
+  const bool has_f16 = a.Nr + a.Ns > 0;
+  // the fp16 rows of this (sequence, KV head), ranges from the counters
+  auto f16_rows = [&]() {
+    F16Rows fr;
+    fr.k_ring = a.k_res + bh * a.Nr * D;
+    fr.v_ring = a.v_res + bh * a.Nr * D;
+    fr.k_sink = a.k_sink + bh * a.Ns * D;
+    fr.v_sink = a.v_sink + bh * a.Ns * D;
+    fr.Nr = a.Nr;
+    fr.rh = s_rng[2];
+    fr.age0 = s_rng[0];
+    fr.age1 = s_rng[1];
+    fr.ls = s_rng[6];
+    return fr;
+  };
 
   // Prologue that touches no global memory; the rest waits for the grid this
   // launch depends on (the append of the same step) to complete.
@@ -454,6 +492,7 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
     const bool pack_now = a.Nr == 0 || Lr == a.Nr;
     const bool full = STEP && pack_now && Lp >= a.cap;
     const bool adds = STEP && !full;
+    const int Ls = a.Ns > 0 ? a.sink_len[b] : 0;
     int r0_, r1_, xflags = 0;
     if (!res_cta) {
       r0_ = (int)((int64_t)Lp * s / a.Sp);
@@ -470,11 +509,12 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
     }
     s_rng[0] = r0_;
     s_rng[1] = r1_;
-    s_rng[2] = a.res_head[b];
+    s_rng[2] = a.res_head[b];  // every split: the last one to finish commits the step
     s_rng[3] = xflags;
     s_rng[4] = Lp;
     s_rng[5] = Lr;
-    if (s == 0 && Lp + Lr == 0 && !adds) err_bits |= KVQ_ERRBIT_EMPTY;
+    s_rng[6] = Ls;
+    if (s == 0 && Lp + Lr + Ls == 0 && !adds) err_bits |= KVQ_ERRBIT_EMPTY;
     if (full && s == 0 && h == 0) err_bits |= KVQ_ERRBIT_CAPACITY;
     if (!res_cta) {
       i0 = r0_;
@@ -489,9 +529,9 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
   // are read before waiting for that kernel; q and the new token never are.
   const bool early = STEP && a.early != 0;
   if (early && threadIdx.x == 0) plan();
-  if (early && res_cta && a.Nr > 0) {  // the window rows too (CTA-uniform branch)
+  if (early && res_cta && has_f16) {  // the fp16 rows too (CTA-uniform branch)
     __syncthreads();
-    residual_issue(a, bh, s_rng[2], s_rng[0], s_rng[1], kResRows * (s - a.Sp), smem + kResTilesOff);
+    residual_issue(f16_rows(), f0, smem + kResTilesOff);
   }
   grid_dependency_wait();
 
@@ -519,8 +559,7 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
   const float kq = a.qk_scale_log2;
   MergeSmem& ms = *reinterpret_cast<MergeSmem*>(smem);
 
-  if (!early && res_cta && a.Nr > 0)
-    residual_issue(a, bh, s_rng[2], s_rng[0], s_rng[1], kResRows * (s - a.Sp), smem + kResTilesOff);
+  if (!early && res_cta && has_f16) residual_issue(f16_rows(), f0, smem + kResTilesOff);
 
   // extra tokens of a fused step, fp32: [K, V][new token, packed token][D]
   float* xbuf = reinterpret_cast<float*>(smem + sizeof(MergeSmem));
@@ -570,12 +609,11 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
   }
 
   if (res_cta) {
-    // ------------------------------------------------ residual-token split
+    // ------------------------------------------------ fp16-token split
     uint8_t* tiles = smem + kResTilesOff;
-    const int c0 = kResRows * (s - a.Sp);
-    if (a.Nr > 0) {
-      residual_tc(a, s_rng[2], s_rng[0], s_rng[1], c0, tiles, warp, lane, q_s, kq, ms);
-    } else {  // no window (the split only takes a fused step's packed token)
+    if (has_f16) {
+      residual_tc(f16_rows(), f0, tiles, warp, lane, q_s, kq, ms);
+    } else {  // no fp16 rows (the split only takes a fused step's packed token)
       __syncthreads();  // warp 1's V row of the extra token is staged
       if (lane < QB) {
         ms.m[warp][lane] = -INFINITY;
@@ -929,9 +967,8 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
       const float4 o = __ldcg(reinterpret_cast<const float4*>(oacc));
       const float L = __ldcg(&a.l_acc[bh * QB + i]);
       const float inv = L > 0.f ? 1.f / L : 0.f;
-      __half2* dst = reinterpret_cast<__half2*>(a.out + ((int64_t)b * a.Hq + h * a.gq + i) * D + e);
-      dst[0] = __floats2half2_rn(o.x * inv, o.y * inv);
-      dst[1] = __floats2half2_rn(o.z * inv, o.w * inv);
+      store_out4(a, ((int64_t)b * a.Hq + h * a.gq + i) * D + e,
+                 make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv));
     }
     // leave the head's accumulators, reference and flag at zero for the next call
     *reinterpret_cast<float4*>(oacc) = make_float4(0.f, 0.f, 0.f, 0.f);

@@ -16,6 +16,7 @@ constexpr int kGroup = 32;  // G: values per quantization group along head_dim
 
 struct Dims {
   int B, Hkv, d, bits, cap, Nr;
+  int Ns;        // attention-sink window length (0: none)
   int Ng;        // groups per token row
   int row_bytes; // packed code bytes per token row
 };
@@ -28,6 +29,7 @@ inline Dims dims_of(const kvq_cache_desc& D) {
   s.bits = D.bits;
   s.cap = D.capacity;
   s.Nr = D.residual;
+  s.Ns = D.sink;
   s.Ng = D.head_dim / kGroup;
   s.row_bytes = D.head_dim * D.bits / 8;
   return s;
@@ -147,10 +149,10 @@ cudaError_t launch_quantize_pack(const Dims& s, const kvq_cache_view& v, const _
                                  cudaStream_t st);
 cudaError_t launch_append(const Dims& s, const kvq_cache_view& v, const __half* k_new,
                           const __half* v_new, cudaStream_t st);
-// k_new/v_new non-null: the fused step (append, then attend).
+// k_new/v_new non-null: the fused step (append, then attend).  out is fp16, or
+// fp32 with KVQ_OUT_F32 in flags.
 cudaError_t launch_decode(const Dims& s, const DecodePlan& p, const kvq_cache_view& v,
-                          const __half* q, int Hq, __half* out, void* workspace,
-                          cudaStream_t st, const __half* k_new = nullptr,
-                          const __half* v_new = nullptr, uint32_t step_flags = 0);
+                          const __half* q, int Hq, void* out, void* workspace, cudaStream_t st,
+                          const __half* k_new, const __half* v_new, uint32_t flags);
 
 }  // namespace kvq

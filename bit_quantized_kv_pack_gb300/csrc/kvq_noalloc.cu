@@ -13,7 +13,11 @@
 // device address is looked up once per device with cudaGetSymbolAddress, with
 // that device current, on the first call there, which also clears the array
 // once (its arrival counters must start at zero; every completed call leaves
-// them at zero again); make that first call before any stream capture.  Two
+// them at zero again); make that first call before any stream capture.  The
+// counters and accumulators that must be zero sit at offsets that depend on the
+// cache shape and head count, so a call whose shape differs from the previous
+// call's on the device first clears that part of the array (cudaMemsetAsync on
+// its stream; the first call after a shape change is then two operations).  Two
 // calls whose kernels overlap on the GPU race on the array: issue them on one
 // stream, or order the streams.
 #include <mutex>
@@ -27,6 +31,18 @@ static __device__ __align__(256) unsigned char g_decode_scratch[KVQ_NOALLOC_SCRA
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {nullptr};
+
+// Shape of the zero-between-calls part of the array as the last call on each
+// device left it (every completed call leaves that part zero for its own shape).
+struct ZeroLayout {
+  int32_t batch, num_kv_heads, head_dim, qb, nqb;
+  bool operator==(const ZeroLayout& o) const {
+    return batch == o.batch && num_kv_heads == o.num_kv_heads && head_dim == o.head_dim &&
+           qb == o.qb && nqb == o.nqb;
+  }
+};
+ZeroLayout g_last_layout[kMaxDevices];
+bool g_has_layout[kMaxDevices] = {false};
 
 // Device address of g_decode_scratch on the current device (set up once).
 kvq_status scratch_address(void** out) {
@@ -51,7 +67,8 @@ kvq_status scratch_address(void** out) {
 
 extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_cache_desc* desc,
                                                    const kvq_cache_view* view, const void* q,
-                                                   int32_t num_q_heads, void* out, void* stream) {
+                                                   int32_t num_q_heads, void* out, uint32_t flags,
+                                                   void* stream) {
   // Sizes are checked first so an oversized request fails without touching the device.
   const size_t need = kvq_decode_workspace_bytes(desc, num_q_heads);
   if (need == 0) return KVQ_ERR_INVALID_ARG;  // invalid description or head count
@@ -59,6 +76,20 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_cache_desc* desc,
   void* scratch = nullptr;
   kvq_status st = scratch_address(&scratch);
   if (st != KVQ_OK) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  const kvq::DecodePlan p = kvq::plan_decode(*desc, num_q_heads, kvq::device_sm_count());
+  const ZeroLayout lay = {desc->batch, desc->num_kv_heads, desc->head_dim, p.qb, p.nqb};
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_has_layout[dev] || !(g_last_layout[dev] == lay)) {
+      // everything before the partials: tickets, reference maxima, flags, accumulators
+      if (cudaMemsetAsync(scratch, 0, p.ws_ml_off, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+      g_last_layout[dev] = lay;
+      g_has_layout[dev] = true;
+    }
+  }
   return kvq_decode_attention(desc, view, q, num_q_heads, out, scratch,
-                              (size_t)KVQ_NOALLOC_SCRATCH_BYTES, stream);
+                              (size_t)KVQ_NOALLOC_SCRATCH_BYTES, flags, stream);
 }

@@ -6,8 +6,10 @@
 // (InnerQ page, section 2.1).  Kernel shape: per-thread min/max over its values,
 // a shuffle-xor reduction inside the group, codes packed in registers and
 // written straight out (BitDecoding page, section 3.1).  Residual split: the
-// last min(Nr, L) tokens stay fp16 (BitDecoding page, section 2.2); append
-// follows the sliding recent window (InnerQ page, section 2.3).
+// last min(Nr, L) tokens stay fp16 (BitDecoding page, section 2.2), and so do
+// the first min(S, L) with an attention-sink window; append follows the sliding
+// recent window and leaves the sink as the prefill set it (InnerQ page,
+// section 2.3).
 //
 // Thread mapping.  The tokens of one (sequence, KV head) are contiguous rows of
 // d fp16 values, so its groups are contiguous 64-byte pieces of memory, and so
@@ -31,12 +33,14 @@ struct PackArgs {
   uint8_t* codes[2];     // [B][Hkv][cap][row_bytes]
   uint32_t* params[2];   // [B][Hkv][cap][Ng]
   __half* res[2];        // [B][Hkv][Nr][d]
+  __half* sink[2];       // [B][Hkv][Ns][d]
   const int32_t* seq_lens;
   int32_t* packed_len;
   int32_t* res_len;
   int32_t* res_head;
+  int32_t* sink_len;
   uint32_t* err_word;
-  int Hkv, d, Ng, row_bytes, cap, Nr, Lmax;
+  int Hkv, d, Ng, row_bytes, cap, Nr, Ns, Lmax;
 };
 
 template <int BITS>
@@ -46,14 +50,17 @@ __global__ void __launch_bounds__(kPackThreads) quantize_pack_kernel(PackArgs a)
   const int b = bh / a.Hkv;
   const int L = a.seq_lens[b];
   const bool bad = (L < 0 || L > a.Lmax);
-  const int nres = bad ? 0 : min(L, a.Nr);
-  const int npk_all = bad ? 0 : L - nres;
+  // tokens [0, ns) -> sink, [ns, ns + npk) -> packed, the last nres -> window
+  const int ns = bad ? 0 : min(L, a.Ns);
+  const int nres = bad ? 0 : min(L - ns, a.Nr);
+  const int npk_all = bad ? 0 : L - ns - nres;
   const int npk = min(npk_all, a.cap);
 
   if (which == 0 && blockIdx.x == 0 && (bh % a.Hkv) == 0 && threadIdx.x == 0) {
     a.packed_len[b] = npk;
     a.res_len[b] = nres;
     a.res_head[b] = 0;
+    if (a.Ns > 0) a.sink_len[b] = ns;
     if (bad) set_error(a.err_word, KVQ_ERRBIT_BADLEN);
     if (npk_all > a.cap) set_error(a.err_word, KVQ_ERRBIT_CAPACITY);
   }
@@ -88,16 +95,19 @@ __global__ void __launch_bounds__(kPackThreads) quantize_pack_kernel(PackArgs a)
     uint32_t prm;
     const uint32_t packed = quantize_quad<BITS>(x, prm);  // all lanes take part
     if (!in_range) continue;
-    if (t < npk) {
-      const int64_t row = (int64_t)bh * a.cap + t;
+    if (t < ns) {
+      __half* dst = a.sink[which] + ((int64_t)bh * a.Ns + t) * a.d + g * kGroup + quad * 8;
+      *reinterpret_cast<uint4*>(dst) = raw[u];
+    } else if (t - ns < npk) {
+      const int64_t row = (int64_t)bh * a.cap + (t - ns);
       uint8_t* dst = a.codes[which] + row * a.row_bytes + g * (4 * BITS) + quad * BITS;
       if (BITS == 4)
         *reinterpret_cast<uint32_t*>(dst) = packed;
       else
         *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
       if (quad == 0) a.params[which][row * a.Ng + g] = prm;
-    } else if (t >= npk_all) {
-      const int j = t - npk_all;  // ring slot; res_head = 0 after a prefill
+    } else if (t - ns >= npk_all) {
+      const int j = t - ns - npk_all;  // ring slot; res_head = 0 after a prefill
       __half* dst = a.res[which] + ((int64_t)bh * a.Nr + j) * a.d + g * kGroup + quad * 8;
       *reinterpret_cast<uint4*>(dst) = raw[u];
     }
@@ -221,10 +231,13 @@ cudaError_t launch_quantize_pack(const Dims& s, const kvq_cache_view& v, const _
   a.params[1] = v.v_params;
   a.res[0] = reinterpret_cast<__half*>(v.k_res);
   a.res[1] = reinterpret_cast<__half*>(v.v_res);
+  a.sink[0] = reinterpret_cast<__half*>(v.k_sink);
+  a.sink[1] = reinterpret_cast<__half*>(v.v_sink);
   a.seq_lens = seq_lens;
   a.packed_len = v.packed_len;
   a.res_len = v.res_len;
   a.res_head = v.res_head;
+  a.sink_len = v.sink_len;
   a.err_word = v.err_word;
   a.Hkv = s.Hkv;
   a.d = s.d;
@@ -232,6 +245,7 @@ cudaError_t launch_quantize_pack(const Dims& s, const kvq_cache_view& v, const _
   a.row_bytes = s.row_bytes;
   a.cap = s.cap;
   a.Nr = s.Nr;
+  a.Ns = s.Ns;
   a.Lmax = Lmax;
   if (s.bits == 4)
     quantize_pack_kernel<4><<<grid, kPackThreads, 0, st>>>(a);

@@ -36,6 +36,7 @@ KVQ_ERRBIT_BADLEN = 0x8
 KVQ_ARRAY_CODES = 0
 KVQ_ARRAY_PARAMS = 1
 KVQ_ARRAY_RESIDUAL = 2
+KVQ_ARRAY_SINK = 3
 
 # Every function the header declares (the tests check the library exports them).
 EXPORTS = ("kvq_cache_bytes", "kvq_decode_workspace_bytes", "kvq_quantize_pack", "kvq_append",
@@ -47,13 +48,14 @@ EXPORTS = ("kvq_cache_bytes", "kvq_decode_workspace_bytes", "kvq_quantize_pack",
 class CacheDesc(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("bits", ctypes.c_int32), ("group", ctypes.c_int32),
-                ("capacity", ctypes.c_int32), ("residual", ctypes.c_int32)]
+                ("capacity", ctypes.c_int32), ("residual", ctypes.c_int32),
+                ("sink", ctypes.c_int32)]
 
 
 class CacheView(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "k_codes", "v_codes", "k_params", "v_params", "k_res", "v_res",
-        "packed_len", "res_len", "res_head", "err_word")]
+        "packed_len", "res_len", "res_head", "err_word", "k_sink", "v_sink", "sink_len")]
 
 
 class KvqError(RuntimeError):
@@ -89,7 +91,7 @@ def load(path: str | None = None):
             lib.kvq_quantize_pack.restype = ctypes.c_int
             lib.kvq_append.argtypes = [DP, VP, P, P, P]
             lib.kvq_append.restype = ctypes.c_int
-            lib.kvq_decode_attention.argtypes = [DP, VP, P, i32, P, P, sz, P]
+            lib.kvq_decode_attention.argtypes = [DP, VP, P, i32, P, P, sz, ctypes.c_uint32, P]
             lib.kvq_decode_attention.restype = ctypes.c_int
             lib.kvq_decode_step.argtypes = [DP, VP, P, i32, P, P, P, P, sz, ctypes.c_uint32, P]
             lib.kvq_decode_step.restype = ctypes.c_int
@@ -97,7 +99,7 @@ def load(path: str | None = None):
             lib.kvq_step_io_bytes.restype = sz
             lib.kvq_decode_step_host.argtypes = [DP, VP, P, i32, P, P, sz, P, sz, ctypes.c_uint32, P]
             lib.kvq_decode_step_host.restype = ctypes.c_int
-            lib.kvq_decode_attention_noalloc.argtypes = [DP, VP, P, i32, P, P]
+            lib.kvq_decode_attention_noalloc.argtypes = [DP, VP, P, i32, P, ctypes.c_uint32, P]
             lib.kvq_decode_attention_noalloc.restype = ctypes.c_int
             lib.kvq_read_error.argtypes = [VP, ctypes.POINTER(ctypes.c_uint32), P]
             lib.kvq_read_error.restype = ctypes.c_int
@@ -139,15 +141,36 @@ def _f16(t: torch.Tensor, name: str) -> torch.Tensor:
     return t
 
 
+KVQ_OUT_F32 = 2
+
+
+def _out(q: torch.Tensor, out: torch.Tensor | None, flags: int):
+    """The output tensor and the flags that match its dtype: float16, or float32
+    (KVQ_OUT_F32).  Without `out`, the dtype follows KVQ_OUT_F32 in flags."""
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32 if flags & KVQ_OUT_F32 else torch.float16,
+                          device=q.device)
+    if out.dtype not in (torch.float16, torch.float32) or not out.is_cuda or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float16 or float32 CUDA tensor")
+    if out.dtype == torch.float32:
+        flags |= KVQ_OUT_F32
+    else:
+        flags &= ~KVQ_OUT_F32
+    return out, flags
+
+
 # --------------------------------------------------------------- caches ----
 
 
 class KVCache:
     """One layer's packed cache in device memory (torch tensors in the layout of
-    include/kvq.h).  Holds the description and the view the calls take."""
+    include/kvq.h).  Holds the description and the view the calls take.
+    ``sink`` > 0 keeps the first ``sink`` tokens of each sequence in fp16 (the
+    attention-sink window, fixed after the prefill)."""
 
-    def __init__(self, batch, num_kv_heads, head_dim, bits, capacity, residual, device="cuda"):
-        self.desc = CacheDesc(batch, num_kv_heads, head_dim, bits, 32, capacity, residual)
+    def __init__(self, batch, num_kv_heads, head_dim, bits, capacity, residual, device="cuda",
+                 sink=0):
+        self.desc = CacheDesc(batch, num_kv_heads, head_dim, bits, 32, capacity, residual, sink)
         self.device = torch.device(device)
         B, H, d = batch, num_kv_heads, head_dim
         rb, ng = d * bits // 8, d // 32
@@ -158,7 +181,10 @@ class KVCache:
         self.v_params = torch.zeros(B, H, capacity, ng, dtype=torch.int32, **kw)
         self.k_res = torch.zeros(B, H, residual, d, dtype=torch.float16, **kw)
         self.v_res = torch.zeros(B, H, residual, d, dtype=torch.float16, **kw)
-        self.counters = torch.zeros(3, B, dtype=torch.int32, **kw)
+        self.k_sink = torch.zeros(B, H, sink, d, dtype=torch.float16, **kw)
+        self.v_sink = torch.zeros(B, H, sink, d, dtype=torch.float16, **kw)
+        # packed_len, res_len, res_head, sink_len
+        self.counters = torch.zeros(4, B, dtype=torch.int32, **kw)
         self.err = torch.zeros(4, dtype=torch.int32, **kw)
         self.view = self._make_view()
 
@@ -166,7 +192,8 @@ class KVCache:
         r = lambda t: _ptr(t) if t.numel() else ctypes.c_void_p(0)
         return CacheView(r(self.k_codes), r(self.v_codes), r(self.k_params), r(self.v_params),
                          r(self.k_res), r(self.v_res), _ptr(self.counters[0]),
-                         _ptr(self.counters[1]), _ptr(self.counters[2]), _ptr(self.err))
+                         _ptr(self.counters[1]), _ptr(self.counters[2]), _ptr(self.err),
+                         r(self.k_sink), r(self.v_sink), _ptr(self.counters[3]))
 
     @property
     def packed_len(self):
@@ -179,6 +206,10 @@ class KVCache:
     @property
     def res_head(self):
         return self.counters[2]
+
+    @property
+    def sink_len(self):
+        return self.counters[3]
 
     def packed_bytes(self) -> int:
         """Code + param bytes of the tokens currently packed (K and V)."""
@@ -226,17 +257,17 @@ def workspace_for(cache: KVCache, num_q_heads: int) -> torch.Tensor:
 
 
 def kvq_decode_attention(cache: KVCache, q: torch.Tensor, out: torch.Tensor | None = None,
-                         workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """O = softmax(q K^T / sqrt(d)) V; q fp16 [B][Hq][d] -> out fp16 [B][Hq][d]."""
+                         workspace: torch.Tensor | None = None, stream=None,
+                         flags: int = 0) -> torch.Tensor:
+    """O = softmax(q K^T / sqrt(d)) V; q fp16 [B][Hq][d] -> out [B][Hq][d], fp16
+    or fp32 (an fp32 `out`, or flags=KVQ_OUT_F32)."""
     _f16(q, "q")
-    if out is None:
-        out = torch.empty_like(q)
-    _f16(out, "out")
+    out, flags = _out(q, out, flags)
     if workspace is None:
         workspace = workspace_for(cache, q.shape[1])
     st = load().kvq_decode_attention(ctypes.byref(cache.desc), ctypes.byref(cache.view), _ptr(q),
                                      int(q.shape[1]), _ptr(out), _ptr(workspace),
-                                     workspace.numel() * workspace.element_size(),
+                                     workspace.numel() * workspace.element_size(), int(flags),
                                      _stream(stream, q.device))
     _check(st, "kvq_decode_attention")
     return out
@@ -251,11 +282,10 @@ def kvq_decode_step(cache: KVCache, q: torch.Tensor, k_new: torch.Tensor, v_new:
     """One serving-loop step: append k_new/v_new (fp16 [B][Hkv][d]), then decode
     attention of q over the updated cache; one kernel launch where the tensor-core
     kernel applies.  flags=KVQ_STEP_EARLY_CACHE_READ: the kernel enqueued just
-    before does not write this cache (see kvq.h)."""
+    before does not write this cache (see kvq.h).  An fp32 `out` (or
+    KVQ_OUT_F32 in flags) gives fp32 output."""
     _f16(q, "q"), _f16(k_new, "k_new"), _f16(v_new, "v_new")
-    if out is None:
-        out = torch.empty_like(q)
-    _f16(out, "out")
+    out, flags = _out(q, out, flags)
     if workspace is None:
         workspace = workspace_for(cache, q.shape[1])
     st = load().kvq_decode_step(ctypes.byref(cache.desc), ctypes.byref(cache.view), _ptr(q),
@@ -285,9 +315,11 @@ def kvq_decode_step_host(cache: KVCache, in_host: torch.Tensor, num_q_heads: int
                          stream=None, flags: int = 0) -> None:
     """One step from host memory: in_host = [q | k_new | v_new] fp16 (pinned for
     an asynchronous call), out_host fp16 [B][Hq][d]; copies, step and copy back
-    enqueued on the stream by one library call."""
+    enqueued on the stream by one library call.  An fp32 out_host gives fp32
+    output."""
     if in_host.is_cuda or out_host.is_cuda:
         raise ValueError("in_host and out_host must be host tensors")
+    flags = (flags | KVQ_OUT_F32) if out_host.dtype == torch.float32 else (flags & ~KVQ_OUT_F32)
     st = load().kvq_decode_step_host(ctypes.byref(cache.desc), ctypes.byref(cache.view),
                                      _ptr(in_host), int(num_q_heads), _ptr(out_host), _ptr(dev_io),
                                      dev_io.numel() * dev_io.element_size(), _ptr(workspace),
@@ -305,11 +337,9 @@ def kvq_decode_attention_noalloc(cache: KVCache, q: torch.Tensor, out: torch.Ten
     library's own static device array holds the split partials.  Calls that
     overlap on the GPU share that array and race; keep them on one stream."""
     _f16(q, "q")
-    if out is None:
-        out = torch.empty_like(q)
-    _f16(out, "out")
+    out, flags = _out(q, out, 0)
     st = load().kvq_decode_attention_noalloc(ctypes.byref(cache.desc), ctypes.byref(cache.view),
-                                             _ptr(q), int(q.shape[1]), _ptr(out),
+                                             _ptr(q), int(q.shape[1]), _ptr(out), int(flags),
                                              _stream(stream, q.device))
     _check(st, "kvq_decode_attention_noalloc")
     return out

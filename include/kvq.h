@@ -3,7 +3,8 @@
  *
  * One operation family: single-token decode attention over a key/value cache
  * whose older tokens are stored as asymmetric uniform INT4 or INT2 codes and
- * whose most recent Nr tokens stay fp16.
+ * whose most recent Nr tokens stay fp16 (and, optionally, whose first tokens
+ * stay fp16 as an attention-sink window).
  *
  * Sources the operations follow (web pages on low-bit KV-cache decoding):
  *   - "Tensor Core accelerated low-bit KV cache decoding" (BitDecoding page),
@@ -17,6 +18,8 @@
  *     inner (head_dim) dimension, one row shares its group parameters.
  *   - same page, section 2.3: recent-token window; a new token enters the window and,
  *     when the window is full, its oldest token is quantized into the main cache.
+ *     Also the attention-sink window: the first tokens stay in full precision, set
+ *     at prefill and fixed afterwards.
  *   - same page, section 3.1: dequantized value = scale * q + zero.
  *   - same page, section 3.2: 32 consecutive head_dim values packed together.
  *
@@ -27,6 +30,7 @@
  *   G   = 32 group size along d       Ng   = d / 32 groups per token and head
  *   b   bits per code, 2 or 4         Nr   fp16 residual window length (0..1024)
  *   cap packed-token capacity per (sequence, KV head)
+ *   S   fp16 attention-sink window length (0..256)
  *
  * ---------------------------------------------------------------------------
  * Memory layout (all arrays are plain device memory owned by the caller; K and V
@@ -43,9 +47,12 @@
  *            min (fp16).  Dequantized value x^ = min + code * scale.
  *   residual fp16   [B][Hkv][Nr][d]
  *            Ring of the most recent tokens, kept in full precision.
- *   packed_len, res_len, res_head   int32 [B]   (device)
+ *   sink     fp16   [B][Hkv][S][d]
+ *            The first sink_len[b] tokens of sequence b, kept in full precision.
+ *   packed_len, res_len, res_head, sink_len   int32 [B]   (device)
  *            Per sequence: packed tokens, residual tokens, ring slot of the oldest
- *            residual token.  Sequence b attends over packed_len[b] + res_len[b] tokens.
+ *            residual token, sink tokens.  Sequence b attends over
+ *            sink_len[b] + packed_len[b] + res_len[b] tokens.
  *   err_word uint32 (device, sticky bit set, see KVQ_ERRBIT_*)
  *
  * Every device pointer must be 16-byte aligned (KVQ_ERR_MISALIGNED otherwise);
@@ -60,11 +67,12 @@
  *       clamp(rint(((float)x_j - (float)mn) / s), 0, 2^b - 1)   fp32 subtract and divide,
  *       rint = round half to even
  *   Q5  pack as in the layout above
- *   Q6  tokens [0, L - min(Nr, L)) are packed, the rest are copied to the residual ring
- *       in order, res_head = 0.
+ *   Q6  with ns = min(S, L) and nr = min(Nr, L - ns): tokens [0, ns) are copied to the
+ *       sink, tokens [ns, L - nr) are packed into slots [0, L - ns - nr), the last nr
+ *       are copied to the residual ring in order, res_head = 0.
  *
- * Decode: O[b][hq] = softmax(q[b][hq] . K^T / sqrt(d)) V over the dequantized packed
- * tokens and the residual tokens of KV head hq / gq, returned as fp16.
+ * Decode: O[b][hq] = softmax(q[b][hq] . K^T / sqrt(d)) V over the sink tokens, the
+ * dequantized packed tokens and the residual tokens of KV head hq / gq, returned as fp16.
  *
  * ---------------------------------------------------------------------------
  * Conventions
@@ -99,11 +107,12 @@ typedef enum {
 
 /* Bits of *err_word (sticky until kvq_read_error clears them). */
 #define KVQ_ERRBIT_CAPACITY 0x1u /* pack or append would pass cap; the token was dropped */
-#define KVQ_ERRBIT_EMPTY 0x2u    /* decode saw packed_len + res_len == 0; output zeroed */
+#define KVQ_ERRBIT_EMPTY 0x2u    /* decode saw a sequence with no tokens; output zeroed */
 #define KVQ_ERRBIT_TIMEOUT 0x4u  /* a bounded wait gave up; that CTA wrote nothing */
 #define KVQ_ERRBIT_BADLEN 0x8u   /* seq_lens[b] < 0 or > Lmax; that sequence was skipped */
 
-/* Static description of one layer's cache.  group must be 32. */
+/* Static description of one layer's cache.  group must be 32.  Every field is
+ * significant: zero-initialise the struct (sink = 0 keeps no sink window). */
 typedef struct {
   int32_t batch;        /* B   >= 1 */
   int32_t num_kv_heads; /* Hkv >= 1 */
@@ -112,10 +121,11 @@ typedef struct {
   int32_t group;        /* G: 32 */
   int32_t capacity;     /* packed tokens per (sequence, KV head), >= 0 */
   int32_t residual;     /* Nr: 0..1024 */
+  int32_t sink;         /* S: 0..256, first tokens kept fp16 (attention-sink window) */
 } kvq_cache_desc;
 
 /* Device pointers of one layer's cache (layout above).  k_res/v_res may be NULL
- * when residual == 0. */
+ * when residual == 0, k_sink/v_sink/sink_len when sink == 0. */
 typedef struct {
   uint8_t* k_codes;
   uint8_t* v_codes;
@@ -127,12 +137,16 @@ typedef struct {
   int32_t* res_len;
   int32_t* res_head;
   uint32_t* err_word;
+  uint16_t* k_sink; /* fp16 bits */
+  uint16_t* v_sink;
+  int32_t* sink_len;
 } kvq_cache_view;
 
 /* Which array kvq_cache_bytes sizes (each of K and V has one of each). */
 #define KVQ_ARRAY_CODES 0
 #define KVQ_ARRAY_PARAMS 1
 #define KVQ_ARRAY_RESIDUAL 2
+#define KVQ_ARRAY_SINK 3
 
 /* Bytes of one array of the layout (for K or for V; allocate twice).
  * Returns 0 for an invalid desc or `which`. */
@@ -148,9 +162,11 @@ size_t kvq_decode_workspace_bytes(const kvq_cache_desc* desc, int32_t num_q_head
  *   k, v      fp16 device [B][Hkv][Lmax][d], row-major.
  *   seq_lens  int32 device [B], 0 <= seq_lens[b] <= Lmax.
  *   Lmax      host int, >= 0.
- * For each sequence b with L = seq_lens[b]: tokens [0, L - min(Nr, L)) become
- * codes and params in slots [0, ...), the rest are copied to the residual ring;
- * packed_len[b], res_len[b] = min(Nr, L) and res_head[b] = 0 are written.
+ * For each sequence b with L = seq_lens[b], split as in Q6: the first min(S, L)
+ * tokens are copied to the sink (InnerQ page section 2.3), the next ones become
+ * codes and params in slots [0, ...), the last min(Nr, ...) are copied to the
+ * residual ring; packed_len[b], res_len[b], res_head[b] = 0 and (S > 0)
+ * sink_len[b] are written.
  * A sequence with more than cap packed tokens sets KVQ_ERRBIT_CAPACITY and stores
  * only the first cap (packed_len[b] = cap).  Asynchronous on `stream`. */
 kvq_status kvq_quantize_pack(const kvq_cache_desc* desc, const kvq_cache_view* view,
@@ -164,26 +180,35 @@ kvq_status kvq_quantize_pack(const kvq_cache_desc* desc, const kvq_cache_view* v
  * is quantized by Q1-Q5 into packed slot packed_len (which then grows by one)
  * and the new token takes its ring slot (res_head advances); otherwise the new
  * token goes to slot (res_head + res_len) % Nr and res_len grows.  With Nr == 0
- * the new token is packed directly.  A full packed cache sets
- * KVQ_ERRBIT_CAPACITY and leaves that sequence unchanged.  Asynchronous. */
+ * the new token is packed directly.  The sink is never written: it stays as the
+ * prefill left it.  A full packed cache sets KVQ_ERRBIT_CAPACITY and leaves that
+ * sequence unchanged.  Asynchronous. */
 kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache_view* view,
                       const void* k_new, const void* v_new, void* stream);
 
+/* Output element type of the decode calls (their `flags`): fp16 by default,
+ * fp32 with KVQ_OUT_F32.  Both are rounded once from the fp32 result; fp16
+ * rounding alone moves an output of magnitude 4 or more by up to 2^-9 * |O|. */
+#define KVQ_OUT_F32 2u
+
 /* Decode attention (BitDecoding page sections 2.2-2.3; InnerQ page section 3.1).
  *   q          fp16 device [B][Hq][d]; query head hq uses KV head hq / (Hq / Hkv).
- *   out        fp16 device [B][Hq][d]: softmax(q K^T / sqrt(d)) V over the
- *              packed tokens (dequantized as min + code * scale) and the residual.
+ *   out        device [B][Hq][d], fp16 (or fp32 with KVQ_OUT_F32):
+ *              softmax(q K^T / sqrt(d)) V over the sink, the packed tokens
+ *              (dequantized as min + code * scale) and the residual.
  *   workspace  device scratch of ws_bytes >= kvq_decode_workspace_bytes(desc, Hq),
  *              16-byte aligned, zeroed before its first use.  Each completed call
- *              leaves it ready for the next one (its arrival counters back at
- *              zero), so it is zeroed once, not per call; zero it again after a
- *              call that reported KVQ_ERR_TIMEOUT.  One workspace serves one call
- *              at a time.
+ *              leaves it ready for the next call with the same batch, KV heads,
+ *              head_dim and Hq (its counters and accumulators back at zero), so
+ *              it is zeroed once, not per call; zero it again before a call with
+ *              another shape and after a call that reported KVQ_ERR_TIMEOUT.
+ *              One workspace serves one call at a time.
+ *   flags      0 or KVQ_OUT_F32; other bits return KVQ_ERR_INVALID_ARG.
  * A sequence with no tokens gets a zero output and sets KVQ_ERRBIT_EMPTY.
  * Asynchronous; lengths are read on the device. */
 kvq_status kvq_decode_attention(const kvq_cache_desc* desc, const kvq_cache_view* view,
                                 const void* q, int32_t num_q_heads, void* out,
-                                void* workspace, size_t ws_bytes, void* stream);
+                                void* workspace, size_t ws_bytes, uint32_t flags, void* stream);
 
 /* One decode step of the serving loop: kvq_append(k_new, v_new) and then
  * kvq_decode_attention(q) over the cache as it is after the append (InnerQ page
@@ -210,8 +235,8 @@ kvq_status kvq_decode_attention(const kvq_cache_desc* desc, const kvq_cache_view
  *              dependent of that kernel) then reads the counters and starts its
  *              first tile copies before it waits for that kernel; q, k_new and
  *              v_new are read, and anything is written, only after the wait.
- *              Without the flag nothing is read before the wait.  Other bits
- *              return KVQ_ERR_INVALID_ARG.
+ *              Without the flag nothing is read before the wait.  KVQ_OUT_F32
+ *              may be or'ed in (fp32 out).  Other bits return KVQ_ERR_INVALID_ARG.
  * Asynchronous. */
 #define KVQ_STEP_EARLY_CACHE_READ 1u
 kvq_status kvq_decode_step(const kvq_cache_desc* desc, const kvq_cache_view* view,
@@ -221,14 +246,15 @@ kvq_status kvq_decode_step(const kvq_cache_desc* desc, const kvq_cache_view* vie
 
 /* Bytes of device staging kvq_decode_step_host needs: the packed input
  * [q | k_new | v_new] (fp16, in that order, no padding) and, at the next
- * 256-byte boundary, out.  Returns 0 for an invalid desc or head count. */
+ * 256-byte boundary, out (room for an fp32 out).  Returns 0 for an invalid desc
+ * or head count. */
 size_t kvq_step_io_bytes(const kvq_cache_desc* desc, int32_t num_q_heads);
 
 /* kvq_decode_step with its inputs and output in host memory (no passage of the
  * pages corresponds to it; it is this library's serving-loop entry point).
  *   in_host    host [q (B*Hq*d) | k_new (B*Hkv*d) | v_new (B*Hkv*d)] fp16, the
  *              layouts of kvq_decode_step, contiguous in that order.
- *   out_host   host [B][Hq][d] fp16.
+ *   out_host   host [B][Hq][d], fp16 (fp32 with KVQ_OUT_F32 in flags).
  *   dev_io     device staging of dev_io_bytes >= kvq_step_io_bytes(desc, Hq),
  *              256-byte aligned, owned by the caller.
  * Enqueues on `stream`: one host-to-device copy of the input block, the step
@@ -250,8 +276,8 @@ kvq_status kvq_decode_step_host(const kvq_cache_desc* desc, const kvq_cache_view
  * its serving loop, an allocator the caller does not own, memory fixed at start
  * up).  No passage of the pages corresponds to this call; it is an addition of
  * this library.
- * Same arguments, output and error bits as kvq_decode_attention, minus the
- * workspace: the split partials go to one static device array of
+ * Same arguments (flags included), output and error bits as
+ * kvq_decode_attention, minus the workspace: the split partials go to one static device array of
  * KVQ_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until the
  * process exits.  Returns KVQ_ERR_UNSUPPORTED when the decode would need more
  * than that (kvq_decode_workspace_bytes(desc, num_q_heads) > the maximum) and
@@ -259,12 +285,14 @@ kvq_status kvq_decode_step_host(const kvq_cache_desc* desc, const kvq_cache_view
  * nothing.  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and clears the array once
  * (cudaMemset); make that first call before any stream capture.  All calls share
- * the array and it keeps the last call's contents (its counters back at zero),
- * so calls whose kernels overlap on the GPU race: keep them on one stream or
- * order the streams. */
+ * the array and it keeps the last call's contents (its counters back at zero).
+ * A call whose cache shape or head count differs from the previous call's on
+ * the device first clears the array's counters and accumulators
+ * (cudaMemsetAsync on `stream`).  Calls whose kernels overlap on the GPU race:
+ * keep them on one stream or order the streams. */
 kvq_status kvq_decode_attention_noalloc(const kvq_cache_desc* desc, const kvq_cache_view* view,
                                         const void* q, int32_t num_q_heads, void* out,
-                                        void* stream);
+                                        uint32_t flags, void* stream);
 
 /* Synchronize `stream`, copy *err_word to *word_out (may be NULL), clear it, and
  * return KVQ_OK if it was 0, else the status of its lowest set bit. */
@@ -274,7 +302,7 @@ kvq_status kvq_read_error(const kvq_cache_view* view, uint32_t* word_out, void* 
 const char* kvq_status_string(kvq_status status);
 
 /* Library version as 10000 * major + 100 * minor + patch. */
-int32_t kvq_version(void);
+int32_t kvq_version(void); /* 110: the attention-sink window and fp32 output */
 
 #ifdef __cplusplus
 }

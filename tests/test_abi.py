@@ -30,7 +30,7 @@ def test_header_declares_and_library_exports(lib):
     assert set(kvq.EXPORTS) <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in kvq.h but not exported"
-    assert kvq.kvq_version() == 100
+    assert kvq.kvq_version() == 110
 
 
 def test_status_strings(lib):
@@ -53,9 +53,12 @@ def test_cache_bytes(lib):
     D2 = _desc(bits=2, head_dim=64)
     assert kvq.kvq_cache_bytes(D2, kvq.KVQ_ARRAY_CODES) == 2 * 8 * 1000 * 16
     assert kvq.kvq_cache_bytes(D2, kvq.KVQ_ARRAY_PARAMS) == 2 * 8 * 1000 * 2 * 4
+    assert kvq.kvq_cache_bytes(D, kvq.KVQ_ARRAY_SINK) == 0
+    assert kvq.kvq_cache_bytes(_desc(sink=32), kvq.KVQ_ARRAY_SINK) == 2 * 8 * 32 * 128 * 2
     assert kvq.kvq_cache_bytes(D, 7) == 0
     for bad in (dict(bits=3), dict(head_dim=96), dict(head_dim=100), dict(group=64),
-                dict(batch=0), dict(residual=-1), dict(residual=2000), dict(capacity=-5)):
+                dict(batch=0), dict(residual=-1), dict(residual=2000), dict(capacity=-5),
+                dict(sink=-1), dict(sink=257)):
         assert kvq.kvq_cache_bytes(_desc(**bad), kvq.KVQ_ARRAY_CODES) == 0, bad
 
 
@@ -69,7 +72,7 @@ def test_workspace_bytes(lib):
 
 def _view(addr=0x10000):
     # fake, well-aligned addresses: only ever passed to calls the host rejects
-    return kvq.CacheView(*[ctypes.c_void_p(addr + 0x1000 * i) for i in range(10)])
+    return kvq.CacheView(*[ctypes.c_void_p(addr + 0x1000 * i) for i in range(13)])
 
 
 @pytest.mark.parametrize("kw,expect", [
@@ -78,6 +81,8 @@ def _view(addr=0x10000):
     (dict(head_dim=40), kvq.KVQ_ERR_INVALID_ARG),
     (dict(group=16), kvq.KVQ_ERR_INVALID_ARG),
     (dict(batch=0), kvq.KVQ_ERR_INVALID_ARG),
+    (dict(sink=-2), kvq.KVQ_ERR_INVALID_ARG),
+    (dict(sink=512), kvq.KVQ_ERR_UNSUPPORTED),
 ])
 def test_rejects_bad_desc(lib, kw, expect):
     D, V = _desc(**kw), _view()
@@ -86,7 +91,7 @@ def test_rejects_bad_desc(lib, kw, expect):
                                  P(0x300000), 16, None) == expect
     assert lib.kvq_append(ctypes.byref(D), ctypes.byref(V), P(0x100000), P(0x200000), None) == expect
     assert lib.kvq_decode_attention(ctypes.byref(D), ctypes.byref(V), P(0x100000), 8, P(0x200000),
-                                    P(0x300000), 1 << 30, None) == expect
+                                    P(0x300000), 1 << 30, 0, None) == expect
 
 
 def test_rejects_bad_view_and_args(lib):
@@ -108,20 +113,48 @@ def test_rejects_bad_view_and_args(lib):
                                  None, 16, None) == kvq.KVQ_ERR_INVALID_ARG
     # decode: Hq not a multiple of Hkv, too small a workspace, misaligned q
     assert lib.kvq_decode_attention(ctypes.byref(D), ctypes.byref(V), P(0x100000), 12, P(0x200000),
-                                    P(0x300000), 1 << 30, None) == kvq.KVQ_ERR_INVALID_ARG
+                                    P(0x300000), 1 << 30, 0, None) == kvq.KVQ_ERR_INVALID_ARG
     need = kvq.kvq_decode_workspace_bytes(D, 32)
     assert lib.kvq_decode_attention(ctypes.byref(D), ctypes.byref(V), P(0x100000), 32, P(0x200000),
-                                    P(0x300000), need - 1, None) == kvq.KVQ_ERR_INVALID_ARG
+                                    P(0x300000), need - 1, 0, None) == kvq.KVQ_ERR_INVALID_ARG
     assert lib.kvq_decode_attention(ctypes.byref(D), ctypes.byref(V), P(0x100002), 32, P(0x200000),
-                                    P(0x300000), need, None) == kvq.KVQ_ERR_MISALIGNED
+                                    P(0x300000), need, 0, None) == kvq.KVQ_ERR_MISALIGNED
+    # flags: only KVQ_OUT_F32 (the misaligned q then fails, so nothing launches)
+    assert lib.kvq_decode_attention(ctypes.byref(D), ctypes.byref(V), P(0x100000), 32, P(0x200000),
+                                    P(0x300000), need, 1, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_decode_attention(ctypes.byref(D), ctypes.byref(V), P(0x100002), 32, P(0x200000),
+                                    P(0x300000), need, kvq.KVQ_OUT_F32, None) == kvq.KVQ_ERR_MISALIGNED
     assert lib.kvq_read_error(None, None, None) == kvq.KVQ_ERR_INVALID_ARG
+
+
+def test_rejects_bad_sink_view(lib):
+    """With a sink window the sink arrays and sink_len are required and aligned;
+    without one they may be NULL."""
+    P = ctypes.c_void_p
+    D = _desc(sink=32)
+    for field in ("k_sink", "v_sink", "sink_len"):
+        V = _view()
+        setattr(V, field, 0)
+        assert lib.kvq_append(ctypes.byref(D), ctypes.byref(V), P(0x100004), P(0x200000), None) == \
+            kvq.KVQ_ERR_INVALID_ARG, field
+    V = _view()
+    V.v_sink = 0x10008
+    assert lib.kvq_append(ctypes.byref(D), ctypes.byref(V), P(0x100000), P(0x200000), None) == kvq.KVQ_ERR_MISALIGNED
+    V = _view()
+    V.sink_len = 0x10002
+    assert lib.kvq_append(ctypes.byref(D), ctypes.byref(V), P(0x100000), P(0x200000), None) == kvq.KVQ_ERR_MISALIGNED
+    # sink == 0: NULL sink pointers pass the view check (the misaligned k_new then fails)
+    V = _view()
+    V.k_sink = V.v_sink = V.sink_len = 0
+    assert lib.kvq_append(ctypes.byref(_desc()), ctypes.byref(V), P(0x100004), P(0x200000), None) == \
+        kvq.KVQ_ERR_MISALIGNED
 
 
 def test_step_io_bytes(lib):
     D = _desc()  # B2, Hkv8, d128
     q, kv = 2 * 32 * 128 * 2, 2 * 8 * 128 * 2
     n_in = q + 2 * kv
-    assert lib.kvq_step_io_bytes(ctypes.byref(D), 32) == ((n_in + 255) // 256) * 256 + q
+    assert lib.kvq_step_io_bytes(ctypes.byref(D), 32) == ((n_in + 255) // 256) * 256 + 2 * q  # fp32 room
     assert lib.kvq_step_io_bytes(ctypes.byref(D), 12) == 0
     assert lib.kvq_step_io_bytes(ctypes.byref(_desc(bits=3)), 32) == 0
 
@@ -143,6 +176,7 @@ def test_step_host_rejects_bad_args(lib):
     assert call(dev_bytes=io - 1) == kvq.KVQ_ERR_INVALID_ARG
     assert call(w_bytes=ws - 1) == kvq.KVQ_ERR_INVALID_ARG
     assert call(flags=4) == kvq.KVQ_ERR_INVALID_ARG
+    assert call(flags=kvq.KVQ_OUT_F32 | 8) == kvq.KVQ_ERR_INVALID_ARG
     assert call(hq=12) == kvq.KVQ_ERR_INVALID_ARG
     assert call(w=P(0x200008)) == kvq.KVQ_ERR_MISALIGNED
 

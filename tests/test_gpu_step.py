@@ -88,28 +88,38 @@ def test_step_capacity_full(Nr):
     assert all(w == kvq.KVQ_ERRBIT_CAPACITY and e & 1 for w, e in words[2:])
 
 
-@pytest.mark.parametrize("num", [2, 3])
+@pytest.mark.parametrize("num", [2, 3, 4])
 def test_step_workload_full_size(num):
-    """Llama-3.1-8B layer (32K INT4, 128K INT2; 128-token window, full): three
-    fused steps, each packing the oldest window token; every output row and the
-    packed slots written against the oracle."""
+    """Llama-3.1-8B layer (32K INT4, 128K INT2; 128-token window, full) and the
+    Llama-2-13B batch of 64 ragged sequences (sequences 0, 17 and 63 checked):
+    three fused steps with fp32 output, each packing the oldest window token,
+    every checked output row against the oracle with the flat max-abs bar; after
+    each step a decode with fp16 output of the same cache; the packed slots
+    written against the oracle."""
     w = synth.WORKLOADS[num]
     k, v, lens = w.prefill(device=DEV)
     cap = w.len_max - w.residual + 8
     g = gpu_cache(w.batch, w.num_kv_heads, w.head_dim, w.bits, cap, w.residual)
     kvq.kvq_quantize_pack(g, k, v, lens.to(DEV))
-    r = ref_cache(w.batch, w.num_kv_heads, w.head_dim, w.bits, cap, w.residual)
-    assert oracle.quantize_pack(r, to_np(k), to_np(v), to_np(lens)) == 0
+    rows = list(range(w.batch)) if w.batch < 8 else [0, 17, 63]
+    r = ref_cache(len(rows), w.num_kv_heads, w.head_dim, w.bits, cap, w.residual)
+    Lm = int(lens[rows].max())
+    assert oracle.quantize_pack(r, to_np(k[rows, :, :Lm]), to_np(v[rows, :, :Lm]), to_np(lens[rows])) == 0
     del k, v
+    ws = kvq.workspace_for(g, w.num_q_heads)
     for step in range(3):
         kn, vn = w.new_tokens(step)
         q = w.query(step)
-        out = kvq.kvq_decode_step(g, q.to(DEV), kn.to(DEV), vn.to(DEV))
+        out = torch.empty(q.shape, dtype=torch.float32, device=DEV)
+        kvq.kvq_decode_step(g, q.to(DEV), kn.to(DEV), vn.to(DEV), out, ws)
         assert kvq.kvq_read_error(g)[0] == kvq.KVQ_OK
-        oracle.append(r, kn.numpy(), vn.numpy())
-        err, rel = assert_attn_close(out, oracle.decode(r, q.numpy()))
-        print(f"workload {num} step {step}: max abs {err:.2e}, rel L2 {rel:.2e}")
-    assert_cache_equal(g, r)
+        oracle.append(r, kn[rows].numpy(), vn[rows].numpy())
+        want = oracle.decode(r, q[rows].numpy())
+        err, rel = assert_attn_close(out[rows], want)
+        err16, rel16 = assert_attn_close(kvq.kvq_decode_attention(g, q.to(DEV), workspace=ws)[rows], want)
+        print(f"workload {num} step {step}: fp32 out max abs {err:.2e}, rel L2 {rel:.2e}; "
+              f"fp16 out max abs {err16:.2e}, rel L2 {rel16:.2e}")
+    assert_cache_equal(g, r, batches=rows)
 
 
 @pytest.mark.parametrize("bits", [4, 2])
@@ -160,11 +170,11 @@ def test_step_rejects_unknown_flags():
     q = torch.zeros(1, 4, 128, dtype=torch.float16, device=DEV)
     kn = torch.zeros(1, 1, 128, dtype=torch.float16, device=DEV)
     with pytest.raises(kvq.KvqError):
-        kvq.kvq_decode_step(g, q, kn, kn, flags=2)
+        kvq.kvq_decode_step(g, q, kn, kn, flags=4)
 
 
-@pytest.mark.parametrize("bits", [4, 2])
-def test_step_host_matches_device_step(bits):
+@pytest.mark.parametrize("bits,out_dtype", [(4, torch.float16), (2, torch.float16), (4, torch.float32)])
+def test_step_host_matches_device_step(bits, out_dtype):
     """kvq_decode_step_host (pinned host input block and output, one call per
     step) on one cache and kvq_decode_step on its twin: identical cache bytes
     after every step, both outputs within tolerance of the oracle."""
@@ -185,10 +195,11 @@ def test_step_host_matches_device_step(bits):
         kn = rng.standard_normal((B, H, d)).astype(np.float16)
         vn = rng.standard_normal((B, H, d)).astype(np.float16)
         in_h = torch.from_numpy(np.concatenate([q.ravel(), kn.ravel(), vn.ravel()])).pin_memory()
-        out_h = torch.empty((B, H * gq, d), dtype=torch.float16).pin_memory()
+        out_h = torch.empty((B, H * gq, d), dtype=out_dtype).pin_memory()
         kvq.kvq_decode_step_host(a, in_h, H * gq, out_h, io, ws_a)
         out_b = kvq.kvq_decode_step(b, torch.from_numpy(q).to(DEV), torch.from_numpy(kn).to(DEV),
-                                    torch.from_numpy(vn).to(DEV), workspace=ws_b)
+                                    torch.from_numpy(vn).to(DEV),
+                                    torch.empty((B, H * gq, d), dtype=out_dtype, device=DEV), ws_b)
         torch.cuda.synchronize()
         assert kvq.kvq_read_error(a)[0] == kvq.KVQ_OK
         _assert_gpu_caches_equal(a, b)

@@ -21,6 +21,7 @@ def _decode_noalloc_abi(cache, q, out):
     st = lib.kvq_decode_attention_noalloc(
         ctypes.byref(cache.desc), ctypes.byref(cache.view), ctypes.c_void_p(q.data_ptr()),
         int(q.shape[1]), ctypes.c_void_p(out.data_ptr()),
+        ctypes.c_uint32(kvq.KVQ_OUT_F32 if out.dtype == torch.float32 else 0),
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     return st
 
@@ -54,8 +55,35 @@ def test_noalloc_rejects_oversized_request():
     D = kvq.CacheDesc(2048, 16, 256, 4, 32, 1 << 20, 0)
     need = kvq.kvq_decode_workspace_bytes(D, 16 * 8)
     assert need > kvq.NOALLOC_SCRATCH_BYTES
-    V = kvq.CacheView(*[ctypes.c_void_p(0x100000 * (i + 1)) for i in range(10)])
+    V = kvq.CacheView(*[ctypes.c_void_p(0x100000 * (i + 1)) for i in range(13)])
     st = kvq.load().kvq_decode_attention_noalloc(ctypes.byref(D), ctypes.byref(V),
                                                  ctypes.c_void_p(0x100000), 16 * 8,
-                                                 ctypes.c_void_p(0x200000), None)
+                                                 ctypes.c_void_p(0x200000), 0, None)
     assert st == kvq.KVQ_ERR_UNSUPPORTED
+
+
+def test_noalloc_alternating_shapes():
+    """Calls that alternate between caches of different shapes (tensor-core and
+    generic kernels, different batch and head counts) share the static array:
+    each call after a shape change clears its counters and accumulators first,
+    so every output still matches the regular entry point."""
+    rng = np.random.default_rng(77)
+    caches = []
+    for B, H, gq, d, L in ((2, 8, 4, 128, 3000), (3, 2, 2, 64, 700), (1, 4, 1, 128, 2000)):
+        c = kvq.KVCache(B, H, d, 4, L, 16, device=DEV)
+        k = torch.from_numpy(rng.standard_normal((B, H, L, d)).astype(np.float16)).to(DEV)
+        v = torch.from_numpy(rng.standard_normal((B, H, L, d)).astype(np.float16)).to(DEV)
+        kvq.kvq_quantize_pack(c, k, v, torch.full((B,), L, dtype=torch.int32, device=DEV))
+        caches.append((c, H * gq))
+    for rnd in range(3):
+        for c, hq in caches:
+            B, d = c.desc.batch, c.desc.head_dim
+            q = torch.from_numpy(rng.standard_normal((B, hq, d)).astype(np.float16)).to(DEV)
+            want = kvq.kvq_decode_attention(c, q)
+            got = torch.full_like(q, float("nan"))
+            assert _decode_noalloc_abi(c, q, got) == kvq.KVQ_OK
+            torch.cuda.synchronize()
+            diff = (got.float() - want.float()).abs().max().item()
+            assert diff <= 2e-3, (rnd, B, hq, d, diff)
+    for c, _ in caches:
+        assert kvq.kvq_read_error(c)[0] == kvq.KVQ_OK
