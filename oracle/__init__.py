@@ -42,7 +42,7 @@ def build(force: bool = False) -> str:
 
 
 class Desc(ctypes.Structure):
-    """Cache shape; the same eight integers as the library's description."""
+    """Cache shape; the same nine integers as the library's description."""
 
     _fields_ = [
         ("batch", ctypes.c_int32),
@@ -53,6 +53,7 @@ class Desc(ctypes.Structure):
         ("capacity", ctypes.c_int32),
         ("residual", ctypes.c_int32),
         ("sink", ctypes.c_int32),
+        ("hybrid", ctypes.c_int32),
     ]
 
 
@@ -70,12 +71,18 @@ def _load():
             lib.oracle_f32_to_f16_array.argtypes = [P, P, i64]
             lib.oracle_f16_to_f64_array.argtypes = [P, P, i64]
             lib.oracle_quantize_group.argtypes = [P, ctypes.c_int, P, P, P]
+            lib.oracle_quantize_group_sym.argtypes = [P, ctypes.c_int, P, P, P]
+            lib.oracle_quantize_group_sym.restype = ctypes.c_int
+            lib.oracle_group_sq_error.argtypes = [P, P, ctypes.c_uint16, ctypes.c_uint16]
+            lib.oracle_group_sq_error.restype = ctypes.c_float
+            lib.oracle_quantize_group_hybrid.argtypes = [P, ctypes.c_int, P, P, P]
+            lib.oracle_quantize_group_hybrid.restype = ctypes.c_int
             lib.oracle_pack_row.argtypes = [P, ctypes.c_int, ctypes.c_int, P]
             lib.oracle_pack_row.restype = ctypes.c_int
             lib.oracle_unpack_row.argtypes = [P, ctypes.c_int, ctypes.c_int, P]
-            lib.oracle_quantize_pack.argtypes = [P, P, P, i32, P, P, P, P, P, P, P, P]
+            lib.oracle_quantize_pack.argtypes = [P, P, P, i32, P, P, P, P, P, P, P, P, P]
             lib.oracle_quantize_pack.restype = ctypes.c_int
-            lib.oracle_append.argtypes = [P] * 11
+            lib.oracle_append.argtypes = [P] * 12
             lib.oracle_append.restype = ctypes.c_int
             lib.oracle_decode_pairs.argtypes = [P] * 13 + [P, i32, P, i32, P]
             lib.oracle_decode_pairs.restype = ctypes.c_int
@@ -132,6 +139,36 @@ def quantize_group(x, bits: int):
     return codes, sh.value, mh.value
 
 
+def quantize_group_sym(x, bits: int):
+    """H1 (symmetric candidate) on 32 fp16 values -> (codes, scale_bits,
+    min_bits, storable)."""
+    x = _u16(x)
+    assert x.size == 32
+    codes = np.zeros(32, dtype=np.uint8)
+    sh, mh = ctypes.c_uint16(), ctypes.c_uint16()
+    ok = _load().oracle_quantize_group_sym(_ptr(x), bits, _ptr(codes), ctypes.byref(sh), ctypes.byref(mh))
+    return codes, sh.value, mh.value, bool(ok)
+
+
+def group_sq_error(x, codes, scale_bits: int, min_bits: int) -> float:
+    """H2: the fp32 squared reconstruction error of one group's candidate."""
+    x = _u16(x)
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    return float(_load().oracle_group_sq_error(_ptr(x), _ptr(codes), scale_bits, min_bits))
+
+
+def quantize_group_hybrid(x, bits: int):
+    """H3 on 32 fp16 values -> (codes, scale_bits, min_bits, mode) with mode 1
+    asymmetric, 0 symmetric."""
+    x = _u16(x)
+    assert x.size == 32
+    codes = np.zeros(32, dtype=np.uint8)
+    sh, mh = ctypes.c_uint16(), ctypes.c_uint16()
+    mode = _load().oracle_quantize_group_hybrid(_ptr(x), bits, _ptr(codes), ctypes.byref(sh),
+                                                ctypes.byref(mh))
+    return codes, sh.value, mh.value, int(mode)
+
+
 def pack_row(codes, bits: int) -> np.ndarray:
     """Q5: d codes -> d*bits/8 bytes."""
     codes = np.ascontiguousarray(codes, dtype=np.uint8)
@@ -151,8 +188,8 @@ def unpack_row(packed, d: int, bits: int) -> np.ndarray:
 class Cache:
     """Host copy of one layer's cache in the library's layout (numpy arrays)."""
 
-    def __init__(self, batch, num_kv_heads, head_dim, bits, capacity, residual, sink=0):
-        self.desc = Desc(batch, num_kv_heads, head_dim, bits, 32, capacity, residual, sink)
+    def __init__(self, batch, num_kv_heads, head_dim, bits, capacity, residual, sink=0, hybrid=0):
+        self.desc = Desc(batch, num_kv_heads, head_dim, bits, 32, capacity, residual, sink, hybrid)
         B, H, d = batch, num_kv_heads, head_dim
         rb, ng = d * bits // 8, d // 32
         self.k_codes = np.zeros((B, H, capacity, rb), np.uint8)
@@ -167,16 +204,20 @@ class Cache:
         self.k_sink = np.zeros((B, H, max(sink, 1), d), np.uint16)  # [B][Hkv][sink][d] fp16 bits
         self.v_sink = np.zeros((B, H, max(sink, 1), d), np.uint16)
         self.sink_len = np.zeros(B, np.int32)
+        # hybrid mode: per packed row, bit g = mode of group g (1 asymmetric, 0 symmetric)
+        self.k_mode = np.zeros((B, H, max(capacity, 1)), np.uint8)
+        self.v_mode = np.zeros((B, H, max(capacity, 1)), np.uint8)
 
     @property
     def shape(self):
         D = self.desc
-        return D.batch, D.num_kv_heads, D.head_dim, D.bits, D.capacity, D.residual, D.sink
+        return D.batch, D.num_kv_heads, D.head_dim, D.bits, D.capacity, D.residual, D.sink, D.hybrid
 
     def copy(self) -> "Cache":
         c = Cache(*self.shape)
         for name in ("k_codes", "v_codes", "k_params", "v_params", "k_res", "v_res",
-                     "packed_len", "res_len", "res_head", "k_sink", "v_sink", "sink_len"):
+                     "packed_len", "res_len", "res_head", "k_sink", "v_sink", "sink_len",
+                     "k_mode", "v_mode"):
             getattr(c, name)[...] = getattr(self, name)
         return c
 
@@ -191,11 +232,11 @@ def quantize_pack(cache: Cache, k, v, seq_lens) -> int:
     D = ctypes.byref(cache.desc)
     e1 = lib.oracle_quantize_pack(D, _ptr(k), _ptr(seq), Lmax, _ptr(cache.k_codes),
                                   _ptr(cache.k_params), _ptr(cache.k_res), _ptr(cache.k_sink),
-                                  _ptr(cache.packed_len), _ptr(cache.res_len), _ptr(cache.res_head),
+                                  _ptr(cache.k_mode), _ptr(cache.packed_len), _ptr(cache.res_len), _ptr(cache.res_head),
                                   _ptr(cache.sink_len))
     e2 = lib.oracle_quantize_pack(D, _ptr(v), _ptr(seq), Lmax, _ptr(cache.v_codes),
                                   _ptr(cache.v_params), _ptr(cache.v_res), _ptr(cache.v_sink),
-                                  _ptr(cache.packed_len), _ptr(cache.res_len), _ptr(cache.res_head),
+                                  _ptr(cache.v_mode), _ptr(cache.packed_len), _ptr(cache.res_len), _ptr(cache.res_head),
                                   _ptr(cache.sink_len))
     if e1 < 0 or e2 < 0:
         raise ValueError("invalid cache description")
@@ -209,10 +250,10 @@ def append(cache: Cache, k_new, v_new) -> int:
     D = ctypes.byref(cache.desc)
     pl, rl, rh = cache.packed_len.copy(), cache.res_len.copy(), cache.res_head.copy()
     e1 = lib.oracle_append(D, _ptr(k_new), _ptr(cache.k_codes), _ptr(cache.k_params),
-                           _ptr(cache.k_res), _ptr(pl), _ptr(rl), _ptr(rh),
+                           _ptr(cache.k_res), _ptr(cache.k_mode), _ptr(pl), _ptr(rl), _ptr(rh),
                            _ptr(cache.packed_len), _ptr(cache.res_len), _ptr(cache.res_head))
     e2 = lib.oracle_append(D, _ptr(v_new), _ptr(cache.v_codes), _ptr(cache.v_params),
-                           _ptr(cache.v_res), _ptr(pl), _ptr(rl), _ptr(rh),
+                           _ptr(cache.v_res), _ptr(cache.v_mode), _ptr(pl), _ptr(rl), _ptr(rh),
                            _ptr(cache.packed_len), _ptr(cache.res_len), _ptr(cache.res_head))
     if e1 < 0 or e2 < 0:
         raise ValueError("invalid cache description")

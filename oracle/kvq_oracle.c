@@ -15,6 +15,15 @@
  *     even; a zero scale gives all-zero codes; a -0 minimum is stored as +0.
  *   Pack (Q5): codes as a little-endian bit string, 32 consecutive head_dim
  *     values per group (InnerQ page, section 3.2); params as half2 {scale, min}.
+ *   Hybrid mode (H1-H3, optional): per group a symmetric candidate beside the
+ *     asymmetric one, the smaller squared error wins and a 1-bit mask records
+ *     the choice (InnerQ page, section 2.2).  Readings of points the page leaves
+ *     open: symmetric = absmax / (2^(b-1) - 1) with codes in +-(2^(b-1) - 1),
+ *     stored offset by 2^(b-1) with min = -2^(b-1) * scale (so both modes
+ *     dequantize as min + code * scale); the error is the sum of squared fp32
+ *     reconstruction errors in a fixed order (below), which decides an integer
+ *     and so is taken in the kernel's precision; a tie keeps the asymmetric
+ *     candidate; a symmetric min that is not a finite fp16 rules it out.
  *   Residual split (Q6): the last min(Nr, L) tokens stay fp16 (BitDecoding page,
  *     section 2.2); with an attention-sink window the first min(sink, L) tokens
  *     stay fp16 too, fixed after the prefill (InnerQ page, section 2.3).
@@ -171,6 +180,83 @@ void oracle_quantize_group(const uint16_t* x, int bits, uint8_t* codes, uint16_t
   }
 }
 
+/* H1: the symmetric candidate of one group.  a = max |x_j| (exact); scale =
+ * fp16(a / (2^(b-1) - 1)) (fp32 IEEE divide); s = the stored scale; t_j =
+ * clamp(rint(x_j / s), -(2^(b-1) - 1), 2^(b-1) - 1) (fp32 IEEE divide, ties to
+ * even; 0 when s == 0); stored code t_j + 2^(b-1); stored min fp16(-2^(b-1) * s
+ * + 0), exact when finite.  Returns 0 when that min overflows fp16 (the
+ * candidate cannot be stored), else 1. */
+int oracle_quantize_group_sym(const uint16_t* x, int bits, uint8_t* codes, uint16_t* scale_h,
+                              uint16_t* min_h) {
+  const int G = 32;
+  const int half = 1 << (bits - 1);
+  const int qs = half - 1;
+  float a = 0.0f;
+  for (int j = 0; j < G; ++j) {
+    float v = fabsf(oracle_f16_to_f32(x[j]));
+    if (v > a) a = v;
+  }
+  volatile float scale_f = a / (float)qs;
+  *scale_h = oracle_f32_to_f16(scale_f);
+  float s = oracle_f16_to_f32(*scale_h);
+  volatile float m = -(float)half * s;
+  *min_h = oracle_f32_to_f16(m + 0.0f);
+  for (int j = 0; j < G; ++j) {
+    float t = 0.0f;
+    if (s != 0.0f) {
+      volatile float ratio = oracle_f16_to_f32(x[j]) / s;
+      t = rintf(ratio);
+      if (t < (float)-qs) t = (float)-qs;
+      if (t > (float)qs) t = (float)qs;
+    }
+    codes[j] = (uint8_t)((int)t + half);
+  }
+  return ((*min_h & 0x7c00u) != 0x7c00u) ? 1 : 0;
+}
+
+/* H2: squared reconstruction error of a group's candidate, fp32, in this order:
+ * x^_j = (float)min + (float)code_j * (float)scale (multiply, then add, each
+ * rounded), e_j = x_j - x^_j, and per quarter q (values 8q .. 8q+7) the running
+ * sum S_q = ((e_8q^2 + e_8q+1^2) + ...) in index order; the result is
+ * (S_0 + S_1) + (S_2 + S_3). */
+float oracle_group_sq_error(const uint16_t* x, const uint8_t* codes, uint16_t scale_h,
+                            uint16_t min_h) {
+  const float sc = oracle_f16_to_f32(scale_h), mn = oracle_f16_to_f32(min_h);
+  volatile float part[4];
+  for (int q = 0; q < 4; ++q) {
+    volatile float acc = 0.0f;
+    for (int j = 8 * q; j < 8 * q + 8; ++j) {
+      volatile float prod = (float)codes[j] * sc;
+      volatile float xh = mn + prod;
+      volatile float e = oracle_f16_to_f32(x[j]) - xh;
+      volatile float e2 = e * e;
+      acc = acc + e2;
+    }
+    part[q] = acc;
+  }
+  volatile float lo = part[0] + part[1];
+  volatile float hi = part[2] + part[3];
+  return lo + hi;
+}
+
+/* H3: hybrid quantization of one group: the symmetric candidate when it can be
+ * stored and its error (H2) is strictly below the asymmetric one's, else the
+ * asymmetric candidate (Q1-Q4).  Returns the mode bit: 1 asymmetric, 0 symmetric. */
+int oracle_quantize_group_hybrid(const uint16_t* x, int bits, uint8_t* codes, uint16_t* scale_h,
+                                 uint16_t* min_h) {
+  uint8_t cs[32];
+  uint16_t ss, ms;
+  oracle_quantize_group(x, bits, codes, scale_h, min_h);
+  if (!oracle_quantize_group_sym(x, bits, cs, &ss, &ms)) return 1;
+  float ea = oracle_group_sq_error(x, codes, *scale_h, *min_h);
+  float es = oracle_group_sq_error(x, cs, ss, ms);
+  if (!(es < ea)) return 1;
+  memcpy(codes, cs, sizeof(cs));
+  *scale_h = ss;
+  *min_h = ms;
+  return 0;
+}
+
 /* Q5: pack d codes of one token row; returns bytes written (d * bits / 8). */
 int oracle_pack_row(const uint8_t* codes, int d, int bits, uint8_t* out) {
   int nbytes = d * bits / 8;
@@ -191,34 +277,41 @@ void oracle_unpack_row(const uint8_t* packed, int d, int bits, uint8_t* codes) {
   }
 }
 
-/* Quantize and pack one token of one head: src = d fp16 values. */
-static void quantize_token(const uint16_t* src, int d, int bits, uint8_t* code_row,
-                           uint32_t* param_row) {
+/* Quantize and pack one token of one head: src = d fp16 values.  With hybrid,
+ * each group takes H3 and *mode_byte gets bit g = group g's mode bit. */
+static void quantize_token(const uint16_t* src, int d, int bits, int hybrid, uint8_t* code_row,
+                           uint32_t* param_row, uint8_t* mode_byte) {
   uint8_t codes[256];
+  uint8_t mode = 0;
   for (int g = 0; g < d / 32; ++g) {
     uint16_t sh, mh;
-    oracle_quantize_group(src + 32 * g, bits, codes + 32 * g, &sh, &mh);
+    if (hybrid)
+      mode |= (uint8_t)(oracle_quantize_group_hybrid(src + 32 * g, bits, codes + 32 * g, &sh, &mh) << g);
+    else
+      oracle_quantize_group(src + 32 * g, bits, codes + 32 * g, &sh, &mh);
     param_row[g] = (uint32_t)sh | ((uint32_t)mh << 16);
   }
   oracle_pack_row(codes, d, bits, code_row);
+  if (hybrid) *mode_byte = mode;
 }
 
 /* Shapes of one cache, mirroring the library's description. */
 typedef struct {
-  int32_t batch, num_kv_heads, head_dim, bits, group, capacity, residual, sink;
+  int32_t batch, num_kv_heads, head_dim, bits, group, capacity, residual, sink, hybrid;
 } oracle_desc;
 
 static int desc_ok(const oracle_desc* D) {
   return D && D->batch >= 1 && D->num_kv_heads >= 1 && D->head_dim >= 32 && D->head_dim <= 256 &&
          D->head_dim % 32 == 0 && (D->bits == 2 || D->bits == 4) && D->group == 32 &&
          D->capacity >= 0 && D->residual >= 0 && D->residual <= 1024 && D->sink >= 0 &&
-         D->sink <= 256;
+         D->sink <= 256 && (D->hybrid == 0 || D->hybrid == 1);
 }
 
 /* Q1-Q6 over a whole prefill for one of K or V.
  *   x         fp16 [B][Hkv][Lmax][d]
  *   codes     [B][Hkv][cap][d*b/8]; params [B][Hkv][cap][Ng]; res [B][Hkv][Nr][d];
  *   sink_rows [B][Hkv][sink][d] (may be NULL when sink == 0)
+ *   modes     [B][Hkv][cap] mode bytes (H3; may be NULL unless hybrid)
  *   packed_len, res_len, res_head, sink_len  [B] outputs.
  * With an attention-sink window (InnerQ page, section 2.3), the first
  * min(sink, L) tokens are kept verbatim in sink_rows and the rest is split as
@@ -226,8 +319,8 @@ static int desc_ok(const oracle_desc* D) {
  * Returns a bit set: 1 = a sequence passed the capacity, 8 = a bad length. */
 int oracle_quantize_pack(const oracle_desc* D, const uint16_t* x, const int32_t* seq_lens,
                          int32_t Lmax, uint8_t* codes, uint32_t* params, uint16_t* res,
-                         uint16_t* sink_rows, int32_t* packed_len, int32_t* res_len,
-                         int32_t* res_head, int32_t* sink_len) {
+                         uint16_t* sink_rows, uint8_t* modes, int32_t* packed_len,
+                         int32_t* res_len, int32_t* res_head, int32_t* sink_len) {
   if (!desc_ok(D)) return -1;
   const int d = D->head_dim, Ng = d / 32, rb = d * D->bits / 8, Nr = D->residual, S = D->sink;
   const int64_t cap = D->capacity;
@@ -252,8 +345,9 @@ int oracle_quantize_pack(const oracle_desc* D, const uint16_t* x, const int32_t*
       for (int32_t j = 0; j < ns; ++j)
         memcpy(sink_rows + (bh * S + j) * d, src + (int64_t)j * d, (size_t)d * sizeof(uint16_t));
       for (int32_t t = 0; t < npk; ++t)
-        quantize_token(src + (int64_t)(ns + t) * d, d, D->bits, codes + (bh * cap + t) * rb,
-                       params + (bh * cap + t) * Ng);
+        quantize_token(src + (int64_t)(ns + t) * d, d, D->bits, D->hybrid,
+                       codes + (bh * cap + t) * rb, params + (bh * cap + t) * Ng,
+                       modes ? modes + bh * cap + t : NULL);
       for (int32_t j = 0; j < nres; ++j)
         memcpy(res + (bh * Nr + j) * d, src + (int64_t)(L - nres + j) * d,
                (size_t)d * sizeof(uint16_t));
@@ -271,7 +365,7 @@ int oracle_quantize_pack(const oracle_desc* D, const uint16_t* x, const int32_t*
  *   and the updated values written to the *_out arrays (so K and V can share the
  *   same inputs).  Returns 1 if a sequence hit the capacity (left unchanged). */
 int oracle_append(const oracle_desc* D, const uint16_t* xnew, uint8_t* codes, uint32_t* params,
-                  uint16_t* res, const int32_t* packed_len, const int32_t* res_len,
+                  uint16_t* res, uint8_t* modes, const int32_t* packed_len, const int32_t* res_len,
                   const int32_t* res_head, int32_t* packed_len_out, int32_t* res_len_out,
                   int32_t* res_head_out) {
   if (!desc_ok(D)) return -1;
@@ -291,13 +385,14 @@ int oracle_append(const oracle_desc* D, const uint16_t* xnew, uint8_t* codes, ui
     for (int h = 0; h < D->num_kv_heads; ++h) {
       int64_t bh = (int64_t)b * D->num_kv_heads + h;
       const uint16_t* src = xnew + bh * d;
+      uint8_t* mode_byte = modes ? modes + bh * cap + pl : NULL;
       if (Nr == 0) {
-        quantize_token(src, d, D->bits, codes + (bh * cap + pl) * rb,
-                       params + (bh * cap + pl) * Ng);
+        quantize_token(src, d, D->bits, D->hybrid, codes + (bh * cap + pl) * rb,
+                       params + (bh * cap + pl) * Ng, mode_byte);
       } else if (full) {
         uint16_t* oldest = res + (bh * Nr + rh) * d;
-        quantize_token(oldest, d, D->bits, codes + (bh * cap + pl) * rb,
-                       params + (bh * cap + pl) * Ng);
+        quantize_token(oldest, d, D->bits, D->hybrid, codes + (bh * cap + pl) * rb,
+                       params + (bh * cap + pl) * Ng, mode_byte);
         memcpy(oldest, src, (size_t)d * sizeof(uint16_t));
       } else {
         memcpy(res + (bh * Nr + (rh + rl) % Nr) * d, src, (size_t)d * sizeof(uint16_t));
