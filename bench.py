@@ -196,7 +196,7 @@ def workload_config(w, packed_tokens, extra=None):
     return cfg
 
 
-def build_state(dev, steps, warmup, e2e_steps, l2_bytes, workload, sink=0):
+def build_state(dev, steps, warmup, e2e_steps, l2_bytes, workload, sink=0, hybrid=0):
     """Pack the workload once, clone it into enough copies to exceed 3x L2,
     and pre-generate the per-step queries and new tokens on the device."""
     from bit_quantized_kv_pack_gb300 import kvq, synth
@@ -214,7 +214,7 @@ def build_state(dev, steps, warmup, e2e_steps, l2_bytes, workload, sink=0):
                + math.ceil((ncopy + max(ncopy, e2e_steps)) / ncopy) + 2)
     cap = max(npk_b) + appends + 8
     base = kvq.KVCache(w.batch, w.num_kv_heads, w.head_dim, w.bits, cap, w.residual, device=dev,
-                       sink=sink)
+                       sink=sink, hybrid=hybrid)
     kvq.kvq_quantize_pack(base, k, v, lens.to(dev))
     st, word = kvq.kvq_read_error(base)
     if st != kvq.KVQ_OK:
@@ -223,9 +223,9 @@ def build_state(dev, steps, warmup, e2e_steps, l2_bytes, workload, sink=0):
     copies = [base]
     for _ in range(ncopy - 1):
         c = kvq.KVCache(w.batch, w.num_kv_heads, w.head_dim, w.bits, cap, w.residual, device=dev,
-                        sink=sink)
+                        sink=sink, hybrid=hybrid)
         for name in ("k_codes", "v_codes", "k_params", "v_params", "k_res", "v_res", "k_sink",
-                     "v_sink", "counters"):
+                     "v_sink", "k_mode", "v_mode", "counters"):
             getattr(c, name).copy_(getattr(base, name))
         copies.append(c)
     nslot = ncopy  # one graph = one pass over the copies
@@ -285,7 +285,8 @@ def run_ours(args, rank, world, local):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
 
-    st = build_state(dev, args.steps, args.warmup, args.e2e_steps, l2, args.workload, args.sink)
+    st = build_state(dev, args.steps, args.warmup, args.e2e_steps, l2, args.workload, args.sink,
+                     args.hybrid)
     w, ncopy = st["w"], st["nslot"]
     K = args.steps
     reps, rem = divmod(K, ncopy)  # K steps = reps whole passes over the copies + rem
@@ -367,13 +368,14 @@ def run_ours(args, rank, world, local):
             "l2": f"rotating {ncopy} cache copies ({ncopy * step_bytes / 2**20:.0f} MiB "
                   f"packed) > 3x L2 ({l2 / 2**20:.0f} MiB)",
             "timing": "CUDA graph replays, CUDA events", "parallelism": "replicas",
-            **({"sink": args.sink} if args.sink else {})}),
+            **({"sink": args.sink} if args.sink else {}),
+            **({"hybrid": "sym/asym per group, mode bytes"} if args.hybrid else {})}),
         "all_bytes_gbs": round(all_bytes_gbs, 2),
         "gpu_launches": launches * K,
         "roofline": {"bound": "hbm", "kernel": rf_kernel,
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": profiled_traffic(w.name, fused) if args.sink == 0 else None,
+                     "traffic": profiled_traffic(w.name, fused) if not (args.sink or args.hybrid) else None,
                      "algorithmic_bytes_per_launch": step_bytes,
                      "us_per_launch": round(rf_us, 3)},
         "decode_only": {"us_per_launch": round(dec_ms_per_launch * 1e3, 3),
@@ -608,8 +610,10 @@ def run_pack(args, rank, world, local):
             k, v, lens = w.prefill(device=dev)
             ins.append((k, v, lens.to(dev)))
         in_bytes = 2 * ins[0][0].numel() * 2
-        cache = kvq.KVCache(w.batch, w.num_kv_heads, w.head_dim, bits, w.len_max, 0, device=dev)
-        out_bytes = sum(cache.k_codes.numel() + cache.k_params.numel() * 4 for _ in range(2))
+        cache = kvq.KVCache(w.batch, w.num_kv_heads, w.head_dim, bits, w.len_max, 0, device=dev,
+                            hybrid=args.hybrid)
+        out_bytes = sum(cache.k_codes.numel() + cache.k_params.numel() * 4 + cache.k_mode.numel()
+                        for _ in range(2))
         for i in range(args.warmup):
             k, v, lens = ins[i % 2]
             kvq.kvq_quantize_pack(cache, k, v, lens)
@@ -636,7 +640,8 @@ def run_pack(args, rank, world, local):
         "data": "synthetic (seeded SplitMix64 + Box-Muller, fp16)",
         "config": {"workload": "pack-32768x8x128-kv", "tokens": 32768, "num_kv_heads": 8,
                    "head_dim": 128, "group": 32, "l2": "two input copies alternate",
-                   "timing": "CUDA events around K launches"},
+                   "timing": "CUDA events around K launches",
+                   **({"hybrid": "sym/asym per group, mode bytes"} if args.hybrid else {})},
         "int2": {"us_per_step": round(out[2]["us"], 3), "value": round(out[2]["gbs"], 2)},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "kernel": "quantize_pack (INT4)",
@@ -650,7 +655,7 @@ def run_pack(args, rank, world, local):
         import oracle
         w = synth.scaled(synth.WORKLOADS[5], bits=4)
         k, v, lens = w.prefill()
-        r = oracle.Cache(w.batch, w.num_kv_heads, w.head_dim, 4, w.len_max, 0)
+        r = oracle.Cache(w.batch, w.num_kv_heads, w.head_dim, 4, w.len_max, 0, 0, args.hybrid)
         t0 = time.perf_counter()
         n = 0
         while n < 1 or time.perf_counter() - t0 < min(args.cpu_seconds, 10.0):
@@ -674,6 +679,8 @@ def main():
                          "standalone quantize/pack throughput case (INT4 and INT2)")
     ap.add_argument("--sink", type=int, default=0,
                     help="attention-sink rows kept fp16 per sequence (0..256; default 0)")
+    ap.add_argument("--hybrid", type=int, default=0, choices=(0, 1),
+                    help="1: hybrid symmetric/asymmetric groups with mode bytes (default 0)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -18,7 +18,7 @@ kvq_status check_desc(const kvq_cache_desc* D) {
   if (D->bits != 2 && D->bits != 4) return KVQ_ERR_UNSUPPORTED;
   if (D->head_dim != 32 && D->head_dim != 64 && D->head_dim != 128 && D->head_dim != 256)
     return KVQ_ERR_UNSUPPORTED;
-  if (D->sink < 0) return KVQ_ERR_INVALID_ARG;
+  if (D->sink < 0 || (D->hybrid != 0 && D->hybrid != 1)) return KVQ_ERR_INVALID_ARG;
   if (D->residual > 1024 || D->sink > 256) return KVQ_ERR_UNSUPPORTED;
   if ((int64_t)D->batch * D->num_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
@@ -31,8 +31,9 @@ kvq_status check_view(const kvq_cache_desc& D, const kvq_cache_view* v) {
     return KVQ_ERR_INVALID_ARG;
   if (D.residual > 0 && (!v->k_res || !v->v_res)) return KVQ_ERR_INVALID_ARG;
   if (D.sink > 0 && (!v->k_sink || !v->v_sink || !v->sink_len)) return KVQ_ERR_INVALID_ARG;
-  const void* a16[] = {v->k_codes, v->v_codes, v->k_params, v->v_params,
-                       v->k_res,   v->v_res,   v->k_sink,   v->v_sink};
+  if (D.hybrid && D.capacity > 0 && (!v->k_mode || !v->v_mode)) return KVQ_ERR_INVALID_ARG;
+  const void* a16[] = {v->k_codes, v->v_codes, v->k_params, v->v_params, v->k_res,
+                       v->v_res,   v->k_sink,   v->v_sink,   v->k_mode,   v->v_mode};
   for (const void* p : a16)
     if (!aligned(p, 16)) return KVQ_ERR_MISALIGNED;
   const void* a4[] = {v->packed_len, v->res_len, v->res_head, v->err_word, v->sink_len};
@@ -58,6 +59,7 @@ size_t kvq_cache_bytes(const kvq_cache_desc* desc, int which) {
     case KVQ_ARRAY_PARAMS: return rows * (size_t)s.cap * s.Ng * sizeof(uint32_t);
     case KVQ_ARRAY_RESIDUAL: return rows * (size_t)s.Nr * s.d * sizeof(uint16_t);
     case KVQ_ARRAY_SINK: return rows * (size_t)s.Ns * s.d * sizeof(uint16_t);
+    case KVQ_ARRAY_MODE: return s.hybrid ? rows * (size_t)s.cap : 0;
     default: return 0;
   }
 }
@@ -220,6 +222,6 @@ const char* kvq_status_string(kvq_status status) {
   }
 }
 
-int32_t kvq_version(void) { return 110; }
+int32_t kvq_version(void) { return 120; }
 
 }  // extern "C"

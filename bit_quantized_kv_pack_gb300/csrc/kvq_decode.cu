@@ -122,6 +122,9 @@ cudaError_t launch_decode(const Dims& s, const DecodePlan& p, const kvq_cache_vi
   a.w_params[1] = v.v_params;
   a.w_res[0] = reinterpret_cast<__half*>(v.k_res);
   a.w_res[1] = reinterpret_cast<__half*>(v.v_res);
+  a.w_modes[0] = v.k_mode;
+  a.w_modes[1] = v.v_mode;
+  a.hybrid = s.hybrid;
   a.w_packed_len = v.packed_len;
   a.w_res_len = v.res_len;
   a.w_res_head = v.res_head;

@@ -43,11 +43,13 @@ struct DecodeArgs {
   uint8_t* w_codes[2];
   uint32_t* w_params[2];
   __half* w_res[2];
+  uint8_t* w_modes[2];  // mode bytes of a hybrid cache
   int32_t* w_packed_len;
   int32_t* w_res_len;
   int32_t* w_res_head;
   int Hkv, Hq, gq, qb, nqb, S, cap, Nr, d, row_bytes;
   int Ns;  // sink rows per (sequence, KV head) in the layout (0: no sink)
+  int hybrid;  // the fused step quantizes by the hybrid rule
   int early;  // fused step: counters and first tiles may be read before griddepcontrol.wait
   int Sp;  // tensor-core kernel: splits s < Sp take packed tokens, s >= Sp fp16 ones
   float qk_scale_log2;  // log2(e) / sqrt(d)

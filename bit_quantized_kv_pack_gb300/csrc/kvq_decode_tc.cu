@@ -580,8 +580,10 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
         src = *reinterpret_cast<const uint4*>(a.w_res[which] + (bh * a.Nr + rh) * D + lane * 8);
       float x[8];
       unpack8_f16(src, x);
-      uint32_t prm;
-      const uint32_t packed = quantize_quad<BITS>(x, prm);
+      uint32_t prm, asym = 1;
+      const uint32_t packed = quantize_quad<BITS>(x, prm, a.hybrid != 0, &asym);
+      const uint32_t modes = __ballot_sync(0xffffffffu, (lane & 3) == 0 && asym);
+      if (a.hybrid && lane == 0) a.w_modes[which][bh * a.cap + Lp] = mode_byte(modes, 0, NG);
       if (active) {
         const int64_t row = bh * a.cap + Lp;
         const int gi = lane >> 2, quad = lane & 3;

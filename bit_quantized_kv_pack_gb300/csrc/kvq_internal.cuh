@@ -17,6 +17,7 @@ constexpr int kGroup = 32;  // G: values per quantization group along head_dim
 struct Dims {
   int B, Hkv, d, bits, cap, Nr;
   int Ns;        // attention-sink window length (0: none)
+  int hybrid;    // 1: hybrid sym/asym groups with mode bytes
   int Ng;        // groups per token row
   int row_bytes; // packed code bytes per token row
 };
@@ -30,6 +31,7 @@ inline Dims dims_of(const kvq_cache_desc& D) {
   s.cap = D.capacity;
   s.Nr = D.residual;
   s.Ns = D.sink;
+  s.hybrid = D.hybrid;
   s.Ng = D.head_dim / kGroup;
   s.row_bytes = D.head_dim * D.bits / 8;
   return s;
@@ -56,8 +58,34 @@ __device__ __forceinline__ void set_error(uint32_t* err_word, uint32_t bit) {
 // bits) and the group's {scale, min} half2 bits.  All 32 lanes of the warp must
 // call it (the shuffles use the full mask); `active` lanes only matter for the
 // result, inactive lanes pass any finite values.
+//
+// hybrid: the group also gets the symmetric candidate (H1 of the header) and
+// keeps it when it can be stored and its squared error (H2) is strictly below
+// the asymmetric one's (H3, InnerQ page section 2.2); *asym_bit = 1 for the
+// asymmetric result, 0 for the symmetric one.
+
+// H2 over a quad: lane q sums e_j^2 over its values j = 8q .. 8q+7 in order,
+// then (S_0 + S_1) + (S_2 + S_3) by two shuffle-xor steps (every lane of the
+// quad ends with the same value).  Every operation is rounded on its own.
 template <int BITS>
-__device__ __forceinline__ uint32_t quantize_quad(const float (&x)[8], uint32_t& params_out) {
+__device__ __forceinline__ float quad_sq_error(const float (&x)[8], uint32_t packed, float sc,
+                                               float mn) {
+  constexpr uint32_t kMask = (1u << BITS) - 1u;
+  float acc = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float xh = __fadd_rn(mn, __fmul_rn((float)((packed >> (BITS * j)) & kMask), sc));
+    const float e = __fsub_rn(x[j], xh);
+    acc = __fadd_rn(acc, __fmul_rn(e, e));
+  }
+  acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 1));
+  acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 2));
+  return acc;
+}
+
+template <int BITS>
+__device__ __forceinline__ uint32_t quantize_quad(const float (&x)[8], uint32_t& params_out,
+                                                  bool hybrid = false, uint32_t* asym_bit = nullptr) {
   constexpr int kQmax = (1 << BITS) - 1;
   float mn = x[0], mx = x[0];
 #pragma unroll
@@ -94,7 +122,52 @@ __device__ __forceinline__ uint32_t quantize_quad(const float (&x)[8], uint32_t&
     packed |= (uint32_t)c << (BITS * j);
   }
   params_out = (uint32_t)__half_as_ushort(scale_h) | ((uint32_t)__half_as_ushort(min_h) << 16);
+  if (hybrid) {
+    constexpr int kHalf = 1 << (BITS - 1);
+    constexpr int kQs = kHalf - 1;
+    // H1: absmax / (2^(b-1) - 1); codes t + 2^(b-1); min = -2^(b-1) * scale
+    const float amax = fmaxf(fabsf(mn), fabsf(mx));
+    const __half ssh = __float2half_rn(__fdiv_rn(amax, (float)kQs));
+    const float ss = __half2float(ssh);
+    const __half smh = __float2half_rn(__fadd_rn(__fmul_rn(-(float)kHalf, ss), 0.0f));
+    const bool storable = (__half_as_ushort(smh) & 0x7c00u) != 0x7c00u;
+    // x / ss through the reciprocal, the IEEE divide near rounding boundaries
+    // (|x / ss| <= 2^(b-1), so the same 3-ulp argument as above holds)
+    const float rs = ss != 0.0f ? __frcp_rn(ss) : 0.0f;
+    uint32_t sp = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      int t = 0;
+      if (ss != 0.0f) {
+        float qf = __fmul_rn(x[j], rs);
+        if (fabsf(qf - floorf(qf) - 0.5f) < 1e-5f) qf = __fdiv_rn(x[j], ss);
+        t = __float2int_rn(qf);
+        t = min(max(t, -kQs), kQs);
+      }
+      sp |= (uint32_t)(t + kHalf) << (BITS * j);
+    }
+    // H2, H3
+    const float ea = quad_sq_error<BITS>(x, packed, s, __half2float(min_h));
+    const float es = quad_sq_error<BITS>(x, sp, ss, __half2float(smh));
+    const bool sym = storable && es < ea;
+    if (sym) {
+      packed = sp;
+      params_out = (uint32_t)__half_as_ushort(ssh) | ((uint32_t)__half_as_ushort(smh) << 16);
+    }
+    if (asym_bit) *asym_bit = sym ? 0u : 1u;
+  } else if (asym_bit) {
+    *asym_bit = 1u;
+  }
   return packed;
+}
+
+// The mode byte of a token row from a ballot of (quad lane 0 && asymmetric):
+// groups k0 .. k0 + ng - 1 of the warp sit at lanes 4k; bit g of the result is
+// group k0 + g's.
+__device__ __forceinline__ uint8_t mode_byte(uint32_t ballot, int k0, int ng) {
+  uint32_t m = 0;
+  for (int g = 0; g < ng; ++g) m |= ((ballot >> (4 * (k0 + g))) & 1u) << g;
+  return (uint8_t)m;
 }
 
 __device__ __forceinline__ void unpack8_f16(const uint4& v, float (&x)[8]) {

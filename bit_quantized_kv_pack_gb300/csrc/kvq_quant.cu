@@ -34,6 +34,7 @@ struct PackArgs {
   uint32_t* params[2];   // [B][Hkv][cap][Ng]
   __half* res[2];        // [B][Hkv][Nr][d]
   __half* sink[2];       // [B][Hkv][Ns][d]
+  uint8_t* modes[2];     // [B][Hkv][cap] mode bytes (hybrid caches)
   const int32_t* seq_lens;
   int32_t* packed_len;
   int32_t* res_len;
@@ -43,7 +44,7 @@ struct PackArgs {
   int Hkv, d, Ng, row_bytes, cap, Nr, Ns, Lmax;
 };
 
-template <int BITS>
+template <int BITS, bool HYB>
 __global__ void __launch_bounds__(kPackThreads) quantize_pack_kernel(PackArgs a) {
   const int bh = blockIdx.y;
   const int which = blockIdx.z;
@@ -92,8 +93,11 @@ __global__ void __launch_bounds__(kPackThreads) quantize_pack_kernel(PackArgs a)
     const int g = in_range ? (int)(gi[u] % a.Ng) : 0;
     float x[8];
     unpack8_f16(raw[u], x);
-    uint32_t prm;
-    const uint32_t packed = quantize_quad<BITS>(x, prm);  // all lanes take part
+    uint32_t prm, asym = 1;
+    const uint32_t packed = quantize_quad<BITS>(x, prm, HYB, &asym);  // all lanes take part
+    // the warp's 8 groups are whole token rows (Ng divides 8): each row's mode
+    // byte comes from one ballot
+    const uint32_t modes = HYB ? __ballot_sync(0xffffffffu, quad == 0 && asym) : 0u;
     if (!in_range) continue;
     if (t < ns) {
       __half* dst = a.sink[which] + ((int64_t)bh * a.Ns + t) * a.d + g * kGroup + quad * 8;
@@ -106,6 +110,7 @@ __global__ void __launch_bounds__(kPackThreads) quantize_pack_kernel(PackArgs a)
       else
         *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
       if (quad == 0) a.params[which][row * a.Ng + g] = prm;
+      if (HYB && quad == 0 && g == 0) a.modes[which][row] = mode_byte(modes, lane >> 2, a.Ng);
     } else if (t - ns >= npk_all) {
       const int j = t - ns - npk_all;  // ring slot; res_head = 0 after a prefill
       __half* dst = a.res[which] + ((int64_t)bh * a.Nr + j) * a.d + g * kGroup + quad * 8;
@@ -122,6 +127,7 @@ struct AppendArgs {
   uint8_t* codes[2];
   uint32_t* params[2];
   __half* res[2];
+  uint8_t* modes[2];
   int32_t* packed_len;
   int32_t* res_len;
   int32_t* res_head;
@@ -129,7 +135,7 @@ struct AppendArgs {
   int Hkv, d, Ng, row_bytes, cap, Nr;
 };
 
-template <int BITS>
+template <int BITS, bool HYB>
 __global__ void __launch_bounds__(1024) append_kernel(AppendArgs a) {
   // The decode of the same step may start launching now; it waits for this
   // grid to finish (griddepcontrol.wait) before it reads the cache.
@@ -140,7 +146,9 @@ __global__ void __launch_bounds__(1024) append_kernel(AppendArgs a) {
   const int nwarps = blockDim.x >> 5;
   const bool active = lane * 8 < a.d;
   // the new tokens do not depend on the counters: start their loads first
-  constexpr int kMaxItems = 4;  // items per warp whose new token is loaded up front
+  // items per warp whose new token is loaded up front (fewer for the hybrid
+  // quantizer, which needs the registers)
+  constexpr int kMaxItems = HYB ? 2 : 4;
   uint4 newv[kMaxItems];
 #pragma unroll
   for (int k = 0; k < kMaxItems; ++k) {
@@ -186,8 +194,12 @@ __global__ void __launch_bounds__(1024) append_kernel(AppendArgs a) {
       if (a.Nr > 0 && active) oldv = *reinterpret_cast<const uint4*>(ring_row + lane * 8);
       float x[8];
       unpack8_f16(oldv, x);
-      uint32_t prm;
-      const uint32_t packed = quantize_quad<BITS>(x, prm);
+      uint32_t prm, asym = 1;
+      const uint32_t packed = quantize_quad<BITS>(x, prm, HYB, &asym);
+      if (HYB) {
+        const uint32_t modes = __ballot_sync(0xffffffffu, (lane & 3) == 0 && asym);
+        if (lane == 0) (which ? a.modes[1] : a.modes[0])[bh * a.cap + pl] = mode_byte(modes, 0, a.Ng);
+      }
       if (active) {
         const int64_t row = bh * a.cap + pl;
         const int g = lane >> 2, quad = lane & 3;
@@ -233,6 +245,8 @@ cudaError_t launch_quantize_pack(const Dims& s, const kvq_cache_view& v, const _
   a.res[1] = reinterpret_cast<__half*>(v.v_res);
   a.sink[0] = reinterpret_cast<__half*>(v.k_sink);
   a.sink[1] = reinterpret_cast<__half*>(v.v_sink);
+  a.modes[0] = v.k_mode;
+  a.modes[1] = v.v_mode;
   a.seq_lens = seq_lens;
   a.packed_len = v.packed_len;
   a.res_len = v.res_len;
@@ -247,10 +261,17 @@ cudaError_t launch_quantize_pack(const Dims& s, const kvq_cache_view& v, const _
   a.Nr = s.Nr;
   a.Ns = s.Ns;
   a.Lmax = Lmax;
-  if (s.bits == 4)
-    quantize_pack_kernel<4><<<grid, kPackThreads, 0, st>>>(a);
-  else
-    quantize_pack_kernel<2><<<grid, kPackThreads, 0, st>>>(a);
+  if (s.bits == 4) {
+    if (s.hybrid)
+      quantize_pack_kernel<4, true><<<grid, kPackThreads, 0, st>>>(a);
+    else
+      quantize_pack_kernel<4, false><<<grid, kPackThreads, 0, st>>>(a);
+  } else {
+    if (s.hybrid)
+      quantize_pack_kernel<2, true><<<grid, kPackThreads, 0, st>>>(a);
+    else
+      quantize_pack_kernel<2, false><<<grid, kPackThreads, 0, st>>>(a);
+  }
   return cudaGetLastError();
 }
 
@@ -265,6 +286,8 @@ cudaError_t launch_append(const Dims& s, const kvq_cache_view& v, const __half* 
   a.params[1] = v.v_params;
   a.res[0] = reinterpret_cast<__half*>(v.k_res);
   a.res[1] = reinterpret_cast<__half*>(v.v_res);
+  a.modes[0] = v.k_mode;
+  a.modes[1] = v.v_mode;
   a.packed_len = v.packed_len;
   a.res_len = v.res_len;
   a.res_head = v.res_head;
@@ -278,10 +301,17 @@ cudaError_t launch_append(const Dims& s, const kvq_cache_view& v, const __half* 
   // one warp per (KV head, K or V) item, up to 32 warps (then more items per warp)
   const int items = 2 * s.Hkv;
   const int threads = 32 * (items < 32 ? items : 32);
-  if (s.bits == 4)
-    append_kernel<4><<<s.B, threads, 0, st>>>(a);
-  else
-    append_kernel<2><<<s.B, threads, 0, st>>>(a);
+  if (s.bits == 4) {
+    if (s.hybrid)
+      append_kernel<4, true><<<s.B, threads, 0, st>>>(a);
+    else
+      append_kernel<4, false><<<s.B, threads, 0, st>>>(a);
+  } else {
+    if (s.hybrid)
+      append_kernel<2, true><<<s.B, threads, 0, st>>>(a);
+    else
+      append_kernel<2, false><<<s.B, threads, 0, st>>>(a);
+  }
   return cudaGetLastError();
 }
 

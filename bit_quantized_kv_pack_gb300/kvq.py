@@ -37,6 +37,7 @@ KVQ_ARRAY_CODES = 0
 KVQ_ARRAY_PARAMS = 1
 KVQ_ARRAY_RESIDUAL = 2
 KVQ_ARRAY_SINK = 3
+KVQ_ARRAY_MODE = 4
 
 # Every function the header declares (the tests check the library exports them).
 EXPORTS = ("kvq_cache_bytes", "kvq_decode_workspace_bytes", "kvq_quantize_pack", "kvq_append",
@@ -49,13 +50,14 @@ class CacheDesc(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("bits", ctypes.c_int32), ("group", ctypes.c_int32),
                 ("capacity", ctypes.c_int32), ("residual", ctypes.c_int32),
-                ("sink", ctypes.c_int32)]
+                ("sink", ctypes.c_int32), ("hybrid", ctypes.c_int32)]
 
 
 class CacheView(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "k_codes", "v_codes", "k_params", "v_params", "k_res", "v_res",
-        "packed_len", "res_len", "res_head", "err_word", "k_sink", "v_sink", "sink_len")]
+        "packed_len", "res_len", "res_head", "err_word", "k_sink", "v_sink", "sink_len",
+        "k_mode", "v_mode")]
 
 
 class KvqError(RuntimeError):
@@ -166,11 +168,14 @@ class KVCache:
     """One layer's packed cache in device memory (torch tensors in the layout of
     include/kvq.h).  Holds the description and the view the calls take.
     ``sink`` > 0 keeps the first ``sink`` tokens of each sequence in fp16 (the
-    attention-sink window, fixed after the prefill)."""
+    attention-sink window, fixed after the prefill); ``hybrid=1`` quantizes each
+    group symmetrically or asymmetrically, whichever reconstructs it better, and
+    keeps a mode byte per packed row."""
 
     def __init__(self, batch, num_kv_heads, head_dim, bits, capacity, residual, device="cuda",
-                 sink=0):
-        self.desc = CacheDesc(batch, num_kv_heads, head_dim, bits, 32, capacity, residual, sink)
+                 sink=0, hybrid=0):
+        self.desc = CacheDesc(batch, num_kv_heads, head_dim, bits, 32, capacity, residual, sink,
+                              hybrid)
         self.device = torch.device(device)
         B, H, d = batch, num_kv_heads, head_dim
         rb, ng = d * bits // 8, d // 32
@@ -183,6 +188,9 @@ class KVCache:
         self.v_res = torch.zeros(B, H, residual, d, dtype=torch.float16, **kw)
         self.k_sink = torch.zeros(B, H, sink, d, dtype=torch.float16, **kw)
         self.v_sink = torch.zeros(B, H, sink, d, dtype=torch.float16, **kw)
+        ncap = capacity if hybrid else 0
+        self.k_mode = torch.zeros(B, H, ncap, dtype=torch.uint8, **kw)
+        self.v_mode = torch.zeros(B, H, ncap, dtype=torch.uint8, **kw)
         # packed_len, res_len, res_head, sink_len
         self.counters = torch.zeros(4, B, dtype=torch.int32, **kw)
         self.err = torch.zeros(4, dtype=torch.int32, **kw)
@@ -193,7 +201,8 @@ class KVCache:
         return CacheView(r(self.k_codes), r(self.v_codes), r(self.k_params), r(self.v_params),
                          r(self.k_res), r(self.v_res), _ptr(self.counters[0]),
                          _ptr(self.counters[1]), _ptr(self.counters[2]), _ptr(self.err),
-                         r(self.k_sink), r(self.v_sink), _ptr(self.counters[3]))
+                         r(self.k_sink), r(self.v_sink), _ptr(self.counters[3]),
+                         r(self.k_mode), r(self.v_mode))
 
     @property
     def packed_len(self):

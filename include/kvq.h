@@ -16,6 +16,8 @@
  *   - same page, section 5.1: cache pointers aligned to 128 bytes.
  *   - "KV cache quantization InnerQ" page, section 2.1: groups of G = 32 along the
  *     inner (head_dim) dimension, one row shares its group parameters.
+ *   - same page, section 2.2: hybrid mode, each group quantized symmetrically or
+ *     asymmetrically, whichever reconstructs it better, with a 1-bit mode mask.
  *   - same page, section 2.3: recent-token window; a new token enters the window and,
  *     when the window is full, its oldest token is quantized into the main cache.
  *     Also the attention-sink window: the first tokens stay in full precision, set
@@ -49,6 +51,10 @@
  *            Ring of the most recent tokens, kept in full precision.
  *   sink     fp16   [B][Hkv][S][d]
  *            The first sink_len[b] tokens of sequence b, kept in full precision.
+ *   mode     uint8  [B][Hkv][cap]   (hybrid caches only)
+ *            Bit g of a packed row's byte = mode of its group g: 1 asymmetric,
+ *            0 symmetric.  Both modes dequantize as min + code * scale, so
+ *            decode does not read it.
  *   packed_len, res_len, res_head, sink_len   int32 [B]   (device)
  *            Per sequence: packed tokens, residual tokens, ring slot of the oldest
  *            residual token, sink tokens.  Sequence b attends over
@@ -67,6 +73,15 @@
  *       clamp(rint(((float)x_j - (float)mn) / s), 0, 2^b - 1)   fp32 subtract and divide,
  *       rint = round half to even
  *   Q5  pack as in the layout above
+ * Hybrid caches (desc.hybrid = 1) replace Q1-Q4 per group by H1-H3:
+ *   H1  symmetric candidate: a = max_j |x_j|, h = 2^(b-1), scale_s = fp16_rne(a / (h - 1))
+ *       (fp32 divide), s = (float)scale_s, t_j = clamp(rint(x_j / s), -(h-1), h-1)
+ *       (fp32 divide; 0 if s == 0), code = t_j + h, min_s = fp16(-h * s + 0.0f).
+ *   H2  error of a candidate (fp32, each operation rounded, no fused multiply-add):
+ *       e_j = x_j - (min + (float)code_j * scale); S_q = sum of e_j^2 over
+ *       j = 8q .. 8q+7 in index order; E = (S_0 + S_1) + (S_2 + S_3).
+ *   H3  the symmetric candidate is stored when min_s is finite and E_s < E_a; otherwise
+ *       the asymmetric one (Q1-Q4).  Mode bit 0 = symmetric, 1 = asymmetric.
  *   Q6  with ns = min(S, L) and nr = min(Nr, L - ns): tokens [0, ns) are copied to the
  *       sink, tokens [ns, L - nr) are packed into slots [0, L - ns - nr), the last nr
  *       are copied to the residual ring in order, res_head = 0.
@@ -122,10 +137,12 @@ typedef struct {
   int32_t capacity;     /* packed tokens per (sequence, KV head), >= 0 */
   int32_t residual;     /* Nr: 0..1024 */
   int32_t sink;         /* S: 0..256, first tokens kept fp16 (attention-sink window) */
+  int32_t hybrid;       /* 0: asymmetric groups; 1: hybrid sym/asym groups with a mode mask */
 } kvq_cache_desc;
 
 /* Device pointers of one layer's cache (layout above).  k_res/v_res may be NULL
- * when residual == 0, k_sink/v_sink/sink_len when sink == 0. */
+ * when residual == 0, k_sink/v_sink/sink_len when sink == 0, k_mode/v_mode when
+ * hybrid == 0. */
 typedef struct {
   uint8_t* k_codes;
   uint8_t* v_codes;
@@ -140,6 +157,8 @@ typedef struct {
   uint16_t* k_sink; /* fp16 bits */
   uint16_t* v_sink;
   int32_t* sink_len;
+  uint8_t* k_mode; /* mode bytes [B][Hkv][cap] */
+  uint8_t* v_mode;
 } kvq_cache_view;
 
 /* Which array kvq_cache_bytes sizes (each of K and V has one of each). */
@@ -147,6 +166,7 @@ typedef struct {
 #define KVQ_ARRAY_PARAMS 1
 #define KVQ_ARRAY_RESIDUAL 2
 #define KVQ_ARRAY_SINK 3
+#define KVQ_ARRAY_MODE 4
 
 /* Bytes of one array of the layout (for K or for V; allocate twice).
  * Returns 0 for an invalid desc or `which`. */
@@ -166,7 +186,8 @@ size_t kvq_decode_workspace_bytes(const kvq_cache_desc* desc, int32_t num_q_head
  * tokens are copied to the sink (InnerQ page section 2.3), the next ones become
  * codes and params in slots [0, ...), the last min(Nr, ...) are copied to the
  * residual ring; packed_len[b], res_len[b], res_head[b] = 0 and (S > 0)
- * sink_len[b] are written.
+ * sink_len[b] are written.  A hybrid cache quantizes by H1-H3 (InnerQ page
+ * section 2.2) and writes each packed row's mode byte.
  * A sequence with more than cap packed tokens sets KVQ_ERRBIT_CAPACITY and stores
  * only the first cap (packed_len[b] = cap).  Asynchronous on `stream`. */
 kvq_status kvq_quantize_pack(const kvq_cache_desc* desc, const kvq_cache_view* view,
@@ -180,7 +201,8 @@ kvq_status kvq_quantize_pack(const kvq_cache_desc* desc, const kvq_cache_view* v
  * is quantized by Q1-Q5 into packed slot packed_len (which then grows by one)
  * and the new token takes its ring slot (res_head advances); otherwise the new
  * token goes to slot (res_head + res_len) % Nr and res_len grows.  With Nr == 0
- * the new token is packed directly.  The sink is never written: it stays as the
+ * the new token is packed directly (a hybrid cache by H1-H3, with its mode
+ * byte).  The sink is never written: it stays as the
  * prefill left it.  A full packed cache sets KVQ_ERRBIT_CAPACITY and leaves that
  * sequence unchanged.  Asynchronous. */
 kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache_view* view,
@@ -302,7 +324,7 @@ kvq_status kvq_read_error(const kvq_cache_view* view, uint32_t* word_out, void* 
 const char* kvq_status_string(kvq_status status);
 
 /* Library version as 10000 * major + 100 * minor + patch. */
-int32_t kvq_version(void); /* 110: the attention-sink window and fp32 output */
+int32_t kvq_version(void); /* 120: hybrid sym/asym groups; 110: sink window, fp32 output */
 
 #ifdef __cplusplus
 }

@@ -11,12 +11,12 @@ ATOL = 2e-3   # max abs error of the fp16 attention output vs the fp64 oracle
 RTOL_L2 = 1e-3  # relative L2 error of the same
 
 
-def gpu_cache(B, H, d, bits, cap, Nr, dev="cuda", sink=0):
-    return kvq.KVCache(B, H, d, bits, cap, Nr, device=dev, sink=sink)
+def gpu_cache(B, H, d, bits, cap, Nr, dev="cuda", sink=0, hybrid=0):
+    return kvq.KVCache(B, H, d, bits, cap, Nr, device=dev, sink=sink, hybrid=hybrid)
 
 
-def ref_cache(B, H, d, bits, cap, Nr, sink=0):
-    return oracle.Cache(B, H, d, bits, cap, Nr, sink)
+def ref_cache(B, H, d, bits, cap, Nr, sink=0, hybrid=0):
+    return oracle.Cache(B, H, d, bits, cap, Nr, sink, hybrid)
 
 
 def to_np(t: torch.Tensor) -> np.ndarray:
@@ -36,7 +36,10 @@ def assert_cache_equal(g, r, batches=None):
         assert pl[b] == r.packed_len[i], (b, pl[b], r.packed_len[i])
         assert rl[b] == r.res_len[i] and rh[b] == r.res_head[i], b
         n = int(r.packed_len[i])
-        for name in ("k_codes", "v_codes", "k_params", "v_params"):
+        names = ("k_codes", "v_codes", "k_params", "v_params")
+        if r.desc.hybrid:
+            names += ("k_mode", "v_mode")
+        for name in names:
             got = to_np(getattr(g, name)[b, :, :n]).view(getattr(r, name).dtype)
             want = getattr(r, name)[i, :, :n]
             if not np.array_equal(got, want):

@@ -30,7 +30,7 @@ def test_header_declares_and_library_exports(lib):
     assert set(kvq.EXPORTS) <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in kvq.h but not exported"
-    assert kvq.kvq_version() == 110
+    assert kvq.kvq_version() == 120
 
 
 def test_status_strings(lib):
@@ -55,10 +55,12 @@ def test_cache_bytes(lib):
     assert kvq.kvq_cache_bytes(D2, kvq.KVQ_ARRAY_PARAMS) == 2 * 8 * 1000 * 2 * 4
     assert kvq.kvq_cache_bytes(D, kvq.KVQ_ARRAY_SINK) == 0
     assert kvq.kvq_cache_bytes(_desc(sink=32), kvq.KVQ_ARRAY_SINK) == 2 * 8 * 32 * 128 * 2
+    assert kvq.kvq_cache_bytes(D, kvq.KVQ_ARRAY_MODE) == 0
+    assert kvq.kvq_cache_bytes(_desc(hybrid=1), kvq.KVQ_ARRAY_MODE) == 2 * 8 * 1000
     assert kvq.kvq_cache_bytes(D, 7) == 0
     for bad in (dict(bits=3), dict(head_dim=96), dict(head_dim=100), dict(group=64),
                 dict(batch=0), dict(residual=-1), dict(residual=2000), dict(capacity=-5),
-                dict(sink=-1), dict(sink=257)):
+                dict(sink=-1), dict(sink=257), dict(hybrid=2), dict(hybrid=-1)):
         assert kvq.kvq_cache_bytes(_desc(**bad), kvq.KVQ_ARRAY_CODES) == 0, bad
 
 
@@ -72,7 +74,7 @@ def test_workspace_bytes(lib):
 
 def _view(addr=0x10000):
     # fake, well-aligned addresses: only ever passed to calls the host rejects
-    return kvq.CacheView(*[ctypes.c_void_p(addr + 0x1000 * i) for i in range(13)])
+    return kvq.CacheView(*[ctypes.c_void_p(addr + 0x1000 * i) for i in range(15)])
 
 
 @pytest.mark.parametrize("kw,expect", [
@@ -83,6 +85,7 @@ def _view(addr=0x10000):
     (dict(batch=0), kvq.KVQ_ERR_INVALID_ARG),
     (dict(sink=-2), kvq.KVQ_ERR_INVALID_ARG),
     (dict(sink=512), kvq.KVQ_ERR_UNSUPPORTED),
+    (dict(hybrid=3), kvq.KVQ_ERR_INVALID_ARG),
 ])
 def test_rejects_bad_desc(lib, kw, expect):
     D, V = _desc(**kw), _view()
@@ -143,6 +146,12 @@ def test_rejects_bad_sink_view(lib):
     V = _view()
     V.sink_len = 0x10002
     assert lib.kvq_append(ctypes.byref(D), ctypes.byref(V), P(0x100000), P(0x200000), None) == kvq.KVQ_ERR_MISALIGNED
+    # a hybrid cache needs its mode arrays
+    for field in ("k_mode", "v_mode"):
+        V = _view()
+        setattr(V, field, 0)
+        assert lib.kvq_append(ctypes.byref(_desc(hybrid=1)), ctypes.byref(V), P(0x100004), P(0x200000),
+                              None) == kvq.KVQ_ERR_INVALID_ARG, field
     # sink == 0: NULL sink pointers pass the view check (the misaligned k_new then fails)
     V = _view()
     V.k_sink = V.v_sink = V.sink_len = 0
