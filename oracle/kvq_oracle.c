@@ -15,6 +15,8 @@
  *     even; a zero scale gives all-zero codes; a -0 minimum is stored as +0.
  *   Pack (Q5): codes as a little-endian bit string, 32 consecutive head_dim
  *     values per group (InnerQ page, section 3.2); params as half2 {scale, min}.
+ *     Bit widths 2, 4 and 3 (eight 3-bit codes per 24 bits, TurboQuant page,
+ *     section 3.1, on the same asymmetric rule).
  *   Hybrid mode (H1-H3, optional): per group a symmetric candidate beside the
  *     asymmetric one, the smaller squared error wins and a 1-bit mask records
  *     the choice (InnerQ page, section 2.2).  Readings of points the page leaves
@@ -257,13 +259,17 @@ int oracle_quantize_group_hybrid(const uint16_t* x, int bits, uint8_t* codes, ui
   return 0;
 }
 
-/* Q5: pack d codes of one token row; returns bytes written (d * bits / 8). */
+/* Q5: pack d codes of one token row; returns bytes written (d * bits / 8).
+ * Code e occupies bits [e*bits, e*bits + bits) of the row's little-endian bit
+ * string; a 3-bit code can straddle two bytes. */
 int oracle_pack_row(const uint8_t* codes, int d, int bits, uint8_t* out) {
   int nbytes = d * bits / 8;
   memset(out, 0, (size_t)nbytes);
   for (int e = 0; e < d; ++e) {
     int bit = e * bits;
-    out[bit / 8] |= (uint8_t)(codes[e] << (bit % 8));
+    unsigned v = (unsigned)codes[e] << (bit % 8); /* up to 16 bits wide */
+    out[bit / 8] |= (uint8_t)(v & 0xffu);
+    if (bit % 8 + bits > 8) out[bit / 8 + 1] |= (uint8_t)(v >> 8);
   }
   return nbytes;
 }
@@ -273,7 +279,9 @@ void oracle_unpack_row(const uint8_t* packed, int d, int bits, uint8_t* codes) {
   int mask = (1 << bits) - 1;
   for (int e = 0; e < d; ++e) {
     int bit = e * bits;
-    codes[e] = (uint8_t)((packed[bit / 8] >> (bit % 8)) & mask);
+    unsigned v = packed[bit / 8];
+    if (bit % 8 + bits > 8) v |= (unsigned)packed[bit / 8 + 1] << 8;
+    codes[e] = (uint8_t)((v >> (bit % 8)) & (unsigned)mask);
   }
 }
 
@@ -302,7 +310,7 @@ typedef struct {
 
 static int desc_ok(const oracle_desc* D) {
   return D && D->batch >= 1 && D->num_kv_heads >= 1 && D->head_dim >= 32 && D->head_dim <= 256 &&
-         D->head_dim % 32 == 0 && (D->bits == 2 || D->bits == 4) && D->group == 32 &&
+         D->head_dim % 32 == 0 && D->bits >= 2 && D->bits <= 4 && D->group == 32 &&
          D->capacity >= 0 && D->residual >= 0 && D->residual <= 1024 && D->sink >= 0 &&
          D->sink <= 256 && (D->hybrid == 0 || D->hybrid == 1);
 }

@@ -84,7 +84,7 @@ def test_capacity_and_bad_length():
     assert err & 8 and c2.packed_len[0] == 16
 
 
-@pytest.mark.parametrize("bits,Nr", [(4, 8), (2, 5), (4, 0)])
+@pytest.mark.parametrize("bits,Nr", [(4, 8), (2, 5), (4, 0), (3, 6)])
 def test_append_equals_prefill(bits, Nr):
     rng = np.random.default_rng(11 + bits + Nr)
     B, H, d, L, L0 = 2, 3, 64, 37, 3
@@ -191,7 +191,8 @@ def test_residual_only_is_textbook_attention():
         assert np.allclose(out[b, 0], _textbook(q[b, 0], k[b, 0], v[b, 0]), rtol=1e-12, atol=1e-13)
 
 
-@pytest.mark.parametrize("bits,d,gq", [(4, 32, 1), (2, 64, 2), (4, 128, 4), (2, 32, 3)])
+@pytest.mark.parametrize("bits,d,gq", [(4, 32, 1), (2, 64, 2), (4, 128, 4), (2, 32, 3), (3, 128, 4),
+                                       (3, 32, 2)])
 def test_second_formulation_tiny(bits, d, gq):
     rng = np.random.default_rng(bits * 100 + d + gq)
     B, H, Nr = 2, 2, 3

@@ -62,7 +62,7 @@ def test_golden_quant_cases(case):
     assert np.array_equal(codes, case["codes"]), codes
 
 
-@pytest.mark.parametrize("case", PACK_CASES, ids=["int4", "int2"])
+@pytest.mark.parametrize("case", PACK_CASES, ids=["int4", "int2", "int3"])
 def test_golden_pack_cases(case):
     got = oracle.pack_row(case["codes"], case["bits"])
     assert np.array_equal(got, case["bytes"]), got
@@ -120,7 +120,7 @@ def _brute_force_codes(x16, mn, s, bits):
     return exp, ambiguous, exact_tie
 
 
-@pytest.mark.parametrize("bits", [4, 2])
+@pytest.mark.parametrize("bits", [4, 2, 3])
 def test_brute_force_and_bounds(bits):
     rng = np.random.default_rng(7 + bits)
     qmax = (1 << bits) - 1
@@ -164,7 +164,7 @@ def test_brute_force_and_bounds(bits):
 
 def test_exact_ties_go_to_even():
     # values k + 0.5 on a unit-scale grid: exact ties in every arithmetic
-    for bits in (2, 4):
+    for bits in (2, 3, 4):
         qmax = (1 << bits) - 1
         x = np.zeros(32)
         x[1] = qmax
@@ -177,7 +177,7 @@ def test_exact_ties_go_to_even():
         assert np.array_equal(got, want.astype(np.uint8))
 
 
-@pytest.mark.parametrize("bits,d", [(4, 128), (2, 128), (4, 64), (2, 32)])
+@pytest.mark.parametrize("bits,d", [(4, 128), (2, 128), (4, 64), (2, 32), (3, 128), (3, 64), (3, 32)])
 def test_pack_bit_order_matches_unpackbits(bits, d):
     rng = np.random.default_rng(bits * 1000 + d)
     codes = rng.integers(0, 1 << bits, d).astype(np.uint8)
