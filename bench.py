@@ -176,6 +176,15 @@ class ClockSampler:
 
 # ------------------------------------------------------------ our arm ------
 
+def workload_for(num, bits=0):
+    """Workload `num`, with its code width changed to `bits` when given."""
+    from bit_quantized_kv_pack_gb300 import synth
+    w = synth.WORKLOADS[num]
+    if bits and bits != w.bits:
+        w = synth.scaled(w, bits=bits, name=w.name.replace(f"int{w.bits}", f"int{bits}"))
+    return w
+
+
 def packed_per_seq(w, lens, sink=0):
     """Packed tokens of each sequence after the prefill: its length minus the
     sink rows and the fp16 window."""
@@ -196,12 +205,12 @@ def workload_config(w, packed_tokens, extra=None):
     return cfg
 
 
-def build_state(dev, steps, warmup, e2e_steps, l2_bytes, workload, sink=0, hybrid=0):
+def build_state(dev, steps, warmup, e2e_steps, l2_bytes, workload, sink=0, hybrid=0, bits=0):
     """Pack the workload once, clone it into enough copies to exceed 3x L2,
     and pre-generate the per-step queries and new tokens on the device."""
     from bit_quantized_kv_pack_gb300 import kvq, synth
 
-    w = synth.WORKLOADS[workload]
+    w = workload_for(workload, bits)
     k, v, lens = w.prefill(device=dev)
     npk_b = packed_per_seq(w, lens, sink)
     npk0 = sum(npk_b)  # packed tokens over the batch, per KV head
@@ -286,7 +295,7 @@ def run_ours(args, rank, world, local):
     l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
 
     st = build_state(dev, args.steps, args.warmup, args.e2e_steps, l2, args.workload, args.sink,
-                     args.hybrid)
+                     args.hybrid, args.bits)
     w, ncopy = st["w"], st["nslot"]
     K = args.steps
     reps, rem = divmod(K, ncopy)  # K steps = reps whole passes over the copies + rem
@@ -330,7 +339,7 @@ def run_ours(args, rank, world, local):
     all_bytes_gbs = (step_bytes + res_bytes + qo_bytes) / (ms_per_step * 1e-3) / 1e9
     # the step is one fused launch on the tensor-core path (append + decode),
     # else an append and a decode launch
-    fused = w.head_dim == 128 and 1 <= w.num_q_heads // w.num_kv_heads <= 4
+    fused = w.head_dim == 128 and w.bits != 3 and 1 <= w.num_q_heads // w.num_kv_heads <= 4
     launches = 1 if fused else 2
     if fused:  # the dominant kernel is the step kernel itself
         rf_kernel, rf_us = "decode_step (append + split-KV decode + combine, one launch)", ms_per_step * 1e3
@@ -362,7 +371,7 @@ def run_ours(args, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "u4 codes, fp16 scale/min, fp32 accumulate",
+        "dtype": f"u{w.bits} codes, fp16 scale/min, fp32 accumulate",
         "data": "synthetic (seeded SplitMix64 + Box-Muller, fp16)",
         "config": workload_config(w, st["npk0"], {
             "l2": f"rotating {ncopy} cache copies ({ncopy * step_bytes / 2**20:.0f} MiB "
@@ -375,7 +384,7 @@ def run_ours(args, rank, world, local):
         "roofline": {"bound": "hbm", "kernel": rf_kernel,
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": profiled_traffic(w.name, fused) if not (args.sink or args.hybrid) else None,
+                     "traffic": profiled_traffic(w.name, fused) if not (args.sink or args.hybrid or args.bits) else None,
                      "algorithmic_bytes_per_launch": step_bytes,
                      "us_per_launch": round(rf_us, 3)},
         "decode_only": {"us_per_launch": round(dec_ms_per_launch * 1e3, 3),
@@ -385,9 +394,10 @@ def run_ours(args, rank, world, local):
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(args.cpu_seconds, workload=args.workload, sink=args.sink)
+        res["cpu_baseline"] = cpu_baseline(args.cpu_seconds, workload=args.workload, sink=args.sink,
+                                           bits=args.bits)
         res["cpu_baseline_all_cores"] = cpu_baseline_all_cores(res["cpu_baseline"], args.workload,
-                                                               sink=args.sink)
+                                                               sink=args.sink, bits=args.bits)
     return res
 
 
@@ -432,13 +442,14 @@ def run_e2e(st, args):
 
 # ---------------------------------------------------------- oracle arm -----
 
-def cpu_baseline(seconds: float, steps: int | None = None, workload: int = WORKLOAD, sink: int = 0):
+def cpu_baseline(seconds: float, steps: int | None = None, workload: int = WORKLOAD, sink: int = 0,
+                 bits: int = 0):
     """The CPU oracle as it stands (single thread) on whole steps of the same
     workload: append + fp64 decode of every query head."""
     import oracle
     from bit_quantized_kv_pack_gb300 import synth
 
-    w = synth.WORKLOADS[workload]
+    w = workload_for(workload, bits)
     k, v, lens = w.prefill()
     npk_b = packed_per_seq(w, lens, sink)
     npk0 = sum(npk_b)
@@ -470,10 +481,10 @@ def _oracle_units_worker(job):
     """One process of the all-cores CPU baseline: whole decode steps (append +
     fp64 decode of every query head) for its (sequence, KV head) units, each in
     a cache of its own.  Returns the seconds of its step loop."""
-    workload, units, n_steps, sink = job
+    workload, units, n_steps, sink, bits = job
     import oracle
     from bit_quantized_kv_pack_gb300 import synth
-    w = synth.WORKLOADS[workload]
+    w = workload_for(workload, bits)
     k, v, lens = w.prefill()
     gq = w.num_q_heads // w.num_kv_heads
     caches = []
@@ -494,13 +505,13 @@ def _oracle_units_worker(job):
 
 
 def cpu_baseline_all_cores(single: dict, workload: int = WORKLOAD, seconds: float = 10.0,
-                           sink: int = 0):
+                           sink: int = 0, bits: int = 0):
     """The same oracle on all host cores: (sequence, KV head) units spread over
     spawned processes, each running whole steps on its units; throughput = step
     bytes x steps / the slowest process's time."""
     import multiprocessing as mp
     from bit_quantized_kv_pack_gb300 import synth
-    w = synth.WORKLOADS[workload]
+    w = workload_for(workload, bits)
     units = [(b, h) for b in range(w.batch) for h in range(w.num_kv_heads)]
     procs = max(1, min(os.cpu_count() or 1, len(units)))
     share = [units[i::procs] for i in range(procs)]
@@ -511,7 +522,7 @@ def cpu_baseline_all_cores(single: dict, workload: int = WORKLOAD, seconds: floa
     # of being restarted, and a stuck one times out
     try:
         with ProcessPoolExecutor(max_workers=procs, mp_context=mp.get_context("spawn")) as ex:
-            futs = [ex.submit(_oracle_units_worker, (workload, sh, n_steps, sink)) for sh in share]
+            futs = [ex.submit(_oracle_units_worker, (workload, sh, n_steps, sink, bits)) for sh in share]
             times = [f.result(timeout=600) for f in futs]
     except Exception as e:  # report, do not hang the benchmark
         return {"value": None, "unit": "GB/s", "cores": procs, "kind": "oracle",
@@ -539,7 +550,7 @@ def run_reference(args, rank, world):
     import oracle
     from bit_quantized_kv_pack_gb300 import synth
 
-    w = synth.WORKLOADS[args.workload]
+    w = workload_for(args.workload, args.bits)
     k, v, lens = w.prefill()
     npk_b = packed_per_seq(w, lens, args.sink)
     n_total = args.warmup + args.steps
@@ -681,6 +692,8 @@ def main():
                     help="attention-sink rows kept fp16 per sequence (0..256; default 0)")
     ap.add_argument("--hybrid", type=int, default=0, choices=(0, 1),
                     help="1: hybrid symmetric/asymmetric groups with mode bytes (default 0)")
+    ap.add_argument("--bits", type=int, default=0, choices=(0, 2, 3, 4),
+                    help="code width instead of the workload's own (3: the 3-bit variant)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

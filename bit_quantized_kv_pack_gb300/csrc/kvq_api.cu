@@ -15,7 +15,7 @@ kvq_status check_desc(const kvq_cache_desc* D) {
   if (D->batch < 1 || D->num_kv_heads < 1 || D->capacity < 0 || D->residual < 0 ||
       D->group != kvq::kGroup || D->head_dim < 32 || D->head_dim % 32 != 0)
     return KVQ_ERR_INVALID_ARG;
-  if (D->bits != 2 && D->bits != 4) return KVQ_ERR_UNSUPPORTED;
+  if (D->bits < 2 || D->bits > 4) return KVQ_ERR_UNSUPPORTED;
   if (D->head_dim != 32 && D->head_dim != 64 && D->head_dim != 128 && D->head_dim != 256)
     return KVQ_ERR_UNSUPPORTED;
   if (D->sink < 0 || (D->hybrid != 0 && D->hybrid != 1)) return KVQ_ERR_INVALID_ARG;
@@ -222,6 +222,6 @@ const char* kvq_status_string(kvq_status status) {
   }
 }
 
-int32_t kvq_version(void) { return 120; }
+int32_t kvq_version(void) { return 130; }
 
 }  // extern "C"

@@ -1066,7 +1066,9 @@ cudaError_t launch_bits(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
 }  // namespace
 
 bool tc_supported(const kvq_cache_desc& D, int gq) {
-  return D.head_dim == 128 && gq >= 1 && gq <= QB && D.capacity > 0 && encode_fn() != nullptr;
+  // 3-bit codes straddle the 16-bit halves the code-to-fp16 conversion works on
+  return D.head_dim == 128 && D.bits != 3 && gq >= 1 && gq <= QB && D.capacity > 0 &&
+         encode_fn() != nullptr;
 }
 
 int tc_threads() { return NTHREADS; }

@@ -161,6 +161,25 @@ __device__ __forceinline__ uint32_t quantize_quad(const float (&x)[8], uint32_t&
   return packed;
 }
 
+// Store a group's 32 codes at its first byte `grp` (4 * BITS bytes; lane q of
+// the quad holds codes 8q .. 8q+7 packed little-endian in 8 * BITS bits).  INT4
+// and INT2: one 32- or 16-bit store per lane.  3-bit: the four 24-bit pieces
+// are spliced into three 32-bit words, written by lanes 0-2.  All 32 lanes must
+// call it; only `active` lanes store.
+template <int BITS>
+__device__ __forceinline__ void store_group_codes(uint8_t* grp, uint32_t packed, int quad,
+                                                  bool active) {
+  if (BITS == 3) {
+    const uint32_t next = __shfl_down_sync(0xffffffffu, packed, 1);
+    if (active && quad < 3)
+      reinterpret_cast<uint32_t*>(grp)[quad] = (packed >> (8 * quad)) | (next << (24 - 8 * quad));
+  } else if (BITS == 4) {
+    if (active) reinterpret_cast<uint32_t*>(grp)[quad] = packed;
+  } else {
+    if (active) reinterpret_cast<uint16_t*>(grp)[quad] = (uint16_t)packed;
+  }
+}
+
 // The mode byte of a token row from a ballot of (quad lane 0 && asymmetric):
 // groups k0 .. k0 + ng - 1 of the warp sit at lanes 4k; bit g of the result is
 // group k0 + g's.

@@ -98,17 +98,15 @@ __global__ void __launch_bounds__(kPackThreads) quantize_pack_kernel(PackArgs a)
     // the warp's 8 groups are whole token rows (Ng divides 8): each row's mode
     // byte comes from one ballot
     const uint32_t modes = HYB ? __ballot_sync(0xffffffffu, quad == 0 && asym) : 0u;
+    const bool to_pack = in_range && t >= ns && t - ns < npk;
+    const int64_t row = (int64_t)bh * a.cap + (t - ns);
+    store_group_codes<BITS>(to_pack ? a.codes[which] + row * a.row_bytes + g * (4 * BITS) : nullptr,
+                            packed, quad, to_pack);
     if (!in_range) continue;
     if (t < ns) {
       __half* dst = a.sink[which] + ((int64_t)bh * a.Ns + t) * a.d + g * kGroup + quad * 8;
       *reinterpret_cast<uint4*>(dst) = raw[u];
-    } else if (t - ns < npk) {
-      const int64_t row = (int64_t)bh * a.cap + (t - ns);
-      uint8_t* dst = a.codes[which] + row * a.row_bytes + g * (4 * BITS) + quad * BITS;
-      if (BITS == 4)
-        *reinterpret_cast<uint32_t*>(dst) = packed;
-      else
-        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
+    } else if (to_pack) {
       if (quad == 0) a.params[which][row * a.Ng + g] = prm;
       if (HYB && quad == 0 && g == 0) a.modes[which][row] = mode_byte(modes, lane >> 2, a.Ng);
     } else if (t - ns >= npk_all) {
@@ -200,16 +198,10 @@ __global__ void __launch_bounds__(1024) append_kernel(AppendArgs a) {
         const uint32_t modes = __ballot_sync(0xffffffffu, (lane & 3) == 0 && asym);
         if (lane == 0) (which ? a.modes[1] : a.modes[0])[bh * a.cap + pl] = mode_byte(modes, 0, a.Ng);
       }
-      if (active) {
-        const int64_t row = bh * a.cap + pl;
-        const int g = lane >> 2, quad = lane & 3;
-        uint8_t* dst = codes_base + row * a.row_bytes + g * (4 * BITS) + quad * BITS;
-        if (BITS == 4)
-          *reinterpret_cast<uint32_t*>(dst) = packed;
-        else
-          *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
-        if (quad == 0) params_base[row * a.Ng + g] = prm;
-      }
+      const int64_t row = bh * a.cap + pl;
+      const int g = lane >> 2, quad = lane & 3;
+      store_group_codes<BITS>(codes_base + row * a.row_bytes + g * (4 * BITS), packed, quad, active);
+      if (active && quad == 0) params_base[row * a.Ng + g] = prm;
     }
     if (a.Nr > 0 && active) *reinterpret_cast<uint4*>(ring_row + lane * 8) = nv;
   }
@@ -266,6 +258,11 @@ cudaError_t launch_quantize_pack(const Dims& s, const kvq_cache_view& v, const _
       quantize_pack_kernel<4, true><<<grid, kPackThreads, 0, st>>>(a);
     else
       quantize_pack_kernel<4, false><<<grid, kPackThreads, 0, st>>>(a);
+  } else if (s.bits == 3) {
+    if (s.hybrid)
+      quantize_pack_kernel<3, true><<<grid, kPackThreads, 0, st>>>(a);
+    else
+      quantize_pack_kernel<3, false><<<grid, kPackThreads, 0, st>>>(a);
   } else {
     if (s.hybrid)
       quantize_pack_kernel<2, true><<<grid, kPackThreads, 0, st>>>(a);
@@ -306,6 +303,11 @@ cudaError_t launch_append(const Dims& s, const kvq_cache_view& v, const __half* 
       append_kernel<4, true><<<s.B, threads, 0, st>>>(a);
     else
       append_kernel<4, false><<<s.B, threads, 0, st>>>(a);
+  } else if (s.bits == 3) {
+    if (s.hybrid)
+      append_kernel<3, true><<<s.B, threads, 0, st>>>(a);
+    else
+      append_kernel<3, false><<<s.B, threads, 0, st>>>(a);
   } else {
     if (s.hybrid)
       append_kernel<2, true><<<s.B, threads, 0, st>>>(a);

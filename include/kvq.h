@@ -2,7 +2,7 @@
  * kvq.h -- C ABI of the low-bit KV-cache library (libkvq.so).
  *
  * One operation family: single-token decode attention over a key/value cache
- * whose older tokens are stored as asymmetric uniform INT4 or INT2 codes and
+ * whose older tokens are stored as asymmetric uniform INT4, INT3 or INT2 codes and
  * whose most recent Nr tokens stay fp16 (and, optionally, whose first tokens
  * stay fp16 as an attention-sink window).
  *
@@ -24,13 +24,14 @@
  *     at prefill and fixed afterwards.
  *   - same page, section 3.1: dequantized value = scale * q + zero.
  *   - same page, section 3.2: 32 consecutive head_dim values packed together.
+ *   - TurboQuant 3-bit article, section 3.1: eight 3-bit codes in 24 bits.
  *
  * ---------------------------------------------------------------------------
  * Notation
  *   B   batch (sequences)             Hkv  KV heads        Hq  query heads (Hq % Hkv == 0)
  *   gq  = Hq / Hkv                    d    head_dim (multiple of 32, 32..256)
  *   G   = 32 group size along d       Ng   = d / 32 groups per token and head
- *   b   bits per code, 2 or 4         Nr   fp16 residual window length (0..1024)
+ *   b   bits per code, 2, 3 or 4      Nr   fp16 residual window length (0..1024)
  *   cap packed-token capacity per (sequence, KV head)
  *   S   fp16 attention-sink window length (0..256)
  *
@@ -41,8 +42,10 @@
  *   codes    uint8  [B][Hkv][cap][d*b/8]
  *            One token row holds d codes as a little-endian bit string: element
  *            e (0 <= e < d) occupies bits [e*b, e*b + b) of the row, so group g
- *            is the contiguous bytes [g*4*b, (g+1)*4*b): 16 bytes for INT4, 8 for INT2.
+ *            is the contiguous bytes [g*4*b, (g+1)*4*b): 16 bytes for INT4, 12 for
+ *            INT3, 8 for INT2.
  *            INT4 byte k = c[2k] | c[2k+1] << 4.
+ *            INT3: eight codes per 3 bytes, a code may straddle two bytes.
  *            INT2 byte k = c[4k] | c[4k+1] << 2 | c[4k+2] << 4 | c[4k+3] << 6.
  *   params   uint32 [B][Hkv][cap][Ng]
  *            One half2 per group: low 16 bits = scale (fp16), high 16 bits =
@@ -132,7 +135,7 @@ typedef struct {
   int32_t batch;        /* B   >= 1 */
   int32_t num_kv_heads; /* Hkv >= 1 */
   int32_t head_dim;     /* d: multiple of 32, 32..256 */
-  int32_t bits;         /* b: 2 or 4 */
+  int32_t bits;         /* b: 2, 3 or 4 */
   int32_t group;        /* G: 32 */
   int32_t capacity;     /* packed tokens per (sequence, KV head), >= 0 */
   int32_t residual;     /* Nr: 0..1024 */
@@ -324,7 +327,7 @@ kvq_status kvq_read_error(const kvq_cache_view* view, uint32_t* word_out, void* 
 const char* kvq_status_string(kvq_status status);
 
 /* Library version as 10000 * major + 100 * minor + patch. */
-int32_t kvq_version(void); /* 120: hybrid sym/asym groups; 110: sink window, fp32 output */
+int32_t kvq_version(void); /* 130: 3-bit codes; 120: hybrid groups; 110: sink, fp32 output */
 
 #ifdef __cplusplus
 }

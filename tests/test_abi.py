@@ -30,7 +30,7 @@ def test_header_declares_and_library_exports(lib):
     assert set(kvq.EXPORTS) <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in kvq.h but not exported"
-    assert kvq.kvq_version() == 120
+    assert kvq.kvq_version() == 130
 
 
 def test_status_strings(lib):
@@ -50,6 +50,7 @@ def test_cache_bytes(lib):
     assert kvq.kvq_cache_bytes(D, kvq.KVQ_ARRAY_CODES) == 2 * 8 * 1000 * 64
     assert kvq.kvq_cache_bytes(D, kvq.KVQ_ARRAY_PARAMS) == 2 * 8 * 1000 * 4 * 4
     assert kvq.kvq_cache_bytes(D, kvq.KVQ_ARRAY_RESIDUAL) == 2 * 8 * 128 * 128 * 2
+    assert kvq.kvq_cache_bytes(_desc(bits=3), kvq.KVQ_ARRAY_CODES) == 2 * 8 * 1000 * 48
     D2 = _desc(bits=2, head_dim=64)
     assert kvq.kvq_cache_bytes(D2, kvq.KVQ_ARRAY_CODES) == 2 * 8 * 1000 * 16
     assert kvq.kvq_cache_bytes(D2, kvq.KVQ_ARRAY_PARAMS) == 2 * 8 * 1000 * 2 * 4
@@ -58,7 +59,7 @@ def test_cache_bytes(lib):
     assert kvq.kvq_cache_bytes(D, kvq.KVQ_ARRAY_MODE) == 0
     assert kvq.kvq_cache_bytes(_desc(hybrid=1), kvq.KVQ_ARRAY_MODE) == 2 * 8 * 1000
     assert kvq.kvq_cache_bytes(D, 7) == 0
-    for bad in (dict(bits=3), dict(head_dim=96), dict(head_dim=100), dict(group=64),
+    for bad in (dict(bits=5), dict(bits=1), dict(head_dim=96), dict(head_dim=100), dict(group=64),
                 dict(batch=0), dict(residual=-1), dict(residual=2000), dict(capacity=-5),
                 dict(sink=-1), dict(sink=257), dict(hybrid=2), dict(hybrid=-1)):
         assert kvq.kvq_cache_bytes(_desc(**bad), kvq.KVQ_ARRAY_CODES) == 0, bad
@@ -78,7 +79,7 @@ def _view(addr=0x10000):
 
 
 @pytest.mark.parametrize("kw,expect", [
-    (dict(bits=3), kvq.KVQ_ERR_UNSUPPORTED),
+    (dict(bits=5), kvq.KVQ_ERR_UNSUPPORTED),
     (dict(head_dim=96), kvq.KVQ_ERR_UNSUPPORTED),
     (dict(head_dim=40), kvq.KVQ_ERR_INVALID_ARG),
     (dict(group=16), kvq.KVQ_ERR_INVALID_ARG),
@@ -165,7 +166,7 @@ def test_step_io_bytes(lib):
     n_in = q + 2 * kv
     assert lib.kvq_step_io_bytes(ctypes.byref(D), 32) == ((n_in + 255) // 256) * 256 + 2 * q  # fp32 room
     assert lib.kvq_step_io_bytes(ctypes.byref(D), 12) == 0
-    assert lib.kvq_step_io_bytes(ctypes.byref(_desc(bits=3)), 32) == 0
+    assert lib.kvq_step_io_bytes(ctypes.byref(_desc(bits=5)), 32) == 0
 
 
 def test_step_host_rejects_bad_args(lib):
