@@ -205,7 +205,8 @@ def workload_config(w, packed_tokens, extra=None):
     return cfg
 
 
-def build_state(dev, steps, warmup, e2e_steps, l2_bytes, workload, sink=0, hybrid=0, bits=0):
+def build_state(dev, steps, warmup, e2e_steps, l2_bytes, workload, sink=0, hybrid=0, bits=0,
+                paged=0):
     """Pack the workload once, clone it into enough copies to exceed 3x L2,
     and pre-generate the per-step queries and new tokens on the device."""
     from bit_quantized_kv_pack_gb300 import kvq, synth
@@ -222,8 +223,16 @@ def build_state(dev, steps, warmup, e2e_steps, l2_bytes, workload, sink=0, hybri
     appends = (math.ceil(warmup / ncopy) + math.ceil(steps / ncopy)
                + math.ceil((ncopy + max(ncopy, e2e_steps)) / ncopy) + 2)
     cap = max(npk_b) + appends + 8
+    paging = {}
+    if paged:  # 32-token pages, each copy's block table a seeded shuffle of its pool
+        cap = (cap + 31) // 32 * 32
+        paging = dict(page_size=32, num_pages=w.batch * cap // 32)
     base = kvq.KVCache(w.batch, w.num_kv_heads, w.head_dim, w.bits, cap, w.residual, device=dev,
-                       sink=sink, hybrid=hybrid)
+                       sink=sink, hybrid=hybrid, **paging)
+    if paged:
+        gen = torch.Generator().manual_seed(1000 + workload)
+        base.block_table.copy_(torch.randperm(paging["num_pages"], generator=gen, dtype=torch.int32)
+                               .view(w.batch, cap // 32))
     kvq.kvq_quantize_pack(base, k, v, lens.to(dev))
     st, word = kvq.kvq_read_error(base)
     if st != kvq.KVQ_OK:
@@ -232,9 +241,9 @@ def build_state(dev, steps, warmup, e2e_steps, l2_bytes, workload, sink=0, hybri
     copies = [base]
     for _ in range(ncopy - 1):
         c = kvq.KVCache(w.batch, w.num_kv_heads, w.head_dim, w.bits, cap, w.residual, device=dev,
-                        sink=sink, hybrid=hybrid)
+                        sink=sink, hybrid=hybrid, **paging)
         for name in ("k_codes", "v_codes", "k_params", "v_params", "k_res", "v_res", "k_sink",
-                     "v_sink", "k_mode", "v_mode", "counters"):
+                     "v_sink", "k_mode", "v_mode", "block_table", "counters"):
             getattr(c, name).copy_(getattr(base, name))
         copies.append(c)
     nslot = ncopy  # one graph = one pass over the copies
@@ -295,7 +304,7 @@ def run_ours(args, rank, world, local):
     l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
 
     st = build_state(dev, args.steps, args.warmup, args.e2e_steps, l2, args.workload, args.sink,
-                     args.hybrid, args.bits)
+                     args.hybrid, args.bits, args.paged)
     w, ncopy = st["w"], st["nslot"]
     K = args.steps
     reps, rem = divmod(K, ncopy)  # K steps = reps whole passes over the copies + rem
@@ -378,13 +387,15 @@ def run_ours(args, rank, world, local):
                   f"packed) > 3x L2 ({l2 / 2**20:.0f} MiB)",
             "timing": "CUDA graph replays, CUDA events", "parallelism": "replicas",
             **({"sink": args.sink} if args.sink else {}),
-            **({"hybrid": "sym/asym per group, mode bytes"} if args.hybrid else {})}),
+            **({"hybrid": "sym/asym per group, mode bytes"} if args.hybrid else {}),
+            **({"paged": "32-token pages, shuffled block tables"} if args.paged else {})}),
         "all_bytes_gbs": round(all_bytes_gbs, 2),
         "gpu_launches": launches * K,
         "roofline": {"bound": "hbm", "kernel": rf_kernel,
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": profiled_traffic(w.name, fused) if not (args.sink or args.hybrid or args.bits) else None,
+                     "traffic": (profiled_traffic(w.name, fused)
+                                 if not (args.sink or args.hybrid or args.bits or args.paged) else None),
                      "algorithmic_bytes_per_launch": step_bytes,
                      "us_per_launch": round(rf_us, 3)},
         "decode_only": {"us_per_launch": round(dec_ms_per_launch * 1e3, 3),
@@ -694,6 +705,8 @@ def main():
                     help="1: hybrid symmetric/asymmetric groups with mode bytes (default 0)")
     ap.add_argument("--bits", type=int, default=0, choices=(0, 2, 3, 4),
                     help="code width instead of the workload's own (3: the 3-bit variant)")
+    ap.add_argument("--paged", type=int, default=0, choices=(0, 1),
+                    help="1: packed rows in 32-token pages found through shuffled block tables")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

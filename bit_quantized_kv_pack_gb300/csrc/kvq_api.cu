@@ -19,6 +19,10 @@ kvq_status check_desc(const kvq_cache_desc* D) {
   if (D->head_dim != 32 && D->head_dim != 64 && D->head_dim != 128 && D->head_dim != 256)
     return KVQ_ERR_UNSUPPORTED;
   if (D->sink < 0 || (D->hybrid != 0 && D->hybrid != 1)) return KVQ_ERR_INVALID_ARG;
+  if (D->page_size != 0 && D->page_size != kvq::kPage) return KVQ_ERR_UNSUPPORTED;
+  if (D->page_size && (D->capacity % kvq::kPage != 0 || D->num_pages < 0 ||
+                       (D->capacity > 0 && D->num_pages < 1)))
+    return KVQ_ERR_INVALID_ARG;
   if (D->residual > 1024 || D->sink > 256) return KVQ_ERR_UNSUPPORTED;
   if ((int64_t)D->batch * D->num_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
@@ -32,11 +36,13 @@ kvq_status check_view(const kvq_cache_desc& D, const kvq_cache_view* v) {
   if (D.residual > 0 && (!v->k_res || !v->v_res)) return KVQ_ERR_INVALID_ARG;
   if (D.sink > 0 && (!v->k_sink || !v->v_sink || !v->sink_len)) return KVQ_ERR_INVALID_ARG;
   if (D.hybrid && D.capacity > 0 && (!v->k_mode || !v->v_mode)) return KVQ_ERR_INVALID_ARG;
+  if (D.page_size && D.capacity > 0 && !v->block_table) return KVQ_ERR_INVALID_ARG;
   const void* a16[] = {v->k_codes, v->v_codes, v->k_params, v->v_params, v->k_res,
                        v->v_res,   v->k_sink,   v->v_sink,   v->k_mode,   v->v_mode};
   for (const void* p : a16)
     if (!aligned(p, 16)) return KVQ_ERR_MISALIGNED;
-  const void* a4[] = {v->packed_len, v->res_len, v->res_head, v->err_word, v->sink_len};
+  const void* a4[] = {v->packed_len, v->res_len, v->res_head, v->err_word, v->sink_len,
+                      v->block_table};
   for (const void* p : a4)
     if (!aligned(p, 4)) return KVQ_ERR_MISALIGNED;
   return KVQ_OK;
@@ -54,12 +60,14 @@ size_t kvq_cache_bytes(const kvq_cache_desc* desc, int which) {
   if (check_desc(desc) != KVQ_OK) return 0;
   const Dims s = kvq::dims_of(*desc);
   const size_t rows = (size_t)s.B * s.Hkv;
+  // packed rows: every (sequence, head, slot), or every (page, head, slot) of the pool
+  const size_t prow = s.page ? (size_t)s.npages * s.Hkv * s.page : rows * (size_t)s.cap;
   switch (which) {
-    case KVQ_ARRAY_CODES: return rows * (size_t)s.cap * s.row_bytes;
-    case KVQ_ARRAY_PARAMS: return rows * (size_t)s.cap * s.Ng * sizeof(uint32_t);
+    case KVQ_ARRAY_CODES: return prow * s.row_bytes;
+    case KVQ_ARRAY_PARAMS: return prow * s.Ng * sizeof(uint32_t);
     case KVQ_ARRAY_RESIDUAL: return rows * (size_t)s.Nr * s.d * sizeof(uint16_t);
     case KVQ_ARRAY_SINK: return rows * (size_t)s.Ns * s.d * sizeof(uint16_t);
-    case KVQ_ARRAY_MODE: return s.hybrid ? rows * (size_t)s.cap : 0;
+    case KVQ_ARRAY_MODE: return s.hybrid ? prow : 0;
     default: return 0;
   }
 }
@@ -204,7 +212,7 @@ kvq_status kvq_read_error(const kvq_cache_view* view, uint32_t* word_out, void* 
   if (w & KVQ_ERRBIT_CAPACITY) return KVQ_ERR_CAPACITY;
   if (w & KVQ_ERRBIT_EMPTY) return KVQ_ERR_EMPTY;
   if (w & KVQ_ERRBIT_TIMEOUT) return KVQ_ERR_TIMEOUT;
-  if (w & KVQ_ERRBIT_BADLEN) return KVQ_ERR_INVALID_ARG;
+  if (w & (KVQ_ERRBIT_BADLEN | KVQ_ERRBIT_BADPAGE)) return KVQ_ERR_INVALID_ARG;
   return KVQ_OK;
 }
 
@@ -222,6 +230,6 @@ const char* kvq_status_string(kvq_status status) {
   }
 }
 
-int32_t kvq_version(void) { return 130; }
+int32_t kvq_version(void) { return 140; }
 
 }  // extern "C"

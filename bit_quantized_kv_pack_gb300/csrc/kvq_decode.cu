@@ -98,6 +98,7 @@ cudaError_t launch_decode(const Dims& s, const DecodePlan& p, const kvq_cache_vi
   a.res_len = v.res_len;
   a.res_head = v.res_head;
   a.err_word = v.err_word;
+  a.rm = row_map(s, v.block_table);
   a.k_sink = reinterpret_cast<const __half*>(v.k_sink);
   a.v_sink = reinterpret_cast<const __half*>(v.v_sink);
   a.sink_len = v.sink_len;

@@ -21,6 +21,7 @@ struct DecodeArgs {
   const int32_t* res_len;
   const int32_t* res_head;
   uint32_t* err_word;
+  RowMap rm;  // packed token -> row of the codes / params / mode arrays
   const __half* k_sink;  // [B][Hkv][Ns][d] (attention-sink window)
   const __half* v_sink;
   const int32_t* sink_len;

@@ -102,7 +102,9 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(DecodeArgs a) 
     for (int i = 0; i < QB; ++i) {
       const float sv = valid ? sc[i] * a.qk_scale_log2 : -INFINITY;
       const float mnew = fmaxf(m[i], warp_max(sv));
-      const float alpha = exp2f(m[i] - mnew);
+      // a chunk with no valid token while nothing is accumulated (a page
+      // outside the pool) leaves the state as it is instead of exp2(-inf + inf)
+      const float alpha = mnew == -INFINITY ? 1.f : exp2f(m[i] - mnew);
       p[i] = valid ? exp2f(sv - mnew) : 0.f;
       l[i] = l[i] * alpha + warp_sum(p[i]);
 #pragma unroll
@@ -114,12 +116,13 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(DecodeArgs a) 
   // ---- packed tokens
   for (int base = i0 + warp * 32; base < i1; base += kThreads) {
     const int t = base + lane;
-    const bool valid = t < i1;
+    const int64_t row = t < i1 ? a.rm.row(b, h, t) : -1;
+    if (t < i1 && row < 0) set_error(a.err_word, KVQ_ERRBIT_BADPAGE);
+    const bool valid = row >= 0;  // a token on a page outside the pool is skipped
     float sc[QB];
 #pragma unroll
     for (int i = 0; i < QB; ++i) sc[i] = 0.f;
     if (valid) {
-      const int64_t row = bh * a.cap + t;
       const uint8_t* krow = a.k_codes + row * RB;
       const uint32_t* kp = a.k_params + row * NG;
 #pragma unroll
@@ -165,7 +168,8 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(DecodeArgs a) 
     const int bo = lane * DPL * BITS;  // bit offset of the lane's values in a row
     const int g_l = (lane * DPL) / kGroup;
     for (int tt = 0; tt < nvalid; ++tt) {
-      const int64_t row = bh * a.cap + base + tt;
+      const int64_t row = a.rm.row(b, h, base + tt);  // the same for every lane
+      if (row < 0) continue;
       const uint32_t prm = a.v_params[row * NG + g_l];
       const float scale = half_lo(prm), mn = half_hi(prm);
       const uint32_t* vw = reinterpret_cast<const uint32_t*>(a.v_codes + row * RB) + bo / 32;

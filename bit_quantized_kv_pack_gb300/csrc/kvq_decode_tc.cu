@@ -47,6 +47,9 @@
 //    exact log-sum-exp merge of the split partials (combine_unit) instead.
 //  * Three CTAs per SM (168 registers each): twelve warps hide the latency of
 //    the dequantize-and-MMA chain.
+//  * Paged caches (32-token pages through a block table, TurboQuant page
+//    section 6.1): packed splits start on page boundaries and a stage is filled
+//    by one 32-row tile load per page of the pool instead of one 128-row load.
 //
 // Every mbarrier wait is bounded; a wait that runs out sets KVQ_ERRBIT_TIMEOUT.
 #include <math.h>
@@ -134,6 +137,7 @@ __host__ __device__ constexpr float w2_weight(int j) {
 }
 
 constexpr float kTwo24 = 16777216.f;  // 2^24
+constexpr int kPagePrefetch = 64;     // page ids of a split kept in shared memory
 // A split whose max (log2 units) is more than this above the head's reference
 // could overflow fp32 once scaled to it: the head then takes the exact merge.
 constexpr float kRefSlack = 80.f;
@@ -418,6 +422,7 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
   __shared__ volatile int s_abort;
   __shared__ int s_last;
   __shared__ uint32_t s_ref[QB];  // the head's reference max per query (float bits + 1; 0: unknown)
+  __shared__ int s_pages[kPagePrefetch];  // paged caches: the split's first page ids
 
   const int s = blockIdx.x;
   const int h = blockIdx.y;  // one query block per KV head (gq <= 4)
@@ -475,12 +480,35 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
     s_last_tile[st] = tile;
     uint8_t* base = smem + (size_t)st * G::STAGE;
     const uint32_t fb = ptx::smem_u32(&full_bar[st]);
-    ptx::mbar_arrive_expect_tx(fb, G::STAGE);
-    const int y = row0 + tile * T;
-    ptx::tma_load_2d(ptx::smem_u32(base + G::KC), &tm_kc, 0, y, fb);
-    ptx::tma_load_2d(ptx::smem_u32(base + G::VC), &tm_vc, 0, y, fb);
-    ptx::tma_load_2d(ptx::smem_u32(base + G::KP), &tm_kp, 0, y, fb);
-    ptx::tma_load_2d(ptx::smem_u32(base + G::VP), &tm_vp, 0, y, fb);
+    if (!a.rm.paged) {
+      ptx::mbar_arrive_expect_tx(fb, G::STAGE);
+      const int y = row0 + tile * T;
+      ptx::tma_load_2d(ptx::smem_u32(base + G::KC), &tm_kc, 0, y, fb);
+      ptx::tma_load_2d(ptx::smem_u32(base + G::VC), &tm_vc, 0, y, fb);
+      ptx::tma_load_2d(ptx::smem_u32(base + G::KP), &tm_kp, 0, y, fb);
+      ptx::tma_load_2d(ptx::smem_u32(base + G::VP), &tm_vp, 0, y, fb);
+    } else {
+      // the tile's pages (i0 is a page boundary), 32 rows of each array apiece;
+      // stage rows past the split's last page keep stale bytes, masked like
+      // any rows past the split end
+      constexpr int kPerTile = T / kPage;
+      const int j0 = tile * kPerTile;
+      const int np = min(kPerTile, (i1 - i0 + kPage - 1) / kPage - j0);
+      ptx::mbar_arrive_expect_tx(fb, (uint32_t)np * (G::STAGE / kPerTile));
+      for (int p = 0; p < np; ++p) {
+        const int j = j0 + p;
+        const int pg = j < kPagePrefetch ? s_pages[j] : a.rm.page_of(b, i0 / kPage + j);
+        int y = -kPage;  // a page outside the pool reads zeros (and is flagged)
+        if (pg >= 0 && pg < a.rm.npages)
+          y = (pg * a.Hkv + h) * kPage;
+        else
+          set_error(a.err_word, KVQ_ERRBIT_BADPAGE);
+        ptx::tma_load_2d(ptx::smem_u32(base + G::KC + p * kPage * G::RB), &tm_kc, 0, y, fb);
+        ptx::tma_load_2d(ptx::smem_u32(base + G::VC + p * kPage * G::RB), &tm_vc, 0, y, fb);
+        ptx::tma_load_2d(ptx::smem_u32(base + G::KP + p * kPage * NG * 4), &tm_kp, 0, y, fb);
+        ptx::tma_load_2d(ptx::smem_u32(base + G::VP + p * kPage * NG * 4), &tm_vp, 0, y, fb);
+      }
+    }
   };
   // Thread 0: read the counters, cut this split's range and start its first
   // NSTAGE tiles.
@@ -497,6 +525,10 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
     if (!res_cta) {
       r0_ = (int)((int64_t)Lp * s / a.Sp);
       r1_ = (int)((int64_t)Lp * (s + 1) / a.Sp);
+      if (a.rm.paged) {  // splits start on page boundaries
+        r0_ = r0_ / kPage * kPage;
+        r1_ = s + 1 == a.Sp ? Lp : r1_ / kPage * kPage;
+      }
     } else {
       const int Sr = a.S - a.Sp, sr = s - a.Sp;
       // window tokens of age [jlo, Lr) take part (a flushed oldest token leaves
@@ -520,7 +552,11 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
       i0 = r0_;
       i1 = r1_;
       ntiles = (i1 - i0 + T - 1) / T;
-      row0 = (int)(bh * a.cap + i0);  // first packed row of this split (TMA y)
+      row0 = (int)(bh * a.cap + i0);  // first packed row of this split (TMA y, contiguous)
+      if (a.rm.paged) {
+        const int npg = min((i1 - i0 + kPage - 1) / kPage, kPagePrefetch);
+        for (int j = 0; j < npg; ++j) s_pages[j] = a.rm.page_of(b, i0 / kPage + j);
+      }
       for (int tile = 0; tile < ntiles && tile < NSTAGE; ++tile) issue(tile);
     }
   };
@@ -583,9 +619,10 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
       uint32_t prm, asym = 1;
       const uint32_t packed = quantize_quad<BITS>(x, prm, a.hybrid != 0, &asym);
       const uint32_t modes = __ballot_sync(0xffffffffu, (lane & 3) == 0 && asym);
-      if (a.hybrid && lane == 0) a.w_modes[which][bh * a.cap + Lp] = mode_byte(modes, 0, NG);
-      if (active) {
-        const int64_t row = bh * a.cap + Lp;
+      const int64_t row = a.rm.row(b, h, Lp);  // warp-uniform
+      if (row < 0 && lane == 0) set_error(a.err_word, KVQ_ERRBIT_BADPAGE);
+      if (a.hybrid && lane == 0 && row >= 0) a.w_modes[which][row] = mode_byte(modes, 0, NG);
+      if (active && row >= 0) {
         const int gi = lane >> 2, quad = lane & 3;
         uint8_t* dst = a.w_codes[which] + row * a.row_bytes + gi * (4 * BITS) + quad * BITS;
         if (BITS == 4)
@@ -593,6 +630,8 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
         else
           *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
         if (quad == 0) a.w_params[which][row * NG + gi] = prm;
+      }
+      if (active) {  // the packed token as it is attended, dequantized in fp32
         const float sc = half_lo(prm), mn = half_hi(prm);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
@@ -1018,14 +1057,14 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// A 2D view [rows][row_bytes] of uint8 with a box of T whole rows.
+// A 2D view [rows][row_bytes] of uint8 with a box of box_rows whole rows.
 bool make_rows_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
-                   CUtensorMapSwizzle swz) {
+                   CUtensorMapSwizzle swz, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
-  if (!fn || rows == 0) return false;
+  if (!fn || rows == 0 || rows > 0x7fffffffull) return false;  // y is a 32-bit coordinate
   cuuint64_t dims[2] = {row_bytes, rows};
   cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {(cuuint32_t)row_bytes, (cuuint32_t)T};
+  cuuint32_t box[2] = {(cuuint32_t)row_bytes, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1035,12 +1074,16 @@ bool make_rows_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint6
 template <int BITS, bool STEP>
 cudaError_t launch_bits(const Dims& s, const DecodePlan& p, const DecodeArgs& a, cudaStream_t st) {
   using Gm = Geo<BITS>;
-  const uint64_t rows = (uint64_t)s.B * s.Hkv * s.cap;
+  // packed rows: every (sequence, head, slot), or every (page, head, slot) of a pool
+  const bool paged = s.page != 0;
+  const uint64_t rows = paged ? (uint64_t)s.npages * s.Hkv * kPage : (uint64_t)s.B * s.Hkv * s.cap;
+  const uint32_t box = paged ? kPage : T;
   CUtensorMap kc, vc, kp, vp;
   const CUtensorMapSwizzle swz = BITS == 4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
-  if (!make_rows_map(&kc, a.k_codes, Gm::RB, rows, swz) || !make_rows_map(&vc, a.v_codes, Gm::RB, rows, swz) ||
-      !make_rows_map(&kp, a.k_params, NG * 4, rows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_rows_map(&vp, a.v_params, NG * 4, rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+  if (!make_rows_map(&kc, a.k_codes, Gm::RB, rows, swz, box) ||
+      !make_rows_map(&vc, a.v_codes, Gm::RB, rows, swz, box) ||
+      !make_rows_map(&kp, a.k_params, NG * 4, rows, CU_TENSOR_MAP_SWIZZLE_NONE, box) ||
+      !make_rows_map(&vp, a.v_params, NG * 4, rows, CU_TENSOR_MAP_SWIZZLE_NONE, box))
     return cudaErrorInvalidValue;
   constexpr size_t smem = tc_smem_bytes<BITS>();
   static bool attr_set = false;

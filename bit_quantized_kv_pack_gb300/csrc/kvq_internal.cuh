@@ -18,6 +18,8 @@ struct Dims {
   int B, Hkv, d, bits, cap, Nr;
   int Ns;        // attention-sink window length (0: none)
   int hybrid;    // 1: hybrid sym/asym groups with mode bytes
+  int page;      // 0: contiguous packed rows; kPage: paged through a block table
+  int npages;    // pages in the pool of a paged cache
   int Ng;        // groups per token row
   int row_bytes; // packed code bytes per token row
 };
@@ -32,9 +34,42 @@ inline Dims dims_of(const kvq_cache_desc& D) {
   s.Nr = D.residual;
   s.Ns = D.sink;
   s.hybrid = D.hybrid;
+  s.page = D.page_size;
+  s.npages = D.page_size ? D.num_pages : 0;
   s.Ng = D.head_dim / kGroup;
   s.row_bytes = D.head_dim * D.bits / 8;
   return s;
+}
+
+constexpr int kPage = 32;  // tokens per page of a paged cache
+
+// Where packed token t of (sequence b, KV head h) sits in the codes, params and
+// mode arrays: row (b * Hkv + h) * cap + t of a contiguous cache, or row
+// (page * Hkv + h) * 32 + t % 32 of a paged one, page = block_table[b][t / 32].
+// -1 for a page outside the pool (the caller sets KVQ_ERRBIT_BADPAGE and skips).
+struct RowMap {
+  const int32_t* block_table;  // [B][cap / 32] (paged)
+  int Hkv, cap, paged, npages;
+
+  __device__ __forceinline__ int page_of(int b, int j) const {  // j = t / 32
+    return __ldg(block_table + (int64_t)b * (cap / kPage) + j);
+  }
+  __device__ __forceinline__ int64_t row(int b, int h, int t) const {
+    if (!paged) return ((int64_t)b * Hkv + h) * cap + t;
+    const int pg = page_of(b, t / kPage);
+    if (pg < 0 || pg >= npages) return -1;
+    return ((int64_t)pg * Hkv + h) * kPage + (t % kPage);
+  }
+};
+
+inline RowMap row_map(const Dims& s, const int32_t* block_table) {
+  RowMap m;
+  m.block_table = block_table;
+  m.Hkv = s.Hkv;
+  m.cap = s.cap;
+  m.paged = s.page != 0;
+  m.npages = s.npages;
+  return m;
 }
 
 // ------------------------------------------------------------ error word ---

@@ -35,6 +35,7 @@ struct PackArgs {
   __half* res[2];        // [B][Hkv][Nr][d]
   __half* sink[2];       // [B][Hkv][Ns][d]
   uint8_t* modes[2];     // [B][Hkv][cap] mode bytes (hybrid caches)
+  RowMap rm;             // packed token -> row (contiguous or paged)
   const int32_t* seq_lens;
   int32_t* packed_len;
   int32_t* res_len;
@@ -98,8 +99,10 @@ __global__ void __launch_bounds__(kPackThreads) quantize_pack_kernel(PackArgs a)
     // the warp's 8 groups are whole token rows (Ng divides 8): each row's mode
     // byte comes from one ballot
     const uint32_t modes = HYB ? __ballot_sync(0xffffffffu, quad == 0 && asym) : 0u;
-    const bool to_pack = in_range && t >= ns && t - ns < npk;
-    const int64_t row = (int64_t)bh * a.cap + (t - ns);
+    const bool packs = in_range && t >= ns && t - ns < npk;
+    const int64_t row = packs ? a.rm.row(b, bh % a.Hkv, t - ns) : -1;
+    if (packs && row < 0 && quad == 0) set_error(a.err_word, KVQ_ERRBIT_BADPAGE);
+    const bool to_pack = packs && row >= 0;
     store_group_codes<BITS>(to_pack ? a.codes[which] + row * a.row_bytes + g * (4 * BITS) : nullptr,
                             packed, quad, to_pack);
     if (!in_range) continue;
@@ -109,7 +112,7 @@ __global__ void __launch_bounds__(kPackThreads) quantize_pack_kernel(PackArgs a)
     } else if (to_pack) {
       if (quad == 0) a.params[which][row * a.Ng + g] = prm;
       if (HYB && quad == 0 && g == 0) a.modes[which][row] = mode_byte(modes, lane >> 2, a.Ng);
-    } else if (t - ns >= npk_all) {
+    } else if (!packs && t - ns >= npk_all) {
       const int j = t - ns - npk_all;  // ring slot; res_head = 0 after a prefill
       __half* dst = a.res[which] + ((int64_t)bh * a.Nr + j) * a.d + g * kGroup + quad * 8;
       *reinterpret_cast<uint4*>(dst) = raw[u];
@@ -126,6 +129,7 @@ struct AppendArgs {
   uint32_t* params[2];
   __half* res[2];
   uint8_t* modes[2];
+  RowMap rm;
   int32_t* packed_len;
   int32_t* res_len;
   int32_t* res_head;
@@ -196,12 +200,15 @@ __global__ void __launch_bounds__(1024) append_kernel(AppendArgs a) {
       const uint32_t packed = quantize_quad<BITS>(x, prm, HYB, &asym);
       if (HYB) {
         const uint32_t modes = __ballot_sync(0xffffffffu, (lane & 3) == 0 && asym);
-        if (lane == 0) (which ? a.modes[1] : a.modes[0])[bh * a.cap + pl] = mode_byte(modes, 0, a.Ng);
+        const int64_t mrow = a.rm.row(b, h, pl);
+        if (lane == 0 && mrow >= 0) (which ? a.modes[1] : a.modes[0])[mrow] = mode_byte(modes, 0, a.Ng);
       }
-      const int64_t row = bh * a.cap + pl;
+      const int64_t row = a.rm.row(b, h, pl);  // warp-uniform
+      if (row < 0 && lane == 0) set_error(a.err_word, KVQ_ERRBIT_BADPAGE);
       const int g = lane >> 2, quad = lane & 3;
-      store_group_codes<BITS>(codes_base + row * a.row_bytes + g * (4 * BITS), packed, quad, active);
-      if (active && quad == 0) params_base[row * a.Ng + g] = prm;
+      store_group_codes<BITS>(codes_base + (row < 0 ? 0 : row) * a.row_bytes + g * (4 * BITS), packed,
+                              quad, active && row >= 0);
+      if (active && row >= 0 && quad == 0) params_base[row * a.Ng + g] = prm;
     }
     if (a.Nr > 0 && active) *reinterpret_cast<uint4*>(ring_row + lane * 8) = nv;
   }
@@ -239,6 +246,7 @@ cudaError_t launch_quantize_pack(const Dims& s, const kvq_cache_view& v, const _
   a.sink[1] = reinterpret_cast<__half*>(v.v_sink);
   a.modes[0] = v.k_mode;
   a.modes[1] = v.v_mode;
+  a.rm = row_map(s, v.block_table);
   a.seq_lens = seq_lens;
   a.packed_len = v.packed_len;
   a.res_len = v.res_len;
@@ -285,6 +293,7 @@ cudaError_t launch_append(const Dims& s, const kvq_cache_view& v, const __half* 
   a.res[1] = reinterpret_cast<__half*>(v.v_res);
   a.modes[0] = v.k_mode;
   a.modes[1] = v.v_mode;
+  a.rm = row_map(s, v.block_table);
   a.packed_len = v.packed_len;
   a.res_len = v.res_len;
   a.res_head = v.res_head;

@@ -32,6 +32,7 @@ KVQ_ERRBIT_CAPACITY = 0x1
 KVQ_ERRBIT_EMPTY = 0x2
 KVQ_ERRBIT_TIMEOUT = 0x4
 KVQ_ERRBIT_BADLEN = 0x8
+KVQ_ERRBIT_BADPAGE = 0x10
 
 KVQ_ARRAY_CODES = 0
 KVQ_ARRAY_PARAMS = 1
@@ -50,14 +51,15 @@ class CacheDesc(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("bits", ctypes.c_int32), ("group", ctypes.c_int32),
                 ("capacity", ctypes.c_int32), ("residual", ctypes.c_int32),
-                ("sink", ctypes.c_int32), ("hybrid", ctypes.c_int32)]
+                ("sink", ctypes.c_int32), ("hybrid", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32)]
 
 
 class CacheView(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "k_codes", "v_codes", "k_params", "v_params", "k_res", "v_res",
         "packed_len", "res_len", "res_head", "err_word", "k_sink", "v_sink", "sink_len",
-        "k_mode", "v_mode")]
+        "k_mode", "v_mode", "block_table")]
 
 
 class KvqError(RuntimeError):
@@ -170,27 +172,34 @@ class KVCache:
     ``sink`` > 0 keeps the first ``sink`` tokens of each sequence in fp16 (the
     attention-sink window, fixed after the prefill); ``hybrid=1`` quantizes each
     group symmetrically or asymmetrically, whichever reconstructs it better, and
-    keeps a mode byte per packed row."""
+    keeps a mode byte per packed row.  ``page_size=32`` keeps the packed rows in
+    a pool of ``num_pages`` pages [page][head][32] found through ``block_table``
+    [B][capacity / 32] (filled with pages b * capacity / 32 + j when the pool has
+    room, for the caller to rewrite)."""
 
     def __init__(self, batch, num_kv_heads, head_dim, bits, capacity, residual, device="cuda",
-                 sink=0, hybrid=0):
+                 sink=0, hybrid=0, page_size=0, num_pages=0):
         self.desc = CacheDesc(batch, num_kv_heads, head_dim, bits, 32, capacity, residual, sink,
-                              hybrid)
+                              hybrid, page_size, num_pages)
         self.device = torch.device(device)
         B, H, d = batch, num_kv_heads, head_dim
         rb, ng = d * bits // 8, d // 32
         kw = dict(device=self.device)
-        self.k_codes = torch.zeros(B, H, capacity, rb, dtype=torch.uint8, **kw)
-        self.v_codes = torch.zeros(B, H, capacity, rb, dtype=torch.uint8, **kw)
-        self.k_params = torch.zeros(B, H, capacity, ng, dtype=torch.int32, **kw)
-        self.v_params = torch.zeros(B, H, capacity, ng, dtype=torch.int32, **kw)
+        rows = (num_pages, H, page_size) if page_size else (B, H, capacity)
+        self.k_codes = torch.zeros(*rows, rb, dtype=torch.uint8, **kw)
+        self.v_codes = torch.zeros(*rows, rb, dtype=torch.uint8, **kw)
+        self.k_params = torch.zeros(*rows, ng, dtype=torch.int32, **kw)
+        self.v_params = torch.zeros(*rows, ng, dtype=torch.int32, **kw)
+        npb = capacity // page_size if page_size else 0
+        self.block_table = (torch.arange(B * npb, dtype=torch.int32, **kw).view(B, npb)
+                            % max(num_pages, 1))
         self.k_res = torch.zeros(B, H, residual, d, dtype=torch.float16, **kw)
         self.v_res = torch.zeros(B, H, residual, d, dtype=torch.float16, **kw)
         self.k_sink = torch.zeros(B, H, sink, d, dtype=torch.float16, **kw)
         self.v_sink = torch.zeros(B, H, sink, d, dtype=torch.float16, **kw)
-        ncap = capacity if hybrid else 0
-        self.k_mode = torch.zeros(B, H, ncap, dtype=torch.uint8, **kw)
-        self.v_mode = torch.zeros(B, H, ncap, dtype=torch.uint8, **kw)
+        mrows = rows if hybrid else (0,)
+        self.k_mode = torch.zeros(*mrows, dtype=torch.uint8, **kw)
+        self.v_mode = torch.zeros(*mrows, dtype=torch.uint8, **kw)
         # packed_len, res_len, res_head, sink_len
         self.counters = torch.zeros(4, B, dtype=torch.int32, **kw)
         self.err = torch.zeros(4, dtype=torch.int32, **kw)
@@ -202,7 +211,7 @@ class KVCache:
                          r(self.k_res), r(self.v_res), _ptr(self.counters[0]),
                          _ptr(self.counters[1]), _ptr(self.counters[2]), _ptr(self.err),
                          r(self.k_sink), r(self.v_sink), _ptr(self.counters[3]),
-                         r(self.k_mode), r(self.v_mode))
+                         r(self.k_mode), r(self.v_mode), r(self.block_table))
 
     @property
     def packed_len(self):

@@ -24,7 +24,8 @@
  *     at prefill and fixed afterwards.
  *   - same page, section 3.1: dequantized value = scale * q + zero.
  *   - same page, section 3.2: 32 consecutive head_dim values packed together.
- *   - TurboQuant 3-bit article, section 3.1: eight 3-bit codes in 24 bits.
+ *   - TurboQuant 3-bit article, section 3.1: eight 3-bit codes in 24 bits; section
+ *     6.1: a paged cache of 32-token blocks.
  *
  * ---------------------------------------------------------------------------
  * Notation
@@ -34,6 +35,7 @@
  *   b   bits per code, 2, 3 or 4      Nr   fp16 residual window length (0..1024)
  *   cap packed-token capacity per (sequence, KV head)
  *   S   fp16 attention-sink window length (0..256)
+ *   P   page size of a paged cache (0: contiguous, 32: paged), NP pages in its pool
  *
  * ---------------------------------------------------------------------------
  * Memory layout (all arrays are plain device memory owned by the caller; K and V
@@ -47,6 +49,10 @@
  *            INT4 byte k = c[2k] | c[2k+1] << 4.
  *            INT3: eight codes per 3 bytes, a code may straddle two bytes.
  *            INT2 byte k = c[4k] | c[4k+1] << 2 | c[4k+2] << 4 | c[4k+3] << 6.
+ *            Paged caches (P = 32): codes, params and mode bytes live in a pool of
+ *            NP pages, codes uint8 [NP][Hkv][32][d*b/8] (params, mode likewise); packed
+ *            token t of sequence b, KV head h is row t % 32 of head h in page
+ *            block_table[b][t / 32].  cap must be a multiple of 32.
  *   params   uint32 [B][Hkv][cap][Ng]
  *            One half2 per group: low 16 bits = scale (fp16), high 16 bits =
  *            min (fp16).  Dequantized value x^ = min + code * scale.
@@ -58,6 +64,7 @@
  *            Bit g of a packed row's byte = mode of its group g: 1 asymmetric,
  *            0 symmetric.  Both modes dequantize as min + code * scale, so
  *            decode does not read it.
+ *   block_table int32 [B][cap / 32]   (paged caches only): page of each 32 packed tokens.
  *   packed_len, res_len, res_head, sink_len   int32 [B]   (device)
  *            Per sequence: packed tokens, residual tokens, ring slot of the oldest
  *            residual token, sink tokens.  Sequence b attends over
@@ -128,6 +135,7 @@ typedef enum {
 #define KVQ_ERRBIT_EMPTY 0x2u    /* decode saw a sequence with no tokens; output zeroed */
 #define KVQ_ERRBIT_TIMEOUT 0x4u  /* a bounded wait gave up; that CTA wrote nothing */
 #define KVQ_ERRBIT_BADLEN 0x8u   /* seq_lens[b] < 0 or > Lmax; that sequence was skipped */
+#define KVQ_ERRBIT_BADPAGE 0x10u /* a block-table page outside [0, NP); that token was skipped */
 
 /* Static description of one layer's cache.  group must be 32.  Every field is
  * significant: zero-initialise the struct (sink = 0 keeps no sink window). */
@@ -141,6 +149,8 @@ typedef struct {
   int32_t residual;     /* Nr: 0..1024 */
   int32_t sink;         /* S: 0..256, first tokens kept fp16 (attention-sink window) */
   int32_t hybrid;       /* 0: asymmetric groups; 1: hybrid sym/asym groups with a mode mask */
+  int32_t page_size;    /* P: 0 (contiguous) or 32 (paged) */
+  int32_t num_pages;    /* NP: pages in the pool of a paged cache (ignored when P == 0) */
 } kvq_cache_desc;
 
 /* Device pointers of one layer's cache (layout above).  k_res/v_res may be NULL
@@ -162,6 +172,7 @@ typedef struct {
   int32_t* sink_len;
   uint8_t* k_mode; /* mode bytes [B][Hkv][cap] */
   uint8_t* v_mode;
+  int32_t* block_table; /* [B][cap / 32], paged caches only */
 } kvq_cache_view;
 
 /* Which array kvq_cache_bytes sizes (each of K and V has one of each). */
@@ -171,7 +182,8 @@ typedef struct {
 #define KVQ_ARRAY_SINK 3
 #define KVQ_ARRAY_MODE 4
 
-/* Bytes of one array of the layout (for K or for V; allocate twice).
+/* Bytes of one array of the layout (for K or for V; allocate twice).  For a
+ * paged cache the codes, params and mode arrays are sized for the page pool.
  * Returns 0 for an invalid desc or `which`. */
 size_t kvq_cache_bytes(const kvq_cache_desc* desc, int which);
 
@@ -327,7 +339,7 @@ kvq_status kvq_read_error(const kvq_cache_view* view, uint32_t* word_out, void* 
 const char* kvq_status_string(kvq_status status);
 
 /* Library version as 10000 * major + 100 * minor + patch. */
-int32_t kvq_version(void); /* 130: 3-bit codes; 120: hybrid groups; 110: sink, fp32 output */
+int32_t kvq_version(void); /* 140: paged caches; 130: 3-bit; 120: hybrid; 110: sink, fp32 out */
 
 #ifdef __cplusplus
 }

@@ -11,8 +11,40 @@ ATOL = 2e-3   # max abs error of the fp16 attention output vs the fp64 oracle
 RTOL_L2 = 1e-3  # relative L2 error of the same
 
 
-def gpu_cache(B, H, d, bits, cap, Nr, dev="cuda", sink=0, hybrid=0):
-    return kvq.KVCache(B, H, d, bits, cap, Nr, device=dev, sink=sink, hybrid=hybrid)
+def gpu_cache(B, H, d, bits, cap, Nr, dev="cuda", sink=0, hybrid=0, pages=0, seed=0):
+    """A device cache; pages > 0 makes it paged with a pool of that many
+    32-token pages and a block table drawn as a seeded random injection."""
+    if not pages:
+        return kvq.KVCache(B, H, d, bits, cap, Nr, device=dev, sink=sink, hybrid=hybrid)
+    c = kvq.KVCache(B, H, d, bits, cap, Nr, device=dev, sink=sink, hybrid=hybrid, page_size=32,
+                    num_pages=pages)
+    perm = np.random.default_rng(seed).permutation(pages)[:B * (cap // 32)]
+    c.block_table.copy_(torch.from_numpy(perm.astype(np.int32)).view(B, cap // 32))
+    return c
+
+
+class _Logical:
+    """A paged cache's packed arrays gathered through its block table into the
+    contiguous [B][Hkv][cap] layout (numpy-style indexing, for comparisons)."""
+
+    def __init__(self, g):
+        bt = g.block_table.long()
+        B, npb = bt.shape
+        for name in ("k_codes", "v_codes", "k_params", "v_params", "k_mode", "v_mode"):
+            pool = getattr(g, name)
+            if pool.numel() == 0:
+                setattr(self, name, pool)
+                continue
+            x = pool[bt]  # [B][npb][H][32](...)
+            x = x.transpose(1, 2).contiguous()  # [B][H][npb][32](...)
+            setattr(self, name, x.view(B, x.shape[1], npb * 32, *x.shape[4:]))
+        for name in ("k_res", "v_res", "k_sink", "v_sink", "packed_len", "res_len", "res_head",
+                     "sink_len"):
+            setattr(self, name, getattr(g, name))
+
+
+def logical(g):
+    return _Logical(g) if g.desc.page_size else g
 
 
 def ref_cache(B, H, d, bits, cap, Nr, sink=0, hybrid=0):
@@ -26,6 +58,7 @@ def to_np(t: torch.Tensor) -> np.ndarray:
 def assert_cache_equal(g, r, batches=None):
     """Packed bytes of every used slot, the residual ring, the sink rows and the
     counters."""
+    g = logical(g)
     pl = to_np(g.packed_len)
     rl = to_np(g.res_len)
     rh = to_np(g.res_head)

@@ -30,7 +30,7 @@ def test_header_declares_and_library_exports(lib):
     assert set(kvq.EXPORTS) <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in kvq.h but not exported"
-    assert kvq.kvq_version() == 130
+    assert kvq.kvq_version() == 140
 
 
 def test_status_strings(lib):
@@ -58,10 +58,17 @@ def test_cache_bytes(lib):
     assert kvq.kvq_cache_bytes(_desc(sink=32), kvq.KVQ_ARRAY_SINK) == 2 * 8 * 32 * 128 * 2
     assert kvq.kvq_cache_bytes(D, kvq.KVQ_ARRAY_MODE) == 0
     assert kvq.kvq_cache_bytes(_desc(hybrid=1), kvq.KVQ_ARRAY_MODE) == 2 * 8 * 1000
+    # paged: the arrays are sized for the pool of pages [page][head][32]
+    P = _desc(capacity=1024, page_size=32, num_pages=70, hybrid=1)
+    assert kvq.kvq_cache_bytes(P, kvq.KVQ_ARRAY_CODES) == 70 * 8 * 32 * 64
+    assert kvq.kvq_cache_bytes(P, kvq.KVQ_ARRAY_PARAMS) == 70 * 8 * 32 * 16
+    assert kvq.kvq_cache_bytes(P, kvq.KVQ_ARRAY_MODE) == 70 * 8 * 32
     assert kvq.kvq_cache_bytes(D, 7) == 0
     for bad in (dict(bits=5), dict(bits=1), dict(head_dim=96), dict(head_dim=100), dict(group=64),
                 dict(batch=0), dict(residual=-1), dict(residual=2000), dict(capacity=-5),
-                dict(sink=-1), dict(sink=257), dict(hybrid=2), dict(hybrid=-1)):
+                dict(sink=-1), dict(sink=257), dict(hybrid=2), dict(hybrid=-1),
+                dict(page_size=16, num_pages=8), dict(page_size=32, num_pages=0),
+                dict(page_size=32, num_pages=4, capacity=1000)):
         assert kvq.kvq_cache_bytes(_desc(**bad), kvq.KVQ_ARRAY_CODES) == 0, bad
 
 
@@ -75,7 +82,7 @@ def test_workspace_bytes(lib):
 
 def _view(addr=0x10000):
     # fake, well-aligned addresses: only ever passed to calls the host rejects
-    return kvq.CacheView(*[ctypes.c_void_p(addr + 0x1000 * i) for i in range(15)])
+    return kvq.CacheView(*[ctypes.c_void_p(addr + 0x1000 * i) for i in range(16)])
 
 
 @pytest.mark.parametrize("kw,expect", [
@@ -153,6 +160,11 @@ def test_rejects_bad_sink_view(lib):
         setattr(V, field, 0)
         assert lib.kvq_append(ctypes.byref(_desc(hybrid=1)), ctypes.byref(V), P(0x100004), P(0x200000),
                               None) == kvq.KVQ_ERR_INVALID_ARG, field
+    # a paged cache needs its block table
+    V = _view()
+    V.block_table = 0
+    assert lib.kvq_append(ctypes.byref(_desc(capacity=1024, page_size=32, num_pages=64)), ctypes.byref(V),
+                          P(0x100004), P(0x200000), None) == kvq.KVQ_ERR_INVALID_ARG
     # sink == 0: NULL sink pointers pass the view check (the misaligned k_new then fails)
     V = _view()
     V.k_sink = V.v_sink = V.sink_len = 0

@@ -55,7 +55,7 @@ def test_noalloc_rejects_oversized_request():
     D = kvq.CacheDesc(2048, 16, 256, 4, 32, 1 << 20, 0)
     need = kvq.kvq_decode_workspace_bytes(D, 16 * 8)
     assert need > kvq.NOALLOC_SCRATCH_BYTES
-    V = kvq.CacheView(*[ctypes.c_void_p(0x100000 * (i + 1)) for i in range(15)])
+    V = kvq.CacheView(*[ctypes.c_void_p(0x100000 * (i + 1)) for i in range(16)])
     st = kvq.load().kvq_decode_attention_noalloc(ctypes.byref(D), ctypes.byref(V),
                                                  ctypes.c_void_p(0x100000), 16 * 8,
                                                  ctypes.c_void_p(0x200000), 0, None)
