@@ -7,8 +7,10 @@
 // query heads of one KV head served by one read of the cache (BitDecoding page
 // section 2.3).  How:
 //
-//  * 128-token tiles -- K codes, V codes, K params, V params -- stream in by 2D
-//    TMA tile loads into a 3-stage (INT4) or 5-stage (INT2) shared-memory ring
+//  * 128-token tiles -- K codes, V codes (2D TMA tile loads), K params, V params
+//    (1D bulk copies: a tile's params are 2 KB of contiguous 16-byte rows, which
+//    a tile load would move row by row) -- stream into a 3-stage (INT4) or
+//    5-stage (INT2) shared-memory ring
 //    guarded by mbarriers (the asynchronous staging of the BitDecoding page,
 //    section 2.3, done with the bulk tensor copy instead of per-thread
 //    cp.async).  One thread issues the first stages up front; the warp that
@@ -406,7 +408,6 @@ __device__ __forceinline__ void residual_tc(const F16Rows& fr, int c0, uint8_t* 
 template <int BITS, bool STEP>
 __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
-                     const __grid_constant__ CUtensorMap tm_kp, const __grid_constant__ CUtensorMap tm_vp,
                      const DecodeArgs a) {
   using G = Geo<BITS>;
   constexpr int NSTAGE = G::NSTAGE;
@@ -464,8 +465,6 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
     if (!res_cta) {
       ptx::prefetch_tensormap(&tm_kc);
       ptx::prefetch_tensormap(&tm_vc);
-      ptx::prefetch_tensormap(&tm_kp);
-      ptx::prefetch_tensormap(&tm_vp);
     }
   }
   // A launch that depends on this one programmatically (the next step) may
@@ -475,18 +474,25 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
 
   int i0 = 0, i1 = 0, ntiles = 0, row0 = 0;
   uint32_t err_bits = 0;
+  // packed rows in the codes / params arrays (bulk copies must stay inside)
+  const int64_t prows = a.rm.paged ? (int64_t)a.rm.npages * a.Hkv * kPage
+                                   : (int64_t)gridDim.z * a.Hkv * a.cap;
+  constexpr uint32_t kParRow = NG * 4;  // param bytes per packed row
   auto issue = [&](int tile) {
     const int st = tile % NSTAGE;
     s_last_tile[st] = tile;
     uint8_t* base = smem + (size_t)st * G::STAGE;
     const uint32_t fb = ptx::smem_u32(&full_bar[st]);
     if (!a.rm.paged) {
-      ptx::mbar_arrive_expect_tx(fb, G::STAGE);
+      // y lies inside this head's rows; the params copy stops at the array end
+      // (rows past the split end are masked)
       const int y = row0 + tile * T;
+      const uint32_t pbytes = (uint32_t)min((int64_t)T, prows - y) * kParRow;
+      ptx::mbar_arrive_expect_tx(fb, 2 * G::CODE_TILE + 2 * pbytes);
       ptx::tma_load_2d(ptx::smem_u32(base + G::KC), &tm_kc, 0, y, fb);
       ptx::tma_load_2d(ptx::smem_u32(base + G::VC), &tm_vc, 0, y, fb);
-      ptx::tma_load_2d(ptx::smem_u32(base + G::KP), &tm_kp, 0, y, fb);
-      ptx::tma_load_2d(ptx::smem_u32(base + G::VP), &tm_vp, 0, y, fb);
+      ptx::bulk_load(ptx::smem_u32(base + G::KP), a.k_params + (int64_t)y * NG, pbytes, fb);
+      ptx::bulk_load(ptx::smem_u32(base + G::VP), a.v_params + (int64_t)y * NG, pbytes, fb);
     } else {
       // the tile's pages (i0 is a page boundary), 32 rows of each array apiece;
       // stage rows past the split's last page keep stale bytes, masked like
@@ -494,19 +500,28 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
       constexpr int kPerTile = T / kPage;
       const int j0 = tile * kPerTile;
       const int np = min(kPerTile, (i1 - i0 + kPage - 1) / kPage - j0);
-      ptx::mbar_arrive_expect_tx(fb, (uint32_t)np * (G::STAGE / kPerTile));
+      int ys[kPerTile];
+      uint32_t bytes = 0;
       for (int p = 0; p < np; ++p) {
         const int j = j0 + p;
         const int pg = j < kPagePrefetch ? s_pages[j] : a.rm.page_of(b, i0 / kPage + j);
-        int y = -kPage;  // a page outside the pool reads zeros (and is flagged)
-        if (pg >= 0 && pg < a.rm.npages)
-          y = (pg * a.Hkv + h) * kPage;
-        else
-          set_error(a.err_word, KVQ_ERRBIT_BADPAGE);
+        // a page outside the pool: its codes read zeros (TMA fill), no params
+        // are copied, and the page is flagged
+        ys[p] = (pg >= 0 && pg < a.rm.npages) ? (pg * a.Hkv + h) * kPage : -kPage;
+        bytes += 2 * kPage * G::RB + (ys[p] >= 0 ? 2 * kPage * kParRow : 0);
+        if (ys[p] < 0) set_error(a.err_word, KVQ_ERRBIT_BADPAGE);
+      }
+      ptx::mbar_arrive_expect_tx(fb, bytes);
+      for (int p = 0; p < np; ++p) {
+        const int y = ys[p];
         ptx::tma_load_2d(ptx::smem_u32(base + G::KC + p * kPage * G::RB), &tm_kc, 0, y, fb);
         ptx::tma_load_2d(ptx::smem_u32(base + G::VC + p * kPage * G::RB), &tm_vc, 0, y, fb);
-        ptx::tma_load_2d(ptx::smem_u32(base + G::KP + p * kPage * NG * 4), &tm_kp, 0, y, fb);
-        ptx::tma_load_2d(ptx::smem_u32(base + G::VP + p * kPage * NG * 4), &tm_vp, 0, y, fb);
+        if (y >= 0) {
+          ptx::bulk_load(ptx::smem_u32(base + G::KP + p * kPage * kParRow),
+                         a.k_params + (int64_t)y * NG, kPage * kParRow, fb);
+          ptx::bulk_load(ptx::smem_u32(base + G::VP + p * kPage * kParRow),
+                         a.v_params + (int64_t)y * NG, kPage * kParRow, fb);
+        }
       }
     }
   };
@@ -1078,12 +1093,10 @@ cudaError_t launch_bits(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
   const bool paged = s.page != 0;
   const uint64_t rows = paged ? (uint64_t)s.npages * s.Hkv * kPage : (uint64_t)s.B * s.Hkv * s.cap;
   const uint32_t box = paged ? kPage : T;
-  CUtensorMap kc, vc, kp, vp;
+  CUtensorMap kc, vc;
   const CUtensorMapSwizzle swz = BITS == 4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
   if (!make_rows_map(&kc, a.k_codes, Gm::RB, rows, swz, box) ||
-      !make_rows_map(&vc, a.v_codes, Gm::RB, rows, swz, box) ||
-      !make_rows_map(&kp, a.k_params, NG * 4, rows, CU_TENSOR_MAP_SWIZZLE_NONE, box) ||
-      !make_rows_map(&vp, a.v_params, NG * 4, rows, CU_TENSOR_MAP_SWIZZLE_NONE, box))
+      !make_rows_map(&vc, a.v_codes, Gm::RB, rows, swz, box))
     return cudaErrorInvalidValue;
   constexpr size_t smem = tc_smem_bytes<BITS>();
   static bool attr_set = false;
@@ -1103,7 +1116,7 @@ cudaError_t launch_bits(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<BITS, STEP>, kc, vc, kp, vp, a);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<BITS, STEP>, kc, vc, a);
 }
 
 }  // namespace
