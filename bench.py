@@ -348,7 +348,7 @@ def run_ours(args, rank, world, local):
     all_bytes_gbs = (step_bytes + res_bytes + qo_bytes) / (ms_per_step * 1e-3) / 1e9
     # the step is one fused launch on the tensor-core path (append + decode),
     # else an append and a decode launch
-    fused = w.head_dim == 128 and w.bits != 3 and 1 <= w.num_q_heads // w.num_kv_heads <= 4
+    fused = w.head_dim == 128 and 1 <= w.num_q_heads // w.num_kv_heads <= 4
     launches = 1 if fused else 2
     if fused:  # the dominant kernel is the step kernel itself
         rf_kernel, rf_us = "decode_step (append + split-KV decode + combine, one launch)", ms_per_step * 1e3

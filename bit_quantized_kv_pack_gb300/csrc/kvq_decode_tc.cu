@@ -1,5 +1,5 @@
 // kvq_decode_tc.cu -- split-KV decode attention on the tensor cores (head_dim
-// 128, up to 4 query heads per KV head, INT4 or INT2 codes).
+// 128, up to 4 query heads per KV head, INT4, INT3 or INT2 codes).
 //
 // What it computes is the same as the generic kernel: O = softmax(q K^T /
 // sqrt(d)) V over the packed tokens (dequantized min + code * scale, InnerQ page
@@ -49,6 +49,9 @@
 //    exact log-sum-exp merge of the split partials (combine_unit) instead.
 //  * Three CTAs per SM (168 registers each): twelve warps hide the latency of
 //    the dequantize-and-MMA chain.
+//  * 3-bit codes (TurboQuant page section 3.1) arrive as plain 48-byte rows;
+//    each warp widens its 32 rows to INT4 nibbles in a buffer of its own (the
+//    INT4 swizzle), and the INT4 arithmetic runs on that buffer.
 //  * Paged caches (32-token pages through a block table, TurboQuant page
 //    section 6.1): packed splits start on page boundaries and a stage is filled
 //    by one 32-row tile load per page of the pool instead of one 128-row load.
@@ -74,6 +77,7 @@ static_assert(NCW == QB, "the merge gives each warp one query");
 
 template <int BITS>
 struct Geo {
+  static constexpr int CB = BITS == 3 ? 4 : BITS;  // code width of the arithmetic
   static constexpr int RB = D * BITS / 8;      // code bytes per token row
   static constexpr int CODE_TILE = T * RB;     // 8192 (INT4) / 4096 (INT2)
   static constexpr int PAR_TILE = T * NG * 4;  // 2048
@@ -82,8 +86,10 @@ struct Geo {
   static constexpr int KP = 2 * CODE_TILE;
   static constexpr int VP = 2 * CODE_TILE + PAR_TILE;
   static constexpr int STAGE = 2 * CODE_TILE + 2 * PAR_TILE;  // 20 KB / 12 KB
-  static constexpr int NSTAGE = BITS == 4 ? 3 : 5;               // 60 KB in flight per CTA
-  static constexpr float CENTER = BITS == 4 ? 7.5f : 1.5f;       // mid code
+  static constexpr int NSTAGE = BITS == 2 ? 5 : 3;  // 60 KB (INT4, INT2) / 48 KB (INT3) in flight
+  static constexpr float CENTER = BITS == 4 ? 7.5f : (BITS == 3 ? 3.5f : 1.5f);  // mid code
+  // INT3: per warp 32 widened rows of K and of V, 64 bytes each
+  static constexpr int XBUF = BITS == 3 ? NCW * 2 * 32 * 64 : 0;
   static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned");
 };
 
@@ -101,12 +107,43 @@ struct MergeSmem {
 constexpr size_t kResTilesOff = (sizeof(MergeSmem) + 4 * D * sizeof(float) + 127) & ~(size_t)127;
 template <int BITS>
 constexpr size_t tc_smem_bytes() {
-  constexpr size_t ring = (size_t)Geo<BITS>::NSTAGE * Geo<BITS>::STAGE;
+  constexpr size_t ring = (size_t)Geo<BITS>::NSTAGE * Geo<BITS>::STAGE + Geo<BITS>::XBUF;
   constexpr size_t res = kResTilesOff + 2 * 64 * (2 * D + 16);  // kResRows rows of K and V
   return 1024 + (ring > res ? ring : res);
 }
 
 // ------------------------------------------------------- code conversion ---
+
+// One 3-bit code row (128 codes, 48 bytes, code e at bits 3e) widened to INT4
+// (64 bytes, code e at bits 4e), stored as row `lrow` of a 32-row INT4 buffer
+// at `dst` with the INT4 tile swizzle (16-byte chunk ^= (lrow >> 1) & 3).  Each
+// output word takes 24 source bits (eight codes) and spreads them to nibbles in
+// three mask-and-shift steps: 12-bit halves to 16-bit halves, 6-bit pairs to
+// bytes, 3-bit codes to nibbles.
+__device__ __forceinline__ void widen_row3(const uint8_t* src, uint32_t dst, int lrow) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  const uint4 a = s4[0], b = s4[1], c = s4[2];
+  const uint32_t w[12] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {  // one 16-byte chunk = one group of 32 codes
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int bit = 24 * (4 * ch + k);
+      const int wi = bit >> 5, sh = bit & 31;
+      uint32_t x = w[wi] >> sh;
+      if (sh > 8) x |= w[wi + 1] << (32 - sh);  // the 24 bits straddle two words
+      x &= 0xFFFFFFu;
+      uint32_t y = (x & 0xFFFu) | ((x & 0xFFF000u) << 4);
+      y = (y & 0x003F003Fu) | ((y & 0x0FC00FC0u) << 2);
+      o[k] = (y & 0x07070707u) | ((y & 0x38383838u) << 1);
+    }
+    const uint32_t addr = dst + lrow * 64 + ((ch ^ ((lrow >> 1) & 3)) << 4);
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(o[0]), "r"(o[1]),
+                 "r"(o[2]), "r"(o[3])
+                 : "memory");
+  }
+}
 
 // Code words -> exact half2 operands (subnormal fp16, see the file comment).
 // INT4: nibble j of each 16-bit half (j = 0..3) -> out[j] = (nibble j of the
@@ -637,14 +674,11 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
       const int64_t row = a.rm.row(b, h, Lp);  // warp-uniform
       if (row < 0 && lane == 0) set_error(a.err_word, KVQ_ERRBIT_BADPAGE);
       if (a.hybrid && lane == 0 && row >= 0) a.w_modes[which][row] = mode_byte(modes, 0, NG);
-      if (active && row >= 0) {
+      {
         const int gi = lane >> 2, quad = lane & 3;
-        uint8_t* dst = a.w_codes[which] + row * a.row_bytes + gi * (4 * BITS) + quad * BITS;
-        if (BITS == 4)
-          *reinterpret_cast<uint32_t*>(dst) = packed;
-        else
-          *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
-        if (quad == 0) a.w_params[which][row * NG + gi] = prm;
+        store_group_codes<BITS>(a.w_codes[which] + (row < 0 ? 0 : row) * a.row_bytes + gi * (4 * BITS),
+                                packed, quad, active && row >= 0);
+        if (active && row >= 0 && quad == 0) a.w_params[which][row * NG + gi] = prm;
       }
       if (active) {  // the packed token as it is attended, dequantized in fp32
         const float sc = half_lo(prm), mn = half_hi(prm);
@@ -771,7 +805,7 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
       for (int P = 0; P < 2; ++P) {
 #pragma unroll
         for (int st = 0; st < 4; ++st) {
-          if (BITS == 4) {
+          if (G::CB == 4) {
             // k rows 2t, 2t+1 <- group P, d = 8t + st (+4); 2t+8, 2t+9 <- group P+2
             const int da = 32 * P + 8 * t + st;
             const int db = 32 * (P + 2) + 8 * t + st;
@@ -816,15 +850,28 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
           }
           __syncwarp();
         }
-        const uint32_t kc = ptx::smem_u32(base + G::KC);
-        const uint32_t vc = ptx::smem_u32(base + G::VC);
+        uint32_t kc = ptx::smem_u32(base + G::KC);
+        uint32_t vc = ptx::smem_u32(base + G::VC);
         const uint32_t* kp = reinterpret_cast<const uint32_t*>(base + G::KP);
         const uint32_t* vp = reinterpret_cast<const uint32_t*>(base + G::VP);
+        int crow = wrow;  // this warp's first row in the code tiles it reads
+        if constexpr (BITS == 3) {
+          // widen the warp's 32 rows of K and V codes (lane = row) into its own
+          // INT4 buffers; the params stay in the stage (rows offset by wrow)
+          uint8_t* xk = smem + (size_t)NSTAGE * G::STAGE + (size_t)warp * (2 * 32 * 64);
+          widen_row3(base + G::KC + (wrow + lane) * G::RB, ptx::smem_u32(xk), lane);
+          widen_row3(base + G::VC + (wrow + lane) * G::RB, ptx::smem_u32(xk + 32 * 64), lane);
+          __syncwarp();
+          kc = ptx::smem_u32(xk);
+          vc = ptx::smem_u32(xk + 32 * 64);
+          vp += wrow * NG;
+          crow = 0;
+        }
 
         // ---------------- QK for both sub-tiles
         float acc[NSUB][2][4];
 #pragma unroll
-        for (int u = 0; u < NSUB; ++u) qk_subtile<BITS>(kc, wrow + 16 * u, lane, bq, acc[u]);
+        for (int u = 0; u < NSUB; ++u) qk_subtile<G::CB>(kc, crow + 16 * u, lane, bq, acc[u]);
 
         // fix-up, fp32: acc_g = 2^-24 sum c q, so 2^-24 s = sum_g scale_g acc_g +
         // min_g (2^-24 qsum_g) for query t; rows past the split end masked
@@ -839,8 +886,8 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
             float acc_s = 0.f;
 #pragma unroll
             for (int P = 0; P < 2; ++P) {
-              const int ga = BITS == 4 ? P : 2 * P;
-              const int gb = BITS == 4 ? P + 2 : 2 * P + 1;
+              const int ga = G::CB == 4 ? P : 2 * P;
+              const int gb = G::CB == 4 ? P + 2 : 2 * P + 1;
               acc_s = fmaf(half_lo(prm[ga]), acc[u][P][2 * rr], acc_s);
               acc_s = fmaf(half_lo(prm[gb]), acc[u][P][2 * rr + 1], acc_s);
             }
@@ -893,7 +940,7 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
           const uint32_t x1 = __shfl_sync(0xffffffffu, pk, srcB);  // (p(2t+1), p(2t+9))
           const uint32_t pb0 = ptx::prmt(x0, x1, 0x5410u);  // tokens 2t, 2t+1
           const uint32_t pb1 = ptx::prmt(x0, x1, 0x7632u);  // tokens 2t+8, 2t+9
-          pv_subtile<BITS>(vc, vp, wrow + 16 * u, lane, pb0, pb1, oc, sb, mnacc);
+          pv_subtile<G::CB>(vc, vp, crow + 16 * u, lane, pb0, pb1, oc, sb, mnacc);
         }
       }
       __syncwarp();
@@ -940,7 +987,7 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
     for (int c = 0; c < 2; ++c)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        if (BITS == 4) {
+        if (G::CB == 4) {
           const float f = kTwo24 / w4_weight(j);
           const int d0 = 64 * c + 4 * g + j;
           ms.o[warp][t][d0] = fmaf(oc[c][j][0], f, ms.mn[warp][2 * c][t]);
@@ -1094,7 +1141,10 @@ cudaError_t launch_bits(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
   const uint64_t rows = paged ? (uint64_t)s.npages * s.Hkv * kPage : (uint64_t)s.B * s.Hkv * s.cap;
   const uint32_t box = paged ? kPage : T;
   CUtensorMap kc, vc;
-  const CUtensorMapSwizzle swz = BITS == 4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  // INT3 rows (48 bytes) load unswizzled: each warp re-lays them out itself
+  const CUtensorMapSwizzle swz = BITS == 4   ? CU_TENSOR_MAP_SWIZZLE_64B
+                                 : BITS == 3 ? CU_TENSOR_MAP_SWIZZLE_NONE
+                                             : CU_TENSOR_MAP_SWIZZLE_32B;
   if (!make_rows_map(&kc, a.k_codes, Gm::RB, rows, swz, box) ||
       !make_rows_map(&vc, a.v_codes, Gm::RB, rows, swz, box))
     return cudaErrorInvalidValue;
@@ -1122,9 +1172,7 @@ cudaError_t launch_bits(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
 }  // namespace
 
 bool tc_supported(const kvq_cache_desc& D, int gq) {
-  // 3-bit codes straddle the 16-bit halves the code-to-fp16 conversion works on
-  return D.head_dim == 128 && D.bits != 3 && gq >= 1 && gq <= QB && D.capacity > 0 &&
-         encode_fn() != nullptr;
+  return D.head_dim == 128 && gq >= 1 && gq <= QB && D.capacity > 0 && encode_fn() != nullptr;
 }
 
 int tc_threads() { return NTHREADS; }
@@ -1133,6 +1181,7 @@ int tc_residual_rows() { return kResRows; }
 
 cudaError_t launch_decode_tc(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
                              cudaStream_t st, bool step) {
+  if (s.bits == 3) return step ? launch_bits<3, true>(s, p, a, st) : launch_bits<3, false>(s, p, a, st);
   if (step) return s.bits == 4 ? launch_bits<4, true>(s, p, a, st) : launch_bits<2, true>(s, p, a, st);
   return s.bits == 4 ? launch_bits<4, false>(s, p, a, st) : launch_bits<2, false>(s, p, a, st);
 }

@@ -257,8 +257,7 @@ kvq_status kvq_decode_attention(const kvq_cache_desc* desc, const kvq_cache_view
  * The cache bytes, counters and error bits afterwards are exactly those of the
  * two calls; the output equals the two calls' within rounding (the token packed
  * by this step is attended in fp32 from its codes rather than on the tensor
- * cores).  With head_dim 128, INT4 or INT2 codes and at most 4 query heads per
- * KV head this is one
+ * cores).  With head_dim 128 and at most 4 query heads per KV head this is one
  * kernel launch: the packed splits read only rows written before the step, the
  * residual split of each head does the append's writes and attends over the new
  * and the packed token, and the counters move when the last head of a sequence

@@ -1,8 +1,9 @@
 """GPU parity of 3-bit codes (eight per 24 bits, TurboQuant page, section 3.1,
 on the same asymmetric rule): pack, append, decode and the decode step against
 the oracle -- codes, scales and mins bit-exact, outputs within max abs 2e-3 /
-relative L2 1e-3 of the fp64 oracle.  3-bit caches decode on the CUDA-core
-kernel; the fused step is its append and decode launches."""
+relative L2 1e-3 of the fp64 oracle.  head_dim 128 with up to 4 query heads
+per KV head decodes on the tensor-core kernel (rows widened to INT4 in shared
+memory, the fused step one launch); other shapes on the CUDA-core kernel."""
 
 import numpy as np
 import pytest
