@@ -44,7 +44,8 @@ def test_int3_pack(d, hybrid):
     assert_cache_equal(g, r)
 
 
-@pytest.mark.parametrize("d,gq,S", [(128, 4, 0), (64, 2, 32), (256, 8, 0), (32, 1, 4), (128, 1, 0)])
+@pytest.mark.parametrize("d,gq,S", [(128, 4, 0), (64, 2, 32), (256, 8, 0), (32, 1, 4), (128, 1, 0),
+                                    (128, 3, 32)])
 def test_int3_decode(d, gq, S):
     rng = np.random.default_rng(d * 7 + gq + S)
     B, H, Nr = 3, 2, 19

@@ -44,7 +44,7 @@ def test_paged_pack(bits, hybrid, S, d):
     assert_cache_equal(g, r)
 
 
-@pytest.mark.parametrize("bits", [4, 2])
+@pytest.mark.parametrize("bits", [4, 2, 3])
 @pytest.mark.parametrize("d,gq", [(128, 4), (128, 1), (64, 2)])
 def test_paged_decode(bits, d, gq):
     """Tensor-core kernel (head_dim 128, page-aligned splits, four page loads per
