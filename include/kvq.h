@@ -266,7 +266,7 @@ kvq_status kvq_decode_attention(const kvq_cache_desc* desc, const kvq_cache_view
  * KVQ_ERRBIT_CAPACITY and is attended as it was.
  *   flags      0, or KVQ_STEP_EARLY_CACHE_READ: the caller states that the
  *              kernel enqueued on `stream` just before this call does not write
- *              this cache (codes, params, window, counters) -- in a serving loop
+ *              this cache (any array of its view, counters included) -- in a serving loop
  *              it computes q, k_new and v_new, and the cache was last written by
  *              this layer's previous step.  The step (launched as a programmatic
  *              dependent of that kernel) then reads the counters and starts its
