@@ -135,7 +135,8 @@ typedef enum {
 #define KVQ_ERRBIT_EMPTY 0x2u    /* decode saw a sequence with no tokens; output zeroed */
 #define KVQ_ERRBIT_TIMEOUT 0x4u  /* a bounded wait gave up; that CTA wrote nothing */
 #define KVQ_ERRBIT_BADLEN 0x8u   /* seq_lens[b] < 0 or > Lmax; that sequence was skipped */
-#define KVQ_ERRBIT_BADPAGE 0x10u /* a block-table page outside [0, NP); that token was skipped */
+#define KVQ_ERRBIT_BADPAGE 0x10u /* a block-table page outside [0, NP): pack/append wrote nothing
+                                   there; decode output of that sequence is undefined */
 
 /* Static description of one layer's cache.  group must be 32.  Every field is
  * significant: zero-initialise the struct (sink = 0 keeps no sink window). */
