@@ -566,7 +566,7 @@ def run_reference(args, rank, world):
     npk_b = packed_per_seq(w, lens, args.sink)
     n_total = args.warmup + args.steps
     r = oracle.Cache(w.batch, w.num_kv_heads, w.head_dim, w.bits, max(npk_b) + n_total + 8, w.residual,
-                     args.sink)
+                     args.sink, args.hybrid)
     oracle.quantize_pack(r, k.numpy(), v.numpy(), lens.numpy())
     del k, v
     per_tok = 2 * (w.head_dim * w.bits // 8 + 4 * (w.head_dim // 32))
@@ -605,7 +605,9 @@ def run_reference(args, rank, world):
         "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded SplitMix64 + Box-Muller, fp16)",
-        "config": workload_config(w, sum(npk_b), {"sink": args.sink} if args.sink else None),
+        "config": workload_config(w, sum(npk_b), {
+            **({"sink": args.sink} if args.sink else {}),
+            **({"hybrid": "sym/asym per group, mode bytes"} if args.hybrid else {})}),
         "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
