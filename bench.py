@@ -406,9 +406,10 @@ def run_ours(args, rank, world, local):
     }
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args.cpu_seconds, workload=args.workload, sink=args.sink,
-                                           bits=args.bits)
+                                           bits=args.bits, hybrid=args.hybrid)
         res["cpu_baseline_all_cores"] = cpu_baseline_all_cores(res["cpu_baseline"], args.workload,
-                                                               sink=args.sink, bits=args.bits)
+                                                               sink=args.sink, bits=args.bits,
+                                                               hybrid=args.hybrid)
     return res
 
 
@@ -454,7 +455,7 @@ def run_e2e(st, args):
 # ---------------------------------------------------------- oracle arm -----
 
 def cpu_baseline(seconds: float, steps: int | None = None, workload: int = WORKLOAD, sink: int = 0,
-                 bits: int = 0):
+                 bits: int = 0, hybrid: int = 0):
     """The CPU oracle as it stands (single thread) on whole steps of the same
     workload: append + fp64 decode of every query head."""
     import oracle
@@ -466,7 +467,7 @@ def cpu_baseline(seconds: float, steps: int | None = None, workload: int = WORKL
     npk0 = sum(npk_b)
     n_steps_max = steps if steps is not None else 1000
     r = oracle.Cache(w.batch, w.num_kv_heads, w.head_dim, w.bits, max(npk_b) + n_steps_max + 8,
-                     w.residual, sink)
+                     w.residual, sink, hybrid)
     oracle.quantize_pack(r, k.numpy(), v.numpy(), lens.numpy())
     del k, v
     per_tok = 2 * (w.head_dim * w.bits // 8 + 4 * (w.head_dim // 32))
@@ -492,7 +493,7 @@ def _oracle_units_worker(job):
     """One process of the all-cores CPU baseline: whole decode steps (append +
     fp64 decode of every query head) for its (sequence, KV head) units, each in
     a cache of its own.  Returns the seconds of its step loop."""
-    workload, units, n_steps, sink, bits = job
+    workload, units, n_steps, sink, bits, hybrid = job
     import oracle
     from bit_quantized_kv_pack_gb300 import synth
     w = workload_for(workload, bits)
@@ -501,7 +502,7 @@ def _oracle_units_worker(job):
     caches = []
     for b, h in units:
         L = int(lens[b])
-        r = oracle.Cache(1, 1, w.head_dim, w.bits, L + n_steps + 8, w.residual, sink)
+        r = oracle.Cache(1, 1, w.head_dim, w.bits, L + n_steps + 8, w.residual, sink, hybrid)
         oracle.quantize_pack(r, k[b:b + 1, h:h + 1].numpy().copy(), v[b:b + 1, h:h + 1].numpy().copy(),
                              lens[b:b + 1].numpy().copy())
         caches.append((b, h, r))
@@ -516,7 +517,7 @@ def _oracle_units_worker(job):
 
 
 def cpu_baseline_all_cores(single: dict, workload: int = WORKLOAD, seconds: float = 10.0,
-                           sink: int = 0, bits: int = 0):
+                           sink: int = 0, bits: int = 0, hybrid: int = 0):
     """The same oracle on all host cores: (sequence, KV head) units spread over
     spawned processes, each running whole steps on its units; throughput = step
     bytes x steps / the slowest process's time."""
@@ -533,7 +534,8 @@ def cpu_baseline_all_cores(single: dict, workload: int = WORKLOAD, seconds: floa
     # of being restarted, and a stuck one times out
     try:
         with ProcessPoolExecutor(max_workers=procs, mp_context=mp.get_context("spawn")) as ex:
-            futs = [ex.submit(_oracle_units_worker, (workload, sh, n_steps, sink, bits)) for sh in share]
+            futs = [ex.submit(_oracle_units_worker, (workload, sh, n_steps, sink, bits, hybrid))
+                    for sh in share]
             times = [f.result(timeout=600) for f in futs]
     except Exception as e:  # report, do not hang the benchmark
         return {"value": None, "unit": "GB/s", "cores": procs, "kind": "oracle",
