@@ -11,15 +11,16 @@
 // (KVQ_NOALLOC_SCRATCH_BYTES) until the process exits, and every call on a
 // device shares it.  The host only ever sees a stand-in for its name, so its
 // device address is looked up once per device with cudaGetSymbolAddress, with
-// that device current, on the first call there, which also clears the array
-// once (its arrival counters must start at zero; every completed call leaves
-// them at zero again); make that first call before any stream capture.  The
-// counters and accumulators that must be zero sit at offsets that depend on the
-// cache shape and head count, so a call whose shape differs from the previous
-// call's on the device first clears that part of the array (cudaMemsetAsync on
-// its stream; the first call after a shape change is then two operations).  Two
-// calls whose kernels overlap on the GPU race on the array: issue them on one
-// stream, or order the streams.
+// that device current, on the first call there; make that first call before any
+// stream capture.  The counters and accumulators that must be zero at the start
+// of a call sit at offsets that depend on the cache shape and head count, and
+// every completed call leaves them zero for its own shape.  So the first call on
+// a device, a call whose shape differs from the previous call's there, and the
+// first call after kvq_read_error reported a timed-out wait (which may leave
+// them non-zero) clear that part of the array first, with cudaMemsetAsync on the
+// call's own stream (the call is then two operations on that stream).  Two calls
+// whose kernels overlap on the GPU race on the array: issue them on one stream,
+// or order the streams.
 #include <mutex>
 
 #include "kvq_internal.cuh"
@@ -44,16 +45,14 @@ struct ZeroLayout {
 ZeroLayout g_last_layout[kMaxDevices];
 bool g_has_layout[kMaxDevices] = {false};
 
-// Device address of g_decode_scratch on the current device (set up once).
+// Device address of g_decode_scratch on the current device (looked up once).
 kvq_status scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_scratch_ptr[dev]) {
     void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
-    if (e == cudaSuccess && p != nullptr) e = cudaMemset(p, 0, KVQ_NOALLOC_SCRATCH_BYTES);
-    if (e != cudaSuccess || p == nullptr) {
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) {
       cudaGetLastError();
       return KVQ_ERR_CUDA;
     }
@@ -64,6 +63,22 @@ kvq_status scratch_address(void** out) {
 }
 
 }  // namespace
+
+namespace kvq {
+
+// After a timed-out wait the counters of the array on this device may be left
+// non-zero: the next call clears them whatever its shape.
+void noalloc_forget_layout() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_has_layout[dev] = false;
+}
+
+}  // namespace kvq
 
 extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_cache_desc* desc,
                                                    const kvq_cache_view* view, const void* q,
