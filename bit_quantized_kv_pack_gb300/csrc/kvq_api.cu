@@ -78,18 +78,33 @@ size_t kvq_decode_workspace_bytes(const kvq_cache_desc* desc, int32_t num_q_head
   return kvq::plan_decode(*desc, num_q_heads, kvq::device_sm_count(), true).ws_total;
 }
 
-kvq_status kvq_quantize_pack(const kvq_cache_desc* desc, const kvq_cache_view* view,
-                             const void* k, const void* v, const int32_t* seq_lens,
-                             int32_t Lmax, void* stream) {
+kvq_status kvq_quantize_pack_strided(const kvq_cache_desc* desc, const kvq_cache_view* view,
+                                     const void* k, const void* v, const int32_t* seq_lens,
+                                     int32_t Lmax, int64_t stride_b, int64_t stride_h,
+                                     int64_t stride_t, void* stream) {
   kvq_status st = check_desc(desc);
   if (st != KVQ_OK) return st;
   if ((st = check_view(*desc, view)) != KVQ_OK) return st;
   if (Lmax < 0 || !seq_lens || (Lmax > 0 && (!k || !v))) return KVQ_ERR_INVALID_ARG;
+  if (stride_b < 0 || stride_h < 0 || stride_t < 0) return KVQ_ERR_INVALID_ARG;
   if (!aligned(k, 16) || !aligned(v, 16) || !aligned(seq_lens, 4)) return KVQ_ERR_MISALIGNED;
+  // every 8-value piece a lane loads must start on a 16-byte boundary
+  if (stride_b % 8 || stride_h % 8 || stride_t % 8) return KVQ_ERR_MISALIGNED;
   const Dims s = kvq::dims_of(*desc);
+  const int64_t strides[3] = {stride_b, stride_h, stride_t};
   return from_cuda(kvq::launch_quantize_pack(s, *view, static_cast<const __half*>(k),
-                                             static_cast<const __half*>(v), seq_lens, Lmax,
+                                             static_cast<const __half*>(v), seq_lens, Lmax, strides,
                                              static_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_quantize_pack(const kvq_cache_desc* desc, const kvq_cache_view* view,
+                             const void* k, const void* v, const int32_t* seq_lens,
+                             int32_t Lmax, void* stream) {
+  if (check_desc(desc) != KVQ_OK) return check_desc(desc);
+  const int64_t d = desc->head_dim;
+  return kvq_quantize_pack_strided(desc, view, k, v, seq_lens, Lmax,
+                                   (int64_t)desc->num_kv_heads * Lmax * d, (int64_t)Lmax * d, d,
+                                   stream);
 }
 
 kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache_view* view, const void* k_new,
@@ -209,6 +224,7 @@ kvq_status kvq_read_error(const kvq_cache_view* view, uint32_t* word_out, void* 
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return KVQ_ERR_CUDA;
   if (word_out) *word_out = w;
+  if (w & KVQ_ERRBIT_TIMEOUT) kvq::noalloc_forget_layout();
   if (w & KVQ_ERRBIT_CAPACITY) return KVQ_ERR_CAPACITY;
   if (w & KVQ_ERRBIT_EMPTY) return KVQ_ERR_EMPTY;
   if (w & KVQ_ERRBIT_TIMEOUT) return KVQ_ERR_TIMEOUT;
@@ -230,6 +246,8 @@ const char* kvq_status_string(kvq_status status) {
   }
 }
 
-int32_t kvq_version(void) { return 140; }
+int32_t kvq_version(void) { return 150; }
+
+void kvq_testing_wait_fault(uint32_t limit_us) { kvq::set_testing_wait_fault_us(limit_us); }
 
 }  // extern "C"

@@ -3,6 +3,8 @@
 // the split partials runs at the end of each decode kernel (combine_unit).
 #include <math.h>
 
+#include <atomic>
+
 #include "kvq_decode_common.cuh"
 
 namespace kvq {
@@ -16,15 +18,28 @@ int next_pow2(int x) {
 
 }  // namespace
 
+// SM count of the current device, queried once per device (every plan needs it).
 int device_sm_count() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cached[kMaxDev];
   int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+  if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();  // clear a no-device error so it does not leak into later calls
     return 152;
   }
+  if (dev >= 0 && dev < kMaxDev && (n = cached[dev].load(std::memory_order_relaxed)) > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 152;
+  }
+  if (dev >= 0 && dev < kMaxDev) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
+
+// Testing hook of kvq_testing_wait_fault (0: off).
+static std::atomic<uint32_t> g_wait_fault_us{0};
+void set_testing_wait_fault_us(uint32_t us) { g_wait_fault_us.store(us, std::memory_order_relaxed); }
+uint32_t testing_wait_fault_us() { return g_wait_fault_us.load(std::memory_order_relaxed); }
 
 DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count, bool step) {
   DecodePlan p;
@@ -143,6 +158,9 @@ cudaError_t launch_decode(const Dims& s, const DecodePlan& p, const kvq_cache_vi
   a.row_bytes = s.row_bytes;
   a.early = (flags & KVQ_STEP_EARLY_CACHE_READ) ? 1 : 0;
   a.qk_scale_log2 = (float)(1.4426950408889634 / sqrt((double)s.d));
+  const uint32_t fault_us = testing_wait_fault_us();
+  a.wait_limit_us = fault_us ? fault_us : 1000000u;
+  a.fault_tx = fault_us ? 16u : 0u;
   const bool step = k_new != nullptr;
   if (p.kernel == 1) return launch_decode_tc(s, p, a, st, step);
   cudaError_t e = cudaSuccess;

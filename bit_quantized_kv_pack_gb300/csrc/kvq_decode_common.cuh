@@ -53,6 +53,8 @@ struct DecodeArgs {
   int hybrid;  // the fused step quantizes by the hybrid rule
   int early;  // fused step: counters and first tiles may be read before griddepcontrol.wait
   int Sp;  // tensor-core kernel: splits s < Sp take packed tokens, s >= Sp fp16 ones
+  uint32_t wait_limit_us;  // bounded waits give up after this long (1 s unless a test set it)
+  uint32_t fault_tx;       // testing hook: extra bytes one tile's barrier expects (0: off)
   float qk_scale_log2;  // log2(e) / sqrt(d)
 };
 

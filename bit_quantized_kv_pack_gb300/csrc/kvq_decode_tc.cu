@@ -59,6 +59,10 @@
 // Every mbarrier wait is bounded; a wait that runs out sets KVQ_ERRBIT_TIMEOUT.
 #include <math.h>
 
+#include <atomic>
+#include <mutex>
+#include <unordered_map>
+
 #include "kvq_decode_common.cuh"
 #include "kvq_ptx.cuh"
 
@@ -461,6 +465,7 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
   __shared__ int s_last;
   __shared__ uint32_t s_ref[QB];  // the head's reference max per query (float bits + 1; 0: unknown)
   __shared__ int s_pages[kPagePrefetch];  // paged caches: the split's first page ids
+  __shared__ uint32_t s_bad[NSTAGE];      // paged caches: bit p = page p of the stage's tile is bad
 
   const int s = blockIdx.x;
   const int h = blockIdx.y;  // one query block per KV head (gq <= 4)
@@ -473,6 +478,10 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
   const int64_t bh = (int64_t)b * a.Hkv + h;
   const int f0 = kResRows * (s - a.Sp);  // an fp16 split's first row
   const bool has_f16 = a.Nr + a.Ns > 0;
+  const uint64_t wait_ns = (uint64_t)a.wait_limit_us * 1000u;
+  // testing hook (off unless the host armed it): the first tile of split 0 of
+  // (sequence 0, KV head 0) expects more bytes than its copies deliver
+  const uint32_t fault_tx = (s == 0 && h == 0 && b == 0) ? a.fault_tx : 0u;
   // the fp16 rows of this (sequence, KV head), ranges from the counters
   auto f16_rows = [&]() {
     F16Rows fr;
@@ -525,7 +534,7 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
       // (rows past the split end are masked)
       const int y = row0 + tile * T;
       const uint32_t pbytes = (uint32_t)min((int64_t)T, prows - y) * kParRow;
-      ptx::mbar_arrive_expect_tx(fb, 2 * G::CODE_TILE + 2 * pbytes);
+      ptx::mbar_arrive_expect_tx(fb, 2 * G::CODE_TILE + 2 * pbytes + (tile == 0 ? fault_tx : 0u));
       ptx::tma_load_2d(ptx::smem_u32(base + G::KC), &tm_kc, 0, y, fb);
       ptx::tma_load_2d(ptx::smem_u32(base + G::VC), &tm_vc, 0, y, fb);
       ptx::bulk_load(ptx::smem_u32(base + G::KP), a.k_params + (int64_t)y * NG, pbytes, fb);
@@ -538,7 +547,7 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
       const int j0 = tile * kPerTile;
       const int np = min(kPerTile, (i1 - i0 + kPage - 1) / kPage - j0);
       int ys[kPerTile];
-      uint32_t bytes = 0;
+      uint32_t bytes = tile == 0 ? fault_tx : 0u, bad = 0;
       for (int p = 0; p < np; ++p) {
         const int j = j0 + p;
         const int pg = j < kPagePrefetch ? s_pages[j] : a.rm.page_of(b, i0 / kPage + j);
@@ -546,8 +555,13 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
         // are copied, and the page is flagged
         ys[p] = (pg >= 0 && pg < a.rm.npages) ? (pg * a.Hkv + h) * kPage : -kPage;
         bytes += 2 * kPage * G::RB + (ys[p] >= 0 ? 2 * kPage * kParRow : 0);
-        if (ys[p] < 0) set_error(a.err_word, KVQ_ERRBIT_BADPAGE);
+        if (ys[p] < 0) {
+          set_error(a.err_word, KVQ_ERRBIT_BADPAGE);
+          bad |= 1u << p;
+        }
       }
+      // the consumers skip a bad page's rows (read after the barrier completes)
+      s_bad[st] = bad;
       ptx::mbar_arrive_expect_tx(fb, bytes);
       for (int p = 0; p < np; ++p) {
         const int y = ys[p];
@@ -651,7 +665,7 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
 
   // extra tokens of a fused step, fp32: [K, V][new token, packed token][D]
   float* xbuf = reinterpret_cast<float*>(smem + sizeof(MergeSmem));
-  if (STEP && res_cta && s_rng[3] != 0 && warp < 2) {
+  if (STEP && res_cta && warp < 2 && s_rng[3] != 0) {
     // the append's writes for this (sequence, KV head): warp 0 the K row, warp
     // 1 the V row, lane l < 16 holding values 8l .. 8l+7 (as in kvq_append)
     const int which = warp;
@@ -666,13 +680,16 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
       uint4 src = nv;
       if (a.Nr > 0 && active)
         src = *reinterpret_cast<const uint4*>(a.w_res[which] + (bh * a.Nr + rh) * D + lane * 8);
-      float x[8];
-      unpack8_f16(src, x);
       uint32_t prm, asym = 1;
-      const uint32_t packed = quantize_quad<BITS>(x, prm, a.hybrid != 0, &asym);
+      const uint32_t packed = quantize_quad<BITS>(src, prm, a.hybrid != 0, &asym);
       const uint32_t modes = __ballot_sync(0xffffffffu, (lane & 3) == 0 && asym);
       const int64_t row = a.rm.row(b, h, Lp);  // warp-uniform
-      if (row < 0 && lane == 0) set_error(a.err_word, KVQ_ERRBIT_BADPAGE);
+      if (row < 0 && lane == 0) {
+        // a page outside the pool: nothing is stored and, as a decode after
+        // kvq_append would, the token is not attended
+        set_error(a.err_word, KVQ_ERRBIT_BADPAGE);
+        s_rng[3] = xflags & ~2;
+      }
       if (a.hybrid && lane == 0 && row >= 0) a.w_modes[which][row] = mode_byte(modes, 0, NG);
       {
         const int gi = lane >> 2, quad = lane & 3;
@@ -832,14 +849,17 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
     bool ref_offered = false;
     for (int tile = 0; tile < ntiles; ++tile) {
       const int st = tile % NSTAGE;
-      if (!ptx::mbar_wait_bounded(ptx::smem_u32(&full_bar[st]), (tile / NSTAGE) & 1)) {
+      if (!ptx::mbar_wait_bounded(ptx::smem_u32(&full_bar[st]), (tile / NSTAGE) & 1, wait_ns)) {
         if (lane == 0) set_error(a.err_word, KVQ_ERRBIT_TIMEOUT);
         s_abort = 1;
         break;
       }
       uint8_t* base = smem + (size_t)st * G::STAGE;
       const int wrow = 32 * warp;                         // first row of this warp
-      const int nvalid = min(npk - tile * T - wrow, 32);  // rows of this warp still ours
+      // rows of this warp still ours; in a paged cache a warp's 32 rows are one
+      // page, and none of a page outside the pool takes part
+      int nvalid = min(npk - tile * T - wrow, 32);
+      if (a.rm.paged && ((s_bad[st] >> warp) & 1u)) nvalid = 0;
       if (nvalid > 0) {
         // rows past the split end may hold anything: zero their params so no
         // Inf/NaN reaches the arithmetic (their scores are masked anyway)
@@ -966,9 +986,26 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
     if (threadIdx.x == 0) {
       for (int st = 0; st < NSTAGE; ++st)
         if (s_last_tile[st] >= 0)
-          ptx::mbar_wait_bounded(ptx::smem_u32(&full_bar[st]), (s_last_tile[st] / NSTAGE) & 1);
+          ptx::mbar_wait_bounded(ptx::smem_u32(&full_bar[st]), (s_last_tile[st] / NSTAGE) & 1, wait_ns);
     }
     __syncthreads();  // the stage ring is idle from here on: reuse it for the merge
+    if (s_abort) {
+      // a wait ran out: this split contributes nothing (it still takes its
+      // ticket below, so the head's merge and the workspace stay consistent)
+      m_ref = -INFINITY;
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) oc[x][m][r] = 0.f;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        mnacc[r] = 0.f;
+        sb[0][r] = 0.f;
+        sb[1][r] = 0.f;
+      }
+    }
     if (ref_offered) s_ref[lane] = ref_cas == 0u ? __float_as_uint(ref_mine) + 1u : ref_cas;
     // per group x and query t, corr_x = sum p min_x + mid (sum p scale_x -
     // sum of the rounded p * scale_x), to shared memory first; then the outputs
@@ -1102,11 +1139,11 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// The driver's cuTensorMapEncodeTiled, looked up once per process.
 EncodeTiledFn encode_fn() {
+  static std::once_flag once;
   static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  std::call_once(once, [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
@@ -1115,13 +1152,13 @@ EncodeTiledFn encode_fn() {
       fn = reinterpret_cast<EncodeTiledFn>(p);
     else
       cudaGetLastError();
-  }
+  });
   return fn;
 }
 
 // A 2D view [rows][row_bytes] of uint8 with a box of box_rows whole rows.
-bool make_rows_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
-                   CUtensorMapSwizzle swz, uint32_t box_rows) {
+bool encode_rows_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
+                     CUtensorMapSwizzle swz, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn || rows == 0 || rows > 0x7fffffffull) return false;  // y is a 32-bit coordinate
   cuuint64_t dims[2] = {row_bytes, rows};
@@ -1131,6 +1168,64 @@ bool make_rows_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint6
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Encoded tensor maps, reused across calls.  A map is a pure function of its
+// key (base address, row bytes, rows, swizzle, box), so an entry stays valid
+// even after the memory behind it is freed and reallocated; a serving loop over
+// the layers of a model finds all its caches here after its first step.  The
+// table is emptied when it reaches kMapCacheMax entries.
+struct RowsMapKey {
+  const void* base;
+  uint64_t row_bytes, rows;
+  int swz;
+  uint32_t box;
+  bool operator==(const RowsMapKey& o) const {
+    return base == o.base && row_bytes == o.row_bytes && rows == o.rows && swz == o.swz &&
+           box == o.box;
+  }
+};
+struct RowsMapKeyHash {
+  size_t operator()(const RowsMapKey& k) const {
+    uint64_t h = reinterpret_cast<uintptr_t>(k.base) * 0x9E3779B97F4A7C15ull;
+    h ^= (k.rows + 0x632BE59BD9B4E019ull * (k.row_bytes + 131 * (uint64_t)k.swz + 7919 * k.box)) +
+         (h << 6) + (h >> 2);
+    return (size_t)h;
+  }
+};
+constexpr size_t kMapCacheMax = 4096;
+
+bool make_rows_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
+                   CUtensorMapSwizzle swz, uint32_t box_rows) {
+  static std::mutex mu;
+  static std::unordered_map<RowsMapKey, CUtensorMap, RowsMapKeyHash> cache;
+  const RowsMapKey k = {base, row_bytes, rows, (int)swz, box_rows};
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(k);
+  if (it != cache.end()) {
+    *map = it->second;
+    return true;
+  }
+  if (!encode_rows_map(map, base, row_bytes, rows, swz, box_rows)) return false;
+  if (cache.size() >= kMapCacheMax) cache.clear();
+  cache.emplace(k, *map);
+  return true;
+}
+
+// Raise the kernel's dynamic shared-memory limit once per device (the attribute
+// is per device; a process may drive several GPUs).
+template <int BITS, bool STEP>
+cudaError_t ensure_smem_attr(size_t smem) {
+  static std::atomic<uint64_t> done{0};  // bit i: set on device i
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(decode_tc_kernel<BITS, STEP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
 }
 
 template <int BITS, bool STEP>
@@ -1149,13 +1244,8 @@ cudaError_t launch_bits(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
       !make_rows_map(&vc, a.v_codes, Gm::RB, rows, swz, box))
     return cudaErrorInvalidValue;
   constexpr size_t smem = tc_smem_bytes<BITS>();
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<BITS, STEP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = ensure_smem_attr<BITS, STEP>(smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.splits, (unsigned)s.Hkv, (unsigned)s.B);
   cfg.blockDim = dim3(NTHREADS, 1, 1);

@@ -81,18 +81,30 @@ __device__ __forceinline__ void set_error(uint32_t* err_word, uint32_t bit) {
 // ----------------------------------------------------- group quantizer ------
 //
 // One group of 32 fp16 values is held by 4 consecutive lanes, 8 values each
-// (lane q of the quad holds values 8q .. 8q+7).  Steps Q1-Q4 with the op order
-// fixed by the header:
-//   Q1  min/max over the quad (local over 8, then shuffle-xor 1 and 2)
+// (lane q of the quad holds values 8q .. 8q+7 as one 16-byte word).  Steps
+// Q1-Q4 with the op order fixed by the header:
+//   Q1  min/max over the quad: fp16 min of the lane's values and of their
+//       negations (max = -min(-x), exact), then shuffle-xor 1 and 2 of both as one
+//       half2 -- min and max of fp16 values are exact in any order
 //   Q2  scale_f = (mx - mn) / (2^b - 1) in fp32, IEEE divide
 //   Q3  scale_h = fp16_rne(scale_f); min_h = fp16(mn + 0)
 //   Q4  code = clamp(rint((x - mn) / s), 0, 2^b - 1) with s = (float)scale_h and
-//       the IEEE divide, or 0 when s == 0 (computed through a reciprocal with
-//       the divide taken near rounding boundaries: the same codes).
-// Returns the lane's 8 codes packed little-endian (b = 4: 32 bits, b = 2: 16
-// bits) and the group's {scale, min} half2 bits.  All 32 lanes of the warp must
-// call it (the shuffles use the full mask); `active` lanes only matter for the
-// result, inactive lanes pass any finite values.
+//       the IEEE divide, or 0 when s == 0.
+// How Q4 is computed (same codes as the plain divide):
+//   dx = x - mn is one fp32 subtraction straight from the fp16 operand (exact
+//   conversion, one rounding, as (float)x - mn).  q = dx * rcp_rn(s), clamped
+//   to 2^b - 1 (every q above it gives code 2^b - 1 however it rounds), lies
+//   within 3 ulp of the IEEE quotient (|q| <= 2^b - 1, so within 6e-6), so rint
+//   can only differ where q is within 1e-5 of a half-integer; there the lane
+//   recomputes its codes with the IEEE divide.  rint itself is the
+//   round-to-nearest-even fp32 addition of 1.5 * 2^23, which leaves the integer
+//   in the low mantissa bits (0 <= q <= 15 < 2^22), and each code is added in
+//   at its bit offset with one shift-add (the constant mantissa bits of the
+//   eight sums are subtracted once at the end, modulo 2^32).
+// Returns the lane's 8 codes packed little-endian (8 * b bits) and the group's
+// {scale, min} half2 bits.  All 32 lanes of the warp must call it (the shuffles
+// use the full mask); `active` lanes only matter for the result, inactive lanes
+// pass any finite values.
 //
 // hybrid: the group also gets the symmetric candidate (H1 of the header) and
 // keeps it when it can be stored and its squared error (H2) is strictly below
@@ -118,46 +130,72 @@ __device__ __forceinline__ float quad_sq_error(const float (&x)[8], uint32_t pac
   return acc;
 }
 
+// (float)h - f with one rounding: the fp16 operand converts exactly.
+__device__ __forceinline__ float sub_f16_f32(unsigned short h, float f) {
+  float d;
+  asm("sub.rn.f32.f16 %0, %1, %2;" : "=f"(d) : "h"(h), "f"(f));
+  return d;
+}
+
 template <int BITS>
-__device__ __forceinline__ uint32_t quantize_quad(const float (&x)[8], uint32_t& params_out,
+__device__ __forceinline__ uint32_t quantize_quad(const uint4& raw, uint32_t& params_out,
                                                   bool hybrid = false, uint32_t* asym_bit = nullptr) {
   constexpr int kQmax = (1 << BITS) - 1;
-  float mn = x[0], mx = x[0];
-#pragma unroll
-  for (int j = 1; j < 8; ++j) {
-    mn = fminf(mn, x[j]);
-    mx = fmaxf(mx, x[j]);
-  }
+  const __half2* hv = reinterpret_cast<const __half2*>(&raw);
+  // Q1: (min, -max) of the lane's values, then of the quad
+  __half2 lo = __hmin2(__hmin2(hv[0], hv[1]), __hmin2(hv[2], hv[3]));
+  __half2 nhi = __hmin2(__hmin2(__hneg2(hv[0]), __hneg2(hv[1])),
+                        __hmin2(__hneg2(hv[2]), __hneg2(hv[3])));
+  __half2 mm = __halves2half2(__hmin(__low2half(lo), __high2half(lo)),
+                              __hmin(__low2half(nhi), __high2half(nhi)));
 #pragma unroll
   for (int o = 1; o <= 2; o <<= 1) {
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const uint32_t other = __shfl_xor_sync(0xffffffffu, *reinterpret_cast<const uint32_t*>(&mm), o);
+    mm = __hmin2(mm, *reinterpret_cast<const __half2*>(&other));
   }
+  const float mn = __low2float(mm);
+  const float mx = -__high2float(mm);
   const float scale_f = __fdiv_rn(__fsub_rn(mx, mn), (float)kQmax);
   const __half scale_h = __float2half_rn(scale_f);
   const __half min_h = __float2half_rn(__fadd_rn(mn, 0.0f));
   const float s = __half2float(scale_h);
-  // The code is rint of the IEEE quotient (x - mn) / s.  (x - mn) * rcp(s), with
-  // the correctly rounded reciprocal, is within 3 ulp of that quotient (it is
-  // at most about 2 * (2^b - 1), so within 6e-6); only when it lies within 1e-5
-  // of a half-integer can rint tell the two apart, and there the IEEE divide
-  // itself decides.  The codes are therefore those of the plain divide.
   const float r = s != 0.0f ? __frcp_rn(s) : 0.0f;
-  uint32_t packed = 0;
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  constexpr uint32_t kMagicBits = 0x4B400000u;
+  uint32_t magic_sum = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) magic_sum += kMagicBits << (BITS * j);
+  const unsigned short* xs = reinterpret_cast<const unsigned short*>(&raw);
+  float dx[8];
+  uint32_t acc = 0;
+  bool near_tie = false;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    int c = 0;
-    if (s != 0.0f) {
-      const float dx = __fsub_rn(x[j], mn);
-      float qf = __fmul_rn(dx, r);
-      if (fabsf(qf - floorf(qf) - 0.5f) < 1e-5f) qf = __fdiv_rn(dx, s);
-      c = __float2int_rn(qf);
-      c = min(max(c, 0), kQmax);
+    dx[j] = sub_f16_f32(xs[j], mn);
+    const float q = fminf(__fmul_rn(dx[j], r), (float)kQmax);
+    const float t = __fadd_rn(q, kMagic);
+    acc += __float_as_uint(t) << (BITS * j);
+    near_tie |= fabsf(__fsub_rn(q, __fsub_rn(t, kMagic))) > 0.49999f;
+  }
+  uint32_t packed = acc - magic_sum;
+  if (near_tie) {
+    // a quotient within 1e-5 of a half-integer: the IEEE divide decides
+    packed = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = s != 0.0f ? min(max(__float2int_rn(__fdiv_rn(dx[j], s)), 0), kQmax) : 0;
+      packed |= (uint32_t)c << (BITS * j);
     }
-    packed |= (uint32_t)c << (BITS * j);
   }
   params_out = (uint32_t)__half_as_ushort(scale_h) | ((uint32_t)__half_as_ushort(min_h) << 16);
   if (hybrid) {
+    float x[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(hv[i]);
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+    }
     constexpr int kHalf = 1 << (BITS - 1);
     constexpr int kQs = kHalf - 1;
     // H1: absmax / (2^(b-1) - 1); codes t + 2^(b-1); min = -2^(b-1) * scale
@@ -268,12 +306,21 @@ struct DecodePlan {
 // residual split per KV head, which takes the appended token).
 DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count, bool step = false);
 int device_sm_count();
+// kvq_decode_attention_noalloc: the next call on the current device clears the
+// static array's counters first (called when a wait ran out).
+void noalloc_forget_layout();
+// kvq_testing_wait_fault: the bounded-wait limit in microseconds the decode
+// calls use to make one wait run out (0: off, normal behaviour).
+void set_testing_wait_fault_us(uint32_t us);
+uint32_t testing_wait_fault_us();
 
 // ------------------------------------------------------------- launchers ---
 
+// k, vv: element (b, h, t, j) at base + b * strides[0] + h * strides[1] +
+// t * strides[2] + j.
 cudaError_t launch_quantize_pack(const Dims& s, const kvq_cache_view& v, const __half* k,
                                  const __half* vv, const int32_t* seq_lens, int Lmax,
-                                 cudaStream_t st);
+                                 const int64_t strides[3], cudaStream_t st);
 cudaError_t launch_append(const Dims& s, const kvq_cache_view& v, const __half* k_new,
                           const __half* v_new, cudaStream_t st);
 // k_new/v_new non-null: the fused step (append, then attend).  out is fp16, or

@@ -49,14 +49,14 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Wait for the phase with the given parity, giving up after about a second of
-// wall time (checked every 1024 polls).  Returns false if it gave up.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Wait for the phase with the given parity, giving up after limit_ns of wall
+// time (checked every 1024 polls).  Returns false if it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 1023u) == 0 && global_timer_ns() - t0 > 1000000000ull) return false;
+    if ((i & 1023u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -29,7 +29,7 @@ constexpr int kGroupsPerCta = kGroupsPerIter * kPackUnroll;
 
 // Index 0 = K, 1 = V (blockIdx.z).
 struct PackArgs {
-  const __half* x[2];    // [B][Hkv][Lmax][d]
+  const __half* x[2];    // element (b, h, t, j) at x + b * sb + h * sh + t * st + j
   uint8_t* codes[2];     // [B][Hkv][cap][row_bytes]
   uint32_t* params[2];   // [B][Hkv][cap][Ng]
   __half* res[2];        // [B][Hkv][Nr][d]
@@ -43,6 +43,8 @@ struct PackArgs {
   int32_t* sink_len;
   uint32_t* err_word;
   int Hkv, d, Ng, row_bytes, cap, Nr, Ns, Lmax;
+  int ng_shift;            // log2(Ng)
+  int64_t sb, sh, st;      // element strides of the input: sequence, head, token
 };
 
 template <int BITS, bool HYB>
@@ -75,7 +77,7 @@ __global__ void __launch_bounds__(kPackThreads) quantize_pack_kernel(PackArgs a)
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int quad = lane & 3;
-  const __half* src = a.x[which] + (int64_t)bh * a.Lmax * a.d;
+  const __half* src = a.x[which] + (int64_t)b * a.sb + (int64_t)(bh % a.Hkv) * a.sh;
 
   uint4 raw[kPackUnroll];
   int64_t gi[kPackUnroll];
@@ -83,19 +85,19 @@ __global__ void __launch_bounds__(kPackThreads) quantize_pack_kernel(PackArgs a)
   for (int u = 0; u < kPackUnroll; ++u) {
     gi[u] = g0 + u * kGroupsPerIter + warp * 8 + (lane >> 2);
     raw[u] = make_uint4(0, 0, 0, 0);
-    if (gi[u] < groups_used)
-      raw[u] = __ldg(reinterpret_cast<const uint4*>(src + gi[u] * kGroup + quad * 8));
+    if (gi[u] < groups_used) {
+      const int64_t t = gi[u] >> a.ng_shift, g = gi[u] & (a.Ng - 1);
+      raw[u] = __ldg(reinterpret_cast<const uint4*>(src + t * a.st + g * kGroup + quad * 8));
+    }
   }
 
 #pragma unroll
   for (int u = 0; u < kPackUnroll; ++u) {
     const bool in_range = gi[u] < groups_used;
-    const int t = in_range ? (int)(gi[u] / a.Ng) : 0;
-    const int g = in_range ? (int)(gi[u] % a.Ng) : 0;
-    float x[8];
-    unpack8_f16(raw[u], x);
+    const int t = in_range ? (int)(gi[u] >> a.ng_shift) : 0;
+    const int g = in_range ? (int)(gi[u] & (a.Ng - 1)) : 0;
     uint32_t prm, asym = 1;
-    const uint32_t packed = quantize_quad<BITS>(x, prm, HYB, &asym);  // all lanes take part
+    const uint32_t packed = quantize_quad<BITS>(raw[u], prm, HYB, &asym);  // all lanes take part
     // the warp's 8 groups are whole token rows (Ng divides 8): each row's mode
     // byte comes from one ballot
     const uint32_t modes = HYB ? __ballot_sync(0xffffffffu, quad == 0 && asym) : 0u;
@@ -194,10 +196,8 @@ __global__ void __launch_bounds__(1024) append_kernel(AppendArgs a) {
     if (pack_now) {
       uint4 oldv = nv;
       if (a.Nr > 0 && active) oldv = *reinterpret_cast<const uint4*>(ring_row + lane * 8);
-      float x[8];
-      unpack8_f16(oldv, x);
       uint32_t prm, asym = 1;
-      const uint32_t packed = quantize_quad<BITS>(x, prm, HYB, &asym);
+      const uint32_t packed = quantize_quad<BITS>(oldv, prm, HYB, &asym);
       if (HYB) {
         const uint32_t modes = __ballot_sync(0xffffffffu, (lane & 3) == 0 && asym);
         const int64_t mrow = a.rm.row(b, h, pl);
@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(1024) append_kernel(AppendArgs a) {
 
 cudaError_t launch_quantize_pack(const Dims& s, const kvq_cache_view& v, const __half* k,
                                  const __half* vv, const int32_t* seq_lens, int Lmax,
-                                 cudaStream_t st) {
+                                 const int64_t strides[3], cudaStream_t st) {
   // With Lmax == 0 one CTA per (sequence, head) still runs to write the counters.
   const int64_t groups = (int64_t)(Lmax > 0 ? Lmax : 1) * s.Ng;
   dim3 grid((unsigned)((groups + kGroupsPerCta - 1) / kGroupsPerCta), (unsigned)(s.B * s.Hkv), 2);
@@ -261,6 +261,10 @@ cudaError_t launch_quantize_pack(const Dims& s, const kvq_cache_view& v, const _
   a.Nr = s.Nr;
   a.Ns = s.Ns;
   a.Lmax = Lmax;
+  a.ng_shift = __builtin_ctz((unsigned)s.Ng);
+  a.sb = strides[0];
+  a.sh = strides[1];
+  a.st = strides[2];
   if (s.bits == 4) {
     if (s.hybrid)
       quantize_pack_kernel<4, true><<<grid, kPackThreads, 0, st>>>(a);

@@ -41,10 +41,11 @@ KVQ_ARRAY_SINK = 3
 KVQ_ARRAY_MODE = 4
 
 # Every function the header declares (the tests check the library exports them).
-EXPORTS = ("kvq_cache_bytes", "kvq_decode_workspace_bytes", "kvq_quantize_pack", "kvq_append",
+EXPORTS = ("kvq_cache_bytes", "kvq_decode_workspace_bytes", "kvq_quantize_pack",
+           "kvq_quantize_pack_strided", "kvq_append",
            "kvq_decode_attention", "kvq_decode_step", "kvq_decode_step_host", "kvq_step_io_bytes",
            "kvq_decode_attention_noalloc",
-           "kvq_read_error", "kvq_status_string", "kvq_version")
+           "kvq_read_error", "kvq_status_string", "kvq_version", "kvq_testing_wait_fault")
 
 
 class CacheDesc(ctypes.Structure):
@@ -93,6 +94,9 @@ def load(path: str | None = None):
             lib.kvq_decode_workspace_bytes.restype = sz
             lib.kvq_quantize_pack.argtypes = [DP, VP, P, P, P, i32, P]
             lib.kvq_quantize_pack.restype = ctypes.c_int
+            i64 = ctypes.c_int64
+            lib.kvq_quantize_pack_strided.argtypes = [DP, VP, P, P, P, i32, i64, i64, i64, P]
+            lib.kvq_quantize_pack_strided.restype = ctypes.c_int
             lib.kvq_append.argtypes = [DP, VP, P, P, P]
             lib.kvq_append.restype = ctypes.c_int
             lib.kvq_decode_attention.argtypes = [DP, VP, P, i32, P, P, sz, ctypes.c_uint32, P]
@@ -111,6 +115,8 @@ def load(path: str | None = None):
             lib.kvq_status_string.restype = ctypes.c_char_p
             lib.kvq_version.argtypes = []
             lib.kvq_version.restype = i32
+            lib.kvq_testing_wait_fault.argtypes = [ctypes.c_uint32]
+            lib.kvq_testing_wait_fault.restype = None
             _lib = lib
     return _lib
 
@@ -258,6 +264,27 @@ def kvq_quantize_pack(cache: KVCache, k: torch.Tensor, v: torch.Tensor, seq_lens
     _check(st, "kvq_quantize_pack")
 
 
+def kvq_quantize_pack_strided(cache: KVCache, k: torch.Tensor, v: torch.Tensor,
+                              seq_lens: torch.Tensor, stream=None) -> None:
+    """Pack a prefill from any strided view: k, v fp16 of logical shape
+    [B][Hkv][Lmax][d] with head_dim contiguous (for example a permuted view of a
+    token-major [B][L][Hkv][d] tensor, or of the key/value columns of a fused
+    QKV projection output).  Nothing is copied: the library reads through the
+    strides."""
+    for t, name in ((k, "k"), (v, "v")):
+        if t.dtype != torch.float16 or not t.is_cuda or t.dim() != 4 or t.stride(3) != 1:
+            raise ValueError(f"{name} must be a float16 CUDA [B][Hkv][Lmax][d] view with d contiguous")
+    if k.shape != v.shape or k.stride() != v.stride():
+        raise ValueError("k and v must have the same shape and strides")
+    if seq_lens.dtype != torch.int32 or not seq_lens.is_cuda:
+        raise ValueError("seq_lens must be an int32 CUDA tensor")
+    st = load().kvq_quantize_pack_strided(ctypes.byref(cache.desc), ctypes.byref(cache.view),
+                                          _ptr(k), _ptr(v), _ptr(seq_lens), int(k.shape[2]),
+                                          int(k.stride(0)), int(k.stride(1)), int(k.stride(2)),
+                                          _stream(stream, k.device))
+    _check(st, "kvq_quantize_pack_strided")
+
+
 def kvq_append(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, stream=None) -> None:
     """Append one token per sequence; k_new, v_new fp16 [B][Hkv][d]."""
     _f16(k_new, "k_new"), _f16(v_new, "v_new")
@@ -373,3 +400,9 @@ def kvq_read_error(cache: KVCache, stream=None) -> tuple[int, int]:
 
 def kvq_version() -> int:
     return int(load().kvq_version())
+
+
+def kvq_testing_wait_fault(limit_us: int) -> None:
+    """Testing hook (see kvq.h): limit_us > 0 makes one bounded wait of the next
+    tensor-core decode calls run out after limit_us microseconds; 0 turns it off."""
+    load().kvq_testing_wait_fault(int(limit_us))

@@ -210,6 +210,26 @@ kvq_status kvq_quantize_pack(const kvq_cache_desc* desc, const kvq_cache_view* v
                              const void* k, const void* v, const int32_t* seq_lens,
                              int32_t Lmax, void* stream);
 
+/* kvq_quantize_pack reading K and V in the layout the prefill produced them, in
+ * the same single pass (the quantizer reads each group straight from the
+ * producer's memory; nothing is transposed or copied first).  Same rule,
+ * split, outputs, errors and asynchrony as kvq_quantize_pack; only the input
+ * addressing differs:
+ *   element j of head_dim of token t, KV head h, sequence b of k (and of v) is
+ *   k[b * stride_b + h * stride_h + t * stride_t + j]   (fp16, strides in elements),
+ *   read for t < seq_lens[b] <= Lmax.
+ * Head-major [B][Hkv][Lmax][d]: (Hkv*Lmax*d, Lmax*d, d) (kvq_quantize_pack).
+ * Token-major [B][L][Hkv][d]: (L*Hkv*d, d, Hkv*d).
+ * A fused QKV projection output [B][L][(Hq + 2*Hkv)*d] (queries, then keys, then
+ * values of each token): k = base + Hq*d, v = base + (Hq + Hkv)*d, strides
+ * (L*W, d, W) with W = (Hq + 2*Hkv)*d.
+ * The strides must be non-negative multiples of 8 (KVQ_ERR_MISALIGNED
+ * otherwise), k and v 16-byte aligned. */
+kvq_status kvq_quantize_pack_strided(const kvq_cache_desc* desc, const kvq_cache_view* view,
+                                     const void* k, const void* v, const int32_t* seq_lens,
+                                     int32_t Lmax, int64_t stride_b, int64_t stride_h,
+                                     int64_t stride_t, void* stream);
+
 /* Append one decode token per sequence (InnerQ page section 2.3, sliding recent
  * window).
  *   k_new, v_new  fp16 device [B][Hkv][d].
@@ -321,13 +341,15 @@ kvq_status kvq_decode_step_host(const kvq_cache_desc* desc, const kvq_cache_view
  * than that (kvq_decode_workspace_bytes(desc, num_q_heads) > the maximum) and
  * KVQ_ERR_INVALID_ARG for an invalid description or head count.  Allocates
  * nothing.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and clears the array once
- * (cudaMemset); make that first call before any stream capture.  All calls share
- * the array and it keeps the last call's contents (its counters back at zero).
- * A call whose cache shape or head count differs from the previous call's on
- * the device first clears the array's counters and accumulators
- * (cudaMemsetAsync on `stream`).  Calls whose kernels overlap on the GPU race:
- * keep them on one stream or order the streams. */
+ * (cudaGetSymbolAddress, with that device current); make that first call before
+ * any stream capture.  All calls share the array and it keeps the last call's
+ * contents (its counters back at zero).  The first call on a device, a call whose
+ * cache shape or head count differs from the previous call's there, and the
+ * first call after kvq_read_error reported KVQ_ERR_TIMEOUT first clear the
+ * array's counters and accumulators with cudaMemsetAsync on `stream`, so that
+ * clear is ordered before the decode on the caller's own stream.  Calls whose
+ * kernels overlap on the GPU race: keep them on one stream or order the
+ * streams. */
 kvq_status kvq_decode_attention_noalloc(const kvq_cache_desc* desc, const kvq_cache_view* view,
                                         const void* q, int32_t num_q_heads, void* out,
                                         uint32_t flags, void* stream);
@@ -340,7 +362,22 @@ kvq_status kvq_read_error(const kvq_cache_view* view, uint32_t* word_out, void* 
 const char* kvq_status_string(kvq_status status);
 
 /* Library version as 10000 * major + 100 * minor + patch. */
-int32_t kvq_version(void); /* 140: paged caches; 130: 3-bit; 120: hybrid; 110: sink, fp32 out */
+int32_t kvq_version(void); /* 150: timeout testing hook, cached tensor maps; 140: paged caches;
+                              130: 3-bit; 120: hybrid; 110: sink, fp32 out */
+
+/* Testing hook, for checking the bounded-wait error path without faulting the
+ * GPU (no passage of the pages corresponds to it).  With limit_us > 0, every
+ * later tensor-core decode call (kvq_decode_attention, kvq_decode_step with
+ * head_dim 128 and at most 4 query heads per KV head, and the calls built on
+ * them) arms the barrier of the first tile of split 0 of (sequence 0, KV head 0)
+ * for 16 bytes more than that tile's copies deliver, and gives every bounded
+ * wait a limit of limit_us microseconds instead of one second.  All copies still
+ * complete, so nothing is in flight when that CTA gives up: it sets
+ * KVQ_ERRBIT_TIMEOUT, contributes nothing to its head's output (which is then
+ * wrong for that head) and returns; the call's other results are unaffected.
+ * limit_us = 0 (the default) restores normal behaviour.  Process-wide; not for
+ * production use. */
+void kvq_testing_wait_fault(uint32_t limit_us);
 
 #ifdef __cplusplus
 }

@@ -1,6 +1,8 @@
 """GPU parity of quantize/pack and append: codes, fp16 scales, fp16 mins,
 residual ring and counters bit-exact with the oracle on the same seeded inputs."""
 
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -113,6 +115,90 @@ def test_pack_ragged_batch_workload_sampled():
     r = ref_cache(len(pick), w.num_kv_heads, w.head_dim, w.bits, cap, w.residual)
     assert oracle.quantize_pack(r, to_np(k[sub.to(DEV)]), to_np(v[sub.to(DEV)]), to_np(lens[sub])) == 0
     assert_cache_equal(g, r, batches=pick)
+
+
+def _token_major(k):
+    """[B][Hkv][L][d] -> a [B][L][Hkv][d] tensor, returned as its permuted
+    [B][Hkv][L][d] view (the layout a prefill's projection writes)."""
+    return k.permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
+
+
+def _qkv_views(k, v, hq, seed):
+    """K and V placed in a fused QKV projection output [B][L][(Hq + 2 Hkv) d]
+    (random queries first), returned as the [B][Hkv][L][d] views of its key and
+    value columns."""
+    B, H, L, d = k.shape
+    g = torch.Generator(device=k.device).manual_seed(seed)
+    qkv = torch.randn(B, L, hq + 2 * H, d, generator=g, device=k.device).to(torch.float16)
+    qkv[:, :, hq:hq + H] = k.permute(0, 2, 1, 3)
+    qkv[:, :, hq + H:] = v.permute(0, 2, 1, 3)
+    return qkv[:, :, hq:hq + H].permute(0, 2, 1, 3), qkv[:, :, hq + H:].permute(0, 2, 1, 3)
+
+
+@pytest.mark.parametrize("layout", ["token", "qkv"])
+@pytest.mark.parametrize("bits,d,sink,paged", [(4, 128, 0, 0), (2, 64, 5, 0), (3, 128, 0, 1),
+                                               (4, 256, 3, 1), (2, 32, 0, 0)])
+def test_pack_strided_layouts(layout, bits, d, sink, paged):
+    """kvq_quantize_pack_strided straight from a token-major prefill or from the
+    key/value columns of a fused QKV projection output: the same bytes as the
+    oracle's pack of the same values (ragged lengths, window, sink, paged)."""
+    rng = np.random.default_rng(bits * 100 + d + sink)
+    B, H, Lmax, Nr, hq = 3, 2, 211, 9, 8
+    k = _special_values(rng, (B, H, Lmax, d))
+    v = torch.from_numpy((rng.standard_normal((B, H, Lmax, d)) * 2).astype(np.float16))
+    lens = torch.tensor([211, 7, 160], dtype=torch.int32)
+    cap = 224
+    kd, vd = k.to(DEV), v.to(DEV)
+    if layout == "token":
+        ks, vs = _token_major(kd), _token_major(vd)
+    else:
+        ks, vs = _qkv_views(kd, vd, hq, 5)
+    assert not ks.is_contiguous()
+    g = gpu_cache(B, H, d, bits, cap, Nr, sink=sink, pages=B * cap // 32 + 3 if paged else 0,
+                  seed=bits)
+    kvq.kvq_quantize_pack_strided(g, ks, vs, lens.to(DEV))
+    st, word = kvq.kvq_read_error(g)
+    r = ref_cache(B, H, d, bits, cap, Nr, sink=sink)
+    err = oracle.quantize_pack(r, to_np(k), to_np(v), to_np(lens))
+    assert st == kvq.KVQ_OK and word == 0 and err == 0
+    assert_cache_equal(g, r)
+
+
+@pytest.mark.parametrize("layout", ["token", "qkv"])
+@pytest.mark.parametrize("bits,paged", [(4, 0), (2, 0), (4, 1)])
+def test_pack_strided_workload_full_size(layout, bits, paged):
+    """The pack workload (32768 tokens x 8 KV heads x d128, K with outlier
+    channels) packed from a token-major prefill or from the key/value columns
+    of a Llama-3.1-8B fused QKV projection output (32 query heads), into a
+    contiguous or a paged cache: every code, scale and min bit-exact."""
+    w = synth.scaled(synth.WORKLOADS[5], bits=bits)
+    k, v, lens = w.prefill(device=DEV)
+    if layout == "token":
+        ks, vs = _token_major(k), _token_major(v)
+    else:
+        ks, vs = _qkv_views(k, v, 32, 6)
+    cap = w.len_max
+    g = gpu_cache(w.batch, w.num_kv_heads, w.head_dim, bits, cap, 0,
+                  pages=cap // 32 + 16 if paged else 0, seed=7)
+    kvq.kvq_quantize_pack_strided(g, ks, vs, lens.to(DEV))
+    assert kvq.kvq_read_error(g)[0] == kvq.KVQ_OK
+    del ks, vs
+    r = ref_cache(w.batch, w.num_kv_heads, w.head_dim, bits, cap, 0)
+    assert oracle.quantize_pack(r, to_np(k), to_np(v), to_np(lens)) == 0
+    assert_cache_equal(g, r)
+
+
+def test_pack_strided_rejects_bad_strides():
+    g = gpu_cache(1, 2, 64, 4, 32, 0)
+    k = torch.zeros(1, 2, 16, 64, dtype=torch.float16, device=DEV)
+    lib = kvq.load()
+    args = lambda sb, sh, st: (ctypes.byref(g.desc), ctypes.byref(g.view), kvq._ptr(k), kvq._ptr(k),
+                               kvq._ptr(g.packed_len), 16, sb, sh, st, None)
+    assert lib.kvq_quantize_pack_strided(*args(2048, 1024, 64)) == kvq.KVQ_OK
+    assert lib.kvq_quantize_pack_strided(*args(2048, 1024, 63)) == kvq.KVQ_ERR_MISALIGNED
+    assert lib.kvq_quantize_pack_strided(*args(2048, 1028, 64)) == kvq.KVQ_ERR_MISALIGNED
+    assert lib.kvq_quantize_pack_strided(*args(-8, 1024, 64)) == kvq.KVQ_ERR_INVALID_ARG
+    torch.cuda.synchronize()
 
 
 @pytest.mark.parametrize("bits,Nr,d", [(4, 8, 64), (2, 5, 128), (4, 0, 32), (4, 128, 128)])

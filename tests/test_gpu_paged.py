@@ -90,9 +90,27 @@ def test_paged_steps(fused, bits, Nr, hybrid):
     assert_cache_equal(g, r)
 
 
+def _without_packed_rows(r, b, lo, hi):
+    """Sequence b of oracle cache r with packed tokens [lo, hi) left out (a
+    one-sequence cache; attention does not depend on token order)."""
+    B, H, d, bits, cap, Nr, S, hyb = r.shape
+    o = oracle.Cache(1, H, d, bits, cap, Nr, S, hyb)
+    n = int(r.packed_len[b])
+    keep = np.r_[0:lo, hi:n]
+    for name in ("k_codes", "v_codes", "k_params", "v_params"):
+        getattr(o, name)[0, :, :len(keep)] = getattr(r, name)[b][:, keep]
+    for name in ("k_res", "v_res", "k_sink", "v_sink"):
+        getattr(o, name)[0] = getattr(r, name)[b]
+    o.packed_len[0] = len(keep)
+    o.res_len[0], o.res_head[0], o.sink_len[0] = r.res_len[b], r.res_head[b], r.sink_len[b]
+    return o
+
+
 def test_paged_bad_page_is_flagged_and_skipped():
     """A block-table entry outside the pool: pack flags it and writes nothing
-    there; decode (both kernels) flags it.  The other sequence is unaffected."""
+    there; decode (both kernels) flags it and leaves that page's tokens out, so
+    sequence 0's output is the attention over its other tokens and sequence 1
+    is unaffected."""
     rng = np.random.default_rng(11)
     B, H, d, cap, Nr = 2, 2, 128, 256, 8
     lens = [200 + Nr, 100 + Nr]
@@ -105,12 +123,47 @@ def test_paged_bad_page_is_flagged_and_skipped():
     assert word == kvq.KVQ_ERRBIT_BADPAGE
     r = ref_cache(B, H, d, 4, cap, Nr)
     oracle.quantize_pack(r, k.numpy(), v.numpy(), np.array(lens, np.int32))
+    r0 = _without_packed_rows(r, 0, 64, 96)
     for gq in (4, 8):  # tensor-core and generic kernels
         q = torch.from_numpy(rng.standard_normal((B, H * gq, d)).astype(np.float16))
         out = kvq.kvq_decode_attention(g, q.to(DEV))
         st, word = kvq.kvq_read_error(g)
         assert word & kvq.KVQ_ERRBIT_BADPAGE
+        assert torch.isfinite(out).all()
         assert_attn_close(out[1:], oracle.decode(r, q.numpy())[1:])
+        assert_attn_close(out[:1], oracle.decode(r0, q.numpy()[:1]))
+
+
+def test_paged_step_into_bad_page_matches_append_then_decode():
+    """A fused step whose packed token lands in a page outside the pool writes
+    nothing there, flags it and leaves that token out of the attention, exactly
+    as kvq_append followed by kvq_decode_attention does."""
+    rng = np.random.default_rng(12)
+    B, H, d, cap, Nr, gq = 1, 2, 128, 128, 16, 4
+    L = 64 + Nr  # 64 packed tokens: the next packed token opens page 2
+    k = torch.from_numpy(rng.standard_normal((B, H, L, d)).astype(np.float16)).to(DEV)
+    v = torch.from_numpy(rng.standard_normal((B, H, L, d)).astype(np.float16)).to(DEV)
+    outs = []
+    for fused in (True, False):
+        g = gpu_cache(B, H, d, 4, cap, Nr, pages=8, seed=5)
+        g.block_table[0, 2] = -1
+        kvq.kvq_quantize_pack(g, k, v, torch.tensor([L], dtype=torch.int32, device=DEV))
+        assert kvq.kvq_read_error(g)[0] == kvq.KVQ_OK
+        rs = np.random.default_rng(13)
+        kn = torch.from_numpy(rs.standard_normal((B, H, d)).astype(np.float16)).to(DEV)
+        vn = torch.from_numpy(rs.standard_normal((B, H, d)).astype(np.float16)).to(DEV)
+        q = torch.from_numpy(rs.standard_normal((B, H * gq, d)).astype(np.float16)).to(DEV)
+        if fused:
+            out = kvq.kvq_decode_step(g, q, kn, vn, flags=kvq.KVQ_OUT_F32)
+        else:
+            kvq.kvq_append(g, kn, vn)
+            out = kvq.kvq_decode_attention(g, q, flags=kvq.KVQ_OUT_F32)
+        st, word = kvq.kvq_read_error(g)
+        assert word == kvq.KVQ_ERRBIT_BADPAGE
+        assert g.counters[:3, 0].tolist() == [65, Nr, 1]
+        outs.append(out)
+    assert torch.isfinite(outs[0]).all()
+    assert (outs[0] - outs[1]).abs().max().item() <= 1e-3
 
 
 def test_paged_workload_full_size():

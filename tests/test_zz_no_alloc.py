@@ -87,3 +87,37 @@ def test_noalloc_alternating_shapes():
             assert diff <= 2e-3, (rnd, B, hq, d, diff)
     for c, _ in caches:
         assert kvq.kvq_read_error(c)[0] == kvq.KVQ_OK
+
+
+def test_noalloc_after_a_timeout_on_a_side_stream():
+    """After a call whose bounded wait ran out (the library's testing hook makes
+    one run out without faulting the GPU), kvq_read_error reports the timeout and
+    the next call clears the array's counters first.  That call and the ones
+    after it run on a side stream (a non-blocking torch stream): the clear is
+    enqueued on the caller's stream, so it is ordered before the decode there."""
+    rng = np.random.default_rng(91)
+    B, H, gq, d, L = 2, 4, 4, 128, 2600
+    c = kvq.KVCache(B, H, d, 4, L, 32, device=DEV)
+    k = torch.from_numpy(rng.standard_normal((B, H, L, d)).astype(np.float16)).to(DEV)
+    v = torch.from_numpy(rng.standard_normal((B, H, L, d)).astype(np.float16)).to(DEV)
+    kvq.kvq_quantize_pack(c, k, v, torch.full((B,), L, dtype=torch.int32, device=DEV))
+    q = torch.from_numpy(rng.standard_normal((B, H * gq, d)).astype(np.float16)).to(DEV)
+    got = torch.empty_like(q)
+    kvq.kvq_testing_wait_fault(1000)
+    try:
+        assert _decode_noalloc_abi(c, q, got) == kvq.KVQ_OK
+        st, word = kvq.kvq_read_error(c)
+    finally:
+        kvq.kvq_testing_wait_fault(0)
+    assert st == kvq.KVQ_ERR_TIMEOUT
+    want = kvq.kvq_decode_attention(c, q)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    for _ in range(2):
+        with torch.cuda.stream(side):
+            got = torch.full_like(q, float("nan"))
+            assert _decode_noalloc_abi(c, q, got) == kvq.KVQ_OK
+        side.synchronize()
+        diff = (got.float() - want.float()).abs().max().item()
+        assert diff <= 2e-3, diff
+    assert kvq.kvq_read_error(c)[0] == kvq.KVQ_OK
