@@ -8,12 +8,17 @@ append of the step's new K/V token (the residual window is full, so its oldest
 token is quantized and packed) and decode attention of the step's 32 query
 heads over the updated cache -- one kernel launch on the tensor-core path.
 
-Timing: the steps are captured in a CUDA graph and replayed; the step rotates
-over copies of the cache whose total size is at least 3x the L2 cache, so the
-packed cache streams from HBM.  value = packed code + scale bytes per step
-(K and V, all heads, the tokens the decode reads) / step time.  The roofline is
-that of the step kernel; kvq_decode_attention alone is timed the same way in a
-decode-only graph and reported beside it.
+Timing: W warm-up steps, then R >= 10 timed regions of exactly K steps each;
+a region is one replay of a CUDA graph of K consecutive steps between CUDA
+events (synchronize, and a barrier for N > 1, on both sides), and the median
+region gives the step time.  Step i runs on cache copy i % n; the copies total
+at least 3x the L2 cache, so the packed cache streams from HBM.  value = packed
+code + scale bytes per step (K and V, all heads, the tokens the decode reads) /
+step time.  The roofline is that of the step kernel; kvq_decode_attention alone
+is timed the same way and reported beside it.  By default the line also carries
+the 128K INT2 layer, the batched Llama-2-13B layer and the standalone
+quantize/pack case under "workloads", each timed the same way with its own
+roofline and clock record.
 
 Output: one JSON line (see --help).  --impl reference times the CPU oracle
 (the plain fp64 implementation) on a bounded sample of the same workload.
@@ -205,11 +210,11 @@ def workload_config(w, packed_tokens, extra=None):
     return cfg
 
 
-def build_state(dev, steps, warmup, e2e_steps, l2_bytes, workload, sink=0, hybrid=0, bits=0,
-                paged=0):
+def build_state(dev, appends_per_copy, l2_bytes, workload, sink=0, hybrid=0, bits=0, paged=0):
     """Pack the workload once, clone it into enough copies to exceed 3x L2,
-    and pre-generate the per-step queries and new tokens on the device."""
-    from bit_quantized_kv_pack_gb300 import kvq, synth
+    and pre-generate the per-step queries and new tokens on the device.
+    `appends_per_copy(ncopy)` is how many fused steps each copy will take."""
+    from bit_quantized_kv_pack_gb300 import kvq
 
     w = workload_for(workload, bits)
     k, v, lens = w.prefill(device=dev)
@@ -219,10 +224,7 @@ def build_state(dev, steps, warmup, e2e_steps, l2_bytes, workload, sink=0, hybri
     step_bytes0 = npk0 * w.num_kv_heads * per_tok
     res_bytes = w.batch * w.num_kv_heads * (w.residual + sink) * w.head_dim * 2 * 2
     ncopy = max(2, math.ceil(3 * l2_bytes / (step_bytes0 + res_bytes)))
-    # appends each copy sees: warm-up and timed graph passes, then the e2e loop
-    appends = (math.ceil(warmup / ncopy) + math.ceil(steps / ncopy)
-               + math.ceil((ncopy + max(ncopy, e2e_steps)) / ncopy) + 2)
-    cap = max(npk_b) + appends + 8
+    cap = max(npk_b) + appends_per_copy(ncopy) + 8
     paging = {}
     if paged:  # 32-token pages, each copy's block table a seeded shuffle of its pool
         cap = (cap + 31) // 32 * 32
@@ -246,164 +248,193 @@ def build_state(dev, steps, warmup, e2e_steps, l2_bytes, workload, sink=0, hybri
                      "v_sink", "k_mode", "v_mode", "block_table", "counters"):
             getattr(c, name).copy_(getattr(base, name))
         copies.append(c)
-    nslot = ncopy  # one graph = one pass over the copies
-    q = torch.stack([w.query(s, device=dev) for s in range(nslot)])
-    kn, vn = zip(*[w.new_tokens(s, device=dev) for s in range(nslot)])
+    q = torch.stack([w.query(s, device=dev) for s in range(ncopy)])
+    kn, vn = zip(*[w.new_tokens(s, device=dev) for s in range(ncopy)])
     kn, vn = torch.stack(kn), torch.stack(vn)
     out = torch.empty_like(q)
     ws = kvq.workspace_for(base, w.num_q_heads)
     return dict(w=w, copies=copies, q=q, kn=kn, vn=vn, out=out, ws=ws, npk0=npk0,
-                per_tok=per_tok, nslot=nslot)
+                per_tok=per_tok, nslot=ncopy, step_bytes=step_bytes0)
 
 
-def capture(state, with_append=True, with_decode=True, ncopies=None):
-    """A graph of one step on each of the first `ncopies` cache copies."""
+def capture(state, nsteps, fused=True):
+    """A graph of `nsteps` consecutive steps, step i on cache copy i % ncopy:
+    fused steps (append + attention, one kvq_decode_step each) or decode-only
+    launches (kvq_decode_attention)."""
     from bit_quantized_kv_pack_gb300 import kvq
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
-    n = len(state["copies"]) if ncopies is None else ncopies
+    n = state["nslot"]
     with torch.cuda.stream(s):
         with torch.cuda.graph(g, stream=s):
-            for i, c in enumerate(state["copies"][:n]):
-                if with_append and with_decode:  # one fused launch: append, then attend
+            for i in range(nsteps):
+                j = i % n
+                c = state["copies"][j]
+                if fused:
                     # consecutive steps use different cache copies, so the kernel
                     # before each step never writes its cache
-                    kvq.kvq_decode_step(c, state["q"][i], state["kn"][i], state["vn"][i],
-                                        state["out"][i], state["ws"],
+                    kvq.kvq_decode_step(c, state["q"][j], state["kn"][j], state["vn"][j],
+                                        state["out"][j], state["ws"],
                                         flags=kvq.KVQ_STEP_EARLY_CACHE_READ)
-                elif with_append:
-                    kvq.kvq_append(c, state["kn"][i], state["vn"][i])
                 else:
-                    kvq.kvq_decode_attention(c, state["q"][i], state["out"][i], state["ws"])
+                    kvq.kvq_decode_attention(c, state["q"][j], state["out"][j], state["ws"])
     torch.cuda.current_stream().wait_stream(s)
     return g
 
 
-def time_graph(g, reps, g_rem=None):
-    """ms for `reps` replays of g plus one of g_rem, bracketed by CUDA events on
-    the current stream (graphs replay on it)."""
+def time_region(g, world=1):
+    """ms of one replay of g (exactly its steps), bracketed by CUDA events on the
+    stream the graph replays on, with a synchronize (and, for N > 1, a barrier)
+    on both sides."""
     torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
-    for _ in range(reps):
-        g.replay()
-    if g_rem is not None:
-        g_rem.replay()
+    g.replay()
     b.record()
     b.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
     return a.elapsed_time(b)
 
 
+def regions_for(args):
+    """Timed regions per measurement (the median of them is reported)."""
+    return max(10, args.regions)
+
+
+def run_decode_workload(args, workload, dev, l2, local, world, sink=0, hybrid=0, bits=0, paged=0):
+    """One decode workload: W warm-up steps, then R timed regions of exactly K
+    fused steps each (median reported), the decode-only launches timed the same
+    way, and the end-to-end steps through the host-buffer entry point."""
+    K, W, R = args.steps, args.warmup, regions_for(args)
+    e2e_steps = args.e2e_steps
+
+    def appends(ncopy):  # fused steps each copy takes: warm-up, regions, e2e
+        return (math.ceil(W / ncopy) + R * math.ceil(K / ncopy) + 2 * math.ceil(e2e_steps / ncopy)
+                + 2)
+
+    st = build_state(dev, appends, l2, workload, sink, hybrid, bits, paged)
+    w, ncopy = st["w"], st["nslot"]
+    g_step = capture(st, K, True)
+    g_dec = capture(st, K, False)
+    g_warm = capture(st, W, True)
+    g_warm.replay()  # exactly W warm-up steps
+    g_dec.replay()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_step = [time_region(g_step, world) for _ in range(R)]
+        t_dec = [time_region(g_dec, world) for _ in range(R)]
+        # keep the same kernels running long enough for several clock samples
+        # (decode only: appends would grow the caches)
+        t_end = time.time() + 0.6
+        while time.time() < t_end:
+            t_dec.append(time_region(g_dec))
+    torch.cuda.synchronize()
+    ms_step = statistics.median(t_step) / K
+    ms_dec = statistics.median(t_dec) / K
+    step_bytes = st["step_bytes"]
+    peak, peak_kind = measured_peak()
+    res_bytes = w.batch * w.num_kv_heads * (w.residual + sink) * w.head_dim * 2 * 2
+    qo_bytes = 2 * w.batch * w.num_q_heads * w.head_dim * 2
+    fused = w.head_dim == 128 and 1 <= w.num_q_heads // w.num_kv_heads <= 4
+    options = bool(sink or hybrid or bits or paged)
+    if fused:  # the dominant kernel is the step kernel itself (one launch per step)
+        rf_kernel, rf_us = "decode_step (append + split-KV decode + combine, one launch)", ms_step * 1e3
+    else:
+        rf_kernel, rf_us = "decode (split-KV + combine)", ms_dec * 1e3
+    achieved = step_bytes / (rf_us * 1e-6) / 1e9
+    e2e = run_e2e(st, e2e_steps)
+    return {
+        "workload": w.name,
+        "us_per_step": round(ms_step * 1e3, 3),
+        "ms_per_step": round(ms_step, 6),
+        "value": round(step_bytes / (ms_step * 1e-3) / 1e9, 2),
+        "unit": "GB/s",
+        "regions": {"count": R, "steps_each": K,
+                    "us_per_step_min": round(min(t_step) / K * 1e3, 3),
+                    "us_per_step_max": round(max(t_step) / K * 1e3, 3)},
+        "all_bytes_gbs": round((step_bytes + res_bytes + qo_bytes) / (ms_step * 1e-3) / 1e9, 2),
+        "gpu_launches": (1 if fused else 2) * K,
+        "roofline": {"bound": "hbm", "kernel": rf_kernel,
+                     "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": None if options else profiled_traffic(w.name, fused),
+                     "algorithmic_bytes_per_launch": step_bytes,
+                     "us_per_launch": round(rf_us, 3)},
+        "decode_only": {"us_per_launch": round(ms_dec * 1e3, 3),
+                        "achieved": round(step_bytes / (ms_dec * 1e-3) / 1e9, 2),
+                        "frac": round(step_bytes / (ms_dec * 1e-3) / 1e9 / peak, 4),
+                        "how": "kvq_decode_attention alone, same copies, median of the same regions"},
+        "e2e": e2e,
+        "clocks": clk.summary(),
+        "config": workload_config(w, st["npk0"], {
+            "l2": f"rotating {ncopy} cache copies ({ncopy * step_bytes / 2**20:.0f} MiB "
+                  f"packed) > 3x L2 ({l2 / 2**20:.0f} MiB)",
+            "timing": f"median of {R} regions, each one CUDA graph replay of exactly {K} steps "
+                      f"between CUDA events", "parallelism": "replicas",
+            **({"sink": sink} if sink else {}),
+            **({"hybrid": "sym/asym per group, mode bytes"} if hybrid else {}),
+            **({"paged": "32-token pages, shuffled block tables"} if paged else {})}),
+        "_state": st,
+    }
+
+
 def run_ours(args, rank, world, local):
-    from bit_quantized_kv_pack_gb300 import _build, kvq
+    from bit_quantized_kv_pack_gb300 import _build
     _build.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
+    head = run_decode_workload(args, args.workload, dev, l2, local, world, args.sink, args.hybrid,
+                               args.bits, args.paged)
+    head.pop("_state")
+    extra = {}
+    if args.extra_workloads and not (args.sink or args.hybrid or args.bits or args.paged):
+        for wl in (3, 4):
+            if wl != args.workload:
+                r = run_decode_workload(args, wl, dev, l2, local, world)
+                r.pop("_state")
+                torch.cuda.empty_cache()
+                extra[r["workload"]] = r
+        pk = run_pack(args, rank, world, local, with_cpu=False)
+        extra[pk["config"]["workload"]] = pk
 
-    st = build_state(dev, args.steps, args.warmup, args.e2e_steps, l2, args.workload, args.sink,
-                     args.hybrid, args.bits, args.paged)
-    w, ncopy = st["w"], st["nslot"]
-    K = args.steps
-    reps, rem = divmod(K, ncopy)  # K steps = reps whole passes over the copies + rem
-    wreps = math.ceil(args.warmup / ncopy)
-
-    g_step = capture(st, True, True)
-    g_dec = capture(st, False, True)
-    g_step_rem = capture(st, True, True, rem) if rem else None
-    g_dec_rem = capture(st, False, True, rem) if rem else None
-    for _ in range(wreps):
-        g_step.replay()
-        g_dec.replay()
-    torch.cuda.synchronize()
-
+    ms_step = head["ms_per_step"]
+    step_bytes = head["roofline"]["algorithmic_bytes_per_launch"]
+    e2e = head["e2e"]
     if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        ms = time_graph(g_step, reps, g_step_rem)
-        ms_dec = time_graph(g_dec, reps, g_dec_rem)
-        # keep the same kernels running long enough for several clock samples
-        # (decode only: appends would grow the caches)
-        t_end = time.time() + 0.8
-        while time.time() < t_end:
-            time_graph(g_dec, max(reps, 1))
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-
-    # packed bytes the decode reads per step: the prefill's packed tokens (each
-    # append adds one more token per sequence and copy, < 0.1% over the run, not counted)
-    step_bytes = st["npk0"] * w.num_kv_heads * st["per_tok"]
-    ms_per_step = ms / K
-    value = step_bytes / (ms_per_step * 1e-3) / 1e9
-
-    dec_ms_per_launch = ms_dec / K
-    peak, peak_kind = measured_peak()
-    # every byte a step moves: packed codes + params, the fp16 window and sink, q and O
-    res_bytes = w.batch * w.num_kv_heads * (w.residual + args.sink) * w.head_dim * 2 * 2
-    qo_bytes = 2 * w.batch * w.num_q_heads * w.head_dim * 2
-    all_bytes_gbs = (step_bytes + res_bytes + qo_bytes) / (ms_per_step * 1e-3) / 1e9
-    # the step is one fused launch on the tensor-core path (append + decode),
-    # else an append and a decode launch
-    fused = w.head_dim == 128 and 1 <= w.num_q_heads // w.num_kv_heads <= 4
-    launches = 1 if fused else 2
-    if fused:  # the dominant kernel is the step kernel itself
-        rf_kernel, rf_us = "decode_step (append + split-KV decode + combine, one launch)", ms_per_step * 1e3
+        ms_all, value_all, e2e["value"] = reduce_across_ranks(ms_step, e2e["value"], step_bytes, dev)
     else:
-        rf_kernel, rf_us = "decode (split-KV + combine)", dec_ms_per_launch * 1e3
-    achieved = step_bytes / (rf_us * 1e-6) / 1e9
-    dec_achieved = step_bytes / (dec_ms_per_launch * 1e-3) / 1e9
-
-    # end to end through the public binding: pinned host inputs -> device,
-    # the step call, output -> pinned host, eager calls (no graph)
-    e2e = run_e2e(st, args)
-
-    clocks = clk.summary()
-    if world > 1:
-        ms_step_all, value_all, e2e["value"] = reduce_across_ranks(ms_per_step, e2e["value"],
-                                                                   step_bytes, dev)
-    else:
-        ms_step_all, value_all = ms_per_step, value
-
+        ms_all, value_all = ms_step, head["value"]
     res = {
         "metric": "quantized-KV decode attention: achieved HBM GB/s (% of peak), us/step",
         "value": round(value_all, 2),
         "unit": "GB/s",
         "n_gpus": world,
-        "steps": K,
-        "warmup": wreps * ncopy,
-        "ms_per_step": round(ms_step_all, 6),
-        "us_per_step": round(ms_step_all * 1e3, 3),
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_all, 6),
+        "us_per_step": round(ms_all * 1e3, 3),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": f"u{w.bits} codes, fp16 scale/min, fp32 accumulate",
+        "dtype": f"u{head['config']['bits']} codes, fp16 scale/min, fp32 accumulate",
         "data": "synthetic (seeded SplitMix64 + Box-Muller, fp16)",
-        "config": workload_config(w, st["npk0"], {
-            "l2": f"rotating {ncopy} cache copies ({ncopy * step_bytes / 2**20:.0f} MiB "
-                  f"packed) > 3x L2 ({l2 / 2**20:.0f} MiB)",
-            "timing": "CUDA graph replays, CUDA events", "parallelism": "replicas",
-            **({"sink": args.sink} if args.sink else {}),
-            **({"hybrid": "sym/asym per group, mode bytes"} if args.hybrid else {}),
-            **({"paged": "32-token pages, shuffled block tables"} if args.paged else {})}),
-        "all_bytes_gbs": round(all_bytes_gbs, 2),
-        "gpu_launches": launches * K,
-        "roofline": {"bound": "hbm", "kernel": rf_kernel,
-                     "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": (profiled_traffic(w.name, fused)
-                                 if not (args.sink or args.hybrid or args.bits or args.paged) else None),
-                     "algorithmic_bytes_per_launch": step_bytes,
-                     "us_per_launch": round(rf_us, 3)},
-        "decode_only": {"us_per_launch": round(dec_ms_per_launch * 1e3, 3),
-                        "achieved": round(dec_achieved, 2), "frac": round(dec_achieved / peak, 4),
-                        "how": "kvq_decode_attention alone, same copies, same timing"},
+        "config": head["config"],
+        "regions": head["regions"],
+        "all_bytes_gbs": head["all_bytes_gbs"],
+        "gpu_launches": head["gpu_launches"],
+        "roofline": head["roofline"],
+        "decode_only": head["decode_only"],
         "e2e": e2e,
-        "clocks": clocks,
+        "clocks": head["clocks"],
     }
+    if extra:
+        res["workloads"] = extra
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args.cpu_seconds, workload=args.workload, sink=args.sink,
                                            bits=args.bits, hybrid=args.hybrid)
@@ -413,7 +444,7 @@ def run_ours(args, rank, world, local):
     return res
 
 
-def run_e2e(st, args):
+def run_e2e(st, nsteps):
     """The same steps end to end through the library's host-buffer entry point:
     per step one kvq_decode_step_host call enqueues the copy of the pinned input
     block [q | k_new | v_new] to the device, the fused step and the copy of out
@@ -426,7 +457,7 @@ def run_e2e(st, args):
     in_h = ins.cpu().pin_memory()
     out_h = torch.empty_like(st["q"], device="cpu").pin_memory()
     dev_io = kvq.step_io_for(st["copies"][0], hq)
-    K = max(n, args.e2e_steps)
+    K = max(n, nsteps)
 
     def step(i):
         j = i % n
@@ -443,7 +474,7 @@ def run_e2e(st, args):
     b.record()
     b.synchronize()
     ms = a.elapsed_time(b) / K
-    step_bytes = st["npk0"] * w.num_kv_heads * st["per_tok"]
+    step_bytes = st["step_bytes"]
     return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "us_per_step": round(ms * 1e3, 3),
             "h2d_bytes_per_step": int(in_h[0].numel() * in_h.element_size()),
@@ -617,67 +648,111 @@ def run_reference(args, rank, world):
     }
 
 
-def run_pack(args, rank, world, local):
+PACK_SOURCES = ("kvq_quant.cu", "kvq_internal.cuh")
+
+
+def pack_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_quantized_kv_pack_gb300", "csrc")
+    for n in PACK_SOURCES:
+        p = os.path.join(csrc, n)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_pack_traffic(workload_name: str):
+    """DRAM bytes per launch of the INT4 pack from its committed ncu summary, if
+    taken on the current pack sources (else None)."""
+    p = os.path.join(ROOT, "profiles", f"quantize_pack_{workload_name}.md")
+    if not os.path.exists(p):
+        return None
+    src_hash, traffic = None, None
+    for line in open(p):
+        if line.startswith("source_hash:"):
+            src_hash = line.split(":", 1)[1].strip()
+        if line.startswith("traffic_bytes_per_launch:"):
+            traffic = float(line.split(":", 1)[1].strip())
+    return traffic if src_hash == pack_source_hash() else None
+
+
+def run_pack(args, rank, world, local, with_cpu=True):
     """Standalone quantize/pack: fp16 K and V of 32768 tokens x 8 KV heads x d128
     (4 outlier channels x10 in K) packed to INT4 and to INT2, all tokens packed
     (no window).  Two input copies alternate so the 134 MB input is not served
-    from L2 (129 MB) between packs; each pack is timed with CUDA events around K
-    launches after W warm-ups.  value = input bytes / time (INT4)."""
+    from L2 (129 MB) between packs.  Each timed region is exactly K launches
+    (after W warm-ups) between CUDA events; the median of R regions is reported.
+    value = input bytes / time (INT4); the roofline counts input + output bytes."""
     from bit_quantized_kv_pack_gb300 import _build, kvq, synth
     _build.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peak, peak_kind = measured_peak()
+    K, R = args.steps, regions_for(args)
     out = {}
-    for bits in (4, 2):
-        w = synth.scaled(synth.WORKLOADS[5], bits=bits)
-        ins = []
-        for _ in range(2):
-            k, v, lens = w.prefill(device=dev)
-            ins.append((k, v, lens.to(dev)))
-        in_bytes = 2 * ins[0][0].numel() * 2
-        cache = kvq.KVCache(w.batch, w.num_kv_heads, w.head_dim, bits, w.len_max, 0, device=dev,
-                            hybrid=args.hybrid)
-        out_bytes = sum(cache.k_codes.numel() + cache.k_params.numel() * 4 + cache.k_mode.numel()
-                        for _ in range(2))
-        for i in range(args.warmup):
-            k, v, lens = ins[i % 2]
-            kvq.kvq_quantize_pack(cache, k, v, lens)
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for i in range(args.steps):
-            k, v, lens = ins[i % 2]
-            kvq.kvq_quantize_pack(cache, k, v, lens)
-        b.record()
-        b.synchronize()
-        st, _ = kvq.kvq_read_error(cache)
-        if st != kvq.KVQ_OK:
-            raise RuntimeError(f"pack failed: {kvq.status_string(st)}")
-        us = a.elapsed_time(b) * 1e3 / args.steps
-        out[bits] = dict(us=us, gbs=in_bytes / (us * 1e-6) / 1e9,
-                         traffic_gbs=(in_bytes + out_bytes) / (us * 1e-6) / 1e9)
+    with ClockSampler(local) as clk:
+        for bits in (4, 2):
+            w = synth.scaled(synth.WORKLOADS[5], bits=bits)
+            ins = []
+            for _ in range(2):
+                k, v, lens = w.prefill(device=dev)
+                ins.append((k, v, lens.to(dev)))
+            in_bytes = 2 * ins[0][0].numel() * 2
+            cache = kvq.KVCache(w.batch, w.num_kv_heads, w.head_dim, bits, w.len_max, 0, device=dev,
+                                hybrid=args.hybrid)
+            out_bytes = sum(cache.k_codes.numel() + cache.k_params.numel() * 4 + cache.k_mode.numel()
+                            for _ in range(2))
+            for i in range(args.warmup):
+                k, v, lens = ins[i % 2]
+                kvq.kvq_quantize_pack(cache, k, v, lens)
+            ts = []
+            for _ in range(R):
+                torch.cuda.synchronize()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                for i in range(K):
+                    k, v, lens = ins[i % 2]
+                    kvq.kvq_quantize_pack(cache, k, v, lens)
+                b.record()
+                b.synchronize()
+                ts.append(a.elapsed_time(b) * 1e3 / K)
+            st, _ = kvq.kvq_read_error(cache)
+            if st != kvq.KVQ_OK:
+                raise RuntimeError(f"pack failed: {kvq.status_string(st)}")
+            us = statistics.median(ts)
+            out[bits] = dict(us=us, gbs=in_bytes / (us * 1e-6) / 1e9,
+                             traffic_gbs=(in_bytes + out_bytes) / (us * 1e-6) / 1e9,
+                             algo=in_bytes + out_bytes)
+            del ins, cache
+            torch.cuda.empty_cache()
+    name = "pack-32768x8x128-kv"
     res = {
         "metric": "quantize/pack throughput: input GB/s (fp16 K+V in, codes + scale/min out)",
-        "value": round(out[4]["gbs"], 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "value": round(out[4]["gbs"], 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(out[4]["us"] * 1e-3, 6),
+        "us_per_step": round(out[4]["us"], 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp16 in, u4/u2 codes + fp16 scale/min out, fp32 arithmetic",
         "data": "synthetic (seeded SplitMix64 + Box-Muller, fp16)",
-        "config": {"workload": "pack-32768x8x128-kv", "tokens": 32768, "num_kv_heads": 8,
+        "config": {"workload": name, "tokens": 32768, "num_kv_heads": 8,
                    "head_dim": 128, "group": 32, "l2": "two input copies alternate",
-                   "timing": "CUDA events around K launches",
+                   "timing": f"median of {R} regions of exactly {K} launches between CUDA events",
                    **({"hybrid": "sym/asym per group, mode bytes"} if args.hybrid else {})},
-        "int2": {"us_per_step": round(out[2]["us"], 3), "value": round(out[2]["gbs"], 2)},
-        "gpu_launches": args.steps,
+        "int2": {"us_per_step": round(out[2]["us"], 3), "value": round(out[2]["gbs"], 2),
+                 "frac": round(out[2]["traffic_gbs"] / peak, 4)},
+        "gpu_launches": K,
         "roofline": {"bound": "hbm", "kernel": "quantize_pack (INT4)",
                      "achieved": round(out[4]["traffic_gbs"], 2), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(out[4]["traffic_gbs"] / peak, 4), "traffic": None,
+                     "frac": round(out[4]["traffic_gbs"] / peak, 4),
+                     "traffic": None if args.hybrid else profiled_pack_traffic(name),
+                     "algorithmic_bytes_per_launch": out[4]["algo"],
                      "us_per_launch": round(out[4]["us"], 3),
                      "note": "achieved counts input + output bytes"},
+        "clocks": clk.summary(),
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if with_cpu and rank == 0 and not args.no_cpu_baseline:
         import oracle
         w = synth.scaled(synth.WORKLOADS[5], bits=4)
         k, v, lens = w.prefill()
@@ -697,12 +772,17 @@ def run_pack(args, rank, world, local):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20, help="steps per timed region (K)")
+    ap.add_argument("--warmup", type=int, default=5, help="untimed warm-up steps (W >= 3)")
+    ap.add_argument("--regions", type=int, default=15,
+                    help="timed regions of K steps each (at least 10); the median is reported")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", type=int, default=WORKLOAD, choices=(1, 2, 3, 4, 5),
                     help="decode workload (default 2: Llama-3.1-8B INT4 32K); 5 = the "
                          "standalone quantize/pack throughput case (INT4 and INT2)")
+    ap.add_argument("--no-extra-workloads", dest="extra_workloads", action="store_false",
+                    help="time only the headline workload (by default the 128K INT2 layer, the "
+                         "batched Llama-2-13B layer and the pack case are added to the line)")
     ap.add_argument("--sink", type=int, default=0,
                     help="attention-sink rows kept fp16 per sequence (0..256; default 0)")
     ap.add_argument("--hybrid", type=int, default=0, choices=(0, 1),
