@@ -205,8 +205,10 @@ kvq_status kvq_decode_step_host(const kvq_cache_desc* desc, const kvq_cache_view
   if (!aligned(workspace, 16)) return KVQ_ERR_MISALIGNED;
   if (cudaMemcpyAsync(d, in_host, io.in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return KVQ_ERR_CUDA;
+  // the step follows this call's own copy, not a kernel: an early cache read
+  // would have nothing to overlap
   st = kvq_decode_step(desc, view, d, num_q_heads, d + io.q, d + io.q + io.kv, d + io.out_off,
-                       workspace, ws_bytes, flags, stream);
+                       workspace, ws_bytes, flags & ~(uint32_t)KVQ_STEP_EARLY_CACHE_READ, stream);
   if (st != KVQ_OK) return st;
   const size_t out_bytes = (flags & KVQ_OUT_F32) ? 2 * io.q : io.q;
   if (cudaMemcpyAsync(out_host, d + io.out_off, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)

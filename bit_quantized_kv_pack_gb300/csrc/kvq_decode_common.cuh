@@ -134,6 +134,25 @@ __device__ __forceinline__ bool take_last_ticket(const DecodeArgs& a, int64_t un
   return *flag != 0;
 }
 
+// The same ticket with one acquire-release atomic instead of fence, atomic,
+// fence: its release makes the CTA's partial and additions (ordered before it
+// by the barrier) visible before the ticket, and the last CTA's acquire makes
+// the others' visible to it.
+template <int NT>
+__device__ __forceinline__ bool take_last_ticket_acq_rel(const DecodeArgs& a, int64_t unit, int* flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(&a.counters[unit]), "r"((unsigned)(a.S - 1))
+                 : "memory");
+    *flag = (old == (unsigned)(a.S - 1));
+  }
+  __syncthreads();
+  return *flag != 0;
+}
+
 // Merge the S partials of one (sequence, KV head, query block).  The first CH
 // partials of a thread's first output are loaded in one round together with the
 // m/l values (all of them when S <= CH); maxima, weights and sums use warp

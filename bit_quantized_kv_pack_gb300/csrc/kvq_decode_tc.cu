@@ -576,9 +576,9 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
       }
     }
   };
-  // Thread 0: read the counters, cut this split's range and start its first
-  // NSTAGE tiles.
-  auto plan = [&]() {
+  // Thread 0: read the counters, cut this split's range and (tma_first) start
+  // its first NSTAGE tiles with TMA copies.
+  auto plan = [&](bool tma_first) {
     const int Lp = a.packed_len[b];
     const int Lr = a.res_len[b];
     // fused step: the append packs a token when the window is full (or absent),
@@ -623,18 +623,21 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
         const int npg = min((i1 - i0 + kPage - 1) / kPage, kPagePrefetch);
         for (int j = 0; j < npg; ++j) s_pages[j] = a.rm.page_of(b, i0 / kPage + j);
       }
-      for (int tile = 0; tile < ntiles && tile < NSTAGE; ++tile) issue(tile);
+      if (tma_first)
+        for (int tile = 0; tile < ntiles && tile < NSTAGE; ++tile) issue(tile);
     }
   };
   // With the caller's word that the kernel before this launch does not write
-  // this cache (KVQ_STEP_EARLY_CACHE_READ), the counters and the first tiles
-  // are read before waiting for that kernel; q and the new token never are.
+  // this cache (KVQ_STEP_EARLY_CACHE_READ), thread 0 reads the counters and cuts
+  // the ranges before waiting for that kernel, so the copies can start the
+  // moment the wait returns.  The copies themselves are issued after the wait:
+  // copies a dependent launch issues before it (bulk, tensor, cp.async, even
+  // plain loads of data that must come from memory) were measured to be served
+  // only once the launch it depends on had completed, and queued ahead of that
+  // launch's last memory operations they delayed its completion and with it
+  // the wait.  q and the new token are read after the wait.
   const bool early = STEP && a.early != 0;
-  if (early && threadIdx.x == 0) plan();
-  if (early && res_cta && has_f16) {  // the fp16 rows too (CTA-uniform branch)
-    __syncthreads();
-    residual_issue(f16_rows(), f0, smem + kResTilesOff);
-  }
+  if (early && threadIdx.x == 0) plan(false);
   grid_dependency_wait();
 
   // The small loads go first -- q by every thread, the lengths by thread 0 --
@@ -645,7 +648,9 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
   if (q_i < a.gq)
     qraw = *reinterpret_cast<const uint2*>(a.q + ((int64_t)b * a.Hq + h * a.gq) * D + threadIdx.x * 4);
   if (threadIdx.x == 0) {
-    if (!early) plan();
+    if (!early) plan(true);
+    else if (!res_cta)  // ranges read before the wait: start the first tiles now
+      for (int tile = 0; tile < ntiles && tile < NSTAGE; ++tile) issue(tile);
     if (err_bits) set_error(a.err_word, err_bits);
   }
   {
@@ -661,7 +666,7 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
   const float kq = a.qk_scale_log2;
   MergeSmem& ms = *reinterpret_cast<MergeSmem*>(smem);
 
-  if (!early && res_cta && has_f16) residual_issue(f16_rows(), f0, smem + kResTilesOff);
+  if (res_cta && has_f16) residual_issue(f16_rows(), f0, smem + kResTilesOff);
 
   // extra tokens of a fused step, fp32: [K, V][new token, packed token][D]
   float* xbuf = reinterpret_cast<float*>(smem + sizeof(MergeSmem));
@@ -1081,16 +1086,16 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
       }
       const float dm = M - __uint_as_float(ref - 1u);
       if (dm > kRefSlack) {
-        if (lane == 0) atomicOr(&a.fb_flag[bh], 1u);  // too far above: exact merge instead
+        if (lane == 0) ptx::red_or_u32(&a.fb_flag[bh], 1u);  // too far above: exact merge instead
       } else {
         const float g = exp2f(dm);
         ptx::red_add_v4(a.o_acc + (bh * QB + i) * D + e, o.x * g, o.y * g, o.z * g, o.w * g);
-        if (lane == 0) atomicAdd(&a.l_acc[bh * QB + i], lsum * g);
+        if (lane == 0) ptx::red_add_f32(&a.l_acc[bh * QB + i], lsum * g);
       }
     }
   }
   // the last split of this KV head to finish merges all S partials
-  if (take_last_ticket<NTHREADS>(a, bh, &s_last)) {
+  if (take_last_ticket_acq_rel<NTHREADS>(a, bh, &s_last)) {
     // Fused step: every split of this head has read the counters.  The head
     // takes a ticket on its sequence now, so the round trip overlaps the
     // combine; the last head of the sequence commits the append's counters,
@@ -1099,13 +1104,15 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
     if (STEP && threadIdx.x == 0) seq_ticket = atomicInc(&a.seq_tickets[b], (unsigned)(a.Hkv - 1));
     const int i = warp, e = lane * 4;
     float* oacc = a.o_acc + (bh * QB + i) * D + e;
-    if (__ldcg(&a.fb_flag[bh]) != 0u) {
+    // the flag and the accumulators in one round trip
+    const uint32_t far = __ldcg(&a.fb_flag[bh]);
+    const float4 o = __ldcg(reinterpret_cast<const float4*>(oacc));
+    const float L = __ldcg(&a.l_acc[bh * QB + i]);
+    if (far != 0u) {
       // some split's max was too far above the reference: log-sum-exp merge of
       // the S partials
       combine_unit<NTHREADS, D, 8>(a, b, h, 0, reinterpret_cast<float*>(smem));
     } else if (i < a.gq) {
-      const float4 o = __ldcg(reinterpret_cast<const float4*>(oacc));
-      const float L = __ldcg(&a.l_acc[bh * QB + i]);
       const float inv = L > 0.f ? 1.f / L : 0.f;
       store_out4(a, ((int64_t)b * a.Hq + h * a.gq + i) * D + e,
                  make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv));

@@ -86,19 +86,22 @@ __device__ __forceinline__ void set_error(uint32_t* err_word, uint32_t bit) {
 //   Q1  min/max over the quad: fp16 min of the lane's values and of their
 //       negations (max = -min(-x), exact), then shuffle-xor 1 and 2 of both as one
 //       half2 -- min and max of fp16 values are exact in any order
-//   Q2  scale_f = (mx - mn) / (2^b - 1) in fp32, IEEE divide
+//   Q2  scale_f = (mx - mn) / (2^b - 1) in fp32, correctly rounded (div_by_const)
 //   Q3  scale_h = fp16_rne(scale_f); min_h = fp16(mn + 0)
 //   Q4  code = clamp(rint((x - mn) / s), 0, 2^b - 1) with s = (float)scale_h and
 //       the IEEE divide, or 0 when s == 0.
 // How Q4 is computed (same codes as the plain divide):
 //   dx = x - mn is one fp32 subtraction straight from the fp16 operand (exact
-//   conversion, one rounding, as (float)x - mn).  q = dx * rcp_rn(s), clamped
-//   to 2^b - 1 (every q above it gives code 2^b - 1 however it rounds), lies
-//   within 3 ulp of the IEEE quotient (|q| <= 2^b - 1, so within 6e-6), so rint
-//   can only differ where q is within 1e-5 of a half-integer; there the lane
-//   recomputes its codes with the IEEE divide.  rint itself is the
-//   round-to-nearest-even fp32 addition of 1.5 * 2^23, which leaves the integer
-//   in the low mantissa bits (0 <= q <= 15 < 2^22), and each code is added in
+//   conversion, one rounding, as (float)x - mn).  While s is fp16-normal it is
+//   within 2^-11 of scale_f, so the quotient stays below 2^b - 1 + 0.008 and
+//   rounds to at most 2^b - 1 (no clamp).  q = dx * rcp(s), with the hardware
+//   reciprocal (within 2^-22 relative over every fp16 value, checked by
+//   kvq_testing_check_arithmetic), lies within 3
+//   ulp of the IEEE quotient (so within 6e-6), so rint can only differ where q is
+//   within 1e-5 of a half-integer; there, and for a subnormal s, the lane
+//   recomputes its codes with the IEEE divide and the clamp.  rint itself is
+//   the round-to-nearest-even fp32 addition of 1.5 * 2^23, which leaves the
+//   integer in the low mantissa bits (0 <= q < 2^22), and each code is added in
 //   at its bit offset with one shift-add (the constant mantissa bits of the
 //   eight sums are subtracted once at the end, modulo 2^32).
 // Returns the lane's 8 codes packed little-endian (8 * b bits) and the group's
@@ -130,6 +133,55 @@ __device__ __forceinline__ float quad_sq_error(const float (&x)[8], uint32_t pac
   return acc;
 }
 
+// Packed fp32 pairs (low element first) and their element-wise IEEE
+// round-to-nearest-even add, subtract and multiply.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ uint32_t lo_bits(uint64_t v) { return (uint32_t)v; }
+__device__ __forceinline__ uint32_t hi_bits(uint64_t v) { return (uint32_t)(v >> 32); }
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// d / K rounded to nearest even, for the divisors of the quantizer (K = 2^b - 1:
+// 15, 7, 3) and d in its domain (0, or a difference of two fp16 values: 2^-24
+// .. 131008).  Markstein's correction of the product by the reciprocal: with
+// c = RN(1/K), q0 = RN(d c) and the exact residual r = d - q0 K (one fused
+// multiply-add), RN(q0 + r c) is the correctly rounded quotient.  Checked
+// against the IEEE divide for every d of that domain and each K (the
+// library's kvq_testing_check_arithmetic).
+template <int K>
+__device__ __forceinline__ float div_by_const(float d) {
+  if (K == 1) return d;
+  constexpr float c = 1.0f / (float)K;
+  const float q0 = __fmul_rn(d, c);
+  const float r = __fmaf_rn(-q0, (float)K, d);
+  return __fmaf_rn(r, c, q0);
+}
+
+// The hardware's approximate reciprocal (within about 1 ulp; the quantizer's
+// near-tie window absorbs it).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // (float)h - f with one rounding: the fp16 operand converts exactly.
 __device__ __forceinline__ float sub_f16_f32(unsigned short h, float f) {
   float d;
@@ -155,31 +207,42 @@ __device__ __forceinline__ uint32_t quantize_quad(const uint4& raw, uint32_t& pa
   }
   const float mn = __low2float(mm);
   const float mx = -__high2float(mm);
-  const float scale_f = __fdiv_rn(__fsub_rn(mx, mn), (float)kQmax);
+  const float scale_f = div_by_const<kQmax>(__fsub_rn(mx, mn));
   const __half scale_h = __float2half_rn(scale_f);
   const __half min_h = __float2half_rn(__fadd_rn(mn, 0.0f));
   const float s = __half2float(scale_h);
-  const float r = s != 0.0f ? __frcp_rn(s) : 0.0f;
+  const float r = s != 0.0f ? rcp_approx(s) : 0.0f;
   constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
   constexpr uint32_t kMagicBits = 0x4B400000u;
   uint32_t magic_sum = 0;
 #pragma unroll
   for (int j = 0; j < 8; ++j) magic_sum += kMagicBits << (BITS * j);
   const unsigned short* xs = reinterpret_cast<const unsigned short*>(&raw);
+  // The pairs of values go through packed fp32x2 instructions (each element
+  // rounded as its scalar operation would be).  No clamp is needed while s is
+  // fp16-normal: s is within 2^-11 of scale_f, so q <= (2^b - 1)(1 + 2^-11 + 2^-23)
+  // rounds to at most 2^b - 1; a subnormal s takes the IEEE path below.
+  const uint64_t r2 = pack_f32x2(r, r);
+  const uint64_t m2 = pack_f32x2(kMagic, kMagic);
   float dx[8];
   uint32_t acc = 0;
-  bool near_tie = false;
+  bool near_tie = s != 0.0f && s < 6.103515625e-05f;  // subnormal fp16 scale (< 2^-14)
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    dx[j] = sub_f16_f32(xs[j], mn);
-    const float q = fminf(__fmul_rn(dx[j], r), (float)kQmax);
-    const float t = __fadd_rn(q, kMagic);
-    acc += __float_as_uint(t) << (BITS * j);
-    near_tie |= fabsf(__fsub_rn(q, __fsub_rn(t, kMagic))) > 0.49999f;
+  for (int jp = 0; jp < 4; ++jp) {
+    dx[2 * jp] = sub_f16_f32(xs[2 * jp], mn);
+    dx[2 * jp + 1] = sub_f16_f32(xs[2 * jp + 1], mn);
+    const uint64_t q2 = mul_f32x2(pack_f32x2(dx[2 * jp], dx[2 * jp + 1]), r2);
+    const uint64_t t2 = add_f32x2(q2, m2);
+    const uint64_t h2 = sub_f32x2(q2, sub_f32x2(t2, m2));  // q - rint(q)
+    acc += lo_bits(t2) << (BITS * 2 * jp);
+    acc += hi_bits(t2) << (BITS * (2 * jp + 1));
+    near_tie |= fabsf(__uint_as_float(lo_bits(h2))) > 0.49999f;
+    near_tie |= fabsf(__uint_as_float(hi_bits(h2))) > 0.49999f;
   }
   uint32_t packed = acc - magic_sum;
   if (near_tie) {
-    // a quotient within 1e-5 of a half-integer: the IEEE divide decides
+    // a quotient within 1e-5 of a half-integer, or a subnormal scale: the IEEE
+    // divide decides, then the clamp
     packed = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {

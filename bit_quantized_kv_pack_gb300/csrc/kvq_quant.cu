@@ -77,7 +77,48 @@ __global__ void __launch_bounds__(kPackThreads) quantize_pack_kernel(PackArgs a)
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int quad = lane & 3;
-  const __half* src = a.x[which] + (int64_t)b * a.sb + (int64_t)(bh % a.Hkv) * a.sh;
+  const int h = bh % a.Hkv;
+  const __half* src = a.x[which] + (int64_t)b * a.sb + (int64_t)h * a.sh;
+
+  // CTA-uniform fast path: every group of this CTA is packed into a contiguous
+  // cache (the prefill's bulk).  Addresses are 32-bit offsets from the CTA's
+  // first token, and no group needs classifying.
+  const int64_t g_last = min(groups_used, g0 + kGroupsPerCta) - 1;
+  const int t_lo = (int)(g0 >> a.ng_shift);
+  if (!a.rm.paged && t_lo >= ns && (int)(g_last >> a.ng_shift) < ns + npk) {
+    const __half* xs = src + (int64_t)t_lo * a.st;
+    const int64_t row_lo = (int64_t)bh * a.cap + (t_lo - ns);
+    uint8_t* cbase = a.codes[which] + row_lo * a.row_bytes;
+    uint32_t* pbase = a.params[which] + row_lo * a.Ng;
+    const int gl0 = warp * 8 + (lane >> 2);  // this lane's group in the first iteration
+    const int ng_used = (int)(g_last - g0) + 1;
+    uint4 raw[kPackUnroll];
+#pragma unroll
+    for (int u = 0; u < kPackUnroll; ++u) {
+      const int gl = gl0 + u * kGroupsPerIter;
+      raw[u] = make_uint4(0, 0, 0, 0);
+      if (gl < ng_used) {
+        const int tl = gl >> a.ng_shift, g = gl & (a.Ng - 1);
+        raw[u] = __ldg(reinterpret_cast<const uint4*>(xs + (int64_t)tl * a.st) + g * (kGroup / 8) + quad);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPackUnroll; ++u) {
+      const int gl = gl0 + u * kGroupsPerIter;
+      const bool in_range = gl < ng_used;
+      uint32_t prm, asym = 1;
+      const uint32_t packed = quantize_quad<BITS>(raw[u], prm, HYB, &asym);  // all lanes take part
+      const uint32_t modes = HYB ? __ballot_sync(0xffffffffu, quad == 0 && asym) : 0u;
+      const int tl = gl >> a.ng_shift, g = gl & (a.Ng - 1);
+      store_group_codes<BITS>(cbase + (uint32_t)(tl * a.row_bytes + g * (4 * BITS)), packed, quad,
+                              in_range);
+      if (in_range && quad == 0) {
+        pbase[(uint32_t)gl] = prm;  // the CTA's groups are consecutive params
+        if (HYB && g == 0) a.modes[which][row_lo + tl] = mode_byte(modes, lane >> 2, a.Ng);
+      }
+    }
+    return;
+  }
 
   uint4 raw[kPackUnroll];
   int64_t gi[kPackUnroll];
@@ -102,7 +143,7 @@ __global__ void __launch_bounds__(kPackThreads) quantize_pack_kernel(PackArgs a)
     // byte comes from one ballot
     const uint32_t modes = HYB ? __ballot_sync(0xffffffffu, quad == 0 && asym) : 0u;
     const bool packs = in_range && t >= ns && t - ns < npk;
-    const int64_t row = packs ? a.rm.row(b, bh % a.Hkv, t - ns) : -1;
+    const int64_t row = packs ? a.rm.row(b, h, t - ns) : -1;
     if (packs && row < 0 && quad == 0) set_error(a.err_word, KVQ_ERRBIT_BADPAGE);
     const bool to_pack = packs && row >= 0;
     store_group_codes<BITS>(to_pack ? a.codes[which] + row * a.row_bytes + g * (4 * BITS) : nullptr,

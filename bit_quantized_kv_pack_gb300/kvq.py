@@ -45,7 +45,8 @@ EXPORTS = ("kvq_cache_bytes", "kvq_decode_workspace_bytes", "kvq_quantize_pack",
            "kvq_quantize_pack_strided", "kvq_append",
            "kvq_decode_attention", "kvq_decode_step", "kvq_decode_step_host", "kvq_step_io_bytes",
            "kvq_decode_attention_noalloc",
-           "kvq_read_error", "kvq_status_string", "kvq_version", "kvq_testing_wait_fault")
+           "kvq_read_error", "kvq_status_string", "kvq_version", "kvq_testing_wait_fault",
+           "kvq_testing_check_arithmetic")
 
 
 class CacheDesc(ctypes.Structure):
@@ -117,6 +118,9 @@ def load(path: str | None = None):
             lib.kvq_version.restype = i32
             lib.kvq_testing_wait_fault.argtypes = [ctypes.c_uint32]
             lib.kvq_testing_wait_fault.restype = None
+            lib.kvq_testing_check_arithmetic.argtypes = [ctypes.POINTER(ctypes.c_uint64),
+                                                         ctypes.POINTER(ctypes.c_double)]
+            lib.kvq_testing_check_arithmetic.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -406,3 +410,13 @@ def kvq_testing_wait_fault(limit_us: int) -> None:
     """Testing hook (see kvq.h): limit_us > 0 makes one bounded wait of the next
     tensor-core decode calls run out after limit_us microseconds; 0 turns it off."""
     load().kvq_testing_wait_fault(int(limit_us))
+
+
+def kvq_testing_check_arithmetic():
+    """Testing hook (see kvq.h): ([mismatches, in domain] for the divisors 15, 7,
+    3, the reciprocal's worst relative error over the fp16 scales)."""
+    mm = (ctypes.c_uint64 * 6)()
+    worst = ctypes.c_double(0.0)
+    _check(load().kvq_testing_check_arithmetic(mm, ctypes.byref(worst)),
+           "kvq_testing_check_arithmetic")
+    return [(int(mm[2 * i]), int(mm[2 * i + 1])) for i in range(3)], worst.value

@@ -290,9 +290,10 @@ kvq_status kvq_decode_attention(const kvq_cache_desc* desc, const kvq_cache_view
  *              this cache (any array of its view, counters included) -- in a serving loop
  *              it computes q, k_new and v_new, and the cache was last written by
  *              this layer's previous step.  The step (launched as a programmatic
- *              dependent of that kernel) then reads the counters and starts its
- *              first tile copies before it waits for that kernel; q, k_new and
- *              v_new are read, and anything is written, only after the wait.
+ *              dependent of that kernel) then reads the counters and cuts its
+ *              ranges before it waits for that kernel, and starts its copies the
+ *              moment the wait returns; q, k_new and v_new are read, and anything
+ *              is written, only after the wait.
  *              Without the flag nothing is read before the wait.  KVQ_OUT_F32
  *              may be or'ed in (fp32 out).  Other bits return KVQ_ERR_INVALID_ARG.
  * Asynchronous. */
@@ -316,8 +317,9 @@ size_t kvq_step_io_bytes(const kvq_cache_desc* desc, int32_t num_q_heads);
  *   dev_io     device staging of dev_io_bytes >= kvq_step_io_bytes(desc, Hq),
  *              256-byte aligned, owned by the caller.
  * Enqueues on `stream`: one host-to-device copy of the input block, the step
- * (as kvq_decode_step with the same workspace and flags), and one
- * device-to-host copy of out.  Asynchronous when the host buffers are pinned
+ * (as kvq_decode_step with the same workspace and flags, less
+ * KVQ_STEP_EARLY_CACHE_READ: the step follows the copy, so there is nothing to
+ * overlap), and one device-to-host copy of out.  Asynchronous when the host buffers are pinned
  * (page-locked), in which case they must stay valid until the stream reaches
  * the copies; with pageable memory the copies are synchronous.  Argument errors
  * return before anything is enqueued. */
@@ -378,6 +380,16 @@ int32_t kvq_version(void); /* 150: timeout testing hook, cached tensor maps; 140
  * limit_us = 0 (the default) restores normal behaviour.  Process-wide; not for
  * production use. */
 void kvq_testing_wait_fault(uint32_t limit_us);
+
+/* Testing hook (no passage of the pages corresponds to it): exhaustive checks,
+ * on the current device, of the quantizer's fast arithmetic against the IEEE
+ * operations it replaces.  div_mismatches[2i], [2i + 1] (i = 0, 1, 2 for the
+ * divisors 2^b - 1 = 15, 7, 3): how many non-negative finite floats d give a
+ * quotient d / (2^b - 1) other than the IEEE divide's, in all and in the
+ * quantizer's domain (0 and the differences of fp16 values, 2^-24 .. 131008);
+ * rcp_worst_rel: the largest relative error of the reciprocal used for the codes,
+ * over every positive finite fp16 scale.  Synchronous (legacy default stream). */
+kvq_status kvq_testing_check_arithmetic(uint64_t* div_mismatches, double* rcp_worst_rel);
 
 #ifdef __cplusplus
 }

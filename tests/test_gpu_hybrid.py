@@ -95,13 +95,14 @@ def test_hybrid_decode(bits, d, gq):
     assert_attn_close(kvq.kvq_decode_attention(g, q.to(DEV)), want)
 
 
-@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("fused", [False, True, "early"])
 @pytest.mark.parametrize("bits,d,gq,Nr", [(4, 128, 4, 16), (2, 128, 4, 0), (4, 64, 2, 8)])
 def test_hybrid_steps(fused, bits, d, gq, Nr):
     """Appends through kvq_append + decode or the fused step (tensor-core path
     for head_dim 128): each packed token quantized by the hybrid rule, its mode
     byte written; bytes and outputs against the oracle after every step."""
-    rng = np.random.default_rng(bits * 7 + d + Nr + fused)
+    rng = np.random.default_rng(bits * 7 + d + Nr + bool(fused))
+    flags = kvq.KVQ_STEP_EARLY_CACHE_READ if fused == "early" else 0
     B, H = 2, 2
     lens = torch.tensor([Nr + 300, 3], dtype=torch.int32)
     p = 0.01 if bits == 4 else 0.0
@@ -114,7 +115,7 @@ def test_hybrid_steps(fused, bits, d, gq, Nr):
         q = torch.from_numpy(rng.standard_normal((B, H * gq, d)).astype(np.float16))
         out = torch.empty(q.shape, dtype=torch.float32, device=DEV)
         if fused:
-            kvq.kvq_decode_step(g, q.to(DEV), kn.to(DEV), vn.to(DEV), out, ws)
+            kvq.kvq_decode_step(g, q.to(DEV), kn.to(DEV), vn.to(DEV), out, ws, flags=flags)
         else:
             kvq.kvq_append(g, kn.to(DEV), vn.to(DEV))
             kvq.kvq_decode_attention(g, q.to(DEV), out, ws)

@@ -60,12 +60,13 @@ def test_int3_decode(d, gq, S):
     assert_attn_close(kvq.kvq_decode_attention(g, q.to(DEV), flags=kvq.KVQ_OUT_F32), want)
 
 
-@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("fused", [False, True, "early"])
 @pytest.mark.parametrize("Nr", [16, 0])
 def test_int3_steps(fused, Nr):
     """Appends: the window fills, then every step packs its oldest token (or,
     with no window, the new one) -- 3-bit codes written by the append kernel."""
-    rng = np.random.default_rng(40 + Nr + fused)
+    rng = np.random.default_rng(40 + Nr + bool(fused))
+    flags = kvq.KVQ_STEP_EARLY_CACHE_READ if fused == "early" else 0
     B, H, d, gq = 2, 2, 128, 4
     lens = torch.tensor([Nr + 200, 3], dtype=torch.int32)
     k = torch.from_numpy(rng.standard_normal((B, H, Nr + 200, d)).astype(np.float16))
@@ -77,7 +78,8 @@ def test_int3_steps(fused, Nr):
         vn = torch.from_numpy(rng.standard_normal((B, H, d)).astype(np.float16))
         q = torch.from_numpy(rng.standard_normal((B, H * gq, d)).astype(np.float16))
         if fused:
-            out = kvq.kvq_decode_step(g, q.to(DEV), kn.to(DEV), vn.to(DEV), workspace=ws)
+            out = kvq.kvq_decode_step(g, q.to(DEV), kn.to(DEV), vn.to(DEV), workspace=ws,
+                                      flags=flags)
         else:
             kvq.kvq_append(g, kn.to(DEV), vn.to(DEV))
             out = kvq.kvq_decode_attention(g, q.to(DEV), workspace=ws)

@@ -63,15 +63,18 @@ def test_paged_decode(bits, d, gq):
     assert kvq.kvq_read_error(g)[0] == kvq.KVQ_OK
 
 
-@pytest.mark.parametrize("fused", [False, True])
-@pytest.mark.parametrize("bits,Nr,hybrid", [(4, 16, 0), (2, 0, 0), (4, 8, 1)])
+@pytest.mark.parametrize("fused", [False, True, "early"])
+@pytest.mark.parametrize("bits,Nr,hybrid", [(4, 16, 0), (2, 0, 0), (4, 8, 1), (3, 16, 0)])
 def test_paged_steps(fused, bits, Nr, hybrid):
     """Appends across page boundaries (the packed count passes multiples of
-    32), through kvq_append + decode or the fused step."""
-    rng = np.random.default_rng(bits * 7 + Nr + fused + hybrid)
+    32), through kvq_append + decode or the fused step (also with its first
+    tiles copied before the grid-dependency wait)."""
+    rng = np.random.default_rng(bits * 7 + Nr + bool(fused) + hybrid)
     B, H, d, gq, cap = 2, 2, 128, 4, 256
     lens = [Nr + 30, 3]
-    g, r, st, word, err = _both(rng, B, H, d, bits, cap, Nr, lens, 24, hybrid=hybrid, seed=fused + 1)
+    g, r, st, word, err = _both(rng, B, H, d, bits, cap, Nr, lens, 24, hybrid=hybrid,
+                                seed=bool(fused) + 1)
+    flags = kvq.KVQ_STEP_EARLY_CACHE_READ if fused == "early" else 0
     assert st == kvq.KVQ_OK and err == 0
     ws = kvq.workspace_for(g, H * gq)
     for _ in range(40):
@@ -79,7 +82,8 @@ def test_paged_steps(fused, bits, Nr, hybrid):
         vn = torch.from_numpy(rng.standard_normal((B, H, d)).astype(np.float16))
         q = torch.from_numpy(rng.standard_normal((B, H * gq, d)).astype(np.float16))
         if fused:
-            out = kvq.kvq_decode_step(g, q.to(DEV), kn.to(DEV), vn.to(DEV), workspace=ws)
+            out = kvq.kvq_decode_step(g, q.to(DEV), kn.to(DEV), vn.to(DEV), workspace=ws,
+                                      flags=flags)
         else:
             kvq.kvq_append(g, kn.to(DEV), vn.to(DEV))
             out = kvq.kvq_decode_attention(g, q.to(DEV), workspace=ws)
@@ -134,7 +138,8 @@ def test_paged_bad_page_is_flagged_and_skipped():
         assert_attn_close(out[:1], oracle.decode(r0, q.numpy()[:1]))
 
 
-def test_paged_step_into_bad_page_matches_append_then_decode():
+@pytest.mark.parametrize("flags", [0, kvq.KVQ_STEP_EARLY_CACHE_READ])
+def test_paged_step_into_bad_page_matches_append_then_decode(flags):
     """A fused step whose packed token lands in a page outside the pool writes
     nothing there, flags it and leaves that token out of the attention, exactly
     as kvq_append followed by kvq_decode_attention does."""
@@ -154,7 +159,7 @@ def test_paged_step_into_bad_page_matches_append_then_decode():
         vn = torch.from_numpy(rs.standard_normal((B, H, d)).astype(np.float16)).to(DEV)
         q = torch.from_numpy(rs.standard_normal((B, H * gq, d)).astype(np.float16)).to(DEV)
         if fused:
-            out = kvq.kvq_decode_step(g, q, kn, vn, flags=kvq.KVQ_OUT_F32)
+            out = kvq.kvq_decode_step(g, q, kn, vn, flags=kvq.KVQ_OUT_F32 | flags)
         else:
             kvq.kvq_append(g, kn, vn)
             out = kvq.kvq_decode_attention(g, q, flags=kvq.KVQ_OUT_F32)

@@ -24,7 +24,7 @@ def _assert_gpu_caches_equal(a, b):
         assert torch.equal(getattr(a, name), getattr(b, name)), name
 
 
-def _run_steps(rng, B, H, d, gq, bits, cap, Nr, lens, nsteps, scale=1.0):
+def _run_steps(rng, B, H, d, gq, bits, cap, Nr, lens, nsteps, scale=1.0, flags=0):
     """Prefill `lens`, then `nsteps` fused steps on one cache and append + decode
     on a twin; both against the oracle after every step."""
     Lmax = max(max(lens), 1)
@@ -43,7 +43,8 @@ def _run_steps(rng, B, H, d, gq, bits, cap, Nr, lens, nsteps, scale=1.0):
         kn = torch.from_numpy((rng.standard_normal((B, H, d)) * scale).astype(np.float16))
         vn = torch.from_numpy(rng.standard_normal((B, H, d)).astype(np.float16))
         q = torch.from_numpy(rng.standard_normal((B, H * gq, d)).astype(np.float16))
-        out = kvq.kvq_decode_step(fused, q.to(DEV), kn.to(DEV), vn.to(DEV), workspace=ws)
+        out = kvq.kvq_decode_step(fused, q.to(DEV), kn.to(DEV), vn.to(DEV), workspace=ws,
+                                  flags=flags)
         st_f, w_f = kvq.kvq_read_error(fused)
         kvq.kvq_append(twin, kn.to(DEV), vn.to(DEV))
         out2 = kvq.kvq_decode_attention(twin, q.to(DEV))
@@ -59,13 +60,16 @@ def _run_steps(rng, B, H, d, gq, bits, cap, Nr, lens, nsteps, scale=1.0):
     return words
 
 
-@pytest.mark.parametrize("bits", [4, 2])
+@pytest.mark.parametrize("early", [0, 1])
+@pytest.mark.parametrize("bits", [4, 2, 3])
 @pytest.mark.parametrize("Nr,lens", [(16, [3, 16, 40]), (0, [5, 130, 1]), (128, [700, 10, 128])])
-def test_step_tensor_core_path(bits, Nr, lens):
+def test_step_tensor_core_path(bits, Nr, lens, early):
     """head_dim 128, 4 query heads per KV head: one launch per step.  Nr 16 with
-    lens 3/16/40: one window fills then packs, two pack every step and wrap."""
+    lens 3/16/40: one window fills then packs, two pack every step and wrap.
+    early: the first tiles are copied before the grid-dependency wait."""
     rng = np.random.default_rng(bits * 100 + Nr)
-    words = _run_steps(rng, 3, 2, 128, 4, bits, 800, Nr, lens, 20, scale=2.0)
+    words = _run_steps(rng, 3, 2, 128, 4, bits, 800, Nr, lens, 20, scale=2.0,
+                       flags=kvq.KVQ_STEP_EARLY_CACHE_READ if early else 0)
     assert all(w == 0 and e == 0 for w, e in words)
 
 
@@ -88,8 +92,8 @@ def test_step_capacity_full(Nr):
     assert all(w == kvq.KVQ_ERRBIT_CAPACITY and e & 1 for w, e in words[2:])
 
 
-@pytest.mark.parametrize("num", [2, 3, 4])
-def test_step_workload_full_size(num):
+@pytest.mark.parametrize("num,flags", [(2, 0), (3, 0), (4, 0), (2, 1), (3, 1), (4, 1)])
+def test_step_workload_full_size(num, flags):
     """Llama-3.1-8B layer (32K INT4, 128K INT2; 128-token window, full) and the
     Llama-2-13B batch of 64 ragged sequences (sequences 0, 17 and 63 checked):
     three fused steps with fp32 output, each packing the oldest window token,
@@ -111,7 +115,7 @@ def test_step_workload_full_size(num):
         kn, vn = w.new_tokens(step)
         q = w.query(step)
         out = torch.empty(q.shape, dtype=torch.float32, device=DEV)
-        kvq.kvq_decode_step(g, q.to(DEV), kn.to(DEV), vn.to(DEV), out, ws)
+        kvq.kvq_decode_step(g, q.to(DEV), kn.to(DEV), vn.to(DEV), out, ws, flags=flags)
         assert kvq.kvq_read_error(g)[0] == kvq.KVQ_OK
         oracle.append(r, kn[rows].numpy(), vn[rows].numpy())
         want = oracle.decode(r, q[rows].numpy())
