@@ -52,6 +52,17 @@ kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR
 
 constexpr uint32_t kStepFlags = KVQ_STEP_EARLY_CACHE_READ | KVQ_OUT_F32;
 
+// A page-locked host buffer the device addresses with the same pointer (the
+// allocation registered with the driver, mapped, and the device pointer equal).
+bool host_mapped(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeHost && at.devicePointer == p && at.hostPointer == p;
+}
+
 }  // namespace
 
 extern "C" {
@@ -191,6 +202,16 @@ kvq_status kvq_decode_step_host(const kvq_cache_desc* desc, const kvq_cache_view
                                 size_t ws_bytes, uint32_t flags, void* stream) {
   kvq_status st = check_desc(desc);
   if (st != KVQ_OK) return st;
+  if (flags & KVQ_STEP_HOST_MAPPED) {
+    // the step reads the input block and writes out in place, over the host link
+    if (!in_host || !out_host || num_q_heads < 1 || num_q_heads % desc->num_kv_heads)
+      return KVQ_ERR_INVALID_ARG;
+    if (!host_mapped(in_host) || !host_mapped(out_host)) return KVQ_ERR_INVALID_ARG;
+    const StepIo io = step_io(*desc, num_q_heads);
+    const char* in = static_cast<const char*>(in_host);
+    return kvq_decode_step(desc, view, in, num_q_heads, in + io.q, in + io.q + io.kv, out_host,
+                           workspace, ws_bytes, flags & ~(uint32_t)KVQ_STEP_HOST_MAPPED, stream);
+  }
   if (!in_host || !out_host || !dev_io || num_q_heads < 1 || num_q_heads % desc->num_kv_heads)
     return KVQ_ERR_INVALID_ARG;
   if (!aligned(dev_io, 256)) return KVQ_ERR_MISALIGNED;

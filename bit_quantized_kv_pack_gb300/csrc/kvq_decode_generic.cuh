@@ -23,6 +23,8 @@
 // and kvq_decode_generic.cu dispatches on the width.
 #pragma once
 
+#include <atomic>
+
 #include <math.h>
 
 #include "kvq_decode_common.cuh"
@@ -260,12 +262,22 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(DecodeArgs a) 
 
 template <int D, int BITS, int QB>
 cudaError_t launch_one(dim3 grid, size_t smem, const DecodeArgs& a, cudaStream_t st) {
-  static size_t smem_set = 0;  // largest dynamic size opted in so far for this instance
-  if (smem > smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_generic_kernel<D, BITS, QB>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // largest dynamic size opted in so far for this instance, per device (the
+  // attribute is per device; a process may drive several GPUs from threads)
+  constexpr int kMaxDev = 64;
+  static std::atomic<size_t> smem_set[kMaxDev];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev || smem > smem_set[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(decode_generic_kernel<D, BITS, QB>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    smem_set = smem;
+    if (dev >= 0 && dev < kMaxDev) {
+      size_t cur = smem_set[dev].load(std::memory_order_relaxed);
+      while (cur < smem && !smem_set[dev].compare_exchange_weak(cur, smem)) {
+      }
+    }
   }
   decode_generic_kernel<D, BITS, QB><<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();

@@ -323,6 +323,7 @@ def kvq_decode_attention(cache: KVCache, q: torch.Tensor, out: torch.Tensor | No
 
 
 KVQ_STEP_EARLY_CACHE_READ = 1
+KVQ_STEP_HOST_MAPPED = 4
 
 
 def kvq_decode_step(cache: KVCache, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
@@ -360,20 +361,23 @@ def step_io_for(cache: KVCache, num_q_heads: int) -> torch.Tensor:
 
 
 def kvq_decode_step_host(cache: KVCache, in_host: torch.Tensor, num_q_heads: int,
-                         out_host: torch.Tensor, dev_io: torch.Tensor, workspace: torch.Tensor,
+                         out_host: torch.Tensor, dev_io: torch.Tensor | None, workspace: torch.Tensor,
                          stream=None, flags: int = 0) -> None:
     """One step from host memory: in_host = [q | k_new | v_new] fp16 (pinned for
     an asynchronous call), out_host fp16 [B][Hq][d]; copies, step and copy back
     enqueued on the stream by one library call.  An fp32 out_host gives fp32
-    output."""
+    output.  flags | KVQ_STEP_HOST_MAPPED (pinned, device-mapped buffers): the
+    step reads and writes them in place, no copies, dev_io unused."""
     if in_host.is_cuda or out_host.is_cuda:
         raise ValueError("in_host and out_host must be host tensors")
     flags = (flags | KVQ_OUT_F32) if out_host.dtype == torch.float32 else (flags & ~KVQ_OUT_F32)
+    io_ptr = _ptr(dev_io) if dev_io is not None else ctypes.c_void_p(0)
+    io_bytes = dev_io.numel() * dev_io.element_size() if dev_io is not None else 0
     st = load().kvq_decode_step_host(ctypes.byref(cache.desc), ctypes.byref(cache.view),
-                                     _ptr(in_host), int(num_q_heads), _ptr(out_host), _ptr(dev_io),
-                                     dev_io.numel() * dev_io.element_size(), _ptr(workspace),
+                                     _ptr(in_host), int(num_q_heads), _ptr(out_host), io_ptr,
+                                     io_bytes, _ptr(workspace),
                                      workspace.numel() * workspace.element_size(), int(flags),
-                                     _stream(stream, dev_io.device))
+                                     _stream(stream, workspace.device))
     _check(st, "kvq_decode_step_host")
 
 

@@ -319,10 +319,20 @@ size_t kvq_step_io_bytes(const kvq_cache_desc* desc, int32_t num_q_heads);
  * Enqueues on `stream`: one host-to-device copy of the input block, the step
  * (as kvq_decode_step with the same workspace and flags, less
  * KVQ_STEP_EARLY_CACHE_READ: the step follows the copy, so there is nothing to
- * overlap), and one device-to-host copy of out.  Asynchronous when the host buffers are pinned
- * (page-locked), in which case they must stay valid until the stream reaches
- * the copies; with pageable memory the copies are synchronous.  Argument errors
- * return before anything is enqueued. */
+ * overlap), and one device-to-host copy of out.  Asynchronous when the host
+ * buffers are pinned (page-locked), in which case they must stay valid until
+ * the stream reaches the copies; with pageable memory the copies are
+ * synchronous.  Argument errors return before anything is enqueued.
+ *   flags | KVQ_STEP_HOST_MAPPED: in_host and out_host are page-locked host
+ *              memory the device addresses with the same pointer (cudaHostAlloc,
+ *              or registered with mapping; checked with cudaPointerGetAttributes,
+ *              KVQ_ERR_INVALID_ARG otherwise).  No copy is enqueued: the step
+ *              kernel reads the input block and writes out in place over the
+ *              host link (NVLink-C2C on Grace hosts), dev_io is unused (may be
+ *              NULL), and KVQ_STEP_EARLY_CACHE_READ keeps its meaning (the
+ *              kernel before this call is the one it overlaps).  The buffers
+ *              must stay valid until the step completes. */
+#define KVQ_STEP_HOST_MAPPED 4u
 kvq_status kvq_decode_step_host(const kvq_cache_desc* desc, const kvq_cache_view* view,
                                 const void* in_host, int32_t num_q_heads, void* out_host,
                                 void* dev_io, size_t dev_io_bytes, void* workspace,
