@@ -1,6 +1,9 @@
 """Shared helpers of the GPU parity tests: run the same seeded inputs through the
 CUDA path (C ABI via the ctypes binding) and the CPU oracle, and compare."""
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
@@ -118,3 +121,27 @@ def assert_attn_close(out, want, atol=ATOL, rtol=RTOL_L2):
     assert excess <= 0 and rel <= rtol, \
         f"max abs {err:.3e} (bound {atol} + fp16 rounding exceeded by {excess:.2e}), rel L2 {rel:.3e} (<= {rtol})"
     return err, rel
+
+
+def per_sequence(fn, n, threads=None):
+    """fn(b) for b in range(n) on a thread pool: the oracle is a C library whose
+    ctypes calls release the interpreter lock, so sequences run in parallel."""
+    with ThreadPoolExecutor(max_workers=threads or min(n, os.cpu_count() or 1)) as ex:
+        return list(ex.map(fn, range(n)))
+
+
+def oracle_sequences(k, v, lens, bits, cap, Nr, sink=0, hybrid=0):
+    """One one-sequence oracle cache per sequence of a prefill (k, v host numpy
+    [B][Hkv][Lmax][d] fp16, lens int32 [B]), packed in parallel."""
+    B, H, _, d = k.shape
+
+    def one(b):
+        L = max(int(lens[b]), 1)
+        r = ref_cache(1, H, d, bits, cap, Nr, sink, hybrid)
+        err = oracle.quantize_pack(r, np.ascontiguousarray(k[b:b + 1, :, :L]),
+                                   np.ascontiguousarray(v[b:b + 1, :, :L]),
+                                   np.ascontiguousarray(lens[b:b + 1], dtype=np.int32))
+        assert err == 0, (b, err)
+        return r
+
+    return per_sequence(one, B)

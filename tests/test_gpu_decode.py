@@ -10,7 +10,7 @@ import torch
 import oracle
 from bit_quantized_kv_pack_gb300 import kvq, synth
 
-from _util import assert_attn_close, attn_errors, gpu_cache, ref_cache, to_np
+from _util import oracle_sequences, per_sequence, assert_attn_close, attn_errors, gpu_cache, ref_cache, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -92,10 +92,10 @@ def test_decode_workload_full_size(num):
     print(f"workload {num}: max abs {err:.2e}, rel L2 {rel:.2e}")
 
 
-def test_decode_ragged_batch_workload_sampled():
+def test_decode_ragged_batch_workload_full():
     """Llama-2-13B batch at full size (B64, 40 heads, ragged 1024..4096, Nr96):
-    the oracle recomputes 48 sampled (sequence, head) rows, including the
-    shortest and longest sequences."""
+    every packed byte of all 64 sequences and all 2560 (sequence, head) output
+    rows against the oracle (one oracle cache per sequence, in parallel)."""
     w = synth.WORKLOADS[4]
     k, v, lens = w.prefill(device=DEV)
     cap = w.len_max - w.residual
@@ -104,21 +104,14 @@ def test_decode_ragged_batch_workload_sampled():
     q = w.query(0)
     out = kvq.kvq_decode_attention(g, q.to(DEV))
     assert kvq.kvq_read_error(g)[0] == kvq.KVQ_OK
-    order = torch.argsort(lens)
-    seqs = sorted({int(order[0]), int(order[-1]), 3, 20, 41, 62})
-    r = ref_cache(len(seqs), w.num_kv_heads, w.head_dim, w.bits, cap, w.residual)
-    sub = torch.tensor(seqs)
-    sd = sub.to(DEV)
-    assert oracle.quantize_pack(r, to_np(k[sd]), to_np(v[sd]), to_np(lens[sub])) == 0
-    rng = np.random.default_rng(4)
-    pairs = np.array([(i, int(h)) for i in range(len(seqs)) for h in rng.choice(40, 8, replace=False)],
-                     np.int32)
-    want = oracle.decode(r, q[sub].numpy(), pairs)
-    rows_b = sub[torch.from_numpy(pairs[:, 0]).long()].to(DEV)
-    rows_h = torch.from_numpy(pairs[:, 1]).long().to(DEV)
-    got = out[rows_b, rows_h]
-    err, rel = assert_attn_close(got, want)
-    print(f"workload 4 (48 rows): max abs {err:.2e}, rel L2 {rel:.2e}")
+    rs = oracle_sequences(to_np(k), to_np(v), to_np(lens), w.bits, cap, w.residual)
+    del k, v
+    for b in range(w.batch):
+        assert_cache_equal(g, rs[b], batches=[b])
+    qn = q.numpy()
+    want = np.concatenate(per_sequence(lambda b: oracle.decode(rs[b], qn[b:b + 1]), w.batch))
+    err, rel = assert_attn_close(out, want)
+    print(f"workload 4 (all 2560 rows): max abs {err:.2e}, rel L2 {rel:.2e}")
 
 
 def test_decode_is_stream_ordered():

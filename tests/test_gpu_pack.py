@@ -10,7 +10,7 @@ import torch
 import oracle
 from bit_quantized_kv_pack_gb300 import kvq, synth
 
-from _util import assert_cache_equal, gpu_cache, ref_cache, to_np
+from _util import oracle_sequences, assert_cache_equal, gpu_cache, ref_cache, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -100,21 +100,19 @@ def test_pack_decode_workloads_full_size(num):
     assert_cache_equal(g, r)
 
 
-def test_pack_ragged_batch_workload_sampled():
-    """Llama-2-13B batch (B64, Hkv40, ragged 1024..4096, Nr96): the GPU packs the
-    whole batch; the oracle checks 6 sequences (shortest, longest and 4 more)."""
+def test_pack_ragged_batch_workload_full():
+    """Llama-2-13B batch (B64, Hkv40, ragged 1024..4096, Nr96): every code,
+    scale, min and window row of all 64 sequences against the oracle (one
+    oracle cache per sequence, in parallel)."""
     w = synth.WORKLOADS[4]
     k, v, lens = w.prefill(device=DEV)
     cap = w.len_max - w.residual
     g = gpu_cache(w.batch, w.num_kv_heads, w.head_dim, w.bits, cap, w.residual)
     kvq.kvq_quantize_pack(g, k, v, lens.to(DEV))
     assert kvq.kvq_read_error(g)[0] == kvq.KVQ_OK
-    order = torch.argsort(lens)
-    pick = sorted({int(order[0]), int(order[-1]), 1, 17, 33, 63})
-    sub = torch.tensor(pick)
-    r = ref_cache(len(pick), w.num_kv_heads, w.head_dim, w.bits, cap, w.residual)
-    assert oracle.quantize_pack(r, to_np(k[sub.to(DEV)]), to_np(v[sub.to(DEV)]), to_np(lens[sub])) == 0
-    assert_cache_equal(g, r, batches=pick)
+    rs = oracle_sequences(to_np(k), to_np(v), to_np(lens), w.bits, cap, w.residual)
+    for b in range(w.batch):
+        assert_cache_equal(g, rs[b], batches=[b])
 
 
 def _token_major(k):

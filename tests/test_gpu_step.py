@@ -12,7 +12,7 @@ import torch
 import oracle
 from bit_quantized_kv_pack_gb300 import kvq, synth
 
-from _util import assert_attn_close, assert_cache_equal, gpu_cache, ref_cache, to_np
+from _util import oracle_sequences, per_sequence, assert_attn_close, assert_cache_equal, gpu_cache, ref_cache, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -95,20 +95,17 @@ def test_step_capacity_full(Nr):
 @pytest.mark.parametrize("num,flags", [(2, 0), (3, 0), (4, 0), (2, 1), (3, 1), (4, 1)])
 def test_step_workload_full_size(num, flags):
     """Llama-3.1-8B layer (32K INT4, 128K INT2; 128-token window, full) and the
-    Llama-2-13B batch of 64 ragged sequences (sequences 0, 17 and 63 checked):
-    three fused steps with fp32 output, each packing the oldest window token,
-    every checked output row against the oracle with the flat max-abs bar; after
-    each step a decode with fp16 output of the same cache; the packed slots
-    written against the oracle."""
+    Llama-2-13B batch of 64 ragged sequences (all of them): three fused steps
+    with fp32 output, each packing the oldest window token, every output row
+    against the oracle with the flat max-abs bar; after each step a decode with
+    fp16 output of the same cache; the packed slots written against the oracle
+    (one oracle cache per sequence, stepped in parallel)."""
     w = synth.WORKLOADS[num]
     k, v, lens = w.prefill(device=DEV)
     cap = w.len_max - w.residual + 8
     g = gpu_cache(w.batch, w.num_kv_heads, w.head_dim, w.bits, cap, w.residual)
     kvq.kvq_quantize_pack(g, k, v, lens.to(DEV))
-    rows = list(range(w.batch)) if w.batch < 8 else [0, 17, 63]
-    r = ref_cache(len(rows), w.num_kv_heads, w.head_dim, w.bits, cap, w.residual)
-    Lm = int(lens[rows].max())
-    assert oracle.quantize_pack(r, to_np(k[rows, :, :Lm]), to_np(v[rows, :, :Lm]), to_np(lens[rows])) == 0
+    rs = oracle_sequences(to_np(k), to_np(v), to_np(lens), w.bits, cap, w.residual)
     del k, v
     ws = kvq.workspace_for(g, w.num_q_heads)
     for step in range(3):
@@ -117,13 +114,16 @@ def test_step_workload_full_size(num, flags):
         out = torch.empty(q.shape, dtype=torch.float32, device=DEV)
         kvq.kvq_decode_step(g, q.to(DEV), kn.to(DEV), vn.to(DEV), out, ws, flags=flags)
         assert kvq.kvq_read_error(g)[0] == kvq.KVQ_OK
-        oracle.append(r, kn[rows].numpy(), vn[rows].numpy())
-        want = oracle.decode(r, q[rows].numpy())
-        err, rel = assert_attn_close(out[rows], want)
-        err16, rel16 = assert_attn_close(kvq.kvq_decode_attention(g, q.to(DEV), workspace=ws)[rows], want)
+        knn, vnn, qn = kn.numpy(), vn.numpy(), q.numpy()
+        assert all(e == 0 for e in per_sequence(
+            lambda b: oracle.append(rs[b], knn[b:b + 1], vnn[b:b + 1]), w.batch))
+        want = np.concatenate(per_sequence(lambda b: oracle.decode(rs[b], qn[b:b + 1]), w.batch))
+        err, rel = assert_attn_close(out, want)
+        err16, rel16 = assert_attn_close(kvq.kvq_decode_attention(g, q.to(DEV), workspace=ws), want)
         print(f"workload {num} step {step}: fp32 out max abs {err:.2e}, rel L2 {rel:.2e}; "
               f"fp16 out max abs {err16:.2e}, rel L2 {rel16:.2e}")
-    assert_cache_equal(g, r, batches=rows)
+    for b in range(w.batch):
+        assert_cache_equal(g, rs[b], batches=[b])
 
 
 @pytest.mark.parametrize("bits", [4, 2])
@@ -211,3 +211,48 @@ def test_step_host_matches_device_step(bits, out_dtype):
         want = oracle.decode(r, q)
         assert_attn_close(out_h, want)
         assert_attn_close(out_b, want)
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_step_host_mapped_matches_device_step(bits):
+    """kvq_decode_step_host with KVQ_STEP_HOST_MAPPED: the step reads the pinned
+    input block and writes the pinned output in place (no copies, no device
+    staging), back to back with the early-read flag; identical cache bytes to
+    kvq_decode_step on a twin, both outputs within tolerance of the oracle."""
+    rng = np.random.default_rng(950 + bits)
+    B, H, d, gq, Nr, L = 2, 2, 128, 4, 16, 700
+    k = torch.from_numpy(rng.standard_normal((B, H, L, d)).astype(np.float16))
+    v = torch.from_numpy(rng.standard_normal((B, H, L, d)).astype(np.float16))
+    lens = torch.tensor([L, L - 91], dtype=torch.int32)
+    a, b = gpu_cache(B, H, d, bits, L + 16, Nr), gpu_cache(B, H, d, bits, L + 16, Nr)
+    for c in (a, b):
+        kvq.kvq_quantize_pack(c, k.to(DEV), v.to(DEV), lens.to(DEV))
+    r = ref_cache(B, H, d, bits, L + 16, Nr)
+    assert oracle.quantize_pack(r, k.numpy(), v.numpy(), lens.numpy()) == 0
+    ws_a, ws_b = kvq.workspace_for(a, H * gq), kvq.workspace_for(b, H * gq)
+    flags = kvq.KVQ_STEP_HOST_MAPPED | kvq.KVQ_STEP_EARLY_CACHE_READ
+    for _ in range(5):
+        q = rng.standard_normal((B, H * gq, d)).astype(np.float16)
+        kn = rng.standard_normal((B, H, d)).astype(np.float16)
+        vn = rng.standard_normal((B, H, d)).astype(np.float16)
+        in_h = torch.from_numpy(np.concatenate([q.ravel(), kn.ravel(), vn.ravel()])).pin_memory()
+        out_h = torch.full((B, H * gq, d), float("nan"), dtype=torch.float16).pin_memory()
+        kvq.kvq_decode_step_host(a, in_h, H * gq, out_h, None, ws_a, flags=flags)
+        out_b = kvq.kvq_decode_step(b, torch.from_numpy(q).to(DEV), torch.from_numpy(kn).to(DEV),
+                                    torch.from_numpy(vn).to(DEV), workspace=ws_b)
+        torch.cuda.synchronize()
+        assert kvq.kvq_read_error(a)[0] == kvq.KVQ_OK
+        _assert_gpu_caches_equal(a, b)
+        assert oracle.append(r, kn, vn) == 0
+        want = oracle.decode(r, q)
+        assert_attn_close(out_h, want)
+        assert_attn_close(out_b, want)
+
+
+def test_step_host_mapped_rejects_pageable_memory():
+    g = gpu_cache(1, 1, 128, 4, 16, 4)
+    ws = kvq.workspace_for(g, 4)
+    in_h = torch.zeros(4 * 128 + 2 * 128, dtype=torch.float16)  # pageable
+    out_h = torch.zeros(1, 4, 128, dtype=torch.float16).pin_memory()
+    with pytest.raises(kvq.KvqError):
+        kvq.kvq_decode_step_host(g, in_h, 4, out_h, None, ws, flags=kvq.KVQ_STEP_HOST_MAPPED)
