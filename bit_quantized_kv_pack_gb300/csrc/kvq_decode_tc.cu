@@ -986,14 +986,17 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
       __syncwarp();
       if (s_abort) break;
     }
-    __syncthreads();
-    // Copies still in flight (only after an abort) land before the ring is reused.
-    if (threadIdx.x == 0) {
-      for (int st = 0; st < NSTAGE; ++st)
-        if (s_last_tile[st] >= 0)
-          ptx::mbar_wait_bounded(ptx::smem_u32(&full_bar[st]), (s_last_tile[st] / NSTAGE) & 1, wait_ns);
-    }
     __syncthreads();  // the stage ring is idle from here on: reuse it for the merge
+    // Copies still in flight (only after an abort: otherwise every issued tile
+    // was consumed) land before the ring is reused.
+    if (s_abort) {  // CTA-uniform after the barrier
+      if (threadIdx.x == 0) {
+        for (int st = 0; st < NSTAGE; ++st)
+          if (s_last_tile[st] >= 0)
+            ptx::mbar_wait_bounded(ptx::smem_u32(&full_bar[st]), (s_last_tile[st] / NSTAGE) & 1, wait_ns);
+      }
+      __syncthreads();
+    }
     if (s_abort) {
       // a wait ran out: this split contributes nothing (it still takes its
       // ticket below, so the head's merge and the workspace stay consistent)

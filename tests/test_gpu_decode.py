@@ -10,7 +10,8 @@ import torch
 import oracle
 from bit_quantized_kv_pack_gb300 import kvq, synth
 
-from _util import oracle_sequences, per_sequence, assert_attn_close, attn_errors, gpu_cache, ref_cache, to_np
+from _util import (assert_attn_close, assert_cache_equal, attn_errors, gpu_cache, oracle_sequences,
+                   per_sequence, ref_cache, to_np)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
