@@ -35,8 +35,12 @@
 //  * PV:  O^T = c^T (p * scale)^T with V codes read through ldmatrix.trans.
 //    The B operand uses the same column order (2 * query + group bit) with
 //    p * scale of that group, so one MMA serves two groups and each thread
-//    again holds one query.  A ninth MMA accumulates sum p * min_g and sum p
-//    (= l), so O = O_c + sum_g p min_g.
+//    again holds one query.  Another MMA accumulates sum p * min_g and sum p
+//    (= l), so O = O_c + sum_g p min_g.  p and p * scale enter every B operand
+//    as two fp16 parts (the rounded value and the rest), each MMA issued once
+//    per part: one fp16 part alone would carry 11 bits, and an output of
+//    magnitude 8 then moves by up to 2e-3 when one token holds most of the
+//    weight.
 //  * The fp16 tokens -- the residual window, then the attention-sink rows
 //    (InnerQ page section 2.3) -- get splits of their own, 64 rows each (all
 //    loads of a split in one round, tensor cores), so no packed split waits on
@@ -91,7 +95,6 @@ struct Geo {
   static constexpr int VP = 2 * CODE_TILE + PAR_TILE;
   static constexpr int STAGE = 2 * CODE_TILE + 2 * PAR_TILE;  // 20 KB / 12 KB
   static constexpr int NSTAGE = BITS == 2 ? 5 : 3;  // 60 KB (INT4, INT2) / 48 KB (INT3) in flight
-  static constexpr float CENTER = BITS == 4 ? 7.5f : (BITS == 3 ? 3.5f : 1.5f);  // mid code
   // INT3: per warp 32 widened rows of K and of V, 64 bytes each
   static constexpr int XBUF = BITS == 3 ? NCW * 2 * 32 * 64 : 0;
   static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned");
@@ -239,36 +242,36 @@ __device__ __forceinline__ void qk_subtile(uint32_t kc, int r0, int lane,
   }
 }
 
-// PV of one 16-token sub-tile: O^T += c^T (p * scale)^T, sb[c] += the column
-// sums of p * scale (fragments 0/1: groups 2c / 2c+1 of query t), and the
-// min/scale/l MMA.
+// PV of one 16-token sub-tile: O^T += c^T (p * scale)^T, and the min/l MMA.
 // pb0/pb1 are the sub-tile's p as B fragments (column n -> query n / 2, tokens
-// 2t, 2t+1 and 2t+8, 2t+9).  The B operand of a code MMA scales column n by
-// the scale of group base + (n & 1), so rows of group base + 1 are right in the
-// odd columns and rows of group base in the even ones.
+// 2t, 2t+1 and 2t+8, 2t+9), rounded to fp16, and pl0/pl1 the rest of p
+// (p - pb, rounded to fp16): p is used as the sum of the two, so the weights
+// carry about 22 bits.  The B operand of a code MMA scales column n by the
+// scale of group base + (n & 1), so rows of group base + 1 are right in the
+// odd columns and rows of group base in the even ones.  p * scale goes in as
+// the same two parts: the fp16 product and what its rounding dropped plus
+// p_lo * scale, each code MMA issued once per part into the same accumulator.
 //   INT4: oc[Pv][j]: row g = dim 64Pv + 4g + j (group 2Pv, fragment 0), row
 //         g+8 = dim 64Pv + 32 + 4g + j (group 2Pv+1, fragment 3).
 //   INT2: oc[c][pp]: rows g / g+8 = dims 64c + 8g + 2pp / +1, group 2c + g/4
 //         (fragments 0, 2 for g < 4; 1, 3 for g >= 4).
 template <int BITS>
 __device__ __forceinline__ void pv_subtile(uint32_t vc, const uint32_t* vp, int r0, int lane,
-                                           uint32_t pb0, uint32_t pb1, float (&oc)[2][4][4],
-                                           float (&sb)[2][4], float (&mnacc)[4]) {
+                                           uint32_t pb0, uint32_t pb1, uint32_t pl0, uint32_t pl1,
+                                           float (&oc)[2][4][4], float (&mnacc)[4]) {
   const int g = lane >> 2, t = lane & 3;
   const int mj = lane >> 3, mi = lane & 7;
   const int lrow = r0 + (mj & 1) * 8 + mi;
   const int ra = r0 + 2 * t, rb = r0 + 2 * t + 8;  // this thread's B rows: ra, ra+1, rb, rb+1
   {
-    // A rows 0-3 = min of group g, rows 4-7 = scale of group g - 4, row 8 =
-    // ones, others zero; B = p
+    // A rows 0-3 = min of group g, row 8 = ones, others zero; B = p (both parts)
     const int xg = g & 3;
-    const uint32_t hsel = g < 4 ? 0x7632u : 0x5410u;
-    const uint32_t am0 = ptx::prmt(vp[ra * NG + xg], vp[(ra + 1) * NG + xg], hsel);
-    const uint32_t am2 = ptx::prmt(vp[rb * NG + xg], vp[(rb + 1) * NG + xg], hsel);
+    const uint32_t am0 = g < 4 ? ptx::prmt(vp[ra * NG + xg], vp[(ra + 1) * NG + xg], 0x7632u) : 0u;
+    const uint32_t am2 = g < 4 ? ptx::prmt(vp[rb * NG + xg], vp[(rb + 1) * NG + xg], 0x7632u) : 0u;
     const uint32_t ones = g == 0 ? 0x3C003C00u : 0u;
     ptx::mma_16816(mnacc, am0, ones, am2, ones, pb0, pb1);
+    ptx::mma_16816(mnacc, am0, ones, am2, ones, pl0, pl1);
   }
-  constexpr uint32_t kOnes = 0x3C003C00u;
   const int gb = g & 1;
   // INT2: w2[2c]/w2[2c+1] = tokens (2t, 2t+1) / (2t+8, 2t+9), dims 64c + 8g .. +7
   uint32_t w2[4];
@@ -279,14 +282,16 @@ __device__ __forceinline__ void pv_subtile(uint32_t vc, const uint32_t* vp, int 
   }
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
-    // p * scale of group 2c + (n & 1) for this thread's column n = g
+    // p * scale of group 2c + (n & 1) for this thread's column n = g: the
+    // rounded product of the fp16 parts, then (exact fma) what that rounding
+    // dropped, plus p_lo * scale
     const int x = 2 * c + gb;
-    const uint32_t bs0 = ptx::hmul2_u32(pb0, ptx::prmt(vp[ra * NG + x], vp[(ra + 1) * NG + x], 0x5410u));
-    const uint32_t bs1 = ptx::hmul2_u32(pb1, ptx::prmt(vp[rb * NG + x], vp[(rb + 1) * NG + x], 0x5410u));
-    // the same rounded p * scale summed over the tokens (all-ones A): lets the
-    // epilogue centre the codes, so the fp16 rounding of p * scale meets
-    // |c - mid| rather than c
-    ptx::mma_16816(sb[c], kOnes, kOnes, kOnes, kOnes, bs0, bs1);
+    const uint32_t sc0 = ptx::prmt(vp[ra * NG + x], vp[(ra + 1) * NG + x], 0x5410u);
+    const uint32_t sc1 = ptx::prmt(vp[rb * NG + x], vp[(rb + 1) * NG + x], 0x5410u);
+    const uint32_t bs0 = ptx::hmul2_rn_u32(pb0, sc0);
+    const uint32_t bs1 = ptx::hmul2_rn_u32(pb1, sc1);
+    const uint32_t bl0 = ptx::hfma2_u32(pl0, sc0, ptx::hfma2_sub_u32(pb0, sc0, bs0));
+    const uint32_t bl1 = ptx::hfma2_u32(pl1, sc1, ptx::hfma2_sub_u32(pb1, sc1, bs1));
     if (BITS == 4) {
       // w[0]/w[1]: group 2c, tokens (2t, 2t+1) / (2t+8, 2t+9), dims 4g..4g+3;
       // w[2]/w[3]: the same for group 2c+1
@@ -301,6 +306,8 @@ __device__ __forceinline__ void pv_subtile(uint32_t vc, const uint32_t* vp, int 
       split_int4(w[3], s3);
 #pragma unroll
       for (int j = 0; j < 4; ++j) ptx::mma_16816(oc[c][j], s0[j], s2[j], s1[j], s3[j], bs0, bs1);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) ptx::mma_16816(oc[c][j], s0[j], s2[j], s1[j], s3[j], bl0, bl1);
     } else {
       uint32_t lo[8], hi[8];
       split_int2(w2[2 * c], lo);
@@ -308,6 +315,9 @@ __device__ __forceinline__ void pv_subtile(uint32_t vc, const uint32_t* vp, int 
 #pragma unroll
       for (int pp = 0; pp < 4; ++pp)
         ptx::mma_16816(oc[c][pp], lo[2 * pp], lo[2 * pp + 1], hi[2 * pp], hi[2 * pp + 1], bs0, bs1);
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp)
+        ptx::mma_16816(oc[c][pp], lo[2 * pp], lo[2 * pp + 1], hi[2 * pp], hi[2 * pp + 1], bl0, bl1);
     }
   }
 }
@@ -402,15 +412,25 @@ __device__ __forceinline__ void residual_tc(const F16Rows& fr, int c0, uint8_t* 
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
   const float mu = m == -INFINITY ? 0.f : m;
-  const uint32_t pk = ptx::pack_h2(exp2f(s0 - mu), exp2f(s1 - mu));
-  const uint32_t x0 = __shfl_sync(0xffffffffu, pk, (2 * t) * 4 + (g >> 1));
-  const uint32_t x1 = __shfl_sync(0xffffffffu, pk, (2 * t + 1) * 4 + (g >> 1));
+  // p in two fp16 parts (rounded, and the rest), used as their sum
+  const float p0 = exp2f(s0 - mu), p1 = exp2f(s1 - mu);
+  const uint32_t pk = ptx::pack_h2(p0, p1);
+  const uint32_t pkl = ptx::pack_h2(p0 - half_lo(pk), p1 - half_hi(pk));
+  const int srcA = (2 * t) * 4 + (g >> 1), srcB = (2 * t + 1) * 4 + (g >> 1);
+  const uint32_t x0 = __shfl_sync(0xffffffffu, pk, srcA);
+  const uint32_t x1 = __shfl_sync(0xffffffffu, pk, srcB);
+  const uint32_t y0 = __shfl_sync(0xffffffffu, pkl, srcA);
+  const uint32_t y1 = __shfl_sync(0xffffffffu, pkl, srcB);
   const uint32_t pb0 = ptx::prmt(x0, x1, 0x5410u);  // tokens 2t, 2t+1 of query g / 2
   const uint32_t pb1 = ptx::prmt(x0, x1, 0x7632u);  // tokens 2t+8, 2t+9
-  // ---- O^T = V^T p^T, one MMA per 16 head_dim values; l = sum of the same p
+  const uint32_t pl0 = ptx::prmt(y0, y1, 0x5410u);
+  const uint32_t pl1 = ptx::prmt(y0, y1, 0x7632u);
+  // ---- O^T = V^T p^T, two MMAs (the parts of p) per 16 head_dim values; l =
+  // sum of the same p
   float lacc[4] = {0.f, 0.f, 0.f, 0.f};
   constexpr uint32_t kOnes = 0x3C003C00u;
   ptx::mma_16816(lacc, kOnes, kOnes, kOnes, kOnes, pb0, pb1);
+  ptx::mma_16816(lacc, kOnes, kOnes, kOnes, kOnes, pl0, pl1);
   const uint32_t vbase = tbase + kResRows * kResStride;
 #pragma unroll
   for (int mb = 0; mb < D / 16; ++mb) {
@@ -421,6 +441,7 @@ __device__ __forceinline__ void residual_tc(const F16Rows& fr, int c0, uint8_t* 
     ptx::ldmatrix_x4_trans(addr, v0, v1, v2, v3);
     float o[4] = {0.f, 0.f, 0.f, 0.f};
     ptx::mma_16816(o, v0, v1, v2, v3, pb0, pb1);
+    ptx::mma_16816(o, v0, v1, v2, v3, pl0, pl1);
     ms.o[warp][t][16 * mb + g] = o[0];
     ms.o[warp][t][16 * mb + g + 8] = o[2];
   }
@@ -797,12 +818,7 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
 
     float m_ref = -INFINITY;  // running max of query t, log2 units
     float oc[2][4][4];        // O^T accumulators (layout at pv_subtile), times 2^-24
-    float mnacc[4];           // C-fragment of the min/scale/l MMA
-    float sb[2][4];           // column sums of the rounded p * scale (pv_subtile)
-#pragma unroll
-    for (int c = 0; c < 2; ++c)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) sb[c][r] = 0.f;
+    float mnacc[4];           // C-fragment of the min/l MMA
 #pragma unroll
     for (int x = 0; x < 2; ++x)
 #pragma unroll
@@ -941,11 +957,7 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
 #pragma unroll
               for (int r = 0; r < 4; ++r) oc[x][m][r] *= al;
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            mnacc[r] *= al;
-            sb[0][r] *= al;
-            sb[1][r] *= al;
-          }
+          for (int r = 0; r < 4; ++r) mnacc[r] *= al;
         }
         if (tile == 0 && warp == 0 && lane < QB) {
           ref_mine = m_ref;
@@ -953,19 +965,26 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
           ref_offered = true;
         }
         const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-        // p as the PV B fragment: thread (g, t) needs p(query g / 2, tokens 2t,
-        // 2t+1, 2t+8, 2t+9); lane 4 * token + query holds that query for rows
-        // token and token + 8 of the sub-tile
+        // p as the PV B fragments, in two fp16 parts (p rounded, and the rest):
+        // thread (g, t) needs p(query g / 2, tokens 2t, 2t+1, 2t+8, 2t+9); lane
+        // 4 * token + query holds that query for rows token and token + 8 of the
+        // sub-tile
         const int srcA = (2 * t) * 4 + (g >> 1);
         const int srcB = (2 * t + 1) * 4 + (g >> 1);
 #pragma unroll
         for (int u = 0; u < NSUB; ++u) {
-          const uint32_t pk = ptx::pack_h2(exp2f(fmaf(sv[u][0], kq24, -mu)), exp2f(fmaf(sv[u][1], kq24, -mu)));
+          const float p0 = exp2f(fmaf(sv[u][0], kq24, -mu)), p1 = exp2f(fmaf(sv[u][1], kq24, -mu));
+          const uint32_t pk = ptx::pack_h2(p0, p1);
+          const uint32_t pkl = ptx::pack_h2(p0 - half_lo(pk), p1 - half_hi(pk));  // exact differences
           const uint32_t x0 = __shfl_sync(0xffffffffu, pk, srcA);  // (p(2t), p(2t+8))
           const uint32_t x1 = __shfl_sync(0xffffffffu, pk, srcB);  // (p(2t+1), p(2t+9))
+          const uint32_t y0 = __shfl_sync(0xffffffffu, pkl, srcA);
+          const uint32_t y1 = __shfl_sync(0xffffffffu, pkl, srcB);
           const uint32_t pb0 = ptx::prmt(x0, x1, 0x5410u);  // tokens 2t, 2t+1
           const uint32_t pb1 = ptx::prmt(x0, x1, 0x7632u);  // tokens 2t+8, 2t+9
-          pv_subtile<G::CB>(vc, vp, crow + 16 * u, lane, pb0, pb1, oc, sb, mnacc);
+          const uint32_t pl0 = ptx::prmt(y0, y1, 0x5410u);
+          const uint32_t pl1 = ptx::prmt(y0, y1, 0x7632u);
+          pv_subtile<G::CB>(vc, vp, crow + 16 * u, lane, pb0, pb1, pl0, pl1, oc, mnacc);
         }
       }
       __syncwarp();
@@ -1008,21 +1027,12 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
 #pragma unroll
           for (int r = 0; r < 4; ++r) oc[x][m][r] = 0.f;
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        mnacc[r] = 0.f;
-        sb[0][r] = 0.f;
-        sb[1][r] = 0.f;
-      }
+      for (int r = 0; r < 4; ++r) mnacc[r] = 0.f;
     }
     if (ref_offered) s_ref[lane] = ref_cas == 0u ? __float_as_uint(ref_mine) + 1u : ref_cas;
-    // per group x and query t, corr_x = sum p min_x + mid (sum p scale_x -
-    // sum of the rounded p * scale_x), to shared memory first; then the outputs
-    // O = 2^24 oc / weight + corr (the layout is at pv_subtile)
-    {
-      const float psc = __shfl_down_sync(0xffffffffu, mnacc[0], 16);  // lane g + 4: sum p scale_g
-      const float sbx = (g & 2) ? ((g & 1) ? sb[1][1] : sb[1][0]) : ((g & 1) ? sb[0][1] : sb[0][0]);
-      if (g < 4) ms.mn[warp][g][t] = fmaf(G::CENTER, psc - sbx, mnacc[0]);
-    }
+    // per group x and query t, sum p min_x to shared memory first; then the
+    // outputs O = 2^24 oc / weight + sum p min (the layout is at pv_subtile)
+    if (g < 4) ms.mn[warp][g][t] = mnacc[0];
     if (g == 0) {
       ms.l[warp][t] = mnacc[2];
       ms.m[warp][t] = m_ref;

@@ -180,8 +180,19 @@ __device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
 __device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
   return h2_as_u32(__hfma2(u32_as_h2(a), u32_as_h2(b), u32_as_h2(c)));
 }
-__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
-  return h2_as_u32(__hmul2(u32_as_h2(a), u32_as_h2(b)));
+// a * b rounded to fp16; the explicit rounding mode keeps it from being fused
+// with a later addition
+__device__ __forceinline__ uint32_t hmul2_rn_u32(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// a * b - c with one rounding
+__device__ __forceinline__ uint32_t hfma2_sub_u32(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("{\n\t.reg .b32 n;\n\tneg.f16x2 n, %3;\n\tfma.rn.f16x2 %0, %1, %2, n;\n\t}"
+      : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
 }
 // two floats -> half2 (low = lo), round to nearest even
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {

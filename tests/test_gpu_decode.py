@@ -162,26 +162,28 @@ def test_decode_far_max_takes_exact_merge(bits):
     assert_attn_close(kvq.kvq_decode_attention(g, q2.to(DEV)), oracle.decode(r, q2.numpy()))
 
 
-def _with_outliers(rng, shape):
-    """N(0, 1) with 1% of the elements replaced by N(0, 8^2): workload 4's recipe."""
+def _with_outliers(rng, shape, p=0.01):
+    """N(0, 1) with a fraction p (1%: workload 4's recipe) of the elements
+    replaced by N(0, 8^2)."""
     x = rng.standard_normal(shape)
-    x = np.where(rng.random(shape) < 0.01, rng.standard_normal(shape) * 8.0, x)
+    x = np.where(rng.random(shape) < p, rng.standard_normal(shape) * 8.0, x)
     return torch.from_numpy(x.astype(np.float16))
 
 
+@pytest.mark.parametrize("bits", [4, 2])
 @pytest.mark.parametrize("d,gq", [(128, 4), (64, 2), (128, 8)])
-def test_decode_fp32_output(d, gq):
+def test_decode_fp32_output(bits, d, gq):
     """KVQ_OUT_F32: the same decode written as fp32, on outlier data with sharp
     attention (|O| up to about 13, where the fp16 spacing is 2^-7).  Against the
     oracle with the flat max-abs bar, which fp16 output alone can miss there.  On
     the generic kernel (deterministic) rounding the fp32 output to fp16 gives the
     fp16 output bit for bit; the allocation-free entry point writes fp32 too."""
-    rng = np.random.default_rng(d * 10 + gq)
+    rng = np.random.default_rng(d * 10 + gq + bits)
     B, H, Nr = 2, 2, 16
     lens = torch.tensor([900, 50], dtype=torch.int32)
     k, v = _with_outliers(rng, (B, H, 900, d)), _with_outliers(rng, (B, H, 900, d))
     q = torch.from_numpy((rng.standard_normal((B, H * gq, d)) * 2).astype(np.float16))
-    g, r = _setup(k, v, lens, 4, 900, Nr)
+    g, r = _setup(k, v, lens, bits, 900, Nr)
     want = oracle.decode(r, q.numpy())
     assert np.abs(want).max() > 2
     out32 = kvq.kvq_decode_attention(g, q.to(DEV), flags=kvq.KVQ_OUT_F32)

@@ -256,3 +256,40 @@ def test_step_host_mapped_rejects_pageable_memory():
     out_h = torch.zeros(1, 4, 128, dtype=torch.float16).pin_memory()
     with pytest.raises(kvq.KvqError):
         kvq.kvq_decode_step_host(g, in_h, 4, out_h, None, ws, flags=kvq.KVQ_STEP_HOST_MAPPED)
+
+
+def _outliers(rng, shape, p):
+    x = rng.standard_normal(shape)
+    x = np.where(rng.random(shape) < p, rng.standard_normal(shape) * 8.0, x)
+    return torch.from_numpy(x.astype(np.float16))
+
+
+@pytest.mark.parametrize("hybrid", [0, 1])
+@pytest.mark.parametrize("bits,Nr", [(2, 0), (2, 16), (4, 0)])
+def test_step_heavy_outliers_fp32(bits, Nr, hybrid):
+    """INT2 and INT4 caches whose groups are often hit by N(0, 8^2) outliers (3%
+    of the prefill, 10% of each new token), so group scales reach ~13 (INT2)
+    and single tokens with outlier values take most of the weight: 20 fused
+    steps with fp32 output, every element within the flat 2e-3 of the oracle
+    (weights in fp16 alone would miss it there)."""
+    rng = np.random.default_rng(bits * 31 + Nr + hybrid)
+    B, H, d, gq, L = 2, 2, 128, 4, 600
+    k, v = _outliers(rng, (B, H, L, d), 0.03), _outliers(rng, (B, H, L, d), 0.03)
+    lens = torch.tensor([L, 200], dtype=torch.int32)
+    cap = L + 32
+    g = gpu_cache(B, H, d, bits, cap, Nr, hybrid=hybrid)
+    kvq.kvq_quantize_pack(g, k.to(DEV), v.to(DEV), lens.to(DEV))
+    r = ref_cache(B, H, d, bits, cap, Nr, hybrid=hybrid)
+    assert oracle.quantize_pack(r, to_np(k), to_np(v), to_np(lens)) == 0
+    ws = kvq.workspace_for(g, H * gq)
+    worst = 0.0
+    for _ in range(20):
+        kn, vn = _outliers(rng, (B, H, d), 0.1), _outliers(rng, (B, H, d), 0.1)
+        q = torch.from_numpy((rng.standard_normal((B, H * gq, d)) * 2).astype(np.float16))
+        out = torch.empty(q.shape, dtype=torch.float32, device=DEV)
+        kvq.kvq_decode_step(g, q.to(DEV), kn.to(DEV), vn.to(DEV), out, ws)
+        assert kvq.kvq_read_error(g)[0] == kvq.KVQ_OK
+        assert oracle.append(r, kn.numpy(), vn.numpy()) == 0
+        worst = max(worst, assert_attn_close(out, oracle.decode(r, q.numpy()))[0])
+    assert_cache_equal(g, r)
+    print(f"INT{bits} Nr {Nr} hybrid {hybrid}: worst max abs {worst:.2e}")
