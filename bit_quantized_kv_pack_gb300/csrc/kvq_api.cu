@@ -269,7 +269,7 @@ const char* kvq_status_string(kvq_status status) {
   }
 }
 
-int32_t kvq_version(void) { return 150; }
+int32_t kvq_version(void) { return 160; }
 
 void kvq_testing_wait_fault(uint32_t limit_us) { kvq::set_testing_wait_fault_us(limit_us); }
 

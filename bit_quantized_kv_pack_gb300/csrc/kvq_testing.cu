@@ -1,5 +1,6 @@
 // kvq_testing.cu -- exhaustive checks of the quantizer's fast arithmetic
-// against the IEEE operations it stands in for (testing hook, see kvq.h).
+// against the IEEE operations it stands in for, and a measurement of how the
+// tensor cores' f16 -> f32 MMA rounds (testing hooks, see kvq.h).
 //
 //  * div_by_const<K> (Markstein's corrected product by the reciprocal) against
 //    __fdiv_rn(d, K) for every non-negative finite float d, K = 15, 7, 3;
@@ -10,6 +11,7 @@
 #include <string.h>
 
 #include "kvq_internal.cuh"
+#include "kvq_ptx.cuh"
 
 namespace kvq {
 namespace {
@@ -43,6 +45,44 @@ __global__ void check_rcp_kernel(unsigned long long* worst_bits) {
 // The counts (a static device array: the check allocates nothing).
 __device__ unsigned long long g_check_counts[7];
 
+// One mma.sync m16n8k16 (f16 operands, f32 accumulate) per case: C = c0 plus
+// products k = 0 -> big, k = 1..15 -> small (as 2^-12 * (small * 2^12), all
+// fp16-exact).  Every row and column of the result is the same; lane 0 writes
+// element (0, 0).
+constexpr int kMmaCases = 8;
+__device__ float g_mma_out[kMmaCases];
+__constant__ float kMmaSmall[kMmaCases] = {0.5f, 0.25f, 0.125f, 0.0625f, 0.5f, 0.25f, -0.5f, -0.25f};
+__constant__ float kMmaC0[kMmaCases] = {0.f, 0.f, 0.f, 0.f, 1.f, 1.f, 0.f, 0.f};
+__constant__ float kMmaBig[kMmaCases] = {1.f, 1.f, 1.f, 1.f, 0.f, 0.f, 1.f, 1.f};
+
+__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__global__ void mma_rounding_kernel() {
+  const int t = threadIdx.x & 3;
+  const float ulp1 = 1.f / 8388608.f;  // 2^-23, the spacing of floats at 1
+  for (int cs = 0; cs < kMmaCases; ++cs) {
+    float av[16], bv[16];
+    for (int k = 0; k < 16; ++k) {
+      av[k] = 1.f / 4096.f;
+      bv[k] = kMmaSmall[cs] * ulp1 * 4096.f;
+    }
+    av[0] = 1.f;
+    bv[0] = kMmaBig[cs];
+    // A fragment (row g; k 2t, 2t+1 | 2t+8, 2t+9), the same for rows g + 8;
+    // B fragment (k 2t, 2t+1 | 2t+8, 2t+9; column g)
+    const uint32_t a0 = pack_f16x2(av[2 * t], av[2 * t + 1]);
+    const uint32_t a2 = pack_f16x2(av[2 * t + 8], av[2 * t + 9]);
+    const uint32_t b0 = pack_f16x2(bv[2 * t], bv[2 * t + 1]);
+    const uint32_t b1 = pack_f16x2(bv[2 * t + 8], bv[2 * t + 9]);
+    float c[4] = {kMmaC0[cs], kMmaC0[cs], kMmaC0[cs], kMmaC0[cs]};
+    ptx::mma_16816(c, a0, a0, a2, a2, b0, b1);
+    if (threadIdx.x == 0) g_mma_out[cs] = c[0];
+  }
+}
+
 }  // namespace
 }  // namespace kvq
 
@@ -68,4 +108,12 @@ extern "C" kvq_status kvq_testing_check_arithmetic(uint64_t* div_mismatches, dou
   for (int i = 0; i < 6; ++i) div_mismatches[i] = h[i];
   memcpy(rcp_worst_rel, &h[6], sizeof(double));
   return KVQ_OK;
+}
+
+extern "C" kvq_status kvq_testing_mma_rounding(float* out, int32_t n) {
+  if (!out || n < 0 || n > kvq::kMmaCases) return KVQ_ERR_INVALID_ARG;
+  kvq::mma_rounding_kernel<<<1, 32>>>();
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(out, kvq::g_mma_out, n * sizeof(float));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

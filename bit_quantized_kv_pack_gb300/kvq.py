@@ -46,7 +46,7 @@ EXPORTS = ("kvq_cache_bytes", "kvq_decode_workspace_bytes", "kvq_quantize_pack",
            "kvq_decode_attention", "kvq_decode_step", "kvq_decode_step_host", "kvq_step_io_bytes",
            "kvq_decode_attention_noalloc",
            "kvq_read_error", "kvq_status_string", "kvq_version", "kvq_testing_wait_fault",
-           "kvq_testing_check_arithmetic")
+           "kvq_testing_check_arithmetic", "kvq_testing_mma_rounding")
 
 
 class CacheDesc(ctypes.Structure):
@@ -121,6 +121,8 @@ def load(path: str | None = None):
             lib.kvq_testing_check_arithmetic.argtypes = [ctypes.POINTER(ctypes.c_uint64),
                                                          ctypes.POINTER(ctypes.c_double)]
             lib.kvq_testing_check_arithmetic.restype = ctypes.c_int
+            lib.kvq_testing_mma_rounding.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int32]
+            lib.kvq_testing_mma_rounding.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -424,3 +426,10 @@ def kvq_testing_check_arithmetic():
     _check(load().kvq_testing_check_arithmetic(mm, ctypes.byref(worst)),
            "kvq_testing_check_arithmetic")
     return [(int(mm[2 * i]), int(mm[2 * i + 1])) for i in range(3)], worst.value
+
+
+def kvq_testing_mma_rounding(n: int = 8):
+    """Testing hook (see kvq.h): the eight MMA rounding cases' results."""
+    out = (ctypes.c_float * 8)()
+    _check(load().kvq_testing_mma_rounding(out, int(n)), "kvq_testing_mma_rounding")
+    return [float(out[i]) for i in range(n)]

@@ -374,7 +374,8 @@ kvq_status kvq_read_error(const kvq_cache_view* view, uint32_t* word_out, void* 
 const char* kvq_status_string(kvq_status status);
 
 /* Library version as 10000 * major + 100 * minor + patch. */
-int32_t kvq_version(void); /* 150: timeout testing hook, cached tensor maps; 140: paged caches;
+int32_t kvq_version(void); /* 160: two-part weights in the tensor-core MMAs, MMA rounding hook;
+                              150: timeout testing hook, cached tensor maps; 140: paged caches;
                               130: 3-bit; 120: hybrid; 110: sink, fp32 out */
 
 /* Testing hook, for checking the bounded-wait error path without faulting the
@@ -400,6 +401,16 @@ void kvq_testing_wait_fault(uint32_t limit_us);
  * rcp_worst_rel: the largest relative error of the reciprocal used for the codes,
  * over every positive finite fp16 scale.  Synchronous (legacy default stream). */
 kvq_status kvq_testing_check_arithmetic(uint64_t* div_mismatches, double* rcp_worst_rel);
+
+/* Testing hook (no passage of the pages corresponds to it): how the tensor
+ * cores round the f16 -> f32 MMA that the decode kernel's contractions use.
+ * Runs eight fixed cases of one mma.sync m16n8k16, each C = c0 plus one product
+ * `big` and fifteen products `small` (small in units of the float spacing at 1,
+ * 2^-23): (c0, big, small) = (0, 1, 1/2), (0, 1, 1/4), (0, 1, 1/8),
+ * (0, 1, 1/16), (1, 0, 1/2), (1, 0, 1/4), (0, 1, -1/2), (0, 1, -1/4), and
+ * writes the first n (<= 8) results to the host array out.  Synchronous (legacy
+ * default stream).  KVQ_ERR_INVALID_ARG for a null out or n outside 0..8. */
+kvq_status kvq_testing_mma_rounding(float* out, int32_t n);
 
 #ifdef __cplusplus
 }

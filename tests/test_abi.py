@@ -30,7 +30,7 @@ def test_header_declares_and_library_exports(lib):
     assert set(kvq.EXPORTS) <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in kvq.h but not exported"
-    assert kvq.kvq_version() == 150
+    assert kvq.kvq_version() == 160
 
 
 def test_status_strings(lib):

@@ -1,5 +1,6 @@
 """The quantizer's fast arithmetic against the IEEE operations it replaces,
-checked exhaustively on the GPU through the library's testing hook:
+checked exhaustively on the GPU through the library's testing hook, and the
+tensor cores' MMA rounding that bounds the decode kernel's precision:
 
   * the scale (max - min) / (2^b - 1) by Markstein's corrected product by the
     reciprocal must equal the IEEE divide for every float of the quantizer's
@@ -24,3 +25,21 @@ def test_constant_division_and_reciprocal_are_exact_enough():
               f"{domain} in the quantizer's domain")
         assert domain == 0, (k, all_floats, domain)
     assert rcp_worst <= 2.0 ** -22, rcp_worst
+
+
+def test_mma_rounding_truncates_at_a_quarter_ulp():
+    """How the f16 -> f32 MMA rounds, measured through the testing hook: the
+    products and C are aligned to the largest term, bits below a quarter of
+    that term's float spacing are dropped, and the sum is truncated toward
+    zero.  So one MMA can be off by up to (terms / 4 + 1) spacings of its
+    largest term, always toward zero, and a chain of MMAs into one accumulator
+    adds those errors up; the decode kernel's precision argument rests on
+    this (it is not round-to-nearest)."""
+    u = 2.0 ** -23  # float spacing at 1
+    got = [(x - 1.0) / u for x in kvq.kvq_testing_mma_rounding()]
+    # (c0, big, small): 15 x 1/2 -> 7 (7.5 truncated); 15 x 1/4 -> 3 (3.75
+    # truncated); 15 x 1/8 and 15 x 1/16 -> 0 (each product dropped); the same
+    # with C = 1 in place of the product 1; below 1 the spacing is 2^-24, so
+    # 1 - 7.5 * 2^-23 is exact and 1 - 3.75 * 2^-23 truncates (toward zero) to
+    # 1 - 4 * 2^-23
+    assert got == [7.0, 3.0, 0.0, 0.0, 7.0, 3.0, -7.5, -4.0], got
