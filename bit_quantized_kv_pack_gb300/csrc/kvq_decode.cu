@@ -45,13 +45,22 @@ DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count, b
   DecodePlan p;
   p.gq = num_q_heads / D.num_kv_heads;
   int64_t target, min_tokens;
+  p.cps = 0;
   if (tc_supported(D, p.gq)) {
-    // tensor-core kernel: 4 query heads per CTA, one wave of resident CTAs
+    // tensor-core kernel: 4 query heads per CTA, one wave of resident CTAs.
+    // When even one packed split per (sequence, KV head) plus its fp16 splits
+    // fills more than a wave, the grid runs in several waves anyway and takes
+    // the 4-CTAs-per-SM variant.
     p.kernel = 1;
     p.qb = 4;
     p.nqb = 1;
     p.threads = tc_threads();
-    target = (int64_t)sm_count * tc_ctas_per_sm();
+    const int64_t units1 = (int64_t)D.batch * D.num_kv_heads;
+    const int64_t fp16_splits = (D.residual + D.sink + tc_residual_rows() - 1) / tc_residual_rows();
+    const bool waves = units1 * (1 + (fp16_splits > 0 ? fp16_splits : (step ? 1 : 0))) >
+                       (int64_t)sm_count * tc_ctas_per_sm(false);
+    p.cps = tc_ctas_per_sm(waves);
+    target = (int64_t)sm_count * p.cps;
     min_tokens = 256;
   } else {
     p.kernel = 0;

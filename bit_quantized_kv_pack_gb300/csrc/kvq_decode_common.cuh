@@ -109,7 +109,7 @@ __device__ __forceinline__ void split_range(int Lp, int Lr, int s, int S, int64_
 // Tensor-core kernel: head_dim 128, 1 <= gq <= 4 (kvq_decode_tc.cu).
 bool tc_supported(const kvq_cache_desc& D, int gq);
 int tc_threads();
-int tc_ctas_per_sm();
+int tc_ctas_per_sm(bool several_waves);  // resident CTAs per SM of the variant launched
 int tc_residual_rows();
 cudaError_t launch_decode_tc(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
                              cudaStream_t st, bool step);

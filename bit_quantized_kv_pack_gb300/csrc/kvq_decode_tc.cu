@@ -80,10 +80,13 @@ constexpr int T = 128;          // tokens per pipeline stage
 constexpr int NCW = 4;          // warps, 32 tokens (two 16-token sub-tiles) each per stage
 constexpr int NSUB = 2;         // sub-tiles per warp per stage
 constexpr int NTHREADS = NCW * 32;
-constexpr int kCtasPerSm = 3;   // 12 warps per SM: 168 registers, ~62 KB of shared memory each
+// CTAs per SM (CPS, a template parameter): 3 (12 warps, up to 168 registers,
+// ~62 KB of shared memory each) for grids of one wave; 4 (16 warps, 128
+// registers, a shorter ring) for grids of several waves, where more warps hide
+// more latency and the ramp of each CTA is overlapped by the others.
 static_assert(NCW == QB, "the merge gives each warp one query");
 
-template <int BITS>
+template <int BITS, int CPS>
 struct Geo {
   static constexpr int CB = BITS == 3 ? 4 : BITS;  // code width of the arithmetic
   static constexpr int RB = D * BITS / 8;      // code bytes per token row
@@ -94,7 +97,8 @@ struct Geo {
   static constexpr int KP = 2 * CODE_TILE;
   static constexpr int VP = 2 * CODE_TILE + PAR_TILE;
   static constexpr int STAGE = 2 * CODE_TILE + 2 * PAR_TILE;  // 20 KB / 12 KB
-  static constexpr int NSTAGE = BITS == 2 ? 5 : 3;  // 60 KB (INT4, INT2) / 48 KB (INT3) in flight
+  // 60 KB (INT4, INT2) / 48 KB (INT3) in flight at 3 CTAs per SM; 40 / 48 / 32 KB at 4
+  static constexpr int NSTAGE = CPS == 4 ? (BITS == 2 ? 4 : 2) : (BITS == 2 ? 5 : 3);
   // INT3: per warp 32 widened rows of K and of V, 64 bytes each
   static constexpr int XBUF = BITS == 3 ? NCW * 2 * 32 * 64 : 0;
   static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned");
@@ -112,9 +116,10 @@ struct MergeSmem {
 // residual split's K and V rows overlap the stage ring (residual splits never
 // use the ring; packed splits reuse it for the merge once it is idle).
 constexpr size_t kResTilesOff = (sizeof(MergeSmem) + 4 * D * sizeof(float) + 127) & ~(size_t)127;
-template <int BITS>
+template <int BITS, int CPS>
 constexpr size_t tc_smem_bytes() {
-  constexpr size_t ring = (size_t)Geo<BITS>::NSTAGE * Geo<BITS>::STAGE + Geo<BITS>::XBUF;
+  using G = Geo<BITS, CPS>;
+  constexpr size_t ring = (size_t)G::NSTAGE * G::STAGE + G::XBUF;
   constexpr size_t res = kResTilesOff + 2 * 64 * (2 * D + 16);  // kResRows rows of K and V
   return 1024 + (ring > res ? ring : res);
 }
@@ -467,11 +472,11 @@ __device__ __forceinline__ void residual_tc(const F16Rows& fr, int c0, uint8_t* 
 // slot, and attends over the window without the leaving token plus the new token
 // (fp16) and the quantized one (dequantized in fp32).  The last head of a
 // sequence to finish commits the counters.
-template <int BITS, bool STEP>
-__global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
+template <int BITS, bool STEP, int CPS>
+__global__ void __launch_bounds__(NTHREADS, CPS)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
                      const DecodeArgs a) {
-  using G = Geo<BITS>;
+  using G = Geo<BITS, CPS>;
   constexpr int NSTAGE = G::NSTAGE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -938,14 +943,18 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
           }
         }
 
-        // ---------------- online softmax over the warp's 32 rows (lazy rescale)
-        float mx = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float mloc = mx * kq24;
-        const bool need = mloc > m_ref + 8.f;
-        if (__any_sync(0xffffffffu, need)) {
+        // ---------------- online softmax over the warp's 32 rows (lazy rescale).
+        // The running max of query t moves only when one of its rows lies more
+        // than 8 above it; each thread checks its own rows, and only then does
+        // the warp reduce the max over the lanes of each query.
+        const float mown =
+            fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1])) * kq24;
+        if (__any_sync(0xffffffffu, mown > m_ref + 8.f)) {
+          float mloc = mown;
+          mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 4));
+          mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 8));
+          mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 16));
+          const bool need = mloc > m_ref + 8.f;  // the same for every lane of query t
           const float mnew = need ? mloc : m_ref;
           const float al = need ? exp2f(m_ref - mnew) : 1.f;
           m_ref = mnew;
@@ -973,7 +982,9 @@ __global__ void __launch_bounds__(NTHREADS, kCtasPerSm)
         const int srcB = (2 * t + 1) * 4 + (g >> 1);
 #pragma unroll
         for (int u = 0; u < NSUB; ++u) {
-          const float p0 = exp2f(fmaf(sv[u][0], kq24, -mu)), p1 = exp2f(fmaf(sv[u][1], kq24, -mu));
+          // (weights below 2^-126 of the running max's are flushed to zero)
+          const float p0 = ptx::ex2_ftz(fmaf(sv[u][0], kq24, -mu));
+          const float p1 = ptx::ex2_ftz(fmaf(sv[u][1], kq24, -mu));
           const uint32_t pk = ptx::pack_h2(p0, p1);
           const uint32_t pkl = ptx::pack_h2(p0 - half_lo(pk), p1 - half_hi(pk));  // exact differences
           const uint32_t x0 = __shfl_sync(0xffffffffu, pk, srcA);  // (p(2t), p(2t+8))
@@ -1234,7 +1245,7 @@ bool make_rows_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint6
 
 // Raise the kernel's dynamic shared-memory limit once per device (the attribute
 // is per device; a process may drive several GPUs).
-template <int BITS, bool STEP>
+template <int BITS, bool STEP, int CPS>
 cudaError_t ensure_smem_attr(size_t smem) {
   static std::atomic<uint64_t> done{0};  // bit i: set on device i
   int dev = 0;
@@ -1242,15 +1253,15 @@ cudaError_t ensure_smem_attr(size_t smem) {
   if (e != cudaSuccess) return e;
   const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
   if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
-  e = cudaFuncSetAttribute(decode_tc_kernel<BITS, STEP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(decode_tc_kernel<BITS, STEP, CPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem);
   if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
   return e;
 }
 
-template <int BITS, bool STEP>
+template <int BITS, bool STEP, int CPS>
 cudaError_t launch_bits(const Dims& s, const DecodePlan& p, const DecodeArgs& a, cudaStream_t st) {
-  using Gm = Geo<BITS>;
+  using Gm = Geo<BITS, CPS>;
   // packed rows: every (sequence, head, slot), or every (page, head, slot) of a pool
   const bool paged = s.page != 0;
   const uint64_t rows = paged ? (uint64_t)s.npages * s.Hkv * kPage : (uint64_t)s.B * s.Hkv * s.cap;
@@ -1263,8 +1274,8 @@ cudaError_t launch_bits(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
   if (!make_rows_map(&kc, a.k_codes, Gm::RB, rows, swz, box) ||
       !make_rows_map(&vc, a.v_codes, Gm::RB, rows, swz, box))
     return cudaErrorInvalidValue;
-  constexpr size_t smem = tc_smem_bytes<BITS>();
-  cudaError_t e = ensure_smem_attr<BITS, STEP>(smem);
+  constexpr size_t smem = tc_smem_bytes<BITS, CPS>();
+  cudaError_t e = ensure_smem_attr<BITS, STEP, CPS>(smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.splits, (unsigned)s.Hkv, (unsigned)s.B);
@@ -1276,7 +1287,7 @@ cudaError_t launch_bits(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<BITS, STEP>, kc, vc, a);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<BITS, STEP, CPS>, kc, vc, a);
 }
 
 }  // namespace
@@ -1286,14 +1297,22 @@ bool tc_supported(const kvq_cache_desc& D, int gq) {
 }
 
 int tc_threads() { return NTHREADS; }
-int tc_ctas_per_sm() { return kCtasPerSm; }
+int tc_ctas_per_sm(bool several_waves) { return several_waves ? 4 : 3; }
 int tc_residual_rows() { return kResRows; }
+
+template <int CPS>
+cudaError_t launch_cps(const Dims& s, const DecodePlan& p, const DecodeArgs& a, cudaStream_t st,
+                       bool step) {
+  if (s.bits == 3)
+    return step ? launch_bits<3, true, CPS>(s, p, a, st) : launch_bits<3, false, CPS>(s, p, a, st);
+  if (step)
+    return s.bits == 4 ? launch_bits<4, true, CPS>(s, p, a, st) : launch_bits<2, true, CPS>(s, p, a, st);
+  return s.bits == 4 ? launch_bits<4, false, CPS>(s, p, a, st) : launch_bits<2, false, CPS>(s, p, a, st);
+}
 
 cudaError_t launch_decode_tc(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
                              cudaStream_t st, bool step) {
-  if (s.bits == 3) return step ? launch_bits<3, true>(s, p, a, st) : launch_bits<3, false>(s, p, a, st);
-  if (step) return s.bits == 4 ? launch_bits<4, true>(s, p, a, st) : launch_bits<2, true>(s, p, a, st);
-  return s.bits == 4 ? launch_bits<4, false>(s, p, a, st) : launch_bits<2, false>(s, p, a, st);
+  return p.cps == 4 ? launch_cps<4>(s, p, a, st, step) : launch_cps<3>(s, p, a, st, step);
 }
 
 }  // namespace kvq

@@ -189,40 +189,62 @@ __device__ __forceinline__ float sub_f16_f32(unsigned short h, float f) {
   return d;
 }
 
-template <int BITS>
-__device__ __forceinline__ uint32_t quantize_quad(const uint4& raw, uint32_t& params_out,
-                                                  bool hybrid = false, uint32_t* asym_bit = nullptr) {
-  constexpr int kQmax = (1 << BITS) - 1;
+// Q1 over the lane's 8 values: (min, -max) as one half2.
+__device__ __forceinline__ __half2 lane_min_negmax(const uint4& raw) {
   const __half2* hv = reinterpret_cast<const __half2*>(&raw);
-  // Q1: (min, -max) of the lane's values, then of the quad
-  __half2 lo = __hmin2(__hmin2(hv[0], hv[1]), __hmin2(hv[2], hv[3]));
-  __half2 nhi = __hmin2(__hmin2(__hneg2(hv[0]), __hneg2(hv[1])),
-                        __hmin2(__hneg2(hv[2]), __hneg2(hv[3])));
-  __half2 mm = __halves2half2(__hmin(__low2half(lo), __high2half(lo)),
-                              __hmin(__low2half(nhi), __high2half(nhi)));
+  const __half2 lo = __hmin2(__hmin2(hv[0], hv[1]), __hmin2(hv[2], hv[3]));
+  const __half2 nhi = __hmin2(__hmin2(__hneg2(hv[0]), __hneg2(hv[1])),
+                              __hmin2(__hneg2(hv[2]), __hneg2(hv[3])));
+  return __halves2half2(__hmin(__low2half(lo), __high2half(lo)),
+                        __hmin(__low2half(nhi), __high2half(nhi)));
+}
+// (min, -max) over the `lanes` lanes of a group (shuffle-xor; full mask).
+template <int LANES>
+__device__ __forceinline__ __half2 group_min_negmax(__half2 mm) {
 #pragma unroll
-  for (int o = 1; o <= 2; o <<= 1) {
+  for (int o = 1; o < LANES; o <<= 1) {
     const uint32_t other = __shfl_xor_sync(0xffffffffu, *reinterpret_cast<const uint32_t*>(&mm), o);
     mm = __hmin2(mm, *reinterpret_cast<const __half2*>(&other));
   }
-  const float mn = __low2float(mm);
-  const float mx = -__high2float(mm);
-  const float scale_f = div_by_const<kQmax>(__fsub_rn(mx, mn));
-  const __half scale_h = __float2half_rn(scale_f);
-  const __half min_h = __float2half_rn(__fadd_rn(mn, 0.0f));
-  const float s = __half2float(scale_h);
-  const float r = s != 0.0f ? rcp_approx(s) : 0.0f;
+  return mm;
+}
+
+// Q2 and the stored params: scale = RN((mx - mn) / (2^b - 1)) in fp32, both
+// rounded to fp16; s = the fp16 scale as a float and r its reciprocal.
+template <int BITS>
+struct GroupScale {
+  __half scale_h, min_h;
+  float s, r;
+  __device__ __forceinline__ GroupScale(float mn, float mx) {
+    constexpr int kQmax = (1 << BITS) - 1;
+    scale_h = __float2half_rn(div_by_const<kQmax>(__fsub_rn(mx, mn)));
+    min_h = __float2half_rn(__fadd_rn(mn, 0.0f));
+    s = __half2float(scale_h);
+    r = s != 0.0f ? rcp_approx(s) : 0.0f;
+  }
+  __device__ __forceinline__ uint32_t params() const {
+    return (uint32_t)__half_as_ushort(scale_h) | ((uint32_t)__half_as_ushort(min_h) << 16);
+  }
+};
+
+// Q3 for 8 values of a group (raw), packed little-endian in 8 * b bits.  The
+// pairs of values go through packed fp32x2 instructions (each element rounded
+// as its scalar operation would be).  No clamp is needed while s is
+// fp16-normal: s is within 2^-11 of the fp32 scale, so q <= (2^b - 1)(1 +
+// 2^-11 + 2^-23) rounds to at most 2^b - 1.  A quotient within 1e-5 of a
+// half-integer, or a subnormal s, sends these 8 values to the IEEE divide and
+// the clamp.
+template <int BITS>
+__device__ __forceinline__ uint32_t codes8(const uint4& raw, float mn, const GroupScale<BITS>& gs) {
+  constexpr int kQmax = (1 << BITS) - 1;
   constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
   constexpr uint32_t kMagicBits = 0x4B400000u;
   uint32_t magic_sum = 0;
 #pragma unroll
   for (int j = 0; j < 8; ++j) magic_sum += kMagicBits << (BITS * j);
   const unsigned short* xs = reinterpret_cast<const unsigned short*>(&raw);
-  // The pairs of values go through packed fp32x2 instructions (each element
-  // rounded as its scalar operation would be).  No clamp is needed while s is
-  // fp16-normal: s is within 2^-11 of scale_f, so q <= (2^b - 1)(1 + 2^-11 + 2^-23)
-  // rounds to at most 2^b - 1; a subnormal s takes the IEEE path below.
-  const uint64_t r2 = pack_f32x2(r, r);
+  const float s = gs.s;
+  const uint64_t r2 = pack_f32x2(gs.r, gs.r);
   const uint64_t m2 = pack_f32x2(kMagic, kMagic);
   float dx[8];
   uint32_t acc = 0;
@@ -241,8 +263,6 @@ __device__ __forceinline__ uint32_t quantize_quad(const uint4& raw, uint32_t& pa
   }
   uint32_t packed = acc - magic_sum;
   if (near_tie) {
-    // a quotient within 1e-5 of a half-integer, or a subnormal scale: the IEEE
-    // divide decides, then the clamp
     packed = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -250,6 +270,21 @@ __device__ __forceinline__ uint32_t quantize_quad(const uint4& raw, uint32_t& pa
       packed |= (uint32_t)c << (BITS * j);
     }
   }
+  return packed;
+}
+
+template <int BITS>
+__device__ __forceinline__ uint32_t quantize_quad(const uint4& raw, uint32_t& params_out,
+                                                  bool hybrid = false, uint32_t* asym_bit = nullptr) {
+  const __half2* hv = reinterpret_cast<const __half2*>(&raw);
+  // Q1: (min, -max) of the lane's values, then of the quad
+  const __half2 mm = group_min_negmax<4>(lane_min_negmax(raw));
+  const float mn = __low2float(mm);
+  const float mx = -__high2float(mm);
+  const GroupScale<BITS> gs(mn, mx);
+  const __half scale_h = gs.scale_h, min_h = gs.min_h;
+  const float s = gs.s;
+  uint32_t packed = codes8<BITS>(raw, mn, gs);
   params_out = (uint32_t)__half_as_ushort(scale_h) | ((uint32_t)__half_as_ushort(min_h) << 16);
   if (hybrid) {
     float x[8];
@@ -348,6 +383,7 @@ struct DecodePlan {
   int splits;   // S (all splits)
   int splits_packed;  // tensor-core kernel: the first splits_packed take packed tokens
   int threads;  // threads per CTA of the split kernel
+  int cps;      // tensor-core kernel: resident CTAs per SM of the variant (3 or 4)
   // Workspace layout.  The tickets sit at fixed offsets (they depend only on the
   // cache shape and head count), so a workspace shared by calls with different
   // split counts never has a partial land on a ticket.

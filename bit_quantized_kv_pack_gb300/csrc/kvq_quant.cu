@@ -90,8 +90,49 @@ __global__ void __launch_bounds__(kPackThreads) quantize_pack_kernel(PackArgs a)
     const int64_t row_lo = (int64_t)bh * a.cap + (t_lo - ns);
     uint8_t* cbase = a.codes[which] + row_lo * a.row_bytes;
     uint32_t* pbase = a.params[which] + row_lo * a.Ng;
-    const int gl0 = warp * 8 + (lane >> 2);  // this lane's group in the first iteration
     const int ng_used = (int)(g_last - g0) + 1;
+    if constexpr (BITS != 3 && !HYB) {
+      // Two lanes per group, 16 values (two 16-byte loads) each: the group's
+      // min/max takes one shuffle and its scale is worked out once per 16
+      // values.  Each lane stores its 16 codes at once (8 bytes INT4, 4 bytes
+      // INT2); the even lane of the pair stores the params.
+      constexpr int kPairIters = kGroupsPerCta / (kPackThreads / 2);
+      const int gp0 = warp * 16 + (lane >> 1);
+      const int half = lane & 1;
+      uint4 raw[kPairIters][2];
+#pragma unroll
+      for (int u = 0; u < kPairIters; ++u) {
+        const int gl = gp0 + u * (kPackThreads / 2);
+        raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);
+        if (gl < ng_used) {
+          const int tl = gl >> a.ng_shift, g = gl & (a.Ng - 1);
+          const uint4* p = reinterpret_cast<const uint4*>(xs + (int64_t)tl * a.st) + g * (kGroup / 8) + 2 * half;
+          raw[u][0] = __ldg(p);
+          raw[u][1] = __ldg(p + 1);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kPairIters; ++u) {
+        const int gl = gp0 + u * (kPackThreads / 2);
+        const __half2 mm = group_min_negmax<2>(__hmin2(lane_min_negmax(raw[u][0]),
+                                                       lane_min_negmax(raw[u][1])));
+        const float mn = __low2float(mm);
+        const GroupScale<BITS> gs(mn, -__high2float(mm));
+        const uint32_t c0 = codes8<BITS>(raw[u][0], mn, gs);
+        const uint32_t c1 = codes8<BITS>(raw[u][1], mn, gs);
+        if (gl < ng_used) {
+          const int tl = gl >> a.ng_shift, g = gl & (a.Ng - 1);
+          uint8_t* dst = cbase + (uint32_t)(tl * a.row_bytes + g * (4 * BITS) + half * (2 * BITS));
+          if (BITS == 4)
+            *reinterpret_cast<uint2*>(dst) = make_uint2(c0, c1);
+          else
+            *reinterpret_cast<uint32_t*>(dst) = c0 | (c1 << 16);
+          if (!half) pbase[(uint32_t)gl] = gs.params();
+        }
+      }
+      return;
+    }
+    const int gl0 = warp * 8 + (lane >> 2);  // this lane's group in the first iteration
     uint4 raw[kPackUnroll];
 #pragma unroll
     for (int u = 0; u < kPackUnroll; ++u) {

@@ -196,3 +196,41 @@ def test_decode_fp32_output(bits, d, gq):
         assert torch.equal(out32.half(), out16)
     noalloc = kvq.kvq_decode_attention_noalloc(g, q.to(DEV), torch.empty_like(out32))
     assert_attn_close(noalloc, want)
+
+
+@pytest.mark.parametrize("bits", [4, 2, 3])
+@pytest.mark.parametrize("pages,hybrid,sink", [(0, 0, 0), (64 * 40, 0, 0), (0, 1, 8)])
+def test_decode_several_waves(bits, pages, hybrid, sink):
+    """A batch whose grid runs in several waves (40 sequences x 8 KV heads, each
+    with its window split): the 4-CTAs-per-SM variant of the tensor-core
+    kernel, plain, paged, and hybrid with a sink; decode and three fused steps
+    against the oracle, bytes bit for bit."""
+    rng = np.random.default_rng(bits * 100 + bool(pages) * 10 + hybrid)
+    B, H, d, gq, Nr, cap = 40, 8, 128, 4, 16, 320
+    lens = [int(x) for x in rng.integers(1, cap + Nr + sink - 3, B)]
+    Lmax = max(lens)
+    k = torch.from_numpy(rng.standard_normal((B, H, Lmax, d)).astype(np.float16))
+    v = torch.from_numpy(rng.standard_normal((B, H, Lmax, d)).astype(np.float16))
+    seq = torch.tensor(lens, dtype=torch.int32)
+    g = gpu_cache(B, H, d, bits, cap, Nr, sink=sink, hybrid=hybrid, pages=pages, seed=bits)
+    kvq.kvq_quantize_pack(g, k.to(DEV), v.to(DEV), seq.to(DEV))
+    assert kvq.kvq_read_error(g)[0] == kvq.KVQ_OK
+    rs = oracle_sequences(to_np(k), to_np(v), to_np(seq), bits, cap, Nr, sink, hybrid)
+    ws = kvq.workspace_for(g, H * gq)
+    q = torch.from_numpy(rng.standard_normal((B, H * gq, d)).astype(np.float16))
+    qn = q.numpy()
+    want = np.concatenate(per_sequence(lambda b: oracle.decode(rs[b], qn[b:b + 1]), B))
+    assert_attn_close(kvq.kvq_decode_attention(g, q.to(DEV), workspace=ws), want)
+    for step in range(3):
+        kn = torch.from_numpy(rng.standard_normal((B, H, d)).astype(np.float16))
+        vn = torch.from_numpy(rng.standard_normal((B, H, d)).astype(np.float16))
+        q = torch.from_numpy(rng.standard_normal((B, H * gq, d)).astype(np.float16))
+        out = kvq.kvq_decode_step(g, q.to(DEV), kn.to(DEV), vn.to(DEV), workspace=ws)
+        assert kvq.kvq_read_error(g)[0] == kvq.KVQ_OK
+        knn, vnn, qn = kn.numpy(), vn.numpy(), q.numpy()
+        assert all(e == 0 for e in per_sequence(
+            lambda b: oracle.append(rs[b], knn[b:b + 1], vnn[b:b + 1]), B))
+        want = np.concatenate(per_sequence(lambda b: oracle.decode(rs[b], qn[b:b + 1]), B))
+        assert_attn_close(out, want)
+    for b in range(B):
+        assert_cache_equal(g, rs[b], batches=[b])
