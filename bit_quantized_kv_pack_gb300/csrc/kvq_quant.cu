@@ -92,43 +92,30 @@ __global__ void __launch_bounds__(kPackThreads) quantize_pack_kernel(PackArgs a)
     uint32_t* pbase = a.params[which] + row_lo * a.Ng;
     const int ng_used = (int)(g_last - g0) + 1;
     if constexpr (BITS != 3 && !HYB) {
-      // Two lanes per group, 16 values (two 16-byte loads) each: the group's
-      // min/max takes one shuffle and its scale is worked out once per 16
-      // values.  Each lane stores its 16 codes at once (8 bytes INT4, 4 bytes
-      // INT2); the even lane of the pair stores the params.
-      constexpr int kPairIters = kGroupsPerCta / (kPackThreads / 2);
-      const int gp0 = warp * 16 + (lane >> 1);
-      const int half = lane & 1;
-      uint4 raw[kPairIters][2];
+      // One lane per group, its 32 values in four 16-byte loads: the group's
+      // min/max needs no shuffle and its scale and reciprocal are worked out
+      // once per 32 values; the lane stores the group's codes at once (16
+      // bytes INT4, 8 bytes INT2) and its params.
+      const int gl = warp * 32 + lane;
+      if (gl < ng_used) {
+        const int tl = gl >> a.ng_shift, g = gl & (a.Ng - 1);
+        const uint4* p = reinterpret_cast<const uint4*>(xs + (int64_t)tl * a.st) + g * (kGroup / 8);
+        uint4 raw[4];
 #pragma unroll
-      for (int u = 0; u < kPairIters; ++u) {
-        const int gl = gp0 + u * (kPackThreads / 2);
-        raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);
-        if (gl < ng_used) {
-          const int tl = gl >> a.ng_shift, g = gl & (a.Ng - 1);
-          const uint4* p = reinterpret_cast<const uint4*>(xs + (int64_t)tl * a.st) + g * (kGroup / 8) + 2 * half;
-          raw[u][0] = __ldg(p);
-          raw[u][1] = __ldg(p + 1);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kPairIters; ++u) {
-        const int gl = gp0 + u * (kPackThreads / 2);
-        const __half2 mm = group_min_negmax<2>(__hmin2(lane_min_negmax(raw[u][0]),
-                                                       lane_min_negmax(raw[u][1])));
+        for (int k = 0; k < 4; ++k) raw[k] = __ldg(p + k);
+        const __half2 mm = __hmin2(__hmin2(lane_min_negmax(raw[0]), lane_min_negmax(raw[1])),
+                                   __hmin2(lane_min_negmax(raw[2]), lane_min_negmax(raw[3])));
         const float mn = __low2float(mm);
         const GroupScale<BITS> gs(mn, -__high2float(mm));
-        const uint32_t c0 = codes8<BITS>(raw[u][0], mn, gs);
-        const uint32_t c1 = codes8<BITS>(raw[u][1], mn, gs);
-        if (gl < ng_used) {
-          const int tl = gl >> a.ng_shift, g = gl & (a.Ng - 1);
-          uint8_t* dst = cbase + (uint32_t)(tl * a.row_bytes + g * (4 * BITS) + half * (2 * BITS));
-          if (BITS == 4)
-            *reinterpret_cast<uint2*>(dst) = make_uint2(c0, c1);
-          else
-            *reinterpret_cast<uint32_t*>(dst) = c0 | (c1 << 16);
-          if (!half) pbase[(uint32_t)gl] = gs.params();
-        }
+        uint32_t c[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) c[k] = codes8<BITS>(raw[k], mn, gs);
+        uint8_t* dst = cbase + (uint32_t)(tl * a.row_bytes + g * (4 * BITS));
+        if (BITS == 4)
+          *reinterpret_cast<uint4*>(dst) = make_uint4(c[0], c[1], c[2], c[3]);
+        else
+          *reinterpret_cast<uint2*>(dst) = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+        pbase[(uint32_t)gl] = gs.params();
       }
       return;
     }
