@@ -248,18 +248,21 @@ __device__ __forceinline__ void qk_subtile(uint32_t kc, int r0, int lane,
 }
 
 // PV of one 16-token sub-tile: O^T += c^T (p * scale)^T, and the min/l MMA.
-// pb0/pb1 are the sub-tile's p as B fragments (column n -> query n / 2, tokens
-// 2t, 2t+1 and 2t+8, 2t+9), rounded to fp16, and pl0/pl1 the rest of p
-// (p - pb, rounded to fp16): p is used as the sum of the two, so the weights
-// carry about 22 bits.  The B operand of a code MMA scales column n by the
-// scale of group base + (n & 1), so rows of group base + 1 are right in the
-// odd columns and rows of group base in the even ones.  p * scale goes in as
-// the same two parts: the fp16 product and what its rounding dropped plus
-// p_lo * scale, each code MMA issued once per part into the same accumulator.
-//   INT4: oc[Pv][j]: row g = dim 64Pv + 4g + j (group 2Pv, fragment 0), row
-//         g+8 = dim 64Pv + 32 + 4g + j (group 2Pv+1, fragment 3).
-//   INT2: oc[c][pp]: rows g / g+8 = dims 64c + 8g + 2pp / +1, group 2c + g/4
-//         (fragments 0, 2 for g < 4; 1, 3 for g >= 4).
+// pb0/pb1 are the sub-tile's p as B fragments (tokens 2t, 2t+1 and 2t+8,
+// 2t+9 of query g / 2), rounded to fp16, and pl0/pl1 the rest of p (p - pb,
+// rounded to fp16): p is used as the sum of the two, so the weights carry
+// about 22 bits.  p * scale goes in as the same two parts: the fp16 product,
+// and what its rounding dropped plus p_lo * scale.
+//   INT4 (and INT3 widened to INT4): each code MMA takes the rows of one group
+//   and spends its 8 columns on 4 queries x the 2 parts: column n = 2 * query
+//   + part, part 0 holding minus the fp16 product and part 1 the rest, so a
+//   thread's accumulator pair (columns 2t, 2t+1) gives query t as [1] - [0].
+//   oc[c][2G + jp]: group 2c + G; row g = dim 4g + 2jp (weight 1), row g+8 =
+//   dim 4g + 2jp + 1 (weight 16).  The min/l MMA uses the same columns.
+//   INT2: a group spans only 4 of the 8 lanes' code units, so its MMAs serve
+//   two groups through the columns (n & 1 = group bit) and take each part
+//   in a separate MMA; oc[c][pp]: rows g / g+8 = dims 64c + 8g + 2pp / +1,
+//   group 2c + g/4 (fragments 0, 2 for g < 4; 1, 3 for g >= 4).
 template <int BITS>
 __device__ __forceinline__ void pv_subtile(uint32_t vc, const uint32_t* vp, int r0, int lane,
                                            uint32_t pb0, uint32_t pb1, uint32_t pl0, uint32_t pl1,
@@ -268,52 +271,72 @@ __device__ __forceinline__ void pv_subtile(uint32_t vc, const uint32_t* vp, int 
   const int mj = lane >> 3, mi = lane & 7;
   const int lrow = r0 + (mj & 1) * 8 + mi;
   const int ra = r0 + 2 * t, rb = r0 + 2 * t + 8;  // this thread's B rows: ra, ra+1, rb, rb+1
-  {
-    // A rows 0-3 = min of group g, row 8 = ones, others zero; B = p (both parts)
-    const int xg = g & 3;
-    const uint32_t am0 = g < 4 ? ptx::prmt(vp[ra * NG + xg], vp[(ra + 1) * NG + xg], 0x7632u) : 0u;
-    const uint32_t am2 = g < 4 ? ptx::prmt(vp[rb * NG + xg], vp[(rb + 1) * NG + xg], 0x7632u) : 0u;
-    const uint32_t ones = g == 0 ? 0x3C003C00u : 0u;
-    ptx::mma_16816(mnacc, am0, ones, am2, ones, pb0, pb1);
-    ptx::mma_16816(mnacc, am0, ones, am2, ones, pl0, pl1);
-  }
-  const int gb = g & 1;
-  // INT2: w2[2c]/w2[2c+1] = tokens (2t, 2t+1) / (2t+8, 2t+9), dims 64c + 8g .. +7
-  uint32_t w2[4];
-  if (BITS == 2) {
-    const int chunk = mj >> 1;
-    const uint32_t addr = vc + lrow * 32 + ((chunk ^ ((lrow >> 2) & 1)) << 4);
-    ptx::ldmatrix_x4_trans(addr, w2[0], w2[1], w2[2], w2[3]);
-  }
+  // A rows 0-3 = min of group g, row 8 = ones, others zero
+  const int xg = g & 3;
+  const uint32_t am0 = g < 4 ? ptx::prmt(vp[ra * NG + xg], vp[(ra + 1) * NG + xg], 0x7632u) : 0u;
+  const uint32_t am2 = g < 4 ? ptx::prmt(vp[rb * NG + xg], vp[(rb + 1) * NG + xg], 0x7632u) : 0u;
+  const uint32_t ones = g == 0 ? 0x3C003C00u : 0u;
+  if constexpr (BITS == 4) {
+    const bool rest = (g & 1) != 0;  // this thread's column holds the rest
+    constexpr uint32_t kNeg = 0x80008000u;
+    ptx::mma_16816(mnacc, am0, ones, am2, ones, rest ? pl0 : pb0 ^ kNeg, rest ? pl1 : pb1 ^ kNeg);
+    // with these, the same three instructions give -fl16(pb * s) in part-0
+    // columns and fl16(pl * s + (pb * s - fl16(pb * s))) in part-1 columns
+    const uint32_t pbz0 = rest ? pb0 : 0u, pbz1 = rest ? pb1 : 0u;
+    const uint32_t plz0 = rest ? pl0 : 0u, plz1 = rest ? pl1 : 0u;
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    // p * scale of group 2c + (n & 1) for this thread's column n = g: the
-    // rounded product of the fp16 parts, then (exact fma) what that rounding
-    // dropped, plus p_lo * scale
-    const int x = 2 * c + gb;
-    const uint32_t sc0 = ptx::prmt(vp[ra * NG + x], vp[(ra + 1) * NG + x], 0x5410u);
-    const uint32_t sc1 = ptx::prmt(vp[rb * NG + x], vp[(rb + 1) * NG + x], 0x5410u);
-    const uint32_t bs0 = ptx::hmul2_rn_u32(pb0, sc0);
-    const uint32_t bs1 = ptx::hmul2_rn_u32(pb1, sc1);
-    const uint32_t bl0 = ptx::hfma2_u32(pl0, sc0, ptx::hfma2_sub_u32(pb0, sc0, bs0));
-    const uint32_t bl1 = ptx::hfma2_u32(pl1, sc1, ptx::hfma2_sub_u32(pb1, sc1, bs1));
-    if (BITS == 4) {
+    for (int c = 0; c < 2; ++c) {
       // w[0]/w[1]: group 2c, tokens (2t, 2t+1) / (2t+8, 2t+9), dims 4g..4g+3;
       // w[2]/w[3]: the same for group 2c+1
       const int chunk = 2 * c + (mj >> 1);
       const uint32_t addr = vc + lrow * 64 + ((chunk ^ ((lrow >> 1) & 3)) << 4);
       uint32_t w[4];
       ptx::ldmatrix_x4_trans(addr, w[0], w[1], w[2], w[3]);
-      uint32_t s0[4], s1[4], s2[4], s3[4];
-      split_int4(w[0], s0);
-      split_int4(w[1], s1);
-      split_int4(w[2], s2);
-      split_int4(w[3], s3);
+      // scale/min of groups 2c, 2c+1 for the thread's four tokens
+      const uint2 pa = *reinterpret_cast<const uint2*>(vp + ra * NG + 2 * c);
+      const uint2 pa1 = *reinterpret_cast<const uint2*>(vp + (ra + 1) * NG + 2 * c);
+      const uint2 pr = *reinterpret_cast<const uint2*>(vp + rb * NG + 2 * c);
+      const uint2 pr1 = *reinterpret_cast<const uint2*>(vp + (rb + 1) * NG + 2 * c);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) ptx::mma_16816(oc[c][j], s0[j], s2[j], s1[j], s3[j], bs0, bs1);
+      for (int G = 0; G < 2; ++G) {
+        const uint32_t sc0 = ptx::prmt(G ? pa.y : pa.x, G ? pa1.y : pa1.x, 0x5410u);
+        const uint32_t sc1 = ptx::prmt(G ? pr.y : pr.x, G ? pr1.y : pr1.x, 0x5410u);
+        const uint32_t u0 = ptx::hmul2_rn_u32(pb0, sc0);
+        const uint32_t u1 = ptx::hmul2_rn_u32(pb1, sc1);
+        const uint32_t b0 = ptx::hfma2_u32(plz0, sc0, ptx::hfma2_sub_u32(pbz0, sc0, u0));
+        const uint32_t b1 = ptx::hfma2_u32(plz1, sc1, ptx::hfma2_sub_u32(pbz1, sc1, u1));
+        uint32_t sa[4], sb[4];
+        split_int4(w[2 * G], sa);      // tokens 2t, 2t+1
+        split_int4(w[2 * G + 1], sb);  // tokens 2t+8, 2t+9
 #pragma unroll
-      for (int j = 0; j < 4; ++j) ptx::mma_16816(oc[c][j], s0[j], s2[j], s1[j], s3[j], bl0, bl1);
-    } else {
+        for (int jp = 0; jp < 2; ++jp)
+          ptx::mma_16816(oc[c][2 * G + jp], sa[2 * jp], sa[2 * jp + 1], sb[2 * jp], sb[2 * jp + 1],
+                         b0, b1);
+      }
+    }
+  } else {
+    ptx::mma_16816(mnacc, am0, ones, am2, ones, pb0, pb1);
+    ptx::mma_16816(mnacc, am0, ones, am2, ones, pl0, pl1);
+    const int gb = g & 1;
+    // w2[2c]/w2[2c+1] = tokens (2t, 2t+1) / (2t+8, 2t+9), dims 64c + 8g .. +7
+    uint32_t w2[4];
+    {
+      const int chunk = mj >> 1;
+      const uint32_t addr = vc + lrow * 32 + ((chunk ^ ((lrow >> 2) & 1)) << 4);
+      ptx::ldmatrix_x4_trans(addr, w2[0], w2[1], w2[2], w2[3]);
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      // p * scale of group 2c + (n & 1) for this thread's column n = g: the
+      // rounded product of the fp16 parts, then (exact fma) what that rounding
+      // dropped, plus p_lo * scale
+      const int x = 2 * c + gb;
+      const uint32_t sc0 = ptx::prmt(vp[ra * NG + x], vp[(ra + 1) * NG + x], 0x5410u);
+      const uint32_t sc1 = ptx::prmt(vp[rb * NG + x], vp[(rb + 1) * NG + x], 0x5410u);
+      const uint32_t bs0 = ptx::hmul2_rn_u32(pb0, sc0);
+      const uint32_t bs1 = ptx::hmul2_rn_u32(pb1, sc1);
+      const uint32_t bl0 = ptx::hfma2_u32(pl0, sc0, ptx::hfma2_sub_u32(pb0, sc0, bs0));
+      const uint32_t bl1 = ptx::hfma2_u32(pl1, sc1, ptx::hfma2_sub_u32(pb1, sc1, bs1));
       uint32_t lo[8], hi[8];
       split_int2(w2[2 * c], lo);
       split_int2(w2[2 * c + 1], hi);
@@ -1042,10 +1065,11 @@ __global__ void __launch_bounds__(NTHREADS, CPS)
     }
     if (ref_offered) s_ref[lane] = ref_cas == 0u ? __float_as_uint(ref_mine) + 1u : ref_cas;
     // per group x and query t, sum p min_x to shared memory first; then the
-    // outputs O = 2^24 oc / weight + sum p min (the layout is at pv_subtile)
-    if (g < 4) ms.mn[warp][g][t] = mnacc[0];
+    // outputs O = 2^24 oc / weight + sum p min (the layouts are at pv_subtile;
+    // INT4 columns hold minus the first part and the rest)
+    if (g < 4) ms.mn[warp][g][t] = G::CB == 4 ? mnacc[1] - mnacc[0] : mnacc[0];
     if (g == 0) {
-      ms.l[warp][t] = mnacc[2];
+      ms.l[warp][t] = G::CB == 4 ? mnacc[3] - mnacc[2] : mnacc[2];
       ms.m[warp][t] = m_ref;
     }
     __syncwarp();
@@ -1054,10 +1078,11 @@ __global__ void __launch_bounds__(NTHREADS, CPS)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if (G::CB == 4) {
-          const float f = kTwo24 / w4_weight(j);
-          const int d0 = 64 * c + 4 * g + j;
-          ms.o[warp][t][d0] = fmaf(oc[c][j][0], f, ms.mn[warp][2 * c][t]);
-          ms.o[warp][t][d0 + 32] = fmaf(oc[c][j][3], f, ms.mn[warp][2 * c + 1][t]);
+          const int grp = 2 * c + (j >> 1), jp = j & 1;
+          const float mnv = ms.mn[warp][grp][t];
+          const int d0 = 32 * grp + 4 * g + 2 * jp;
+          ms.o[warp][t][d0] = fmaf(oc[c][j][1] - oc[c][j][0], kTwo24 / w4_weight(2 * jp), mnv);
+          ms.o[warp][t][d0 + 1] = fmaf(oc[c][j][3] - oc[c][j][2], kTwo24 / w4_weight(2 * jp + 1), mnv);
         } else {
           const int hb = g >> 2;
           const float mnv = ms.mn[warp][2 * c + hb][t];
