@@ -47,8 +47,10 @@ struct PackArgs {
   int64_t sb, sh, st;      // element strides of the input: sequence, head, token
 };
 
+// Without hybrid groups the kernel fits 40 registers, so six CTAs (1536 threads)
+// share an SM and keep more loads in flight; the hybrid rule needs more (4).
 template <int BITS, bool HYB>
-__global__ void __launch_bounds__(kPackThreads) quantize_pack_kernel(PackArgs a) {
+__global__ void __launch_bounds__(kPackThreads, HYB ? 4 : 6) quantize_pack_kernel(PackArgs a) {
   const int bh = blockIdx.y;
   const int which = blockIdx.z;
   const int b = bh / a.Hkv;
