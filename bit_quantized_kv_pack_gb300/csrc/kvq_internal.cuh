@@ -118,7 +118,7 @@ __device__ __forceinline__ void set_error(uint32_t* err_word, uint32_t bit) {
 // then (S_0 + S_1) + (S_2 + S_3) by two shuffle-xor steps (every lane of the
 // quad ends with the same value).  Every operation is rounded on its own.
 template <int BITS>
-__device__ __forceinline__ float quad_sq_error(const float (&x)[8], uint32_t packed, float sc,
+__device__ __forceinline__ float lane_sq_error(const float (&x)[8], uint32_t packed, float sc,
                                                float mn) {
   constexpr uint32_t kMask = (1u << BITS) - 1u;
   float acc = 0.0f;
@@ -128,6 +128,12 @@ __device__ __forceinline__ float quad_sq_error(const float (&x)[8], uint32_t pac
     const float e = __fsub_rn(x[j], xh);
     acc = __fadd_rn(acc, __fmul_rn(e, e));
   }
+  return acc;
+}
+template <int BITS>
+__device__ __forceinline__ float quad_sq_error(const float (&x)[8], uint32_t packed, float sc,
+                                               float mn) {
+  float acc = lane_sq_error<BITS>(x, packed, sc, mn);
   acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 1));
   acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 2));
   return acc;
@@ -273,10 +279,64 @@ __device__ __forceinline__ uint32_t codes8(const uint4& raw, float mn, const Gro
   return packed;
 }
 
+__device__ __forceinline__ void unpack8_f16(const uint4& v, float (&x)[8]) {
+  const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f = __half22float2(h[i]);
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+}
+
+// H1, the symmetric candidate: scale = absmax / (2^(b-1) - 1), codes t +
+// 2^(b-1), min = -2^(b-1) * scale (both fp16); storable unless that min
+// overflows fp16.
+template <int BITS>
+struct SymScale {
+  __half ssh, smh;
+  float ss, rs;
+  bool storable;
+  __device__ __forceinline__ SymScale(float mn, float mx) {
+    constexpr int kHalf = 1 << (BITS - 1);
+    constexpr int kQs = kHalf - 1;
+    const float amax = fmaxf(fabsf(mn), fabsf(mx));
+    ssh = __float2half_rn(__fdiv_rn(amax, (float)kQs));
+    ss = __half2float(ssh);
+    smh = __float2half_rn(__fadd_rn(__fmul_rn(-(float)kHalf, ss), 0.0f));
+    storable = (__half_as_ushort(smh) & 0x7c00u) != 0x7c00u;
+    rs = ss != 0.0f ? __frcp_rn(ss) : 0.0f;
+  }
+  __device__ __forceinline__ uint32_t params() const {
+    return (uint32_t)__half_as_ushort(ssh) | ((uint32_t)__half_as_ushort(smh) << 16);
+  }
+};
+
+// Symmetric codes of 8 values: x / ss through the reciprocal, the IEEE divide
+// near rounding boundaries (|x / ss| <= 2^(b-1), so the same 3-ulp argument as
+// for the asymmetric codes holds), clamped to +-(2^(b-1) - 1).
+template <int BITS>
+__device__ __forceinline__ uint32_t sym_codes8(const float (&x)[8], const SymScale<BITS>& ys) {
+  constexpr int kHalf = 1 << (BITS - 1);
+  constexpr int kQs = kHalf - 1;
+  uint32_t sp = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    int t = 0;
+    if (ys.ss != 0.0f) {
+      float qf = __fmul_rn(x[j], ys.rs);
+      if (fabsf(qf - floorf(qf) - 0.5f) < 1e-5f) qf = __fdiv_rn(x[j], ys.ss);
+      t = __float2int_rn(qf);
+      t = min(max(t, -kQs), kQs);
+    }
+    sp |= (uint32_t)(t + kHalf) << (BITS * j);
+  }
+  return sp;
+}
+
 template <int BITS>
 __device__ __forceinline__ uint32_t quantize_quad(const uint4& raw, uint32_t& params_out,
                                                   bool hybrid = false, uint32_t* asym_bit = nullptr) {
-  const __half2* hv = reinterpret_cast<const __half2*>(&raw);
   // Q1: (min, -max) of the lane's values, then of the quad
   const __half2 mm = group_min_negmax<4>(lane_min_negmax(raw));
   const float mn = __low2float(mm);
@@ -288,48 +348,62 @@ __device__ __forceinline__ uint32_t quantize_quad(const uint4& raw, uint32_t& pa
   params_out = (uint32_t)__half_as_ushort(scale_h) | ((uint32_t)__half_as_ushort(min_h) << 16);
   if (hybrid) {
     float x[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = __half22float2(hv[i]);
-      x[2 * i] = f.x;
-      x[2 * i + 1] = f.y;
-    }
-    constexpr int kHalf = 1 << (BITS - 1);
-    constexpr int kQs = kHalf - 1;
-    // H1: absmax / (2^(b-1) - 1); codes t + 2^(b-1); min = -2^(b-1) * scale
-    const float amax = fmaxf(fabsf(mn), fabsf(mx));
-    const __half ssh = __float2half_rn(__fdiv_rn(amax, (float)kQs));
-    const float ss = __half2float(ssh);
-    const __half smh = __float2half_rn(__fadd_rn(__fmul_rn(-(float)kHalf, ss), 0.0f));
-    const bool storable = (__half_as_ushort(smh) & 0x7c00u) != 0x7c00u;
-    // x / ss through the reciprocal, the IEEE divide near rounding boundaries
-    // (|x / ss| <= 2^(b-1), so the same 3-ulp argument as above holds)
-    const float rs = ss != 0.0f ? __frcp_rn(ss) : 0.0f;
-    uint32_t sp = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      int t = 0;
-      if (ss != 0.0f) {
-        float qf = __fmul_rn(x[j], rs);
-        if (fabsf(qf - floorf(qf) - 0.5f) < 1e-5f) qf = __fdiv_rn(x[j], ss);
-        t = __float2int_rn(qf);
-        t = min(max(t, -kQs), kQs);
-      }
-      sp |= (uint32_t)(t + kHalf) << (BITS * j);
-    }
+    unpack8_f16(raw, x);
+    const SymScale<BITS> ys(mn, mx);
+    const uint32_t sp = sym_codes8<BITS>(x, ys);
     // H2, H3
     const float ea = quad_sq_error<BITS>(x, packed, s, __half2float(min_h));
-    const float es = quad_sq_error<BITS>(x, sp, ss, __half2float(smh));
-    const bool sym = storable && es < ea;
+    const float es = quad_sq_error<BITS>(x, sp, ys.ss, __half2float(ys.smh));
+    const bool sym = ys.storable && es < ea;
     if (sym) {
       packed = sp;
-      params_out = (uint32_t)__half_as_ushort(ssh) | ((uint32_t)__half_as_ushort(smh) << 16);
+      params_out = ys.params();
     }
     if (asym_bit) *asym_bit = sym ? 0u : 1u;
   } else if (asym_bit) {
     *asym_bit = 1u;
   }
   return packed;
+}
+
+// One lane quantizes a whole group (its 32 values in raw[0..3]): the same
+// operations as quantize_quad, with the error sums of the hybrid rule taken
+// in the same order (8 values at a time, then (S0 + S1) + (S2 + S3)).  codes[k]
+// holds values 8k .. 8k+7 packed little-endian (8 * b bits).
+template <int BITS, bool HYB>
+__device__ __forceinline__ void quantize_group32(const uint4 (&raw)[4], uint32_t (&codes)[4],
+                                                 uint32_t& params_out, uint32_t& asym_bit) {
+  const __half2 mm = __hmin2(__hmin2(lane_min_negmax(raw[0]), lane_min_negmax(raw[1])),
+                             __hmin2(lane_min_negmax(raw[2]), lane_min_negmax(raw[3])));
+  const float mn = __low2float(mm);
+  const float mx = -__high2float(mm);
+  const GroupScale<BITS> gs(mn, mx);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) codes[k] = codes8<BITS>(raw[k], mn, gs);
+  params_out = gs.params();
+  asym_bit = 1u;
+  if constexpr (HYB) {
+    const SymScale<BITS> ys(mn, mx);
+    const float amin = __half2float(gs.min_h), smin = __half2float(ys.smh);
+    uint32_t sp[4];
+    float ea[4], es[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float x[8];
+      unpack8_f16(raw[k], x);
+      sp[k] = sym_codes8<BITS>(x, ys);
+      ea[k] = lane_sq_error<BITS>(x, codes[k], gs.s, amin);
+      es[k] = lane_sq_error<BITS>(x, sp[k], ys.ss, smin);
+    }
+    const float eat = __fadd_rn(__fadd_rn(ea[0], ea[1]), __fadd_rn(ea[2], ea[3]));
+    const float est = __fadd_rn(__fadd_rn(es[0], es[1]), __fadd_rn(es[2], es[3]));
+    if (ys.storable && est < eat) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) codes[k] = sp[k];
+      params_out = ys.params();
+      asym_bit = 0u;
+    }
+  }
 }
 
 // Store a group's 32 codes at its first byte `grp` (4 * BITS bytes; lane q of
@@ -360,15 +434,6 @@ __device__ __forceinline__ uint8_t mode_byte(uint32_t ballot, int k0, int ng) {
   return (uint8_t)m;
 }
 
-__device__ __forceinline__ void unpack8_f16(const uint4& v, float (&x)[8]) {
-  const __half2* h = reinterpret_cast<const __half2*>(&v);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float2 f = __half22float2(h[i]);
-    x[2 * i] = f.x;
-    x[2 * i + 1] = f.y;
-  }
-}
 
 // -------------------------------------------------------- decode planning ---
 

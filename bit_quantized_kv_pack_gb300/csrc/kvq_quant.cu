@@ -93,61 +93,47 @@ __global__ void __launch_bounds__(kPackThreads, HYB ? 4 : 6) quantize_pack_kerne
     uint8_t* cbase = a.codes[which] + row_lo * a.row_bytes;
     uint32_t* pbase = a.params[which] + row_lo * a.Ng;
     const int ng_used = (int)(g_last - g0) + 1;
-    if constexpr (BITS != 3 && !HYB) {
+    {
       // One lane per group, its 32 values in four 16-byte loads: the group's
       // min/max needs no shuffle and its scale and reciprocal are worked out
       // once per 32 values; the lane stores the group's codes at once (16
-      // bytes INT4, 8 bytes INT2) and its params.
+      // bytes INT4, 12 bytes INT3, 8 bytes INT2) and its params.  A warp's 32 groups are whole
+      // token rows (Ng divides 32), so each row's mode byte comes from one ballot.
       const int gl = warp * 32 + lane;
-      if (gl < ng_used) {
-        const int tl = gl >> a.ng_shift, g = gl & (a.Ng - 1);
+      const bool act = gl < ng_used;
+      if (!HYB && !act) return;  // (with hybrid groups every lane takes part in the ballot)
+      const int tl = gl >> a.ng_shift, g = gl & (a.Ng - 1);
+      uint4 raw[4];
+      if (act) {
         const uint4* p = reinterpret_cast<const uint4*>(xs + (int64_t)tl * a.st) + g * (kGroup / 8);
-        uint4 raw[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) raw[k] = __ldg(p + k);
-        const __half2 mm = __hmin2(__hmin2(lane_min_negmax(raw[0]), lane_min_negmax(raw[1])),
-                                   __hmin2(lane_min_negmax(raw[2]), lane_min_negmax(raw[3])));
-        const float mn = __low2float(mm);
-        const GroupScale<BITS> gs(mn, -__high2float(mm));
-        uint32_t c[4];
+      } else {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) c[k] = codes8<BITS>(raw[k], mn, gs);
+        for (int k = 0; k < 4; ++k) raw[k] = make_uint4(0, 0, 0, 0);
+      }
+      uint32_t c[4], prm, asym;
+      quantize_group32<BITS, HYB>(raw, c, prm, asym);
+      if constexpr (HYB) {
+        const uint32_t modes = __ballot_sync(0xffffffffu, act && asym);
+        if (act && g == 0) a.modes[which][row_lo + tl] = (uint8_t)((modes >> lane) & ((1u << a.Ng) - 1u));
+      }
+      if (act) {
         uint8_t* dst = cbase + (uint32_t)(tl * a.row_bytes + g * (4 * BITS));
-        if (BITS == 4)
+        if (BITS == 4) {
           *reinterpret_cast<uint4*>(dst) = make_uint4(c[0], c[1], c[2], c[3]);
-        else
+        } else if (BITS == 3) {  // four 24-bit pieces spliced into three words
+          uint32_t* d3 = reinterpret_cast<uint32_t*>(dst);
+          d3[0] = c[0] | (c[1] << 24);
+          d3[1] = (c[1] >> 8) | (c[2] << 16);
+          d3[2] = (c[2] >> 16) | (c[3] << 8);
+        } else {
           *reinterpret_cast<uint2*>(dst) = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-        pbase[(uint32_t)gl] = gs.params();
+        }
+        pbase[(uint32_t)gl] = prm;
       }
       return;
     }
-    const int gl0 = warp * 8 + (lane >> 2);  // this lane's group in the first iteration
-    uint4 raw[kPackUnroll];
-#pragma unroll
-    for (int u = 0; u < kPackUnroll; ++u) {
-      const int gl = gl0 + u * kGroupsPerIter;
-      raw[u] = make_uint4(0, 0, 0, 0);
-      if (gl < ng_used) {
-        const int tl = gl >> a.ng_shift, g = gl & (a.Ng - 1);
-        raw[u] = __ldg(reinterpret_cast<const uint4*>(xs + (int64_t)tl * a.st) + g * (kGroup / 8) + quad);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kPackUnroll; ++u) {
-      const int gl = gl0 + u * kGroupsPerIter;
-      const bool in_range = gl < ng_used;
-      uint32_t prm, asym = 1;
-      const uint32_t packed = quantize_quad<BITS>(raw[u], prm, HYB, &asym);  // all lanes take part
-      const uint32_t modes = HYB ? __ballot_sync(0xffffffffu, quad == 0 && asym) : 0u;
-      const int tl = gl >> a.ng_shift, g = gl & (a.Ng - 1);
-      store_group_codes<BITS>(cbase + (uint32_t)(tl * a.row_bytes + g * (4 * BITS)), packed, quad,
-                              in_range);
-      if (in_range && quad == 0) {
-        pbase[(uint32_t)gl] = prm;  // the CTA's groups are consecutive params
-        if (HYB && g == 0) a.modes[which][row_lo + tl] = mode_byte(modes, lane >> 2, a.Ng);
-      }
-    }
-    return;
   }
 
   uint4 raw[kPackUnroll];
