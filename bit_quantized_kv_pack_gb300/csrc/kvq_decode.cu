@@ -46,6 +46,7 @@ DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count, b
   p.gq = num_q_heads / D.num_kv_heads;
   int64_t target, min_tokens;
   p.cps = 0;
+  p.fold = 0;
   if (tc_supported(D, p.gq)) {
     // tensor-core kernel: 4 query heads per CTA, one wave of resident CTAs.
     // When even one packed split per (sequence, KV head) plus its fp16 splits
@@ -89,6 +90,12 @@ DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count, b
     const int rr = tc_residual_rows();
     int sr = (D.residual + D.sink + rr - 1) / rr;
     if (step && sr < 1) sr = 1;
+    // A grid of several waves gives its fp16 rows to the last packed split of
+    // each (sequence, KV head) instead of CTAs of their own.
+    if (p.cps == 4) {
+      sr = 0;
+      p.fold = 1;
+    }
     const int sp = (int)S - sr > 1 ? (int)S - sr : 1;
     p.splits_packed = sp;
     p.splits = sp + sr;
@@ -160,6 +167,7 @@ cudaError_t launch_decode(const Dims& s, const DecodePlan& p, const kvq_cache_vi
   a.nqb = p.nqb;
   a.S = p.splits;
   a.Sp = p.splits_packed;
+  a.fold = p.fold;
   a.Ns = s.Ns;
   a.cap = s.cap;
   a.Nr = s.Nr;

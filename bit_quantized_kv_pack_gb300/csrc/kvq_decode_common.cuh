@@ -55,6 +55,7 @@ struct DecodeArgs {
   int Sp;  // tensor-core kernel: splits s < Sp take packed tokens, s >= Sp fp16 ones
   uint32_t wait_limit_us;  // bounded waits give up after this long (1 s unless a test set it)
   uint32_t fault_tx;       // testing hook: extra bytes one tile's barrier expects (0: off)
+  int fold;                // tensor-core kernel: the last packed split also takes the fp16 rows
   float qk_scale_log2;  // log2(e) / sqrt(d)
 };
 

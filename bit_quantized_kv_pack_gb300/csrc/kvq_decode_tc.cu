@@ -44,7 +44,8 @@
 //  * The fp16 tokens -- the residual window, then the attention-sink rows
 //    (InnerQ page section 2.3) -- get splits of their own, 64 rows each (all
 //    loads of a split in one round, tensor cores), so no packed split waits on
-//    them.
+//    them.  In a grid of several waves the last packed split of each
+//    (sequence, KV head) takes them instead, once its stage ring is idle.
 //  * Per-warp states merge in shared memory.  The first split of a KV head to
 //    finish its first tile sets the head's reference max per query (atomicCAS);
 //    every split adds its (o, l), scaled to that reference, into the head's fp32
@@ -410,7 +411,7 @@ __device__ __forceinline__ void residual_issue(const F16Rows& fr, int c0, uint8_
 // Wait for the copies, then attend (every thread of the CTA calls it).
 __device__ __forceinline__ void residual_tc(const F16Rows& fr, int c0, uint8_t* tiles, int warp,
                                             int lane, const float (&q_s)[QB][D], float kq,
-                                            MergeSmem& ms) {
+                                            MergeSmem& ms, bool merge) {
   const int g = lane >> 2, t = lane & 3;
   auto valid_slot = [&](int j) { return fr.valid(j); };
   const uint32_t tbase = ptx::smem_u32(tiles);
@@ -453,6 +454,16 @@ __device__ __forceinline__ void residual_tc(const F16Rows& fr, int c0, uint8_t* 
   const uint32_t pb1 = ptx::prmt(x0, x1, 0x7632u);  // tokens 2t+8, 2t+9
   const uint32_t pl0 = ptx::prmt(y0, y1, 0x5410u);
   const uint32_t pl1 = ptx::prmt(y0, y1, 0x7632u);
+  // with merge, the warp's state already in ms (o, m, l of query t) is combined
+  // with these rows': both are scaled to the larger max
+  float al_old = 0.f, al_new = 1.f;
+  if (merge) {
+    const float m_old = ms.m[warp][t];
+    const float mm = fmaxf(m_old, m);
+    al_old = m_old == -INFINITY ? 0.f : exp2f(m_old - mm);
+    al_new = m == -INFINITY ? 0.f : exp2f(mu - mm);
+    if (mm == -INFINITY) al_new = 0.f;
+  }
   // ---- O^T = V^T p^T, two MMAs (the parts of p) per 16 head_dim values; l =
   // sum of the same p
   float lacc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -470,12 +481,20 @@ __device__ __forceinline__ void residual_tc(const F16Rows& fr, int c0, uint8_t* 
     float o[4] = {0.f, 0.f, 0.f, 0.f};
     ptx::mma_16816(o, v0, v1, v2, v3, pb0, pb1);
     ptx::mma_16816(o, v0, v1, v2, v3, pl0, pl1);
-    ms.o[warp][t][16 * mb + g] = o[0];
-    ms.o[warp][t][16 * mb + g + 8] = o[2];
+    float* dst = &ms.o[warp][t][16 * mb + g];
+    dst[0] = merge ? fmaf(dst[0], al_old, o[0] * al_new) : o[0];
+    dst[8] = merge ? fmaf(dst[8], al_old, o[2] * al_new) : o[2];
   }
+  __syncwarp();  // every lane has read the old (m, l) of its query
   if (g == 0) {
-    ms.m[warp][t] = m;
-    ms.l[warp][t] = lacc[0];
+    if (merge) {
+      const float m_old = ms.m[warp][t];
+      ms.l[warp][t] = fmaf(ms.l[warp][t], al_old, lacc[0] * al_new);
+      ms.m[warp][t] = fmaxf(m_old, m);
+    } else {
+      ms.m[warp][t] = m;
+      ms.l[warp][t] = lacc[0];
+    }
   }
 }
 
@@ -509,7 +528,9 @@ __global__ void __launch_bounds__(NTHREADS, CPS)
   __shared__ int s_last_tile[NSTAGE];  // last tile issued into each stage (-1: none)
   __shared__ float q_s[QB][D];
   __shared__ float qsum_s[QB][NG];  // sum of q over each group
-  __shared__ int s_rng[7];  // range lo, hi, ring head, step flags, packed_len, res_len, sink_len
+  // range lo, hi, ring head, step flags, packed_len, res_len, sink_len, and the
+  // fp16 rows' age range of a packed split that also takes them
+  __shared__ int s_rng[9];
   __shared__ volatile int s_abort;
   __shared__ int s_last;
   __shared__ uint32_t s_ref[QB];  // the head's reference max per query (float bits + 1; 0: unknown)
@@ -524,6 +545,9 @@ __global__ void __launch_bounds__(NTHREADS, CPS)
   const int g = lane >> 2;  // MMA group id
   const int t = lane & 3;   // thread in group
   const bool res_cta = s >= a.Sp;  // an fp16 split: window and sink rows
+  // in a grid of several waves the last packed split of the (sequence, KV head)
+  // also takes its fp16 rows (and, in a fused step, the append)
+  const bool fold_cta = a.fold != 0 && s == a.Sp - 1;
   const int64_t bh = (int64_t)b * a.Hkv + h;
   const int f0 = kResRows * (s - a.Sp);  // an fp16 split's first row
   const bool has_f16 = a.Nr + a.Ns > 0;
@@ -533,6 +557,7 @@ __global__ void __launch_bounds__(NTHREADS, CPS)
   const uint32_t fault_tx = (s == 0 && h == 0 && b == 0) ? a.fault_tx : 0u;
   // the fp16 rows of this (sequence, KV head), ranges from the counters
   auto f16_rows = [&]() {
+    const int ia = res_cta ? 0 : 7;  // where plan() left the window's age range
     F16Rows fr;
     fr.k_ring = a.k_res + bh * a.Nr * D;
     fr.v_ring = a.v_res + bh * a.Nr * D;
@@ -540,8 +565,8 @@ __global__ void __launch_bounds__(NTHREADS, CPS)
     fr.v_sink = a.v_sink + bh * a.Ns * D;
     fr.Nr = a.Nr;
     fr.rh = s_rng[2];
-    fr.age0 = s_rng[0];
-    fr.age1 = s_rng[1];
+    fr.age0 = s_rng[ia];
+    fr.age1 = s_rng[ia + 1];
     fr.ls = s_rng[6];
     return fr;
   };
@@ -644,16 +669,20 @@ __global__ void __launch_bounds__(NTHREADS, CPS)
         r0_ = r0_ / kPage * kPage;
         r1_ = s + 1 == a.Sp ? Lp : r1_ / kPage * kPage;
       }
-    } else {
+    }
+    // window tokens of age [jlo, Lr) take part (a flushed oldest token leaves
+    // the window); residual split sr holds ring slots [64 sr, 64 sr + 64)
+    const int jlo = (adds && a.Nr > 0 && pack_now) ? 1 : 0;
+    if (res_cta) {
       const int Sr = a.S - a.Sp, sr = s - a.Sp;
-      // window tokens of age [jlo, Lr) take part (a flushed oldest token leaves
-      // the window); residual split sr holds ring slots [64 sr, 64 sr + 64)
-      const int jlo = (adds && a.Nr > 0 && pack_now) ? 1 : 0;
       r0_ = jlo;
       r1_ = Lr;
       // bit 0: the new token joins the window; bit 1: a token is packed into slot Lp
       if (adds && sr == Sr - 1) xflags = (a.Nr > 0 ? 1 : 0) | (pack_now ? 2 : 0);
     }
+    if (fold_cta && adds) xflags = (a.Nr > 0 ? 1 : 0) | (pack_now ? 2 : 0);
+    s_rng[7] = jlo;
+    s_rng[8] = Lr;
     s_rng[0] = r0_;
     s_rng[1] = r1_;
     s_rng[2] = a.res_head[b];  // every split: the last one to finish commits the step
@@ -719,7 +748,7 @@ __global__ void __launch_bounds__(NTHREADS, CPS)
 
   // extra tokens of a fused step, fp32: [K, V][new token, packed token][D]
   float* xbuf = reinterpret_cast<float*>(smem + sizeof(MergeSmem));
-  if (STEP && res_cta && warp < 2 && s_rng[3] != 0) {
+  auto append_work = [&]() {
     // the append's writes for this (sequence, KV head): warp 0 the K row, warp
     // 1 the V row, lane l < 16 holding values 8l .. 8l+7 (as in kvq_append)
     const int which = warp;
@@ -767,25 +796,8 @@ __global__ void __launch_bounds__(NTHREADS, CPS)
       const int slot = (xflags & 2) ? rh : (rh + Lr) % a.Nr;
       *reinterpret_cast<uint4*>(a.w_res[which] + (bh * a.Nr + slot) * D + lane * 8) = nv;
     }
-  }
-
-  if (res_cta) {
-    // ------------------------------------------------ fp16-token split
-    uint8_t* tiles = smem + kResTilesOff;
-    if (has_f16) {
-      residual_tc(f16_rows(), f0, tiles, warp, lane, q_s, kq, ms);
-    } else {  // no fp16 rows (the split only takes a fused step's packed token)
-      __syncthreads();  // warp 1's V row of the extra token is staged
-      if (lane < QB) {
-        ms.m[warp][lane] = -INFINITY;
-        ms.l[warp][lane] = 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < QB; ++i)
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) ms.o[warp][i][lane * 4 + jj] = 0.f;
-    }
-    if (STEP) {
+  };
+  auto join_extra = [&]() {
       // the appended tokens (new fp16 token, quantized token), staged in xbuf by
       // warps 0 and 1 before the barrier above, join warp 0's state; lane = four
       // head_dim values
@@ -822,7 +834,26 @@ __global__ void __launch_bounds__(NTHREADS, CPS)
           for (int jj = 0; jj < 4; ++jj) ms.o[0][i][lane * 4 + jj] = ro[jj];
         }
       }
+  };
+  if (STEP && res_cta && warp < 2 && s_rng[3] != 0) append_work();
+
+  if (res_cta) {
+    // ------------------------------------------------ fp16-token split
+    uint8_t* tiles = smem + kResTilesOff;
+    if (has_f16) {
+      residual_tc(f16_rows(), f0, tiles, warp, lane, q_s, kq, ms, false);
+    } else {  // no fp16 rows (the split only takes a fused step's packed token)
+      __syncthreads();  // warp 1's V row of the extra token is staged
+      if (lane < QB) {
+        ms.m[warp][lane] = -INFINITY;
+        ms.l[warp][lane] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < QB; ++i)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) ms.o[warp][i][lane * 4 + jj] = 0.f;
     }
+    if (STEP) join_extra();
   } else {
     // ---------------------------------------------------- packed-token split
     {
@@ -1091,6 +1122,27 @@ __global__ void __launch_bounds__(NTHREADS, CPS)
           ms.o[warp][t][d0 + 1] = fmaf(hb ? oc[c][j][3] : oc[c][j][2], kTwo24 / w2_weight(2 * j + 1), mnv);
         }
       }
+  }
+
+  if (fold_cta) {
+    // this split also takes the fp16 rows (window, then sink) and, in a fused
+    // step, the append, as an fp16 split would; the stage ring is idle
+    __syncthreads();  // every warp's packed state is in ms
+    uint8_t* tiles = smem + kResTilesOff;
+    if (has_f16) residual_issue(f16_rows(), 0, tiles);
+    if (STEP && warp < 2 && s_rng[3] != 0) append_work();
+    if (has_f16) {
+      for (int c0 = 0; c0 < a.Nr + a.Ns; c0 += kResRows) {
+        if (c0 > 0) {
+          __syncthreads();  // the previous rows are read
+          residual_issue(f16_rows(), c0, tiles);
+        }
+        residual_tc(f16_rows(), c0, tiles, warp, lane, q_s, kq, ms, true);
+      }
+    } else {
+      __syncthreads();  // warp 1's V row of the extra token is staged
+    }
+    if (STEP) join_extra();
   }
 
   // ---------------- merge the four warps' states.  The split's partial (o, m, l)

@@ -449,6 +449,7 @@ struct DecodePlan {
   int splits_packed;  // tensor-core kernel: the first splits_packed take packed tokens
   int threads;  // threads per CTA of the split kernel
   int cps;      // tensor-core kernel: resident CTAs per SM of the variant (3 or 4)
+  int fold;     // tensor-core kernel: no fp16 splits; the last packed split takes those rows
   // Workspace layout.  The tickets sit at fixed offsets (they depend only on the
   // cache shape and head count), so a workspace shared by calls with different
   // split counts never has a partial land on a ticket.
