@@ -280,9 +280,10 @@ kvq_status kvq_decode_attention(const kvq_cache_desc* desc, const kvq_cache_view
  * by this step is attended in fp32 from its codes rather than on the tensor
  * cores).  With head_dim 128 and at most 4 query heads per KV head this is one
  * kernel launch: the packed splits read only rows written before the step, the
- * residual split of each head does the append's writes and attends over the new
- * and the packed token, and the counters move when the last head of a sequence
- * finishes.  Other shapes launch the append and the decode kernels in turn.  A
+ * split of each head that takes its fp16 rows (a split of its own, or in a
+ * grid of several waves the last packed split) does the append's writes and
+ * attends over the new and the packed token, and the counters move when the
+ * last head of a sequence finishes.  Other shapes launch the append and the decode kernels in turn.  A
  * sequence whose packed cache is full is left unchanged, sets
  * KVQ_ERRBIT_CAPACITY and is attended as it was.
  *   flags      0, or KVQ_STEP_EARLY_CACHE_READ: the caller states that the
