@@ -1022,7 +1022,7 @@ __global__ void __launch_bounds__(NTHREADS, CPS)
 #pragma unroll
           for (int r = 0; r < 4; ++r) mnacc[r] *= al;
         }
-        if (tile == 0 && warp == 0 && lane < QB) {
+        if (tile == 0 && warp == 0 && lane < QB && a.S > 1) {
           ref_mine = m_ref;
           ref_cas = atomicCAS(&a.ref_max[bh * QB + lane], 0u, __float_as_uint(m_ref) + 1u);
           ref_offered = true;
@@ -1172,6 +1172,15 @@ __global__ void __launch_bounds__(NTHREADS, CPS)
         }
       }
     }
+    if (a.S == 1) {
+      // the head's only split: its state is the result (no partials, no
+      // accumulators, no ticket)
+      if (i < a.gq) {
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        store_out4(a, ((int64_t)b * a.Hq + h * a.gq + i) * D + e,
+                   make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv));
+      }
+    } else {
     *reinterpret_cast<float4*>(a.o_part + (pidx * QB + i) * D + e) = o;
     if (lane == 0) a.ml_part[pidx * QB + i] = make_float2(M, lsum);
     if (M > -INFINITY) {  // warp-uniform
@@ -1194,13 +1203,32 @@ __global__ void __launch_bounds__(NTHREADS, CPS)
         if (lane == 0) ptx::red_add_f32(&a.l_acc[bh * QB + i], lsum * g);
       }
     }
+    }
+  }
+  // Fused step: once every split of a head has read the counters, the head takes
+  // a ticket on its sequence; the last head of the sequence commits the append's
+  // counters, computed from the values this CTA read at its start.
+  auto commit_step = [&](unsigned seq_ticket) {
+    if (STEP && threadIdx.x == 0 && seq_ticket == (unsigned)(a.Hkv - 1)) {
+      const int Lp = s_rng[4], Lr = s_rng[5], rh = s_rng[2];
+      const bool pack_now = a.Nr == 0 || Lr == a.Nr;
+      if (!(pack_now && Lp >= a.cap)) {
+        if (pack_now) {
+          a.w_packed_len[b] = Lp + 1;
+          if (a.Nr > 0) a.w_res_head[b] = (rh + 1) % a.Nr;
+        } else {
+          a.w_res_len[b] = Lr + 1;
+        }
+      }
+    }
+  };
+  if (a.S == 1) {
+    if (STEP && threadIdx.x == 0) commit_step(atomicInc(&a.seq_tickets[b], (unsigned)(a.Hkv - 1)));
+    return;
   }
   // the last split of this KV head to finish merges all S partials
   if (take_last_ticket_acq_rel<NTHREADS>(a, bh, &s_last)) {
-    // Fused step: every split of this head has read the counters.  The head
-    // takes a ticket on its sequence now, so the round trip overlaps the
-    // combine; the last head of the sequence commits the append's counters,
-    // computed from the values this CTA read at its start.
+    // (the sequence ticket's round trip overlaps the combine)
     unsigned seq_ticket = 0;
     if (STEP && threadIdx.x == 0) seq_ticket = atomicInc(&a.seq_tickets[b], (unsigned)(a.Hkv - 1));
     const int i = warp, e = lane * 4;
@@ -1225,18 +1253,7 @@ __global__ void __launch_bounds__(NTHREADS, CPS)
       a.ref_max[bh * QB + i] = 0u;
     }
     if (threadIdx.x == 0) a.fb_flag[bh] = 0u;
-    if (STEP && threadIdx.x == 0 && seq_ticket == (unsigned)(a.Hkv - 1)) {
-      const int Lp = s_rng[4], Lr = s_rng[5], rh = s_rng[2];
-      const bool pack_now = a.Nr == 0 || Lr == a.Nr;
-      if (!(pack_now && Lp >= a.cap)) {
-        if (pack_now) {
-          a.w_packed_len[b] = Lp + 1;
-          if (a.Nr > 0) a.w_res_head[b] = (rh + 1) % a.Nr;
-        } else {
-          a.w_res_len[b] = Lr + 1;
-        }
-      }
-    }
+    commit_step(seq_ticket);
   }
 }
 
