@@ -199,14 +199,17 @@ def test_decode_fp32_output(bits, d, gq):
 
 
 @pytest.mark.parametrize("bits", [4, 2, 3])
-@pytest.mark.parametrize("pages,hybrid,sink", [(0, 0, 0), (64 * 40, 0, 0), (0, 1, 8)])
-def test_decode_several_waves(bits, pages, hybrid, sink):
-    """A batch whose grid runs in several waves (40 sequences x 8 KV heads, each
-    with its window split): the 4-CTAs-per-SM variant of the tensor-core
-    kernel, plain, paged, and hybrid with a sink; decode and three fused steps
-    against the oracle, bytes bit for bit."""
-    rng = np.random.default_rng(bits * 100 + bool(pages) * 10 + hybrid)
-    B, H, d, gq, Nr, cap = 40, 8, 128, 4, 16, 320
+@pytest.mark.parametrize("pages,hybrid,sink,Nr", [(0, 0, 0, 16), (64 * 40, 0, 0, 16), (0, 1, 8, 16),
+                                                  (0, 0, 32, 96)])
+def test_decode_several_waves(bits, pages, hybrid, sink, Nr):
+    """A batch whose grid runs in several waves (40 sequences x 8 KV heads): the
+    4-CTAs-per-SM variant of the tensor-core kernel, where the last packed
+    split of each head also takes the fp16 rows (in two passes of 64 when the
+    window and the sink hold more); plain, paged, hybrid with a sink, and a
+    96-token window with a 32-token sink; decode and three fused steps against
+    the oracle, bytes bit for bit."""
+    rng = np.random.default_rng(bits * 100 + bool(pages) * 10 + hybrid + Nr)
+    B, H, d, gq, cap = 40, 8, 128, 4, 320
     lens = [int(x) for x in rng.integers(1, cap + Nr + sink - 3, B)]
     Lmax = max(lens)
     k = torch.from_numpy(rng.standard_normal((B, H, Lmax, d)).astype(np.float16))
@@ -234,3 +237,23 @@ def test_decode_several_waves(bits, pages, hybrid, sink):
         assert_attn_close(out, want)
     for b in range(B):
         assert_cache_equal(g, rs[b], batches=[b])
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+@pytest.mark.parametrize("gq", [4, 1])
+def test_decode_single_split(bits, gq):
+    """Short sequences and no window, so each (sequence, KV head) is one split
+    that writes its output straight from its own state; a sequence of one
+    token among them."""
+    rng = np.random.default_rng(7 * bits + gq)
+    B, H, d, cap = 3, 2, 128, 200
+    lens = torch.tensor([200, 1, 77], dtype=torch.int32)
+    k = torch.from_numpy(rng.standard_normal((B, H, 200, d)).astype(np.float16))
+    v = torch.from_numpy(rng.standard_normal((B, H, 200, d)).astype(np.float16))
+    g, r = _setup(k, v, lens, bits, cap, 0)
+    ws = kvq.workspace_for(g, H * gq)
+    for _ in range(2):
+        q = torch.from_numpy(rng.standard_normal((B, H * gq, d)).astype(np.float16))
+        out = kvq.kvq_decode_attention(g, q.to(DEV), workspace=ws, flags=kvq.KVQ_OUT_F32)
+        assert kvq.kvq_read_error(g)[0] == kvq.KVQ_OK
+        assert_attn_close(out, oracle.decode(r, q.numpy()))
