@@ -9,8 +9,8 @@
 //
 //  * 128-token tiles -- K codes, V codes (2D TMA tile loads), K params, V params
 //    (1D bulk copies: a tile's params are 2 KB of contiguous 16-byte rows, which
-//    a tile load would move row by row) -- stream into a 3-stage (INT4) or
-//    5-stage (INT2) shared-memory ring
+//    a tile load would move row by row) -- stream into a 3-stage (INT4, INT3)
+//    or 5-stage (INT2) shared-memory ring (2 / 4 stages in the 4-CTA variant)
 //    guarded by mbarriers (the asynchronous staging of the BitDecoding page,
 //    section 2.3, done with the bulk tensor copy instead of per-thread
 //    cp.async).  One thread issues the first stages up front; the warp that
@@ -31,16 +31,17 @@
 //    2 * query + group bit), so each thread holds one query for both groups,
 //    then  s = sum_g scale_g * acc_g + min_g * sum_{d in g} q_d.
 //  * Online softmax in fp32 (exp2 domain) with a lazy rescale: the running max
-//    only moves when it grows by more than 2^8.
+//    only moves when it grows by more than 2^8, and the warp reduces it only
+//    when one of a thread's own rows lies that far above it.
 //  * PV:  O^T = c^T (p * scale)^T with V codes read through ldmatrix.trans.
-//    The B operand uses the same column order (2 * query + group bit) with
-//    p * scale of that group, so one MMA serves two groups and each thread
-//    again holds one query.  Another MMA accumulates sum p * min_g and sum p
-//    (= l), so O = O_c + sum_g p min_g.  p and p * scale enter every B operand
-//    as two fp16 parts (the rounded value and the rest), each MMA issued once
-//    per part: one fp16 part alone would carry 11 bits, and an output of
+//    Another MMA accumulates sum p * min_g and sum p (= l), so O = O_c +
+//    sum_g p min_g.  p and p * scale enter as two fp16 parts (the rounded value
+//    and the rest): one fp16 part alone would carry 11 bits, and an output of
 //    magnitude 8 then moves by up to 2e-3 when one token holds most of the
-//    weight.
+//    weight.  INT4 (and INT3): each code MMA takes the rows of one group and
+//    spends its 8 columns on 4 queries x the 2 parts.  INT2: a group spans half
+//    of the lanes' code units, so its MMAs serve two groups through the columns
+//    (2 * query + group bit), each part in an MMA of its own.
 //  * The fp16 tokens -- the residual window, then the attention-sink rows
 //    (InnerQ page section 2.3) -- get splits of their own, 64 rows each (all
 //    loads of a split in one round, tensor cores), so no packed split waits on
@@ -51,9 +52,11 @@
 //    every split adds its (o, l), scaled to that reference, into the head's fp32
 //    accumulators (vector red.add), and the last split to finish divides by l.
 //    A split whose max lies too far above the reference sends the head to the
-//    exact log-sum-exp merge of the split partials (combine_unit) instead.
-//  * Three CTAs per SM (168 registers each): twelve warps hide the latency of
-//    the dequantize-and-MMA chain.
+//    exact log-sum-exp merge of the split partials (combine_unit) instead.  A
+//    head with a single split writes its output straight from its own state.
+//  * Three CTAs per SM (168 registers each) for grids of one wave: twelve warps
+//    hide the latency of the dequantize-and-MMA chain; four (128 registers) for
+//    grids of several waves.
 //  * 3-bit codes (TurboQuant page section 3.1) arrive as plain 48-byte rows;
 //    each warp widens its 32 rows to INT4 nibbles in a buffer of its own (the
 //    INT4 swizzle), and the INT4 arithmetic runs on that buffer.
