@@ -9,9 +9,8 @@
 //
 //  * 128-token tiles -- K codes, V codes (2D TMA tile loads), K params, V params
 //    (1D bulk copies: a tile's params are 2 KB of contiguous 16-byte rows, which
-//    a tile load would move row by row) -- stream into a 3-stage (INT4, INT3)
-//    or 5-stage (INT2) shared-memory ring (2 / 4 stages in the 4-CTA variant)
-//    guarded by mbarriers (the asynchronous staging of the BitDecoding page,
+//    a tile load would move row by row) -- stream into a 2-stage shared-memory
+//    ring guarded by mbarriers (the asynchronous staging of the BitDecoding page,
 //    section 2.3, done with the bulk tensor copy instead of per-thread
 //    cp.async).  One thread issues the first stages up front; the warp that
 //    releases a stage last refills it at once.  Code
@@ -85,9 +84,9 @@ constexpr int NCW = 4;          // warps, 32 tokens (two 16-token sub-tiles) eac
 constexpr int NSUB = 2;         // sub-tiles per warp per stage
 constexpr int NTHREADS = NCW * 32;
 // CTAs per SM (CPS, a template parameter): 3 (12 warps, up to 168 registers,
-// ~62 KB of shared memory each) for grids of one wave; 4 (16 warps, 128
-// registers, a shorter ring) for grids of several waves, where more warps hide
-// more latency and the ramp of each CTA is overlapped by the others.
+// ~47 KB of shared memory each) for grids of one wave; 4 (16 warps, 128
+// registers) for grids of several waves, where more warps hide more latency
+// and the ramp of each CTA is overlapped by the others.
 static_assert(NCW == QB, "the merge gives each warp one query");
 
 template <int BITS, int CPS>
@@ -101,8 +100,12 @@ struct Geo {
   static constexpr int KP = 2 * CODE_TILE;
   static constexpr int VP = 2 * CODE_TILE + PAR_TILE;
   static constexpr int STAGE = 2 * CODE_TILE + 2 * PAR_TILE;  // 20 KB / 12 KB
-  // 60 KB (INT4, INT2) / 48 KB (INT3) in flight at 3 CTAs per SM; 40 / 48 / 32 KB at 4
-  static constexpr int NSTAGE = CPS == 4 ? (BITS == 2 ? 4 : 2) : (BITS == 2 ? 5 : 3);
+  // One tile in flight while the other is read: 20 KB (INT4) / 16 KB (INT3) /
+  // 12 KB (INT2) of copies per CTA ahead of the compute.  Deeper rings (3 INT4
+  // or 5 INT2 stages at 3 CTAs per SM, 4 INT2 at 4) were slower or no faster:
+  // a tile's compute outlasts a copy's latency, and the extra bytes in flight
+  // only delay the other CTAs' tiles.
+  static constexpr int NSTAGE = 2;
   // INT3: per warp 32 widened rows of K and of V, 64 bytes each
   static constexpr int XBUF = BITS == 3 ? NCW * 2 * 32 * 64 : 0;
   static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned");
