@@ -466,12 +466,17 @@ def run_e2e(st, nsteps):
     step_bytes = st["step_bytes"]
     modes = {"mapped": (kvq.KVQ_STEP_HOST_MAPPED | kvq.KVQ_STEP_EARLY_CACHE_READ, None),
              "copies": (kvq.KVQ_STEP_EARLY_CACHE_READ, dev_io)}
+    # per-slot buffers and the stream handle are taken once, as a serving loop
+    # holding its own buffers would
+    ins_j = [in_h[j] for j in range(n)]
+    outs_j = [out_h[j] for j in range(n)]
+    stream = torch.cuda.current_stream().cuda_stream
     res = {}
     for name, (flags, io) in modes.items():
         def step(i):
             j = i % n
-            kvq.kvq_decode_step_host(st["copies"][j], in_h[j], hq, out_h[j], io, st["ws"],
-                                     flags=flags)
+            kvq.kvq_decode_step_host(st["copies"][j], ins_j[j], hq, outs_j[j], io, st["ws"],
+                                     stream=stream, flags=flags)
 
         for i in range(n):
             step(i)
