@@ -719,9 +719,20 @@ __global__ void __launch_bounds__(NTHREADS, CPS)
   // plain loads of data that must come from memory) were measured to be served
   // only once the launch it depends on had completed, and queued ahead of that
   // launch's last memory operations they delayed its completion and with it
-  // the wait.  q and the new token are read after the wait.
+  // the wait.  An L2 prefetch of tile 0 alone (a ninth of the cache at 32K) is
+  // cheap enough there: in a grid of one wave it lets tile 0 land sooner.  q
+  // and the new token are read after the wait.
   const bool early = STEP && a.early != 0;
-  if (early && threadIdx.x == 0) plan(false);
+  if (early && threadIdx.x == 0) {
+    plan(false);
+    if (!res_cta && !a.rm.paged && !a.fold && ntiles > 0) {
+      const uint32_t rows = (uint32_t)min(T, i1 - i0);  // this head's rows from row0
+      ptx::prefetch_l2(a.k_codes + (int64_t)row0 * G::RB, rows * G::RB);
+      ptx::prefetch_l2(a.v_codes + (int64_t)row0 * G::RB, rows * G::RB);
+      ptx::prefetch_l2(a.k_params + (int64_t)row0 * NG, rows * kParRow);
+      ptx::prefetch_l2(a.v_params + (int64_t)row0 * NG, rows * kParRow);
+    }
+  }
   grid_dependency_wait();
 
   // The small loads go first -- q by every thread, the lengths by thread 0 --
