@@ -47,6 +47,7 @@ DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count, b
   int64_t target, min_tokens;
   p.cps = 0;
   p.fold = 0;
+  p.tile = 128;
   if (tc_supported(D, p.gq)) {
     // tensor-core kernel: 4 query heads per CTA, one wave of resident CTAs.
     // When even one packed split per (sequence, KV head) plus its fp16 splits
@@ -99,6 +100,7 @@ DecodePlan plan_decode(const kvq_cache_desc& D, int num_q_heads, int sm_count, b
     const int sp = (int)S - sr > 1 ? (int)S - sr : 1;
     p.splits_packed = sp;
     p.splits = sp + sr;
+    p.tile = tc_tile_tokens(D, p.cps, ((int64_t)D.capacity + sp - 1) / sp);
   }
   const int64_t nparts = units * p.splits * p.qb;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };

@@ -112,6 +112,9 @@ bool tc_supported(const kvq_cache_desc& D, int gq);
 int tc_threads();
 int tc_ctas_per_sm(bool several_waves);  // resident CTAs per SM of the variant launched
 int tc_residual_rows();
+// tokens per pipeline stage of the variant for packed splits of up to
+// split_tokens tokens each (128, or 192 for long INT2 splits in one wave)
+int tc_tile_tokens(const kvq_cache_desc& D, int cps, int64_t split_tokens);
 cudaError_t launch_decode_tc(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
                              cudaStream_t st, bool step);
 

@@ -7,7 +7,8 @@
 // query heads of one KV head served by one read of the cache (BitDecoding page
 // section 2.3).  How:
 //
-//  * 128-token tiles -- K codes, V codes (2D TMA tile loads), K params, V params
+//  * 128-token tiles (192 for long INT2 splits in a grid of one wave) -- K
+//    codes, V codes (2D TMA tile loads), K params, V params
 //    (1D bulk copies: a tile's params are 2 KB of contiguous 16-byte rows, which
 //    a tile load would move row by row) -- stream into a 2-stage shared-memory
 //    ring guarded by mbarriers (the asynchronous staging of the BitDecoding page,
@@ -18,7 +19,8 @@
 //    swizzle of the BitDecoding page's equation (2), which makes every ldmatrix
 //    below conflict-free.
 //  * Four warps take 32 tokens (two independent 16-token sub-tiles) each per
-//    tile.  ldmatrix brings code words to registers, and a single AND turns
+//    tile (48 tokens, three sub-tiles, in the 192-token variant).  ldmatrix
+//    brings code words to registers, and a single AND turns
 //    two codes into one exact half2: a code c sitting in the low mantissa bits
 //    of an fp16 whose exponent field is zero is the subnormal c * 2^-24 (a code
 //    at bit offset 2 or 4 is 4c or 16c times 2^-24).  The tensor cores take
@@ -79,9 +81,7 @@ namespace {
 constexpr int D = 128;
 constexpr int NG = D / kGroup;  // 4 groups per row
 constexpr int QB = 4;           // query heads per CTA
-constexpr int T = 128;          // tokens per pipeline stage
-constexpr int NCW = 4;          // warps, 32 tokens (two 16-token sub-tiles) each per stage
-constexpr int NSUB = 2;         // sub-tiles per warp per stage
+constexpr int NCW = 4;          // warps; each takes a quarter of every tile
 constexpr int NTHREADS = NCW * 32;
 // CTAs per SM (CPS, a template parameter): 3 (12 warps, up to 168 registers,
 // ~47 KB of shared memory each) for grids of one wave; 4 (16 warps, 128
@@ -89,12 +89,21 @@ constexpr int NTHREADS = NCW * 32;
 // and the ramp of each CTA is overlapped by the others.
 static_assert(NCW == QB, "the merge gives each warp one query");
 
-template <int BITS, int CPS>
+// TT, tokens per pipeline stage: 128 (two independent 16-token sub-tiles per
+// warp), or 192 (three) for INT2 splits of many tiles in a grid of one wave --
+// the third sub-tile hides more of each warp's latency chain, which pays once a
+// split is long enough that its larger first tile and ragged last one do not
+// matter (contiguous caches only: a warp's 48 rows would straddle pages).
+template <int BITS, int CPS, int TT>
 struct Geo {
+  static constexpr int T = TT;
+  static constexpr int NSUB = TT / (16 * NCW);  // sub-tiles per warp per stage
+  static constexpr int WR = 16 * NSUB;          // a warp's rows of the stage
+  static_assert(TT == 128 || TT == 192, "two or three sub-tiles per warp");
   static constexpr int CB = BITS == 3 ? 4 : BITS;  // code width of the arithmetic
   static constexpr int RB = D * BITS / 8;      // code bytes per token row
-  static constexpr int CODE_TILE = T * RB;     // 8192 (INT4) / 4096 (INT2)
-  static constexpr int PAR_TILE = T * NG * 4;  // 2048
+  static constexpr int CODE_TILE = T * RB;     // 8192 (INT4) / 4096 (INT2) at 128 tokens
+  static constexpr int PAR_TILE = T * NG * 4;  // 2048 at 128 tokens
   static constexpr int KC = 0;
   static constexpr int VC = CODE_TILE;
   static constexpr int KP = 2 * CODE_TILE;
@@ -106,8 +115,8 @@ struct Geo {
   // a tile's compute outlasts a copy's latency, and the extra bytes in flight
   // only delay the other CTAs' tiles.
   static constexpr int NSTAGE = 2;
-  // INT3: per warp 32 widened rows of K and of V, 64 bytes each
-  static constexpr int XBUF = BITS == 3 ? NCW * 2 * 32 * 64 : 0;
+  // INT3: per warp its widened rows of K and of V, 64 bytes each
+  static constexpr int XBUF = BITS == 3 ? NCW * 2 * WR * 64 : 0;
   static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned");
 };
 
@@ -123,9 +132,9 @@ struct MergeSmem {
 // residual split's K and V rows overlap the stage ring (residual splits never
 // use the ring; packed splits reuse it for the merge once it is idle).
 constexpr size_t kResTilesOff = (sizeof(MergeSmem) + 4 * D * sizeof(float) + 127) & ~(size_t)127;
-template <int BITS, int CPS>
+template <int BITS, int CPS, int TT>
 constexpr size_t tc_smem_bytes() {
-  using G = Geo<BITS, CPS>;
+  using G = Geo<BITS, CPS, TT>;
   constexpr size_t ring = (size_t)G::NSTAGE * G::STAGE + G::XBUF;
   constexpr size_t res = kResTilesOff + 2 * 64 * (2 * D + 16);  // kResRows rows of K and V
   return 1024 + (ring > res ? ring : res);
@@ -520,12 +529,13 @@ __device__ __forceinline__ void residual_tc(const F16Rows& fr, int c0, uint8_t* 
 // slot, and attends over the window without the leaving token plus the new token
 // (fp16) and the quantized one (dequantized in fp32).  The last head of a
 // sequence to finish commits the counters.
-template <int BITS, bool STEP, int CPS>
+template <int BITS, bool STEP, int CPS, int TT>
 __global__ void __launch_bounds__(NTHREADS, CPS)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
                      const DecodeArgs a) {
-  using G = Geo<BITS, CPS>;
+  using G = Geo<BITS, CPS, TT>;
   constexpr int NSTAGE = G::NSTAGE;
+  constexpr int T = G::T, NSUB = G::NSUB, WR = G::WR;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -952,19 +962,20 @@ __global__ void __launch_bounds__(NTHREADS, CPS)
         break;
       }
       uint8_t* base = smem + (size_t)st * G::STAGE;
-      const int wrow = 32 * warp;                         // first row of this warp
-      // rows of this warp still ours; in a paged cache a warp's 32 rows are one
-      // page, and none of a page outside the pool takes part
-      int nvalid = min(npk - tile * T - wrow, 32);
-      if (a.rm.paged && ((s_bad[st] >> warp) & 1u)) nvalid = 0;
+      const int wrow = WR * warp;                         // first row of this warp
+      // rows of this warp still ours; in a paged cache (128-token tiles) a
+      // warp's 32 rows are one page, and none of a page outside the pool takes part
+      int nvalid = min(npk - tile * T - wrow, WR);
+      if (a.rm.paged && ((s_bad[st] >> (wrow / kPage)) & 1u)) nvalid = 0;
       if (nvalid > 0) {
         // rows past the split end may hold anything: zero their params so no
         // Inf/NaN reaches the arithmetic (their scores are masked anyway)
-        if (nvalid < 32) {
-          if (lane >= nvalid) {
-            reinterpret_cast<uint4*>(base + G::KP)[wrow + lane] = make_uint4(0, 0, 0, 0);
-            reinterpret_cast<uint4*>(base + G::VP)[wrow + lane] = make_uint4(0, 0, 0, 0);
-          }
+        if (nvalid < WR) {
+          for (int r = lane; r < WR; r += 32)
+            if (r >= nvalid) {
+              reinterpret_cast<uint4*>(base + G::KP)[wrow + r] = make_uint4(0, 0, 0, 0);
+              reinterpret_cast<uint4*>(base + G::VP)[wrow + r] = make_uint4(0, 0, 0, 0);
+            }
           __syncwarp();
         }
         uint32_t kc = ptx::smem_u32(base + G::KC);
@@ -973,14 +984,16 @@ __global__ void __launch_bounds__(NTHREADS, CPS)
         const uint32_t* vp = reinterpret_cast<const uint32_t*>(base + G::VP);
         int crow = wrow;  // this warp's first row in the code tiles it reads
         if constexpr (BITS == 3) {
-          // widen the warp's 32 rows of K and V codes (lane = row) into its own
+          // widen the warp's rows of K and V codes (lane = row) into its own
           // INT4 buffers; the params stay in the stage (rows offset by wrow)
-          uint8_t* xk = smem + (size_t)NSTAGE * G::STAGE + (size_t)warp * (2 * 32 * 64);
-          widen_row3(base + G::KC + (wrow + lane) * G::RB, ptx::smem_u32(xk), lane);
-          widen_row3(base + G::VC + (wrow + lane) * G::RB, ptx::smem_u32(xk + 32 * 64), lane);
+          uint8_t* xk = smem + (size_t)NSTAGE * G::STAGE + (size_t)warp * (2 * WR * 64);
+          for (int r = lane; r < WR; r += 32) {
+            widen_row3(base + G::KC + (wrow + r) * G::RB, ptx::smem_u32(xk), r);
+            widen_row3(base + G::VC + (wrow + r) * G::RB, ptx::smem_u32(xk + WR * 64), r);
+          }
           __syncwarp();
           kc = ptx::smem_u32(xk);
-          vc = ptx::smem_u32(xk + 32 * 64);
+          vc = ptx::smem_u32(xk + WR * 64);
           vp += wrow * NG;
           crow = 0;
         }
@@ -1018,8 +1031,10 @@ __global__ void __launch_bounds__(NTHREADS, CPS)
         // The running max of query t moves only when one of its rows lies more
         // than 8 above it; each thread checks its own rows, and only then does
         // the warp reduce the max over the lanes of each query.
-        const float mown =
-            fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1])) * kq24;
+        float mown = fmaxf(sv[0][0], sv[0][1]);
+#pragma unroll
+        for (int u = 1; u < NSUB; ++u) mown = fmaxf(mown, fmaxf(sv[u][0], sv[u][1]));
+        mown *= kq24;
         if (__any_sync(0xffffffffu, mown > m_ref + 8.f)) {
           float mloc = mown;
           mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 4));
@@ -1356,7 +1371,7 @@ bool make_rows_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint6
 
 // Raise the kernel's dynamic shared-memory limit once per device (the attribute
 // is per device; a process may drive several GPUs).
-template <int BITS, bool STEP, int CPS>
+template <int BITS, bool STEP, int CPS, int TT>
 cudaError_t ensure_smem_attr(size_t smem) {
   static std::atomic<uint64_t> done{0};  // bit i: set on device i
   int dev = 0;
@@ -1364,19 +1379,20 @@ cudaError_t ensure_smem_attr(size_t smem) {
   if (e != cudaSuccess) return e;
   const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
   if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
-  e = cudaFuncSetAttribute(decode_tc_kernel<BITS, STEP, CPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(decode_tc_kernel<BITS, STEP, CPS, TT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem);
   if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
   return e;
 }
 
-template <int BITS, bool STEP, int CPS>
+template <int BITS, bool STEP, int CPS, int TT>
 cudaError_t launch_bits(const Dims& s, const DecodePlan& p, const DecodeArgs& a, cudaStream_t st) {
-  using Gm = Geo<BITS, CPS>;
+  using Gm = Geo<BITS, CPS, TT>;
   // packed rows: every (sequence, head, slot), or every (page, head, slot) of a pool
   const bool paged = s.page != 0;
+  if (paged && TT != 128) return cudaErrorInvalidValue;  // a warp's rows must be one page
   const uint64_t rows = paged ? (uint64_t)s.npages * s.Hkv * kPage : (uint64_t)s.B * s.Hkv * s.cap;
-  const uint32_t box = paged ? kPage : T;
+  const uint32_t box = paged ? kPage : Gm::T;
   CUtensorMap kc, vc;
   // INT3 rows (48 bytes) load unswizzled: each warp re-lays them out itself
   const CUtensorMapSwizzle swz = BITS == 4   ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -1385,8 +1401,8 @@ cudaError_t launch_bits(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
   if (!make_rows_map(&kc, a.k_codes, Gm::RB, rows, swz, box) ||
       !make_rows_map(&vc, a.v_codes, Gm::RB, rows, swz, box))
     return cudaErrorInvalidValue;
-  constexpr size_t smem = tc_smem_bytes<BITS, CPS>();
-  cudaError_t e = ensure_smem_attr<BITS, STEP, CPS>(smem);
+  constexpr size_t smem = tc_smem_bytes<BITS, CPS, TT>();
+  cudaError_t e = ensure_smem_attr<BITS, STEP, CPS, TT>(smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.splits, (unsigned)s.Hkv, (unsigned)s.B);
@@ -1398,7 +1414,7 @@ cudaError_t launch_bits(const Dims& s, const DecodePlan& p, const DecodeArgs& a,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<BITS, STEP, CPS>, kc, vc, a);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<BITS, STEP, CPS, TT>, kc, vc, a);
 }
 
 }  // namespace
@@ -1410,15 +1426,22 @@ bool tc_supported(const kvq_cache_desc& D, int gq) {
 int tc_threads() { return NTHREADS; }
 int tc_ctas_per_sm(bool several_waves) { return several_waves ? 4 : 3; }
 int tc_residual_rows() { return kResRows; }
+int tc_tile_tokens(const kvq_cache_desc& D, int cps, int64_t split_tokens) {
+  // measured on INT2 only: 128K tokens, 2,425 per split: 38.0 -> 37.1 us; 32K
+  // tokens, 604 per split: 14.5 -> 15.0 us
+  return D.bits == 2 && cps == 3 && D.page_size == 0 && split_tokens >= 8 * 192 ? 192 : 128;
+}
 
 template <int CPS>
 cudaError_t launch_cps(const Dims& s, const DecodePlan& p, const DecodeArgs& a, cudaStream_t st,
                        bool step) {
   if (s.bits == 3)
-    return step ? launch_bits<3, true, CPS>(s, p, a, st) : launch_bits<3, false, CPS>(s, p, a, st);
-  if (step)
-    return s.bits == 4 ? launch_bits<4, true, CPS>(s, p, a, st) : launch_bits<2, true, CPS>(s, p, a, st);
-  return s.bits == 4 ? launch_bits<4, false, CPS>(s, p, a, st) : launch_bits<2, false, CPS>(s, p, a, st);
+    return step ? launch_bits<3, true, CPS, 128>(s, p, a, st) : launch_bits<3, false, CPS, 128>(s, p, a, st);
+  if (s.bits == 4)
+    return step ? launch_bits<4, true, CPS, 128>(s, p, a, st) : launch_bits<4, false, CPS, 128>(s, p, a, st);
+  if (CPS == 3 && p.tile == 192)
+    return step ? launch_bits<2, true, 3, 192>(s, p, a, st) : launch_bits<2, false, 3, 192>(s, p, a, st);
+  return step ? launch_bits<2, true, CPS, 128>(s, p, a, st) : launch_bits<2, false, CPS, 128>(s, p, a, st);
 }
 
 cudaError_t launch_decode_tc(const Dims& s, const DecodePlan& p, const DecodeArgs& a,

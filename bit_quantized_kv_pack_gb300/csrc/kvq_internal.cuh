@@ -450,6 +450,7 @@ struct DecodePlan {
   int threads;  // threads per CTA of the split kernel
   int cps;      // tensor-core kernel: resident CTAs per SM of the variant (3 or 4)
   int fold;     // tensor-core kernel: no fp16 splits; the last packed split takes those rows
+  int tile;     // tensor-core kernel: tokens per pipeline stage (128 or 192)
   // Workspace layout.  The tickets sit at fixed offsets (they depend only on the
   // cache shape and head count), so a workspace shared by calls with different
   // split counts never has a partial land on a ticket.
