@@ -145,6 +145,78 @@ def test_decision_follows_the_smaller_error(bits):
     assert 0 < sum(modes) < len(modes)
 
 
+
+def _dyadic(v: float) -> int:
+    """v (an fp16 or fp32 value of modest size) as an integer multiple of 2^-40."""
+    n = v * (1 << 40)
+    assert n == int(n)
+    return int(n)
+
+
+def _is_f32(n: int) -> bool:
+    """A multiple of a power of two (2^-40 or 2^-80 here) is an fp32 value when
+    its odd part has at most 24 bits (the magnitudes here stay in fp32's
+    normal range)."""
+    n = abs(n)
+    if n == 0:
+        return True
+    n >>= (n & -n).bit_length() - 1
+    return n.bit_length() <= 24
+
+
+def _exact_sq_error(x, codes, sh, mh):
+    """The sum of (x - (min + code * scale))^2 in exact integer arithmetic (in
+    units of 2^-80), or None unless fp32 arithmetic reproduces it without a
+    single rounding: every product, reconstruction, difference and square is
+    an fp32 value, and all terms are multiples of the lowest set bit among them
+    with a total below 2^24 such units, so every partial sum, in any order, is
+    exact."""
+    mn, sc = _dyadic(_f16v(mh)), _dyadic(_f16v(sh))
+    terms = []
+    for v, c in zip(x.astype(np.float64), codes):
+        prod = int(c) * sc
+        rec = mn + prod
+        d = _dyadic(float(v)) - rec
+        sq = d * d
+        if not all(_is_f32(t) for t in (prod, rec, d, sq)):
+            return None
+        terms.append(sq)
+    nz = [t for t in terms if t]
+    if nz:
+        unit = min((t & -t).bit_length() - 1 for t in nz)
+        if sum(terms) >> unit >= 1 << 24:
+            return None
+    return sum(terms)
+
+
+@pytest.mark.parametrize("bits,p_zero", [(4, 0.0), (2, 0.3)])
+def test_exact_near_ties_follow_the_exact_comparison(bits, p_zero):
+    """Near ties decided without rounding.  Groups on a quarter-step grid with
+    ends -1.5 and 1.5 (some values pulled to 0) whose two candidate errors fp32
+    arithmetic computes exactly, so the decision cannot depend on the order of
+    the sums: it must be the exact comparison, symmetric only when its error is
+    strictly smaller.  Errors within 8% of each other, of both signs, and exact
+    ties (INT2) occur; a swapped comparison, a non-strict one or a dropped term
+    fails here even though the fp64 check above only looks at clear gaps."""
+    rng = np.random.default_rng(40 + bits)
+    seen = {-1: 0, 0: 0, 1: 0}
+    for _ in range(1500):
+        k = rng.integers(-6, 7, 32)
+        k[rng.random(32) < p_zero] = 0
+        k[0], k[1] = -6, 6
+        x = (k * 0.25).astype(np.float16)
+        ca, ash, amh = oracle.quantize_group(x, bits)
+        cs, ssh, smh, ok = oracle.quantize_group_sym(x, bits)
+        ea, es = _exact_sq_error(x, ca, ash, amh), _exact_sq_error(x, cs, ssh, smh)
+        if not ok or ea is None or es is None or abs(ea - es) * 12 > max(ea, es):
+            continue
+        mode = oracle.quantize_group_hybrid(x, bits)[3]
+        assert mode == (0 if es < ea else 1), (bits, ea, es, mode)
+        seen[(es > ea) - (es < ea)] += 1
+    assert seen[-1] >= 10 and seen[1] >= 10, seen
+    if bits == 2:
+        assert seen[0] >= 10, seen
+
 def test_error_is_a_sum_of_squares():
     """H2 against its definition on hand-made cases: exact reconstruction gives
     0, one element off by 0.5 gives 0.25, and the sum is over all 32."""
