@@ -729,9 +729,9 @@ __global__ void __launch_bounds__(NTHREADS, CPS)
   // plain loads of data that must come from memory) were measured to be served
   // only once the launch it depends on had completed, and queued ahead of that
   // launch's last memory operations they delayed its completion and with it
-  // the wait.  An L2 prefetch of tile 0 alone (a ninth of the cache at 32K) is
-  // cheap enough there: in a grid of one wave it lets tile 0 land sooner.  q
-  // and the new token are read after the wait.
+  // the wait.  An L2 prefetch of each split's tile 0 alone (9 of the 42 MB a
+  // 32K INT4 step reads) is cheap enough there: in a grid of one wave it lets
+  // tile 0 land sooner.  q and the new token are read after the wait.
   const bool early = STEP && a.early != 0;
   if (early && threadIdx.x == 0) {
     plan(false);
@@ -1427,8 +1427,8 @@ int tc_threads() { return NTHREADS; }
 int tc_ctas_per_sm(bool several_waves) { return several_waves ? 4 : 3; }
 int tc_residual_rows() { return kResRows; }
 int tc_tile_tokens(const kvq_cache_desc& D, int cps, int64_t split_tokens) {
-  // measured on INT2 only: 128K tokens, 2,425 per split: 38.0 -> 37.1 us; 32K
-  // tokens, 604 per split: 14.5 -> 15.0 us
+  // measured on INT2 only: 128K tokens (2,425 per split) 38.0 -> 37.0 us;
+  // 32K tokens (604 per split) 14.5 -> 15.0 us, so short splits keep 128
   return D.bits == 2 && cps == 3 && D.page_size == 0 && split_tokens >= 8 * 192 ? 192 : 128;
 }
 
