@@ -1,7 +1,9 @@
 """Host-side helpers the parity tests and the benchmark rely on, checked on
 the CPU: the gather of a paged cache's pool through its block table into the
 contiguous layout the oracle uses, the packed-token count of a prefill with a
-sink and a window, and the code-width override of a workload."""
+sink and a window, the code-width override of a workload, and the rule that a
+committed profile's DRAM traffic is used only while the sources it was taken on
+are unchanged."""
 
 import numpy as np
 import torch
@@ -48,3 +50,29 @@ def test_workload_bits_override():
     assert w.bits == 3 and w.name == "llama3.1-8b-int3-32k"
     assert w.len_max == synth.WORKLOADS[2].len_max and w.seed == synth.WORKLOADS[2].seed
     assert bench.workload_for(3).name == "llama3.1-8b-int2-128k"
+
+
+def test_profile_traffic_only_for_the_sources_it_was_taken_on(tmp_path, monkeypatch):
+    """The bench line's roofline traffic comes from a committed ncu summary only
+    while its source hash matches the current kernel sources: a copy of the
+    sources with one byte changed makes it null."""
+    import shutil
+    csrc = tmp_path / "bit_quantized_kv_pack_gb300" / "csrc"
+    shutil.copytree(bench.os.path.join(bench.ROOT, "bit_quantized_kv_pack_gb300", "csrc"), csrc)
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    for kind, name, hash_fn, read in (
+            ("decode_step", "w", bench.decode_source_hash, bench.profiled_traffic),
+            ("quantize_pack", "w", bench.pack_source_hash, bench.profiled_pack_traffic)):
+        prof = tmp_path / "profiles" / f"{kind}_{name}.md"
+        prof.write_text(f"# summary\n\nsource_hash: {hash_fn()}\ntraffic_bytes_per_launch: 12345\n")
+        assert read(name) == 12345.0
+        assert read("absent") is None
+    def touch(name):
+        f = csrc / name
+        f.write_bytes(f.read_bytes() + b"\n")
+    touch("kvq_decode_tc.cu")  # a decode source only
+    assert bench.profiled_traffic("w") is None
+    assert bench.profiled_pack_traffic("w") == 12345.0
+    touch("kvq_quant.cu")  # a pack source
+    assert bench.profiled_pack_traffic("w") is None
