@@ -257,3 +257,41 @@ def test_decode_single_split(bits, gq):
         out = kvq.kvq_decode_attention(g, q.to(DEV), workspace=ws, flags=kvq.KVQ_OUT_F32)
         assert kvq.kvq_read_error(g)[0] == kvq.KVQ_OK
         assert_attn_close(out, oracle.decode(r, q.numpy()))
+
+
+def test_decode_tall_tiles():
+    """INT2 splits long enough for the 192-token tiles (4 sequences x 8 KV heads
+    of up to 20,000 packed tokens: 13 packed splits per head in one wave on a
+    152-SM GB300, about 1,540 tokens each), ragged so the splits end inside a
+    tile at different rows; decode and two fused steps against the oracle,
+    bytes bit for bit."""
+    rng = np.random.default_rng(192)
+    B, H, d, gq, cap, Nr = 4, 8, 128, 4, 20000, 16
+    lens = [cap + Nr - 2, 19001, 12345, 3001]  # room for the two steps' packed tokens
+    Lmax = max(lens)
+    k = torch.from_numpy(rng.standard_normal((B, H, Lmax, d)).astype(np.float16))
+    v = torch.from_numpy(rng.standard_normal((B, H, Lmax, d)).astype(np.float16))
+    seq = torch.tensor(lens, dtype=torch.int32)
+    g = gpu_cache(B, H, d, 2, cap, Nr, seed=2)
+    kvq.kvq_quantize_pack(g, k.to(DEV), v.to(DEV), seq.to(DEV))
+    assert kvq.kvq_read_error(g)[0] == kvq.KVQ_OK
+    rs = oracle_sequences(to_np(k), to_np(v), to_np(seq), 2, cap, Nr)
+    del k, v
+    ws = kvq.workspace_for(g, H * gq)
+    q = torch.from_numpy(rng.standard_normal((B, H * gq, d)).astype(np.float16))
+    qn = q.numpy()
+    want = np.concatenate(per_sequence(lambda b: oracle.decode(rs[b], qn[b:b + 1]), B))
+    assert_attn_close(kvq.kvq_decode_attention(g, q.to(DEV), workspace=ws, flags=kvq.KVQ_OUT_F32), want)
+    for _ in range(2):
+        kn = torch.from_numpy(rng.standard_normal((B, H, d)).astype(np.float16))
+        vn = torch.from_numpy(rng.standard_normal((B, H, d)).astype(np.float16))
+        q = torch.from_numpy(rng.standard_normal((B, H * gq, d)).astype(np.float16))
+        out = kvq.kvq_decode_step(g, q.to(DEV), kn.to(DEV), vn.to(DEV), workspace=ws)
+        assert kvq.kvq_read_error(g)[0] == kvq.KVQ_OK
+        knn, vnn, qn = kn.numpy(), vn.numpy(), q.numpy()
+        assert all(e == 0 for e in per_sequence(
+            lambda b: oracle.append(rs[b], knn[b:b + 1], vnn[b:b + 1]), B))
+        want = np.concatenate(per_sequence(lambda b: oracle.decode(rs[b], qn[b:b + 1]), B))
+        assert_attn_close(out, want)
+    for b in range(B):
+        assert_cache_equal(g, rs[b], batches=[b])
